@@ -1,0 +1,190 @@
+"""CPU oracle for the routed-expert FFN layer -- TEST INFRASTRUCTURE ONLY.
+
+Python bindings (ctypes) over ``moe_oracle.c``, a plain fp64 C statement of the
+layer. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package; the CUDA library never does, and the
+oracle never imports the library. The only inputs the two sides share come
+from ``synth`` (seeded random bytes, no arithmetic of the method).
+
+What pins it (tests/test_oracle_*.py): exhaustive E2M1/E8M0 tables against
+their bit-field definitions, the 13,219,200-byte expert of the "Neural Server"
+technical page, hand-computed closed-form layers, brute-force top-k over all
+subsets, exact ties, gate and bucketing invariants, exact power-of-two scaling,
+expert-relabel equivariance, and an independent dense float64 PyTorch
+restatement on tiny layers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EINVAL, ENAN_SCALE, ENOMEM = 0, -1, -2, -3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with plain flags (no fast-math, no contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    src = os.path.join(_HERE, "moe_oracle.c")
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+                               "-o", tmp, src, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32, vp, dbl, u8, u16 = ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_uint8, ctypes.c_uint16
+            lib.oracle_e2m1.argtypes = [i32]
+            lib.oracle_e2m1.restype = dbl
+            lib.oracle_e8m0.argtypes = [i32]
+            lib.oracle_e8m0.restype = dbl
+            lib.oracle_bf16.argtypes = [u16]
+            lib.oracle_bf16.restype = dbl
+            lib.oracle_mx_element.argtypes = [vp, vp, i32, i32, i32]
+            lib.oracle_mx_element.restype = dbl
+            lib.oracle_expert_code_bytes.argtypes = [i32, i32]
+            lib.oracle_expert_code_bytes.restype = ctypes.c_size_t
+            lib.oracle_expert_scale_bytes.argtypes = [i32, i32]
+            lib.oracle_expert_scale_bytes.restype = ctypes.c_size_t
+            lib.oracle_logits_token.argtypes = [vp, i32, vp, vp, i32, vp]
+            lib.oracle_topk_token.argtypes = [vp, i32, i32, vp, vp]
+            lib.oracle_bucket.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+            lib.oracle_expert_ffn.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+            lib.oracle_expert_ffn.restype = i32
+            lib.oracle_route.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+            lib.oracle_route.restype = i32
+            lib.oracle_layer_tokens.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+            lib.oracle_layer_tokens.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "need a C-contiguous numpy array"
+    return a.ctypes.data
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def e2m1(code: int) -> float:
+    return _load().oracle_e2m1(code)
+
+
+def e8m0(e: int) -> float:
+    return _load().oracle_e8m0(e)
+
+
+def bf16(bits: int) -> float:
+    return _load().oracle_bf16(bits)
+
+
+def mx_element(codes: np.ndarray, scales: np.ndarray, K: int, r: int, c: int) -> float:
+    return _load().oracle_mx_element(_p(codes), _p(scales), K, r, c)
+
+
+def expert_code_bytes(d: int, f: int) -> int:
+    return _load().oracle_expert_code_bytes(d, f)
+
+
+def expert_scale_bytes(d: int, f: int) -> int:
+    return _load().oracle_expert_scale_bytes(d, f)
+
+
+def logits_token(x_row: np.ndarray, w_router: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    x_row = np.ascontiguousarray(x_row, dtype=np.uint16)
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    E, d = w_router.shape
+    out = np.empty((E,), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _load().oracle_logits_token(_p(x_row), d, _p(w_router), _p(b), E, _p(out))
+    return out
+
+
+def topk_token(logits: np.ndarray, k: int):
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    ids = np.empty((k,), dtype=np.int32)
+    gates = np.empty((k,), dtype=np.float64)
+    _load().oracle_topk_token(_p(logits), logits.shape[0], k, _p(ids), _p(gates))
+    return ids, gates
+
+
+def bucket(ids: np.ndarray, E: int):
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    P = ids.shape[0]
+    counts = np.empty((E,), dtype=np.int32)
+    offsets = np.empty((E + 1,), dtype=np.int32)
+    perm = np.empty((P,), dtype=np.int32)
+    inv = np.empty((P,), dtype=np.int32)
+    _load().oracle_bucket(_p(ids), P, E, _p(counts), _p(offsets), _p(perm), _p(inv))
+    return counts, offsets, perm, inv
+
+
+def expert_ffn(codes_e: np.ndarray, scales_e: np.ndarray, d: int, f: int, x: np.ndarray):
+    """One expert on one fp64 input vector; returns (h[f], out[d])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    h = np.empty((f,), dtype=np.float64)
+    out = np.empty((d,), dtype=np.float64)
+    _check(_load().oracle_expert_ffn(_p(np.ascontiguousarray(codes_e)), _p(np.ascontiguousarray(scales_e)),
+                                     d, f, _p(x), _p(h), _p(out)), "expert_ffn")
+    return h, out
+
+
+def route(x: np.ndarray, w_router: np.ndarray, bias: np.ndarray | None, k: int) -> dict:
+    """Routing of all tokens: logits, ids, gates, counts, offsets, perm, inv."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    T, d = x.shape
+    E = w_router.shape[0]
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    out = {
+        "logits": np.empty((T, E), dtype=np.float64),
+        "ids": np.empty((T, k), dtype=np.int32),
+        "gates": np.empty((T, k), dtype=np.float64),
+        "counts": np.empty((E,), dtype=np.int32),
+        "offsets": np.empty((E + 1,), dtype=np.int32),
+        "perm": np.empty((T * k,), dtype=np.int32),
+        "inv": np.empty((T * k,), dtype=np.int32),
+    }
+    _check(_load().oracle_route(_p(x), T, d, _p(w_router), _p(b), E, k, _p(out["logits"]), _p(out["ids"]),
+                                _p(out["gates"]), _p(out["counts"]), _p(out["offsets"]), _p(out["perm"]),
+                                _p(out["inv"])), "route")
+    return out
+
+
+def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router: np.ndarray,
+                 bias: np.ndarray | None, codes: np.ndarray, scales: np.ndarray, tokens=None,
+                 want_h: bool = False) -> dict:
+    """fp64 layer output of the listed tokens (default: all): y [n][d], ids, gates, optional h [n][k][F]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    y = np.empty((n, d), dtype=np.float64)
+    h = np.empty((n, k, F), dtype=np.float64) if want_h else None
+    ids = np.empty((n, k), dtype=np.int32)
+    gates = np.empty((n, k), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _check(_load().oracle_layer_tokens(d, F, E, k, S, _p(x), _p(np.ascontiguousarray(w_router, dtype=np.float32)),
+                                       _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
+                                       _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates)), "layer_tokens")
+    return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}

@@ -1,0 +1,244 @@
+/*
+ * CPU oracle for the routed-expert FFN layer. TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct statement of what the layer computes, in
+ * fp64, written to be checked against the pages by eye. Only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg load it; the CUDA library
+ * shares no code, header, table or helper with it.
+ *
+ * The layer (one MoE block of a large MoE language model):
+ *   logits  l[t,e] = sum_i W_r[e,i] x[t,i] + b[e]
+ *   top-k   the k largest logits of token t, largest first, ties to the lower e
+ *   gates   g[t,j] = softmax over the k selected logits
+ *   expert  h = SiLU(W_gate x) * (W_up x),   part = W_down h
+ *   combine y[t] = sum_j g[t,j] part(t, j) + shared(x_t)   (shared: unweighted)
+ *
+ * Sources (page title, section):
+ *   "Neural Server" technical page, "How one token and one prompt are
+ *     processed": the router and top-k kernels emit 4 expert ids and 4 weights
+ *     per token; resident experts then run as MXFP4 GEMVs.
+ *   "Neural Server" technical page, "What it runs on and what it runs": 128
+ *     experts per layer, four active per token, hidden size 2880, and the
+ *     13,219,200-byte MXFP4 expert.
+ *   "NInfer" Qwen3.8-Flash-Next notes, MoE execution: (token, expert) pairs are
+ *     grouped by expert; a fused gate/up kernel, then a down kernel; weighted
+ *     expert outputs are summed; expert weights are renormalised per token.
+ *   "Nebula", "Description": the router selects experts and assigns them
+ *     normalised weights; gate/up/down expert tensors.
+ *   "Running Qwen3.8-Flash-Next on a 32 GB Mac with Transformers",
+ *     architecture: routed experts plus one shared expert per layer.
+ * None of the pages defines MXFP4's values; they follow the OCP Microscaling
+ * Formats (MX) v1.0 specification: E2M1 elements, one E8M0 scale per 32
+ * consecutive elements along the reduction axis, value = E2M1 * 2^(e - 127).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   nibble order: the low nibble of byte i is element 2i, the high nibble 2i+1;
+ *   gate/up: one [2F x d] matrix per expert, rows [0,F) gate, rows [F,2F) up;
+ *   SiLU(z) = z / (1 + exp(-z)); no biases, no clamp;
+ *   gates: softmax over the k selected logits (equal to the softmax over all
+ *   E logits renormalised over the selected k);
+ *   ties in top-k go to the lower expert index;
+ *   the shared expert is added with weight 1.
+ *
+ * Canonical expert-major weight layout (one contiguous byte range per expert):
+ *   codes : expert j at j * (3 F d / 2): gate/up [2F][d/2], then down [d][F/2]
+ *   scales: expert j at j * (3 F d / 32): gate/up [2F][d/32], then down [d][F/32]
+ *   the shared expert (ffn S) follows expert E-1 in both arrays.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENAN_SCALE -2
+#define ORACLE_ENOMEM -3
+
+/* E2M1 (OCP MX v1.0): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit. */
+double oracle_e2m1(int code) {
+  static const double magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  double v = magnitude[code & 7];
+  return (code & 8) ? -v : v;
+}
+
+/* E8M0 scale (OCP MX v1.0): 2^(e - 127); the byte 0xFF encodes NaN. */
+double oracle_e8m0(int e) {
+  if (e == 255) return NAN;
+  return ldexp(1.0, e - 127);
+}
+
+/* Exact value of a bf16 bit pattern. */
+double oracle_bf16(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Element (r, c) of an MXFP4 matrix whose rows hold K elements (K % 32 == 0). */
+double oracle_mx_element(const uint8_t* codes, const uint8_t* scales, int K, int r, int c) {
+  uint8_t byte = codes[(size_t)r * (size_t)(K / 2) + (size_t)(c / 2)];
+  int code = (c & 1) ? (byte >> 4) : (byte & 0x0F);
+  int e = scales[(size_t)r * (size_t)(K / 32) + (size_t)(c / 32)];
+  return oracle_e2m1(code) * oracle_e8m0(e);
+}
+
+size_t oracle_expert_code_bytes(int d, int f) { return (size_t)3 * (size_t)f * (size_t)d / 2; }
+size_t oracle_expert_scale_bytes(int d, int f) { return (size_t)3 * (size_t)f * (size_t)d / 32; }
+
+/* Router logits of one token: l[e] = sum_i W_r[e,i] x[i] + b[e], fp64, index order. */
+void oracle_logits_token(const uint16_t* x, int d, const float* w_router, const float* bias, int E,
+                         double* logits) {
+  for (int e = 0; e < E; ++e) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i) acc += (double)w_router[(size_t)e * d + i] * oracle_bf16(x[i]);
+    logits[e] = acc + (bias ? (double)bias[e] : 0.0);
+  }
+}
+
+/* Top-k of one token: repeatedly take the largest remaining logit, the lower
+ * expert index winning an exact tie. Gates are the softmax of the selected
+ * logits, shifted by the largest for range. */
+void oracle_topk_token(const double* logits, int E, int k, int32_t* ids, double* gates) {
+  char* taken = (char*)calloc((size_t)E, 1);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || logits[e] > logits[best]) best = e; /* strict '>' keeps the lower index on ties */
+    }
+    taken[best] = 1;
+    ids[j] = best;
+  }
+  free(taken);
+  double top = logits[ids[0]];
+  double denom = 0.0;
+  for (int j = 0; j < k; ++j) denom += exp(logits[ids[j]] - top);
+  for (int j = 0; j < k; ++j) gates[j] = exp(logits[ids[j]] - top) / denom;
+}
+
+/* Counting sort of the P = T*k (token, slot) pairs by expert, stable in p = t*k + j.
+ * counts[e], offsets[0..E] (exclusive prefix sum), perm[row] = p, inv[p] = row. */
+void oracle_bucket(const int32_t* ids, int P, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                   int32_t* inv) {
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int p = 0; p < P; ++p) counts[ids[p]] += 1;
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int row = 0;
+  for (int e = 0; e < E; ++e)
+    for (int p = 0; p < P; ++p)
+      if (ids[p] == e) {
+        perm[row] = p;
+        if (inv) inv[p] = row;
+        ++row;
+      }
+}
+
+static int scales_finite(const uint8_t* scales, size_t n) {
+  for (size_t i = 0; i < n; ++i)
+    if (scales[i] == 255) return 0;
+  return 1;
+}
+
+/* One expert (ffn f) on one input vector x[d] (fp64):
+ *   gate_i = sum_c Wgu[i][c] x[c],  up_i = sum_c Wgu[f + i][c] x[c]   (i < f)
+ *   h_i = SiLU(gate_i) * up_i
+ *   out_r = sum_i Wd[r][i] h_i                                         (r < d)
+ * codes/scales point at the expert's own byte range. h may be NULL. */
+int oracle_expert_ffn(const uint8_t* codes, const uint8_t* scales, int d, int f, const double* x, double* h,
+                      double* out) {
+  if (d <= 0 || f <= 0 || d % 32 || f % 32) return ORACLE_EINVAL;
+  if (!scales_finite(scales, oracle_expert_scale_bytes(d, f))) return ORACLE_ENAN_SCALE;
+  const uint8_t* gu_codes = codes;
+  const uint8_t* gu_scales = scales;
+  const uint8_t* dn_codes = codes + (size_t)2 * f * d / 2;
+  const uint8_t* dn_scales = scales + (size_t)2 * f * d / 32;
+  double* hv = (double*)malloc(sizeof(double) * (size_t)f);
+  if (!hv) return ORACLE_ENOMEM;
+  for (int i = 0; i < f; ++i) {
+    double gate = 0.0, up = 0.0;
+    for (int c = 0; c < d; ++c) {
+      gate += oracle_mx_element(gu_codes, gu_scales, d, i, c) * x[c];
+      up += oracle_mx_element(gu_codes, gu_scales, d, f + i, c) * x[c];
+    }
+    double silu = gate / (1.0 + exp(-gate));
+    hv[i] = silu * up;
+    if (h) h[i] = hv[i];
+  }
+  for (int r = 0; r < d; ++r) {
+    double acc = 0.0;
+    for (int i = 0; i < f; ++i) acc += oracle_mx_element(dn_codes, dn_scales, f, r, i) * hv[i];
+    out[r] = acc;
+  }
+  free(hv);
+  return ORACLE_OK;
+}
+
+/* Routing of all T tokens: logits [T][E], ids [T][k], gates [T][k], and the
+ * bucketing of the T*k pairs (counts [E], offsets [E+1], perm [T*k], inv [T*k]).
+ * Any output pointer except ids may be NULL. */
+int oracle_route(const uint16_t* x, int T, int d, const float* w_router, const float* bias, int E, int k,
+                 double* logits, int32_t* ids, double* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 int32_t* inv) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || !ids) return ORACLE_EINVAL;
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  if (!l || !g) { free(l); free(g); return ORACLE_ENOMEM; }
+  for (int t = 0; t < T; ++t) {
+    oracle_logits_token(x + (size_t)t * d, d, w_router, bias, E, l);
+    if (logits) memcpy(logits + (size_t)t * E, l, sizeof(double) * (size_t)E);
+    oracle_topk_token(l, E, k, ids + (size_t)t * k, g);
+    if (gates) memcpy(gates + (size_t)t * k, g, sizeof(double) * (size_t)k);
+  }
+  free(l);
+  free(g);
+  if (counts && offsets && perm) {
+    oracle_bucket(ids, T * k, E, counts, offsets, perm, inv);
+  }
+  return ORACLE_OK;
+}
+
+/* Layer output of the listed tokens (fp64, unrounded):
+ *   y[n] = sum_j g[t,j] * expert(ids[t,j], x_t) + shared(x_t),   t = tokens[n]
+ * summed in slot order j, the shared expert (when S > 0) last.
+ * h_out (may be NULL) receives h of every (n, j) as [n_tokens][k][F]. */
+int oracle_layer_tokens(int d, int F, int E, int k, int S, const uint16_t* x, const float* w_router,
+                        const float* bias, const uint8_t* codes, const uint8_t* scales, const int32_t* tokens,
+                        int n_tokens, double* y, double* h_out, int32_t* ids_out, double* gates_out) {
+  if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || S < 0 || d % 32 || F % 32 || S % 32) return ORACLE_EINVAL;
+  size_t cb = oracle_expert_code_bytes(d, F), sb = oracle_expert_scale_bytes(d, F);
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  double* xv = (double*)malloc(sizeof(double) * (size_t)d);
+  double* part = (double*)malloc(sizeof(double) * (size_t)d);
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+  double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  int rc = ORACLE_OK;
+  if (!l || !xv || !part || !ids || !g) { rc = ORACLE_ENOMEM; goto done; }
+  for (int n = 0; n < n_tokens; ++n) {
+    const uint16_t* xt = x + (size_t)tokens[n] * d;
+    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(xt[i]);
+    oracle_logits_token(xt, d, w_router, bias, E, l);
+    oracle_topk_token(l, E, k, ids, g);
+    if (ids_out) memcpy(ids_out + (size_t)n * k, ids, sizeof(int32_t) * (size_t)k);
+    if (gates_out) memcpy(gates_out + (size_t)n * k, g, sizeof(double) * (size_t)k);
+    double* yn = y + (size_t)n * d;
+    for (int r = 0; r < d; ++r) yn[r] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      double* hj = h_out ? h_out + ((size_t)n * k + j) * F : NULL;
+      rc = oracle_expert_ffn(codes + (size_t)ids[j] * cb, scales + (size_t)ids[j] * sb, d, F, xv, hj, part);
+      if (rc) goto done;
+      for (int r = 0; r < d; ++r) yn[r] += g[j] * part[r];
+    }
+    if (S > 0) {
+      rc = oracle_expert_ffn(codes + (size_t)E * cb, scales + (size_t)E * sb, d, S, xv, NULL, part);
+      if (rc) goto done;
+      for (int r = 0; r < d; ++r) yn[r] += part[r];
+    }
+  }
+done:
+  free(l); free(xv); free(part); free(ids); free(g);
+  return rc;
+}
