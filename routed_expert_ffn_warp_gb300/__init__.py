@@ -1,0 +1,222 @@
+"""Routed-expert FFN (MoE layer) for NVIDIA GB300 -- Python binding of ``libmoe_gb300.so``.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels (``csrc/``). The functions keep the C ABI's names (``include/moe.h``):
+``moe_create``, ``moe_load_router``, ``moe_load_experts``, ``moe_forward``,
+``moe_forward_host``, ``moe_get_routing``, ``moe_get_logits``,
+``moe_get_status``, ``moe_weight_bytes``, ``moe_last_error``, ``moe_destroy``.
+Pointers may come from numpy arrays (host) or torch tensors (host or device);
+PyTorch is used for device memory and streams only.
+
+There is no fallback: if the compiled library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_T_TOO_LARGE = -2
+MOE_ERR_NOT_LOADED = -3
+MOE_ERR_CUDA = -4
+MOE_ERR_TIMEOUT = -5
+MOE_ERR_NAN_SCALE = -6
+MOE_ERR_NOMEM = -7
+MOE_OUT_BF16 = 0
+MOE_OUT_F32 = 1
+
+EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
+            "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_weight_bytes", "moe_last_error",
+            "moe_destroy"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int), ("ffn", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("shared_ffn", ctypes.c_int), ("t_max", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("flags", ctypes.c_uint)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the compiled library (build it with ``routed_expert_ffn_warp_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: run `python -m routed_expert_ffn_warp_gb300.build` "
+                                   "(there is no CPU fallback)")
+            lib = ctypes.CDLL(path)
+            vp, i32, P = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER
+            lib.moe_create.argtypes = [P(moe_config), i32, P(vp)]
+            lib.moe_load_router.argtypes = [vp, vp, vp]
+            lib.moe_load_experts.argtypes = [vp, vp, vp]
+            lib.moe_forward.argtypes = [vp, vp, i32, vp, vp]
+            lib.moe_forward_host.argtypes = [vp, vp, i32, vp, vp]
+            lib.moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            lib.moe_get_logits.argtypes = [vp, vp, vp, vp]
+            lib.moe_get_status.argtypes = [vp, i32]
+            lib.moe_weight_bytes.argtypes = [vp]
+            lib.moe_weight_bytes.restype = ctypes.c_size_t
+            lib.moe_last_error.argtypes = [vp]
+            lib.moe_last_error.restype = ctypes.c_char_p
+            lib.moe_destroy.argtypes = [vp]
+            lib.moe_destroy.restype = None
+            for name in ("moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
+                         "moe_get_routing", "moe_get_logits", "moe_get_status"):
+                getattr(lib, name).restype = i32
+            _lib = lib
+    return _lib
+
+
+def ptr(a) -> int | None:
+    """Address of a numpy array or torch tensor (None stays None)."""
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    if hasattr(a, "data_ptr"):
+        assert a.is_contiguous(), "tensor must be contiguous"
+        return a.data_ptr()
+    assert a.flags["C_CONTIGUOUS"], "array must be C-contiguous"
+    return a.ctypes.data
+
+
+def stream_handle(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(ctx, rc: int, what: str) -> int:
+    if rc < 0:
+        msg = load_library().moe_last_error(ctx).decode(errors="replace")
+        raise MoeError(rc, f"{what}: {msg}")
+    return rc
+
+
+# ---------------------------------------------------------------- C ABI, same names
+
+def moe_create(cfg: moe_config, device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(None, load_library().moe_create(ctypes.byref(cfg), device, ctypes.byref(h)), "moe_create")
+    return h.value
+
+
+def moe_load_router(ctx: int, w, bias=None) -> None:
+    _check(ctx, load_library().moe_load_router(ctx, ptr(w), ptr(bias)), "moe_load_router")
+
+
+def moe_load_experts(ctx: int, codes, scales) -> None:
+    _check(ctx, load_library().moe_load_experts(ctx, ptr(codes), ptr(scales)), "moe_load_experts")
+
+
+def moe_forward(ctx: int, x, T: int, out, stream=None) -> None:
+    _check(ctx, load_library().moe_forward(ctx, ptr(x), T, ptr(out), stream_handle(stream)), "moe_forward")
+
+
+def moe_forward_host(ctx: int, x_host, T: int, out_host, stream=None) -> None:
+    _check(ctx, load_library().moe_forward_host(ctx, ptr(x_host), T, ptr(out_host), stream_handle(stream)),
+           "moe_forward_host")
+
+
+def moe_get_routing(ctx: int, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
+    _check(ctx, load_library().moe_get_routing(ctx, ptr(ids), ptr(gates), ptr(counts), ptr(offsets), ptr(perm),
+                                               stream_handle(stream)), "moe_get_routing")
+
+
+def moe_get_logits(ctx: int, hi=None, lo=None, stream=None) -> None:
+    _check(ctx, load_library().moe_get_logits(ctx, ptr(hi), ptr(lo), stream_handle(stream)), "moe_get_logits")
+
+
+def moe_get_status(ctx: int, clear: bool = False) -> int:
+    return load_library().moe_get_status(ctx, 1 if clear else 0)
+
+
+def moe_weight_bytes(ctx: int) -> int:
+    return load_library().moe_weight_bytes(ctx)
+
+
+def moe_last_error(ctx: int | None) -> str:
+    return load_library().moe_last_error(ctx).decode(errors="replace")
+
+
+def moe_destroy(ctx: int | None) -> None:
+    if ctx:
+        load_library().moe_destroy(ctx)
+
+
+# ---------------------------------------------------------------- convenience wrapper
+
+@dataclass
+class LayerShape:
+    d: int
+    ffn: int
+    n_experts: int
+    top_k: int
+    shared_ffn: int = 0
+    t_max: int = 16
+    out_dtype: int = MOE_OUT_BF16
+
+    def config(self) -> moe_config:
+        return moe_config(self.d, self.ffn, self.n_experts, self.top_k, self.shared_ffn, self.t_max,
+                          self.out_dtype, 0)
+
+
+class MoeLayer:
+    """Owns one context (one layer's weights and workspace) on one device."""
+
+    def __init__(self, shape: LayerShape, device: int = 0):
+        self.shape = shape
+        self.device = device
+        self.ctx = moe_create(shape.config(), device)
+
+    def load(self, w_router, bias, codes, scales) -> "MoeLayer":
+        moe_load_router(self.ctx, w_router, bias)
+        moe_load_experts(self.ctx, codes, scales)
+        return self
+
+    def forward(self, x, T: int, out, stream=None) -> None:
+        moe_forward(self.ctx, x, T, out, stream)
+
+    def forward_host(self, x_host, T: int, out_host, stream=None) -> None:
+        moe_forward_host(self.ctx, x_host, T, out_host, stream)
+
+    def routing(self, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
+        moe_get_routing(self.ctx, ids, gates, counts, offsets, perm, stream)
+
+    def logits(self, hi=None, lo=None, stream=None) -> None:
+        moe_get_logits(self.ctx, hi, lo, stream)
+
+    def status(self, clear: bool = False) -> int:
+        return moe_get_status(self.ctx, clear)
+
+    def weight_bytes(self) -> int:
+        return moe_weight_bytes(self.ctx)
+
+    def close(self) -> None:
+        if self.ctx:
+            moe_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,341 @@
+// Host side of the routed-expert FFN library: context, loads, forward, debug
+// exports. The C ABI is declared in include/moe.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/moe.h"
+#include "moe_internal.h"
+
+struct moe_ctx {
+  moe_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  bool router_loaded = false;
+  bool experts_loaded = false;
+  std::string err;
+  // weights
+  uint8_t* packed = nullptr;
+  size_t packed_bytes = 0;
+  size_t expert_stride = 0;
+  float* w_router = nullptr;
+  float* bias = nullptr;
+  bool has_bias = false;
+  // workspace (one allocation, zeroed at create)
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  moe::FwdParams base{};
+  void* x_dev = nullptr;    // host-API staging of x
+  void* out_dev = nullptr;  // host-API staging of out
+  int* load_err = nullptr;  // repack NaN-scale flag
+  int last_T = 0;
+};
+
+namespace {
+
+std::string g_create_error;
+
+// Makes ctx's device current for the duration of a call and restores the
+// caller's device afterwards.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+int fail(moe_ctx* ctx, int code, const std::string& msg) {
+  if (ctx) ctx->err = msg;
+  else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(moe_ctx* ctx, cudaError_t e, const char* what) {
+  return fail(ctx, MOE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
+  if (!out) return fail(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return fail(nullptr, MOE_ERR_INVALID_ARG, "cfg is NULL");
+  const moe_config& c = *cfg;
+  if (c.d <= 0 || c.d % 32 || c.ffn <= 0 || c.ffn % 32 || c.shared_ffn < 0 || c.shared_ffn % 32 ||
+      c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
+      c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) || c.flags)
+    return fail(nullptr, MOE_ERR_INVALID_ARG,
+                "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
+                "0 <= t_max <= 65536; out_dtype 0/1; flags 0)");
+  moe_ctx* ctx = new (std::nothrow) moe_ctx();
+  if (!ctx) return fail(nullptr, MOE_ERR_NOMEM, "host allocation failed");
+  ctx->cfg = c;
+  ctx->device = device;
+  DeviceGuard guard(device);
+  if (!guard.ok) {
+    delete ctx;
+    return fail(nullptr, MOE_ERR_CUDA, "cudaSetDevice failed");
+  }
+  cudaError_t e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) {
+    delete ctx;
+    return fail(nullptr, MOE_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+  }
+  const int d = c.d, F = c.ffn, E = c.n_experts, k = c.top_k, S = c.shared_ffn, Tm = std::max(c.t_max, 1);
+  ctx->expert_stride = moe::expert_packed_bytes(d, F);
+  ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
+
+  const size_t Pm = (size_t)Tm * k, Qm = Pm + (S > 0 ? (size_t)Tm : 0);
+  const int d64 = moe::k64_tiles(d) * 64;
+  const int fmax64 = moe::k64_tiles(std::max(F, S)) * 64;
+  const int hgroups = fmax64 / 16;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_x16 = take((size_t)Tm * d64 * 2), o_xinv = take((size_t)Tm * 4);
+  const size_t o_lh = take((size_t)Tm * E * 4), o_ll = take((size_t)Tm * E * 4);
+  const size_t o_ids = take(Pm * 4), o_gates = take(Pm * 4), o_counts = take((size_t)E * 4),
+               o_offsets = take((size_t)(E + 1) * 4), o_perm = take(Pm * 4), o_inv = take(Pm * 4);
+  const size_t o_ns = take(4), o_se = take((size_t)(E + 1) * 4), o_sq = take((size_t)(E + 1) * 4),
+               o_sn = take((size_t)(E + 1) * 4), o_gp = take((size_t)(E + 2) * 4), o_dp = take((size_t)(E + 2) * 4);
+  const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
+  const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
+  const size_t o_status = take(4), o_lerr = take(4);
+  ctx->ws_bytes = off;
+
+  if ((e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&ctx->w_router, (size_t)E * d * 4)) != cudaSuccess ||
+      (e = cudaMalloc(&ctx->bias, (size_t)E * 4)) != cudaSuccess ||
+      (e = cudaMalloc(&ctx->ws, ctx->ws_bytes)) != cudaSuccess) {
+    moe_destroy(ctx);
+    return fail(nullptr, MOE_ERR_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  }
+  if ((e = cudaMemset(ctx->ws, 0, ctx->ws_bytes)) != cudaSuccess ||
+      (e = cudaMemset(ctx->bias, 0, (size_t)E * 4)) != cudaSuccess) {
+    moe_destroy(ctx);
+    return fail(nullptr, MOE_ERR_CUDA, std::string("cudaMemset: ") + cudaGetErrorString(e));
+  }
+  char* w = static_cast<char*>(ctx->ws);
+  moe::FwdParams& p = ctx->base;
+  p.d = d;
+  p.F = F;
+  p.E = E;
+  p.k = k;
+  p.S = S;
+  p.d64 = d64;
+  p.fmax64 = fmax64;
+  p.hgroups = hgroups;
+  p.out_f32 = c.out_dtype == MOE_OUT_F32;
+  p.w_router = ctx->w_router;
+  p.bias = nullptr;
+  p.packed = ctx->packed;
+  p.expert_stride = ctx->expert_stride;
+  p.x16 = reinterpret_cast<uint16_t*>(w + o_x16);
+  p.xinv = reinterpret_cast<float*>(w + o_xinv);
+  p.logit_hi = reinterpret_cast<float*>(w + o_lh);
+  p.logit_lo = reinterpret_cast<float*>(w + o_ll);
+  p.ids = reinterpret_cast<int32_t*>(w + o_ids);
+  p.gates = reinterpret_cast<float*>(w + o_gates);
+  p.counts = reinterpret_cast<int32_t*>(w + o_counts);
+  p.offsets = reinterpret_cast<int32_t*>(w + o_offsets);
+  p.perm = reinterpret_cast<int32_t*>(w + o_perm);
+  p.inv = reinterpret_cast<int32_t*>(w + o_inv);
+  p.n_slots = reinterpret_cast<int32_t*>(w + o_ns);
+  p.slot_expert = reinterpret_cast<int32_t*>(w + o_se);
+  p.slot_q0 = reinterpret_cast<int32_t*>(w + o_sq);
+  p.slot_n = reinterpret_cast<int32_t*>(w + o_sn);
+  p.gu_prefix = reinterpret_cast<int32_t*>(w + o_gp);
+  p.dn_prefix = reinterpret_cast<int32_t*>(w + o_dp);
+  p.hbuf = reinterpret_cast<uint16_t*>(w + o_h);
+  p.hscale = reinterpret_cast<float*>(w + o_hs);
+  p.part = reinterpret_cast<float*>(w + o_part);
+  p.status = reinterpret_cast<int*>(w + o_status);
+  ctx->x_dev = w + o_xd;
+  ctx->out_dev = w + o_od;
+  ctx->load_err = reinterpret_cast<int*>(w + o_lerr);
+  *out = ctx;
+  return MOE_OK;
+}
+
+int moe_load_router(moe_ctx* ctx, const float* wr, const float* bias) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (!wr) return fail(ctx, MOE_ERR_INVALID_ARG, "router weights are NULL");
+  DeviceGuard guard(ctx->device);
+  const size_t n = (size_t)ctx->cfg.n_experts * ctx->cfg.d;
+  cudaError_t e = cudaMemcpy(ctx->w_router, wr, n * 4, cudaMemcpyDefault);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router copy");
+  if (bias) {
+    e = cudaMemcpy(ctx->bias, bias, (size_t)ctx->cfg.n_experts * 4, cudaMemcpyDefault);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "bias copy");
+  }
+  ctx->has_bias = bias != nullptr;
+  ctx->base.bias = ctx->has_bias ? ctx->bias : nullptr;
+  ctx->router_loaded = true;
+  return MOE_OK;
+}
+
+int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (!codes || !scales) return fail(ctx, MOE_ERR_INVALID_ARG, "codes or scales are NULL");
+  DeviceGuard guard(ctx->device);
+  const int d = ctx->cfg.d, F = ctx->cfg.ffn, E = ctx->cfg.n_experts, S = ctx->cfg.shared_ffn;
+  const size_t ccs = (size_t)3 * F * d / 2, css = (size_t)3 * F * d / 32;  // canonical strides
+  const size_t chunk_bytes = (size_t)256 << 20;
+  const int per_chunk = (int)std::max<size_t>(1, chunk_bytes / ccs);
+  const size_t stage_c = std::max(ccs * (size_t)std::min(per_chunk, E), S > 0 ? (size_t)3 * S * d / 2 : 0);
+  const size_t stage_s = std::max(css * (size_t)std::min(per_chunk, E), S > 0 ? (size_t)3 * S * d / 32 : 0);
+  uint8_t* sc = nullptr;
+  uint8_t* ss = nullptr;
+  cudaError_t e = cudaMalloc(&sc, stage_c);
+  if (e == cudaSuccess) e = cudaMalloc(&ss, stage_s);
+  if (e != cudaSuccess) {
+    cudaFree(sc);
+    return fail(ctx, MOE_ERR_NOMEM, std::string("staging cudaMalloc: ") + cudaGetErrorString(e));
+  }
+  int rc = MOE_OK;
+  e = cudaMemset(ctx->load_err, 0, 4);
+  for (int x0 = 0; x0 < E && e == cudaSuccess; x0 += per_chunk) {
+    const int n = std::min(per_chunk, E - x0);
+    if ((e = cudaMemcpy(sc, codes + (size_t)x0 * ccs, ccs * n, cudaMemcpyDefault)) != cudaSuccess) break;
+    if ((e = cudaMemcpy(ss, scales + (size_t)x0 * css, css * n, cudaMemcpyDefault)) != cudaSuccess) break;
+    if ((e = moe::launch_repack(sc, ss, n, d, F, ccs, css, ctx->packed + (size_t)x0 * ctx->expert_stride,
+                                ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
+      break;
+    e = cudaDeviceSynchronize();
+  }
+  if (e == cudaSuccess && S > 0) {
+    const size_t sc_b = (size_t)3 * S * d / 2, ss_b = (size_t)3 * S * d / 32;
+    if ((e = cudaMemcpy(sc, codes + (size_t)E * ccs, sc_b, cudaMemcpyDefault)) == cudaSuccess &&
+        (e = cudaMemcpy(ss, scales + (size_t)E * css, ss_b, cudaMemcpyDefault)) == cudaSuccess &&
+        (e = moe::launch_repack(sc, ss, 1, d, S, sc_b, ss_b, ctx->packed + (size_t)E * ctx->expert_stride,
+                                moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess)
+      e = cudaDeviceSynchronize();
+  }
+  int nan_flag = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&nan_flag, ctx->load_err, 4, cudaMemcpyDeviceToHost);
+  cudaFree(sc);
+  cudaFree(ss);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "expert load");
+  if (nan_flag) {
+    ctx->experts_loaded = false;
+    return fail(ctx, MOE_ERR_NAN_SCALE, "an E8M0 scale byte is 0xFF (NaN)");
+  }
+  ctx->experts_loaded = true;
+  return rc;
+}
+
+int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return fail(ctx, MOE_ERR_INVALID_ARG, "T < 0");
+  if (T > ctx->cfg.t_max) return fail(ctx, MOE_ERR_T_TOO_LARGE, "T exceeds t_max");
+  if (!ctx->router_loaded || !ctx->experts_loaded) return fail(ctx, MOE_ERR_NOT_LOADED, "router or experts not loaded");
+  if (T > 0 && (!x || !out)) return fail(ctx, MOE_ERR_INVALID_ARG, "x or out is NULL");
+  if (T > 0 && (!aligned16(x) || !aligned16(out)))
+    return fail(ctx, MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  DeviceGuard guard(ctx->device);
+  moe::FwdParams p = ctx->base;
+  p.T = T;
+  p.P = T * ctx->cfg.top_k;
+  p.x = static_cast<const uint16_t*>(x);
+  p.out = out;
+  ctx->last_T = T;
+  cudaError_t e = moe::launch_forward(p, static_cast<cudaStream_t>(stream), ctx->num_sms);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "forward launch");
+  return MOE_OK;
+}
+
+int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || T > ctx->cfg.t_max) return moe_forward(ctx, x_host, T, out_host, stream);
+  if (T > 0 && (!x_host || !out_host)) return fail(ctx, MOE_ERR_INVALID_ARG, "x or out is NULL");
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * ctx->cfg.d * 2;
+  const size_t ob = (size_t)T * ctx->cfg.d * (ctx->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
+  cudaError_t e = cudaSuccess;
+  if (T > 0) e = cudaMemcpyAsync(ctx->x_dev, x_host, xb, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "x copy");
+  int rc = moe_forward(ctx, ctx->x_dev, T, ctx->out_dev, stream);
+  if (rc != MOE_OK) return rc;
+  if (T > 0) e = cudaMemcpyAsync(out_host, ctx->out_dev, ob, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "out copy");
+  return MOE_OK;
+}
+
+int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
+                    void* stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t P = (size_t)ctx->last_T * ctx->cfg.top_k;
+  const moe::FwdParams& p = ctx->base;
+  cudaError_t e = cudaSuccess;
+  if (ids && P && e == cudaSuccess) e = cudaMemcpyAsync(ids, p.ids, P * 4, cudaMemcpyDefault, s);
+  if (gates && P && e == cudaSuccess) e = cudaMemcpyAsync(gates, p.gates, P * 4, cudaMemcpyDefault, s);
+  if (counts && e == cudaSuccess) e = cudaMemcpyAsync(counts, p.counts, (size_t)ctx->cfg.n_experts * 4, cudaMemcpyDefault, s);
+  if (offsets && e == cudaSuccess)
+    e = cudaMemcpyAsync(offsets, p.offsets, (size_t)(ctx->cfg.n_experts + 1) * 4, cudaMemcpyDefault, s);
+  if (perm && P && e == cudaSuccess) e = cudaMemcpyAsync(perm, p.perm, P * 4, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "routing copy");
+  return MOE_OK;
+}
+
+int moe_get_logits(moe_ctx* ctx, float* hi, float* lo, void* stream) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t n = (size_t)ctx->last_T * ctx->cfg.n_experts * 4;
+  cudaError_t e = cudaSuccess;
+  if (hi && n) e = cudaMemcpyAsync(hi, ctx->base.logit_hi, n, cudaMemcpyDefault, s);
+  if (lo && n && e == cudaSuccess) e = cudaMemcpyAsync(lo, ctx->base.logit_lo, n, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "logits copy");
+  return MOE_OK;
+}
+
+int moe_get_status(moe_ctx* ctx, int clear) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  int st = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&st, ctx->base.status, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(ctx->base.status, 0, 4);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
+  return st;
+}
+
+size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }
+
+const char* moe_last_error(const moe_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+void moe_destroy(moe_ctx* ctx) {
+  if (!ctx) return;
+  {
+    DeviceGuard guard(ctx->device);
+    cudaFree(ctx->packed);
+    cudaFree(ctx->w_router);
+    cudaFree(ctx->bias);
+    cudaFree(ctx->ws);
+  }
+  delete ctx;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Internal structures shared by the host side (moe_api.cu) and the kernels
+// (moe_kernels.cu) of the routed-expert FFN library. Not part of the ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- packed weight tiles
+//
+// Every MXFP4 matrix (R rows x K columns, K along the reduction axis) is stored
+// as tiles of 16 rows x 64 columns: 512 code bytes followed by 32 scale bytes
+// (kTileBytes = 544, 16-byte aligned). Lane L = 4*g + c of a warp owns code
+// bytes [16L, 16L+16) of a tile:
+//   [0,4)   row g,   block 0 of the tile, code bytes 4c..4c+3 of that block
+//   [4,8)   row g+8, block 0
+//   [8,12)  row g,   block 1
+//   [12,16) row g+8, block 1
+// and the quad of lanes with the same g shares the 4 scale bytes at 512 + 4g:
+//   scale(row g, block 0), scale(row g+8, block 0), scale(row g, block 1),
+//   scale(row g+8, block 1).
+// A "block" is one 32-element scale block (16 code bytes). Columns past K are
+// padding: code 0 and scale 127. One warp-wide 16-byte load per lane therefore
+// brings exactly the A fragments of four m16n8k16 MMAs (two per block).
+//
+// Which 16 rows a tile holds:
+//   down [d x f]:     tile m holds rows 16m .. 16m+15.
+//   gate/up [2f x d]: pair-tile tau holds gate rows S_tau and up rows f + S_tau,
+//                     S_tau[r] = 32*(tau/2) + 8*(r/4) + 4*(tau%2) + (r%4),
+//                     which is the element set one MMA of the down projection
+//                     consumes, so h can be scaled per MMA (see the kernels).
+// Expert layout: gate/up tiles ordered [tau][kt][gate, up], then down tiles
+// ordered [m][kt].
+constexpr int kTileBytes = 544;
+constexpr int kTileCodeBytes = 512;
+
+__host__ __device__ inline int k64_tiles(int K) { return (K + 63) / 64; }
+__host__ __device__ inline size_t gu_packed_bytes(int d, int f) {
+  return (size_t)(f / 16) * (size_t)k64_tiles(d) * 2 * kTileBytes;
+}
+__host__ __device__ inline size_t dn_packed_bytes(int d, int f) {
+  return (size_t)(d / 16) * (size_t)k64_tiles(f) * kTileBytes;
+}
+__host__ __device__ inline size_t expert_packed_bytes(int d, int f) {
+  return gu_packed_bytes(d, f) + dn_packed_bytes(d, f);
+}
+
+// ---------------------------------------------------------------- forward parameters
+
+struct FwdParams {
+  // sizes
+  int T, d, F, E, k, S;  // S = shared ffn (0 = none)
+  int P;                 // T * k
+  int d64, fmax64;       // padded row pitches (elements) of x16 and h planes
+  int hgroups;           // fmax64 / 16: h scale groups per pair row
+  int out_f32;
+  // inputs
+  const uint16_t* x;     // bf16 [T][d]
+  const float* w_router; // [E][d]
+  const float* bias;     // [E] or nullptr
+  const uint8_t* packed; // packed experts
+  size_t expert_stride;  // packed bytes per routed expert
+  // workspace
+  uint16_t* x16;         // f16 [t_max][d64], x * 2^sigma_t
+  float* xinv;           // [t_max]: 2^-sigma_t
+  float* logit_hi;       // [t_max][E]
+  float* logit_lo;
+  int32_t* ids;          // [t_max][k]
+  float* gates;          // [t_max][k]
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* perm;         // [P_max]
+  int32_t* inv;          // [P_max]
+  // work list (one slot per expert that received pairs, then the shared expert)
+  int32_t* n_slots;      // [1]
+  int32_t* slot_expert;  // [E+1]  (E = shared)
+  int32_t* slot_q0;      // [E+1]  first h/part row of the slot
+  int32_t* slot_n;       // [E+1]  rows (pairs) in the slot
+  int32_t* gu_prefix;    // [E+2]  prefix of gate/up units (f/16 per slot)
+  int32_t* dn_prefix;    // [E+2]  prefix of down units (d/16 per slot)
+  uint16_t* hbuf;        // f16 [Q_max][2][fmax64]: hi and lo planes of h * 2^sigma
+  float* hscale;         // [Q_max][hgroups]: 2^-sigma per 16-element group
+  float* part;           // [Q_max][d]: W_down h of every row q
+  void* out;             // [T][d] bf16 or fp32
+  int* status;           // device status word
+};
+
+// Launchers (moe_kernels.cu). All are asynchronous on `stream`.
+cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
+                          size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
+                          int* err_flag, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,684 @@
+// sm_103a kernels of the routed-expert FFN layer.
+//
+// Forward = seven stream-ordered steps:
+//   prep_x   per-token power-of-two scaling of x into f16 (exact for bf16 x)
+//   router   l[t,e] = W_r[e] . x_t + b[e] as a double-float (hi + lo) sum
+//   topk     warp top-k with lower-index tie break, softmax gates over the k
+//   bucket   counting sort of the T*k pairs by expert, and the work list
+//   gateup   grouped MXFP4 dequant-GEMV on tensor cores: h = SiLU(gate) * up
+//   down     grouped MXFP4 dequant-GEMV: part = W_down h
+//   combine  y_t = sum_j g[t,j] part(t,j) + shared_t, slot order, one rounding
+//
+// Where the pages describe the step (page title, section):
+//   router/top-k: "Neural Server" technical page, "How one token and one prompt
+//     are processed" (router and top-k write 4 ids and 4 weights per token).
+//   grouping by expert, fused gate/up then down, per-token summation of a row
+//     over all its experts in a fixed order: "NInfer" Qwen3.8-Flash-Next notes,
+//     MoE execution bullets; fixed-order reductions: "Neural Server", "The CPU
+//     kernel".
+//
+// Numerics. MXFP4 weights decode exactly to f16 (cvt.rn.f16x2.e2m1x2); the
+// E8M0 scale of each 32-element block is applied in fp32 to that block's
+// partial MMA sum. x (bf16) enters the MMA as f16 after multiplication by
+// 2^sigma_t with max|x_t| * 2^sigma_t in [2^14, 2^15): exact except for
+// elements below max|x_t| * 2^-28. h enters the down MMA as two f16 terms
+// (hi + lo, about 22 significant bits) with a power-of-two scale per 16
+// elements. All accumulation is fp32; all reductions run in a fixed order, so
+// a token's output bits do not depend on timing.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kNW = 8;  // warps per CTA of the expert kernels
+constexpr int kGuNT = 2;  // n8 token tiles per gate/up pass (16 tokens)
+constexpr int kDnNT = 4;  // n8 tiles per down pass (16 pairs: hi and lo columns)
+
+// ---------------------------------------------------------------- primitives
+
+__device__ __forceinline__ uint4 ld16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ uint32_t ld4(const void* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
+
+// Two E2M1 codes (low nibble -> low half, high nibble -> high half) to f16x2.
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t word, int byte) {
+  uint32_t r;
+  uint16_t b = (uint16_t)((word >> (8 * byte)) & 0xFFu);
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "h"(b));
+  return r;
+}
+
+// E8M0 byte to fp32: 2^(e-127); e = 0 is the subnormal 2^-127.
+__device__ __forceinline__ float e8m0_f32(uint32_t e) { return __uint_as_float(e ? (e << 23) : 0x00400000u); }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragments of the two MMAs of scale block bb from a lane's 16 code bytes.
+// MMA 1 takes code bytes 4c, 4c+1 of the block (elements 8c..8c+3), MMA 2 bytes
+// 4c+2, 4c+3 (elements 8c+4..8c+7); the B fragment is loaded to match.
+__device__ __forceinline__ void a_frags(const uint4 q, int bb, uint32_t (&a1)[4], uint32_t (&a2)[4]) {
+  const uint32_t rg = bb ? q.z : q.x, rg8 = bb ? q.w : q.y;
+  a1[0] = e2m1x2_f16x2(rg, 0);
+  a1[1] = e2m1x2_f16x2(rg8, 0);
+  a1[2] = e2m1x2_f16x2(rg, 1);
+  a1[3] = e2m1x2_f16x2(rg8, 1);
+  a2[0] = e2m1x2_f16x2(rg, 2);
+  a2[1] = e2m1x2_f16x2(rg8, 2);
+  a2[2] = e2m1x2_f16x2(rg, 3);
+  a2[3] = e2m1x2_f16x2(rg8, 3);
+}
+
+// Gate/up tile: acc[nt] (rows g, g+8 x columns 2c, 2c+1 of n8 tile nt) +=
+// sum over the tile's two scale blocks of scale(row, block) * (codes . x16).
+template <int NT>
+__device__ __forceinline__ void gu_tile(const uint4 q, uint32_t sc, const uint4 (&bx)[NT][2], float (&acc)[NT][4]) {
+#pragma unroll
+  for (int bb = 0; bb < 2; ++bb) {
+    uint32_t a1[4], a2[4];
+    a_frags(q, bb, a1, a2);
+    const float sg = e8m0_f32((sc >> (16 * bb)) & 0xFFu);
+    const float sg8 = e8m0_f32((sc >> (16 * bb + 8)) & 0xFFu);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float t[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(t, a1, bx[nt][bb].x, bx[nt][bb].y);
+      mma16816(t, a2, bx[nt][bb].z, bx[nt][bb].w);
+      acc[nt][0] = fmaf(t[0], sg, acc[nt][0]);
+      acc[nt][1] = fmaf(t[1], sg, acc[nt][1]);
+      acc[nt][2] = fmaf(t[2], sg8, acc[nt][2]);
+      acc[nt][3] = fmaf(t[3], sg8, acc[nt][3]);
+    }
+  }
+}
+
+// Down tile: columns are (hi, lo) planes of pairs; acc[nt][0|1] = rows g | g+8
+// of pair c of tile nt. sb[nt][bb] holds the two per-MMA scales of pair c's h.
+template <int NT>
+__device__ __forceinline__ void dn_tile(const uint4 q, uint32_t sc, const uint4 (&bh)[NT][2],
+                                        const float2 (&sb)[NT][2], float (&acc)[NT][2]) {
+#pragma unroll
+  for (int bb = 0; bb < 2; ++bb) {
+    uint32_t a1[4], a2[4];
+    a_frags(q, bb, a1, a2);
+    const float sg = e8m0_f32((sc >> (16 * bb)) & 0xFFu);
+    const float sg8 = e8m0_f32((sc >> (16 * bb + 8)) & 0xFFu);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float t1[4] = {0.f, 0.f, 0.f, 0.f}, t2[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(t1, a1, bh[nt][bb].x, bh[nt][bb].y);
+      mma16816(t2, a2, bh[nt][bb].z, bh[nt][bb].w);
+      const float s1 = sb[nt][bb].x, s2 = sb[nt][bb].y;
+      acc[nt][0] = fmaf(t1[0] + t1[1], sg * s1, acc[nt][0]);
+      acc[nt][0] = fmaf(t2[0] + t2[1], sg * s2, acc[nt][0]);
+      acc[nt][1] = fmaf(t1[2] + t1[3], sg8 * s1, acc[nt][1]);
+      acc[nt][1] = fmaf(t2[2] + t2[3], sg8 * s2, acc[nt][1]);
+    }
+  }
+}
+
+// Power-of-two exponent sigma with m * 2^sigma in [2^14, 2^15) for m > 0,
+// clamped so that both 2^sigma and 2^-sigma are normal fp32 numbers.
+__device__ __forceinline__ int f16_headroom_exponent(float m) {
+  if (!(m > 0.f)) return 0;
+  int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;  // floor(log2 m) for normal m
+  int s = 14 - ex;
+  return s < -112 ? -112 : (s > 126 ? 126 : s);
+}
+__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
+
+// ---------------------------------------------------------------- double-float helpers
+// Error-free transformations (Knuth TwoSum, FMA-based TwoProduct); the _rn
+// intrinsics keep the compiler from contracting or reassociating them.
+struct dd {
+  float hi, lo;
+};
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+__device__ __forceinline__ void dd_mac(dd& acc, float a, float b) {
+  float p = __fmul_rn(a, b);
+  float pe = __fmaf_rn(a, b, -p);
+  float s, e;
+  two_sum(acc.hi, p, s, e);
+  acc.hi = s;
+  acc.lo = __fadd_rn(acc.lo, __fadd_rn(e, pe));
+}
+__device__ __forceinline__ dd dd_add(dd a, dd b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  dd r;
+  r.hi = __fadd_rn(s, e);
+  r.lo = __fsub_rn(e, __fsub_rn(r.hi, s));
+  return r;
+}
+__device__ __forceinline__ dd dd_shfl_xor(dd a, int m) {
+  dd r;
+  r.hi = __shfl_xor_sync(0xffffffffu, a.hi, m);
+  r.lo = __shfl_xor_sync(0xffffffffu, a.lo, m);
+  return r;
+}
+__device__ __forceinline__ bool dd_greater(float ah, float al, int ai, float bh, float bl, int bi) {
+  // (a > b) in value, then the lower index first; pairs are normalised (|lo| <= ulp(hi)/2).
+  if (ah != bh) return ah > bh;
+  if (al != bl) return al > bl;
+  return ai < bi;
+}
+
+// ---------------------------------------------------------------- prep_x
+
+__global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
+  const int t = blockIdx.x;
+  const uint16_t* xt = p.x + (size_t)t * p.d;
+  __shared__ float wmax[8];
+  float m = 0.f;
+  for (int i = threadIdx.x; i < p.d; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)xt[i] << 16)));
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, wmax[w]);
+  const int s = f16_headroom_exponent(m);
+  const float sc = pow2f(s);
+  __half* dst = reinterpret_cast<__half*>(p.x16) + (size_t)t * p.d64;
+  for (int i = threadIdx.x; i < p.d; i += blockDim.x)
+    dst[i] = __float2half_rn(__uint_as_float((uint32_t)xt[i] << 16) * sc);
+  if (threadIdx.x == 0) p.xinv[t] = pow2f(-s);
+}
+
+// ---------------------------------------------------------------- router
+
+// Block (e, token tile of 16): lanes stride over d in groups of 8 elements,
+// accumulate double-float sums, then a fixed-shape block reduction.
+constexpr int kRouterThreads = 128;
+constexpr int kRouterTT = 16;
+
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(FwdParams p) {
+  const int e = blockIdx.x;
+  const int t0 = blockIdx.y * kRouterTT;
+  const int nt = min(kRouterTT, p.T - t0);
+  dd acc[kRouterTT];
+#pragma unroll
+  for (int i = 0; i < kRouterTT; ++i) acc[i] = dd{0.f, 0.f};
+  const float* w = p.w_router + (size_t)e * p.d;
+  for (int i8 = threadIdx.x; i8 < p.d / 8; i8 += kRouterThreads) {
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8);
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8 + 1);
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int tt = 0; tt < kRouterTT; ++tt) {
+      if (tt < nt) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + tt) * p.d) + i8);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dd_mac(acc[tt], __uint_as_float(xw[j] << 16), wv[2 * j]);
+          dd_mac(acc[tt], __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
+        }
+      }
+    }
+  }
+  __shared__ dd part[kRouterThreads / 32][kRouterTT];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int tt = 0; tt < kRouterTT; ++tt) {
+    dd v = acc[tt];
+    for (int o = 16; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
+    if (lane == 0) part[warp][tt] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    const int tt = threadIdx.x;
+    dd v = part[0][tt];
+    for (int w2 = 1; w2 < kRouterThreads / 32; ++w2) v = dd_add(v, part[w2][tt]);
+    if (p.bias) v = dd_add(v, dd{p.bias[e], 0.f});
+    p.logit_hi[(size_t)(t0 + tt) * p.E + e] = v.hi;
+    p.logit_lo[(size_t)(t0 + tt) * p.E + e] = v.lo;
+  }
+}
+
+// ---------------------------------------------------------------- top-k and gates
+
+constexpr int kTopkWarps = 8;
+constexpr int kMaxEPerLane = 16;  // E <= 512
+
+// One warp per token: k rounds of a warp arg-max over the double-float logits
+// (value first, then the lower expert index), then the softmax of the k.
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(FwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+  if (t >= p.T) return;
+  const int E = p.E, k = p.k;
+  float vh[kMaxEPerLane], vl[kMaxEPerLane];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxEPerLane; ++i) {
+    const int e = lane + 32 * i;
+    vh[i] = (e < E) ? p.logit_hi[(size_t)t * E + e] : -INFINITY;
+    vl[i] = (e < E) ? p.logit_lo[(size_t)t * E + e] : 0.f;
+    if (e >= E) taken |= 1u << i;
+  }
+  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  int sel_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bh = -INFINITY, bl = 0.f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxEPerLane; ++i) {
+      if (!((taken >> i) & 1u) && dd_greater(vh[i], vl[i], lane + 32 * i, bh, bl, bi)) {
+        bh = vh[i];
+        bl = vl[i];
+        bi = lane + 32 * i;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
+        bh = oh;
+        bl = ol;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) {
+      top_h = bh;
+      top_l = bl;
+    }
+    if (lane == j) {
+      sel_h = bh;
+      sel_l = bl;
+      sel_id = bi;
+    }
+  }
+  float ex = 0.f;
+  if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
+  float sum = ex;
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    p.ids[(size_t)t * k + lane] = sel_id;
+    p.gates[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
+// ---------------------------------------------------------------- bucketing and work list
+
+constexpr int kBucketThreads = 1024;
+
+// Counting sort of the P = T*k pairs by expert (histogram, exclusive scan,
+// ranks within a bucket in pair order), then one work-list slot per expert
+// that received pairs (expert order) and the shared expert last.
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = p.E, T = p.T, P = p.P;
+  __shared__ int cnt[512];
+  __shared__ int run[512];
+  __shared__ int offs[513];
+  for (int e = threadIdx.x; e < E; e += kBucketThreads) {
+    cnt[e] = 0;
+    run[e] = 0;
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < P; q += kBucketThreads) atomicAdd(&cnt[p.ids[q]], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      offs[e] = acc;
+      acc += cnt[e];
+    }
+    offs[E] = acc;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kBucketThreads) {
+    p.offsets[e] = offs[e];
+    if (e < E) p.counts[e] = cnt[e];
+  }
+  if (warp == 0) {
+    for (int base = 0; base < P; base += 32) {
+      const int q = base + lane;
+      const bool valid = q < P;
+      const int e = valid ? p.ids[q] : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      const int before = valid ? run[e] : 0;
+      __syncwarp();
+      if (valid && rank == 0) run[e] = before + __popc(same);
+      __syncwarp();
+      if (valid) {
+        const int pos = offs[e] + before + rank;
+        p.perm[pos] = q;
+        p.inv[q] = pos;
+      }
+    }
+  }
+  if (threadIdx.x == 32) {
+    int ns = 0, gu = 0, dn = 0;
+    for (int e = 0; e < E; ++e) {
+      if (cnt[e] == 0) continue;
+      p.slot_expert[ns] = e;
+      p.slot_q0[ns] = offs[e];
+      p.slot_n[ns] = cnt[e];
+      p.gu_prefix[ns] = gu;
+      p.dn_prefix[ns] = dn;
+      gu += p.F / 16;
+      dn += p.d / 16;
+      ++ns;
+    }
+    if (p.S > 0 && T > 0) {
+      p.slot_expert[ns] = E;
+      p.slot_q0[ns] = P;
+      p.slot_n[ns] = T;
+      p.gu_prefix[ns] = gu;
+      p.dn_prefix[ns] = dn;
+      gu += p.S / 16;
+      dn += p.d / 16;
+      ++ns;
+    }
+    p.gu_prefix[ns] = gu;
+    p.dn_prefix[ns] = dn;
+    *p.n_slots = ns;
+  }
+}
+
+// ---------------------------------------------------------------- expert kernels
+
+__device__ __forceinline__ int find_slot(const int32_t* prefix, int n, int unit) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= unit) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int token_of_row(const FwdParams& p, int q) { return q < p.P ? p.perm[q] / p.k : q - p.P; }
+
+template <int NT>
+__global__ void __launch_bounds__(kNW * 32) gateup_kernel(FwdParams p) {
+  __shared__ float red[kNW][2 * NT * 4][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int nslots = *p.n_slots;
+  const int total = p.gu_prefix[nslots];
+  const int K64 = k64_tiles(p.d);
+  for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+    const int s = find_slot(p.gu_prefix, nslots, unit);
+    const int tau = unit - p.gu_prefix[s];
+    const int e = p.slot_expert[s], q0 = p.slot_q0[s], n = p.slot_n[s];
+    const uint8_t* wb = p.packed + (size_t)e * p.expert_stride + (size_t)tau * K64 * 2 * kTileBytes;
+    for (int m0 = 0; m0 < n; m0 += 8 * NT) {
+      int tokB[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int m = m0 + 8 * nt + g;
+        tokB[nt] = (m < n) ? token_of_row(p, q0 + m) : -1;
+      }
+      float accg[NT][4], accu[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) accg[nt][r] = accu[nt][r] = 0.f;
+      for (int kt = warp; kt < K64; kt += kNW) {
+        const uint8_t* tg = wb + (size_t)kt * 2 * kTileBytes;
+        const uint8_t* tu = tg + kTileBytes;
+        const uint4 qg = ld16(tg + 16 * lane);
+        const uint32_t sg = ld4(tg + kTileCodeBytes + 4 * g);
+        const uint4 qu = ld16(tu + 16 * lane);
+        const uint32_t su = ld4(tu + kTileCodeBytes + 4 * g);
+        uint4 bx[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb)
+            bx[nt][bb] = tokB[nt] >= 0 ? ld16(p.x16 + (size_t)tokB[nt] * p.d64 + kt * 64 + bb * 32 + c * 8)
+                                       : make_uint4(0, 0, 0, 0);
+        gu_tile<NT>(qg, sg, bx, accg);
+        gu_tile<NT>(qu, su, bx, accu);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          red[warp][nt * 4 + r][lane] = accg[nt][r];
+          red[warp][NT * 4 + nt * 4 + r][lane] = accu[nt][r];
+        }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float hv[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float gs = 0.f, us = 0.f;
+            for (int w = 0; w < kNW; ++w) {
+              gs += red[w][nt * 4 + r][lane];
+              us += red[w][NT * 4 + nt * 4 + r][lane];
+            }
+            const int m = m0 + 8 * nt + 2 * c + (r & 1);
+            float h = 0.f;
+            if (m < n) {
+              const float xi = p.xinv[token_of_row(p, q0 + m)];
+              const float gate = gs * xi, up = us * xi;
+              h = gate / (1.f + expf(-gate)) * up;
+            }
+            hv[r] = h;
+          }
+          // power-of-two scale per (row q, 16-element group tau): max over rows g, g+8, all g
+          float m0v = fmaxf(fabsf(hv[0]), fabsf(hv[2]));  // column 2c
+          float m1v = fmaxf(fabsf(hv[1]), fabsf(hv[3]));  // column 2c+1
+          for (int o = 4; o < 32; o <<= 1) {
+            m0v = fmaxf(m0v, __shfl_xor_sync(0xffffffffu, m0v, o));
+            m1v = fmaxf(m1v, __shfl_xor_sync(0xffffffffu, m1v, o));
+          }
+#pragma unroll
+          for (int col = 0; col < 2; ++col) {
+            const int m = m0 + 8 * nt + 2 * c + col;
+            if (m >= n) continue;
+            const int q = q0 + m;
+            const int sh = f16_headroom_exponent(col ? m1v : m0v);
+            const float sc = pow2f(sh);
+            __half* hi = reinterpret_cast<__half*>(p.hbuf) + (size_t)q * 2 * p.fmax64;
+            __half* lo = hi + p.fmax64;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const int rr = g + 8 * half;
+              const int i = 32 * (tau >> 1) + 8 * (rr >> 2) + 4 * (tau & 1) + (rr & 3);
+              const float v = hv[2 * half + col] * sc;
+              const __half vh = __float2half_rn(v);
+              hi[i] = vh;
+              lo[i] = __float2half_rn(v - __half2float(vh));
+            }
+            if (g == 0) p.hscale[(size_t)q * p.hgroups + tau] = pow2f(-sh);
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kNW * 32) down_kernel(FwdParams p) {
+  __shared__ float red[kNW][2 * NT][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int nslots = *p.n_slots;
+  const int total = p.dn_prefix[nslots];
+  for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+    const int s = find_slot(p.dn_prefix, nslots, unit);
+    const int rho = unit - p.dn_prefix[s];
+    const int e = p.slot_expert[s], q0 = p.slot_q0[s], n = p.slot_n[s];
+    const int f = (e == p.E) ? p.S : p.F;
+    const int K64 = k64_tiles(f);
+    const uint8_t* wb =
+        p.packed + (size_t)e * p.expert_stride + gu_packed_bytes(p.d, f) + (size_t)rho * K64 * kTileBytes;
+    for (int m0 = 0; m0 < n; m0 += 4 * NT) {
+      int qB[NT], qD[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int mb = m0 + 4 * nt + (g >> 1);
+        qB[nt] = (mb < n) ? q0 + mb : -1;
+        const int md = m0 + 4 * nt + c;
+        qD[nt] = (md < n) ? q0 + md : -1;
+      }
+      float acc[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+      for (int kt = warp; kt < K64; kt += kNW) {
+        const uint8_t* tile = wb + (size_t)kt * kTileBytes;
+        const uint4 q = ld16(tile + 16 * lane);
+        const uint32_t sc = ld4(tile + kTileCodeBytes + 4 * g);
+        uint4 bh[NT][2];
+        float2 sb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            bh[nt][bb] = qB[nt] >= 0 ? ld16(p.hbuf + ((size_t)qB[nt] * 2 + (g & 1)) * p.fmax64 + kt * 64 + bb * 32 + c * 8)
+                                     : make_uint4(0, 0, 0, 0);
+            sb[nt][bb] = qD[nt] >= 0 ? __ldg(reinterpret_cast<const float2*>(p.hscale + (size_t)qD[nt] * p.hgroups +
+                                                                              2 * (2 * kt + bb)))
+                                     : make_float2(0.f, 0.f);
+          }
+        dn_tile<NT>(q, sc, bh, sb, acc);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        red[warp][2 * nt][lane] = acc[nt][0];
+        red[warp][2 * nt + 1][lane] = acc[nt][1];
+      }
+      __syncthreads();
+      if (warp == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float r0 = 0.f, r1 = 0.f;
+          for (int w = 0; w < kNW; ++w) {
+            r0 += red[w][2 * nt][lane];
+            r1 += red[w][2 * nt + 1][lane];
+          }
+          if (qD[nt] >= 0) {
+            float* dst = p.part + (size_t)qD[nt] * p.d + 16 * rho;
+            dst[g] = r0;
+            dst[g + 8] = r1;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
+  const int t = blockIdx.y;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= p.d) return;
+  float acc = 0.f;
+  for (int j = 0; j < p.k; ++j) {
+    const int pj = t * p.k + j;
+    acc = fmaf(p.gates[pj], p.part[(size_t)p.inv[pj] * p.d + r], acc);
+  }
+  if (p.S > 0) acc += p.part[(size_t)(p.P + t) * p.d + r];
+  if (p.out_f32) reinterpret_cast<float*>(p.out)[(size_t)t * p.d + r] = acc;
+  else reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)t * p.d + r] = __float2bfloat16_rn(acc);
+}
+
+// ---------------------------------------------------------------- repack
+
+__device__ __forceinline__ int gu_row(int tau, int r) { return 32 * (tau >> 1) + 8 * (r >> 2) + 4 * (tau & 1) + (r & 3); }
+
+// One thread per (expert, tile, lane). Canonical matrix: codes [R][K/2], scales [R][K/32].
+__global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
+                              size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
+                              int* err) {
+  const int K64d = k64_tiles(d), K64f = k64_tiles(f);
+  const long long gu_tiles = (long long)(f / 16) * K64d * 2;
+  const long long dn_tiles = (long long)(d / 16) * K64f;
+  const long long per_exp = gu_tiles + dn_tiles;
+  const long long total = per_exp * n_exp * 32;
+  for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
+       gid += (long long)gridDim.x * blockDim.x) {
+    const int lane = (int)(gid & 31);
+    const long long tile = gid >> 5;
+    const int x = (int)(tile / per_exp);
+    const long long tl = tile % per_exp;
+    const int g = lane >> 2, c = lane & 3;
+    const uint8_t* mc;
+    const uint8_t* ms;
+    int K, kt, rows[2];
+    uint8_t* dst = out + (size_t)x * out_stride + (size_t)tl * kTileBytes;
+    if (tl < gu_tiles) {
+      const int tau = (int)(tl / (2 * K64d));
+      const int rem = (int)(tl % (2 * K64d));
+      kt = rem >> 1;
+      const int half = rem & 1;
+      K = d;
+      mc = codes + (size_t)x * canon_code_stride;
+      ms = scales + (size_t)x * canon_scale_stride;
+      rows[0] = half * f + gu_row(tau, g);
+      rows[1] = half * f + gu_row(tau, g + 8);
+    } else {
+      const long long t2 = tl - gu_tiles;
+      const int mt = (int)(t2 / K64f);
+      kt = (int)(t2 % K64f);
+      K = f;
+      mc = codes + (size_t)x * canon_code_stride + (size_t)f * d;
+      ms = scales + (size_t)x * canon_scale_stride + (size_t)2 * f * d / 32;
+      rows[0] = 16 * mt + g;
+      rows[1] = 16 * mt + g + 8;
+    }
+    __align__(16) uint8_t cb[16];
+    __align__(4) uint8_t sb[4];
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      const int blk = 2 * kt + bb;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const bool in = blk < K / 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          cb[8 * bb + 4 * rr + i] = in ? mc[(size_t)rows[rr] * (K / 2) + blk * 16 + 4 * c + i] : (uint8_t)0;
+        const uint8_t s = in ? ms[(size_t)rows[rr] * (K / 32) + blk] : (uint8_t)127;
+        if (s == 255) atomicExch(err, 1);
+        sb[2 * bb + rr] = s;
+      }
+    }
+    *reinterpret_cast<uint4*>(dst + 16 * lane) = *reinterpret_cast<const uint4*>(cb);
+    if (c == 0) *reinterpret_cast<uint32_t*>(dst + kTileCodeBytes + 4 * g) = *reinterpret_cast<const uint32_t*>(sb);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms) {
+  if (p.T == 0) return cudaSuccess;
+  prep_x_kernel<<<p.T, 256, 0, stream>>>(p);
+  router_kernel<<<dim3(p.E, (p.T + kRouterTT - 1) / kRouterTT), kRouterThreads, 0, stream>>>(p);
+  topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
+  bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
+  gateup_kernel<kGuNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  down_kernel<kDnNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  combine_kernel<<<dim3((p.d + 255) / 256, p.T), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
+                          size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
+                          int* err_flag, cudaStream_t stream) {
+  repack_kernel<<<1024, 256, 0, stream>>>(codes, scales, n_exp, d, f, canon_code_stride, canon_scale_stride, out,
+                                          out_stride, err_flag);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,185 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing (ids, counts, offsets, perm) must match bit for bit; gates within
+1e-6; outputs within 2e-2 * ||ref||_inf for bf16 and 1e-4 * ||ref||_inf for
+fp32 outputs. Sizes span several tiles and ragged tails; the full-size
+workloads are checked on sampled tokens (routing on all tokens).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from moe_testlib import (BF16_TOL, F32_TOL, build_lib, check_output, check_routing, make_layer, oracle_layer,
+                         oracle_route, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU not available for a gpu-marked test")
+    return build_lib()
+
+
+def _parity(m, wl, L, out_f32=False, tokens=None, t_max=None):
+    layer = make_layer(m, wl, L, t_max=t_max, out_f32=out_f32)
+    g = run_gpu(m, layer, L["x"], out_f32=out_f32)
+    assert g["status"] == 0
+    rr = oracle_route(wl, L)
+    check_routing(g, rr, wl.E)
+    ref = oracle_layer(wl, L, tokens=tokens)
+    y = g["y"] if tokens is None else g["y"][np.asarray(tokens)]
+    rel = check_output(y, ref["y"], F32_TOL if out_f32 else BF16_TOL)
+    layer.close()
+    return g, ref, rel
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_tiny_layer(m, out_f32):
+    wl = synth.WORKLOADS["tiny"]
+    _parity(m, wl, synth.gen_layer(wl, 0), out_f32=out_f32)
+
+
+SMALL_SHAPES = [
+    # (T, d, ffn, E, k, shared, zipf)
+    (1, 96, 160, 8, 1, 0, 0.0),
+    (3, 224, 96, 16, 2, 0, 1.1),
+    (5, 160, 224, 128, 4, 64, 0.0),
+    (7, 64, 64, 256, 8, 96, 1.1),
+    (9, 128, 32, 8, 8, 0, 0.0),
+    (13, 288, 320, 32, 4, 0, 0.0),
+    (16, 352, 96, 16, 4, 128, 1.1),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_small_shapes(m, shape, out_f32):
+    T, d, F, E, k, S, z = shape
+    wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
+    _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32)
+
+
+def test_every_token_count_up_to_16(m):
+    """Row counts 1..16 (ragged n8 tiles) through one context sized t_max = 16."""
+    wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=4, shared_ffn=64)
+    L = synth.gen_layer(wl, 3)
+    layer = make_layer(m, wl, L, t_max=16, out_f32=True)
+    full_ref = oracle_layer(wl, L)
+    for T in range(1, 17):
+        g = run_gpu(m, layer, L["x"][:T], out_f32=True)
+        check_output(g["y"], full_ref["y"][:T], F32_TOL)
+        assert np.array_equal(g["ids"], full_ref["ids"][:T])
+    layer.close()
+
+
+def test_batch_invariance(m):
+    """A token's output bits do not depend on the batch it is in."""
+    wl = synth.WORKLOADS["tiny"].with_(T=16, E=32, k=4)
+    L = synth.gen_layer(wl, 5)
+    layer = make_layer(m, wl, L, t_max=16, out_f32=True)
+    full = run_gpu(m, layer, L["x"], out_f32=True)
+    for t in (0, 7, 15):
+        one = run_gpu(m, layer, L["x"][t:t + 1].copy(), out_f32=True)
+        assert np.array_equal(one["y"][0], full["y"][t])
+    layer.close()
+
+
+def test_down_scale_plus_one_doubles_exactly(m):
+    wl = synth.WORKLOADS["tiny"].with_(T=6)
+    L = synth.gen_layer(wl, 0)
+    layer = make_layer(m, wl, L, out_f32=True)
+    g1 = run_gpu(m, layer, L["x"], out_f32=True)
+    sc = L["scales"].copy()
+    per, gu = wl.scale_bytes(), 2 * wl.ffn * wl.d // 32
+    for e in range(wl.E):
+        sc[e * per + gu:(e + 1) * per] += 1
+    layer2 = make_layer(m, wl, dict(L, scales=sc), out_f32=True)
+    g2 = run_gpu(m, layer2, L["x"], out_f32=True)
+    assert np.array_equal(g2["y"], 2.0 * g1["y"])
+    layer.close()
+    layer2.close()
+
+
+def test_exact_ties_lower_index(m):
+    wl = synth.WORKLOADS["tiny"].with_(T=3, E=8, k=3)
+    L = synth.gen_layer(wl, 0)
+    w = np.zeros((wl.E, wl.d), dtype=np.float32)
+    w[[2, 5, 6]] = 0.25  # three identical router rows -> exact ties
+    w[1] = 0.125
+    L = dict(L, w_router=w)
+    g, ref, _ = _parity(m, wl, L)
+    for t in range(wl.T):
+        s = np.sign(synth.bf16_bits_to_f32(L["x"][t]).sum())
+        expect = [2, 5, 6] if s > 0 else [0, 3, 4]
+        assert list(g["ids"][t]) == expect
+
+
+def test_skewed_all_tokens_one_expert(m):
+    wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=2)
+    L = synth.gen_layer(wl, 4)
+    b = np.zeros(wl.E, dtype=np.float32)
+    b[11] = 100.0
+    b[3] = 90.0
+    _parity(m, wl, dict(L, bias=b))
+
+
+def test_k_equals_E(m):
+    wl = synth.WORKLOADS["tiny"].with_(T=5, E=4, k=4, shared_ffn=32)
+    _parity(m, wl, synth.gen_layer(wl, 8), out_f32=True)
+
+
+def test_empty_batch_and_errors(m):
+    wl = synth.WORKLOADS["tiny"]
+    L = synth.gen_layer(wl, 0)
+    layer = make_layer(m, wl, L, t_max=4)
+    import torch
+    x = torch.zeros((8, wl.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((8, wl.d), dtype=torch.bfloat16, device="cuda")
+    layer.forward(x, 0, out)  # T = 0 is a no-op
+    torch.cuda.synchronize()
+    assert float(out.abs().sum()) == 0.0
+    with pytest.raises(m.MoeError) as ei:
+        layer.forward(x, 5, out)
+    assert ei.value.code == m.MOE_ERR_T_TOO_LARGE
+    bad = L["scales"].copy()
+    bad[123] = 255
+    layer2 = m.MoeLayer(layer.shape)
+    with pytest.raises(m.MoeError) as ei:
+        layer2.load(L["w_router"], None, L["codes"], bad)
+    assert ei.value.code == m.MOE_ERR_NAN_SCALE
+    with pytest.raises(m.MoeError) as ei:
+        layer2.forward(x, 1, out)
+    assert ei.value.code == m.MOE_ERR_NOT_LOADED
+    layer.close()
+    layer2.close()
+
+
+def test_forward_host_matches_device(m):
+    wl = synth.WORKLOADS["tiny"].with_(T=5)
+    L = synth.gen_layer(wl, 2)
+    layer = make_layer(m, wl, L, t_max=8)
+    g = run_gpu(m, layer, L["x"])
+    out = np.zeros((wl.T, wl.d), dtype=np.uint16)
+    layer.forward_host(L["x"], wl.T, out)
+    y = (out.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(y, g["y"])
+    layer.close()
+
+
+# ---------------------------------------------------------------- full-size workloads (sampled outputs)
+
+@pytest.mark.parametrize("name,layer_idx,tokens", [
+    ("decode", 0, None),
+    ("decode", 35, None),
+    ("verify", 0, [0, 9, 15]),
+    ("small", 0, [0, 5, 7]),
+    ("prefill", 0, [0, 511, 1023]),
+])
+def test_full_size_workloads(m, name, layer_idx, tokens):
+    wl = synth.WORKLOADS[name]
+    L = synth.gen_layer(wl, layer_idx)
+    _parity(m, wl, L, tokens=tokens)
