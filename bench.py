@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-expert FFN layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|verify|small|prefill|tiny]
+
+A step is one pass of the whole layer (router, top-k, bucketing, gate/up,
+SwiGLU, down, shared expert, combine) over every layer of the workload, each
+layer on its own synthetic batch: for the default ``decode`` workload that is
+36 independent gpt-oss-120B-shaped MoE layers (T=1, d=ffn=2880, E=128, k=4,
+MXFP4 experts) back to back. The metric is MoE-layer tokens per second
+(T * layers * steps / time) with the achieved HBM GB/s over the algorithmic
+bytes beside it.
+
+``--impl ours`` (default): inputs resident in HBM, the layers captured in one
+CUDA graph, K timed replays between CUDA events after W warm-up replays. The
+weights a step touches exceed the 129 MB L2, so no flush is needed. Also
+reported: the per-kernel roofline of the dominant kernel (CUDA events the
+library records at its phase boundaries), an end-to-end number through the
+host-buffer entry point, the CPU oracle on a bounded sample, and SM clocks
+sampled during the timed region.
+
+``--impl reference``: the CPU oracle (plain fp64 C) as the reference arm on
+the host cores, one layer-token per step.
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(independent batches, no collective on the data path); rank 0 prints the
+whole-job number (units of all ranks over the slowest rank's time).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s (achieved HBM GB/s alongside)"
+UNIT = "tokens/s"
+
+
+# ---------------------------------------------------------------- algorithmic work (per layer)
+
+def layer_bytes(wl: synth.Workload, U: int, T: int) -> int:
+    """Bytes the method must move for one layer call: the U distinct routed experts
+    (+ the shared expert), router weights (+ bias), x in and y out (bf16)."""
+    b = U * wl.expert_bytes() + wl.E * wl.d * 4 + 2 * T * wl.d + 2 * T * wl.d
+    if wl.shared_ffn:
+        b += wl.expert_bytes(wl.shared_ffn)
+    if wl.zipf_bias:
+        b += 4 * wl.E
+    return b
+
+
+def phase_bytes(wl: synth.Workload, U: int, T: int) -> dict:
+    d, F, S = wl.d, wl.ffn, wl.shared_ffn
+    gu = U * (F * d + F * d // 16) + (S * d + S * d // 16 if S else 0) + 2 * T * d
+    dn = U * (F * d // 2 + F * d // 32) + (S * d // 2 + S * d // 32 if S else 0)
+    route = wl.E * d * 4 + (4 * wl.E if wl.zipf_bias else 0) + 2 * T * d
+    return {"route": route, "gateup": gu, "down": dn, "combine": 2 * T * d}
+
+
+def layer_flops(wl: synth.Workload, T: int) -> int:
+    return 2 * T * wl.E * wl.d + 2 * T * wl.k * 3 * wl.d * wl.ffn + 2 * T * 3 * wl.d * wl.shared_ffn
+
+
+# ---------------------------------------------------------------- clocks (NVML via ctypes; nvidia-smi fallback)
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons on a thread while running."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap",
+               0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle", 0x2: "applications_clocks_setting"}
+
+    def __init__(self, device_index: int, interval_s: float = 0.002):
+        self.dev = device_index
+        self.interval = interval_s
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._th = None
+        self._nvml = None
+        self._h = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM = 1
+                        self.max_mhz = mx.value
+        except OSError:
+            self._nvml = None
+
+    def _sample(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        nv, h = self._nvml, self._h
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(self.interval)
+
+    def start(self):
+        if self._nvml is not None:
+            self._th = threading.Thread(target=self._sample, daemon=True)
+            self._th.start()
+
+    def stop(self) -> dict:
+        if self._th is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable: NVML not loadable"]}
+        self._stop.set()
+        self._th.join()
+        mhz = [s[0] for s in self.samples]
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "routed_expert_ffn_warp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(phase: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(workload, {}).get(phase)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_x(wl: synth.Workload, layer: int, rank: int) -> np.ndarray:
+    """x of one layer for one rank (rank 0 uses the layer's own x)."""
+    seed = wl.seed(layer) if rank == 0 else wl.seed(layer) + 1_000_003 * rank
+    return synth.gen_x(seed, wl.T, wl.d)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(wl: synth.Workload, budget_s: float, max_samples: int, first_layer: int = 0):
+    """Time the CPU oracle on layer-token evaluations of the workload (layer l,
+    token 0 for l = first_layer, ...) until budget_s of oracle time is spent.
+    Input generation is outside the timed region."""
+    import oracle
+    done, spent = 0, 0.0
+    for i in range(max_samples):
+        layer = (first_layer + i) % wl.layers
+        L = synth.gen_layer(wl, layer)
+        t0 = time.perf_counter()
+        oracle.layer_tokens(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, L["x"], L["w_router"], L["bias"],
+                            L["codes"], L["scales"], tokens=[0])
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return done, spent
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    for i in range(args.warmup):
+        oracle_sample(wl, 0.0, 1, first_layer=i)
+    times = []
+    for i in range(args.steps):
+        n, s = oracle_sample(wl, 0.0, 1, first_layer=args.warmup + i)
+        times.append(s)
+    total = sum(times)
+    value = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one layer-token per step: workload '{wl.name}', layer = step index, token 0, "
+                                   "full layer (router, top-k, k experts, combine) in fp64"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl: synth.Workload, args) -> dict:
+    return {"workload": f"{wl.name}: MoE layer T={wl.T}, d={wl.d}, ffn={wl.ffn}, E={wl.E}, k={wl.k}, "
+                        f"shared_ffn={wl.shared_ffn}, zipf_bias={wl.zipf_bias}, layers={args.layers}, MXFP4 experts",
+            "T": wl.T, "d": wl.d, "ffn": wl.ffn, "n_experts": wl.E, "top_k": wl.k, "shared_ffn": wl.shared_ffn,
+            "layers": args.layers, "zipf_bias": wl.zipf_bias, "parallelism": f"replica x{args.gpus}",
+            "l2": "inputs larger than L2: each step streams every layer's routed experts from HBM; no flush"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, wl):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from routed_expert_ffn_warp_gb300 import build as lib_build
+    lib_build.build()
+    import routed_expert_ffn_warp_gb300 as m
+
+    nl = args.layers
+    T = wl.T
+    shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T)
+    codes_h = torch.empty((wl.total_code_bytes,), dtype=torch.uint8, pin_memory=True)
+    scales_h = torch.empty((wl.total_scale_bytes,), dtype=torch.uint8, pin_memory=True)
+    layers, xs, outs, xh, oh = [], [], [], [], []
+    t_gen = time.perf_counter()
+    for l in range(nl):
+        L = synth.gen_layer(wl, l, with_experts=False)
+        synth.gen_experts(wl, wl.seed(l), codes_h.numpy(), scales_h.numpy())
+        lay = m.MoeLayer(shape, device=local)
+        lay.load(L["w_router"], L["bias"], codes_h, scales_h)
+        layers.append(lay)
+        x = rank_x(wl, l, rank)
+        xh.append(torch.from_numpy(x.view(np.int16).copy()).pin_memory())
+        xs.append(xh[-1].cuda())
+        outs.append(torch.empty((T, wl.d), dtype=torch.bfloat16, device="cuda"))
+        oh.append(torch.empty((T, wl.d), dtype=torch.int16, pin_memory=True))
+    del codes_h, scales_h
+    t_gen = time.perf_counter() - t_gen
+    stream = torch.cuda.Stream()
+
+    # routing of every layer (distinct experts U -> algorithmic bytes)
+    counts = torch.empty((wl.E,), dtype=torch.int32, device="cuda")
+    U = []
+    with torch.cuda.stream(stream):
+        for l in range(nl):
+            layers[l].forward(xs[l], T, outs[l], stream)
+            layers[l].routing(counts=counts, stream=stream)
+            stream.synchronize()
+            U.append(int((counts > 0).sum().item()))
+    bytes_step = sum(layer_bytes(wl, u, T) for u in U)
+    flops_step = nl * layer_flops(wl, T)
+
+    # device-resident timing: the layers in one CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for l in range(nl):
+                layers[l].forward(xs[l], T, outs[l], stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for l in range(nl):
+            layers[l].forward(xs[l], T, outs[l], stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    clocks = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(ws)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = reduce_max(ms_local, ws)
+    value = ws * T * nl / (ms / 1000.0)
+    status = max(lay.status() for lay in layers)
+
+    # per-kernel timing: the library records events at its phase boundaries
+    phases = m.moe_forward_phases(layers[0].ctx, T)
+    ksteps = max(1, args.kernel_steps)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(nl)]
+          for _ in range(ksteps)]
+    with torch.cuda.stream(stream):
+        for s_ev in ev:  # torch creates the CUDA event at its first record
+            for l_ev in s_ev:
+                for e_ in l_ev:
+                    e_.record(stream)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        for s in range(ksteps):
+            for l in range(nl):
+                m.moe_profile_events(layers[l].ctx, ev[s][l])
+                layers[l].forward(xs[l], T, outs[l], stream)
+        for l in range(nl):
+            m.moe_profile_events(layers[l].ctx, None)
+    torch.cuda.synchronize()
+    ph_ms = {p: 0.0 for p in phases}
+    for s in range(ksteps):
+        for l in range(nl):
+            for i, p in enumerate(phases):
+                ph_ms[p] += ev[s][l][i].elapsed_time(ev[s][l][i + 1])
+    ph_bytes = {p: 0 for p in phases}
+    for u in U:
+        pb = phase_bytes(wl, u, T)
+        for p in phases:
+            ph_bytes[p] += pb.get(p, 0) * ksteps
+    dom = max(phases, key=lambda p: ph_ms[p])
+    launches = ksteps * nl
+    peaks = measured_peaks()
+    achieved = ph_bytes[dom] / (ph_ms[dom] / 1000.0) / 1e9
+    traffic = ncu_traffic(dom, wl.name)
+
+    # end to end through the host-buffer entry point (pinned x in, result out, every step)
+    with torch.cuda.stream(stream):
+        for l in range(nl):
+            layers[l].forward_host(xh[l], T, oh[l], stream, synchronize=(l == nl - 1))
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for l in range(nl):
+            layers[l].forward_host(xh[l], T, oh[l], stream, synchronize=(l == nl - 1))
+    t_e2e = (time.perf_counter() - t0) / args.steps
+    t_e2e = reduce_max(t_e2e, ws)
+    e2e_value = ws * T * nl / t_e2e
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        n, spent = oracle_sample(wl, args.cpu_budget, 64)
+        cpu = {"value": n / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n} layer-token evaluations (layers 0..{n - 1}, token 0 of each) of the '{wl.name}' "
+                         f"workload, full layer in fp64, {spent:.1f} s single-threaded"}
+
+    launches_per_fwd = m.moe_launches_per_forward(layers[0].ctx, T)
+    for lay in layers:
+        lay.close()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4-f16-f32acc", "data": "synthetic (seeded counter-based generator; random MXFP4 weights)",
+        "config": config_of(wl, args),
+        "hbm_gbs": ws * bytes_step / (ms / 1000.0) / 1e9,
+        "hbm_frac_of_measured": (bytes_step / (ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
+        "tflops": ws * flops_step / (ms / 1000.0) / 1e12,
+        "us_per_layer": 1000.0 * ms / nl,
+        "distinct_experts_per_layer": statistics.mean(U),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": ph_bytes[dom] / launches,
+                     "avg_launch_us": 1000.0 * ph_ms[dom] / launches,
+                     "phase_ms_share": {p: ph_ms[p] / sum(ph_ms.values()) for p in phases}},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": nl * T * wl.d * 2,
+                "d2h_bytes_per_step": nl * T * wl.d * 2, "via": "moe_forward_host (pinned host buffers)"},
+        "gpu_launches": args.steps * nl * launches_per_fwd,
+        "clocks": clk,
+        "device_status": status,
+        "setup_s": t_gen,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
+    ap.add_argument("--layers", type=int, default=None, help="layers per step (default: the workload's)")
+    ap.add_argument("--kernel-steps", type=int, default=3, help="eager steps for per-kernel event timing")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    wl = synth.WORKLOADS[args.workload]
+    if args.layers is None:
+        args.layers = wl.layers
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -68,7 +68,7 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
 typedef struct moe_config {
   int d;          /* hidden size; a multiple of 32 */
   int ffn;        /* routed expert intermediate size; a multiple of 32 */
-  int n_experts;  /* E, 1..1024 */
+  int n_experts;  /* E, 1..512 */
   int top_k;      /* k, 1..min(E, 32) */
   int shared_ffn; /* shared expert intermediate size (multiple of 32), 0 = none */
   int t_max;      /* largest T a forward will be given; sizes the workspace */
@@ -103,11 +103,13 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales);
  * Device-side failures are reported by moe_get_status after synchronising. */
 int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream);
 
-/* moe_forward with HOST buffers: copies x (host, bf16 [T][d]) into the
- * context, runs the layer, copies the result back to out (host) and
- * synchronises the stream before returning. Pinned host memory is fastest;
- * pageable memory works. Not capturable (it synchronises). */
-int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream);
+/* moe_forward with HOST buffers: enqueues the copy of x (host, bf16 [T][d])
+ * into the context, the layer, and the copy of the result back to out (host)
+ * on `stream`. With synchronize != 0 it waits for the stream before returning;
+ * with 0 the caller synchronises before reading out or reusing x. Pinned host
+ * memory is needed for the copies to be asynchronous; pageable works too.
+ * Each context has one staging buffer: do not overlap two calls on a context. */
+int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream, int synchronize);
 
 /* Debug export of the last forward's routing (device or host pointers, any
  * may be NULL): ids int32 [T][k], gates fp32 [T][k], counts int32 [E],
@@ -125,6 +127,20 @@ int moe_get_logits(moe_ctx* ctx, float* hi, float* lo, void* stream);
  * kernel, e.g. MOE_ERR_TIMEOUT). Synchronises the context's device; clears the
  * word when `clear` is nonzero. */
 int moe_get_status(moe_ctx* ctx, int clear);
+
+/* Tracing hook. Registers n_events cudaEvent_t handles (created by the
+ * caller) that every later moe_forward records on its stream at its phase
+ * boundaries: event i just before phase i starts and event n_phases after the
+ * last phase, where the phases are those moe_forward_phases() names. Pass
+ * NULL / 0 to stop recording. n_events must be 0 or n_phases + 1. */
+int moe_profile_events(moe_ctx* ctx, void* const* events, int n_events);
+
+/* Number of phases of a forward of T tokens, and (if names != NULL) a
+ * pointer to a static, comma-separated list of their names. */
+int moe_forward_phases(const moe_ctx* ctx, int T, const char** names);
+
+/* Number of kernels one moe_forward of T tokens launches. */
+int moe_launches_per_forward(const moe_ctx* ctx, int T);
 
 /* Bytes of packed expert weights the context holds (codes + scales). */
 size_t moe_weight_bytes(const moe_ctx* ctx);

@@ -32,8 +32,8 @@ MOE_OUT_BF16 = 0
 MOE_OUT_F32 = 1
 
 EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
-            "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_weight_bytes", "moe_last_error",
-            "moe_destroy"]
+            "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
+            "moe_launches_per_forward", "moe_weight_bytes", "moe_last_error", "moe_destroy"]
 
 
 class MoeError(RuntimeError):
@@ -66,7 +66,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_load_router.argtypes = [vp, vp, vp]
             lib.moe_load_experts.argtypes = [vp, vp, vp]
             lib.moe_forward.argtypes = [vp, vp, i32, vp, vp]
-            lib.moe_forward_host.argtypes = [vp, vp, i32, vp, vp]
+            lib.moe_forward_host.argtypes = [vp, vp, i32, vp, vp, i32]
+            lib.moe_profile_events.argtypes = [vp, P(vp), i32]
+            lib.moe_forward_phases.argtypes = [vp, i32, P(ctypes.c_char_p)]
+            lib.moe_launches_per_forward.argtypes = [vp, i32]
             lib.moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp]
             lib.moe_get_logits.argtypes = [vp, vp, vp, vp]
             lib.moe_get_status.argtypes = [vp, i32]
@@ -77,7 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_destroy.argtypes = [vp]
             lib.moe_destroy.restype = None
             for name in ("moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
-                         "moe_get_routing", "moe_get_logits", "moe_get_status"):
+                         "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events",
+                         "moe_forward_phases", "moe_launches_per_forward"):
                 getattr(lib, name).restype = i32
             _lib = lib
     return _lib
@@ -131,9 +135,9 @@ def moe_forward(ctx: int, x, T: int, out, stream=None) -> None:
     _check(ctx, load_library().moe_forward(ctx, ptr(x), T, ptr(out), stream_handle(stream)), "moe_forward")
 
 
-def moe_forward_host(ctx: int, x_host, T: int, out_host, stream=None) -> None:
-    _check(ctx, load_library().moe_forward_host(ctx, ptr(x_host), T, ptr(out_host), stream_handle(stream)),
-           "moe_forward_host")
+def moe_forward_host(ctx: int, x_host, T: int, out_host, stream=None, synchronize: bool = True) -> None:
+    _check(ctx, load_library().moe_forward_host(ctx, ptr(x_host), T, ptr(out_host), stream_handle(stream),
+                                                1 if synchronize else 0), "moe_forward_host")
 
 
 def moe_get_routing(ctx: int, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
@@ -147,6 +151,27 @@ def moe_get_logits(ctx: int, hi=None, lo=None, stream=None) -> None:
 
 def moe_get_status(ctx: int, clear: bool = False) -> int:
     return load_library().moe_get_status(ctx, 1 if clear else 0)
+
+
+def moe_profile_events(ctx: int, events=None) -> None:
+    """events: list of torch.cuda.Event (created with enable_timing=True) or None to stop."""
+    if not events:
+        _check(ctx, load_library().moe_profile_events(ctx, None, 0), "moe_profile_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event if hasattr(ev, "cuda_event") else ev for ev in events])
+    _check(ctx, load_library().moe_profile_events(ctx, arr, len(events)), "moe_profile_events")
+
+
+def moe_forward_phases(ctx: int, T: int = 1) -> list[str]:
+    names = ctypes.c_char_p()
+    n = load_library().moe_forward_phases(ctx, T, ctypes.byref(names))
+    out = names.value.decode().split(",")
+    assert len(out) == n
+    return out
+
+
+def moe_launches_per_forward(ctx: int, T: int) -> int:
+    return load_library().moe_launches_per_forward(ctx, T)
 
 
 def moe_weight_bytes(ctx: int) -> int:
@@ -195,8 +220,8 @@ class MoeLayer:
     def forward(self, x, T: int, out, stream=None) -> None:
         moe_forward(self.ctx, x, T, out, stream)
 
-    def forward_host(self, x_host, T: int, out_host, stream=None) -> None:
-        moe_forward_host(self.ctx, x_host, T, out_host, stream)
+    def forward_host(self, x_host, T: int, out_host, stream=None, synchronize: bool = True) -> None:
+        moe_forward_host(self.ctx, x_host, T, out_host, stream, synchronize)
 
     def routing(self, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
         moe_get_routing(self.ctx, ids, gates, counts, offsets, perm, stream)

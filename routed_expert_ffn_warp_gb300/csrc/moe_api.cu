@@ -32,6 +32,8 @@ struct moe_ctx {
   void* out_dev = nullptr;  // host-API staging of out
   int* load_err = nullptr;  // repack NaN-scale flag
   int last_T = 0;
+  cudaEvent_t prof[moe::kForwardPhases + 1] = {};
+  bool profiling = false;
 };
 
 namespace {
@@ -257,12 +259,13 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
   p.x = static_cast<const uint16_t*>(x);
   p.out = out;
   ctx->last_T = T;
-  cudaError_t e = moe::launch_forward(p, static_cast<cudaStream_t>(stream), ctx->num_sms);
+  cudaError_t e = moe::launch_forward(p, static_cast<cudaStream_t>(stream), ctx->num_sms,
+                                      ctx->profiling ? ctx->prof : nullptr);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "forward launch");
   return MOE_OK;
 }
 
-int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream) {
+int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream, int synchronize) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (T < 0 || T > ctx->cfg.t_max) return moe_forward(ctx, x_host, T, out_host, stream);
   if (T > 0 && (!x_host || !out_host)) return fail(ctx, MOE_ERR_INVALID_ARG, "x or out is NULL");
@@ -276,7 +279,7 @@ int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, vo
   int rc = moe_forward(ctx, ctx->x_dev, T, ctx->out_dev, stream);
   if (rc != MOE_OK) return rc;
   if (T > 0) e = cudaMemcpyAsync(out_host, ctx->out_dev, ob, cudaMemcpyDefault, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && synchronize) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "out copy");
   return MOE_OK;
 }
@@ -320,6 +323,33 @@ int moe_get_status(moe_ctx* ctx, int clear) {
   if (e == cudaSuccess && clear) e = cudaMemset(ctx->base.status, 0, 4);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "status read");
   return st;
+}
+
+int moe_profile_events(moe_ctx* ctx, void* const* events, int n_events) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (!events || n_events == 0) {
+    ctx->profiling = false;
+    return MOE_OK;
+  }
+  if (n_events != moe::kForwardPhases + 1) return fail(ctx, MOE_ERR_INVALID_ARG, "n_events must be n_phases + 1");
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return fail(ctx, MOE_ERR_INVALID_ARG, "NULL event");
+    ctx->prof[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  ctx->profiling = true;
+  return MOE_OK;
+}
+
+int moe_forward_phases(const moe_ctx* ctx, int T, const char** names) {
+  (void)ctx;
+  (void)T;
+  if (names) *names = moe::kForwardPhaseNames;
+  return moe::kForwardPhases;
+}
+
+int moe_launches_per_forward(const moe_ctx* ctx, int T) {
+  (void)ctx;
+  return T > 0 ? moe::kLaunchesPerForward : 0;
 }
 
 size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }

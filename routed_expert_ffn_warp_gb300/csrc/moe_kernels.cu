@@ -661,15 +661,22 @@ __global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n
 
 }  // namespace
 
-cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms) {
+const char* const kForwardPhaseNames = "route,gateup,down,combine";
+
+cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events) {
   if (p.T == 0) return cudaSuccess;
+  if (events) cudaEventRecord(events[0], stream);
   prep_x_kernel<<<p.T, 256, 0, stream>>>(p);
   router_kernel<<<dim3(p.E, (p.T + kRouterTT - 1) / kRouterTT), kRouterThreads, 0, stream>>>(p);
   topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
+  if (events) cudaEventRecord(events[1], stream);
   gateup_kernel<kGuNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  if (events) cudaEventRecord(events[2], stream);
   down_kernel<kDnNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  if (events) cudaEventRecord(events[3], stream);
   combine_kernel<<<dim3((p.d + 255) / 256, p.T), 256, 0, stream>>>(p);
+  if (events) cudaEventRecord(events[4], stream);
   return cudaGetLastError();
 }
 
