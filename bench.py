@@ -317,6 +317,9 @@ def run_ours(args, wl):
         for _ in range(args.warmup):
             graph.replay()
     stream.synchronize()
+    bad = [lay.status() for lay in layers]
+    if any(bad):
+        raise RuntimeError(f"device status after warm-up: {bad[:4]}... (a bounded device wait gave up)")
     clocks = ClockSampler(local)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)

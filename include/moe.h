@@ -65,6 +65,15 @@ enum {
 
 enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
 
+/* moe_config.flags bits.
+ * MOE_FLAG_TEST_FORCE_TIMEOUT exists for failure-detection tests only: one
+ *   device-side wait of every single-kernel decode forward targets a count
+ *   nothing reaches and gives up after 2 ms, so the forward completes with
+ *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
+ * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path that
+ *   otherwise serves T > 16 (for testing both paths on the same shapes). */
+enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u };
+
 typedef struct moe_config {
   int d;          /* hidden size; a multiple of 32 */
   int ffn;        /* routed expert intermediate size; a multiple of 32 */
@@ -73,7 +82,7 @@ typedef struct moe_config {
   int shared_ffn; /* shared expert intermediate size (multiple of 32), 0 = none */
   int t_max;      /* largest T a forward will be given; sizes the workspace */
   int out_dtype;  /* MOE_OUT_BF16 (bf16, round to nearest even) or MOE_OUT_F32 */
-  unsigned flags; /* reserved, must be 0 */
+  unsigned flags; /* MOE_FLAG_* bits; 0 for normal use */
 } moe_config;
 
 typedef struct moe_ctx moe_ctx;

@@ -30,6 +30,8 @@ MOE_ERR_NAN_SCALE = -6
 MOE_ERR_NOMEM = -7
 MOE_OUT_BF16 = 0
 MOE_OUT_F32 = 1
+MOE_FLAG_TEST_FORCE_TIMEOUT = 1
+MOE_FLAG_GENERAL_PATH = 2
 
 EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
@@ -198,10 +200,11 @@ class LayerShape:
     shared_ffn: int = 0
     t_max: int = 16
     out_dtype: int = MOE_OUT_BF16
+    flags: int = 0
 
     def config(self) -> moe_config:
         return moe_config(self.d, self.ffn, self.n_experts, self.top_k, self.shared_ffn, self.t_max,
-                          self.out_dtype, 0)
+                          self.out_dtype, self.flags)
 
 
 class MoeLayer:

@@ -33,7 +33,10 @@ struct moe_ctx {
   int* load_err = nullptr;  // repack NaN-scale flag
   int last_T = 0;
   cudaEvent_t prof[moe::kForwardPhases + 1] = {};
-  bool profiling = false;
+  int n_prof = 0;
+  int max_smem = 0;
+  bool decode_ok = false;  // the fused single-kernel path fits this config
+  moe::DecParams dec{};
 };
 
 namespace {
@@ -80,7 +83,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const moe_config& c = *cfg;
   if (c.d <= 0 || c.d % 32 || c.ffn <= 0 || c.ffn % 32 || c.shared_ffn < 0 || c.shared_ffn % 32 ||
       c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
-      c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) || c.flags)
+      c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) ||
+      (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH)))
     return fail(nullptr, MOE_ERR_INVALID_ARG,
                 "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
                 "0 <= t_max <= 65536; out_dtype 0/1; flags 0)");
@@ -94,6 +98,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return fail(nullptr, MOE_ERR_CUDA, "cudaSetDevice failed");
   }
   cudaError_t e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) {
     delete ctx;
     return fail(nullptr, MOE_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
@@ -121,6 +126,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
+  const size_t o_done = take((size_t)(E + 1) * 4), o_rowcnt = take((size_t)(d / 16) * 4),
+               o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
+               o_lw = take((size_t)std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
   ctx->ws_bytes = off;
 
   if ((e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
@@ -173,6 +181,17 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->x_dev = w + o_xd;
   ctx->out_dev = w + o_od;
   ctx->load_err = reinterpret_cast<int*>(w + o_lerr);
+  moe::DecParams& dp = ctx->dec;
+  dp.f = p;
+  dp.done = reinterpret_cast<int*>(w + o_done);
+  dp.rowcnt = reinterpret_cast<int*>(w + o_rowcnt);
+  dp.bar_flags = reinterpret_cast<unsigned*>(w + o_bar);
+  dp.lwords = reinterpret_cast<unsigned long long*>(w + o_lw);
+  dp.tcap = std::min(Tm, moe::kDecodeMaxT);
+  dp.wait_ns = 50000000LL;  // 50 ms: orders of magnitude above a layer's runtime
+  dp.test_extra = (c.flags & MOE_FLAG_TEST_FORCE_TIMEOUT) ? 1 : 0;
+  dp.test_wait_ns = 2000000LL;  // 2 ms
+  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem);
   *out = ctx;
   return MOE_OK;
 }
@@ -258,9 +277,20 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
   p.P = T * ctx->cfg.top_k;
   p.x = static_cast<const uint16_t*>(x);
   p.out = out;
+  p.bias = ctx->has_bias ? ctx->bias : nullptr;
   ctx->last_T = T;
-  cudaError_t e = moe::launch_forward(p, static_cast<cudaStream_t>(stream), ctx->num_sms,
-                                      ctx->profiling ? ctx->prof : nullptr);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT) {
+    moe::DecParams dp = ctx->dec;
+    dp.f = p;
+    const bool prof = ctx->n_prof >= 2;
+    if (prof) cudaEventRecord(ctx->prof[0], s);
+    e = moe::launch_decode(dp, s, ctx->num_sms, ctx->max_smem);
+    if (prof && e == cudaSuccess) cudaEventRecord(ctx->prof[1], s);
+  } else {
+    e = moe::launch_forward(p, s, ctx->num_sms, ctx->n_prof == moe::kForwardPhases + 1 ? ctx->prof : nullptr);
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "forward launch");
   return MOE_OK;
 }
@@ -325,31 +355,40 @@ int moe_get_status(moe_ctx* ctx, int clear) {
   return st;
 }
 
+namespace {
+bool uses_decode(const moe_ctx* ctx, int T) { return T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT; }
+}  // namespace
+
 int moe_profile_events(moe_ctx* ctx, void* const* events, int n_events) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (!events || n_events == 0) {
-    ctx->profiling = false;
+    ctx->n_prof = 0;
     return MOE_OK;
   }
-  if (n_events != moe::kForwardPhases + 1) return fail(ctx, MOE_ERR_INVALID_ARG, "n_events must be n_phases + 1");
+  if (n_events != 2 && n_events != moe::kForwardPhases + 1)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "n_events must be moe_forward_phases(T) + 1");
   for (int i = 0; i < n_events; ++i) {
     if (!events[i]) return fail(ctx, MOE_ERR_INVALID_ARG, "NULL event");
     ctx->prof[i] = static_cast<cudaEvent_t>(events[i]);
   }
-  ctx->profiling = true;
+  ctx->n_prof = n_events;
   return MOE_OK;
 }
 
 int moe_forward_phases(const moe_ctx* ctx, int T, const char** names) {
-  (void)ctx;
-  (void)T;
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (uses_decode(ctx, T)) {
+    if (names) *names = "layer";
+    return 1;
+  }
   if (names) *names = moe::kForwardPhaseNames;
   return moe::kForwardPhases;
 }
 
 int moe_launches_per_forward(const moe_ctx* ctx, int T) {
-  (void)ctx;
-  return T > 0 ? moe::kLaunchesPerForward : 0;
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (T <= 0) return 0;
+  return uses_decode(ctx, T) ? 1 : moe::kLaunchesPerForward;
 }
 
 size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }

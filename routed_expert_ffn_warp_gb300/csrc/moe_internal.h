@@ -86,6 +86,25 @@ struct FwdParams {
   int* status;           // device status word
 };
 
+// Fused single-kernel decode path (moe_decode.cu), used for T <= kDecodeMaxT.
+constexpr int kDecodeMaxT = 16;
+struct DecParams {
+  FwdParams f;
+  int* done;            // [E+1] finished gate/up units per slot
+  int* rowcnt;          // [d/16] finished down units per row tile
+  unsigned* bar_flags;  // [grid] per-CTA launch sequence numbers (each only grows)
+  unsigned long long* lwords;  // [tcap][E][2] published logits: (fp32 bits << 32) | sequence
+  int tcap;             // tokens the x16 shared area holds (min(t_max, kDecodeMaxT))
+  int ns, stage_bytes;  // ring stages and bytes per stage
+  int pfloats, pbuf_depth;  // per-unit partial floats per lane and partial buffers
+  int off_x16, off_xinv, off_pbuf, off_route, off_ring, smem_bytes;
+  long long wait_ns;       // bound of every device-side wait
+  int test_extra;          // > 0: one wait targets an unreachable count (timeout test)
+  long long test_wait_ns;  // bound of that wait
+};
+bool decode_plan(DecParams& p, int max_smem);
+cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem);
+
 // Launchers (moe_kernels.cu). All are asynchronous on `stream`.
 // `events` (may be null) receives kForwardPhases + 1 cudaEvent_t to record at
 // the phase boundaries.

@@ -25,154 +25,19 @@
 // (hi + lo, about 22 significant bits) with a power-of-two scale per 16
 // elements. All accumulation is fp32; all reductions run in a fixed order, so
 // a token's output bits do not depend on timing.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "moe_device.cuh"
 #include "moe_internal.h"
 
 namespace moe {
 namespace {
 
+using namespace dev;
+
 constexpr int kNW = 8;  // warps per CTA of the expert kernels
 constexpr int kGuNT = 2;  // n8 token tiles per gate/up pass (16 tokens)
 constexpr int kDnNT = 4;  // n8 tiles per down pass (16 pairs: hi and lo columns)
-
-// ---------------------------------------------------------------- primitives
-
-__device__ __forceinline__ uint4 ld16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-__device__ __forceinline__ uint32_t ld4(const void* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
-
-// Two E2M1 codes (low nibble -> low half, high nibble -> high half) to f16x2.
-__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t word, int byte) {
-  uint32_t r;
-  uint16_t b = (uint16_t)((word >> (8 * byte)) & 0xFFu);
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "h"(b));
-  return r;
-}
-
-// E8M0 byte to fp32: 2^(e-127); e = 0 is the subnormal 2^-127.
-__device__ __forceinline__ float e8m0_f32(uint32_t e) { return __uint_as_float(e ? (e << 23) : 0x00400000u); }
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// A fragments of the two MMAs of scale block bb from a lane's 16 code bytes.
-// MMA 1 takes code bytes 4c, 4c+1 of the block (elements 8c..8c+3), MMA 2 bytes
-// 4c+2, 4c+3 (elements 8c+4..8c+7); the B fragment is loaded to match.
-__device__ __forceinline__ void a_frags(const uint4 q, int bb, uint32_t (&a1)[4], uint32_t (&a2)[4]) {
-  const uint32_t rg = bb ? q.z : q.x, rg8 = bb ? q.w : q.y;
-  a1[0] = e2m1x2_f16x2(rg, 0);
-  a1[1] = e2m1x2_f16x2(rg8, 0);
-  a1[2] = e2m1x2_f16x2(rg, 1);
-  a1[3] = e2m1x2_f16x2(rg8, 1);
-  a2[0] = e2m1x2_f16x2(rg, 2);
-  a2[1] = e2m1x2_f16x2(rg8, 2);
-  a2[2] = e2m1x2_f16x2(rg, 3);
-  a2[3] = e2m1x2_f16x2(rg8, 3);
-}
-
-// Gate/up tile: acc[nt] (rows g, g+8 x columns 2c, 2c+1 of n8 tile nt) +=
-// sum over the tile's two scale blocks of scale(row, block) * (codes . x16).
-template <int NT>
-__device__ __forceinline__ void gu_tile(const uint4 q, uint32_t sc, const uint4 (&bx)[NT][2], float (&acc)[NT][4]) {
-#pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-    uint32_t a1[4], a2[4];
-    a_frags(q, bb, a1, a2);
-    const float sg = e8m0_f32((sc >> (16 * bb)) & 0xFFu);
-    const float sg8 = e8m0_f32((sc >> (16 * bb + 8)) & 0xFFu);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float t[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(t, a1, bx[nt][bb].x, bx[nt][bb].y);
-      mma16816(t, a2, bx[nt][bb].z, bx[nt][bb].w);
-      acc[nt][0] = fmaf(t[0], sg, acc[nt][0]);
-      acc[nt][1] = fmaf(t[1], sg, acc[nt][1]);
-      acc[nt][2] = fmaf(t[2], sg8, acc[nt][2]);
-      acc[nt][3] = fmaf(t[3], sg8, acc[nt][3]);
-    }
-  }
-}
-
-// Down tile: columns are (hi, lo) planes of pairs; acc[nt][0|1] = rows g | g+8
-// of pair c of tile nt. sb[nt][bb] holds the two per-MMA scales of pair c's h.
-template <int NT>
-__device__ __forceinline__ void dn_tile(const uint4 q, uint32_t sc, const uint4 (&bh)[NT][2],
-                                        const float2 (&sb)[NT][2], float (&acc)[NT][2]) {
-#pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-    uint32_t a1[4], a2[4];
-    a_frags(q, bb, a1, a2);
-    const float sg = e8m0_f32((sc >> (16 * bb)) & 0xFFu);
-    const float sg8 = e8m0_f32((sc >> (16 * bb + 8)) & 0xFFu);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float t1[4] = {0.f, 0.f, 0.f, 0.f}, t2[4] = {0.f, 0.f, 0.f, 0.f};
-      mma16816(t1, a1, bh[nt][bb].x, bh[nt][bb].y);
-      mma16816(t2, a2, bh[nt][bb].z, bh[nt][bb].w);
-      const float s1 = sb[nt][bb].x, s2 = sb[nt][bb].y;
-      acc[nt][0] = fmaf(t1[0] + t1[1], sg * s1, acc[nt][0]);
-      acc[nt][0] = fmaf(t2[0] + t2[1], sg * s2, acc[nt][0]);
-      acc[nt][1] = fmaf(t1[2] + t1[3], sg8 * s1, acc[nt][1]);
-      acc[nt][1] = fmaf(t2[2] + t2[3], sg8 * s2, acc[nt][1]);
-    }
-  }
-}
-
-// Power-of-two exponent sigma with m * 2^sigma in [2^14, 2^15) for m > 0,
-// clamped so that both 2^sigma and 2^-sigma are normal fp32 numbers.
-__device__ __forceinline__ int f16_headroom_exponent(float m) {
-  if (!(m > 0.f)) return 0;
-  int ex = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;  // floor(log2 m) for normal m
-  int s = 14 - ex;
-  return s < -112 ? -112 : (s > 126 ? 126 : s);
-}
-__device__ __forceinline__ float pow2f(int s) { return __uint_as_float((uint32_t)(s + 127) << 23); }
-
-// ---------------------------------------------------------------- double-float helpers
-// Error-free transformations (Knuth TwoSum, FMA-based TwoProduct); the _rn
-// intrinsics keep the compiler from contracting or reassociating them.
-struct dd {
-  float hi, lo;
-};
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  float bp = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
-}
-__device__ __forceinline__ void dd_mac(dd& acc, float a, float b) {
-  float p = __fmul_rn(a, b);
-  float pe = __fmaf_rn(a, b, -p);
-  float s, e;
-  two_sum(acc.hi, p, s, e);
-  acc.hi = s;
-  acc.lo = __fadd_rn(acc.lo, __fadd_rn(e, pe));
-}
-__device__ __forceinline__ dd dd_add(dd a, dd b) {
-  float s, e;
-  two_sum(a.hi, b.hi, s, e);
-  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
-  dd r;
-  r.hi = __fadd_rn(s, e);
-  r.lo = __fsub_rn(e, __fsub_rn(r.hi, s));
-  return r;
-}
-__device__ __forceinline__ dd dd_shfl_xor(dd a, int m) {
-  dd r;
-  r.hi = __shfl_xor_sync(0xffffffffu, a.hi, m);
-  r.lo = __shfl_xor_sync(0xffffffffu, a.lo, m);
-  return r;
-}
-__device__ __forceinline__ bool dd_greater(float ah, float al, int ai, float bh, float bl, int bi) {
-  // (a > b) in value, then the lower index first; pairs are normalised (|lo| <= ulp(hi)/2).
-  if (ah != bh) return ah > bh;
-  if (al != bl) return al > bl;
-  return ai < bi;
-}
 
 // ---------------------------------------------------------------- prep_x
 

@@ -29,10 +29,11 @@ def build_lib():
     return m
 
 
-def make_layer(m, wl: synth.Workload, L: dict, t_max: int | None = None, out_f32: bool = False, device: int = 0):
+def make_layer(m, wl: synth.Workload, L: dict, t_max: int | None = None, out_f32: bool = False, device: int = 0,
+               flags: int = 0):
     shape = m.LayerShape(d=wl.d, ffn=wl.ffn, n_experts=wl.E, top_k=wl.k, shared_ffn=wl.shared_ffn,
                          t_max=wl.T if t_max is None else t_max,
-                         out_dtype=m.MOE_OUT_F32 if out_f32 else m.MOE_OUT_BF16)
+                         out_dtype=m.MOE_OUT_F32 if out_f32 else m.MOE_OUT_BF16, flags=flags)
     layer = m.MoeLayer(shape, device)
     layer.load(L["w_router"], L["bias"], L["codes"], L["scales"])
     return layer

@@ -24,8 +24,8 @@ def m():
     return build_lib()
 
 
-def _parity(m, wl, L, out_f32=False, tokens=None, t_max=None):
-    layer = make_layer(m, wl, L, t_max=t_max, out_f32=out_f32)
+def _parity(m, wl, L, out_f32=False, tokens=None, t_max=None, flags=0):
+    layer = make_layer(m, wl, L, t_max=t_max, out_f32=out_f32, flags=flags)
     g = run_gpu(m, layer, L["x"], out_f32=out_f32)
     assert g["status"] == 0
     rr = oracle_route(wl, L)
@@ -57,17 +57,49 @@ SMALL_SHAPES = [
 
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 @pytest.mark.parametrize("out_f32", [False, True])
-def test_small_shapes(m, shape, out_f32):
+@pytest.mark.parametrize("path", ["fused", "general"])
+def test_small_shapes(m, shape, out_f32, path):
     T, d, F, E, k, S, z = shape
     wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
-    _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32)
+    flags = m.MOE_FLAG_GENERAL_PATH if path == "general" else 0
+    _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32, flags=flags)
 
 
-def test_every_token_count_up_to_16(m):
+@pytest.mark.parametrize("flags", [0, 2])
+def test_wide_scale_exponent_range(m, flags):
+    """E8M0 exponents over [96, 150] (2^-31 .. 2^23): the scale decode is exact across the range."""
+    wl = synth.WORKLOADS["tiny"].with_(name="wide", T=5, d=128, ffn=96, E=8, k=2, scale_lo=96, scale_hi=150)
+    _parity(m, wl, synth.gen_layer(wl, 21), out_f32=True, flags=flags)
+
+
+def test_path_selection(m):
+    wl = synth.WORKLOADS["decode"]
+    lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024))
+    assert m.moe_launches_per_forward(lay.ctx, 1) == 1 and m.moe_forward_phases(lay.ctx, 1) == ["layer"]
+    assert m.moe_launches_per_forward(lay.ctx, 16) == 1
+    assert m.moe_launches_per_forward(lay.ctx, 17) > 1
+    lay.close()
+
+
+def test_forced_timeout_is_reported_and_context_survives(m):
+    """A device-side wait that cannot be satisfied gives up within its bound,
+    the status word says MOE_ERR_TIMEOUT, and the GPU stays usable."""
+    wl = synth.WORKLOADS["tiny"]
+    L = synth.gen_layer(wl, 0)
+    layer = make_layer(m, wl, L, flags=m.MOE_FLAG_TEST_FORCE_TIMEOUT)
+    run_gpu(m, layer, L["x"])  # run_gpu synchronises; the kernel returned
+    assert layer.status(clear=True) == m.MOE_ERR_TIMEOUT
+    assert layer.status() == 0
+    layer.close()
+    _parity(m, wl, L)  # a normal context on the same GPU still matches the oracle
+
+
+@pytest.mark.parametrize("flags", [0, 2])
+def test_every_token_count_up_to_16(m, flags):
     """Row counts 1..16 (ragged n8 tiles) through one context sized t_max = 16."""
     wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=4, shared_ffn=64)
     L = synth.gen_layer(wl, 3)
-    layer = make_layer(m, wl, L, t_max=16, out_f32=True)
+    layer = make_layer(m, wl, L, t_max=16, out_f32=True, flags=flags)
     full_ref = oracle_layer(wl, L)
     for T in range(1, 17):
         g = run_gpu(m, layer, L["x"][:T], out_f32=True)
@@ -183,3 +215,18 @@ def test_full_size_workloads(m, name, layer_idx, tokens):
     wl = synth.WORKLOADS[name]
     L = synth.gen_layer(wl, layer_idx)
     _parity(m, wl, L, tokens=tokens)
+
+
+@pytest.mark.parametrize("name", ["decode", "verify", "small"])
+def test_fused_and_general_paths_agree_on_full_size(m, name):
+    """Both paths, same inputs: routing identical, outputs within fp32 tolerance of each other."""
+    wl = synth.WORKLOADS[name]
+    L = synth.gen_layer(wl, 1)
+    a = make_layer(m, wl, L, out_f32=True)
+    b = make_layer(m, wl, L, out_f32=True, flags=m.MOE_FLAG_GENERAL_PATH)
+    ga = run_gpu(m, a, L["x"], out_f32=True)
+    gb = run_gpu(m, b, L["x"], out_f32=True)
+    assert np.array_equal(ga["ids"], gb["ids"]) and np.array_equal(ga["perm"], gb["perm"])
+    check_output(ga["y"], gb["y"], 1e-5)
+    a.close()
+    b.close()
