@@ -151,6 +151,33 @@ int moe_forward_phases(const moe_ctx* ctx, int T, const char** names);
 /* Number of kernels one moe_forward of T tokens launches. */
 int moe_launches_per_forward(const moe_ctx* ctx, int T);
 
+/* Routing without any allocation, for callers that cannot call cudaMalloc
+ * (for example code running under an allocator that owns all device memory,
+ * or inside a region where allocation is forbidden). No counterpart on the
+ * pages: it is a packaging of the router, top-k and counting-sort steps above.
+ *
+ * Computes, for T tokens, the router logits (double-float), the top-k ids and
+ * softmax gates, and the counting sort of the T*top_k pairs by expert -- the
+ * same kernels and results as the routing of moe_forward's multi-kernel path.
+ * The caller passes device pointers: x bf16 [T][d] and w_router fp32
+ * [n_experts][d] (both 16-byte aligned), bias fp32 [n_experts] or NULL, and
+ * the outputs ids int32 [T][top_k], gates fp32 [T][top_k], counts int32
+ * [n_experts], offsets int32 [n_experts+1], perm int32 [T*top_k].
+ * The scratch is one static 1 MiB device array that every device loading the
+ * library holds until exit; sizes beyond it (T*n_experts > 65536 or
+ * T*top_k > 32768) are rejected with MOE_ERR_INVALID_ARG. The array keeps the
+ * last call's contents and is shared by all calls: calls whose kernels
+ * overlap on the GPU (other streams, other threads) race. The first call on
+ * each device looks the array up (with that device current); make that first
+ * call before any stream capture. Uses the current device; asynchronous on
+ * `stream`. Error text: moe_last_error(NULL) does not cover this call, use
+ * moe_route_static_error(). */
+int moe_route_static(const void* x, int T, int d, const float* w_router, const float* bias, int n_experts, int top_k,
+                     int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, void* stream);
+
+/* Text of the last error returned by moe_route_static ("" if none). */
+const char* moe_route_static_error(void);
+
 /* Bytes of packed expert weights the context holds (codes + scales). */
 size_t moe_weight_bytes(const moe_ctx* ctx);
 

@@ -35,7 +35,8 @@ MOE_FLAG_GENERAL_PATH = 2
 
 EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
-            "moe_launches_per_forward", "moe_weight_bytes", "moe_last_error", "moe_destroy"]
+            "moe_launches_per_forward", "moe_route_static", "moe_route_static_error", "moe_weight_bytes",
+            "moe_last_error", "moe_destroy"]
 
 
 class MoeError(RuntimeError):
@@ -75,6 +76,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp]
             lib.moe_get_logits.argtypes = [vp, vp, vp, vp]
             lib.moe_get_status.argtypes = [vp, i32]
+            lib.moe_route_static.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
+            lib.moe_route_static.restype = i32
+            lib.moe_route_static_error.argtypes = []
+            lib.moe_route_static_error.restype = ctypes.c_char_p
             lib.moe_weight_bytes.argtypes = [vp]
             lib.moe_weight_bytes.restype = ctypes.c_size_t
             lib.moe_last_error.argtypes = [vp]
@@ -174,6 +179,16 @@ def moe_forward_phases(ctx: int, T: int = 1) -> list[str]:
 
 def moe_launches_per_forward(ctx: int, T: int) -> int:
     return load_library().moe_launches_per_forward(ctx, T)
+
+
+def moe_route_static(x, T: int, d: int, w_router, bias, n_experts: int, top_k: int, ids, gates, counts, offsets,
+                     perm, stream=None) -> None:
+    """Routing without allocation (static device scratch); device pointers throughout."""
+    lib = load_library()
+    rc = lib.moe_route_static(ptr(x), T, d, ptr(w_router), ptr(bias), n_experts, top_k, ptr(ids), ptr(gates),
+                              ptr(counts), ptr(offsets), ptr(perm), stream_handle(stream))
+    if rc < 0:
+        raise MoeError(rc, "moe_route_static: " + lib.moe_route_static_error().decode(errors="replace"))
 
 
 def moe_weight_bytes(ctx: int) -> int:

@@ -112,6 +112,8 @@ constexpr int kForwardPhases = 4;
 extern const char* const kForwardPhaseNames;  // "route,gateup,down,combine"
 constexpr int kLaunchesPerForward = 7;
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);
+// Routing only (router logits, top-k gates, counting sort) of the general path.
+cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream);

@@ -545,6 +545,14 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   return cudaGetLastError();
 }
 
+cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
+  if (p.T == 0) return cudaSuccess;
+  router_kernel<<<dim3(p.E, (p.T + kRouterTT - 1) / kRouterTT), kRouterThreads, 0, stream>>>(p);
+  topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
+  bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream) {
