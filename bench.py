@@ -69,7 +69,8 @@ def phase_bytes(wl: synth.Workload, U: int, T: int) -> dict:
     gu = U * (F * d + F * d // 16) + (S * d + S * d // 16 if S else 0) + 2 * T * d
     dn = U * (F * d // 2 + F * d // 32) + (S * d // 2 + S * d // 32 if S else 0)
     route = wl.E * d * 4 + (4 * wl.E if wl.zipf_bias else 0) + 2 * T * d
-    return {"route": route, "gateup": gu, "down": dn, "combine": 2 * T * d}
+    # "layer" is the fused single-kernel path (T <= 16): every byte of the layer in one launch
+    return {"route": route, "gateup": gu, "down": dn, "combine": 2 * T * d, "layer": layer_bytes(wl, U, T)}
 
 
 def layer_flops(wl: synth.Workload, T: int) -> int:
@@ -183,6 +184,11 @@ def reduce_max(x: float, ws: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_value(ws: int, units_per_rank: int, seconds_max: float) -> float:
+    """Units of every rank over the slowest rank's time (weak scaling: each rank has its own batch)."""
+    return ws * units_per_rank / seconds_max
 
 
 def barrier(ws: int):
@@ -336,7 +342,7 @@ def run_ours(args, wl):
     barrier(ws)
     ms_local = e0.elapsed_time(e1) / args.steps
     ms = reduce_max(ms_local, ws)
-    value = ws * T * nl / (ms / 1000.0)
+    value = whole_job_value(ws, T * nl, ms / 1000.0)
     status = max(lay.status() for lay in layers)
 
     # per-kernel timing: the library records events at its phase boundaries
@@ -386,7 +392,7 @@ def run_ours(args, wl):
             layers[l].forward_host(xh[l], T, oh[l], stream, synchronize=(l == nl - 1))
     t_e2e = (time.perf_counter() - t0) / args.steps
     t_e2e = reduce_max(t_e2e, ws)
-    e2e_value = ws * T * nl / t_e2e
+    e2e_value = whole_job_value(ws, T * nl, t_e2e)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
