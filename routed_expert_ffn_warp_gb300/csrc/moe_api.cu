@@ -126,7 +126,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
-  const size_t o_done = take((size_t)(E + 1) * 4), o_rowcnt = take((size_t)(d / 16) * 4),
+  // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
+  const size_t o_done = take((size_t)2 * (E + 1) * 4), o_rowcnt = take((size_t)2 * (d / 16) * 4),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
                o_lw = take((size_t)std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
   ctx->ws_bytes = off;

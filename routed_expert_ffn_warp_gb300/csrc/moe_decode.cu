@@ -1,5 +1,5 @@
 // Fused decode path: the whole MoE layer for T <= 16 tokens in ONE persistent
-// kernel, one CTA per SM (16 warps: 15 consumers in 5 groups of 3, 1 producer).
+// kernel, one CTA per SM, 16 warps.
 //
 //   A  CTA b computes the double-float router logits of experts b, b+G, ...
 //      and publishes each as two 64-bit words (value bits | launch sequence
@@ -8,17 +8,22 @@
 //      barrier: no grid-wide sync, no atomics), then every CTA redundantly runs
 //      top-k + softmax gates, the counting sort of the T*k pairs and the slot
 //      list (identical, deterministic results in every CTA).
-//   C  gate/up units (slot, 16-row pair tile) are split evenly over the CTAs;
-//      each unit goes to a group of 3 consumer warps that split its K tiles in
-//      fixed thirds, while the producer warp streams the unit's chunks into a
-//      shared-memory ring with cp.async.bulk (TMA) + mbarriers. The group
-//      reduces its three partial sums in a fixed order, applies SiLU(gate)*up,
-//      and writes h (f16 hi + lo with a power-of-two scale per 16 elements);
-//      every finished unit bumps its slot's counter.
-//   D  down units (slot, 16 output rows), slot-major: the producer keeps
-//      streaming (down tiles arrive while gate/up still runs); a group waits
-//      (bounded) for its slot's h, multiplies, writes the partial rows, and the
-//      group finishing a row tile's last slot combines it:
+//   C  gate/up units (slot, 16-row pair tile) are split evenly over the CTAs,
+//      and each unit's k tiles into 3 fixed chunks (a split that depends on the
+//      unit alone, so its sums do not depend on the batch). A CTA's chunks are
+//      dealt to its 16 warps round-robin. Every warp streams its own chunks
+//      through a private shared-memory ring with cp.async (16-byte copies, no
+//      L1), several KB ahead of its math, so no warp waits on another for
+//      data. The last of a unit's 3 chunk warps to finish adds the 3 partial
+//      sums in chunk order, applies SiLU(gate)*up and writes h (f16 hi + lo
+//      with a power-of-two scale per 16 elements); every finished unit bumps
+//      its slot's counter.
+//   D  down units (slot, token half of <= 8 tokens, 16 output rows) in that
+//      order, chunked and dealt the same way; the warps prefetch their down
+//      tiles while gate/up still runs. For each (slot, half) of the CTA the
+//      CTA waits (bounded) for the slot's h and stages it in shared memory;
+//      the last chunk warp of a unit writes its partial rows, and the CTA
+//      finishing a row tile's last (slot, half) combines it:
 //      y = sum_j g_j part_j (slot order j) + shared, one rounding.
 //
 // The pages: expert pairs grouped by expert, one pass over each selected
@@ -47,24 +52,21 @@ using namespace dev;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = 16;
-constexpr int kGroups = 5;         // consumer groups of 3 warps; a group processes one unit at a time
-constexpr int kGroupWarps = 3;
-constexpr int kMemBlock = 5;       // member r of a group owns the k tiles kt with (kt / 5) % 3 == r
-constexpr int kProd = 15;          // producer warp
 constexpr int kRouterWarps = 12;   // warps 0..11 compute logits, 12..15 scale x
-constexpr int kStageTiles = 30;    // 544-byte tiles per ring stage: 16,320-byte bulk copies
-constexpr int kStageBytes = kStageTiles * kTileBytes;
-static_assert(kStageTiles % 2 == 0, "a gate/up tile pair never straddles two stages");
+constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
+constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
+constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
+constexpr int kMaxUS = 8;          // unit slots (partial-sum buffers) per phase, at most
 
 struct Shared {
-  uint64_t* full;
-  uint64_t* empty;
-  int* seq;     // [ns] stage index currently occupying each ring slot
-  __half* x16;
-  float* xinv;
+  int* ctl;     // [0, 8) gate/up arrivals, [8, 16) gate/up slot owners, [16, 24) down arrivals, [24, 32) down owners
+  __half* x16;  // phase C: [tcap][xstride] f16 x * 2^sigma_t
+  __half* hst;  // phase D (same memory): [kHalf][2][hstride] f16 h planes of one (slot, half)
+  float* hsc;   //   [kHalf][hgroups] their scales
+  float* xinv;  // [16]
   dd* red;      // [12 warps][16 tokens] router partials
-  float* part;     // [5 groups][2 members][pfloats][32 lanes] group partial sums
-  uint64_t* ubar;  // reserved
+  float* pgu;   // [n_us][3 chunks][2][16 rows][tcap] gate/up partial sums
+  float* pdn;   // [n_us][3 chunks][16 rows][min(8, tcap)] down partial sums
   int* ids;
   float* gates;
   int* cnt;
@@ -74,20 +76,25 @@ struct Shared {
   int* slot_e;
   int* slot_n;
   int* slot_q0;
-  int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number
-  uint8_t* ring;
+  int* hs_slot;  // (slot, half) list of the down phase
+  int* hs_half;
+  int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
+              // [4] (slot, half) pairs, [5] pairs of routed slots
+  uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
+  int* done;      // this launch's half of the global counters
+  int* rowcnt;
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* sm, const DecParams& p) {
   Shared s;
-  s.ubar = reinterpret_cast<uint64_t*>(sm);
-  s.full = s.ubar + 4;
-  s.empty = s.full + p.ns;
-  s.seq = reinterpret_cast<int*>(s.empty + p.ns);
+  s.ctl = reinterpret_cast<int*>(sm);
   s.x16 = reinterpret_cast<__half*>(sm + p.off_x16);
+  s.hst = s.x16;
+  s.hsc = reinterpret_cast<float*>(sm + p.off_hsc);
   s.xinv = reinterpret_cast<float*>(sm + p.off_xinv);
-  s.red = reinterpret_cast<dd*>(sm + p.off_pbuf);
-  s.part = reinterpret_cast<float*>(sm + p.off_pbuf + kRouterWarps * kDecodeMaxT * sizeof(dd));
+  s.red = reinterpret_cast<dd*>(sm + p.off_red);
+  s.pgu = reinterpret_cast<float*>(sm + p.off_pgu);
+  s.pdn = reinterpret_cast<float*>(sm + p.off_pdn);
   int* r = reinterpret_cast<int*>(sm + p.off_route);
   const int Pm = kDecodeMaxT * p.f.k, E = p.f.E;
   s.ids = r;
@@ -99,7 +106,9 @@ __device__ __forceinline__ Shared carve(uint8_t* sm, const DecParams& p) {
   s.slot_e = s.inv + Pm;
   s.slot_n = s.slot_e + E + 1;
   s.slot_q0 = s.slot_n + E + 1;
-  s.misc = s.slot_q0 + E + 1;
+  s.hs_slot = s.slot_q0 + E + 1;
+  s.hs_half = s.hs_slot + E + 1 + 64;
+  s.misc = s.hs_half + E + 1 + 64;
   s.ring = sm + p.off_ring;
   return s;
 }
@@ -115,39 +124,6 @@ __device__ void set_status(int* status, int code) { atomicCAS(status, 0, code); 
 __device__ void give_up(volatile int* abort, int* status) {
   *abort = 1;
   set_status(status, MOE_ERR_TIMEOUT);
-}
-
-__device__ bool wait_mbar(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit, int* status) {
-  if (*abort) return false;
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (timed_out(t0, limit)) {
-      give_up(abort, status);
-      return false;
-    }
-  }
-  return true;
-}
-
-// A consumer may parity-wait on a ring slot only once the producer has put
-// the stage it wants into that slot (a parity test cannot tell phases that are
-// two or more apart): spin on the slot's stage stamp, then on the mbarrier.
-__device__ bool wait_stage(const DecParams& p, const Shared& s, uint32_t st, volatile int* abort) {
-  const uint32_t j = st % p.ns;
-  volatile int* sq = s.seq + j;
-  if (*sq != (int)st) {
-    const uint64_t t0 = globaltimer();
-    while (*sq != (int)st) {
-      if (*abort) return false;
-      if (timed_out(t0, p.wait_ns)) {
-        give_up(abort, p.f.status);
-        return false;
-      }
-    }
-  }
-  return wait_mbar(&s.full[j], (st / p.ns) & 1u, abort, p.wait_ns, p.f.status);
 }
 
 __device__ bool wait_counter(const int* ctr, int target, volatile int* abort, long long limit, int* status) {
@@ -167,7 +143,7 @@ __device__ bool wait_counter(const int* ctr, int target, volatile int* abort, lo
 // ---------------------------------------------------------------- work units
 
 struct Unit {
-  int slot, idx, e, q0, n, f;
+  int slot, idx, e, q0, n, f;  // q0, n: first h/part row and rows (tokens) of the unit
 };
 
 __device__ __forceinline__ Unit gu_unit(const DecParams& p, const Shared& s, int u) {
@@ -189,14 +165,17 @@ __device__ __forceinline__ Unit gu_unit(const DecParams& p, const Shared& s, int
   return r;
 }
 
+// Down unit u: (slot, half) pair u / (d/16), row tile u % (d/16).
 __device__ __forceinline__ Unit dn_unit(const DecParams& p, const Shared& s, int u) {
   const int ud = p.f.d / 16;
+  const int hs = u / ud;
   Unit r;
-  r.slot = u / ud;
-  r.idx = u - r.slot * ud;
+  r.slot = s.hs_slot[hs];
+  r.idx = u - hs * ud;
+  const int half = s.hs_half[hs];
   r.e = s.slot_e[r.slot];
-  r.q0 = s.slot_q0[r.slot];
-  r.n = s.slot_n[r.slot];
+  r.q0 = s.slot_q0[r.slot] + kHalf * half;
+  r.n = min(kHalf, s.slot_n[r.slot] - kHalf * half);
   r.f = (r.e == p.f.E) ? p.f.S : p.f.F;
   return r;
 }
@@ -210,14 +189,11 @@ __device__ __forceinline__ void unit_range(int total, int& b0, int& b1) {
   b1 = (int)(((long long)(blockIdx.x + 1) * total) / gridDim.x);
 }
 
-// The CTA's weight stream is a sequence of 544-byte tiles: its gate/up units
-// (2 * K64(d) tiles each, gate and up of every k tile adjacent), then its down
-// units (K64(f) tiles each). Ring stage S holds stream tiles [30 S, 30 S + 30).
-__device__ __forceinline__ int dn_tile0(const DecParams& p, const Shared& s, int d0, int i, int n_gu_tiles) {
-  const int nrd = s.misc[0] * (p.f.d / 16);
-  const int before_r = max(0, min(d0 + i, nrd) - d0);
-  const int before_s = i - before_r;
-  return n_gu_tiles + before_r * k64_tiles(p.f.F) + before_s * (p.f.S > 0 ? k64_tiles(p.f.S) : 0);
+// k-tile range [k0, k1) of chunk c of a unit with K64 k tiles.
+__device__ __forceinline__ void chunk_range(int K64, int c, int& k0, int& k1) {
+  const int ck = (K64 + kChunks - 1) / kChunks;
+  k0 = min(K64, c * ck);
+  k1 = min(K64, k0 + ck);
 }
 
 // ---------------------------------------------------------------- phase A: router + x scaling
@@ -227,7 +203,25 @@ __device__ __forceinline__ unsigned long long pack_logit(float v, unsigned seq) 
   return ((unsigned long long)__float_as_uint(v) << 32) | seq;
 }
 
-__device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
+// The first 8 router weights of the thread (expert blockIdx.x, elements
+// 8 tid .. 8 tid + 7) are loaded before the kernel waits for the preceding
+// grid: the router weights are constant inputs of the layer.
+struct RouterPrefetch {
+  float4 w0, w1;
+};
+
+__device__ __forceinline__ RouterPrefetch router_prefetch(const DecParams& p) {
+  RouterPrefetch r;
+  const int tid = threadIdx.x;
+  if (tid < kRouterWarps * 32 && (int)blockIdx.x < p.f.E && tid < p.f.d / 8) {
+    const float4* wr = reinterpret_cast<const float4*>(p.f.w_router + (size_t)blockIdx.x * p.f.d);
+    r.w0 = __ldg(wr + 2 * tid);
+    r.w1 = __ldg(wr + 2 * tid + 1);
+  }
+  return r;
+}
+
+__device__ void router(const DecParams& p, const Shared& s, unsigned seq, const RouterPrefetch& pre) {
   const FwdParams& f = p.f;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d8 = f.d / 8, T = f.T;
@@ -237,8 +231,9 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
     for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = dd{0.f, 0.f};
     const float* wr = f.w_router + (size_t)e * f.d;
     for (int o = tid; o < d8; o += kRouterWarps * 32) {
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(wr) + 2 * o);
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(wr) + 2 * o + 1);
+      const bool first = e == (int)blockIdx.x && o == tid;
+      const float4 w0 = first ? pre.w0 : __ldg(reinterpret_cast<const float4*>(wr) + 2 * o);
+      const float4 w1 = first ? pre.w1 : __ldg(reinterpret_cast<const float4*>(wr) + 2 * o + 1);
       const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int t = 0; t < kDecodeMaxT; ++t) {
@@ -262,16 +257,19 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
       }
     }
     named_bar(1, kRouterWarps * 32);
-    if (tid < T) {
-      dd v = s.red[tid];
-      for (int w2 = 1; w2 < kRouterWarps; ++w2) v = dd_add(v, s.red[w2 * kDecodeMaxT + tid]);
-      if (f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
-      f.logit_hi[(size_t)tid * f.E + e] = v.hi;  // debug export
-      f.logit_lo[(size_t)tid * f.E + e] = v.lo;
-      __threadfence();  // orders this CTA's earlier writes (counter zeroing) before the words
-      unsigned long long* w = p.lwords + ((size_t)tid * f.E + e) * 2;
-      st_relaxed_u64(w, pack_logit(v.hi, seq));
-      st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
+    // warp t adds token t's 12 warp partials in a fixed tree, then publishes
+    for (int t = warp; t < T; t += kRouterWarps) {
+      dd v = lane < kRouterWarps ? s.red[lane * kDecodeMaxT + t] : dd{0.f, 0.f};
+      for (int o = 8; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
+      if (lane == 0) {
+        if (f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
+        f.logit_hi[(size_t)t * f.E + e] = v.hi;  // debug export
+        f.logit_lo[(size_t)t * f.E + e] = v.lo;
+        // the word carries its own value: no other data is published with it
+        unsigned long long* w = p.lwords + ((size_t)t * f.E + e) * 2;
+        st_relaxed_u64(w, pack_logit(v.hi, seq));
+        st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
+      }
     }
     named_bar(1, kRouterWarps * 32);
   }
@@ -305,10 +303,10 @@ __device__ void scale_x(const DecParams& p, const Shared& s, int w0, int nw) {
             __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
         h[j] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * f.d64 + 8 * o) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o) = make_uint4(h[0], h[1], h[2], h[3]);
     }
     for (int o = d8 + lane; o < f.d64 / 8; o += 32)  // K padding must be finite: zero
-      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * f.d64 + 8 * o) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o) = make_uint4(0, 0, 0, 0);
     if (lane == 0) s.xinv[t] = pow2f(-sg);
   }
 }
@@ -355,7 +353,6 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
       break;
     }
   }
-  __threadfence();  // acquire: later reads see what the publishers wrote before their words
   unsigned kh[NPL], kl[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
@@ -547,6 +544,33 @@ __device__ void bucket_large(const DecParams& p, const Shared& s) {
   }
 }
 
+// The (slot, half) pairs of the down phase, in slot order: a slot with more
+// than kHalf tokens contributes two (tokens [0, 8) and [8, n)). One warp.
+__device__ void build_halves(const Shared& s) {
+  const int lane = threadIdx.x & 31;
+  const int nsl = s.misc[1], nr = s.misc[0];
+  int base = 0, routed = 0;
+  for (int s0 = 0; s0 < nsl; s0 += 32) {
+    const int sl = s0 + lane;
+    const int h = sl < nsl ? (s.slot_n[sl] > kHalf ? 2 : 1) : 0;
+    int inc = h;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    for (int j = 0; j < h; ++j) {
+      s.hs_slot[base + inc - h + j] = sl;
+      s.hs_half[base + inc - h + j] = j;
+    }
+    routed += (int)__reduce_add_sync(0xffffffffu, (unsigned)(sl < nr ? h : 0));
+    base += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) {
+    s.misc[4] = base;
+    s.misc[5] = routed;
+  }
+}
+
 __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volatile int* abort) {
   const int warp = threadIdx.x >> 5;
   if (warp < p.f.T) {
@@ -558,140 +582,334 @@ __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volat
   if (warp == 0) {
     if (p.f.P <= 32) bucket_small(p, s);
     else bucket_large(p, s);
+    __syncwarp();
+    build_halves(s);
   } else if (warp == 1 && blockIdx.x == 0 && p.f.P <= 32) {
     export_counts_small(p, s);
   }
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- phases C + D: producer
+// ---------------------------------------------------------------- phases C + D: per-warp weight streams
+//
+// The CTA's items (unit, chunk) -- its gate/up items, then its down items --
+// are dealt to the 16 warps round-robin (item i to warp i % 16). A warp copies
+// the weight tiles of its items, in order, through its own ring of RG slots of
+// 1,088 bytes (a gate/up tile pair, or two consecutive down tiles) with
+// cp.async, RG slots ahead of the math; completion
+// is tracked with per-thread cp.async groups (one group per slot, empty groups
+// past the end of the stream keep the count uniform).
 
-// Source address of stream unit `u` of the CTA (gate/up units first).
-struct StreamCursor {
-  const uint8_t* src;  // next tile of the current unit
-  int left;            // tiles left in the current unit
-  int u;               // CTA-local unit index across both phases
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Wait until at most N of this thread's most recent groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// L2 policy for the weight stream: each byte is read once per layer call.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// The CTA's work: its ranges of gate/up and down units.
+struct Plan {
+  int g0, ngu;  // gate/up units [g0, g0 + ngu)
+  int d0, ndn;  // down units [d0, d0 + ndn)
+  int nguw, ndnw;  // items of this warp in each phase
 };
 
-__device__ void producer(const DecParams& p, const Shared& s, volatile int* abort) {
+__device__ __forceinline__ int warp_items(int n_items, int w) { return n_items > w ? (n_items - w + kWarps - 1) / kWarps : 0; }
+
+__device__ __forceinline__ Plan make_plan(const DecParams& p, const Shared& s, int w) {
   const FwdParams& f = p.f;
-  const int nr = s.misc[0], nsl = s.misc[1];
-  const int NUg = nr * (f.F / 16) + (f.S > 0 ? f.S / 16 : 0);
-  const int NUd = nsl * (f.d / 16);
-  const int K64d = k64_tiles(f.d);
-  int g0, g1, d0, d1;
-  unit_range(NUg, g0, g1);
-  unit_range(NUd, d0, d1);
-  const int ngu = g1 - g0, ndn = d1 - d0;
-  const int n_tiles = dn_tile0(p, s, d0, ndn, ngu * 2 * K64d);
-  auto unit_src = [&](int u, int& tiles) -> const uint8_t* {
-    if (u < ngu) {
-      const Unit un = gu_unit(p, s, g0 + u);
-      tiles = 2 * K64d;
-      return f.packed + (size_t)un.e * f.expert_stride + (size_t)un.idx * K64d * 2 * kTileBytes;
-    }
-    const Unit un = dn_unit(p, s, d0 + (u - ngu));
+  const int NUg = s.misc[0] * (f.F / 16) + (f.S > 0 ? f.S / 16 : 0);
+  const int NUd = s.misc[4] * (f.d / 16);
+  Plan pl;
+  int b1;
+  unit_range(NUg, pl.g0, b1);
+  pl.ngu = b1 - pl.g0;
+  unit_range(NUd, pl.d0, b1);
+  pl.ndn = b1 - pl.d0;
+  pl.nguw = warp_items(kChunks * pl.ngu, w);
+  pl.ndnw = warp_items(kChunks * pl.ndn, w);
+  return pl;
+}
+
+// Item j of warp w: CTA-local unit, chunk, k-tile range, source of its first
+// group, and its groups.
+struct Item {
+  int u;     // CTA-local unit index within its phase
+  int c;     // chunk
+  int k0, k1;
+  bool down;
+  const uint8_t* src;
+  int ng;         // slots (groups) of the item
+  int last_bytes; // bytes of its last group
+};
+
+__device__ __forceinline__ Item item_of(const DecParams& p, const Shared& s, const Plan& pl, int w, int j) {
+  const FwdParams& f = p.f;
+  Item it;
+  if (j < pl.nguw) {
+    const int i = w + kWarps * j;
+    it.u = i / kChunks;
+    it.c = i - it.u * kChunks;
+    it.down = false;
+    const Unit un = gu_unit(p, s, pl.g0 + it.u);
+    const int K64d = k64_tiles(f.d);
+    chunk_range(K64d, it.c, it.k0, it.k1);
+    it.src = f.packed + (size_t)un.e * f.expert_stride + ((size_t)un.idx * K64d + it.k0) * kGroupBytes;
+    it.ng = it.k1 - it.k0;
+    it.last_bytes = kGroupBytes;
+  } else {
+    const int i = w + kWarps * (j - pl.nguw);
+    it.u = i / kChunks;
+    it.c = i - it.u * kChunks;
+    it.down = true;
+    const Unit un = dn_unit(p, s, pl.d0 + it.u);
     const int K64f = k64_tiles(un.f);
-    tiles = K64f;
-    return f.packed + (size_t)un.e * f.expert_stride + gu_packed_bytes(f.d, un.f) + (size_t)un.idx * K64f * kTileBytes;
-  };
-  StreamCursor cur;
-  cur.u = 0;
-  cur.src = (ngu + ndn > 0) ? unit_src(0, cur.left) : nullptr;
-  if (ngu + ndn == 0) cur.left = 0;
-  const int n_stages = (n_tiles + kStageTiles - 1) / kStageTiles;
-  for (int st = 0; st < n_stages; ++st) {
-    const uint32_t j = st % p.ns, par = ((st / p.ns) & 1u) ^ 1u;
-    wait_mbar(&s.empty[j], par, abort, p.wait_ns, f.status);
-    if (*abort) break;
-    const int nt = min(kStageTiles, n_tiles - st * kStageTiles);
-    *reinterpret_cast<volatile int*>(s.seq + j) = st;
-    mbar_arrive_expect_tx(&s.full[j], (uint32_t)nt * kTileBytes);
-    uint8_t* dst = s.ring + (size_t)j * kStageBytes;
-    const uint8_t* run_src = nullptr;  // pending copy: merged while the source stays contiguous
-    uint32_t run_bytes = 0;
-    for (int left = nt; left > 0;) {
-      if (cur.left == 0) {
-        ++cur.u;
-        cur.src = unit_src(cur.u, cur.left);
-      }
-      const int take = min(left, cur.left);
-      if (run_src && run_src + run_bytes == cur.src) {
-        run_bytes += (uint32_t)take * kTileBytes;
-      } else {
-        if (run_src) {
-          bulk_g2s(dst, run_src, run_bytes, &s.full[j]);
-          dst += run_bytes;
-        }
-        run_src = cur.src;
-        run_bytes = (uint32_t)take * kTileBytes;
-      }
-      cur.src += (size_t)take * kTileBytes;
-      cur.left -= take;
-      left -= take;
-    }
-    if (run_src) bulk_g2s(dst, run_src, run_bytes, &s.full[j]);
-    if (nt < kStageTiles) mbar_arrive_cnt(&s.empty[j], (uint32_t)(kStageTiles - nt));  // tiles nobody consumes
+    chunk_range(K64f, it.c, it.k0, it.k1);
+    it.src = f.packed + (size_t)un.e * f.expert_stride + gu_packed_bytes(f.d, un.f) +
+             ((size_t)un.idx * K64f + it.k0) * kTileBytes;
+    const int nt = it.k1 - it.k0;
+    it.ng = (nt + 1) / 2;
+    it.last_bytes = (nt & 1) ? kTileBytes : kGroupBytes;
   }
-  // every issued copy lands before the CTA may exit: wait (bounded) on the
-  // last phase of each ring slot that was used
-  const int used = n_stages < p.ns ? n_stages : p.ns;
-  for (int i = 0; i < used; ++i) {
-    const int sidx = n_stages - 1 - i;
-    const uint32_t j = sidx % p.ns, par = (sidx / p.ns) & 1u;
+  return it;
+}
+
+// Issue cursor of a warp's stream.
+struct Cursor {
+  int j, g, ng, nitems, last_bytes;
+  const uint8_t* src;
+};
+
+__device__ __forceinline__ void cursor_seek(const DecParams& p, const Shared& s, const Plan& pl, int w, Cursor& cu) {
+  while (cu.j < cu.nitems) {
+    const Item it = item_of(p, s, pl, w, cu.j);
+    if (it.ng > 0) {
+      cu.src = it.src;
+      cu.ng = it.ng;
+      cu.last_bytes = it.last_bytes;
+      cu.g = 0;
+      return;
+    }
+    ++cu.j;
+  }
+}
+
+// Copy the cursor's next group into ring slot `dst` (one cp.async group; an
+// empty group once the stream is exhausted) and advance.
+__device__ __forceinline__ void issue_group(const DecParams& p, const Shared& s, const Plan& pl, int w, Cursor& cu,
+                                            uint8_t* dst, uint64_t pol) {
+  const int lane = threadIdx.x & 31;
+  if (cu.j < cu.nitems) {
+    const int n16 = (cu.g == cu.ng - 1 ? cu.last_bytes : kGroupBytes) / 16;
+    for (int k = lane; k < n16; k += 32) cp_async16(dst + 16 * k, cu.src + 16 * k, pol);
+    cu.src += kGroupBytes;
+    if (++cu.g == cu.ng) {
+      ++cu.j;
+      cursor_seek(p, s, pl, w, cu);
+    }
+  }
+  cp_async_commit();
+}
+
+// Per-unit partial-sum slots: writers of CTA-local unit u use slot u % n_us
+// once its owner word says u; the reducer hands the slot to unit u + n_us.
+__device__ bool claim_slot(const DecParams& p, int* owner, int u, volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && ld_acquire_cta_shared(owner) != u) {
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&s.full[j], par)) {
-      if (timed_out(t0, p.wait_ns)) {
-        set_status(f.status, MOE_ERR_TIMEOUT);
+    while (ld_acquire_cta_shared(owner) != u) {
+      if (*abort || timed_out(t0, p.wait_ns)) {
+        if (!*abort) give_up(abort, p.f.status);
+        ok = 0;
         break;
       }
     }
   }
-}
-
-// ---------------------------------------------------------------- phases C + D: consumer groups
-//
-// Group g (3 warps) takes the CTA's units g, g+5, ...; member r of the group
-// owns the unit's k tiles kt with (kt / 5) % 3 == r -- a fixed split, so a
-// unit's sums do not depend on the batch -- and the three members share every
-// ring stage of their unit. After its k tiles each member hands its partial
-// sums to member 0, which adds them in the order member 0, 1, 2.
-
-__device__ __forceinline__ int member_first(int r) { return r * kMemBlock; }
-__device__ __forceinline__ int member_next(int kt) {
-  return ((kt + 1) % kMemBlock) ? kt + 1 : kt + 1 + (kGroupWarps - 1) * kMemBlock;
-}
-
-template <int NV>
-__device__ __forceinline__ void group_reduce(const DecParams& p, const Shared& s, int grp, int mem, float (&v)[NV]) {
-  const int lane = threadIdx.x & 31;
-  float* buf = s.part + (size_t)grp * 2 * p.pfloats * 32;
-  if (mem > 0) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) buf[((size_t)(mem - 1) * p.pfloats + i) * 32 + lane] = v[i];
-  }
-  named_bar(2 + grp, kGroupWarps * 32);
-  if (mem == 0) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = (v[i] + buf[(size_t)i * 32 + lane]) + buf[((size_t)p.pfloats + i) * 32 + lane];
-  }
-  named_bar(2 + grp, kGroupWarps * 32);
-}
-
-// Release `used` tiles of ring stage `cur` (the empty barrier counts tiles).
-__device__ __forceinline__ void release_tiles(const DecParams& p, const Shared& s, int cur, int used) {
-  if (cur < 0) return;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive_cnt(&s.empty[cur % p.ns], (uint32_t)used);
+  return ok != 0;
+}
+
+// Count this warp's chunk of unit slot `us`; true for the last of the 3.
+__device__ __forceinline__ bool arrive_chunk(int* arrivals) {
+  __syncwarp();
+  int last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    __threadfence_block();
+    last = atomicAdd(arrivals, 1) == kChunks - 1;
+    if (last) __threadfence_block();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();
+  return last != 0;
+}
+
+__device__ __forceinline__ void free_slot(int* arrivals, int* owner, int next_owner) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    *arrivals = 0;
+    st_release_cta_shared(owner, next_owner);
+  }
+}
+
+// Gate/up unit epilogue (the last chunk warp): h for the 16 rows S_tau of the
+// unit and each of its tokens. Lanes 0-15 take rows 0-15 of an even token,
+// lanes 16-31 of the next one; the f16 scale of h is shared by a token's 16 rows.
+__device__ void gateup_reduce(const DecParams& p, const Shared& s, const Unit& un, const float* pb) {
+  const FwdParams& f = p.f;
+  const int lane = threadIdx.x & 31, r = lane & 15;
+  const int tc = p.tcap, cs = 32 * tc;  // chunk stride
+  for (int m0 = 0; m0 < un.n; m0 += 2) {
+    const int m = m0 + (lane >> 4);
+    float h = 0.f;
+    if (m < un.n) {
+      float gs = 0.f, us = 0.f;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        gs += pb[c * cs + r * tc + m];
+        us += pb[c * cs + (16 + r) * tc + m];
+      }
+      const float xi = s.xinv[token_of(p, s, un.q0 + m)];
+      const float gate = gs * xi, up = us * xi;
+      h = gate / (1.f + expf(-gate)) * up;
+    }
+    float mx = fabsf(h);
+    for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (m < un.n) {
+      const int sh = f16_headroom_exponent(mx);
+      const int q = un.q0 + m;
+      __half* hi = reinterpret_cast<__half*>(f.hbuf) + (size_t)q * 2 * f.fmax64;
+      __half* lo = hi + f.fmax64;
+      const int i = 32 * (un.idx >> 1) + 8 * (r >> 2) + 4 * (un.idx & 1) + (r & 3);
+      const float v = h * pow2f(sh);
+      const __half vh = __float2half_rn(v);
+      hi[i] = vh;
+      lo[i] = __float2half_rn(v - __half2float(vh));
+      if (r == 0) f.hscale[(size_t)q * f.hgroups + un.idx] = pow2f(-sh);
+    }
+  }
+}
+
+// Down unit epilogue (the last chunk warp): the unit's 16 partial rows of each
+// of its tokens; the CTA finishing a row tile's last (slot, half) combines it.
+__device__ void down_reduce(const DecParams& p, const Shared& s, const Unit& un, const float* pb) {
+  const FwdParams& f = p.f;
+  const int lane = threadIdx.x & 31;
+  const int hh = min(kHalf, p.tcap), cs = 16 * hh;
+  for (int o = lane; o < 16 * un.n; o += 32) {
+    const int r = o & 15, m = o >> 4;
+    float a = 0.f;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) a += pb[c * cs + r * hh + m];
+    f.part[(size_t)(un.q0 + m) * f.d + 16 * un.idx + r] = a;
+  }
+}
+
+__device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
+  const FwdParams& f = p.f;
+  const int lane = threadIdx.x & 31;
+  const int r0 = 16 * idx;
+  for (int o = lane; o < f.T * 16; o += 32) {
+    const int t = o >> 4, r = o & 15;
+    float a = 0.f;
+    for (int j0 = 0; j0 < f.k; j0 += 4) {  // loads of a group issued together, sums kept in slot order
+      float pv[4];
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu)
+        pv[uu] = (j0 + uu < f.k) ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + uu] * f.d + r0 + r) : 0.f;
+#pragma unroll
+      for (int uu = 0; uu < 4; ++uu)
+        if (j0 + uu < f.k) a = fmaf(s.gates[t * f.k + j0 + uu], pv[uu], a);
+    }
+    if (f.S > 0) a += __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
+    if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = a;
+    else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(a);
+  }
+}
+
+// Stage h of (slot, half) pair hs in shared memory (all threads of the CTA,
+// after the slot's h is complete): planes [m][hi | lo][hstride] and scales.
+__device__ void stage_h(const DecParams& p, const Shared& s, int hs) {
+  const FwdParams& f = p.f;
+  const int slot = s.hs_slot[hs], half = s.hs_half[hs];
+  const int q0 = s.slot_q0[slot] + kHalf * half, n = min(kHalf, s.slot_n[slot] - kHalf * half);
+  const int per_row = 2 * f.fmax64 / 8;  // 16-byte pieces of a row's two planes
+  for (int o = threadIdx.x; o < n * per_row; o += kThreads) {
+    const int m = o / per_row, k = o - m * per_row;
+    const int plane = k / (f.fmax64 / 8), kk = k - plane * (f.fmax64 / 8);
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(f.hbuf + ((size_t)(q0 + m) * 2 + plane) * f.fmax64) + kk);
+    *reinterpret_cast<uint4*>(s.hst + (size_t)(m * 2 + plane) * p.hstride + 8 * kk) = v;
+  }
+  for (int o = threadIdx.x; o < n * f.hgroups; o += kThreads) {
+    const int m = o / f.hgroups, k = o - m * f.hgroups;
+    s.hsc[m * f.hgroups + k] = __ldcg(f.hscale + (size_t)(q0 + m) * f.hgroups + k);
+  }
 }
 
 template <int NT>
-__device__ void gateup_unit(const DecParams& p, const Shared& s, const Unit& un, int t0, int grp, int mem,
-                            volatile int* abort) {
-  const FwdParams& f = p.f;
+__device__ __forceinline__ void gateup_group(const DecParams& p, const Shared& s, const uint8_t* slot, int kt,
+                                             const int (&tokB)[NT], float (&acc)[2 * NT * 4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int K64d = k64_tiles(f.d);
-  float acc[2 * NT * 4];  // gate then up, n8 tile nt, fragment r
+  const uint4 qg = *reinterpret_cast<const uint4*>(slot + 16 * lane);
+  const uint32_t sgv = *reinterpret_cast<const uint32_t*>(slot + kTileCodeBytes + 4 * g);
+  const uint4 qu = *reinterpret_cast<const uint4*>(slot + kTileBytes + 16 * lane);
+  const uint32_t suv = *reinterpret_cast<const uint32_t*>(slot + kTileBytes + kTileCodeBytes + 4 * g);
+  uint4 bx[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb)
+      bx[nt][bb] = tokB[nt] >= 0 ? *reinterpret_cast<const uint4*>(s.x16 + (size_t)tokB[nt] * p.xstride + kt * 64 +
+                                                                   bb * 32 + c * 8)
+                                 : make_uint4(0, 0, 0, 0);
+  float (&ag)[NT][4] = *reinterpret_cast<float(*)[NT][4]>(acc);
+  float (&au)[NT][4] = *reinterpret_cast<float(*)[NT][4]>(acc + NT * 4);
+  gu_tile<NT>(qg, sgv, bx, ag);
+  gu_tile<NT>(qu, suv, bx, au);
+}
+
+template <int NT>
+__device__ __forceinline__ void down_tile_smem(const DecParams& p, const Shared& s, const uint8_t* t8, int kt,
+                                               int nh, float (&acc)[NT][2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const uint4 q = *reinterpret_cast<const uint4*>(t8 + 16 * lane);
+  const uint32_t scv = *reinterpret_cast<const uint32_t*>(t8 + kTileCodeBytes + 4 * g);
+  uint4 bh[NT][2];
+  float2 sb[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int mb = 4 * nt + (g >> 1), md = 4 * nt + c;
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      bh[nt][bb] = mb < nh ? *reinterpret_cast<const uint4*>(s.hst + (size_t)(mb * 2 + (g & 1)) * p.hstride +
+                                                             kt * 64 + bb * 32 + c * 8)
+                           : make_uint4(0, 0, 0, 0);
+      sb[nt][bb] = md < nh ? *reinterpret_cast<const float2*>(s.hsc + md * p.f.hgroups + 2 * (2 * kt + bb))
+                           : make_float2(0.f, 0.f);
+    }
+  }
+  dn_tile<NT>(q, scv, bh, sb, acc);
+}
+
+// Consume the groups of one item from the warp's ring (kc: the warp's count
+// of consumed groups; every consumed slot is refilled from the cursor).
+template <int NT, int RG>
+__device__ void gateup_item(const DecParams& p, const Shared& s, const Plan& pl, const Item& it, const Unit& un,
+                            uint8_t* ring, int& slot, Cursor& cu, uint64_t pol, int w, volatile int* abort) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  float acc[2 * NT * 4];
 #pragma unroll
   for (int i = 0; i < 2 * NT * 4; ++i) acc[i] = 0.f;
   int tokB[NT];
@@ -700,242 +918,151 @@ __device__ void gateup_unit(const DecParams& p, const Shared& s, const Unit& un,
     const int m = 8 * nt + g;
     tokB[nt] = (m < un.n) ? token_of(p, s, un.q0 + m) : -1;
   }
-  int cur = -1, used = 0;
-  bool ok = false;
-  for (int kt = member_first(mem); kt < K64d; kt = member_next(kt)) {
-    const int tile = t0 + 2 * kt;
-    const int st = tile / kStageTiles;
-    if (st != cur) {
-      release_tiles(p, s, cur, used);
-      ok = wait_stage(p, s, (uint32_t)st, abort);
-      cur = st;
-      used = 0;
-    }
-    used += 2;
-    if (ok) {
-      const uint8_t* tg = s.ring + (size_t)(st % p.ns) * kStageBytes + (size_t)(tile % kStageTiles) * kTileBytes;
-      const uint8_t* tu = tg + kTileBytes;
-      const uint4 qg = *reinterpret_cast<const uint4*>(tg + 16 * lane);
-      const uint32_t sgv = *reinterpret_cast<const uint32_t*>(tg + kTileCodeBytes + 4 * g);
-      const uint4 qu = *reinterpret_cast<const uint4*>(tu + 16 * lane);
-      const uint32_t suv = *reinterpret_cast<const uint32_t*>(tu + kTileCodeBytes + 4 * g);
-      uint4 bx[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb)
-          bx[nt][bb] = tokB[nt] >= 0 ? *reinterpret_cast<const uint4*>(s.x16 + (size_t)tokB[nt] * f.d64 + kt * 64 +
-                                                                       bb * 32 + c * 8)
-                                     : make_uint4(0, 0, 0, 0);
-      float (&ag)[NT][4] = *reinterpret_cast<float(*)[NT][4]>(acc);
-      float (&au)[NT][4] = *reinterpret_cast<float(*)[NT][4]>(acc + NT * 4);
-      gu_tile<NT>(qg, sgv, bx, ag);
-      gu_tile<NT>(qu, suv, bx, au);
-    }
+  for (int kt = it.k0; kt < it.k1; ++kt) {
+    cp_async_wait<RG - 1>();
+    __syncwarp();
+    uint8_t* sl = ring + slot * kGroupBytes;
+    gateup_group<NT>(p, s, sl, kt, tokB, acc);
+    __syncwarp();
+    issue_group(p, s, pl, w, cu, sl, pol);
+    if (++slot == RG) slot = 0;
   }
-  release_tiles(p, s, cur, used);
-  group_reduce<2 * NT * 4>(p, s, grp, mem, acc);
-  if (mem != 0) return;
-  // SwiGLU epilogue (member 0): h for the 16 rows S_tau of this unit and each token column
+  const int us = it.u % p.n_us;
+  if (!claim_slot(p, s.ctl + kMaxUS + us, it.u, abort)) return;
+  float* pb = s.pgu + (size_t)us * kChunks * 32 * p.tcap;
+  {
+    float* pw = pb + it.c * 32 * p.tcap;  // [gate | up][16 rows][tcap columns]
+    const int tc = p.tcap;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float hv[4];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int m = 8 * nt + 2 * c + (r & 1);
-      float h = 0.f;
-      if (m < un.n) {
-        const float xi = s.xinv[token_of(p, s, un.q0 + m)];
-        const float gate = acc[nt * 4 + r] * xi, up = acc[NT * 4 + nt * 4 + r] * xi;
-        h = gate / (1.f + expf(-gate)) * up;
+      for (int r = 0; r < 4; ++r) {
+        const int row = g + 8 * (r >> 1), col = 8 * nt + 2 * c + (r & 1);
+        if (col < un.n) {
+          pw[row * tc + col] = acc[nt * 4 + r];
+          pw[(16 + row) * tc + col] = acc[NT * 4 + nt * 4 + r];
+        }
       }
-      hv[r] = h;
-    }
-    float mx0 = fmaxf(fabsf(hv[0]), fabsf(hv[2]));
-    float mx1 = fmaxf(fabsf(hv[1]), fabsf(hv[3]));
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-#pragma unroll
-    for (int col = 0; col < 2; ++col) {
-      const int m = 8 * nt + 2 * c + col;
-      if (m >= un.n) continue;
-      const int q = un.q0 + m;
-      const int sh = f16_headroom_exponent(col ? mx1 : mx0);
-      const float sc = pow2f(sh);
-      __half* hi = reinterpret_cast<__half*>(f.hbuf) + (size_t)q * 2 * f.fmax64;
-      __half* lo = hi + f.fmax64;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int rr = g + 8 * half;
-        const int i = 32 * (un.idx >> 1) + 8 * (rr >> 2) + 4 * (un.idx & 1) + (rr & 3);
-        const float v = hv[2 * half + col] * sc;
-        const __half vh = __float2half_rn(v);
-        hi[i] = vh;
-        lo[i] = __float2half_rn(v - __half2float(vh));
-      }
-      if (g == 0) f.hscale[(size_t)q * f.hgroups + un.idx] = pow2f(-sh);
-    }
   }
+  if (!arrive_chunk(s.ctl + us)) return;
+  gateup_reduce(p, s, un, pb);
+  free_slot(s.ctl + us, s.ctl + kMaxUS + us, it.u + p.n_us);
   __threadfence();
   __syncwarp();
-  if (lane == 0) atomicAdd(&p.done[un.slot], 1);
+  if (lane == 0) atomicAdd(&s.done[un.slot], 1);
 }
 
-template <int NT>
-__device__ void down_unit(const DecParams& p, const Shared& s, const Unit& un, int t0, int grp, int mem,
-                          volatile int* abort) {
-  const FwdParams& f = p.f;
+template <int NT, int RG>
+__device__ void down_item(const DecParams& p, const Shared& s, const Plan& pl, const Item& it, const Unit& un,
+                          uint8_t* ring, int& slot, Cursor& cu, uint64_t pol, int w, volatile int* abort) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int K64f = k64_tiles(un.f);
-  float acc[2 * NT];
+  float acc[NT][2];
 #pragma unroll
-  for (int i = 0; i < 2 * NT; ++i) acc[i] = 0.f;
-  const uint16_t* hrow[NT];
-  const float* srow[NT];
-  int qD[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int mb = 4 * nt + (g >> 1), md = 4 * nt + c;
-    qD[nt] = (md < un.n) ? un.q0 + md : -1;
-    hrow[nt] = (mb < un.n) ? f.hbuf + ((size_t)(un.q0 + mb) * 2 + (g & 1)) * f.fmax64 + c * 8 : nullptr;
-    srow[nt] = qD[nt] >= 0 ? f.hscale + (size_t)qD[nt] * f.hgroups : nullptr;
-  }
-  if (member_first(mem) < K64f) {
-    // h of this slot is written by other CTAs: wait (bounded) for all its gate/up units
-    if (lane == 0)
-      wait_counter(&p.done[un.slot], un.f / 16 + p.test_extra, abort, p.test_extra ? p.test_wait_ns : p.wait_ns,
-                   f.status);
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+  for (int kt = it.k0; kt < it.k1; kt += 2) {
+    cp_async_wait<RG - 1>();
     __syncwarp();
+    uint8_t* sl = ring + slot * kGroupBytes;
+    down_tile_smem<NT>(p, s, sl, kt, un.n, acc);
+    if (kt + 1 < it.k1) down_tile_smem<NT>(p, s, sl + kTileBytes, kt + 1, un.n, acc);
+    __syncwarp();
+    issue_group(p, s, pl, w, cu, sl, pol);
+    if (++slot == RG) slot = 0;
   }
-  int cur = -1, used = 0;
-  bool ok = false;
-  // h fragment loads are batched (BATCH k tiles at a time, all loads before the MMAs)
-  constexpr int BATCH = NT == 1 ? kMemBlock : 1;
-  for (int kb = member_first(mem); kb < K64f; kb = member_next(kb + BATCH - 1)) {
-    uint4 bh[BATCH][NT][2];
-    float2 sb[BATCH][NT][2];
+  const int us = it.u % p.n_us;
+  if (!claim_slot(p, s.ctl + 3 * kMaxUS + us, it.u, abort)) return;
+  const int hh = min(kHalf, p.tcap);
+  float* pb = s.pdn + (size_t)us * kChunks * 16 * hh;
+  {
+    float* pw = pb + it.c * 16 * hh;  // [16 rows][min(8, tcap) token columns]
 #pragma unroll
-    for (int i = 0; i < BATCH; ++i)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int kt = kb + i;
-          const bool in = kt < K64f;
-          // plain (L1-cached) loads: h is final once the slot counter was seen
-          bh[i][nt][bb] = (in && hrow[nt]) ? *reinterpret_cast<const uint4*>(hrow[nt] + kt * 64 + bb * 32)
-                                           : make_uint4(0, 0, 0, 0);
-          sb[i][nt][bb] = (in && srow[nt]) ? *reinterpret_cast<const float2*>(srow[nt] + 2 * (2 * kt + bb))
-                                           : make_float2(0.f, 0.f);
-        }
-#pragma unroll
-    for (int i = 0; i < BATCH; ++i) {
-      const int kt = kb + i;
-      if (kt >= K64f) break;
-      const int tile = t0 + kt;
-      const int st = tile / kStageTiles;
-      if (st != cur) {
-        release_tiles(p, s, cur, used);
-        ok = wait_stage(p, s, (uint32_t)st, abort);
-        cur = st;
-        used = 0;
-      }
-      ++used;
-      if (ok) {
-        const uint8_t* t8 = s.ring + (size_t)(st % p.ns) * kStageBytes + (size_t)(tile % kStageTiles) * kTileBytes;
-        const uint4 q = *reinterpret_cast<const uint4*>(t8 + 16 * lane);
-        const uint32_t scv = *reinterpret_cast<const uint32_t*>(t8 + kTileCodeBytes + 4 * g);
-        float (&a2)[NT][2] = *reinterpret_cast<float(*)[NT][2]>(acc);
-        dn_tile<NT>(q, scv, bh[i], sb[i], a2);
+    for (int nt = 0; nt < NT; ++nt) {
+      const int md = 4 * nt + c;
+      if (md < un.n) {
+        pw[g * hh + md] = acc[nt][0];
+        pw[(g + 8) * hh + md] = acc[nt][1];
       }
     }
   }
-  release_tiles(p, s, cur, used);
-  group_reduce<2 * NT>(p, s, grp, mem, acc);
-  if (mem != 0) return;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    if (qD[nt] >= 0) {
-      float* dst = f.part + (size_t)qD[nt] * f.d + 16 * un.idx;
-      dst[g] = acc[2 * nt];
-      dst[g + 8] = acc[2 * nt + 1];
-    }
-  }
+  if (!arrive_chunk(s.ctl + 2 * kMaxUS + us)) return;
+  down_reduce(p, s, un, pb);
+  free_slot(s.ctl + 2 * kMaxUS + us, s.ctl + 3 * kMaxUS + us, it.u + p.n_us);
   __threadfence();
   __syncwarp();
   int last = 0;
-  if (lane == 0) last = atomicAdd(&p.rowcnt[un.idx], 1) == s.misc[1] - 1;
+  if (lane == 0) last = atomicAdd(&s.rowcnt[un.idx], 1) == s.misc[4] - 1;
   last = __shfl_sync(0xffffffffu, last, 0);
   if (last) {
-    // this group finished the row tile's last slot: combine its 16 rows
     __threadfence();
-    const int r0 = 16 * un.idx;
-    for (int idx = lane; idx < f.T * 16; idx += 32) {
-      const int t = idx >> 4, r = idx & 15;
-      float a = 0.f;
-      for (int j0 = 0; j0 < f.k; j0 += 4) {  // loads of a group issued together, sums kept in slot order
-        float pv[4];
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu)
-          pv[uu] = (j0 + uu < f.k) ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + uu] * f.d + r0 + r) : 0.f;
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu)
-          if (j0 + uu < f.k) a = fmaf(s.gates[t * f.k + j0 + uu], pv[uu], a);
-      }
-      if (f.S > 0) a += __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
-      if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = a;
-      else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(a);
-    }
+    combine_rows(p, s, un.idx);
   }
 }
 
-__device__ void consumers(const DecParams& p, const Shared& s, volatile int* abort) {
+template <int RG>
+__device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* abort) {
   const FwdParams& f = p.f;
   const int w = threadIdx.x >> 5;
-  const int grp = w / kGroupWarps, mem = w % kGroupWarps;
-  const int nr = s.misc[0], nsl = s.misc[1];
-  const int NUg = nr * (f.F / 16) + (f.S > 0 ? f.S / 16 : 0);
-  const int NUd = nsl * (f.d / 16);
-  const int K64d = k64_tiles(f.d);
-  int b0, b1;
-  unit_range(NUg, b0, b1);
-  const int n_gu_tiles = (b1 - b0) * 2 * K64d;
-  for (int i = grp; i < b1 - b0; i += kGroups) {
-    const Unit un = gu_unit(p, s, b0 + i);
-    const int t0 = i * 2 * K64d;
-    if (un.n <= 8) gateup_unit<1>(p, s, un, t0, grp, mem, abort);
-    else gateup_unit<2>(p, s, un, t0, grp, mem, abort);
+  const Plan pl = make_plan(p, s, w);
+  const uint64_t pol = evict_first_policy();
+  uint8_t* ring = s.ring + (size_t)w * RG * kGroupBytes;
+  Cursor cu;
+  cu.j = 0;
+  cu.nitems = pl.nguw + pl.ndnw;
+  cursor_seek(p, s, pl, w, cu);
+  for (int i = 0; i < RG; ++i) issue_group(p, s, pl, w, cu, ring + i * kGroupBytes, pol);
+  int slot = 0;
+  // C: gate/up items
+  for (int j = 0; j < pl.nguw; ++j) {
+    const Item it = item_of(p, s, pl, w, j);
+    const Unit un = gu_unit(p, s, pl.g0 + it.u);
+    if (un.n <= 8) gateup_item<1, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
+    else gateup_item<2, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
   }
-  int d0, d1;
-  unit_range(NUd, d0, d1);
-  for (int i = grp; i < d1 - d0; i += kGroups) {
-    const Unit un = dn_unit(p, s, d0 + i);
-    const int t0 = dn_tile0(p, s, d0, i, n_gu_tiles);
-    if (un.n <= 4) down_unit<1>(p, s, un, t0, grp, mem, abort);
-    else if (un.n <= 8) down_unit<2>(p, s, un, t0, grp, mem, abort);
-    else if (un.n <= 12) down_unit<3>(p, s, un, t0, grp, mem, abort);
-    else down_unit<4>(p, s, un, t0, grp, mem, abort);
+  // D: down items, one (slot, half) pair at a time; every warp takes part in
+  // every pair's staging barriers, with or without items of that pair
+  const int ud = f.d / 16;
+  int j = pl.nguw;
+  if (pl.ndn > 0) {
+    const int hs_first = pl.d0 / ud, hs_last = (pl.d0 + pl.ndn - 1) / ud;
+    for (int hs = hs_first; hs <= hs_last; ++hs) {
+      named_bar(2, kThreads);  // the shared x / previous h is no longer read
+      const int hslot = s.hs_slot[hs];
+      const int fsl = (s.slot_e[hslot] == f.E) ? f.S : f.F;
+      if ((threadIdx.x & 31) == 0)
+        wait_counter(&s.done[hslot], fsl / 16 + p.test_extra, abort, p.test_extra ? p.test_wait_ns : p.wait_ns,
+                     f.status);
+      __syncwarp();
+      if (!*abort) stage_h(p, s, hs);
+      named_bar(2, kThreads);
+      for (; j < pl.nguw + pl.ndnw; ++j) {
+        const Item it = item_of(p, s, pl, w, j);
+        const Unit un = dn_unit(p, s, pl.d0 + it.u);
+        if ((pl.d0 + it.u) / ud != hs) break;
+        if (un.n <= 4) down_item<1, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
+        else down_item<2, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
+      }
+    }
   }
+  cp_async_wait_all();
 }
 
+template <int RG>
 __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) {
   extern __shared__ __align__(128) uint8_t sm[];
-  const Shared s = carve(sm, p);
+  Shared s = carve(sm, p);
   volatile int* abort = &s.misc[2];
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    for (int i = 0; i < p.ns; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], kStageTiles);
-      s.seq[i] = -1;
+    for (int b = 0; b < kMaxUS; ++b) {
+      s.ctl[b] = 0;               // gate/up arrivals
+      s.ctl[kMaxUS + b] = b;      // gate/up slot b serves unit b first
+      s.ctl[2 * kMaxUS + b] = 0;  // down arrivals
+      s.ctl[3 * kMaxUS + b] = b;
     }
-
-    fence_mbar_init();
     *abort = 0;
   }
   for (int e = tid; e < p.f.E; e += kThreads) s.cnt[e] = 0;
+  const RouterPrefetch pre = router_prefetch(p);
   pdl_wait();  // inputs and workspace are the preceding grid's until here
   if (tid == 0) {
     // launch sequence number: this CTA's word only ever grows, one step per launch,
@@ -944,22 +1071,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
     p.bar_flags[blockIdx.x] = seq;
     s.misc[3] = (int)seq;
   }
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= p.f.E; i += kThreads) p.done[i] = 0;
-    for (int i = tid; i < p.f.d / 16; i += kThreads) p.rowcnt[i] = 0;
-  }
   __syncthreads();
   const unsigned seq = (unsigned)s.misc[3];
-  if (warp < kRouterWarps) router(p, s, seq);
+  // This launch counts in half seq & 1 of the counters (zeroed by the previous
+  // launch, or at creation) and zeroes the other half for the next launch.
+  if (blockIdx.x == 0) {
+    int* dn = p.done + (size_t)((seq + 1) & 1) * (p.f.E + 1);
+    int* rc = p.rowcnt + (size_t)((seq + 1) & 1) * (p.f.d / 16);
+    for (int i = tid; i <= p.f.E; i += kThreads) dn[i] = 0;
+    for (int i = tid; i < p.f.d / 16; i += kThreads) rc[i] = 0;
+  }
+  s.done = p.done + (size_t)(seq & 1) * (p.f.E + 1);
+  s.rowcnt = p.rowcnt + (size_t)(seq & 1) * (p.f.d / 16);
+  if (warp < kRouterWarps) router(p, s, seq, pre);
   else scale_x(p, s, kRouterWarps, kWarps - kRouterWarps);
   __syncthreads();
   routing(p, s, seq, abort);
   pdl_launch_dependents();
-  if (warp == kProd) {
-    if ((tid & 31) == 0) producer(p, s, abort);
-  } else {
-    consumers(p, s, abort);
-  }
+  stream_layer<RG>(p, s, abort);
 }
 
 }  // namespace
@@ -968,37 +1097,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
 bool decode_plan(DecParams& p, int max_smem) {
   const FwdParams& f = p.f;
   if (f.E > 512 || f.k * kDecodeMaxT > 512) return false;
-  p.stage_bytes = kStageBytes;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
-  const int Pm = kDecodeMaxT * f.k;
-  size_t off = 0;
-  const size_t bars_max = 32 + (2 * 8 + 4) * 128;  // 4 unit barriers; up to 128 stages: two mbarriers and a stamp each
-  off = bars_max;
+  const int Pm = kDecodeMaxT * f.k, hh = std::min(kHalf, p.tcap);
+  p.xstride = f.d64 + 8;      // f16 row strides padded by 16 bytes: rows of a fragment load
+  p.hstride = f.fmax64 + 8;   // fall in different banks
+  size_t off = 4 * kMaxUS * 4;
+  off = up(off, 128);
   p.off_x16 = (int)off;
-  off = up(off + (size_t)p.tcap * f.d64 * 2, 16);
+  const size_t xbytes = (size_t)p.tcap * p.xstride * 2;
+  const size_t hbytes = (size_t)hh * 2 * p.hstride * 2;
+  p.off_hsc = (int)up(off + hbytes, 16);
+  const size_t union_end = std::max(off + xbytes, (size_t)p.off_hsc + (size_t)hh * f.hgroups * 4);
+  off = up(union_end, 16);
   p.off_xinv = (int)off;
   off = up(off + kDecodeMaxT * 4, 16);
-  p.off_pbuf = (int)off;
-  p.pfloats = p.tcap <= 8 ? 8 : 16;  // gate/up partials: 8 per n8 token tile (NT = 2 above 8 tokens)
-  p.pbuf_depth = 1;
-  off = up(off + (size_t)kRouterWarps * kDecodeMaxT * sizeof(dd) + (size_t)kGroups * 2 * p.pfloats * 32 * 4, 16);
-  p.off_route = (int)off;
-  off = up(off + (size_t)(4 * Pm + 5 * (f.E + 1) + 8) * 4, 128);
-  (void)Pm;
-  p.off_ring = (int)off;
-  const long long room = (long long)max_smem - (long long)off;
-  int ns = (int)(room / p.stage_bytes);
-  if (ns > 128) ns = 128;
-  if (ns < 4) return false;
-  p.ns = ns;
-  p.smem_bytes = (int)(off + (size_t)ns * p.stage_bytes);
-  return true;
+  p.off_red = (int)off;
+  off = up(off + (size_t)kRouterWarps * kDecodeMaxT * sizeof(dd), 16);
+  const size_t route_bytes = (size_t)(4 * Pm + 5 * (f.E + 1) + 2 * (f.E + 1 + 64) + 8) * 4;
+  // ring of 8 slots per warp (139 KB in flight per SM) when it fits, else 4
+  const int tries[5][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 4}, {4, 4}, {2, 4}};
+  for (const auto& tr : tries) {
+    const int n_us = tr[0], rg_want = tr[1];
+    size_t o = off;
+    p.n_us = n_us;
+    p.off_pgu = (int)o;
+    o = up(o + (size_t)n_us * kChunks * 32 * p.tcap * 4, 16);
+    p.off_pdn = (int)o;
+    o = up(o + (size_t)n_us * kChunks * 16 * hh * 4, 16);
+    p.off_route = (int)o;
+    o = up(o + route_bytes, 128);
+    p.off_ring = (int)o;
+    const long long room = (long long)max_smem - (long long)o;
+    const int rg = (int)(room / ((long long)kWarps * kGroupBytes));
+    if (rg >= rg_want) {
+      p.ring_groups = rg_want;
+      p.smem_bytes = (int)(o + (size_t)kWarps * rg_want * kGroupBytes);
+      // one CTA per SM: more than half of the shared memory keeps a second CTA out
+      if (p.smem_bytes <= max_smem / 2) p.smem_bytes = max_smem / 2 + 128;
+      return true;
+    }
+  }
+  return false;
 }
 
 cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem) {
   static int configured = 0;
   if (configured < max_smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     configured = max_smem;
   }
@@ -1009,14 +1156,15 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
   cfg.stream = stream;
   // Programmatic dependent launch: the kernel may be scheduled while the
   // preceding kernel drains; it waits (griddepcontrol.wait) before touching
-  // any global memory. Co-residency of the grid holds by construction (one
-  // CTA per SM, more than half an SM's shared memory each).
+  // any global memory written by it. Co-residency of the grid holds by
+  // construction (one CTA per SM, more than half an SM's shared memory each).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel, p);
+  if (p.ring_groups == 8) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, p);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<4>, p);
 }
 
 }  // namespace moe

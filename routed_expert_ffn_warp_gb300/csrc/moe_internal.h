@@ -90,14 +90,15 @@ struct FwdParams {
 constexpr int kDecodeMaxT = 16;
 struct DecParams {
   FwdParams f;
-  int* done;            // [E+1] finished gate/up units per slot
-  int* rowcnt;          // [d/16] finished down units per row tile
+  int* done;            // [2][E+1] finished gate/up units per slot (half = launch sequence & 1)
+  int* rowcnt;          // [2][d/16] finished down units per row tile
   unsigned* bar_flags;  // [grid] per-CTA launch sequence numbers (each only grows)
   unsigned long long* lwords;  // [tcap][E][2] published logits: (fp32 bits << 32) | sequence
   int tcap;             // tokens the x16 shared area holds (min(t_max, kDecodeMaxT))
-  int ns, stage_bytes;  // ring stages and bytes per stage
-  int pfloats, pbuf_depth;  // per-unit partial floats per lane and partial buffers
-  int off_x16, off_xinv, off_pbuf, off_route, off_ring, smem_bytes;
+  int ring_groups;      // 1,088-byte slots of each warp's weight ring
+  int n_us;             // partial-sum unit slots per phase
+  int xstride, hstride; // f16 row strides of the shared x and h
+  int off_x16, off_hsc, off_xinv, off_red, off_pgu, off_pdn, off_route, off_ring, smem_bytes;
   long long wait_ns;       // bound of every device-side wait
   int test_extra;          // > 0: one wait targets an unreachable count (timeout test)
   long long test_wait_ns;  // bound of that wait
