@@ -341,7 +341,8 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
     for (int i = 0; i < NPL; ++i) {
       if ((need >> i) & 1u) {
         const int e = lane + 32 * i;
-        const unsigned long long a = ld_relaxed_u64(wt + 2 * e), b = ld_relaxed_u64(wt + 2 * e + 1);
+        unsigned long long a, b;
+        ld_relaxed_u64x2(wt + 2 * e, a, b);
         vh[i] = __uint_as_float((unsigned)(a >> 32));
         vl[i] = __uint_as_float((unsigned)(b >> 32));
         if ((unsigned)a == seq && (unsigned)b == seq) need &= ~(1u << i);
@@ -378,8 +379,14 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
       }
     }
     const unsigned mh = __reduce_max_sync(0xffffffffu, bh);
-    const unsigned ml = __reduce_max_sync(0xffffffffu, bh == mh ? bl : 0u);
-    const int mi = (int)__reduce_min_sync(0xffffffffu, (bh == mh && bl == ml) ? (unsigned)bi : 0x7fffffffu);
+    const unsigned tie = __ballot_sync(0xffffffffu, bh == mh);
+    int mi;
+    if (__popc(tie) == 1) {  // one lane holds the largest hi part: it wins
+      mi = __shfl_sync(0xffffffffu, bi, __ffs(tie) - 1);
+    } else {  // equal hi parts: the lo part decides, then the lower index
+      const unsigned ml = __reduce_max_sync(0xffffffffu, bh == mh ? bl : 0u);
+      mi = (int)__reduce_min_sync(0xffffffffu, (bh == mh && bl == ml) ? (unsigned)bi : 0x7fffffffu);
+    }
     const int owner = mi & 31;
     if (owner == lane) taken |= 1u << (mi >> 5);
     const float wh = __shfl_sync(0xffffffffu, fh, owner), wl = __shfl_sync(0xffffffffu, fl, owner);
@@ -404,19 +411,24 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
   }
 }
 
-// Counting sort of P <= 32 pairs by expert with one warp: a bitonic sort of
-// the keys (expert << 8 | pair) leaves the pairs stably ordered by expert.
+// Counting sort of P <= 32 pairs by expert with one warp: pair q's position
+// is the number of pairs with a smaller expert, or the same expert and a
+// smaller pair index (a stable sort), counted over all pairs at once.
 __device__ void bucket_small(const DecParams& p, const Shared& s) {
   const FwdParams& f = p.f;
   const int lane = threadIdx.x & 31;
   const int P = f.P, E = f.E, T = f.T;
-  unsigned key = lane < P ? ((unsigned)s.ids[lane] << 8) | (unsigned)lane : 0xffffffffu;
-  for (int kk = 2; kk <= 32; kk <<= 1)
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      const unsigned other = __shfl_xor_sync(0xffffffffu, key, jj);
-      const bool up = (lane & kk) == 0, lower = (lane & jj) == 0;
-      key = (lower == up) ? min(key, other) : max(key, other);
-    }
+  const int my_e = lane < P ? s.ids[lane] : 0x7fffffff;
+  int rank = 0;
+  for (int j = 0; j < P; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    rank += (ej < my_e) || (ej == my_e && j < lane);
+  }
+  if (lane < P) s.perm[rank] = lane;
+  __syncwarp();
+  const int qs = lane < P ? s.perm[lane] : 0;
+  const unsigned key = lane < P ? ((unsigned)s.ids[qs] << 8) | (unsigned)qs : 0xffffffffu;
+  __syncwarp();
   const int e = (int)(key >> 8), q = (int)(key & 0xffu);
   const int eprev = __shfl_up_sync(0xffffffffu, e, 1);
   const bool first = lane < P && (lane == 0 || e != eprev);
@@ -601,9 +613,14 @@ __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volat
 // past the end of the stream keep the count uniform).
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t pol) {
+#ifndef MOE_NO_L2_HINT
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "l"(pol)
                : "memory");
+#else
+  (void)pol;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+#endif
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -1099,8 +1116,11 @@ bool decode_plan(DecParams& p, int max_smem) {
   if (f.E > 512 || f.k * kDecodeMaxT > 512) return false;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
   const int Pm = kDecodeMaxT * f.k, hh = std::min(kHalf, p.tcap);
-  p.xstride = f.d64 + 8;      // f16 row strides padded by 16 bytes: rows of a fragment load
-  p.hstride = f.fmax64 + 8;   // fall in different banks
+  // f16 row strides 64 bytes past a multiple of 128 (d64, fmax64 are multiples
+  // of 64 elements): the 8 rows x 4 16-byte columns of a fragment load hit
+  // distinct banks
+  p.xstride = f.d64 + 32;
+  p.hstride = f.fmax64 + 32;
   size_t off = 4 * kMaxUS * 4;
   off = up(off, 128);
   p.off_x16 = (int)off;
@@ -1114,8 +1134,8 @@ bool decode_plan(DecParams& p, int max_smem) {
   p.off_red = (int)off;
   off = up(off + (size_t)kRouterWarps * kDecodeMaxT * sizeof(dd), 16);
   const size_t route_bytes = (size_t)(4 * Pm + 5 * (f.E + 1) + 2 * (f.E + 1 + 64) + 8) * 4;
-  // ring of 8 slots per warp (139 KB in flight per SM) when it fits, else 4
-  const int tries[5][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 4}, {4, 4}, {2, 4}};
+  // the deepest weight ring per warp that fits: 8, 6 or 4 slots
+  const int tries[7][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 6}, {4, 6}, {kMaxUS, 4}, {4, 4}, {2, 4}};
   for (const auto& tr : tries) {
     const int n_us = tr[0], rg_want = tr[1];
     size_t o = off;
@@ -1145,6 +1165,8 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
   if (configured < max_smem) {
     cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_layer_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
     configured = max_smem;
@@ -1164,6 +1186,7 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.ring_groups == 8) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, p);
+  if (p.ring_groups == 6) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<6>, p);
   return cudaLaunchKernelEx(&cfg, decode_layer_kernel<4>, p);
 }
 

@@ -106,6 +106,14 @@ struct DecParams {
 bool decode_plan(DecParams& p, int max_smem);
 cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem);
 
+// Expert GEMMs of the general path (moe_gemm.cu). Work units: (slot, group of
+// kGemmTiles 16-row weight tiles, block of up to kGemmRows rows of the slot);
+// gu_prefix / dn_prefix hold the running unit counts per slot.
+constexpr int kGemmRows = 48;
+constexpr int kGemmTiles = 12;
+cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_gemm_down(const FwdParams& p, cudaStream_t stream, int num_sms);
+
 // Launchers (moe_kernels.cu). All are asynchronous on `stream`.
 // `events` (may be null) receives kForwardPhases + 1 cudaEvent_t to record at
 // the phase boundaries.

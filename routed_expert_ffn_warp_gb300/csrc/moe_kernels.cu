@@ -5,8 +5,8 @@
 //   router   l[t,e] = W_r[e] . x_t + b[e] as a double-float (hi + lo) sum
 //   topk     warp top-k with lower-index tie break, softmax gates over the k
 //   bucket   counting sort of the T*k pairs by expert, and the work list
-//   gateup   grouped MXFP4 dequant-GEMV on tensor cores: h = SiLU(gate) * up
-//   down     grouped MXFP4 dequant-GEMV: part = W_down h
+//   gateup   grouped MXFP4 GEMM on tensor cores: h = SiLU(gate) * up (moe_gemm.cu)
+//   down     grouped MXFP4 GEMM: part = W_down h (moe_gemm.cu)
 //   combine  y_t = sum_j g[t,j] part(t,j) + shared_t, slot order, one rounding
 //
 // Where the pages describe the step (page title, section):
@@ -35,9 +35,6 @@ namespace {
 
 using namespace dev;
 
-constexpr int kNW = 8;  // warps per CTA of the expert kernels
-constexpr int kGuNT = 2;  // n8 token tiles per gate/up pass (16 tokens)
-constexpr int kDnNT = 4;  // n8 tiles per down pass (16 pairs: hi and lo columns)
 
 // ---------------------------------------------------------------- prep_x
 
@@ -236,8 +233,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.slot_n[ns] = cnt[e];
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
-      gu += p.F / 16;
-      dn += p.d / 16;
+      const int blocks = (cnt[e] + kGemmRows - 1) / kGemmRows;
+      gu += blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
+      dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
     if (p.S > 0 && T > 0) {
@@ -246,8 +244,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.slot_n[ns] = T;
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
-      gu += p.S / 16;
-      dn += p.d / 16;
+      const int blocks = (T + kGemmRows - 1) / kGemmRows;
+      gu += blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
+      dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
     p.gu_prefix[ns] = gu;
@@ -256,194 +255,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   }
 }
 
-// ---------------------------------------------------------------- expert kernels
-
-__device__ __forceinline__ int find_slot(const int32_t* prefix, int n, int unit) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= unit) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ int token_of_row(const FwdParams& p, int q) { return q < p.P ? p.perm[q] / p.k : q - p.P; }
-
-template <int NT>
-__global__ void __launch_bounds__(kNW * 32) gateup_kernel(FwdParams p) {
-  __shared__ float red[kNW][2 * NT * 4][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int nslots = *p.n_slots;
-  const int total = p.gu_prefix[nslots];
-  const int K64 = k64_tiles(p.d);
-  for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
-    const int s = find_slot(p.gu_prefix, nslots, unit);
-    const int tau = unit - p.gu_prefix[s];
-    const int e = p.slot_expert[s], q0 = p.slot_q0[s], n = p.slot_n[s];
-    const uint8_t* wb = p.packed + (size_t)e * p.expert_stride + (size_t)tau * K64 * 2 * kTileBytes;
-    for (int m0 = 0; m0 < n; m0 += 8 * NT) {
-      int tokB[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = m0 + 8 * nt + g;
-        tokB[nt] = (m < n) ? token_of_row(p, q0 + m) : -1;
-      }
-      float accg[NT][4], accu[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) accg[nt][r] = accu[nt][r] = 0.f;
-      for (int kt = warp; kt < K64; kt += kNW) {
-        const uint8_t* tg = wb + (size_t)kt * 2 * kTileBytes;
-        const uint8_t* tu = tg + kTileBytes;
-        const uint4 qg = ld16(tg + 16 * lane);
-        const uint32_t sg = ld4(tg + kTileCodeBytes + 4 * g);
-        const uint4 qu = ld16(tu + 16 * lane);
-        const uint32_t su = ld4(tu + kTileCodeBytes + 4 * g);
-        uint4 bx[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int bb = 0; bb < 2; ++bb)
-            bx[nt][bb] = tokB[nt] >= 0 ? ld16(p.x16 + (size_t)tokB[nt] * p.d64 + kt * 64 + bb * 32 + c * 8)
-                                       : make_uint4(0, 0, 0, 0);
-        gu_tile<NT>(qg, sg, bx, accg);
-        gu_tile<NT>(qu, su, bx, accu);
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          red[warp][nt * 4 + r][lane] = accg[nt][r];
-          red[warp][NT * 4 + nt * 4 + r][lane] = accu[nt][r];
-        }
-      __syncthreads();
-      if (warp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float hv[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < kNW; ++w) {
-              gs += red[w][nt * 4 + r][lane];
-              us += red[w][NT * 4 + nt * 4 + r][lane];
-            }
-            const int m = m0 + 8 * nt + 2 * c + (r & 1);
-            float h = 0.f;
-            if (m < n) {
-              const float xi = p.xinv[token_of_row(p, q0 + m)];
-              const float gate = gs * xi, up = us * xi;
-              h = gate / (1.f + expf(-gate)) * up;
-            }
-            hv[r] = h;
-          }
-          // power-of-two scale per (row q, 16-element group tau): max over rows g, g+8, all g
-          float m0v = fmaxf(fabsf(hv[0]), fabsf(hv[2]));  // column 2c
-          float m1v = fmaxf(fabsf(hv[1]), fabsf(hv[3]));  // column 2c+1
-          for (int o = 4; o < 32; o <<= 1) {
-            m0v = fmaxf(m0v, __shfl_xor_sync(0xffffffffu, m0v, o));
-            m1v = fmaxf(m1v, __shfl_xor_sync(0xffffffffu, m1v, o));
-          }
-#pragma unroll
-          for (int col = 0; col < 2; ++col) {
-            const int m = m0 + 8 * nt + 2 * c + col;
-            if (m >= n) continue;
-            const int q = q0 + m;
-            const int sh = f16_headroom_exponent(col ? m1v : m0v);
-            const float sc = pow2f(sh);
-            __half* hi = reinterpret_cast<__half*>(p.hbuf) + (size_t)q * 2 * p.fmax64;
-            __half* lo = hi + p.fmax64;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const int rr = g + 8 * half;
-              const int i = 32 * (tau >> 1) + 8 * (rr >> 2) + 4 * (tau & 1) + (rr & 3);
-              const float v = hv[2 * half + col] * sc;
-              const __half vh = __float2half_rn(v);
-              hi[i] = vh;
-              lo[i] = __float2half_rn(v - __half2float(vh));
-            }
-            if (g == 0) p.hscale[(size_t)q * p.hgroups + tau] = pow2f(-sh);
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-template <int NT>
-__global__ void __launch_bounds__(kNW * 32) down_kernel(FwdParams p) {
-  __shared__ float red[kNW][2 * NT][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int nslots = *p.n_slots;
-  const int total = p.dn_prefix[nslots];
-  for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
-    const int s = find_slot(p.dn_prefix, nslots, unit);
-    const int rho = unit - p.dn_prefix[s];
-    const int e = p.slot_expert[s], q0 = p.slot_q0[s], n = p.slot_n[s];
-    const int f = (e == p.E) ? p.S : p.F;
-    const int K64 = k64_tiles(f);
-    const uint8_t* wb =
-        p.packed + (size_t)e * p.expert_stride + gu_packed_bytes(p.d, f) + (size_t)rho * K64 * kTileBytes;
-    for (int m0 = 0; m0 < n; m0 += 4 * NT) {
-      int qB[NT], qD[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int mb = m0 + 4 * nt + (g >> 1);
-        qB[nt] = (mb < n) ? q0 + mb : -1;
-        const int md = m0 + 4 * nt + c;
-        qD[nt] = (md < n) ? q0 + md : -1;
-      }
-      float acc[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
-      for (int kt = warp; kt < K64; kt += kNW) {
-        const uint8_t* tile = wb + (size_t)kt * kTileBytes;
-        const uint4 q = ld16(tile + 16 * lane);
-        const uint32_t sc = ld4(tile + kTileCodeBytes + 4 * g);
-        uint4 bh[NT][2];
-        float2 sb[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            bh[nt][bb] = qB[nt] >= 0 ? ld16(p.hbuf + ((size_t)qB[nt] * 2 + (g & 1)) * p.fmax64 + kt * 64 + bb * 32 + c * 8)
-                                     : make_uint4(0, 0, 0, 0);
-            sb[nt][bb] = qD[nt] >= 0 ? __ldg(reinterpret_cast<const float2*>(p.hscale + (size_t)qD[nt] * p.hgroups +
-                                                                              2 * (2 * kt + bb)))
-                                     : make_float2(0.f, 0.f);
-          }
-        dn_tile<NT>(q, sc, bh, sb, acc);
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        red[warp][2 * nt][lane] = acc[nt][0];
-        red[warp][2 * nt + 1][lane] = acc[nt][1];
-      }
-      __syncthreads();
-      if (warp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float r0 = 0.f, r1 = 0.f;
-          for (int w = 0; w < kNW; ++w) {
-            r0 += red[w][2 * nt][lane];
-            r1 += red[w][2 * nt + 1][lane];
-          }
-          if (qD[nt] >= 0) {
-            float* dst = p.part + (size_t)qD[nt] * p.d + 16 * rho;
-            dst[g] = r0;
-            dst[g + 8] = r1;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
+// ---------------------------------------------------------------- combine
 
 __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
   const int t = blockIdx.y;
@@ -536,9 +348,11 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   if (events) cudaEventRecord(events[1], stream);
-  gateup_kernel<kGuNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  cudaError_t e = launch_gemm_gateup(p, stream, num_sms);
+  if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[2], stream);
-  down_kernel<kDnNT><<<2 * num_sms, kNW * 32, 0, stream>>>(p);
+  e = launch_gemm_down(p, stream, num_sms);
+  if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[3], stream);
   combine_kernel<<<dim3((p.d + 255) / 256, p.T), 256, 0, stream>>>(p);
   if (events) cudaEventRecord(events[4], stream);
