@@ -71,8 +71,12 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *   nothing reaches and gives up after 2 ms, so the forward completes with
  *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
  * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path that
- *   otherwise serves T > 16 (for testing both paths on the same shapes). */
-enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u };
+ *   otherwise serves T > 16 (for testing both paths on the same shapes).
+ * MOE_FLAG_TC_GATEUP makes the multi-kernel path run gate/up + SwiGLU as a
+ *   block-scaled tcgen05 MMA (MXFP4 weights x two MXFP8 planes of x) instead
+ *   of the register-decode tensor-core GEMM; same results within the bf16 and
+ *   fp32 tolerances (experimental: currently slower). */
+enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u };
 
 typedef struct moe_config {
   int d;          /* hidden size; a multiple of 32 */

@@ -84,7 +84,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (c.d <= 0 || c.d % 32 || c.ffn <= 0 || c.ffn % 32 || c.shared_ffn < 0 || c.shared_ffn % 32 ||
       c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
       c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) ||
-      (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH)))
+      (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH | MOE_FLAG_TC_GATEUP)))
     return fail(nullptr, MOE_ERR_INVALID_ARG,
                 "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
                 "0 <= t_max <= 65536; out_dtype 0/1; flags 0)");
@@ -118,6 +118,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return o;
   };
   const size_t o_x16 = take((size_t)Tm * d64 * 2), o_xinv = take((size_t)Tm * 4);
+  const int xq_spitch = (d64 / 32 + 3) / 4 * 4;
+  const size_t o_xq = take((size_t)Tm * 2 * d64), o_xqs = take((size_t)Tm * 2 * xq_spitch);
   const size_t o_lh = take((size_t)Tm * E * 4), o_ll = take((size_t)Tm * E * 4);
   const size_t o_ids = take(Pm * 4), o_gates = take(Pm * 4), o_counts = take((size_t)E * 4),
                o_offsets = take((size_t)(E + 1) * 4), o_perm = take(Pm * 4), o_inv = take(Pm * 4);
@@ -155,12 +157,16 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.fmax64 = fmax64;
   p.hgroups = hgroups;
   p.out_f32 = c.out_dtype == MOE_OUT_F32;
+  p.tc_gateup = (c.flags & MOE_FLAG_TC_GATEUP) ? 1 : 0;
   p.w_router = ctx->w_router;
   p.bias = nullptr;
   p.packed = ctx->packed;
   p.expert_stride = ctx->expert_stride;
   p.x16 = reinterpret_cast<uint16_t*>(w + o_x16);
   p.xinv = reinterpret_cast<float*>(w + o_xinv);
+  p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
+  p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
+  p.xq_spitch = xq_spitch;
   p.logit_hi = reinterpret_cast<float*>(w + o_lh);
   p.logit_lo = reinterpret_cast<float*>(w + o_ll);
   p.ids = reinterpret_cast<int32_t*>(w + o_ids);

@@ -64,6 +64,10 @@ struct FwdParams {
   // workspace
   uint16_t* x16;         // f16 [t_max][d64], x * 2^sigma_t
   float* xinv;           // [t_max]: 2^-sigma_t
+  int tc_gateup;         // gate/up on the tcgen05 block-scaled GEMM (moe_tcgemm.cu)
+  uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
+  uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
+  int xq_spitch;         // scale bytes per plane row (a multiple of 4)
   float* logit_hi;       // [t_max][E]
   float* logit_lo;
   int32_t* ids;          // [t_max][k]
@@ -111,8 +115,13 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
 // gu_prefix / dn_prefix hold the running unit counts per slot.
 constexpr int kGemmRows = 48;
 constexpr int kGemmTiles = 12;
-cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
 cudaError_t launch_gemm_down(const FwdParams& p, cudaStream_t stream, int num_sms);
+// Gate/up of the general path on tcgen05 block-scaled MMAs (moe_tcgemm.cu):
+// units (slot, 4 pair tiles, block of up to kTcGemmRows tokens); gu_prefix
+// holds their running counts per slot.
+constexpr int kTcGemmRows = 48;
+cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
 
 // Launchers (moe_kernels.cu). All are asynchronous on `stream`.
 // `events` (may be null) receives kForwardPhases + 1 cudaEvent_t to record at

@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
       const int blocks = (cnt[e] + kGemmRows - 1) / kGemmRows;
-      gu += blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
+      gu += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * ((p.F / 16 + 3) / 4)
+                        : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
       dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
@@ -245,7 +246,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
       const int blocks = (T + kGemmRows - 1) / kGemmRows;
-      gu += blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
+      gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * ((p.S / 16 + 3) / 4)
+                        : blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
       dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
@@ -348,7 +350,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   if (events) cudaEventRecord(events[1], stream);
-  cudaError_t e = launch_gemm_gateup(p, stream, num_sms);
+  cudaError_t e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[2], stream);
   e = launch_gemm_down(p, stream, num_sms);

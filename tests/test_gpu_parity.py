@@ -57,11 +57,12 @@ SMALL_SHAPES = [
 
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 @pytest.mark.parametrize("out_f32", [False, True])
-@pytest.mark.parametrize("path", ["fused", "general"])
+@pytest.mark.parametrize("path", ["fused", "general", "general-tc"])
 def test_small_shapes(m, shape, out_f32, path):
     T, d, F, E, k, S, z = shape
     wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
-    flags = m.MOE_FLAG_GENERAL_PATH if path == "general" else 0
+    flags = {"fused": 0, "general": m.MOE_FLAG_GENERAL_PATH,
+             "general-tc": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_TC_GATEUP}[path]
     _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32, flags=flags)
 
 
@@ -215,6 +216,12 @@ def test_full_size_workloads(m, name, layer_idx, tokens):
     wl = synth.WORKLOADS[name]
     L = synth.gen_layer(wl, layer_idx)
     _parity(m, wl, L, tokens=tokens)
+
+
+def test_tc_gateup_prefill_sampled(m):
+    """The tcgen05 block-scaled gate/up on the full prefill chunk (sampled tokens)."""
+    wl = synth.WORKLOADS["prefill"]
+    _parity(m, wl, synth.gen_layer(wl, 2), tokens=[3, 700], flags=m.MOE_FLAG_TC_GATEUP)
 
 
 @pytest.mark.parametrize("name", ["decode", "verify", "small"])
