@@ -198,7 +198,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   dp.wait_ns = 50000000LL;  // 50 ms: orders of magnitude above a layer's runtime
   dp.test_extra = (c.flags & MOE_FLAG_TEST_FORCE_TIMEOUT) ? 1 : 0;
   dp.test_wait_ns = 2000000LL;  // 2 ms
-  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem);
+  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms);
   *out = ctx;
   return MOE_OK;
 }

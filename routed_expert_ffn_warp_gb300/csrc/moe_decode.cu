@@ -1,9 +1,10 @@
 // Fused decode path: the whole MoE layer for T <= 16 tokens in ONE persistent
 // kernel, one CTA per SM, 16 warps.
 //
-//   A  CTA b computes the double-float router logits of experts b, b+G, ...
-//      and publishes each as two 64-bit words (value bits | launch sequence
-//      number); meanwhile 4 warps scale x into f16 in shared memory.
+//   A  x is staged in shared memory; CTA b computes the double-float router
+//      logits of experts b, b+G, ... from it and publishes each as two 64-bit
+//      words (value bits | launch sequence number); x is then scaled to f16 in
+//      place.
 //   B  token warps poll the published words of all experts (a dataflow
 //      barrier: no grid-wide sync, no atomics), then every CTA redundantly runs
 //      top-k + softmax gates, the counting sort of the T*k pairs and the slot
@@ -52,7 +53,6 @@ using namespace dev;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = 16;
-constexpr int kRouterWarps = 12;   // warps 0..11 compute logits, 12..15 scale x
 constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
 constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
 constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
@@ -196,95 +196,102 @@ __device__ __forceinline__ void chunk_range(int K64, int c, int& k0, int& k1) {
   k1 = min(K64, k0 + ck);
 }
 
-// ---------------------------------------------------------------- phase A: router + x scaling
+// ---------------------------------------------------------------- phase A: x, router, x scaling
 
 // Published logit word: (fp32 bits << 32) | launch sequence number.
 __device__ __forceinline__ unsigned long long pack_logit(float v, unsigned seq) {
   return ((unsigned long long)__float_as_uint(v) << 32) | seq;
 }
 
-// The first 8 router weights of the thread (expert blockIdx.x, elements
-// 8 tid .. 8 tid + 7) are loaded before the kernel waits for the preceding
-// grid: the router weights are constant inputs of the layer.
-struct RouterPrefetch {
-  float4 w0, w1;
-};
-
-__device__ __forceinline__ RouterPrefetch router_prefetch(const DecParams& p) {
-  RouterPrefetch r;
-  const int tid = threadIdx.x;
-  if (tid < kRouterWarps * 32 && (int)blockIdx.x < p.f.E && tid < p.f.d / 8) {
-    const float4* wr = reinterpret_cast<const float4*>(p.f.w_router + (size_t)blockIdx.x * p.f.d);
-    r.w0 = __ldg(wr + 2 * tid);
-    r.w1 = __ldg(wr + 2 * tid + 1);
-  }
-  return r;
+// The router rows of this CTA's experts (blockIdx.x, + G, ...) are copied into
+// shared memory (the weight ring, idle until phase C) before the kernel waits
+// for the preceding grid: the router weights are constant inputs of the layer.
+__device__ void stage_router(const DecParams& p, const Shared& s) {
+  const int d4 = p.f.d / 4;
+  float* wsm = reinterpret_cast<float*>(s.ring);
+  int r = 0;
+  for (int e = blockIdx.x; e < p.f.E; e += gridDim.x, ++r)
+    for (int o = threadIdx.x; o < d4; o += kThreads)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(wsm + (size_t)r * p.f.d + 4 * o)),
+                   "l"(p.f.w_router + (size_t)e * p.f.d + 4 * o)
+                   : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-__device__ void router(const DecParams& p, const Shared& s, unsigned seq, const RouterPrefetch& pre) {
+// x rows (bf16, as stored) into the shared x area with cp.async; all threads.
+// The wait also covers the router rows staged before.
+__device__ void stage_x(const DecParams& p, const Shared& s) {
+  const int d8 = p.f.d / 8;
+  for (int o = threadIdx.x; o < p.f.T * d8; o += kThreads) {
+    const int t = o / d8, i = o - t * d8;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(s.x16 + (size_t)t * p.xstride + 8 * i)),
+                 "l"(p.f.x + (size_t)t * p.f.d + 8 * i)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Router logits from the staged weights and bf16 x. Token t is taken by the
+// wpt = 16 / T warps [t wpt, (t+1) wpt), each over an interleaved share of d;
+// every lane keeps a double-float sum, then a fixed warp tree and a fixed
+// tree over the token's warps.
+__device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
   const FwdParams& f = p.f;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int d8 = f.d / 8, T = f.T;
-  for (int e = blockIdx.x; e < f.E; e += gridDim.x) {
-    dd acc[kDecodeMaxT];
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = dd{0.f, 0.f};
-    const float* wr = f.w_router + (size_t)e * f.d;
-    for (int o = tid; o < d8; o += kRouterWarps * 32) {
-      const bool first = e == (int)blockIdx.x && o == tid;
-      const float4 w0 = first ? pre.w0 : __ldg(reinterpret_cast<const float4*>(wr) + 2 * o);
-      const float4 w1 = first ? pre.w1 : __ldg(reinterpret_cast<const float4*>(wr) + 2 * o + 1);
-      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int t = 0; t < kDecodeMaxT; ++t) {
-        if (t < T) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(f.x + (size_t)t * f.d) + o);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            dd_mac(acc[t], __uint_as_float(xw[j] << 16), wv[2 * j]);
-            dd_mac(acc[t], __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
-          }
-        }
+  const int wpt = max(1, kWarps / T), t = warp / wpt, q = warp - t * wpt;
+  const float* wsm = reinterpret_cast<const float*>(s.ring);
+  int r = 0;
+  for (int e = blockIdx.x; e < f.E; e += gridDim.x, ++r) {
+    const float* wr = wsm + (size_t)r * f.d;
+    if (t < T) {
+      dd acc = dd{0.f, 0.f};
+      for (int o = q * 32 + lane; o < d8; o += 32 * wpt) {
+        const float4 w0 = *reinterpret_cast<const float4*>(wr + 8 * o);
+        const float4 w1 = *reinterpret_cast<const float4*>(wr + 8 * o + 4);
+        const uint4 xv = *reinterpret_cast<const uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o);
+        dd_mac(acc, __uint_as_float(xv.x << 16), w0.x);
+        dd_mac(acc, __uint_as_float(xv.x & 0xFFFF0000u), w0.y);
+        dd_mac(acc, __uint_as_float(xv.y << 16), w0.z);
+        dd_mac(acc, __uint_as_float(xv.y & 0xFFFF0000u), w0.w);
+        dd_mac(acc, __uint_as_float(xv.z << 16), w1.x);
+        dd_mac(acc, __uint_as_float(xv.z & 0xFFFF0000u), w1.y);
+        dd_mac(acc, __uint_as_float(xv.w << 16), w1.z);
+        dd_mac(acc, __uint_as_float(xv.w & 0xFFFF0000u), w1.w);
       }
+      for (int o = 16; o; o >>= 1) acc = dd_add(acc, dd_shfl_xor(acc, o));
+      if (lane == 0) s.red[warp] = acc;
     }
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxT; ++t) {
-      if (t < T) {
-        dd v = acc[t];
-        for (int o = 16; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
-        if (lane == 0) s.red[warp * kDecodeMaxT + t] = v;
-      }
-    }
-    named_bar(1, kRouterWarps * 32);
-    // warp t adds token t's 12 warp partials in a fixed tree, then publishes
-    for (int t = warp; t < T; t += kRouterWarps) {
-      dd v = lane < kRouterWarps ? s.red[lane * kDecodeMaxT + t] : dd{0.f, 0.f};
+    __syncthreads();
+    // warp t adds token t's wpt warp partials in a fixed tree, then publishes
+    if (warp < T) {
+      dd v = lane < wpt ? s.red[warp * wpt + lane] : dd{0.f, 0.f};
       for (int o = 8; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
       if (lane == 0) {
         if (f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
-        f.logit_hi[(size_t)t * f.E + e] = v.hi;  // debug export
-        f.logit_lo[(size_t)t * f.E + e] = v.lo;
+        f.logit_hi[(size_t)warp * f.E + e] = v.hi;  // debug export
+        f.logit_lo[(size_t)warp * f.E + e] = v.lo;
         // the word carries its own value: no other data is published with it
-        unsigned long long* w = p.lwords + ((size_t)t * f.E + e) * 2;
+        unsigned long long* w = p.lwords + ((size_t)warp * f.E + e) * 2;
         st_relaxed_u64(w, pack_logit(v.hi, seq));
         st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
       }
     }
-    named_bar(1, kRouterWarps * 32);
+    __syncthreads();
   }
 }
 
-// x -> f16 * 2^sigma_t in shared memory, one warp per token (warps 12..15); padding zeroed.
-__device__ void scale_x(const DecParams& p, const Shared& s, int w0, int nw) {
+// Staged x (bf16, in place) -> f16 * 2^sigma_t, one warp per token; K padding zeroed.
+__device__ void scale_x(const DecParams& p, const Shared& s) {
   const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5) - w0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int d8 = f.d / 8;
-  for (int t = warp; t < f.T; t += nw) {
-    const uint4* xr = reinterpret_cast<const uint4*>(f.x + (size_t)t * f.d);
+  for (int t = warp; t < f.T; t += kWarps) {
+    uint4* xr = reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride);
     float m = 0.f;
     for (int o = lane; o < d8; o += 32) {
-      const uint4 v = __ldg(xr + o);
+      const uint4 v = xr[o];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -294,7 +301,7 @@ __device__ void scale_x(const DecParams& p, const Shared& s, int w0, int nw) {
     const int sg = f16_headroom_exponent(m);
     const float sc = pow2f(sg);
     for (int o = lane; o < d8; o += 32) {
-      const uint4 v = __ldg(xr + o);
+      const uint4 v = xr[o];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t h[4];
 #pragma unroll
@@ -303,10 +310,9 @@ __device__ void scale_x(const DecParams& p, const Shared& s, int w0, int nw) {
             __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
         h[j] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o) = make_uint4(h[0], h[1], h[2], h[3]);
+      xr[o] = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    for (int o = d8 + lane; o < f.d64 / 8; o += 32)  // K padding must be finite: zero
-      *reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o) = make_uint4(0, 0, 0, 0);
+    for (int o = d8 + lane; o < f.d64 / 8; o += 32) xr[o] = make_uint4(0, 0, 0, 0);
     if (lane == 0) s.xinv[t] = pow2f(-sg);
   }
 }
@@ -330,25 +336,27 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
   const int E = f.E, k = f.k;
   const unsigned long long* wt = p.lwords + (size_t)t * E * 2;
   float vh[NPL], vl[NPL];
-  unsigned need = 0;
+  unsigned valid = 0;
 #pragma unroll
   for (int i = 0; i < NPL; ++i)
-    if (lane + 32 * i < E) need |= 1u << i;
-  const unsigned valid = need;
+    if (lane + 32 * i < E) valid |= 1u << i;
   const uint64_t t0 = globaltimer();
   while (true) {
+    // every word of the lane in one round of loads, then one check
+    unsigned long long a[NPL], b[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      if ((need >> i) & 1u) {
-        const int e = lane + 32 * i;
-        unsigned long long a, b;
-        ld_relaxed_u64x2(wt + 2 * e, a, b);
-        vh[i] = __uint_as_float((unsigned)(a >> 32));
-        vl[i] = __uint_as_float((unsigned)(b >> 32));
-        if ((unsigned)a == seq && (unsigned)b == seq) need &= ~(1u << i);
-      }
+      if ((valid >> i) & 1u) ld_relaxed_u64x2(wt + 2 * (lane + 32 * i), a[i], b[i]);
+      else a[i] = b[i] = (unsigned long long)seq;
     }
-    if (!__any_sync(0xffffffffu, need != 0)) break;
+    bool ready = true;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      vh[i] = __uint_as_float((unsigned)(a[i] >> 32));
+      vl[i] = __uint_as_float((unsigned)(b[i] >> 32));
+      ready = ready && (unsigned)a[i] == seq && (unsigned)b[i] == seq;
+    }
+    if (__all_sync(0xffffffffu, ready)) break;
     if (*abort || timed_out(t0, p.wait_ns)) {
       if (lane == 0) give_up(abort, f.status);
       break;
@@ -837,22 +845,38 @@ __device__ void down_reduce(const DecParams& p, const Shared& s, const Unit& un,
 __device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
   const FwdParams& f = p.f;
   const int lane = threadIdx.x & 31;
-  const int r0 = 16 * idx;
-  for (int o = lane; o < f.T * 16; o += 32) {
-    const int t = o >> 4, r = o & 15;
-    float a = 0.f;
-    for (int j0 = 0; j0 < f.k; j0 += 4) {  // loads of a group issued together, sums kept in slot order
-      float pv[4];
+  const int r0 = 16 * idx, n = f.T * 16;
+  constexpr int kO = 2, kJ = 8;  // outputs per lane and pairs per round: their loads are all in flight at once
+  for (int o0 = lane; o0 < n; o0 += 32 * kO) {
+    float a[kO];
 #pragma unroll
-      for (int uu = 0; uu < 4; ++uu)
-        pv[uu] = (j0 + uu < f.k) ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + uu] * f.d + r0 + r) : 0.f;
+    for (int i = 0; i < kO; ++i) a[i] = 0.f;
+    for (int j0 = 0; j0 < f.k; j0 += kJ) {  // sums kept in slot order
+      float pv[kO][kJ];
 #pragma unroll
-      for (int uu = 0; uu < 4; ++uu)
-        if (j0 + uu < f.k) a = fmaf(s.gates[t * f.k + j0 + uu], pv[uu], a);
+      for (int i = 0; i < kO; ++i) {
+        const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
+#pragma unroll
+        for (int jj = 0; jj < kJ; ++jj)
+          pv[i][jj] = (o < n && j0 + jj < f.k) ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + jj] * f.d + r0 + r) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kO; ++i) {
+        const int t = (o0 + 32 * i) >> 4;
+#pragma unroll
+        for (int jj = 0; jj < kJ; ++jj)
+          if (j0 + jj < f.k && o0 + 32 * i < n) a[i] = fmaf(s.gates[t * f.k + j0 + jj], pv[i][jj], a[i]);
+      }
     }
-    if (f.S > 0) a += __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
-    if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = a;
-    else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(a);
+#pragma unroll
+    for (int i = 0; i < kO; ++i) {
+      const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
+      if (o >= n) continue;
+      float y = a[i];
+      if (f.S > 0) y += __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
+      if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = y;
+      else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(y);
+    }
   }
 }
 
@@ -1079,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
     *abort = 0;
   }
   for (int e = tid; e < p.f.E; e += kThreads) s.cnt[e] = 0;
-  const RouterPrefetch pre = router_prefetch(p);
+  stage_router(p, s);
   pdl_wait();  // inputs and workspace are the preceding grid's until here
   if (tid == 0) {
     // launch sequence number: this CTA's word only ever grows, one step per launch,
@@ -1098,10 +1122,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
     for (int i = tid; i <= p.f.E; i += kThreads) dn[i] = 0;
     for (int i = tid; i < p.f.d / 16; i += kThreads) rc[i] = 0;
   }
+  stage_x(p, s);
+  __syncthreads();
   s.done = p.done + (size_t)(seq & 1) * (p.f.E + 1);
   s.rowcnt = p.rowcnt + (size_t)(seq & 1) * (p.f.d / 16);
-  if (warp < kRouterWarps) router(p, s, seq, pre);
-  else scale_x(p, s, kRouterWarps, kWarps - kRouterWarps);
+  router(p, s, seq);
+  scale_x(p, s);
   __syncthreads();
   routing(p, s, seq, abort);
   pdl_launch_dependents();
@@ -1111,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
 }  // namespace
 
 // Shared-memory plan of the fused kernel; returns false if it does not fit.
-bool decode_plan(DecParams& p, int max_smem) {
+bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   const FwdParams& f = p.f;
   if (f.E > 512 || f.k * kDecodeMaxT > 512) return false;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
@@ -1132,7 +1158,7 @@ bool decode_plan(DecParams& p, int max_smem) {
   p.off_xinv = (int)off;
   off = up(off + kDecodeMaxT * 4, 16);
   p.off_red = (int)off;
-  off = up(off + (size_t)kRouterWarps * kDecodeMaxT * sizeof(dd), 16);
+  off = up(off + (size_t)kWarps * kDecodeMaxT * sizeof(dd), 16);
   const size_t route_bytes = (size_t)(4 * Pm + 5 * (f.E + 1) + 2 * (f.E + 1 + 64) + 8) * 4;
   // the deepest weight ring per warp that fits: 8, 6 or 4 slots
   const int tries[7][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 6}, {4, 6}, {kMaxUS, 4}, {4, 4}, {2, 4}};
@@ -1149,7 +1175,9 @@ bool decode_plan(DecParams& p, int max_smem) {
     p.off_ring = (int)o;
     const long long room = (long long)max_smem - (long long)o;
     const int rg = (int)(room / ((long long)kWarps * kGroupBytes));
-    if (rg >= rg_want) {
+    // the ring also holds the CTA's router rows during phase A
+    const long long router_bytes = (long long)((f.E + num_sms - 1) / num_sms) * f.d * 4;
+    if (rg >= rg_want && (long long)kWarps * rg_want * kGroupBytes >= router_bytes) {
       p.ring_groups = rg_want;
       p.smem_bytes = (int)(o + (size_t)kWarps * rg_want * kGroupBytes);
       // one CTA per SM: more than half of the shared memory keeps a second CTA out

@@ -107,7 +107,7 @@ struct DecParams {
   int test_extra;          // > 0: one wait targets an unreachable count (timeout test)
   long long test_wait_ns;  // bound of that wait
 };
-bool decode_plan(DecParams& p, int max_smem);
+bool decode_plan(DecParams& p, int max_smem, int num_sms);
 cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem);
 
 // Expert GEMMs of the general path (moe_gemm.cu). Work units: (slot, group of
