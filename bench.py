@@ -277,7 +277,7 @@ def run_ours(args, wl):
 
     nl = args.layers
     T = wl.T
-    shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T)
+    shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T, flags=args.flags)
     codes_h = torch.empty((wl.total_code_bytes,), dtype=torch.uint8, pin_memory=True)
     scales_h = torch.empty((wl.total_scale_bytes,), dtype=torch.uint8, pin_memory=True)
     layers, xs, outs, xh, oh = [], [], [], [], []
@@ -451,6 +451,7 @@ def main(argv=None):
     ap.add_argument("--kernel-steps", type=int, default=3, help="eager steps for per-kernel event timing")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 4: tcgen05 gate/up)")
     args = ap.parse_args(argv)
     wl = synth.WORKLOADS[args.workload]
     if args.layers is None:

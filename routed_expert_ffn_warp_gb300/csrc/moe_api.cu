@@ -21,6 +21,9 @@ struct moe_ctx {
   uint8_t* packed = nullptr;
   size_t packed_bytes = 0;
   size_t expert_stride = 0;
+  uint8_t* tcw = nullptr;  // gate/up copy for the tcgen05 GEMM (MOE_FLAG_TC_GATEUP)
+  size_t tcw_bytes = 0;
+  size_t tcw_stride = 0;
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
@@ -106,6 +109,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const int d = c.d, F = c.ffn, E = c.n_experts, k = c.top_k, S = c.shared_ffn, Tm = std::max(c.t_max, 1);
   ctx->expert_stride = moe::expert_packed_bytes(d, F);
   ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
+  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) != 0;
+  if (tc) {
+    ctx->tcw_stride = moe::tc_expert_bytes(d, F);
+    ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
+  }
 
   const size_t Pm = (size_t)Tm * k, Qm = Pm + (S > 0 ? (size_t)Tm : 0);
   const int d64 = moe::k64_tiles(d) * 64;
@@ -125,6 +133,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
                o_offsets = take((size_t)(E + 1) * 4), o_perm = take(Pm * 4), o_inv = take(Pm * 4);
   const size_t o_ns = take(4), o_se = take((size_t)(E + 1) * 4), o_sq = take((size_t)(E + 1) * 4),
                o_sn = take((size_t)(E + 1) * 4), o_gp = take((size_t)(E + 2) * 4), o_dp = take((size_t)(E + 2) * 4);
+  // activation panels of the tcgen05 GEMM: at most ceil(Q / 48) + slots blocks
+  const size_t n_panels = tc ? Qm / moe::kTcGemmRows + (size_t)E + 2 : 0;
+  const size_t o_panel = take(n_panels * moe::tc_ksteps(d) * moe::kTcPanelStep), o_pp = take((size_t)(E + 2) * 4);
   const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
@@ -134,7 +145,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
                o_lw = take((size_t)std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
   ctx->ws_bytes = off;
 
-  if ((e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
+  if ((tc && (e = cudaMalloc(&ctx->tcw, ctx->tcw_bytes)) != cudaSuccess) ||
+      (e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->w_router, (size_t)E * d * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->bias, (size_t)E * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->ws, ctx->ws_bytes)) != cudaSuccess) {
@@ -164,6 +176,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.expert_stride = ctx->expert_stride;
   p.x16 = reinterpret_cast<uint16_t*>(w + o_x16);
   p.xinv = reinterpret_cast<float*>(w + o_xinv);
+  p.tcw = ctx->tcw;
+  p.tcw_stride = ctx->tcw_stride;
+  p.xpanel = reinterpret_cast<uint8_t*>(w + o_panel);
+  p.panel_prefix = reinterpret_cast<int32_t*>(w + o_pp);
   p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
   p.xq_spitch = xq_spitch;
@@ -247,6 +263,9 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
     if ((e = moe::launch_repack(sc, ss, n, d, F, ccs, css, ctx->packed + (size_t)x0 * ctx->expert_stride,
                                 ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
       break;
+    if (ctx->tcw && (e = moe::launch_repack_tc(sc, ss, n, d, F, ccs, css, ctx->tcw + (size_t)x0 * ctx->tcw_stride,
+                                               ctx->tcw_stride, 0)) != cudaSuccess)
+      break;
     e = cudaDeviceSynchronize();
   }
   if (e == cudaSuccess && S > 0) {
@@ -254,7 +273,9 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
     if ((e = cudaMemcpy(sc, codes + (size_t)E * ccs, sc_b, cudaMemcpyDefault)) == cudaSuccess &&
         (e = cudaMemcpy(ss, scales + (size_t)E * css, ss_b, cudaMemcpyDefault)) == cudaSuccess &&
         (e = moe::launch_repack(sc, ss, 1, d, S, sc_b, ss_b, ctx->packed + (size_t)E * ctx->expert_stride,
-                                moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess)
+                                moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess &&
+        (!ctx->tcw || (e = moe::launch_repack_tc(sc, ss, 1, d, S, sc_b, ss_b, ctx->tcw + (size_t)E * ctx->tcw_stride,
+                                                 moe::tc_expert_bytes(d, S), 0)) == cudaSuccess))
       e = cudaDeviceSynchronize();
   }
   int nan_flag = 0;
@@ -407,6 +428,7 @@ void moe_destroy(moe_ctx* ctx) {
   {
     DeviceGuard guard(ctx->device);
     cudaFree(ctx->packed);
+    cudaFree(ctx->tcw);
     cudaFree(ctx->w_router);
     cudaFree(ctx->bias);
     cudaFree(ctx->ws);

@@ -46,6 +46,35 @@ __host__ __device__ inline size_t expert_packed_bytes(int d, int f) {
   return gu_packed_bytes(d, f) + dn_packed_bytes(d, f);
 }
 
+// Second copy of the gate/up weights for the block-scaled tcgen05 GEMM of the
+// general path: per expert, blocks of kTcBlockBytes ordered [M tile a][K step
+// ks]. M tile a is the 64 gate rows then the 64 up rows of pair tiles 4a ..
+// 4a+3 (M row m: tile t = m / 16 -- pair tile 4a + t % 4, gate if t < 4 --
+// and row m % 16 of it); a K step is 128 elements of d. A block is
+//  * 8,192 code bytes in core-matrix order: the 8 packed bytes (16 codes,
+//    low nibble = even element) of M row m and 16-element chunk kc at
+//    ((m / 8) * 8 + kc) * 64 + (m % 8) * 8, so that widening every 8 bytes to
+//    16 gives the K-major operand layout of the MMA (LBO 128, SBO 1024);
+//  * 512 scale bytes as 32-bit words [lane l][r]: byte kb of word (l, r) is
+//    the scale of M row 32 r + l in K block 4 ks + kb, the order in which a
+//    warp stores them to tensor memory.
+// Rows of missing pair tiles and K past d are code 0 with scale 127.
+constexpr int kTcStepK = 128;
+constexpr int kTcCodeBytes = 8192;
+constexpr int kTcBlockBytes = kTcCodeBytes + 512;
+__host__ __device__ inline int tc_msteps(int f) { return (f / 16 + 3) / 4; }
+__host__ __device__ inline int tc_ksteps(int d) { return (d + kTcStepK - 1) / kTcStepK; }
+__host__ __device__ inline size_t tc_expert_bytes(int d, int f) {
+  return (size_t)tc_msteps(f) * tc_ksteps(d) * kTcBlockBytes;
+}
+// Activation panels of the tcgen05 gate/up GEMM: per (slot, block of up to 48
+// tokens) and K step, the B operand -- row n = plane * npad + m (hi plane
+// rows, then lo plane rows; npad = tokens rounded up to 8, at least 8) --
+// in core-matrix order ((n / 8) * 8 + kc) * 128 + (n % 8) * 16, then 512
+// scale bytes as words [lane l][r] for B row 32 r + l (127 past the rows).
+constexpr int kTcPanelRows = 96;
+constexpr int kTcPanelStep = kTcPanelRows * kTcStepK + 512;
+
 // ---------------------------------------------------------------- forward parameters
 
 struct FwdParams {
@@ -65,6 +94,10 @@ struct FwdParams {
   uint16_t* x16;         // f16 [t_max][d64], x * 2^sigma_t
   float* xinv;           // [t_max]: 2^-sigma_t
   int tc_gateup;         // gate/up on the tcgen05 block-scaled GEMM (moe_tcgemm.cu)
+  const uint8_t* tcw;    // its weight copy (see tc_expert_bytes)
+  size_t tcw_stride;     // bytes per routed expert of it
+  uint8_t* xpanel;       // its activation panels (kTcPanelStep per K step)
+  int32_t* panel_prefix; // [E+2] first panel of each slot
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
   int xq_spitch;         // scale bytes per plane row (a multiple of 4)
@@ -135,5 +168,9 @@ cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream);
+// The tcgen05 gate/up weight copy of n_exp experts from the canonical layout.
+cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
+                             size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
+                             cudaStream_t stream);
 
 }  // namespace moe

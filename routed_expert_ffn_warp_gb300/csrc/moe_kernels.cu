@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
     }
   }
   if (threadIdx.x == 32) {
-    int ns = 0, gu = 0, dn = 0;
+    int ns = 0, gu = 0, dn = 0, pn = 0;
     for (int e = 0; e < E; ++e) {
       if (cnt[e] == 0) continue;
       p.slot_expert[ns] = e;
@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.slot_n[ns] = cnt[e];
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
+      if (p.tc_gateup) p.panel_prefix[ns] = pn;
+      pn += (cnt[e] + kTcGemmRows - 1) / kTcGemmRows;
       const int blocks = (cnt[e] + kGemmRows - 1) / kGemmRows;
       gu += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * ((p.F / 16 + 3) / 4)
                         : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
@@ -245,6 +247,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.slot_n[ns] = T;
       p.gu_prefix[ns] = gu;
       p.dn_prefix[ns] = dn;
+      if (p.tc_gateup) p.panel_prefix[ns] = pn;
+      pn += (T + kTcGemmRows - 1) / kTcGemmRows;
       const int blocks = (T + kGemmRows - 1) / kGemmRows;
       gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * ((p.S / 16 + 3) / 4)
                         : blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
@@ -253,6 +257,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
     }
     p.gu_prefix[ns] = gu;
     p.dn_prefix[ns] = dn;
+    if (p.tc_gateup) p.panel_prefix[ns] = pn;
     *p.n_slots = ns;
   }
 }
