@@ -24,6 +24,9 @@ struct moe_ctx {
   uint8_t* tcw = nullptr;  // gate/up copy for the tcgen05 GEMM (MOE_FLAG_TC_GATEUP)
   size_t tcw_bytes = 0;
   size_t tcw_stride = 0;
+  uint8_t* tcwd = nullptr;  // down copy for the tcgen05 GEMM
+  size_t tcwd_bytes = 0;
+  size_t tcwd_stride = 0;
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
@@ -113,6 +116,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
+    ctx->tcwd_stride = moe::tc_down_bytes(d, F);
+    ctx->tcwd_bytes = ctx->tcwd_stride * (size_t)E + (S > 0 ? moe::tc_down_bytes(d, S) : 0);
   }
 
   const size_t Pm = (size_t)Tm * k, Qm = Pm + (S > 0 ? (size_t)Tm : 0);
@@ -136,6 +141,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // activation panels of the tcgen05 GEMM: at most ceil(Q / 48) + slots blocks
   const size_t n_panels = tc ? Qm / moe::kTcGemmRows + (size_t)E + 2 : 0;
   const size_t o_panel = take(n_panels * moe::tc_ksteps(d) * moe::kTcPanelStep), o_pp = take((size_t)(E + 2) * 4);
+  const size_t o_hpanel = take(n_panels * moe::tc_ksteps(std::max(F, S)) * moe::kTcPanelStepD);
   const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
@@ -146,6 +152,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->ws_bytes = off;
 
   if ((tc && (e = cudaMalloc(&ctx->tcw, ctx->tcw_bytes)) != cudaSuccess) ||
+      (tc && (e = cudaMalloc(&ctx->tcwd, ctx->tcwd_bytes)) != cudaSuccess) ||
       (e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->w_router, (size_t)E * d * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->bias, (size_t)E * 4)) != cudaSuccess ||
@@ -179,6 +186,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.tcw = ctx->tcw;
   p.tcw_stride = ctx->tcw_stride;
   p.xpanel = reinterpret_cast<uint8_t*>(w + o_panel);
+  p.tcwd = ctx->tcwd;
+  p.tcwd_stride = ctx->tcwd_stride;
+  p.hpanel = reinterpret_cast<uint8_t*>(w + o_hpanel);
   p.panel_prefix = reinterpret_cast<int32_t*>(w + o_pp);
   p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
@@ -264,7 +274,10 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
                                 ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
       break;
     if (ctx->tcw && (e = moe::launch_repack_tc(sc, ss, n, d, F, ccs, css, ctx->tcw + (size_t)x0 * ctx->tcw_stride,
-                                               ctx->tcw_stride, 0)) != cudaSuccess)
+                                               ctx->tcw_stride, false, 0)) != cudaSuccess)
+      break;
+    if (ctx->tcwd && (e = moe::launch_repack_tc(sc, ss, n, d, F, ccs, css, ctx->tcwd + (size_t)x0 * ctx->tcwd_stride,
+                                                ctx->tcwd_stride, true, 0)) != cudaSuccess)
       break;
     e = cudaDeviceSynchronize();
   }
@@ -275,7 +288,9 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
         (e = moe::launch_repack(sc, ss, 1, d, S, sc_b, ss_b, ctx->packed + (size_t)E * ctx->expert_stride,
                                 moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess &&
         (!ctx->tcw || (e = moe::launch_repack_tc(sc, ss, 1, d, S, sc_b, ss_b, ctx->tcw + (size_t)E * ctx->tcw_stride,
-                                                 moe::tc_expert_bytes(d, S), 0)) == cudaSuccess))
+                                                 moe::tc_expert_bytes(d, S), false, 0)) == cudaSuccess) &&
+        (!ctx->tcwd || (e = moe::launch_repack_tc(sc, ss, 1, d, S, sc_b, ss_b, ctx->tcwd + (size_t)E * ctx->tcwd_stride,
+                                                  moe::tc_down_bytes(d, S), true, 0)) == cudaSuccess))
       e = cudaDeviceSynchronize();
   }
   int nan_flag = 0;
@@ -429,6 +444,7 @@ void moe_destroy(moe_ctx* ctx) {
     DeviceGuard guard(ctx->device);
     cudaFree(ctx->packed);
     cudaFree(ctx->tcw);
+    cudaFree(ctx->tcwd);
     cudaFree(ctx->w_router);
     cudaFree(ctx->bias);
     cudaFree(ctx->ws);

@@ -74,6 +74,17 @@ __host__ __device__ inline size_t tc_expert_bytes(int d, int f) {
 // scale bytes as words [lane l][r] for B row 32 r + l (127 past the rows).
 constexpr int kTcPanelRows = 96;
 constexpr int kTcPanelStep = kTcPanelRows * kTcStepK + 512;
+// The down projection on the same GEMM: a weight copy of the down matrices in
+// the same block format (M tile a = rows 128a .. 128a+127 of d, K steps of 128
+// over f; rows past d are code 0 with scale 127) and per-(slot, token block)
+// panels of h as four MXFP8 planes (row n = plane * npad + m, up to 192 rows;
+// scale words [lane l][r], r < 8, 1,024 bytes).
+constexpr int kTcPanelRowsD = 192;
+constexpr int kTcPanelStepD = kTcPanelRowsD * kTcStepK + 1024;
+__host__ __device__ inline int tc_dtiles(int d) { return (d + 127) / 128; }
+__host__ __device__ inline size_t tc_down_bytes(int d, int f) {
+  return (size_t)tc_dtiles(d) * tc_ksteps(f) * kTcBlockBytes;
+}
 
 // ---------------------------------------------------------------- forward parameters
 
@@ -97,6 +108,9 @@ struct FwdParams {
   const uint8_t* tcw;    // its weight copy (see tc_expert_bytes)
   size_t tcw_stride;     // bytes per routed expert of it
   uint8_t* xpanel;       // its activation panels (kTcPanelStep per K step)
+  const uint8_t* tcwd;   // the down matrices' copy for the same GEMM (see tc_down_bytes)
+  size_t tcwd_stride;    // bytes per routed expert of it
+  uint8_t* hpanel;       // h panels of the down step (kTcPanelStepD per K step)
   int32_t* panel_prefix; // [E+2] first panel of each slot
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
@@ -168,9 +182,11 @@ cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream);
-// The tcgen05 gate/up weight copy of n_exp experts from the canonical layout.
+// The tcgen05 weight copies of n_exp experts from the canonical layout: gate/up
+// (down = false) or down (down = true).
 cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                              size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
-                             cudaStream_t stream);
+                             bool down, cudaStream_t stream);
+cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms);
 
 }  // namespace moe

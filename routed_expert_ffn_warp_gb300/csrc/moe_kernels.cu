@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       const int blocks = (cnt[e] + kGemmRows - 1) / kGemmRows;
       gu += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * ((p.F / 16 + 3) / 4)
                         : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
-      dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+      dn += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * tc_dtiles(p.d)
+                        : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
     if (p.S > 0 && T > 0) {
@@ -252,7 +253,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       const int blocks = (T + kGemmRows - 1) / kGemmRows;
       gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * ((p.S / 16 + 3) / 4)
                         : blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
-      dn += blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dtiles(p.d)
+                        : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
     p.gu_prefix[ns] = gu;
@@ -358,7 +360,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   cudaError_t e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[2], stream);
-  e = launch_gemm_down(p, stream, num_sms);
+  e = p.tc_gateup ? launch_gemm_down_tc(p, stream, num_sms) : launch_gemm_down(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[3], stream);
   combine_kernel<<<dim3((p.d + 255) / 256, p.T), 256, 0, stream>>>(p);
