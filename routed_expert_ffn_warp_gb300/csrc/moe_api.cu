@@ -1,5 +1,6 @@
 // Host side of the routed-expert FFN library: context, loads, forward, debug
 // exports. The C ABI is declared in include/moe.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -27,6 +28,8 @@ struct moe_ctx {
   uint8_t* tcwd = nullptr;  // down copy for the tcgen05 GEMM
   size_t tcwd_bytes = 0;
   size_t tcwd_stride = 0;
+  CUtensorMap tmap_gu{};  // tensor maps the tcgen05 GEMM loads tcw / tcwd through
+  CUtensorMap tmap_dn{};
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
@@ -113,6 +116,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->expert_stride = moe::expert_packed_bytes(d, F);
   ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
   const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) != 0;
+  if (tc && std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) > (size_t)ctx->max_smem) {
+    delete ctx;
+    return fail(nullptr, MOE_ERR_INVALID_ARG, "too many experts for the tcgen05 GEMM's shared-memory tables");
+  }
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
@@ -160,6 +167,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
   }
+  if (tc && (!moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu) ||
+             !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn))) {
+    moe_destroy(ctx);
+    return fail(nullptr, MOE_ERR_CUDA, "cuTensorMapEncodeTiled refused the tcgen05 weight copy");
+  }
   if ((e = cudaMemset(ctx->ws, 0, ctx->ws_bytes)) != cudaSuccess ||
       (e = cudaMemset(ctx->bias, 0, (size_t)E * 4)) != cudaSuccess) {
     moe_destroy(ctx);
@@ -189,6 +201,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.tcwd = ctx->tcwd;
   p.tcwd_stride = ctx->tcwd_stride;
   p.hpanel = reinterpret_cast<uint8_t*>(w + o_hpanel);
+  p.tmap_gu = &ctx->tmap_gu;
+  p.tmap_dn = &ctx->tmap_dn;
   p.panel_prefix = reinterpret_cast<int32_t*>(w + o_pp);
   p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
@@ -431,7 +445,8 @@ int moe_forward_phases(const moe_ctx* ctx, int T, const char** names) {
 int moe_launches_per_forward(const moe_ctx* ctx, int T) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (T <= 0) return 0;
-  return uses_decode(ctx, T) ? 1 : moe::kLaunchesPerForward;
+  if (uses_decode(ctx, T)) return 1;
+  return ctx->base.tc_gateup ? moe::kLaunchesPerForwardTc : moe::kLaunchesPerForward;
 }
 
 size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }

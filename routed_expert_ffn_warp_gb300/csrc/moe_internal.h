@@ -54,10 +54,11 @@ __host__ __device__ inline size_t expert_packed_bytes(int d, int f) {
 //  * 8,192 code bytes in core-matrix order: the 8 packed bytes (16 codes,
 //    low nibble = even element) of M row m and 16-element chunk kc at
 //    ((m / 8) * 8 + kc) * 64 + (m % 8) * 8, so that widening every 8 bytes to
-//    16 gives the K-major operand layout of the MMA (LBO 128, SBO 1024);
+//    16 (what a TMA copy of the "16 x U4, 16-byte aligned" type does) gives
+//    the K-major operand layout of the MMA (LBO 128, SBO 1024);
 //  * 512 scale bytes as 32-bit words [lane l][r]: byte kb of word (l, r) is
-//    the scale of M row 32 r + l in K block 4 ks + kb, the order in which a
-//    warp stores them to tensor memory.
+//    the scale of M row 32 r + l in K block 4 ks + kb, the order tcgen05.cp
+//    copies to tensor memory.
 // Rows of missing pair tiles and K past d are code 0 with scale 127.
 constexpr int kTcStepK = 128;
 constexpr int kTcCodeBytes = 8192;
@@ -78,7 +79,8 @@ constexpr int kTcPanelStep = kTcPanelRows * kTcStepK + 512;
 // the same block format (M tile a = rows 128a .. 128a+127 of d, K steps of 128
 // over f; rows past d are code 0 with scale 127) and per-(slot, token block)
 // panels of h as four MXFP8 planes (row n = plane * npad + m, up to 192 rows;
-// scale words [lane l][r], r < 8, 1,024 bytes).
+// scales as two 512-byte blocks of words [lane l][r % 4] for B row 32 r + l,
+// block r / 4), written by the gate/up GEMM's epilogue.
 constexpr int kTcPanelRowsD = 192;
 constexpr int kTcPanelStepD = kTcPanelRowsD * kTcStepK + 1024;
 __host__ __device__ inline int tc_dtiles(int d) { return (d + 127) / 128; }
@@ -111,6 +113,8 @@ struct FwdParams {
   const uint8_t* tcwd;   // the down matrices' copy for the same GEMM (see tc_down_bytes)
   size_t tcwd_stride;    // bytes per routed expert of it
   uint8_t* hpanel;       // h panels of the down step (kTcPanelStepD per K step)
+  const void* tmap_gu;   // host: CUtensorMap of tcw (see encode_tc_weight_map)
+  const void* tmap_dn;   // host: CUtensorMap of tcwd
   int32_t* panel_prefix; // [E+2] first panel of each slot
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
@@ -176,6 +180,7 @@ cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_
 constexpr int kForwardPhases = 4;
 extern const char* const kForwardPhaseNames;  // "route,gateup,down,combine"
 constexpr int kLaunchesPerForward = 7;
+constexpr int kLaunchesPerForwardTc = 9;  // + x planes, x panels (MOE_FLAG_TC_GATEUP)
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);
 // Routing only (router logits, top-k gates, counting sort) of the general path.
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
@@ -188,5 +193,11 @@ cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_
                              size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                              bool down, cudaStream_t stream);
 cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms);
+// Dynamic shared memory of the tcgen05 GEMM kernel for E experts.
+size_t tc_gemm_smem_bytes(int E, bool down);
+// Fills `map` (a 64-byte aligned CUtensorMap) with the tensor map the tcgen05
+// GEMM loads a weight copy of `bytes` bytes at `base` through; false if the
+// driver refuses it.
+bool encode_tc_weight_map(const void* base, size_t bytes, void* map);
 
 }  // namespace moe

@@ -11,8 +11,9 @@
 //    bytes apart;
 //  * scale factors (one E8M0 byte per row and 32-element K block) live in
 //    TMEM: for rows 32 r + l, byte b of column base + r in lane l holds the
-//    scale of K block b, replicated in all four lane quadrants; the MMA picks
-//    the byte with the scale-factor ids of its instruction descriptor.
+//    scale of K block b, replicated in all four lane quadrants (tcgen05.cp
+//    32x128b.warpx4 of 512-byte blocks [lane][4 words]); the MMA picks the
+//    byte with the scale-factor ids of its instruction descriptor.
 #pragma once
 #include <stdint.h>
 
@@ -55,6 +56,23 @@ __device__ __forceinline__ void mma_mxf4_mxf8(uint32_t d_tmem, uint64_t adesc, u
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory (described like an MMA operand:
+// 8-row groups SBO bytes apart) to TMEM lanes 0..31 of 4 consecutive columns
+// at taddr, replicated into all four lane quadrants. Runs in issue order with
+// the MMAs this thread issues after it.
+__device__ __forceinline__ void cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// TMA tiled load of the box at (x, y) of a 2-D tensor map (a kernel parameter
+// declared __grid_constant__) into this CTA's shared memory; completion is
+// signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.

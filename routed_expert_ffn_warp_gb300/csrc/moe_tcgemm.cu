@@ -1,32 +1,38 @@
-// Gate/up + SwiGLU of the general path on the 5th-generation tensor cores:
-// a block-scaled MMA of the MXFP4 expert weights (E2M1 codes with their E8M0
-// scales) by MXFP8 activations (tcgen05.mma kind::mxf8f6f4.block_scale),
-// accumulators in tensor memory.
+// Gate/up + SwiGLU and the down projection of the general path on the
+// 5th-generation tensor cores: block-scaled MMAs of the MXFP4 expert weights
+// (E2M1 codes with their E8M0 scales) by MXFP8 activations
+// (tcgen05.mma kind::mxf8f6f4.block_scale), accumulators in tensor memory.
 //
 // The activation x (bf16) enters as two MXFP8 planes, x = 2^sh * hi + 2^sl * lo
 // per 32-element block (E4M3 codes hi and lo with their own E8M0 scales): a
 // bf16 value has 8 significant bits, hi keeps its top 4 and lo the remaining 4,
 // so the split is exact except for elements below about 2^-10 of their block's
 // largest one. Token m of a unit is B row m (hi) and B row npad + m (lo); its
-// gate (up) value is D[., m] + D[., npad + m].
+// gate (up) value is D[., m] + D[., npad + m]. h enters the down GEMM the same
+// way in four planes (about 16 significant bits per block).
 //
-// Work unit: (slot, M tile of 4 pair tiles = 64 gate + 64 up rows, block of
-// up to 48 tokens of the slot); K = d in steps of 128 (four K=32 MMAs). The
-// weights come from their own copy, one contiguous block per (M tile, K step)
-// already in the operand's core-matrix order, and the activations from
-// per-(slot, token block) panels packed once per call in the same order, so a
-// stage is three bulk copies (cp.async.bulk) issued by one thread. The CTA is
-// warp-specialized: a producer lane, four converter warps that widen the
-// packed E2M1 codes (8 bytes -> 16 bytes, the MMA's E2M1 operand layout) and
-// store the stage's scale factors to tensor memory, an MMA lane, and four
-// epilogue warps that read a finished unit's accumulators (double-buffered in
-// tensor memory, so the next unit's MMAs run meanwhile) and write h =
-// SiLU(gate) * up in the f16 hi + lo format of the down step. Stages are
-// handed on with mbarriers: full (bulk bytes landed), ready (operands
-// widened, scales stored), empty (the stage's MMAs completed).
+// Work unit: (slot, M tile, block of up to 48 tokens of the slot), K in steps
+// of 128 (four K=32 MMAs). Gate/up: M tile = 64 gate + 64 up rows (4 pair
+// tiles), K = d. Down: M tile = 128 rows of d, K = f. The weights come from
+// their own copy, one contiguous block per (M tile, K step) in the operand's
+// core-matrix order with the E2M1 codes packed; a TMA tensor copy of the
+// 4-bit "16 x U4, 16-byte aligned" type widens every 8 code bytes to the
+// 16-byte rows the MMA reads on the way into shared memory. The activations
+// come from per-(slot, token block) panels in the MMA's order: x panels are
+// packed once per call, h panels are written by the gate/up epilogue itself.
+//
+// The CTA is warp-specialized: a weight producer lane (tensor copies, and L2
+// prefetches further ahead), an activation producer lane (bulk copies), an
+// MMA lane (scale factors to tensor memory with tcgen05.cp, then the MMAs),
+// and eight epilogue warps that read a finished unit's accumulators
+// (double-buffered in tensor memory, so the next unit's MMAs run meanwhile).
+// Stages are handed on with mbarriers: full (bytes landed), empty (the
+// stage's MMAs completed), accfull / accempty (accumulator buffer states).
 //
 // The pages: tokens grouped by expert on the GPU for the prompt, one GEMM per
 // expert over its rows ("Neural Server" technical page, "Prompt processing").
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include "../../include/moe.h"
@@ -41,26 +47,36 @@ using namespace dev;
 
 constexpr int kThr = 384;                  // 12 warps: see the roles below
 constexpr int kMaxTok = kTcGemmRows;       // tokens per unit
-constexpr int kSA = 8;                     // weight stages in flight (bulk copies from HBM)
+constexpr int kPf = 12;                    // L2 prefetch distance of the weight blocks, in K steps
 constexpr int kAOp = 128 * kTcStepK;       // widened E2M1 operand: 16 bytes per 16 elements
-constexpr int kAStage = kAOp + 512;        // [operand (packed codes land in its first half) | SFA]
-constexpr uint32_t kTmemCols = 512;        // D: 2 buffers at columns 0 and 192; scale factors from 384
-constexpr int kDCol = 192;                 // D buffer stride (N <= 192)
-constexpr int kSfCol = 384;                // set s (the weight stage): SFA columns +16 s .. +3, SFB +8 .. +15
+constexpr int kAStage = kAOp + 512;        // [operand | SFA]
+constexpr int kCmRows = kTcBlockBytes / 64;  // 64-byte tensor rows per weight block (8,192 code + 512 scale bytes)
+constexpr uint32_t kTmemCols = 512;        // accumulators from column 0, scale factors from 384
+constexpr int kSfCol = 384;                // set s (the stage): SFA columns +16 s .. +3, SFB +8 .. +15
 constexpr long long kWaitNs = 50000000LL;
-// roles
-constexpr int kProducerWarp = 0, kMmaWarp = 1, kConvWarp0 = 4, kEpiWarp0 = 8;
+// roles: warp 0 weights, 1 and 2 MMA lanes, 3 activations, 4 .. 11 epilogue (lane quadrant = warp % 4)
+constexpr int kProducerWarp = 0, kMmaWarp0 = 1, kPanelWarp = 3, kEpiWarp0 = 4, kEpiThreads = 256;
 
 // The two uses of the GEMM. Gate/up: M tiles of 64 gate + 64 up rows, K = d,
-// B = x in 2 MXFP8 planes, epilogue h = SiLU(gate) * up. Down: M tiles of
-// 128 rows of d, K = f, B = h in 4 MXFP8 planes, epilogue part = D.
+// B = x in 2 MXFP8 planes, epilogue h = SiLU(gate) * up into the h panels.
+// Down: M tiles of 128 rows of d, K = f, B = h in 4 MXFP8 planes, epilogue
+// part = D. A stage holds one K step of both operands: [A | B panel step].
+// With kMma MMA lanes, lane t takes the CTA's K steps j = t (mod kMma) and
+// accumulates them in its own accumulator of the unit's buffer (the epilogue
+// adds them): one lane cannot issue MMAs of N <= 96 as fast as the tensor
+// core runs them.
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
   static constexpr int kPanelRows = kDown ? kTcPanelRowsD : kTcPanelRows;
   static constexpr int kPanelStep = kDown ? kTcPanelStepD : kTcPanelStep;
-  static constexpr int kSfWords = kDown ? 8 : 4;  // B scale words per lane in a panel step
-  static constexpr int kSB = kDown ? 3 : 5;       // activation-panel stages (from L2)
+  static constexpr int kSfBlocks = kDown ? 2 : 1;  // 512-byte B scale blocks per panel step (32 rows x 4 words each)
+  static constexpr int kStage = kAStage + kPanelStep;
+  static constexpr int kS = kDown ? 5 : 6;         // stages (scale sets in TMEM: at most 8)
+  static constexpr int kMma = kDown ? 1 : 2;       // MMA lanes
+  static constexpr int kDCol = kDown ? 192 : 96;   // accumulator width (N <= kDCol); buffer b, lane t at kDCol (kMma b + t)
+  static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values [4 blocks][token][32]
+  static_assert(2 * kMma * kDCol <= kSfCol && kS <= 8, "TMEM columns");
 };
 
 // Per-slot tables the roles look units up in, copied to shared memory once:
@@ -69,8 +85,7 @@ constexpr size_t tc_table_bytes(int E) { return (size_t)5 * (E + 2) * 4; }
 
 template <bool kDown>
 constexpr size_t tc_smem_fixed() {
-  return (size_t)kSA * kAStage + (size_t)Mode<kDown>::kSB * Mode<kDown>::kPanelStep +
-         (kDown ? 0 : (size_t)64 * kMaxTok * 4) + 8 * (3 * kSA + 2 * Mode<kDown>::kSB + 4) + 16;
+  return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (2 * Mode<kDown>::kS + 4) + 16;
 }
 
 __device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity, int* status) {
@@ -109,6 +124,7 @@ struct TcUnit {
   int mt;       // M tile
   int nks;      // K steps
   int panel;    // panel of the (slot, token block)
+  int y;        // tensor row (64 bytes each) of the M tile's first weight block
   const uint8_t* w;  // weight blocks of the M tile (K step 0)
 };
 
@@ -126,13 +142,23 @@ __device__ __forceinline__ TcUnit tc_unit(const FwdParams& p, const SlotTab& st,
   g.n = min(kMaxTok, st.sn[s] - kMaxTok * tb);
   g.nks = tc_ksteps(kDown ? g.f : p.d);
   g.panel = st.ppre[s] + tb;
-  g.w = kDown ? p.tcwd + (size_t)g.e * p.tcwd_stride + (size_t)g.mt * g.nks * kTcBlockBytes
-              : p.tcw + (size_t)g.e * p.tcw_stride + (size_t)g.mt * g.nks * kTcBlockBytes;
+  const size_t stride = kDown ? p.tcwd_stride : p.tcw_stride;  // a multiple of kTcBlockBytes
+  g.y = (int)((size_t)g.e * (stride / 64)) + g.mt * g.nks * kCmRows;
+  g.w = (kDown ? p.tcwd : p.tcw) + (size_t)g.e * stride + (size_t)g.mt * g.nks * kTcBlockBytes;
   return g;
 }
 
 __device__ __forceinline__ int tok_of(const FwdParams& p, int q) { return q < p.P ? p.perm[q] / p.k : q - p.P; }
 __device__ __forceinline__ int npad_of(int n) { return max(8, (n + 7) & ~7); }
+
+// Byte offset, within an h panel step, of the E8M0 scale of B row `row` and
+// K block kb: two 512-byte blocks of words [lane][4], block r / 4 holding B
+// rows 32 r + lane in word r % 4 (r = row / 32), the order tcgen05.cp
+// 32x128b copies to tensor memory.
+__device__ __forceinline__ int hsf_off(int row, int kb) {
+  const int r = row >> 5;
+  return kTcPanelRowsD * kTcStepK + 512 * (r >> 2) + 16 * (row & 31) + 4 * (r & 3) + kb;
+}
 
 // The producer's walk over the steps (unit, K step) of the CTA.
 template <bool kDown>
@@ -146,251 +172,6 @@ __device__ __forceinline__ void cursor_next(const FwdParams& p, const SlotTab& s
   if (++c.ks == c.g.nks) {
     c.ks = 0;
     if (++c.i < n_units) c.g = tc_unit<kDown>(p, st, blockIdx.x + c.i * gridDim.x);
-  }
-}
-
-template <bool kDown>
-__global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(FwdParams p) {
-  using M = Mode<kDown>;
-  constexpr int kSB = M::kSB;
-  extern __shared__ __align__(1024) uint8_t sm[];
-  uint8_t* astg = sm;                                              // [kSA][kAStage]
-  uint8_t* bstg = astg + (size_t)kSA * kAStage;                   // [kSB][panel step]
-  float* upx = reinterpret_cast<float*>(bstg + (size_t)kSB * M::kPanelStep);  // gate/up: [64 rows][kMaxTok]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(upx) + (kDown ? 0 : 64 * kMaxTok * 4));
-  uint64_t* fullA = bars;                 // bulk weight bytes landed
-  uint64_t* emptyA = fullA + kSA;         // the MMAs reading the weight stage completed
-  uint64_t* ready = emptyA + kSA;         // the stage's operand is widened and its scale set stored
-  uint64_t* fullB = ready + kSA;          // bulk panel bytes landed
-  uint64_t* emptyB = fullB + kSB;         // the MMAs reading the panel stage completed
-  uint64_t* accfull = emptyB + kSB;       // [2]
-  uint64_t* accempty = accfull + 2;       // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
-  int* tab = reinterpret_cast<int*>(tslot + 4);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ns = *p.n_slots;
-  const int total = (kDown ? p.dn_prefix : p.gu_prefix)[ns];
-  const int n_units = total > (int)blockIdx.x ? (total - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  if (n_units == 0) return;
-  SlotTab st;
-  st.ns = ns;
-  st.upre = tab;
-  st.ppre = tab + (p.E + 2);
-  st.sexp = tab + 2 * (p.E + 2);
-  st.sq0 = tab + 3 * (p.E + 2);
-  st.sn = tab + 4 * (p.E + 2);
-  for (int i = tid; i <= ns; i += kThr) {
-    tab[i] = (kDown ? p.dn_prefix : p.gu_prefix)[i];
-    tab[(p.E + 2) + i] = p.panel_prefix[i];
-    if (i < ns) {
-      tab[2 * (p.E + 2) + i] = p.slot_expert[i];
-      tab[3 * (p.E + 2) + i] = p.slot_q0[i];
-      tab[4 * (p.E + 2) + i] = p.slot_n[i];
-    }
-  }
-  if (tid == 0) {
-    for (int s = 0; s < kSA; ++s) {
-      mbar_init(&fullA[s], 1);
-      mbar_init(&emptyA[s], 1);
-      mbar_init(&ready[s], 128);
-    }
-    for (int s = 0; s < kSB; ++s) {
-      mbar_init(&fullB[s], 1);
-      mbar_init(&emptyB[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&accfull[a], 1);
-      mbar_init(&accempty[a], 128);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 0) tc::alloc(tslot, kTmemCols);
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tmem = *tslot;
-  const int G = gridDim.x, b0 = blockIdx.x;
-
-  if (warp == kProducerWarp) {
-    if (lane == 0) {
-      // weights run kSA - kSB steps ahead of the panels: both wait for the
-      // same point of the pipeline when their stage comes round
-      Cursor<kDown> ca, cb;
-      ca.i = cb.i = 0;
-      ca.ks = cb.ks = 0;
-      ca.g = cb.g = tc_unit<kDown>(p, st, b0);
-      int ja = 0, jb = 0;
-      while (ca.i < n_units || cb.i < n_units) {
-        if (ca.i < n_units && (cb.i >= n_units || ja - jb < kSA - kSB)) {
-          const int s = ja % kSA;
-          if (ja >= kSA) bounded_wait(&emptyA[s], (uint32_t)((ja / kSA - 1) & 1), p.status);
-          uint8_t* sb = astg + (size_t)s * kAStage;
-          mbar_arrive_expect_tx(&fullA[s], (uint32_t)kTcBlockBytes);
-          bulk_g2s(sb, ca.g.w + (size_t)ca.ks * kTcBlockBytes, kTcCodeBytes, &fullA[s]);
-          bulk_g2s(sb + kAOp, ca.g.w + (size_t)ca.ks * kTcBlockBytes + kTcCodeBytes, 512, &fullA[s]);
-          ++ja;
-          cursor_next<kDown>(p, st, ca, n_units);
-        } else {
-          const int s = jb % kSB;
-          if (jb >= kSB) bounded_wait(&emptyB[s], (uint32_t)((jb / kSB - 1) & 1), p.status);
-          const int N = M::kPlanes * npad_of(cb.g.n);
-          uint8_t* sb = bstg + (size_t)s * M::kPanelStep;
-          // panels of every slot use the stride of the largest K step count
-          const int pstride = kDown ? tc_ksteps(p.F > p.S ? p.F : p.S) : tc_ksteps(p.d);
-          const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
-          mbar_arrive_expect_tx(&fullB[s], (uint32_t)(N * kTcStepK + 32 * 4 * M::kSfWords));
-          bulk_g2s(sb, src, (uint32_t)(N * kTcStepK), &fullB[s]);
-          bulk_g2s(sb + M::kPanelRows * kTcStepK, src + M::kPanelRows * kTcStepK, 32 * 4 * M::kSfWords, &fullB[s]);
-          ++jb;
-          cursor_next<kDown>(p, st, cb, n_units);
-        }
-      }
-    }
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
-    const int ct = tid - kConvWarp0 * 32, q = warp & 3;
-    int j = 0;
-    for (int i = 0; i < n_units; ++i) {
-      const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
-      for (int ks = 0; ks < g.nks; ++ks, ++j) {
-        const int sa = j % kSA, sbi = j % kSB;
-        bounded_wait(&fullA[sa], (uint32_t)((j / kSA) & 1), p.status);
-        bounded_wait(&fullB[sbi], (uint32_t)((j / kSB) & 1), p.status);
-        uint8_t* ap = astg + (size_t)sa * kAStage;
-        const uint8_t* sb_p = bstg + (size_t)sbi * M::kPanelStep;
-        // widen in place: every converter thread reads its packed chunks, then
-        // (after the converters' barrier) writes each 8 bytes into its 16-byte slot
-        uint4 v[kTcCodeBytes / 16 / 128];
-#pragma unroll
-        for (int r = 0; r < kTcCodeBytes / 16 / 128; ++r) v[r] = *reinterpret_cast<const uint4*>(ap + 16 * (ct + 128 * r));
-        const uint4 wa = *reinterpret_cast<const uint4*>(ap + kAOp + 16 * lane);
-        const uint4 wb0 = *reinterpret_cast<const uint4*>(sb_p + M::kPanelRows * kTcStepK + 4 * M::kSfWords * lane);
-        uint4 wb1 = make_uint4(0, 0, 0, 0);
-        if (kDown) wb1 = *reinterpret_cast<const uint4*>(sb_p + M::kPanelRows * kTcStepK + 4 * M::kSfWords * lane + 16);
-        named_bar(2, 128);
-#pragma unroll
-        for (int r = 0; r < kTcCodeBytes / 16 / 128; ++r) {
-          const int o = ct + 128 * r;  // 16 code bytes = two 8-byte row chunks
-          *reinterpret_cast<uint4*>(ap + 32 * o) = make_uint4(v[r].x, v[r].y, 0u, 0u);
-          *reinterpret_cast<uint4*>(ap + 32 * o + 16) = make_uint4(v[r].z, v[r].w, 0u, 0u);
-        }
-        // scale set sa: free, the MMAs of the stage's previous step completed before it was refilled
-        const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + kSfCol + 16 * sa;
-        tc::st4(lanebase, wa.x, wa.y, wa.z, wa.w);
-        tc::st4(lanebase + 8, wb0.x, wb0.y, wb0.z, wb0.w);
-        if (kDown) tc::st4(lanebase + 12, wb1.x, wb1.y, wb1.z, wb1.w);
-        tc::wait_st();
-        tc::fence_proxy_async();
-        tc::fence_before();
-        mbar_arrive(&ready[sa]);
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      int j = 0;
-      for (int i = 0; i < n_units; ++i) {
-        const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
-        const int N = M::kPlanes * npad_of(g.n), acc = i & 1;
-        if (i >= 2) bounded_wait(&accempty[acc], (uint32_t)((i / 2 - 1) & 1), p.status);
-        tc::fence_after();
-        for (int ks = 0; ks < g.nks; ++ks, ++j) {
-          const int sa = j % kSA;
-          bounded_wait(&ready[sa], (uint32_t)((j / kSA) & 1), p.status);
-          tc::fence_after();
-          const uint8_t* ab = astg + (size_t)sa * kAStage;
-          const uint8_t* bb = bstg + (size_t)(j % kSB) * M::kPanelStep;
-          const uint32_t sf = tmem + kSfCol + 16 * sa;
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const uint64_t ad = tc::smem_desc(ab + 2 * kb * 128, 128, 8 * 128);
-            const uint64_t bd = tc::smem_desc(bb + 2 * kb * 128, 128, 8 * 128);
-            tc::mma_mxf4_mxf8(tmem + kDCol * acc, ad, bd, tc::idesc_mxf4_mxf8(128, N, kb, kb), sf, sf + 8,
-                              (ks > 0 || kb > 0) ? 1u : 0u);
-          }
-          tc::commit(&emptyA[sa]);
-          tc::commit(&emptyB[j % kSB]);
-        }
-        tc::commit(&accfull[acc]);
-      }
-    }
-  } else if (warp >= kEpiWarp0) {
-    const int qd = warp & 3;
-    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-    for (int i = 0; i < n_units; ++i) {
-      const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
-      const int npad = npad_of(g.n), acc = i & 1;
-      bounded_wait(&accfull[acc], (uint32_t)((i / 2) & 1), p.status);
-      tc::fence_after();
-      const uint32_t dcol = trow + kDCol * acc;
-      if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
-        const int row = 128 * g.mt + 32 * qd + lane;
-        for (int c0 = 0; c0 < npad; c0 += 16) {
-          float v[16], w[16];
-          tc::ld16(dcol + c0, v);
-#pragma unroll
-          for (int pl = 1; pl < 4; ++pl) {
-            tc::ld16(dcol + pl * npad + c0, w);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) v[x] += w[x];
-          }
-          if (row < p.d) {
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-              if (c0 + x < g.n) p.part[(size_t)(g.q0 + c0 + x) * p.d + row] = v[x];
-          }
-        }
-      } else {
-        if (qd >= 2) {  // up rows 64 + 32 (qd - 2) + lane -> shared memory
-          for (int c0 = 0; c0 < npad; c0 += 16) {
-            float hi[16], lo[16];
-            tc::ld16(dcol + c0, hi);
-            tc::ld16(dcol + npad + c0, lo);
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-              if (c0 + x < g.n) upx[(32 * (qd - 2) + lane) * kMaxTok + c0 + x] = hi[x] + lo[x];
-          }
-        }
-        named_bar(1, 128);
-        if (qd < 2) {  // gate rows 32 qd + lane: pair tile 4 mt + 2 qd + lane / 16, row lane % 16
-          const int tau = 4 * g.mt + 2 * qd + (lane >> 4), r = lane & 15;
-          const bool valid = tau < g.f / 16;
-          for (int c0 = 0; c0 < npad; c0 += 16) {
-            float hi[16], lo[16];
-            tc::ld16(dcol + c0, hi);
-            tc::ld16(dcol + npad + c0, lo);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              const int m = c0 + x;
-              if (m >= g.n) break;  // uniform over the warp
-              const float gate = hi[x] + lo[x];
-              const float up = upx[(32 * qd + lane) * kMaxTok + m];
-              const float h = gate / (1.f + expf(-gate)) * up;
-              float mx = fabsf(h);
-              for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-              if (valid) {
-                const int qq = g.q0 + m;
-                const int sh = f16_headroom_exponent(mx);
-                __half* hh = reinterpret_cast<__half*>(p.hbuf) + (size_t)qq * 2 * p.fmax64;
-                const int ii = 32 * (tau >> 1) + 8 * (r >> 2) + 4 * (tau & 1) + (r & 3);
-                const float v = h * pow2f(sh);
-                const __half vh = __float2half_rn(v);
-                hh[ii] = vh;
-                hh[p.fmax64 + ii] = __float2half_rn(v - __half2float(vh));
-                if (r == 0) p.hscale[(size_t)qq * p.hgroups + tau] = pow2f(-sh);
-              }
-            }
-          }
-        }
-      }
-      tc::fence_before();
-      named_bar(1, 128);  // the up buffer and this accumulator are free
-      mbar_arrive(&accempty[acc]);
-    }
-  }
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc::fence_after();
-    tc::dealloc(tmem, kTmemCols);
   }
 }
 
@@ -418,44 +199,291 @@ __device__ __forceinline__ void split_planes(float v, uint32_t (&code)[kPl], uin
   }
 }
 
-// h panels of the down step: one CTA per (panel, K step over f), a warp per
-// (token row m, 32-element block b of the step), a lane per element. h comes
-// from its f16 hi + lo planes and their per-pair-tile scale.
-__global__ void __launch_bounds__(256) pack_h_panels_kernel(FwdParams p) {
-  const int pb = blockIdx.x, ks = blockIdx.y;
-  const int ns = *p.n_slots;
-  if (pb >= p.panel_prefix[ns]) return;
-  const int s = find_unit_slot(p.panel_prefix, ns, pb);
-  const int tb = pb - p.panel_prefix[s];
-  const int f = (p.slot_expert[s] == p.E) ? p.S : p.F, nks = tc_ksteps(f);
-  if (ks >= nks) return;
-  const int n = min(kMaxTok, p.slot_n[s] - kMaxTok * tb), q0 = p.slot_q0[s] + kMaxTok * tb, npad = npad_of(n);
-  uint8_t* dst = p.hpanel + ((size_t)pb * tc_ksteps(p.F > p.S ? p.F : p.S) + ks) * kTcPanelStepD;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int o = warp; o < npad * 4; o += 8) {
-    const int m = o >> 2, b = o & 3, k = kTcStepK * ks + 32 * b + lane;
-    float h = 0.f;
-    if (m < n && k < f) {
-      const int q = q0 + m;
-      const __half* hh = reinterpret_cast<const __half*>(p.hbuf) + (size_t)q * 2 * p.fmax64;
-      // the scale of h is per pair tile: element k belongs to pair tile 2 (k / 32) + (k / 4) % 2
-      h = (__half2float(hh[k]) + __half2float(hh[p.fmax64 + k])) *
-          p.hscale[(size_t)q * p.hgroups + 2 * (k >> 5) + ((k >> 2) & 1)];
-    }
-    uint32_t code[4], sc[4];
-    split_planes<4>(h, code, sc);
+
+// Split the 32 values of a block (one per lane) into 4 MXFP8 planes with one
+// reduction: plane 0 takes the block maximum into [128, 256) as above; every
+// later plane's scale is the previous one divided by 32. An E4M3 code of a
+// value below 256 errs by at most 8 (half its spacing there), so a plane's
+// remainder, scaled by 32, stays at most 256 and fits the next plane; after
+// the 4 planes the error is below 2^-19 of the block maximum.
+__device__ __forceinline__ void split_planes4_fixed(float v, uint32_t (&code)[4], uint32_t (&sc)[4]) {
+  float amax = fabsf(v);
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
 #pragma unroll
-    for (int pl = 0; pl < 4; ++pl) {
-      const int row = pl * npad + m;
-      dst[((row >> 3) * 8 + 2 * b + (lane >> 4)) * 128 + (row & 7) * 16 + (lane & 15)] = (uint8_t)code[pl];
-      // scale byte b of the word of B row `row`: word (lane row % 32, r row / 32)
-      if (lane == 0) dst[kTcPanelRowsD * kTcStepK + 4 * 8 * (row & 31) + 4 * (row >> 5) + b] = (uint8_t)sc[pl];
+  for (int pl = 0; pl < 4; ++pl) {
+    const int s = max(-127, min(127, sh));
+    const float ish = __uint_as_float((uint32_t)(127 - s) << 23), fsh = __uint_as_float((uint32_t)(127 + s) << 23);
+    uint16_t c2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(0.f), "f"(v * ish));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    code[pl] = c2 & 0xFFu;
+    v -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;
+    sc[pl] = (uint32_t)(s + 127);
+    sh -= 5;
+  }
+}
+
+template <bool kDown>
+__global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap wmap) {
+  using M = Mode<kDown>;
+  constexpr int kS = M::kS, kMma = M::kMma;
+  extern __shared__ __align__(1024) uint8_t sm[];
+  uint8_t* stg = sm;                                               // [kS][A stage | B panel step]
+  float* hx = reinterpret_cast<float*>(stg + (size_t)kS * M::kStage);  // gate/up: [4][kMaxTok][32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(hx) + M::kEpiSmem);
+  uint64_t* full = bars;                  // both operands of the stage landed (two producers)
+  uint64_t* empty = full + kS;            // the MMAs reading the stage completed
+  uint64_t* accfull = empty + kS;         // [2] every MMA lane's part of the buffer's unit completed
+  uint64_t* accempty = accfull + 2;       // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
+  int* tab = reinterpret_cast<int*>(tslot + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = *p.n_slots;
+  const int total = (kDown ? p.dn_prefix : p.gu_prefix)[ns];
+  const int n_units = total > (int)blockIdx.x ? (total - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  if (n_units == 0) return;
+  SlotTab st;
+  st.ns = ns;
+  st.upre = tab;
+  st.ppre = tab + (p.E + 2);
+  st.sexp = tab + 2 * (p.E + 2);
+  st.sq0 = tab + 3 * (p.E + 2);
+  st.sn = tab + 4 * (p.E + 2);
+  for (int i = tid; i <= ns; i += kThr) {
+    tab[i] = (kDown ? p.dn_prefix : p.gu_prefix)[i];
+    tab[(p.E + 2) + i] = p.panel_prefix[i];
+    if (i < ns) {
+      tab[2 * (p.E + 2) + i] = p.slot_expert[i];
+      tab[3 * (p.E + 2) + i] = p.slot_q0[i];
+      tab[4 * (p.E + 2) + i] = p.slot_n[i];
     }
   }
-  // scale bytes of rows past the block's 4 npad rows (the words the MMA reads: r < 8)
-  for (int o = threadIdx.x; o < 32 * 8 * 4; o += 256) {
-    const int l = o >> 5, r = (o >> 2) & 7, bb = o & 3, row = 32 * r + l;
-    if (row >= 4 * npad) dst[kTcPanelRowsD * kTcStepK + 4 * 8 * l + 4 * r + bb] = 127;
+  // the tensor copies write the first 8 bytes of every 16-byte operand row;
+  // the other 8 stay as set here
+  for (int c = tid; c < kS * (kAOp / 16); c += kThr)
+    *reinterpret_cast<uint2*>(stg + (size_t)(c / (kAOp / 16)) * M::kStage + 16 * (c % (kAOp / 16)) + 8) =
+        make_uint2(0u, 0u);
+  tc::fence_proxy_async();
+  if (tid == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accfull[a], kMma);
+      mbar_init(&accempty[a], kEpiThreads);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const int G = gridDim.x, b0 = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      Cursor<kDown> ca, cp;
+      ca.i = cp.i = 0;
+      ca.ks = cp.ks = 0;
+      ca.g = cp.g = tc_unit<kDown>(p, st, b0);
+      // weight blocks are read once: start them towards L2 kPf steps before their tensor copy
+      for (int q = 0; q < kPf && cp.i < n_units; ++q) {
+        prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
+        cursor_next<kDown>(p, st, cp, n_units);
+      }
+      for (int j = 0; ca.i < n_units; ++j) {
+        const int s = j % kS;
+        if (j >= kS) bounded_wait(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        uint8_t* sb = stg + (size_t)s * M::kStage;
+        // 8,192 code bytes (counted as read from global memory) + 512 scale bytes
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kTcBlockBytes);
+        tc::tma_load_2d(sb, &wmap, 0, ca.g.y + ca.ks * kCmRows, &full[s]);
+        bulk_g2s(sb + kAOp, ca.g.w + (size_t)ca.ks * kTcBlockBytes + kTcCodeBytes, 512, &full[s]);
+        if (cp.i < n_units) {
+          prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
+          cursor_next<kDown>(p, st, cp, n_units);
+        }
+        cursor_next<kDown>(p, st, ca, n_units);
+      }
+    }
+  } else if (warp == kPanelWarp) {
+    if (lane == 0) {
+      Cursor<kDown> cb;
+      cb.i = 0;
+      cb.ks = 0;
+      cb.g = tc_unit<kDown>(p, st, b0);
+      // panels of every slot use the stride of the largest K step count
+      const int pstride = kDown ? tc_ksteps(p.F > p.S ? p.F : p.S) : tc_ksteps(p.d);
+      for (int j = 0; cb.i < n_units; ++j) {
+        const int s = j % kS;
+        if (j >= kS) bounded_wait(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        const int N = M::kPlanes * npad_of(cb.g.n);
+        uint8_t* sb = stg + (size_t)s * M::kStage + kAStage;
+        const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(N * kTcStepK + 512 * M::kSfBlocks));
+        bulk_g2s(sb, src, (uint32_t)(N * kTcStepK), &full[s]);
+        bulk_g2s(sb + M::kPanelRows * kTcStepK, src + M::kPanelRows * kTcStepK, 512 * M::kSfBlocks, &full[s]);
+        cursor_next<kDown>(p, st, cb, n_units);
+      }
+    }
+  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMma) {
+    if (lane == 0) {
+      const int t = warp - kMmaWarp0;
+      int jtot = 0;  // K steps of the CTA
+      for (int i = 0; i < n_units; ++i) jtot += tc_unit<kDown>(p, st, b0 + i * G).nks;
+      // scale factors of stage s -> set s, issued one own step ahead of that step's MMAs
+      auto load_sf = [&](int jj) {
+        const int s = jj % kS;
+        bounded_wait(&full[s], (uint32_t)((jj / kS) & 1), p.status);
+        tc::fence_after();
+        const uint8_t* sb = stg + (size_t)s * M::kStage;
+        const uint32_t sf = tmem + kSfCol + 16 * s;
+        tc::cp_32x128b_x4(sf, tc::smem_desc(sb + kAOp, 128, 128));
+#pragma unroll
+        for (int h = 0; h < M::kSfBlocks; ++h)
+          tc::cp_32x128b_x4(sf + 8 + 4 * h,
+                            tc::smem_desc(sb + kAStage + M::kPanelRows * kTcStepK + 512 * h, 128, 128));
+      };
+      if (t < jtot) load_sf(t);
+      int j0 = 0;  // first K step of unit i
+      for (int i = 0; i < n_units; ++i) {
+        const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
+        const int N = M::kPlanes * npad_of(g.n), acc = i & 1;
+        const int first = ((t - j0) % kMma + kMma) % kMma;  // this lane's first K step of the unit
+        if (first >= g.nks) tc::commit(&accfull[acc]);  // no K step of this unit
+        else if (i >= 2) bounded_wait(&accempty[acc], (uint32_t)((i / 2 - 1) & 1), p.status);
+        tc::fence_after();
+        const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
+        for (int ks = first; ks < g.nks; ks += kMma) {
+          const int jj = j0 + ks, s = jj % kS;
+          const uint8_t* ab = stg + (size_t)s * M::kStage;
+          const uint8_t* bb = ab + kAStage;
+          const uint32_t sf = tmem + kSfCol + 16 * s;
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint64_t ad = tc::smem_desc(ab + 2 * kb * 128, 128, 8 * 128);
+            const uint64_t bd = tc::smem_desc(bb + 2 * kb * 128, 128, 8 * 128);
+            tc::mma_mxf4_mxf8(d, ad, bd, tc::idesc_mxf4_mxf8(128, N, kb, kb), sf, sf + 8,
+                              (ks > first || kb > 0) ? 1u : 0u);
+          }
+          tc::commit(&empty[s]);
+          if (ks + kMma >= g.nks) tc::commit(&accfull[acc]);  // this lane's last K step of the unit
+          if (jj + kMma < jtot) load_sf(jj + kMma);
+        }
+        j0 += g.nks;
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31; the two warps of a
+    // quadrant take alternate 16-column chunks
+    const int qd = warp & 3, eg = (warp - kEpiWarp0) >> 2, ew = warp - kEpiWarp0, et = tid - kEpiWarp0 * 32;
+    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+    // gate/up: TMEM lane l of a quadrant is f offset kk(l) within its 32-element block
+    const int kk = 8 * ((lane & 15) >> 2) + 4 * (lane >> 4) + (lane & 3);
+    const int pstride = tc_ksteps(p.F > p.S ? p.F : p.S);
+    int j0 = 0;
+    for (int i = 0; i < n_units; ++i) {
+      const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
+      const int npad = npad_of(g.n), acc = i & 1;
+      // MMA lanes with at least one K step of this unit
+      const int nacc = g.nks >= kMma ? kMma : g.nks;
+      const int t0 = j0 % kMma;  // the lane of the unit's first K step
+      j0 += g.nks;
+      bounded_wait(&accfull[acc], (uint32_t)((i / 2) & 1), p.status);
+      tc::fence_after();
+      if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
+        const int row = 128 * g.mt + 32 * qd + lane;
+        for (int c0 = 16 * eg; c0 < npad; c0 += 32) {
+          float v[16], w[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+          for (int a = 0; a < nacc; ++a) {
+            const uint32_t dcol = trow + M::kDCol * (kMma * acc + (t0 + a) % kMma);
+#pragma unroll
+            for (int pl = 0; pl < 4; ++pl) {
+              tc::ld16(dcol + pl * npad + c0, w);
+#pragma unroll
+              for (int x = 0; x < 16; ++x) v[x] += w[x];
+            }
+          }
+          if (row < p.d) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              if (c0 + x < g.n) p.part[(size_t)(g.q0 + c0 + x) * p.d + row] = v[x];
+          }
+        }
+        tc::fence_before();
+        mbar_arrive(&accempty[acc]);
+      } else {
+        // 1. accumulators -> hx[block][token][f offset]: blocks 0, 1 gate, 2, 3 up
+        named_bar(1, kEpiThreads);  // the previous unit's readers of hx are done
+        for (int c0 = 16 * eg; c0 < npad; c0 += 32) {
+          float v[16], w[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+          for (int a = 0; a < nacc; ++a) {
+            const uint32_t dcol = trow + M::kDCol * (kMma * acc + (t0 + a) % kMma);
+#pragma unroll
+            for (int pl = 0; pl < 2; ++pl) {
+              tc::ld16(dcol + pl * npad + c0, w);
+#pragma unroll
+              for (int x = 0; x < 16; ++x) v[x] += w[x];
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            if (c0 + x < npad) hx[(qd * kMaxTok + c0 + x) * 32 + kk] = v[x];
+        }
+        tc::fence_before();
+        mbar_arrive(&accempty[acc]);  // the accumulator buffer is free for the unit after next
+        named_bar(1, kEpiThreads);
+        // 2. h = SiLU(gate) * up, four MXFP8 planes, straight into the down step's
+        // h panel: f block 2 mt + b is K step mt / 2, elements 64 (mt % 2) + 32 b ..
+        uint8_t* dst = p.hpanel + ((size_t)g.panel * pstride + (g.mt >> 1)) * kTcPanelStepD;
+        const int kh = 64 * (g.mt & 1), nblk = g.f / 32;
+        for (int it = ew; it < 2 * npad; it += kEpiThreads / 32) {
+          const int m = it >> 1, b = it & 1;
+          float h = 0.f;
+          if (m < g.n && 2 * g.mt + b < nblk) {
+            const float gate = hx[(b * kMaxTok + m) * 32 + lane], up = hx[((2 + b) * kMaxTok + m) * 32 + lane];
+            h = gate / (1.f + __expf(-gate)) * up;
+          }
+          uint32_t code[4], sc[4];
+          split_planes4_fixed(h, code, sc);
+          const int k = kh + 32 * b + lane;
+#pragma unroll
+          for (int pl = 0; pl < 4; ++pl) {
+            const int row = pl * npad + m;
+            dst[((row >> 3) * 8 + (k >> 4)) * 128 + (row & 7) * 16 + (k & 15)] = (uint8_t)code[pl];
+          }
+          if (lane < 4) {
+            const uint32_t s = lane == 0 ? sc[0] : lane == 1 ? sc[1] : lane == 2 ? sc[2] : sc[3];
+            dst[hsf_off(lane * npad + m, 2 * (g.mt & 1) + b)] = (uint8_t)s;
+          }
+        }
+        // 3. scale bytes of the rows past the 4 planes (127), and the half K step
+        // past the last M tile when the tile count is odd (codes 0, scales 127)
+        for (int o = et; o < 2 * (kTcPanelRowsD - 4 * npad); o += kEpiThreads)
+          dst[hsf_off(4 * npad + (o >> 1), 2 * (g.mt & 1) + (o & 1))] = 127;
+        if ((g.mt & 1) == 0 && g.mt + 1 == tc_msteps(g.f)) {
+          for (int o = et; o < 4 * npad * 4; o += kEpiThreads) {
+            const int row = o >> 2, kc = 4 + (o & 3);
+            *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          for (int o = et; o < 2 * kTcPanelRowsD; o += kEpiThreads) dst[hsf_off(o >> 1, 2 + (o & 1))] = 127;
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
   }
 }
 
@@ -583,33 +611,57 @@ cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_
 }
 
 cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(tc_smem_fixed<false>() + tc_table_bytes(512)));
+  static size_t configured = 0;
+  const size_t smem = tc_gemm_smem_bytes(p.E, false);
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured = smem;
   }
   prep_xq_kernel<<<(p.T * p.xq_spitch + 7) / 8, 256, 0, stream>>>(p);
   // panels: at most ceil(Q / 48) + slots blocks (the kernels skip the ones past the count)
   const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
   pack_panels_kernel<<<dim3(max_panels, tc_ksteps(p.d)), 256, 0, stream>>>(p);
-  gemm_tc_kernel<false><<<num_sms, kThr, tc_smem_fixed<false>() + tc_table_bytes(p.E), stream>>>(p);
+  gemm_tc_kernel<false><<<num_sms, kThr, smem, stream>>>(p, *static_cast<const CUtensorMap*>(p.tmap_gu));
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(tc_smem_fixed<true>() + tc_table_bytes(512)));
+  static size_t configured = 0;
+  const size_t smem = tc_gemm_smem_bytes(p.E, true);
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured = smem;
   }
-  const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
-  pack_h_panels_kernel<<<dim3(max_panels, tc_ksteps(p.F > p.S ? p.F : p.S)), 256, 0, stream>>>(p);
-  gemm_tc_kernel<true><<<num_sms, kThr, tc_smem_fixed<true>() + tc_table_bytes(p.E), stream>>>(p);
+  gemm_tc_kernel<true><<<num_sms, kThr, smem, stream>>>(p, *static_cast<const CUtensorMap*>(p.tmap_dn));
   return cudaGetLastError();
+}
+
+size_t tc_gemm_smem_bytes(int E, bool down) {
+  return (down ? tc_smem_fixed<true>() : tc_smem_fixed<false>()) + tc_table_bytes(E);
+}
+
+// The weight copy as a 2-D tensor of "16 x U4, 16-byte aligned" elements:
+// rows of 128 codes (64 bytes: one core matrix of 8 rows x 16 codes), so that
+// a box of 128 rows is the 8,192 code bytes of one block, widened on the way
+// into shared memory.
+bool encode_tc_weight_map(const void* base, size_t bytes, void* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (bytes % 64 != 0 || bytes / 64 >= (1ull << 31)) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 64)}, strides[1] = {64};
+  const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
+  return encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace moe
