@@ -63,8 +63,9 @@ constexpr int kProducerWarp = 0, kMmaWarp0 = 1, kPanelWarp = 3, kEpiWarp0 = 4, k
 // part = D. A stage holds one K step of both operands: [A | B panel step].
 // With kMma MMA lanes, lane t takes the CTA's K steps j = t (mod kMma) and
 // accumulates them in its own accumulator of the unit's buffer (the epilogue
-// adds them): one lane cannot issue MMAs of N <= 96 as fast as the tensor
-// core runs them.
+// adds them): one lane, which also waits for stages and copies scale
+// factors, cannot issue MMAs as fast as the tensor core runs them. The down
+// step's wider accumulators leave room for one buffer only.
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
@@ -73,10 +74,11 @@ struct Mode {
   static constexpr int kSfBlocks = kDown ? 2 : 1;  // 512-byte B scale blocks per panel step (32 rows x 4 words each)
   static constexpr int kStage = kAStage + kPanelStep;
   static constexpr int kS = kDown ? 5 : 6;         // stages (scale sets in TMEM: at most 8)
-  static constexpr int kMma = kDown ? 1 : 2;       // MMA lanes
+  static constexpr int kMma = 2;                   // MMA lanes
   static constexpr int kDCol = kDown ? 192 : 96;   // accumulator width (N <= kDCol); buffer b, lane t at kDCol (kMma b + t)
+  static constexpr int kBufs = kDown ? 1 : 2;      // accumulator buffers (units in flight between MMA and epilogue)
   static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values [4 blocks][token][32]
-  static_assert(2 * kMma * kDCol <= kSfCol && kS <= 8, "TMEM columns");
+  static_assert(kBufs * kMma * kDCol <= kSfCol && kS <= 8, "TMEM columns");
 };
 
 // Per-slot tables the roles look units up in, copied to shared memory once:
@@ -228,15 +230,15 @@ __device__ __forceinline__ void split_planes4_fixed(float v, uint32_t (&code)[4]
 template <bool kDown>
 __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap wmap) {
   using M = Mode<kDown>;
-  constexpr int kS = M::kS, kMma = M::kMma;
+  constexpr int kS = M::kS, kMma = M::kMma, kBufs = M::kBufs;
   extern __shared__ __align__(1024) uint8_t sm[];
   uint8_t* stg = sm;                                               // [kS][A stage | B panel step]
   float* hx = reinterpret_cast<float*>(stg + (size_t)kS * M::kStage);  // gate/up: [4][kMaxTok][32]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(hx) + M::kEpiSmem);
   uint64_t* full = bars;                  // both operands of the stage landed (two producers)
   uint64_t* empty = full + kS;            // the MMAs reading the stage completed
-  uint64_t* accfull = empty + kS;         // [2] every MMA lane's part of the buffer's unit completed
-  uint64_t* accempty = accfull + 2;       // [2]
+  uint64_t* accfull = empty + kS;         // [kBufs] every MMA lane's part of the buffer's unit completed
+  uint64_t* accempty = accfull + 2;       // [kBufs]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   int* tab = reinterpret_cast<int*>(tslot + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kBufs; ++a) {
       mbar_init(&accfull[a], kMma);
       mbar_init(&accempty[a], kEpiThreads);
     }
@@ -352,10 +354,10 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       int j0 = 0;  // first K step of unit i
       for (int i = 0; i < n_units; ++i) {
         const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
-        const int N = M::kPlanes * npad_of(g.n), acc = i & 1;
+        const int N = M::kPlanes * npad_of(g.n), acc = i % kBufs;
         const int first = ((t - j0) % kMma + kMma) % kMma;  // this lane's first K step of the unit
         if (first >= g.nks) tc::commit(&accfull[acc]);  // no K step of this unit
-        else if (i >= 2) bounded_wait(&accempty[acc], (uint32_t)((i / 2 - 1) & 1), p.status);
+        else if (i >= kBufs) bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status);
         tc::fence_after();
         const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
         for (int ks = first; ks < g.nks; ks += kMma) {
@@ -388,12 +390,12 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     int j0 = 0;
     for (int i = 0; i < n_units; ++i) {
       const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
-      const int npad = npad_of(g.n), acc = i & 1;
+      const int npad = npad_of(g.n), acc = i % kBufs;
       // MMA lanes with at least one K step of this unit
       const int nacc = g.nks >= kMma ? kMma : g.nks;
       const int t0 = j0 % kMma;  // the lane of the unit's first K step
       j0 += g.nks;
-      bounded_wait(&accfull[acc], (uint32_t)((i / 2) & 1), p.status);
+      bounded_wait(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status);
       tc::fence_after();
       if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
         const int row = 128 * g.mt + 32 * qd + lane;
