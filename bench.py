@@ -451,7 +451,7 @@ def main(argv=None):
     ap.add_argument("--kernel-steps", type=int, default=3, help="eager steps for per-kernel event timing")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 4: tcgen05 gate/up)")
+    ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 8: register-decode GEMMs instead of tcgen05)")
     args = ap.parse_args(argv)
     wl = synth.WORKLOADS[args.workload]
     if args.layers is None:

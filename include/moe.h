@@ -72,11 +72,15 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
  * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path that
  *   otherwise serves T > 16 (for testing both paths on the same shapes).
- * MOE_FLAG_TC_GATEUP makes the multi-kernel path run gate/up + SwiGLU as a
- *   block-scaled tcgen05 MMA (MXFP4 weights x two MXFP8 planes of x) instead
- *   of the register-decode tensor-core GEMM; same results within the bf16 and
- *   fp32 tolerances (experimental: currently slower). */
-enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u };
+ * The multi-kernel path runs both expert GEMMs as block-scaled tcgen05 MMAs
+ *   (MXFP4 weights x MXFP8 planes of x and of h) from a second copy of the
+ *   experts in the MMA's layout, made at load time, whenever t_max > 16 and
+ *   the shared-memory tables fit (n_experts up to about 400).
+ * MOE_FLAG_TC_GATEUP asks for those MMAs for every t_max (an error if the
+ *   tables do not fit); MOE_FLAG_NO_TC keeps the register-decode tensor-core
+ *   GEMMs instead (no second copy). Results agree within the bf16 and fp32
+ *   tolerances either way. */
+enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u, MOE_FLAG_NO_TC = 8u };
 
 typedef struct moe_config {
   int d;          /* hidden size; a multiple of 32 */
@@ -133,7 +137,11 @@ int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, i
                     void* stream);
 
 /* Debug export of the last forward's router logits as an unevaluated sum of
- * two fp32 numbers, logit = hi + lo (hi = fl(logit)): hi, lo fp32 [T][E]. */
+ * two fp32 numbers, logit = hi + lo: hi, lo fp32 [T][E]. The single-kernel
+ * path (T <= 16) computes every logit as a double-float sum (hi = fl(logit)).
+ * The multi-kernel path computes every logit in fp32 with an error bound and
+ * the double-float sum only for the experts that bound cannot rule out of the
+ * top k: those hold hi + lo as above, the others their fp32 value and lo = 0. */
 int moe_get_logits(moe_ctx* ctx, float* hi, float* lo, void* stream);
 
 /* Device status word of the context (0 = fine, else a MOE_ERR_* code set by a

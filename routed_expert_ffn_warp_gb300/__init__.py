@@ -33,6 +33,7 @@ MOE_OUT_F32 = 1
 MOE_FLAG_TEST_FORCE_TIMEOUT = 1
 MOE_FLAG_GENERAL_PATH = 2
 MOE_FLAG_TC_GATEUP = 4
+MOE_FLAG_NO_TC = 8
 
 EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",

@@ -93,10 +93,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   if (c.d <= 0 || c.d % 32 || c.ffn <= 0 || c.ffn % 32 || c.shared_ffn < 0 || c.shared_ffn % 32 ||
       c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
       c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) ||
-      (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH | MOE_FLAG_TC_GATEUP)))
+      (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH | MOE_FLAG_TC_GATEUP | MOE_FLAG_NO_TC)) ||
+      ((c.flags & MOE_FLAG_TC_GATEUP) && (c.flags & MOE_FLAG_NO_TC)))
     return fail(nullptr, MOE_ERR_INVALID_ARG,
                 "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
-                "0 <= t_max <= 65536; out_dtype 0/1; flags 0)");
+                "0 <= t_max <= 65536; out_dtype 0/1; known flags, not both TC_GATEUP and NO_TC)");
   moe_ctx* ctx = new (std::nothrow) moe_ctx();
   if (!ctx) return fail(nullptr, MOE_ERR_NOMEM, "host allocation failed");
   ctx->cfg = c;
@@ -115,11 +116,15 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const int d = c.d, F = c.ffn, E = c.n_experts, k = c.top_k, S = c.shared_ffn, Tm = std::max(c.t_max, 1);
   ctx->expert_stride = moe::expert_packed_bytes(d, F);
   ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
-  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) != 0;
-  if (tc && std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) > (size_t)ctx->max_smem) {
+  const bool tc_fits =
+      std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) <= (size_t)ctx->max_smem;
+  if ((c.flags & MOE_FLAG_TC_GATEUP) && !tc_fits) {
     delete ctx;
     return fail(nullptr, MOE_ERR_INVALID_ARG, "too many experts for the tcgen05 GEMM's shared-memory tables");
   }
+  // the block-scaled tcgen05 GEMMs serve the multi-kernel path unless asked not to
+  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
+                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && c.t_max > moe::kDecodeMaxT);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
@@ -141,6 +146,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const int xq_spitch = (d64 / 32 + 3) / 4 * 4;
   const size_t o_xq = take((size_t)Tm * 2 * d64), o_xqs = take((size_t)Tm * 2 * xq_spitch);
   const size_t o_lh = take((size_t)Tm * E * 4), o_ll = take((size_t)Tm * E * 4);
+  const size_t o_xn = take((size_t)Tm * 4), o_wn = take((size_t)E * 4);
   const size_t o_ids = take(Pm * 4), o_gates = take(Pm * 4), o_counts = take((size_t)E * 4),
                o_offsets = take((size_t)(E + 1) * 4), o_perm = take(Pm * 4), o_inv = take(Pm * 4);
   const size_t o_ns = take(4), o_se = take((size_t)(E + 1) * 4), o_sq = take((size_t)(E + 1) * 4),
@@ -188,7 +194,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.fmax64 = fmax64;
   p.hgroups = hgroups;
   p.out_f32 = c.out_dtype == MOE_OUT_F32;
-  p.tc_gateup = (c.flags & MOE_FLAG_TC_GATEUP) ? 1 : 0;
+  p.tc_gateup = tc ? 1 : 0;
   p.w_router = ctx->w_router;
   p.bias = nullptr;
   p.packed = ctx->packed;
@@ -209,6 +215,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.xq_spitch = xq_spitch;
   p.logit_hi = reinterpret_cast<float*>(w + o_lh);
   p.logit_lo = reinterpret_cast<float*>(w + o_ll);
+  p.xnorm = reinterpret_cast<float*>(w + o_xn);
+  p.wnorm = reinterpret_cast<float*>(w + o_wn);
   p.ids = reinterpret_cast<int32_t*>(w + o_ids);
   p.gates = reinterpret_cast<float*>(w + o_gates);
   p.counts = reinterpret_cast<int32_t*>(w + o_counts);

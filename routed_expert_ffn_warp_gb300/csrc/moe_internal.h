@@ -121,6 +121,8 @@ struct FwdParams {
   int xq_spitch;         // scale bytes per plane row (a multiple of 4)
   float* logit_hi;       // [t_max][E]
   float* logit_lo;
+  float* xnorm;          // [t_max] upper bounds of |x_t|_2 (router error bounds)
+  float* wnorm;          // [E] upper bounds of |W_r[e]|_2
   int32_t* ids;          // [t_max][k]
   float* gates;          // [t_max][k]
   int32_t* counts;       // [E]

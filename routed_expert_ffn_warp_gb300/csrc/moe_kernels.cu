@@ -2,8 +2,9 @@
 //
 // Forward = seven stream-ordered steps:
 //   prep_x   per-token power-of-two scaling of x into f16 (exact for bf16 x)
-//   router   l[t,e] = W_r[e] . x_t + b[e] as a double-float (hi + lo) sum
-//   topk     warp top-k with lower-index tie break, softmax gates over the k
+//   router   l[t,e] = W_r[e] . x_t + b[e] in fp32, with an error bound
+//   topk     candidates from the bounds, their logits as double-float (hi + lo)
+//            sums, warp top-k with lower-index tie break, softmax gates
 //   bucket   counting sort of the T*k pairs by expert, and the work list
 //   gateup   grouped MXFP4 GEMM on tensor cores: h = SiLU(gate) * up (moe_gemm.cu)
 //   down     grouped MXFP4 GEMM: part = W_down h (moe_gemm.cu)
@@ -59,53 +60,128 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
 
 // ---------------------------------------------------------------- router
 
-// Block (e, token tile of 16): lanes stride over d in groups of 8 elements,
-// accumulate double-float sums, then a fixed-shape block reduction.
-constexpr int kRouterThreads = 128;
-constexpr int kRouterTT = 16;
+// The router in two passes. Pass 1 (router_fp32_kernel): every logit in fp32
+// by fused multiply-adds, 64 elements of d per partial sum, the partial sums
+// added in order, then the bias: a sum in which every product passes at most
+// D = 64 + ceil(d / 64) roundings, so |fp32 - exact| <= gamma_D sum|x_i w_i|
+// + 2^-23 |logit| with gamma_D = D u / (1 - D u), u = 2^-24, and
+// sum|x_i w_i| <= |x|_2 |w_e|_2 (Cauchy-Schwarz); the same pass bounds the
+// two norms from above. Pass 2 (topk_kernel): per token, the k-th largest
+// lower bound decides which experts can still be among the top k; only those
+// get the double-float logit, and the top k, the order and the gates come from
+// those values alone. The selection equals that of double-float logits for all
+// experts: an expert whose upper bound is below the k-th largest lower bound
+// is beaten by at least k others.
+constexpr int kRfTok = 32, kRfExp = 32, kRfK = 64, kRfThreads = 128;
 
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(FwdParams p) {
-  const int e = blockIdx.x;
-  const int t0 = blockIdx.y * kRouterTT;
-  const int nt = min(kRouterTT, p.T - t0);
-  dd acc[kRouterTT];
+__device__ __forceinline__ float router_gamma(int d) {
+  const float D = (float)(kRfK + (d + kRfK - 1) / kRfK);
+  return D * 0x1p-24f / (1.f - D * 0x1p-24f);
+}
+
+// Block (32 tokens, 32 experts); thread (token pair tid / 8, expert quad tid % 8).
+__global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
+  __shared__ __align__(16) float xs[kRfK][kRfTok + 4];  // [k][token]
+  __shared__ __align__(16) float ws[kRfK][kRfExp + 4];  // [k][expert]
+  const int tid = threadIdx.x, t0 = blockIdx.x * kRfTok, e0 = blockIdx.y * kRfExp;
+  const int tt = tid >> 3, te = tid & 7;
+  float tot[2][4] = {};
+  float xsq[2] = {0.f, 0.f}, wsq[4] = {0.f, 0.f, 0.f, 0.f};  // sums of squares of the rows this thread loads
+  for (int kc = 0; kc < p.d; kc += kRfK) {
+    for (int j = 0; j < 2; ++j) {  // x: 32 tokens x 64 elements, 8 per load
+      const int r = tid + kRfThreads * j, tok = r >> 3, k8 = (r & 7) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (t0 + tok < p.T && kc + k8 < p.d) v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + tok) * p.d + kc + k8));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < kRouterTT; ++i) acc[i] = dd{0.f, 0.f};
+      for (int q = 0; q < 4; ++q) {
+        const float a = __uint_as_float(w4[q] << 16), b = __uint_as_float(w4[q] & 0xFFFF0000u);
+        xs[k8 + 2 * q][tok] = a;
+        xs[k8 + 2 * q + 1][tok] = b;
+        s = fmaf(a, a, s);
+        s = fmaf(b, b, s);
+      }
+      xsq[j] += s;
+    }
+    for (int j = 0; j < 4; ++j) {  // w: 32 experts x 64 elements, 4 per load
+      const int r = tid + kRfThreads * j, ex = r >> 4, k4 = (r & 15) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + ex < p.E && kc + k4 < p.d) v = __ldg(reinterpret_cast<const float4*>(p.w_router + (size_t)(e0 + ex) * p.d + kc + k4));
+      ws[k4][ex] = v.x;
+      ws[k4 + 1][ex] = v.y;
+      ws[k4 + 2][ex] = v.z;
+      ws[k4 + 3][ex] = v.w;
+      wsq[j] += fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+    }
+    __syncthreads();
+    float c[2][4] = {};
+#pragma unroll 16
+    for (int k = 0; k < kRfK; ++k) {
+      const float2 xv = *reinterpret_cast<const float2*>(&xs[k][2 * tt]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[k][4 * te]);
+      const float xa[2] = {xv.x, xv.y}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) c[a][b] = fmaf(xa[a], wa[b], c[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) tot[a][b] += c[a][b];
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const int t = t0 + 2 * tt + a;
+    if (t >= p.T) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int e = e0 + 4 * te + b;
+      if (e < p.E) p.logit_hi[(size_t)t * p.E + e] = p.bias ? tot[a][b] + p.bias[e] : tot[a][b];
+    }
+  }
+  // norms, rounded up: the 8 (16) threads that loaded a token's (expert's) rows are adjacent lanes
+  const float up = 1.f + (float)(p.d / 8 + 16) * 0x1p-22f;
+  for (int j = 0; j < 2; ++j) {
+    float s = xsq[j];
+    for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int tok = (tid + kRfThreads * j) >> 3;
+    if (blockIdx.y == 0 && (tid & 7) == 0 && t0 + tok < p.T) p.xnorm[t0 + tok] = sqrtf(s * up) * up;
+  }
+  for (int j = 0; j < 4; ++j) {
+    float s = wsq[j];
+    for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int ex = (tid + kRfThreads * j) >> 4;
+    if (blockIdx.x == 0 && (tid & 15) == 0 && e0 + ex < p.E) p.wnorm[e0 + ex] = sqrtf(s * up) * up;
+  }
+}
+
+// Double-float logit of expert e for token t by one warp (the value of lane 0,
+// broadcast): lanes stride over d in groups of 8, then a fixed-shape tree.
+__device__ __forceinline__ dd warp_logit_dd(const FwdParams& p, int t, int e) {
+  const int lane = threadIdx.x & 31;
+  dd acc{0.f, 0.f};
   const float* w = p.w_router + (size_t)e * p.d;
-  for (int i8 = threadIdx.x; i8 < p.d / 8; i8 += kRouterThreads) {
+  const uint16_t* x = p.x + (size_t)t * p.d;
+  for (int i8 = lane; i8 < p.d / 8; i8 += 32) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + i8);
     const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8);
     const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8 + 1);
     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-    for (int tt = 0; tt < kRouterTT; ++tt) {
-      if (tt < nt) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + tt) * p.d) + i8);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dd_mac(acc[tt], __uint_as_float(xw[j] << 16), wv[2 * j]);
-          dd_mac(acc[tt], __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
-        }
-      }
+    for (int j = 0; j < 4; ++j) {
+      dd_mac(acc, __uint_as_float(xw[j] << 16), wv[2 * j]);
+      dd_mac(acc, __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
     }
   }
-  __shared__ dd part[kRouterThreads / 32][kRouterTT];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int tt = 0; tt < kRouterTT; ++tt) {
-    dd v = acc[tt];
-    for (int o = 16; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
-    if (lane == 0) part[warp][tt] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x < nt) {
-    const int tt = threadIdx.x;
-    dd v = part[0][tt];
-    for (int w2 = 1; w2 < kRouterThreads / 32; ++w2) v = dd_add(v, part[w2][tt]);
-    if (p.bias) v = dd_add(v, dd{p.bias[e], 0.f});
-    p.logit_hi[(size_t)(t0 + tt) * p.E + e] = v.hi;
-    p.logit_lo[(size_t)(t0 + tt) * p.E + e] = v.lo;
-  }
+  for (int o = 16; o; o >>= 1) acc = dd_add(acc, dd_shfl_xor(acc, o));
+  acc.hi = __shfl_sync(0xffffffffu, acc.hi, 0);
+  acc.lo = __shfl_sync(0xffffffffu, acc.lo, 0);
+  if (p.bias) acc = dd_add(acc, dd{p.bias[e], 0.f});
+  return acc;
 }
 
 // ---------------------------------------------------------------- top-k and gates
@@ -113,22 +189,81 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(FwdParams p) {
 constexpr int kTopkWarps = 8;
 constexpr int kMaxEPerLane = 16;  // E <= 512
 
-// One warp per token: k rounds of a warp arg-max over the double-float logits
-// (value first, then the lower expert index), then the softmax of the k.
+// One warp per token: the candidate set from the fp32 bounds, double-float
+// logits of the candidates, then k rounds of a warp arg-max over them (value
+// first, then the lower expert index) and the softmax of the k. The exported
+// logits (hi + lo) are the double-float values for the candidates and the
+// fp32 values (lo = 0) for the rest.
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(FwdParams p) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
   if (t >= p.T) return;
   const int E = p.E, k = p.k;
-  float vh[kMaxEPerLane], vl[kMaxEPerLane];
-  uint32_t taken = 0;
+  const float xb = router_gamma(p.d) * 1.01f * p.xnorm[t];
+  float vh[kMaxEPerLane], vl[kMaxEPerLane], lb[kMaxEPerLane], ub[kMaxEPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxEPerLane; ++i) {
     const int e = lane + 32 * i;
-    vh[i] = (e < E) ? p.logit_hi[(size_t)t * E + e] : -INFINITY;
-    vl[i] = (e < E) ? p.logit_lo[(size_t)t * E + e] : 0.f;
-    if (e >= E) taken |= 1u << i;
+    vh[i] = -INFINITY;
+    vl[i] = 0.f;
+    lb[i] = -INFINITY;
+    ub[i] = -INFINITY;
+    if (e < E) {
+      const float l = p.logit_hi[(size_t)t * E + e];
+      const float beta = fmaf(xb, p.wnorm[e], 0x1p-22f * fabsf(l)) + 0x1p-126f;
+      vh[i] = l;
+      lb[i] = l - beta;
+      ub[i] = l + beta;
+    }
   }
+  // the k-th largest lower bound
+  uint32_t taken = 0;
+  float kth = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    float b = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxEPerLane; ++i)
+      if (!((taken >> i) & 1u) && 32 * i + lane < E && (lb[i] > b || (lb[i] == b && 32 * i + lane < bi))) {
+        b = lb[i];
+        bi = 32 * i + lane;
+      }
+    for (int o = 16; o; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, b, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > b || (ob == b && oi < bi)) {
+        b = ob;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    kth = b;
+  }
+  // candidates: double-float logits
+  uint32_t cand = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxEPerLane; ++i) {
+    const bool c = 32 * i + lane < E && ub[i] >= kth;
+    if (c) cand |= 1u << i;
+    unsigned cm = __ballot_sync(0xffffffffu, c);
+    while (cm) {
+      const int l = __ffs(cm) - 1;
+      cm &= cm - 1;
+      const dd v = warp_logit_dd(p, t, l + 32 * i);
+      if (lane == l) {
+        vh[i] = v.hi;
+        vl[i] = v.lo;
+      }
+    }
+  }
+  for (int i = 0; i < kMaxEPerLane; ++i) {  // the exported logits
+    const int e = lane + 32 * i;
+    if (e < E) {
+      p.logit_hi[(size_t)t * E + e] = vh[i];
+      p.logit_lo[(size_t)t * E + e] = vl[i];
+    }
+  }
+  taken = ~cand;
   float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {
@@ -353,7 +488,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   if (p.T == 0) return cudaSuccess;
   if (events) cudaEventRecord(events[0], stream);
   prep_x_kernel<<<p.T, 256, 0, stream>>>(p);
-  router_kernel<<<dim3(p.E, (p.T + kRouterTT - 1) / kRouterTT), kRouterThreads, 0, stream>>>(p);
+  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp), kRfThreads, 0, stream>>>(p);
   topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   if (events) cudaEventRecord(events[1], stream);
@@ -370,7 +505,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
 
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  router_kernel<<<dim3(p.E, (p.T + kRouterTT - 1) / kRouterTT), kRouterThreads, 0, stream>>>(p);
+  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp), kRfThreads, 0, stream>>>(p);
   topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   return cudaGetLastError();

@@ -1,5 +1,5 @@
-// Routing entry point that allocates nothing: its scratch (double-float
-// router logits and the bucketing work list) lives in one file-scope device
+// Routing entry point that allocates nothing: its scratch (router logits,
+// norm bounds and the bucketing work list) lives in one file-scope device
 // array of fixed size instead of memory obtained from cudaMalloc.
 #include <cuda_runtime.h>
 
@@ -18,14 +18,16 @@ constexpr size_t kMaxPairs = 32768;               // T * top_k
 constexpr int kMaxDevices = 64;
 
 // Layout of the scratch array (byte offsets): logit hi, logit lo, inverse
-// permutation, work-list slots (these are fully rewritten by every call; no
-// part must start at zero).
+// permutation, work-list slots, norm bounds of the router rows and of x
+// (these are fully rewritten by every call; no part must start at zero).
 constexpr size_t kOffHi = 0;
 constexpr size_t kOffLo = kOffHi + kMaxLogits * 4;
 constexpr size_t kOffInv = kOffLo + kMaxLogits * 4;
 constexpr size_t kOffSlots = kOffInv + kMaxPairs * 4;
 constexpr size_t kSlotInts = 1 + 3 * 513 + 2 * 514;
-static_assert(kOffSlots + kSlotInts * 4 <= kScratchBytes, "scratch layout exceeds the array");
+constexpr size_t kOffWn = (kOffSlots + kSlotInts * 4 + 255) / 256 * 256;
+constexpr size_t kOffXn = kOffWn + 512 * 4;
+static_assert(kOffXn + kMaxLogits * 4 <= kScratchBytes, "scratch layout exceeds the array");
 
 __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
@@ -91,6 +93,8 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
   p.bias = bias;
   p.logit_hi = reinterpret_cast<float*>(sc + kOffHi);
   p.logit_lo = reinterpret_cast<float*>(sc + kOffLo);
+  p.wnorm = reinterpret_cast<float*>(sc + kOffWn);
+  p.xnorm = reinterpret_cast<float*>(sc + kOffXn);
   p.ids = ids;
   p.gates = gates;
   p.counts = counts;

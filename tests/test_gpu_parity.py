@@ -137,18 +137,37 @@ def test_down_scale_plus_one_doubles_exactly(m):
     layer2.close()
 
 
-def test_exact_ties_lower_index(m):
+@pytest.mark.parametrize("flags", [0, 2])
+def test_exact_ties_lower_index(m, flags):
     wl = synth.WORKLOADS["tiny"].with_(T=3, E=8, k=3)
     L = synth.gen_layer(wl, 0)
     w = np.zeros((wl.E, wl.d), dtype=np.float32)
     w[[2, 5, 6]] = 0.25  # three identical router rows -> exact ties
     w[1] = 0.125
     L = dict(L, w_router=w)
-    g, ref, _ = _parity(m, wl, L)
+    g, ref, _ = _parity(m, wl, L, flags=flags)
     for t in range(wl.T):
         s = np.sign(synth.bf16_bits_to_f32(L["x"][t]).sum())
         expect = [2, 5, 6] if s > 0 else [0, 3, 4]
         assert list(g["ids"][t]) == expect
+
+
+@pytest.mark.parametrize("flags", [0, 2])
+def test_near_ties_need_double_float(m, flags):
+    """Router rows 3 and 7 differ by one ulp in one element and carry a large bias:
+    both are every token's top 2, their order is set by a logit difference far
+    below fp32 resolution (the multi-kernel path's fp32 bound cannot order them,
+    its double-float recompute must)."""
+    wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=2)
+    L = synth.gen_layer(wl, 6)
+    w = L["w_router"].copy()
+    w[7] = w[3]
+    w[7, 5] = np.nextafter(w[3, 5], np.float32(np.inf))
+    b = np.zeros(wl.E, dtype=np.float32)
+    b[3] = b[7] = 50.0
+    g, ref, _ = _parity(m, wl, dict(L, w_router=w, bias=b), flags=flags)
+    assert set(np.unique(g["ids"])) == {3, 7}
+    assert len({tuple(r) for r in g["ids"]}) == 2  # both orders occur (the sign of x[t, 5] decides)
 
 
 def test_skewed_all_tokens_one_expert(m):
@@ -218,10 +237,31 @@ def test_full_size_workloads(m, name, layer_idx, tokens):
     _parity(m, wl, L, tokens=tokens)
 
 
-def test_tc_gateup_prefill_sampled(m):
-    """The tcgen05 block-scaled gate/up on the full prefill chunk (sampled tokens)."""
+def test_register_decode_gemms_prefill_sampled(m):
+    """The multi-kernel path without the tcgen05 GEMMs (MOE_FLAG_NO_TC) on the full prefill chunk."""
     wl = synth.WORKLOADS["prefill"]
-    _parity(m, wl, synth.gen_layer(wl, 2), tokens=[3, 700], flags=m.MOE_FLAG_TC_GATEUP)
+    _parity(m, wl, synth.gen_layer(wl, 2), tokens=[3, 700], flags=m.MOE_FLAG_NO_TC)
+
+
+MEDIUM_SHAPES = [
+    # (T, d, ffn, E, k, shared, zipf): token blocks of 48 with ragged tails, experts over several blocks,
+    # K step counts odd and even, M tile counts odd and even
+    (17, 256, 320, 16, 2, 0, 0.0),
+    (100, 384, 192, 8, 4, 96, 1.1),
+    (300, 160, 416, 32, 3, 0, 1.1),
+]
+
+
+@pytest.mark.parametrize("shape", MEDIUM_SHAPES)
+@pytest.mark.parametrize("flags", [0, 8])
+def test_medium_shapes(m, shape, flags):
+    """T > 16: the multi-kernel path with (default) and without (MOE_FLAG_NO_TC) the tcgen05 GEMMs."""
+    T, d, F, E, k, S, z = shape
+    wl = synth.WORKLOADS["tiny"].with_(name="medium", number=11, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S,
+                                       zipf_bias=z)
+    L = synth.gen_layer(wl, 23)
+    tokens = None if T <= 100 else list(range(0, T, 7))
+    _parity(m, wl, L, out_f32=True, tokens=tokens, flags=flags)
 
 
 @pytest.mark.parametrize("name", ["decode", "verify", "small"])
