@@ -175,7 +175,7 @@ int moe_launches_per_forward(const moe_ctx* ctx, int T);
  * [n_experts][d] (both 16-byte aligned), bias fp32 [n_experts] or NULL, and
  * the outputs ids int32 [T][top_k], gates fp32 [T][top_k], counts int32
  * [n_experts], offsets int32 [n_experts+1], perm int32 [T*top_k].
- * The scratch is one static 1 MiB device array that every device loading the
+ * The scratch is one static 3 MiB device array that every device loading the
  * library holds until exit; sizes beyond it (T*n_experts > 65536 or
  * T*top_k > 32768) are rejected with MOE_ERR_INVALID_ARG. The array keeps the
  * last call's contents and is shared by all calls: calls whose kernels

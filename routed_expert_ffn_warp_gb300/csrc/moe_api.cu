@@ -145,8 +145,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_x16 = take((size_t)Tm * d64 * 2), o_xinv = take((size_t)Tm * 4);
   const int xq_spitch = (d64 / 32 + 3) / 4 * 4;
   const size_t o_xq = take((size_t)Tm * 2 * d64), o_xqs = take((size_t)Tm * 2 * xq_spitch);
-  const size_t o_lh = take((size_t)Tm * E * 4), o_ll = take((size_t)Tm * E * 4);
-  const size_t o_xn = take((size_t)Tm * 4), o_wn = take((size_t)E * 4);
+  const size_t o_lh = take((size_t)moe::kRouterSplits * Tm * E * 4);
+  const size_t o_xsq = take((size_t)moe::kRouterSplits * Tm * 4), o_wsq = take((size_t)moe::kRouterSplits * E * 4);
   const size_t o_ids = take(Pm * 4), o_gates = take(Pm * 4), o_counts = take((size_t)E * 4),
                o_offsets = take((size_t)(E + 1) * 4), o_perm = take(Pm * 4), o_inv = take(Pm * 4);
   const size_t o_ns = take(4), o_se = take((size_t)(E + 1) * 4), o_sq = take((size_t)(E + 1) * 4),
@@ -214,9 +214,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
   p.xq_spitch = xq_spitch;
   p.logit_hi = reinterpret_cast<float*>(w + o_lh);
-  p.logit_lo = reinterpret_cast<float*>(w + o_ll);
-  p.xnorm = reinterpret_cast<float*>(w + o_xn);
-  p.wnorm = reinterpret_cast<float*>(w + o_wn);
+  p.lstride = (size_t)Tm * E;
+  p.logit_lo = p.logit_hi + p.lstride;
+  p.xsq = reinterpret_cast<float*>(w + o_xsq);
+  p.wsq = reinterpret_cast<float*>(w + o_wsq);
   p.ids = reinterpret_cast<int32_t*>(w + o_ids);
   p.gates = reinterpret_cast<float*>(w + o_gates);
   p.counts = reinterpret_cast<int32_t*>(w + o_counts);

@@ -90,6 +90,8 @@ __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
 
 // ---------------------------------------------------------------- forward parameters
 
+constexpr int kRouterSplits = 4;  // most ranges of d the router's fp32 pass splits into
+
 struct FwdParams {
   // sizes
   int T, d, F, E, k, S;  // S = shared ffn (0 = none)
@@ -119,10 +121,12 @@ struct FwdParams {
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
   int xq_spitch;         // scale bytes per plane row (a multiple of 4)
-  float* logit_hi;       // [t_max][E]
-  float* logit_lo;
-  float* xnorm;          // [t_max] upper bounds of |x_t|_2 (router error bounds)
-  float* wnorm;          // [E] upper bounds of |W_r[e]|_2
+  float* logit_hi;       // [t_max][E]: exported logits; the first of kRouterSplits planes lstride floats apart
+  float* logit_lo;       // = logit_hi + lstride
+  size_t lstride;        // t_max * E
+  int rsplit;            // ranges of d in the router's fp32 pass (set by the launcher)
+  float* xsq;            // [kRouterSplits][t_max]: sums of squares of x_t per range (lstride / E apart)
+  float* wsq;            // [kRouterSplits][E]: sums of squares of W_r[e] per range
   int32_t* ids;          // [t_max][k]
   float* gates;          // [t_max][k]
   int32_t* counts;       // [E]
@@ -186,6 +190,8 @@ constexpr int kLaunchesPerForwardTc = 9;  // + x planes, x panels (MOE_FLAG_TC_G
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);
 // Routing only (router logits, top-k gates, counting sort) of the general path.
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
+// Router logits and top-k of the multi-kernel path (moe_kernels.cu).
+void launch_router(FwdParams p, cudaStream_t stream);
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream);

@@ -61,60 +61,91 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
 // ---------------------------------------------------------------- router
 
 // The router in two passes. Pass 1 (router_fp32_kernel): every logit in fp32
-// by fused multiply-adds, 64 elements of d per partial sum, the partial sums
-// added in order, then the bias: a sum in which every product passes at most
-// D = 64 + ceil(d / 64) roundings, so |fp32 - exact| <= gamma_D sum|x_i w_i|
-// + 2^-23 |logit| with gamma_D = D u / (1 - D u), u = 2^-24, and
-// sum|x_i w_i| <= |x|_2 |w_e|_2 (Cauchy-Schwarz); the same pass bounds the
-// two norms from above. Pass 2 (topk_kernel): per token, the k-th largest
-// lower bound decides which experts can still be among the top k; only those
-// get the double-float logit, and the top k, the order and the gates come from
-// those values alone. The selection equals that of double-float logits for all
-// experts: an expert whose upper bound is below the k-th largest lower bound
-// is beaten by at least k others.
-constexpr int kRfTok = 32, kRfExp = 32, kRfK = 64, kRfThreads = 128;
+// by fused multiply-adds, 128 elements of d per partial sum, the partial sums
+// added in order within each of rsplit ranges of d (one per block column), the
+// ranges added in order and then the bias by the top-k kernel: a sum in which
+// every product passes at most D = 128 + ceil(d / 128) + 3 roundings, so
+// |fp32 - exact| <= gamma_D sum|x_i w_i| + 2^-23 |logit| with
+// gamma_D = D u / (1 - D u), u = 2^-24, and sum|x_i w_i| <= |x|_2 |w_e|_2
+// (Cauchy-Schwarz); the same pass sums the squares for the two norms. Pass 2
+// (topk_kernel): per token, the k-th largest lower bound decides which experts
+// can still be among the top k; only those get the double-float logit, and
+// the top k, the order and the gates come from those values alone. The
+// selection equals that of double-float logits for all experts: an expert
+// whose upper bound is below the k-th largest lower bound is beaten by at
+// least k others.
+constexpr int kRfTok = 32, kRfExp = 32, kRfK = 128, kRfThreads = 128;
 
 __device__ __forceinline__ float router_gamma(int d) {
-  const float D = (float)(kRfK + (d + kRfK - 1) / kRfK);
+  const float D = (float)(kRfK + (d + kRfK - 1) / kRfK + 3);
   return D * 0x1p-24f / (1.f - D * 0x1p-24f);
 }
 
-// Block (32 tokens, 32 experts); thread (token pair tid / 8, expert quad tid % 8).
+// Block (32 tokens, 32 experts, range z of d); thread (token pair tid / 8,
+// expert quad tid % 8) in the products. Loads: lane l takes token (expert) l,
+// warps and repeats step through K, so that the transposed stores to shared
+// memory hit 32 banks. The next chunk of x and W_r is loaded into registers
+// while the current one is multiplied out of shared memory.
 __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
   __shared__ __align__(16) float xs[kRfK][kRfTok + 4];  // [k][token]
   __shared__ __align__(16) float ws[kRfK][kRfExp + 4];  // [k][expert]
-  const int tid = threadIdx.x, t0 = blockIdx.x * kRfTok, e0 = blockIdx.y * kRfExp;
+  __shared__ float nsq[2][kRfThreads / 32][32];         // per-warp sums of squares: x rows, W_r rows
+  constexpr int kXL = kRfTok * kRfK / 8 / kRfThreads;   // 8-element x loads per thread and chunk
+  constexpr int kWL = kRfExp * kRfK / 4 / kRfThreads;   // 4-element W_r loads per thread and chunk
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * kRfTok, e0 = blockIdx.y * kRfExp, z = blockIdx.z;
+  const int nch = (p.d + kRfK - 1) / kRfK, cps = (nch + p.rsplit - 1) / p.rsplit;
+  const int kbeg = z * cps * kRfK, kend = min(p.d, (z + 1) * cps * kRfK);
   const int tt = tid >> 3, te = tid & 7;
   float tot[2][4] = {};
-  float xsq[2] = {0.f, 0.f}, wsq[4] = {0.f, 0.f, 0.f, 0.f};  // sums of squares of the rows this thread loads
-  for (int kc = 0; kc < p.d; kc += kRfK) {
-    for (int j = 0; j < 2; ++j) {  // x: 32 tokens x 64 elements, 8 per load
-      const int r = tid + kRfThreads * j, tok = r >> 3, k8 = (r & 7) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (t0 + tok < p.T && kc + k8 < p.d) v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + tok) * p.d + kc + k8));
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      float s = 0.f;
+  float xsq = 0.f, wsq = 0.f;  // sums of squares of token t0 + lane's and expert e0 + lane's loaded elements
+  uint4 xr[kXL];
+  float4 wr[kWL];
+  const bool xok = t0 + lane < p.T, wok = e0 + lane < p.E;
+  const uint16_t* xrow = p.x + (size_t)(t0 + lane) * p.d;
+  const float* wrow = p.w_router + (size_t)(e0 + lane) * p.d;
+  auto load = [&](int kc) {
+#pragma unroll
+    for (int j = 0; j < kXL; ++j) {
+      const int k8 = 8 * (warp + (kRfThreads / 32) * j);
+      xr[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (xok && kc + k8 < kend) xr[j] = __ldg(reinterpret_cast<const uint4*>(xrow + kc + k8));
+    }
+#pragma unroll
+    for (int j = 0; j < kWL; ++j) {
+      const int k4 = 4 * (warp + (kRfThreads / 32) * j);
+      wr[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (wok && kc + k4 < kend) wr[j] = __ldg(reinterpret_cast<const float4*>(wrow + kc + k4));
+    }
+  };
+  if (kbeg < kend) load(kbeg);
+  for (int kc = kbeg; kc < kend; kc += kRfK) {
+#pragma unroll
+    for (int j = 0; j < kXL; ++j) {
+      const int k8 = 8 * (warp + (kRfThreads / 32) * j);
+      const uint32_t w4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
+      float sq = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float a = __uint_as_float(w4[q] << 16), b = __uint_as_float(w4[q] & 0xFFFF0000u);
-        xs[k8 + 2 * q][tok] = a;
-        xs[k8 + 2 * q + 1][tok] = b;
-        s = fmaf(a, a, s);
-        s = fmaf(b, b, s);
+        xs[k8 + 2 * q][lane] = a;
+        xs[k8 + 2 * q + 1][lane] = b;
+        sq = fmaf(a, a, sq);
+        sq = fmaf(b, b, sq);
       }
-      xsq[j] += s;
+      xsq += sq;
     }
-    for (int j = 0; j < 4; ++j) {  // w: 32 experts x 64 elements, 4 per load
-      const int r = tid + kRfThreads * j, ex = r >> 4, k4 = (r & 15) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + ex < p.E && kc + k4 < p.d) v = __ldg(reinterpret_cast<const float4*>(p.w_router + (size_t)(e0 + ex) * p.d + kc + k4));
-      ws[k4][ex] = v.x;
-      ws[k4 + 1][ex] = v.y;
-      ws[k4 + 2][ex] = v.z;
-      ws[k4 + 3][ex] = v.w;
-      wsq[j] += fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, v.w * v.w)));
+#pragma unroll
+    for (int j = 0; j < kWL; ++j) {
+      const int k4 = 4 * (warp + (kRfThreads / 32) * j);
+      ws[k4][lane] = wr[j].x;
+      ws[k4 + 1][lane] = wr[j].y;
+      ws[k4 + 2][lane] = wr[j].z;
+      ws[k4 + 3][lane] = wr[j].w;
+      wsq += fmaf(wr[j].x, wr[j].x, fmaf(wr[j].y, wr[j].y, fmaf(wr[j].z, wr[j].z, wr[j].w * wr[j].w)));
     }
     __syncthreads();
+    if (kc + kRfK < kend) load(kc + kRfK);
     float c[2][4] = {};
 #pragma unroll 16
     for (int k = 0; k < kRfK; ++k) {
@@ -132,6 +163,7 @@ __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
       for (int b = 0; b < 4; ++b) tot[a][b] += c[a][b];
     __syncthreads();
   }
+  float* plane = p.logit_hi + (size_t)z * p.lstride;  // partial sums of range z
 #pragma unroll
   for (int a = 0; a < 2; ++a) {
     const int t = t0 + 2 * tt + a;
@@ -139,155 +171,202 @@ __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const int e = e0 + 4 * te + b;
-      if (e < p.E) p.logit_hi[(size_t)t * p.E + e] = p.bias ? tot[a][b] + p.bias[e] : tot[a][b];
+      if (e < p.E) plane[(size_t)t * p.E + e] = tot[a][b];
     }
   }
-  // norms, rounded up: the 8 (16) threads that loaded a token's (expert's) rows are adjacent lanes
-  const float up = 1.f + (float)(p.d / 8 + 16) * 0x1p-22f;
-  for (int j = 0; j < 2; ++j) {
-    float s = xsq[j];
-    for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const int tok = (tid + kRfThreads * j) >> 3;
-    if (blockIdx.y == 0 && (tid & 7) == 0 && t0 + tok < p.T) p.xnorm[t0 + tok] = sqrtf(s * up) * up;
+  // sums of squares of range z: the four warps' sums in warp order
+  nsq[0][warp][lane] = xsq;
+  nsq[1][warp][lane] = wsq;
+  __syncthreads();
+  if (warp < 2) {
+    float sq = 0.f;
+    for (int w = 0; w < kRfThreads / 32; ++w) sq += nsq[warp][w][lane];
+    if (warp == 0 && blockIdx.y == 0 && xok) p.xsq[(size_t)z * p.lstride / p.E + t0 + lane] = sq;
+    if (warp == 1 && blockIdx.x == 0 && wok) p.wsq[z * p.E + e0 + lane] = sq;
   }
-  for (int j = 0; j < 4; ++j) {
-    float s = wsq[j];
-    for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const int ex = (tid + kRfThreads * j) >> 4;
-    if (blockIdx.x == 0 && (tid & 15) == 0 && e0 + ex < p.E) p.wnorm[e0 + ex] = sqrtf(s * up) * up;
-  }
-}
-
-// Double-float logit of expert e for token t by one warp (the value of lane 0,
-// broadcast): lanes stride over d in groups of 8, then a fixed-shape tree.
-__device__ __forceinline__ dd warp_logit_dd(const FwdParams& p, int t, int e) {
-  const int lane = threadIdx.x & 31;
-  dd acc{0.f, 0.f};
-  const float* w = p.w_router + (size_t)e * p.d;
-  const uint16_t* x = p.x + (size_t)t * p.d;
-  for (int i8 = lane; i8 < p.d / 8; i8 += 32) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + i8);
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8);
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8 + 1);
-    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      dd_mac(acc, __uint_as_float(xw[j] << 16), wv[2 * j]);
-      dd_mac(acc, __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
-    }
-  }
-  for (int o = 16; o; o >>= 1) acc = dd_add(acc, dd_shfl_xor(acc, o));
-  acc.hi = __shfl_sync(0xffffffffu, acc.hi, 0);
-  acc.lo = __shfl_sync(0xffffffffu, acc.lo, 0);
-  if (p.bias) acc = dd_add(acc, dd{p.bias[e], 0.f});
-  return acc;
 }
 
 // ---------------------------------------------------------------- top-k and gates
 
-constexpr int kTopkWarps = 8;
-constexpr int kMaxEPerLane = 16;  // E <= 512
+constexpr int kTopkThreads = 128;
+constexpr int kTopkMaxE = 512;
 
-// One warp per token: the candidate set from the fp32 bounds, double-float
-// logits of the candidates, then k rounds of a warp arg-max over them (value
-// first, then the lower expert index) and the softmax of the k. The exported
-// logits (hi + lo) are the double-float values for the candidates and the
-// fp32 values (lo = 0) for the rest.
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(FwdParams p) {
+// Double-float partial logits, over elements [k0, k1) of d, of up to 4
+// experts es[0 .. n) for token t by one warp (the values of lane 0,
+// broadcast): lanes stride over the range in groups of 8, one accumulator per
+// expert, then a fixed-shape tree per expert.
+__device__ __forceinline__ void warp_logits_dd(const FwdParams& p, int t, const int (&es)[4], int n, int k0, int k1,
+                                               dd (&out)[4]) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
-  if (t >= p.T) return;
-  const int E = p.E, k = p.k;
-  const float xb = router_gamma(p.d) * 1.01f * p.xnorm[t];
-  float vh[kMaxEPerLane], vl[kMaxEPerLane], lb[kMaxEPerLane], ub[kMaxEPerLane];
+  dd acc[4] = {};
+  const uint16_t* x = p.x + (size_t)t * p.d;
+  for (int i8 = k0 / 8 + lane; i8 < k1 / 8; i8 += 32) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x) + i8);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-  for (int i = 0; i < kMaxEPerLane; ++i) {
-    const int e = lane + 32 * i;
+    for (int c = 0; c < 4; ++c) {
+      if (c >= n) continue;
+      const float* w = p.w_router + (size_t)es[c] * p.d;
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8);
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w) + 2 * i8 + 1);
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        dd_mac(acc[c], __uint_as_float(xw[j] << 16), wv[2 * j]);
+        dd_mac(acc[c], __uint_as_float(xw[j] & 0xFFFF0000u), wv[2 * j + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    for (int o = 16; o; o >>= 1) acc[c] = dd_add(acc[c], dd_shfl_xor(acc[c], o));
+    out[c].hi = __shfl_sync(0xffffffffu, acc[c].hi, 0);
+    out[c].lo = __shfl_sync(0xffffffffu, acc[c].lo, 0);
+  }
+}
+
+// One block per token. (1) fp32 logits (range sums in order, then the bias)
+// and their bounds; (2) warp 0: the k-th largest lower bound and the list of
+// candidates in index order; (3) every warp: double-float partial logits of the
+// candidates over its quarter of d; (4) warp 0: the quarters added in order,
+// the bias, k rounds of a warp arg-max over the candidates (value first, then
+// the lower expert index), the softmax of the k. The exported logits (hi + lo)
+// are the double-float values for the candidates and the fp32 values (lo = 0)
+// for the rest.
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(FwdParams p) {
+  __shared__ float lf[kTopkMaxE], lb[kTopkMaxE], ub[kTopkMaxE];
+  __shared__ short cl[kTopkMaxE];
+  __shared__ dd part[kTopkThreads / 32][kTopkMaxE];
+  __shared__ int s_nc;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E, k = p.k;
+  const float up = 1.f + (float)(p.d / 8 + 16) * 0x1p-22f;
+  float xs2 = 0.f;
+  for (int z = 0; z < p.rsplit; ++z) xs2 += p.xsq[(size_t)z * p.lstride / E + t];
+  const float xb = router_gamma(p.d) * 1.01f * (sqrtf(xs2 * up) * up);
+  for (int e = tid; e < E; e += kTopkThreads) {
+    float l = p.logit_hi[(size_t)t * E + e], ws2 = p.wsq[e];
+    for (int z = 1; z < p.rsplit; ++z) {
+      l += p.logit_hi[(size_t)z * p.lstride + (size_t)t * E + e];
+      ws2 += p.wsq[z * E + e];
+    }
+    if (p.bias) l += p.bias[e];
+    const float beta = fmaf(xb, sqrtf(ws2 * up) * up, 0x1p-22f * fabsf(l)) + 0x1p-126f;
+    lf[e] = l;
+    lb[e] = l - beta;
+    ub[e] = l + beta;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // the k-th largest lower bound (ties: lower index first, for a fixed choice)
+    uint32_t taken = 0;
+    float kth = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      float b = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int i = 0; 32 * i + lane < E; ++i) {
+        const int e = 32 * i + lane;
+        if (!((taken >> i) & 1u) && (lb[e] > b || (lb[e] == b && e < bi))) {
+          b = lb[e];
+          bi = e;
+        }
+      }
+      for (int o = 16; o; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, b, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ob > b || (ob == b && oi < bi)) {
+          b = ob;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      kth = b;
+    }
+    int nc = 0;
+    for (int i = 0; 32 * i < E; ++i) {
+      const int e = 32 * i + lane;
+      const bool c = e < E && ub[e] >= kth;
+      const unsigned cm = __ballot_sync(0xffffffffu, c);
+      if (c) cl[nc + __popc(cm & ((1u << lane) - 1u))] = (short)e;
+      nc += __popc(cm);
+    }
+    if (lane == 0) s_nc = nc;
+  }
+  __syncthreads();
+  const int nc = s_nc;
+  {
+    // quarter `warp` of d, in whole groups of 8
+    const int g8 = p.d / 8, k0 = 8 * (g8 * warp / 4), k1 = 8 * (g8 * (warp + 1) / 4);
+    for (int g0 = 0; g0 < nc; g0 += 4) {
+      const int n = min(4, nc - g0);
+      int es[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) es[c] = c < n ? cl[g0 + c] : 0;
+      dd v[4];
+      warp_logits_dd(p, t, es, n, k0, k1, v);
+      if (lane == 0)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (c < n) part[warp][g0 + c] = v[c];
+    }
+  }
+  __syncthreads();
+  // the exported logits of the non-candidates: fp32, lo = 0 (candidates below)
+  for (int e = tid; e < E; e += kTopkThreads) {
+    p.logit_hi[(size_t)t * E + e] = lf[e];
+    p.logit_lo[(size_t)t * E + e] = 0.f;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // candidates c = lane + 32 i: the quarters in order, then the bias
+  float vh[kTopkMaxE / 32], vl[kTopkMaxE / 32];
+  int vid[kTopkMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kTopkMaxE / 32; ++i) {
+    const int c = lane + 32 * i;
     vh[i] = -INFINITY;
     vl[i] = 0.f;
-    lb[i] = -INFINITY;
-    ub[i] = -INFINITY;
-    if (e < E) {
-      const float l = p.logit_hi[(size_t)t * E + e];
-      const float beta = fmaf(xb, p.wnorm[e], 0x1p-22f * fabsf(l)) + 0x1p-126f;
-      vh[i] = l;
-      lb[i] = l - beta;
-      ub[i] = l + beta;
+    vid[i] = 0x7fffffff;
+    if (c < nc) {
+      dd v = part[0][c];
+      for (int w = 1; w < kTopkThreads / 32; ++w) v = dd_add(v, part[w][c]);
+      const int e = cl[c];
+      if (p.bias) v = dd_add(v, dd{p.bias[e], 0.f});
+      vh[i] = v.hi;
+      vl[i] = v.lo;
+      vid[i] = e;
+      p.logit_hi[(size_t)t * E + e] = v.hi;
+      p.logit_lo[(size_t)t * E + e] = v.lo;
     }
   }
-  // the k-th largest lower bound
   uint32_t taken = 0;
-  float kth = -INFINITY;
-  for (int j = 0; j < k; ++j) {
-    float b = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i)
-      if (!((taken >> i) & 1u) && 32 * i + lane < E && (lb[i] > b || (lb[i] == b && 32 * i + lane < bi))) {
-        b = lb[i];
-        bi = 32 * i + lane;
-      }
-    for (int o = 16; o; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, b, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ob > b || (ob == b && oi < bi)) {
-        b = ob;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    kth = b;
-  }
-  // candidates: double-float logits
-  uint32_t cand = 0;
-#pragma unroll
-  for (int i = 0; i < kMaxEPerLane; ++i) {
-    const bool c = 32 * i + lane < E && ub[i] >= kth;
-    if (c) cand |= 1u << i;
-    unsigned cm = __ballot_sync(0xffffffffu, c);
-    while (cm) {
-      const int l = __ffs(cm) - 1;
-      cm &= cm - 1;
-      const dd v = warp_logit_dd(p, t, l + 32 * i);
-      if (lane == l) {
-        vh[i] = v.hi;
-        vl[i] = v.lo;
-      }
-    }
-  }
-  for (int i = 0; i < kMaxEPerLane; ++i) {  // the exported logits
-    const int e = lane + 32 * i;
-    if (e < E) {
-      p.logit_hi[(size_t)t * E + e] = vh[i];
-      p.logit_lo[(size_t)t * E + e] = vl[i];
-    }
-  }
-  taken = ~cand;
   float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {
     float bh = -INFINITY, bl = 0.f;
-    int bi = 0x7fffffff;
+    int bi = 0x7fffffff, bs = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxEPerLane; ++i) {
-      if (!((taken >> i) & 1u) && dd_greater(vh[i], vl[i], lane + 32 * i, bh, bl, bi)) {
+    for (int i = 0; i < kTopkMaxE / 32; ++i) {
+      if (lane + 32 * i < nc && !((taken >> i) & 1u) && dd_greater(vh[i], vl[i], vid[i], bh, bl, bi)) {
         bh = vh[i];
         bl = vl[i];
-        bi = lane + 32 * i;
+        bi = vid[i];
+        bs = lane + 32 * i;
       }
     }
     for (int o = 16; o; o >>= 1) {
       const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
       const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const int os = __shfl_xor_sync(0xffffffffu, bs, o);
       if (dd_greater(oh, ol, oi, bh, bl, bi)) {
         bh = oh;
         bl = ol;
         bi = oi;
+        bs = os;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if ((bs & 31) == lane) taken |= 1u << (bs >> 5);
     if (j == 0) {
       top_h = bh;
       top_l = bl;
@@ -308,75 +387,127 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(FwdParams p) {
   }
 }
 
+// K ranges of the router's fp32 pass: enough blocks for about two per SM.
+__host__ inline int router_splits(int T, int E, int d) {
+  const int tiles = ((T + kRfTok - 1) / kRfTok) * ((E + kRfExp - 1) / kRfExp);
+  const int nch = (d + kRfK - 1) / kRfK;
+  int s = (296 + tiles - 1) / tiles;
+  s = s < 1 ? 1 : s > kRouterSplits ? kRouterSplits : s;
+  return s < nch ? s : nch;
+}
+
 // ---------------------------------------------------------------- bucketing and work list
 
 constexpr int kBucketThreads = 1024;
+constexpr int kBucketChunks = 16;  // warps that count and place the pairs, each over a contiguous chunk
 
-// Counting sort of the P = T*k pairs by expert (histogram, exclusive scan,
-// ranks within a bucket in pair order), then one work-list slot per expert
-// that received pairs (expert order) and the shared expert last.
-__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
+// Exclusive prefix sum over the block (every thread gives v; threads past the
+// data give 0); returns the prefix and, in *total, the block's sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int E = p.E, T = p.T, P = p.P;
-  __shared__ int cnt[512];
-  __shared__ int run[512];
-  __shared__ int offs[513];
-  for (int e = threadIdx.x; e < E; e += kBucketThreads) {
-    cnt[e] = 0;
-    run[e] = 0;
+  int incl = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
   }
+  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  for (int q = threadIdx.x; q < P; q += kBucketThreads) atomicAdd(&cnt[p.ids[q]], 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      offs[e] = acc;
-      acc += cnt[e];
-    }
-    offs[E] = acc;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += kBucketThreads) {
-    p.offsets[e] = offs[e];
-    if (e < E) p.counts[e] = cnt[e];
-  }
   if (warp == 0) {
-    for (int base = 0; base < P; base += 32) {
+    int w = lane < kBucketThreads / 32 ? wsum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    wsum[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = warp > 0 ? wsum[warp - 1] : 0;
+  *total = wsum[kBucketThreads / 32 - 1];
+  __syncthreads();  // wsum is reused by the next scan
+  return before + incl - v;
+}
+
+// Counting sort of the P = T*k pairs by expert: chunk warps count their
+// contiguous range of pairs per expert, a prefix over chunks and one over
+// experts give every (chunk, expert) its first position, and the chunk warps
+// place their pairs in pair order (ranks within a bucket follow the pair
+// index). Then one work-list slot per expert that received pairs (expert
+// order) and the shared expert last, from prefix sums of the per-slot unit
+// counts.
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
+  const int E = p.E, T = p.T, P = p.P;
+  __shared__ int wc[kBucketChunks][512];  // per (chunk, expert): count, then first position
+  __shared__ int wsum[32];
+  const int chunk = (P + kBucketChunks - 1) / kBucketChunks;
+  for (int i = tid; i < kBucketChunks * E; i += kBucketThreads) wc[i / E][i % E] = 0;
+  __syncthreads();
+  if (warp < kBucketChunks) {
+    const int q1 = min(P, (warp + 1) * chunk);
+    for (int base = warp * chunk; base < q1; base += 32) {
       const int q = base + lane;
-      const bool valid = q < P;
+      const int e = q < q1 ? p.ids[q] : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      if (q < q1 && (same & ((1u << lane) - 1u)) == 0) wc[warp][e] += __popc(same);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  int cnt = 0;
+  if (tid < E)
+    for (int w = 0; w < kBucketChunks; ++w) {
+      const int c = wc[w][tid];
+      wc[w][tid] = cnt;
+      cnt += c;
+    }
+  int tot;
+  const int off = block_exclusive_scan(tid < E ? cnt : 0, wsum, &tot);
+  if (tid < E) {
+    p.counts[tid] = cnt;
+    p.offsets[tid] = off;
+    for (int w = 0; w < kBucketChunks; ++w) wc[w][tid] += off;
+  }
+  if (tid == 0) p.offsets[E] = tot;
+  __syncthreads();
+  if (warp < kBucketChunks) {
+    const int q1 = min(P, (warp + 1) * chunk);
+    for (int base = warp * chunk; base < q1; base += 32) {
+      const int q = base + lane;
+      const bool valid = q < q1;
       const int e = valid ? p.ids[q] : -1 - lane;
       const unsigned same = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(same & ((1u << lane) - 1u));
-      const int before = valid ? run[e] : 0;
+      const int first = valid ? wc[warp][e] : 0;
       __syncwarp();
-      if (valid && rank == 0) run[e] = before + __popc(same);
+      if (valid && rank == 0) wc[warp][e] = first + __popc(same);
       __syncwarp();
       if (valid) {
-        const int pos = offs[e] + before + rank;
+        const int pos = first + rank;
         p.perm[pos] = q;
         p.inv[q] = pos;
       }
     }
   }
-  if (threadIdx.x == 32) {
-    int ns = 0, gu = 0, dn = 0, pn = 0;
-    for (int e = 0; e < E; ++e) {
-      if (cnt[e] == 0) continue;
-      p.slot_expert[ns] = e;
-      p.slot_q0[ns] = offs[e];
-      p.slot_n[ns] = cnt[e];
-      p.gu_prefix[ns] = gu;
-      p.dn_prefix[ns] = dn;
-      if (p.tc_gateup) p.panel_prefix[ns] = pn;
-      pn += (cnt[e] + kTcGemmRows - 1) / kTcGemmRows;
-      const int blocks = (cnt[e] + kGemmRows - 1) / kGemmRows;
-      gu += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * ((p.F / 16 + 3) / 4)
-                        : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
-      dn += p.tc_gateup ? (cnt[e] + kTcGemmRows - 1) / kTcGemmRows * tc_dtiles(p.d)
-                        : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
-      ++ns;
-    }
+  // work list
+  const bool nz = tid < E && cnt > 0;
+  const int blocks = (cnt + kGemmRows - 1) / kGemmRows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
+  const int ugu = !nz ? 0
+                      : p.tc_gateup ? tcb * ((p.F / 16 + 3) / 4) : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
+  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dtiles(p.d) : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+  int ns, gu, dn, pn;
+  const int slot = block_exclusive_scan(nz ? 1 : 0, wsum, &ns);
+  const int gpre = block_exclusive_scan(ugu, wsum, &gu);
+  const int dpre = block_exclusive_scan(udn, wsum, &dn);
+  const int ppre = block_exclusive_scan(nz ? tcb : 0, wsum, &pn);
+  if (nz) {
+    p.slot_expert[slot] = tid;
+    p.slot_q0[slot] = off;
+    p.slot_n[slot] = cnt;
+    p.gu_prefix[slot] = gpre;
+    p.dn_prefix[slot] = dpre;
+    if (p.tc_gateup) p.panel_prefix[slot] = ppre;
+  }
+  if (tid == 0) {
     if (p.S > 0 && T > 0) {
       p.slot_expert[ns] = E;
       p.slot_q0[ns] = P;
@@ -385,11 +516,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.dn_prefix[ns] = dn;
       if (p.tc_gateup) p.panel_prefix[ns] = pn;
       pn += (T + kTcGemmRows - 1) / kTcGemmRows;
-      const int blocks = (T + kGemmRows - 1) / kGemmRows;
+      const int sb = (T + kGemmRows - 1) / kGemmRows;
       gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * ((p.S / 16 + 3) / 4)
-                        : blocks * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
+                        : sb * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
       dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dtiles(p.d)
-                        : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+                        : sb * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }
     p.gu_prefix[ns] = gu;
@@ -482,14 +613,20 @@ __global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n
 
 }  // namespace
 
+void launch_router(FwdParams p, cudaStream_t stream) {
+  p.rsplit = router_splits(p.T, p.E, p.d);
+  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp, p.rsplit), kRfThreads, 0,
+                       stream>>>(p);
+  topk_kernel<<<p.T, kTopkThreads, 0, stream>>>(p);
+}
+
 const char* const kForwardPhaseNames = "route,gateup,down,combine";
 
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events) {
   if (p.T == 0) return cudaSuccess;
   if (events) cudaEventRecord(events[0], stream);
-  prep_x_kernel<<<p.T, 256, 0, stream>>>(p);
-  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp), kRfThreads, 0, stream>>>(p);
-  topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
+  if (!p.tc_gateup) prep_x_kernel<<<p.T, 256, 0, stream>>>(p);  // f16 x of the register-decode GEMMs
+  launch_router(p, stream);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   if (events) cudaEventRecord(events[1], stream);
   cudaError_t e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
@@ -505,8 +642,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
 
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp), kRfThreads, 0, stream>>>(p);
-  topk_kernel<<<(p.T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(p);
+  launch_router(p, stream);
   bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -1,5 +1,5 @@
 // Routing entry point that allocates nothing: its scratch (router logits,
-// norm bounds and the bucketing work list) lives in one file-scope device
+// sums of squares and the bucketing work list) lives in one file-scope device
 // array of fixed size instead of memory obtained from cudaMalloc.
 #include <cuda_runtime.h>
 
@@ -12,22 +12,22 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(1) << 20;  // 1 MiB on every device that loads the library
+constexpr size_t kScratchBytes = size_t(3) << 20;  // 3 MiB on every device that loads the library
 constexpr size_t kMaxLogits = 65536;              // T * n_experts
 constexpr size_t kMaxPairs = 32768;               // T * top_k
 constexpr int kMaxDevices = 64;
 
-// Layout of the scratch array (byte offsets): logit hi, logit lo, inverse
-// permutation, work-list slots, norm bounds of the router rows and of x
-// (these are fully rewritten by every call; no part must start at zero).
+// Layout of the scratch array (byte offsets): the router's partial-logit
+// planes (the first two are the logits' hi and lo), inverse permutation,
+// work-list slots, sums of squares of the router rows and of x (these are
+// fully rewritten by every call; no part must start at zero).
 constexpr size_t kOffHi = 0;
-constexpr size_t kOffLo = kOffHi + kMaxLogits * 4;
-constexpr size_t kOffInv = kOffLo + kMaxLogits * 4;
+constexpr size_t kOffInv = kOffHi + moe::kRouterSplits * kMaxLogits * 4;
 constexpr size_t kOffSlots = kOffInv + kMaxPairs * 4;
 constexpr size_t kSlotInts = 1 + 3 * 513 + 2 * 514;
-constexpr size_t kOffWn = (kOffSlots + kSlotInts * 4 + 255) / 256 * 256;
-constexpr size_t kOffXn = kOffWn + 512 * 4;
-static_assert(kOffXn + kMaxLogits * 4 <= kScratchBytes, "scratch layout exceeds the array");
+constexpr size_t kOffWsq = (kOffSlots + kSlotInts * 4 + 255) / 256 * 256;
+constexpr size_t kOffXsq = kOffWsq + moe::kRouterSplits * 512 * 4;
+static_assert(kOffXsq + moe::kRouterSplits * kMaxLogits * 4 <= kScratchBytes, "scratch layout exceeds the array");
 
 __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
@@ -55,7 +55,7 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
                                      "1 <= top_k <= min(n_experts, 32)");
   if ((size_t)T * (size_t)n_experts > kMaxLogits || (size_t)T * (size_t)top_k > kMaxPairs)
     return fail(MOE_ERR_INVALID_ARG, "moe_route_static: T * n_experts must be <= 65536 and T * top_k <= 32768 "
-                                     "(the static scratch holds 1 MiB)");
+                                     "(the static scratch holds 3 MiB)");
   if (T == 0) return MOE_OK;
   if (!x || !w_router || !ids || !gates || !counts || !offsets || !perm)
     return fail(MOE_ERR_INVALID_ARG, "moe_route_static: a required pointer is NULL");
@@ -92,9 +92,10 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
   p.w_router = w_router;
   p.bias = bias;
   p.logit_hi = reinterpret_cast<float*>(sc + kOffHi);
-  p.logit_lo = reinterpret_cast<float*>(sc + kOffLo);
-  p.wnorm = reinterpret_cast<float*>(sc + kOffWn);
-  p.xnorm = reinterpret_cast<float*>(sc + kOffXn);
+  p.lstride = (size_t)T * n_experts;
+  p.logit_lo = p.logit_hi + p.lstride;
+  p.wsq = reinterpret_cast<float*>(sc + kOffWsq);
+  p.xsq = reinterpret_cast<float*>(sc + kOffXsq);
   p.ids = ids;
   p.gates = gates;
   p.counts = counts;
