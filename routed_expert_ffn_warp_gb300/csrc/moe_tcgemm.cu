@@ -100,6 +100,19 @@ __device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity, int
     }
   }
 }
+// The same wait for the roles off the MMA lanes' critical path (producers,
+// epilogue): each try may suspend the thread for up to 20 us until the phase
+// completes, so that waiting warps leave their issue slots to the MMA lanes.
+__device__ __forceinline__ void bounded_wait_sleep(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_hint(bar, parity, 20000u)) {
+    if ((long long)(globaltimer() - t0) > kWaitNs) {
+      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
 
 __device__ __forceinline__ int find_unit_slot(const int32_t* prefix, int n, int unit) {
   int lo = 0, hi = n - 1;
@@ -299,7 +312,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       }
       for (int j = 0; ca.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS) bounded_wait(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
         uint8_t* sb = stg + (size_t)s * M::kStage;
         // 8,192 code bytes (counted as read from global memory) + 512 scale bytes
         mbar_arrive_expect_tx(&full[s], (uint32_t)kTcBlockBytes);
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       const int pstride = kDown ? tc_ksteps(p.F > p.S ? p.F : p.S) : tc_ksteps(p.d);
       for (int j = 0; cb.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS) bounded_wait(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
         const int N = M::kPlanes * npad_of(cb.g.n);
         uint8_t* sb = stg + (size_t)s * M::kStage + kAStage;
         const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
@@ -395,7 +408,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       const int nacc = g.nks >= kMma ? kMma : g.nks;
       const int t0 = j0 % kMma;  // the lane of the unit's first K step
       j0 += g.nks;
-      bounded_wait(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status);
+      bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status);
       tc::fence_after();
       if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
         const int row = 128 * g.mt + 32 * qd + lane;
