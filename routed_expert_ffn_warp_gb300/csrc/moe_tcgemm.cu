@@ -22,12 +22,13 @@
 // packed once per call, h panels are written by the gate/up epilogue itself.
 //
 // The CTA is warp-specialized: a weight producer lane (tensor copies, and L2
-// prefetches further ahead), an activation producer lane (bulk copies), an
-// MMA lane (scale factors to tensor memory with tcgen05.cp, then the MMAs),
-// and eight epilogue warps that read a finished unit's accumulators
-// (double-buffered in tensor memory, so the next unit's MMAs run meanwhile).
-// Stages are handed on with mbarriers: full (bytes landed), empty (the
-// stage's MMAs completed), accfull / accempty (accumulator buffer states).
+// prefetches further ahead), an activation producer lane (bulk copies), MMA
+// lanes that take the K steps in turn, four warps that move each stage's
+// scale factors to tensor memory (tcgen05.st, one per lane quadrant), and
+// eight epilogue warps that read a finished unit's accumulators. Stages are
+// handed on with mbarriers: full (bytes landed), ready (scale factors in
+// tensor memory), empty (the stage's MMAs completed), accfull / accempty
+// (accumulator states).
 //
 // The pages: tokens grouped by expert on the GPU for the prompt, one GEMM per
 // expert over its rows ("Neural Server" technical page, "Prompt processing").
@@ -45,7 +46,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThr = 384;                  // 12 warps: see the roles below
+constexpr int kThr = 576;                  // 18 warps: see the roles below
 constexpr int kMaxTok = kTcGemmRows;       // tokens per unit
 constexpr int kPf = 12;                    // L2 prefetch distance of the weight blocks, in K steps
 constexpr int kAOp = 128 * kTcStepK;       // widened E2M1 operand: 16 bytes per 16 elements
@@ -54,18 +55,22 @@ constexpr int kCmRows = kTcBlockBytes / 64;  // 64-byte tensor rows per weight b
 constexpr uint32_t kTmemCols = 512;        // accumulators from column 0, scale factors from 384
 constexpr int kSfCol = 384;                // set s (the stage): SFA columns +16 s .. +3, SFB +8 .. +15
 constexpr long long kWaitNs = 50000000LL;
-// roles: warp 0 weights, 1 and 2 MMA lanes, 3 activations, 4 .. 11 epilogue (lane quadrant = warp % 4)
-constexpr int kProducerWarp = 0, kMmaWarp0 = 1, kPanelWarp = 3, kEpiWarp0 = 4, kEpiThreads = 256;
+// roles: warp 0 weights, 1 activations, 2 .. 5 MMA lanes, 6 .. 9 scale factors to TMEM, 10 .. 17
+// epilogue (a warp's TMEM lane quadrant is warp % 4)
+constexpr int kProducerWarp = 0, kPanelWarp = 1, kMmaWarp0 = 2, kSfWarp0 = 6, kEpiWarp0 = 10, kEpiThreads = 256;
+constexpr int kEpiPerQuad = kEpiThreads / 128;  // epilogue warps per TMEM lane quadrant
 
 // The two uses of the GEMM. Gate/up: M tiles of 64 gate + 64 up rows, K = d,
 // B = x in 2 MXFP8 planes, epilogue h = SiLU(gate) * up into the h panels.
 // Down: M tiles of 128 rows of d, K = f, B = h in 4 MXFP8 planes, epilogue
 // part = D. A stage holds one K step of both operands: [A | B panel step].
 // With kMma MMA lanes, lane t takes the CTA's K steps j = t (mod kMma) and
-// accumulates them in its own accumulator of the unit's buffer (the epilogue
-// adds them): one lane, which also waits for stages and copies scale
-// factors, cannot issue MMAs as fast as the tensor core runs them. The down
-// step's wider accumulators leave room for one buffer only.
+// accumulates them in its own accumulator (the epilogue adds them): a lane
+// issues its MMAs, waits for its next stage and copies that stage's scale
+// factors in turn, and only with several lanes does one of them keep the
+// tensor core busy meanwhile. The accumulators of all lanes fill the 384
+// TMEM columns below the scale factors, so a unit's MMAs start once the
+// epilogue has read the previous unit's accumulators.
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
@@ -87,7 +92,7 @@ constexpr size_t tc_table_bytes(int E) { return (size_t)5 * (E + 2) * 4; }
 
 template <bool kDown>
 constexpr size_t tc_smem_fixed() {
-  return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (2 * Mode<kDown>::kS + 4) + 16;
+  return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (3 * Mode<kDown>::kS + 4) + 16;
 }
 
 __device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity, int* status) {
@@ -250,7 +255,8 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(hx) + M::kEpiSmem);
   uint64_t* full = bars;                  // both operands of the stage landed (two producers)
   uint64_t* empty = full + kS;            // the MMAs reading the stage completed
-  uint64_t* accfull = empty + kS;         // [kBufs] every MMA lane's part of the buffer's unit completed
+  uint64_t* ready = empty + kS;           // the stage's scale factors are in TMEM set s (4 warps x 32)
+  uint64_t* accfull = ready + kS;         // [kBufs] every MMA lane's part of the buffer's unit completed
   uint64_t* accempty = accfull + 2;       // [kBufs]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   int* tab = reinterpret_cast<int*>(tslot + 4);
@@ -285,6 +291,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     for (int s = 0; s < kS; ++s) {
       mbar_init(&full[s], 2);
       mbar_init(&empty[s], 1);
+      mbar_init(&ready[s], 128);
     }
     for (int a = 0; a < kBufs; ++a) {
       mbar_init(&accfull[a], kMma);
@@ -348,33 +355,22 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMma) {
     if (lane == 0) {
       const int t = warp - kMmaWarp0;
-      int jtot = 0;  // K steps of the CTA
-      for (int i = 0; i < n_units; ++i) jtot += tc_unit<kDown>(p, st, b0 + i * G).nks;
-      // scale factors of stage s -> set s, issued one own step ahead of that step's MMAs
-      auto load_sf = [&](int jj) {
-        const int s = jj % kS;
-        bounded_wait(&full[s], (uint32_t)((jj / kS) & 1), p.status);
-        tc::fence_after();
-        const uint8_t* sb = stg + (size_t)s * M::kStage;
-        const uint32_t sf = tmem + kSfCol + 16 * s;
-        tc::cp_32x128b_x4(sf, tc::smem_desc(sb + kAOp, 128, 128));
-#pragma unroll
-        for (int h = 0; h < M::kSfBlocks; ++h)
-          tc::cp_32x128b_x4(sf + 8 + 4 * h,
-                            tc::smem_desc(sb + kAStage + M::kPanelRows * kTcStepK + 512 * h, 128, 128));
-      };
-      if (t < jtot) load_sf(t);
       int j0 = 0;  // first K step of unit i
       for (int i = 0; i < n_units; ++i) {
         const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
         const int N = M::kPlanes * npad_of(g.n), acc = i % kBufs;
         const int first = ((t - j0) % kMma + kMma) % kMma;  // this lane's first K step of the unit
-        if (first >= g.nks) tc::commit(&accfull[acc]);  // no K step of this unit
-        else if (i >= kBufs) bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status);
+        // every lane, with or without K steps in this unit, waits for the
+        // buffer's previous unit to be read: its arrival on accfull then
+        // belongs to this unit's phase
+        if (i >= kBufs) bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status);
         tc::fence_after();
+        if (first >= g.nks) tc::commit(&accfull[acc]);  // no K step of this unit
         const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
         for (int ks = first; ks < g.nks; ks += kMma) {
           const int jj = j0 + ks, s = jj % kS;
+          bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status);  // operands landed, scales in TMEM
+          tc::fence_after();
           const uint8_t* ab = stg + (size_t)s * M::kStage;
           const uint8_t* bb = ab + kAStage;
           const uint32_t sf = tmem + kSfCol + 16 * s;
@@ -387,14 +383,39 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
           }
           tc::commit(&empty[s]);
           if (ks + kMma >= g.nks) tc::commit(&accfull[acc]);  // this lane's last K step of the unit
-          if (jj + kMma < jtot) load_sf(jj + kMma);
         }
         j0 += g.nks;
       }
     }
+  } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
+    // scale factors of every stage into TMEM set s, in the warp's lane
+    // quadrant (each quadrant holds the same copy): SFA words [lane][4] to
+    // columns +0 .. +3, SFB to +8 .. (+4 per 512-byte block)
+    const uint32_t qbase = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol;
+    int jtot = 0;  // K steps of the CTA
+    for (int i = 0; i < n_units; ++i) jtot += tc_unit<kDown>(p, st, b0 + i * G).nks;
+    for (int j = 0; j < jtot; ++j) {
+      const int s = j % kS;
+      bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status);
+      const uint8_t* sb = stg + (size_t)s * M::kStage;
+      const uint4 wa = *reinterpret_cast<const uint4*>(sb + kAOp + 16 * lane);
+      const uint4 wb0 = *reinterpret_cast<const uint4*>(sb + kAStage + M::kPanelRows * kTcStepK + 16 * lane);
+      tc::fence_after();
+      const uint32_t sf = qbase + 16 * s;
+      tc::st4(sf, wa.x, wa.y, wa.z, wa.w);
+      tc::st4(sf + 8, wb0.x, wb0.y, wb0.z, wb0.w);
+      if (M::kSfBlocks > 1) {
+        const uint4 wb1 =
+            *reinterpret_cast<const uint4*>(sb + kAStage + M::kPanelRows * kTcStepK + 512 + 16 * lane);
+        tc::st4(sf + 12, wb1.x, wb1.y, wb1.z, wb1.w);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      mbar_arrive(&ready[s]);
+    }
   } else if (warp >= kEpiWarp0) {
-    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31; the two warps of a
-    // quadrant take alternate 16-column chunks
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31; the warps of a
+    // quadrant take 16-column chunks in turn
     const int qd = warp & 3, eg = (warp - kEpiWarp0) >> 2, ew = warp - kEpiWarp0, et = tid - kEpiWarp0 * 32;
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     // gate/up: TMEM lane l of a quadrant is f offset kk(l) within its 32-element block
@@ -412,7 +433,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       tc::fence_after();
       if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
         const int row = 128 * g.mt + 32 * qd + lane;
-        for (int c0 = 16 * eg; c0 < npad; c0 += 32) {
+        for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
           float v[16], w[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) v[x] = 0.f;
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       } else {
         // 1. accumulators -> hx[block][token][f offset]: blocks 0, 1 gate, 2, 3 up
         named_bar(1, kEpiThreads);  // the previous unit's readers of hx are done
-        for (int c0 = 16 * eg; c0 < npad; c0 += 32) {
+        for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
           float v[16], w[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) v[x] = 0.f;
