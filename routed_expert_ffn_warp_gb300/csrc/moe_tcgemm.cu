@@ -48,7 +48,6 @@ using namespace dev;
 
 constexpr int kThr = 576;                  // 18 warps: see the roles below
 constexpr int kMaxTok = kTcGemmRows;       // tokens per unit
-constexpr int kPf = 12;                    // L2 prefetch distance of the weight blocks, in K steps
 constexpr int kAOp = 128 * kTcStepK;       // widened E2M1 operand: 16 bytes per 16 elements
 constexpr int kAStage = kAOp + 512;        // [operand | SFA]
 constexpr int kCmRows = kTcBlockBytes / 64;  // 64-byte tensor rows per weight block (8,192 code + 512 scale bytes)
@@ -82,6 +81,9 @@ struct Mode {
   static constexpr int kMma = 2;                   // MMA lanes
   static constexpr int kDCol = kDown ? 192 : 96;   // accumulator width (N <= kDCol); buffer b, lane t at kDCol (kMma b + t)
   static constexpr int kBufs = kDown ? 1 : 2;      // accumulator buffers (units in flight between MMA and epilogue)
+  // L2 prefetch distance of the weight blocks, in K steps (measured: it
+  // shortens the down GEMM and lengthens gate/up, whose panel reads compete)
+  static constexpr int kPf = kDown ? 12 : 0;
   static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values [4 blocks][token][32]
   static_assert(kBufs * kMma * kDCol <= kSfCol && kS <= 8, "TMEM columns");
 };
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       ca.ks = cp.ks = 0;
       ca.g = cp.g = tc_unit<kDown>(p, st, b0);
       // weight blocks are read once: start them towards L2 kPf steps before their tensor copy
-      for (int q = 0; q < kPf && cp.i < n_units; ++q) {
+      for (int q = 0; q < M::kPf && cp.i < n_units; ++q) {
         prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
         cursor_next<kDown>(p, st, cp, n_units);
       }
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         mbar_arrive_expect_tx(&full[s], (uint32_t)kTcBlockBytes);
         tc::tma_load_2d(sb, &wmap, 0, ca.g.y + ca.ks * kCmRows, &full[s]);
         bulk_g2s(sb + kAOp, ca.g.w + (size_t)ca.ks * kTcBlockBytes + kTcCodeBytes, 512, &full[s]);
-        if (cp.i < n_units) {
+        if (M::kPf > 0 && cp.i < n_units) {
           prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
           cursor_next<kDown>(p, st, cp, n_units);
         }
