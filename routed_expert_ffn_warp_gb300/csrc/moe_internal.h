@@ -84,6 +84,9 @@ constexpr int kTcPanelStep = kTcPanelRows * kTcStepK + 512;
 constexpr int kTcPanelRowsD = 192;
 constexpr int kTcPanelStepD = kTcPanelRowsD * kTcStepK + 1024;
 __host__ __device__ inline int tc_dtiles(int d) { return (d + 127) / 128; }
+// Units of the tcgen05 GEMMs per (slot, token block): pairs of M tiles.
+__host__ __device__ inline int tc_gu_pairs(int f) { return (tc_msteps(f) + 1) / 2; }
+__host__ __device__ inline int tc_dn_pairs(int d) { return (tc_dtiles(d) + 1) / 2; }
 __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
   return (size_t)tc_dtiles(d) * tc_ksteps(f) * kTcBlockBytes;
 }

@@ -492,8 +492,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   const bool nz = tid < E && cnt > 0;
   const int blocks = (cnt + kGemmRows - 1) / kGemmRows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
   const int ugu = !nz ? 0
-                      : p.tc_gateup ? tcb * ((p.F / 16 + 3) / 4) : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
-  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dtiles(p.d) : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+                      : p.tc_gateup ? tcb * tc_gu_pairs(p.F) : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
+  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dn_pairs(p.d) : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
   int ns, gu, dn, pn;
   const int slot = block_exclusive_scan(nz ? 1 : 0, wsum, &ns);
   const int gpre = block_exclusive_scan(ugu, wsum, &gu);
@@ -517,9 +517,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       if (p.tc_gateup) p.panel_prefix[ns] = pn;
       pn += (T + kTcGemmRows - 1) / kTcGemmRows;
       const int sb = (T + kGemmRows - 1) / kGemmRows;
-      gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * ((p.S / 16 + 3) / 4)
+      gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_gu_pairs(p.S)
                         : sb * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
-      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dtiles(p.d)
+      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dn_pairs(p.d)
                         : sb * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
       ++ns;
     }

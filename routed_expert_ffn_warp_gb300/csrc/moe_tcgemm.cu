@@ -11,9 +11,10 @@
 // gate (up) value is D[., m] + D[., npad + m]. h enters the down GEMM the same
 // way in four planes (about 16 significant bits per block).
 //
-// Work unit: (slot, M tile, block of up to 48 tokens of the slot), K in steps
-// of 128 (four K=32 MMAs). Gate/up: M tile = 64 gate + 64 up rows (4 pair
-// tiles), K = d. Down: M tile = 128 rows of d, K = f. The weights come from
+// Work unit: (slot, pair of M tiles, block of up to 48 tokens of the slot), K
+// in steps of 128 (four K=32 MMAs per M tile). Gate/up: M tile = 64 gate + 64
+// up rows (4 pair tiles), K = d. Down: M tile = 128 rows of d, K = f. The two
+// M tiles of a unit share each K step's activation panel. The weights come from
 // their own copy, one contiguous block per (M tile, K step) in the operand's
 // core-matrix order with the E2M1 codes packed; a TMA tensor copy of the
 // 4-bit "16 x U4, 16-byte aligned" type widens every 8 code bytes to the
@@ -46,46 +47,43 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThr = 576;                  // 18 warps: see the roles below
+constexpr int kThr = 512;                  // 16 warps: see the roles below
 constexpr int kMaxTok = kTcGemmRows;       // tokens per unit
 constexpr int kAOp = 128 * kTcStepK;       // widened E2M1 operand: 16 bytes per 16 elements
 constexpr int kAStage = kAOp + 512;        // [operand | SFA]
 constexpr int kCmRows = kTcBlockBytes / 64;  // 64-byte tensor rows per weight block (8,192 code + 512 scale bytes)
 constexpr uint32_t kTmemCols = 512;        // accumulators from column 0, scale factors from 384
-constexpr int kSfCol = 384;                // set s (the stage): SFA columns +16 s .. +3, SFB +8 .. +15
+constexpr int kSfCol = 384;                // set s (the stage) at +32 s: SFA of M tile 0 / 1 at +0 / +8, SFB at +16
+constexpr int kSfSet = 32;
 constexpr long long kWaitNs = 50000000LL;
-// roles: warp 0 weights, 1 activations, 2 .. 5 MMA lanes, 6 .. 9 scale factors to TMEM, 10 .. 17
+// roles: warp 0 weights, 1 activations, 2 and 3 MMA lanes, 4 .. 7 scale factors to TMEM, 8 .. 15
 // epilogue (a warp's TMEM lane quadrant is warp % 4)
-constexpr int kProducerWarp = 0, kPanelWarp = 1, kMmaWarp0 = 2, kSfWarp0 = 6, kEpiWarp0 = 10, kEpiThreads = 256;
+constexpr int kProducerWarp = 0, kPanelWarp = 1, kMmaWarp0 = 2, kSfWarp0 = 4, kEpiWarp0 = 8, kEpiThreads = 256;
 constexpr int kEpiPerQuad = kEpiThreads / 128;  // epilogue warps per TMEM lane quadrant
 
 // The two uses of the GEMM. Gate/up: M tiles of 64 gate + 64 up rows, K = d,
 // B = x in 2 MXFP8 planes, epilogue h = SiLU(gate) * up into the h panels.
 // Down: M tiles of 128 rows of d, K = f, B = h in 4 MXFP8 planes, epilogue
-// part = D. A stage holds one K step of both operands: [A | B panel step].
-// With kMma MMA lanes, lane t takes the CTA's K steps j = t (mod kMma) and
-// accumulates them in its own accumulator (the epilogue adds them): a lane
-// issues its MMAs, waits for its next stage and copies that stage's scale
-// factors in turn, and only with several lanes does one of them keep the
-// tensor core busy meanwhile. The accumulators of all lanes fill the 384
-// TMEM columns below the scale factors, so a unit's MMAs start once the
-// epilogue has read the previous unit's accumulators.
+// part = D. A stage holds one K step of both operands: [A of M tile 0 | A of
+// M tile 1 | B panel step]. MMA lane t issues the MMAs of M tile t of the
+// unit into its own accumulator.
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
   static constexpr int kPanelRows = kDown ? kTcPanelRowsD : kTcPanelRows;
   static constexpr int kPanelStep = kDown ? kTcPanelStepD : kTcPanelStep;
   static constexpr int kSfBlocks = kDown ? 2 : 1;  // 512-byte B scale blocks per panel step (32 rows x 4 words each)
-  static constexpr int kStage = kAStage + kPanelStep;
-  static constexpr int kS = kDown ? 5 : 6;         // stages (scale sets in TMEM: at most 8)
-  static constexpr int kMma = 2;                   // MMA lanes
+  static constexpr int kAPair = 2 * kAStage;
+  static constexpr int kStage = kAPair + kPanelStep;
+  static constexpr int kS = kDown ? 3 : 4;         // stages
+  static constexpr int kMma = 2;                   // MMA lanes = M tiles of a unit
   static constexpr int kDCol = kDown ? 192 : 96;   // accumulator width (N <= kDCol); buffer b, lane t at kDCol (kMma b + t)
   static constexpr int kBufs = kDown ? 1 : 2;      // accumulator buffers (units in flight between MMA and epilogue)
   // L2 prefetch distance of the weight blocks, in K steps (measured: it
   // shortens the down GEMM and lengthens gate/up, whose panel reads compete)
   static constexpr int kPf = kDown ? 12 : 0;
-  static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values [4 blocks][token][32]
-  static_assert(kBufs * kMma * kDCol <= kSfCol && kS <= 8, "TMEM columns");
+  static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values of one M tile [4 blocks][token][32]
+  static_assert(kBufs * kMma * kDCol <= kSfCol && kSfCol + kS * kSfSet <= (int)kTmemCols, "TMEM columns");
 };
 
 // Per-slot tables the roles look units up in, copied to shared memory once:
@@ -143,11 +141,11 @@ struct SlotTab {
 struct TcUnit {
   int e, f;     // expert (E = shared) and its ffn
   int q0, n;    // first h/part row and tokens of the block
-  int mt;       // M tile
+  int mt, nt;   // first M tile of the pair and tiles in it (1 or 2)
   int nks;      // K steps
   int panel;    // panel of the (slot, token block)
-  int y;        // tensor row (64 bytes each) of the M tile's first weight block
-  const uint8_t* w;  // weight blocks of the M tile (K step 0)
+  int y;        // tensor row (64 bytes each) of M tile mt's first weight block (tile mt + 1: + nks * kCmRows)
+  const uint8_t* w;  // weight blocks of M tile mt (K step 0; tile mt + 1: + nks * kTcBlockBytes)
 };
 
 template <bool kDown>
@@ -157,9 +155,10 @@ __device__ __forceinline__ TcUnit tc_unit(const FwdParams& p, const SlotTab& st,
   TcUnit g;
   g.e = st.sexp[s];
   g.f = (g.e == p.E) ? p.S : p.F;
-  const int ngrp = kDown ? tc_dtiles(p.d) : tc_msteps(g.f);
+  const int ntiles = kDown ? tc_dtiles(p.d) : tc_msteps(g.f), ngrp = (ntiles + 1) / 2;
   const int tb = r / ngrp;
-  g.mt = r - tb * ngrp;
+  g.mt = 2 * (r - tb * ngrp);
+  g.nt = min(2, ntiles - g.mt);
   g.q0 = st.sq0[s] + kMaxTok * tb;
   g.n = min(kMaxTok, st.sn[s] - kMaxTok * tb);
   g.nks = tc_ksteps(kDown ? g.f : p.d);
@@ -285,14 +284,15 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   }
   // the tensor copies write the first 8 bytes of every 16-byte operand row;
   // the other 8 stay as set here
-  for (int c = tid; c < kS * (kAOp / 16); c += kThr)
-    *reinterpret_cast<uint2*>(stg + (size_t)(c / (kAOp / 16)) * M::kStage + 16 * (c % (kAOp / 16)) + 8) =
+  for (int c = tid; c < kS * 2 * (kAOp / 16); c += kThr)
+    *reinterpret_cast<uint2*>(stg + (size_t)(c / (2 * (kAOp / 16))) * M::kStage +
+                              (size_t)((c / (kAOp / 16)) & 1) * kAStage + 16 * (c % (kAOp / 16)) + 8) =
         make_uint2(0u, 0u);
   tc::fence_proxy_async();
   if (tid == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(&full[s], 2);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kMma);
       mbar_init(&ready[s], 128);
     }
     for (int a = 0; a < kBufs; ++a) {
@@ -315,22 +315,24 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       ca.ks = cp.ks = 0;
       ca.g = cp.g = tc_unit<kDown>(p, st, b0);
       // weight blocks are read once: start them towards L2 kPf steps before their tensor copy
-      for (int q = 0; q < M::kPf && cp.i < n_units; ++q) {
-        prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
+      auto prefetch = [&]() {
+        for (int t = 0; t < cp.g.nt; ++t)
+          prefetch_l2(cp.g.w + ((size_t)t * cp.g.nks + cp.ks) * kTcBlockBytes, kTcBlockBytes);
         cursor_next<kDown>(p, st, cp, n_units);
-      }
+      };
+      for (int q = 0; q < M::kPf && cp.i < n_units; ++q) prefetch();
       for (int j = 0; ca.i < n_units; ++j) {
         const int s = j % kS;
         if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
         uint8_t* sb = stg + (size_t)s * M::kStage;
-        // 8,192 code bytes (counted as read from global memory) + 512 scale bytes
-        mbar_arrive_expect_tx(&full[s], (uint32_t)kTcBlockBytes);
-        tc::tma_load_2d(sb, &wmap, 0, ca.g.y + ca.ks * kCmRows, &full[s]);
-        bulk_g2s(sb + kAOp, ca.g.w + (size_t)ca.ks * kTcBlockBytes + kTcCodeBytes, 512, &full[s]);
-        if (M::kPf > 0 && cp.i < n_units) {
-          prefetch_l2(cp.g.w + (size_t)cp.ks * kTcBlockBytes, kTcBlockBytes);
-          cursor_next<kDown>(p, st, cp, n_units);
+        // per M tile: 8,192 code bytes (counted as read from global memory) + 512 scale bytes
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(ca.g.nt * kTcBlockBytes));
+        for (int t = 0; t < ca.g.nt; ++t) {
+          tc::tma_load_2d(sb + t * kAStage, &wmap, 0, ca.g.y + (t * ca.g.nks + ca.ks) * kCmRows, &full[s]);
+          bulk_g2s(sb + t * kAStage + kAOp, ca.g.w + ((size_t)t * ca.g.nks + ca.ks) * kTcBlockBytes + kTcCodeBytes,
+                   512, &full[s]);
         }
+        if (M::kPf > 0 && cp.i < n_units) prefetch();
         cursor_next<kDown>(p, st, ca, n_units);
       }
     }
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         const int s = j % kS;
         if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
         const int N = M::kPlanes * npad_of(cb.g.n);
-        uint8_t* sb = stg + (size_t)s * M::kStage + kAStage;
+        uint8_t* sb = stg + (size_t)s * M::kStage + M::kAPair;
         const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
         mbar_arrive_expect_tx(&full[s], (uint32_t)(N * kTcStepK + 512 * M::kSfBlocks));
         bulk_g2s(sb, src, (uint32_t)(N * kTcStepK), &full[s]);
@@ -356,64 +358,69 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + kMma) {
     if (lane == 0) {
-      const int t = warp - kMmaWarp0;
-      int j0 = 0;  // first K step of unit i
+      const int t = warp - kMmaWarp0;  // M tile t of every unit
+      int j0 = 0;                      // first K step of unit i
       for (int i = 0; i < n_units; ++i) {
         const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
         const int N = M::kPlanes * npad_of(g.n), acc = i % kBufs;
-        const int first = ((t - j0) % kMma + kMma) % kMma;  // this lane's first K step of the unit
-        // every lane, with or without K steps in this unit, waits for the
-        // buffer's previous unit to be read: its arrival on accfull then
-        // belongs to this unit's phase
+        const bool mine = t < g.nt;  // a pair of one tile leaves lane 1 without MMAs
         if (i >= kBufs) bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status);
         tc::fence_after();
-        if (first >= g.nks) tc::commit(&accfull[acc]);  // no K step of this unit
         const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
-        for (int ks = first; ks < g.nks; ks += kMma) {
+        for (int ks = 0; ks < g.nks; ++ks) {
           const int jj = j0 + ks, s = jj % kS;
+          // every lane takes part in every step's hand-off, with or without MMAs
           bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status);  // operands landed, scales in TMEM
           tc::fence_after();
-          const uint8_t* ab = stg + (size_t)s * M::kStage;
-          const uint8_t* bb = ab + kAStage;
-          const uint32_t sf = tmem + kSfCol + 16 * s;
+          if (mine) {
+            const uint8_t* ab = stg + (size_t)s * M::kStage + (size_t)t * kAStage;
+            const uint8_t* bb = stg + (size_t)s * M::kStage + M::kAPair;
+            const uint32_t sf = tmem + kSfCol + kSfSet * s;
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const uint64_t ad = tc::smem_desc(ab + 2 * kb * 128, 128, 8 * 128);
-            const uint64_t bd = tc::smem_desc(bb + 2 * kb * 128, 128, 8 * 128);
-            tc::mma_mxf4_mxf8(d, ad, bd, tc::idesc_mxf4_mxf8(128, N, kb, kb), sf, sf + 8,
-                              (ks > first || kb > 0) ? 1u : 0u);
+            for (int kb = 0; kb < 4; ++kb) {
+              const uint64_t ad = tc::smem_desc(ab + 2 * kb * 128, 128, 8 * 128);
+              const uint64_t bd = tc::smem_desc(bb + 2 * kb * 128, 128, 8 * 128);
+              tc::mma_mxf4_mxf8(d, ad, bd, tc::idesc_mxf4_mxf8(128, N, kb, kb), sf + 8 * t, sf + 16,
+                                (ks > 0 || kb > 0) ? 1u : 0u);
+            }
           }
           tc::commit(&empty[s]);
-          if (ks + kMma >= g.nks) tc::commit(&accfull[acc]);  // this lane's last K step of the unit
         }
+        tc::commit(&accfull[acc]);
         j0 += g.nks;
       }
     }
   } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
     // scale factors of every stage into TMEM set s, in the warp's lane
-    // quadrant (each quadrant holds the same copy): SFA words [lane][4] to
-    // columns +0 .. +3, SFB to +8 .. (+4 per 512-byte block)
+    // quadrant (each quadrant holds the same copy): SFA words [lane][4] of M
+    // tile 0 / 1 to columns +0 / +8, SFB to +16 (+4 per 512-byte block)
     const uint32_t qbase = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol;
-    int jtot = 0;  // K steps of the CTA
-    for (int i = 0; i < n_units; ++i) jtot += tc_unit<kDown>(p, st, b0 + i * G).nks;
-    for (int j = 0; j < jtot; ++j) {
-      const int s = j % kS;
-      bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status);
-      const uint8_t* sb = stg + (size_t)s * M::kStage;
-      const uint4 wa = *reinterpret_cast<const uint4*>(sb + kAOp + 16 * lane);
-      const uint4 wb0 = *reinterpret_cast<const uint4*>(sb + kAStage + M::kPanelRows * kTcStepK + 16 * lane);
-      tc::fence_after();
-      const uint32_t sf = qbase + 16 * s;
-      tc::st4(sf, wa.x, wa.y, wa.z, wa.w);
-      tc::st4(sf + 8, wb0.x, wb0.y, wb0.z, wb0.w);
-      if (M::kSfBlocks > 1) {
-        const uint4 wb1 =
-            *reinterpret_cast<const uint4*>(sb + kAStage + M::kPanelRows * kTcStepK + 512 + 16 * lane);
-        tc::st4(sf + 12, wb1.x, wb1.y, wb1.z, wb1.w);
+    int j = 0;
+    for (int i = 0; i < n_units; ++i) {
+      const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
+      for (int ks = 0; ks < g.nks; ++ks, ++j) {
+        const int s = j % kS;
+        bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status);
+        const uint8_t* sb = stg + (size_t)s * M::kStage;
+        const uint8_t* sbf = sb + M::kAPair + M::kPanelRows * kTcStepK;
+        const uint4 wa0 = *reinterpret_cast<const uint4*>(sb + kAOp + 16 * lane);
+        const uint4 wb0 = *reinterpret_cast<const uint4*>(sbf + 16 * lane);
+        tc::fence_after();
+        const uint32_t sf = qbase + kSfSet * s;
+        tc::st4(sf, wa0.x, wa0.y, wa0.z, wa0.w);
+        if (g.nt > 1) {
+          const uint4 wa1 = *reinterpret_cast<const uint4*>(sb + kAStage + kAOp + 16 * lane);
+          tc::st4(sf + 8, wa1.x, wa1.y, wa1.z, wa1.w);
+        }
+        tc::st4(sf + 16, wb0.x, wb0.y, wb0.z, wb0.w);
+        if (M::kSfBlocks > 1) {
+          const uint4 wb1 = *reinterpret_cast<const uint4*>(sbf + 512 + 16 * lane);
+          tc::st4(sf + 20, wb1.x, wb1.y, wb1.z, wb1.w);
+        }
+        tc::wait_st();
+        tc::fence_before();
+        mbar_arrive(&ready[s]);
       }
-      tc::wait_st();
-      tc::fence_before();
-      mbar_arrive(&ready[s]);
     }
   } else if (warp >= kEpiWarp0) {
     // epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31; the warps of a
@@ -423,96 +430,87 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     // gate/up: TMEM lane l of a quadrant is f offset kk(l) within its 32-element block
     const int kk = 8 * ((lane & 15) >> 2) + 4 * (lane >> 4) + (lane & 3);
     const int pstride = tc_ksteps(p.F > p.S ? p.F : p.S);
-    int j0 = 0;
     for (int i = 0; i < n_units; ++i) {
       const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
       const int npad = npad_of(g.n), acc = i % kBufs;
-      // MMA lanes with at least one K step of this unit
-      const int nacc = g.nks >= kMma ? kMma : g.nks;
-      const int t0 = j0 % kMma;  // the lane of the unit's first K step
-      j0 += g.nks;
       bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status);
       tc::fence_after();
-      if (kDown) {  // part rows q0 + m, column 128 mt + 32 qd + lane: the sum of the 4 planes
-        const int row = 128 * g.mt + 32 * qd + lane;
-        for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
-          float v[16], w[16];
+      if (kDown) {  // part rows q0 + m, column 128 (mt + t) + 32 qd + lane: the sum of the 4 planes
+        for (int t = 0; t < g.nt; ++t) {
+          const int row = 128 * (g.mt + t) + 32 * qd + lane;
+          const uint32_t dcol = trow + M::kDCol * (kMma * acc + t);
+          for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
+            float v[16], w[16];
+            tc::ld16(dcol + c0, v);
 #pragma unroll
-          for (int x = 0; x < 16; ++x) v[x] = 0.f;
-          for (int a = 0; a < nacc; ++a) {
-            const uint32_t dcol = trow + M::kDCol * (kMma * acc + (t0 + a) % kMma);
-#pragma unroll
-            for (int pl = 0; pl < 4; ++pl) {
+            for (int pl = 1; pl < 4; ++pl) {
               tc::ld16(dcol + pl * npad + c0, w);
 #pragma unroll
               for (int x = 0; x < 16; ++x) v[x] += w[x];
             }
-          }
-          if (row < p.d) {
+            if (row < p.d) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x)
-              if (c0 + x < g.n) p.part[(size_t)(g.q0 + c0 + x) * p.d + row] = v[x];
+              for (int x = 0; x < 16; ++x)
+                if (c0 + x < g.n) p.part[(size_t)(g.q0 + c0 + x) * p.d + row] = v[x];
+            }
           }
         }
         tc::fence_before();
         mbar_arrive(&accempty[acc]);
       } else {
-        // 1. accumulators -> hx[block][token][f offset]: blocks 0, 1 gate, 2, 3 up
-        named_bar(1, kEpiThreads);  // the previous unit's readers of hx are done
-        for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
-          float v[16], w[16];
+        for (int t = 0; t < g.nt; ++t) {
+          const int mt = g.mt + t;
+          // 1. accumulator of M tile mt -> hx[block][token][f offset]: blocks 0, 1 gate, 2, 3 up
+          named_bar(1, kEpiThreads);  // the previous readers of hx are done
+          const uint32_t dcol = trow + M::kDCol * (kMma * acc + t);
+          for (int c0 = 16 * eg; c0 < npad; c0 += 16 * kEpiPerQuad) {
+            float v[16], w[16];
+            tc::ld16(dcol + c0, v);
+            tc::ld16(dcol + npad + c0, w);
 #pragma unroll
-          for (int x = 0; x < 16; ++x) v[x] = 0.f;
-          for (int a = 0; a < nacc; ++a) {
-            const uint32_t dcol = trow + M::kDCol * (kMma * acc + (t0 + a) % kMma);
+            for (int x = 0; x < 16; ++x)
+              if (c0 + x < npad) hx[(qd * kMaxTok + c0 + x) * 32 + kk] = v[x] + w[x];
+          }
+          if (t == g.nt - 1) {
+            tc::fence_before();
+            mbar_arrive(&accempty[acc]);  // every accumulator of the unit has been read
+          }
+          named_bar(1, kEpiThreads);
+          // 2. h = SiLU(gate) * up, four MXFP8 planes, straight into the down step's
+          // h panel: f block 2 mt + b is K step mt / 2, elements 64 (mt % 2) + 32 b ..
+          uint8_t* dst = p.hpanel + ((size_t)g.panel * pstride + (mt >> 1)) * kTcPanelStepD;
+          const int kh = 64 * (mt & 1), nblk = g.f / 32;
+          for (int it = ew; it < 2 * npad; it += kEpiThreads / 32) {
+            const int m = it >> 1, b = it & 1;
+            float h = 0.f;
+            if (m < g.n && 2 * mt + b < nblk) {
+              const float gate = hx[(b * kMaxTok + m) * 32 + lane], up = hx[((2 + b) * kMaxTok + m) * 32 + lane];
+              h = gate / (1.f + __expf(-gate)) * up;
+            }
+            uint32_t code[4], sc[4];
+            split_planes4_fixed(h, code, sc);
+            const int k = kh + 32 * b + lane;
 #pragma unroll
-            for (int pl = 0; pl < 2; ++pl) {
-              tc::ld16(dcol + pl * npad + c0, w);
-#pragma unroll
-              for (int x = 0; x < 16; ++x) v[x] += w[x];
+            for (int pl = 0; pl < 4; ++pl) {
+              const int row = pl * npad + m;
+              dst[((row >> 3) * 8 + (k >> 4)) * 128 + (row & 7) * 16 + (k & 15)] = (uint8_t)code[pl];
+            }
+            if (lane < 4) {
+              const uint32_t sv = lane == 0 ? sc[0] : lane == 1 ? sc[1] : lane == 2 ? sc[2] : sc[3];
+              dst[hsf_off(lane * npad + m, 2 * (mt & 1) + b)] = (uint8_t)sv;
             }
           }
-#pragma unroll
-          for (int x = 0; x < 16; ++x)
-            if (c0 + x < npad) hx[(qd * kMaxTok + c0 + x) * 32 + kk] = v[x];
-        }
-        tc::fence_before();
-        mbar_arrive(&accempty[acc]);  // the accumulator buffer is free for the unit after next
-        named_bar(1, kEpiThreads);
-        // 2. h = SiLU(gate) * up, four MXFP8 planes, straight into the down step's
-        // h panel: f block 2 mt + b is K step mt / 2, elements 64 (mt % 2) + 32 b ..
-        uint8_t* dst = p.hpanel + ((size_t)g.panel * pstride + (g.mt >> 1)) * kTcPanelStepD;
-        const int kh = 64 * (g.mt & 1), nblk = g.f / 32;
-        for (int it = ew; it < 2 * npad; it += kEpiThreads / 32) {
-          const int m = it >> 1, b = it & 1;
-          float h = 0.f;
-          if (m < g.n && 2 * g.mt + b < nblk) {
-            const float gate = hx[(b * kMaxTok + m) * 32 + lane], up = hx[((2 + b) * kMaxTok + m) * 32 + lane];
-            h = gate / (1.f + __expf(-gate)) * up;
+          // 3. scale bytes of the rows past the 4 planes (127), and the half K step
+          // past the last M tile when the tile count is odd (codes 0, scales 127)
+          for (int o = et; o < 2 * (kTcPanelRowsD - 4 * npad); o += kEpiThreads)
+            dst[hsf_off(4 * npad + (o >> 1), 2 * (mt & 1) + (o & 1))] = 127;
+          if ((mt & 1) == 0 && mt + 1 == tc_msteps(g.f)) {
+            for (int o = et; o < 4 * npad * 4; o += kEpiThreads) {
+              const int row = o >> 2, kc = 4 + (o & 3);
+              *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            for (int o = et; o < 2 * kTcPanelRowsD; o += kEpiThreads) dst[hsf_off(o >> 1, 2 + (o & 1))] = 127;
           }
-          uint32_t code[4], sc[4];
-          split_planes4_fixed(h, code, sc);
-          const int k = kh + 32 * b + lane;
-#pragma unroll
-          for (int pl = 0; pl < 4; ++pl) {
-            const int row = pl * npad + m;
-            dst[((row >> 3) * 8 + (k >> 4)) * 128 + (row & 7) * 16 + (k & 15)] = (uint8_t)code[pl];
-          }
-          if (lane < 4) {
-            const uint32_t s = lane == 0 ? sc[0] : lane == 1 ? sc[1] : lane == 2 ? sc[2] : sc[3];
-            dst[hsf_off(lane * npad + m, 2 * (g.mt & 1) + b)] = (uint8_t)s;
-          }
-        }
-        // 3. scale bytes of the rows past the 4 planes (127), and the half K step
-        // past the last M tile when the tile count is odd (codes 0, scales 127)
-        for (int o = et; o < 2 * (kTcPanelRowsD - 4 * npad); o += kEpiThreads)
-          dst[hsf_off(4 * npad + (o >> 1), 2 * (g.mt & 1) + (o & 1))] = 127;
-        if ((g.mt & 1) == 0 && g.mt + 1 == tc_msteps(g.f)) {
-          for (int o = et; o < 4 * npad * 4; o += kEpiThreads) {
-            const int row = o >> 2, kc = 4 + (o & 3);
-            *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          for (int o = et; o < 2 * kTcPanelRowsD; o += kEpiThreads) dst[hsf_off(o >> 1, 2 + (o & 1))] = 127;
         }
       }
     }
