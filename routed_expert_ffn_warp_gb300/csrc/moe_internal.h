@@ -47,48 +47,52 @@ __host__ __device__ inline size_t expert_packed_bytes(int d, int f) {
 }
 
 // Second copy of the gate/up weights for the block-scaled tcgen05 GEMM of the
-// general path: per expert, blocks of kTcBlockBytes ordered [M tile a][K step
-// ks]. M tile a is the 64 gate rows then the 64 up rows of pair tiles 4a ..
-// 4a+3 (M row m: tile t = m / 16 -- pair tile 4a + t % 4, gate if t < 4 --
-// and row m % 16 of it); a K step is 128 elements of d. A block is
-//  * 8,192 code bytes in core-matrix order: the 8 packed bytes (16 codes,
-//    low nibble = even element) of M row m and 16-element chunk kc at
-//    ((m / 8) * 8 + kc) * 64 + (m % 8) * 8, so that widening every 8 bytes to
-//    16 (what a TMA copy of the "16 x U4, 16-byte aligned" type does) gives
-//    the K-major operand layout of the MMA (LBO 128, SBO 1024);
-//  * 512 scale bytes as 32-bit words [lane l][r]: byte kb of word (l, r) is
-//    the scale of M row 32 r + l in K block 4 ks + kb, the order tcgen05.cp
-//    copies to tensor memory.
-// Rows of missing pair tiles and K past d are code 0 with scale 127.
+// general path. M tile a is the 64 gate rows then the 64 up rows of pair
+// tiles 4a .. 4a+3 (M row m: tile t = m / 16 -- pair tile 4a + t % 4, gate if
+// t < 4 -- and row m % 16 of it); a K step is 128 elements of d. Per expert,
+// blocks of kTcPairBytes ordered [tile pair P = a / 2][K step ks], each
+//  * the 8,192 code bytes of M tile 2P, then those of M tile 2P + 1, in
+//    core-matrix order: the 8 packed bytes (16 codes, low nibble = even
+//    element) of M row m and 16-element chunk kc at ((m / 8) * 8 + kc) * 64 +
+//    (m % 8) * 8, so that widening every 8 bytes to 16 (what a TMA copy of the
+//    "16 x U4, 16-byte aligned" type does) gives the K-major operand layout of
+//    the MMA (LBO 128, SBO 1024) -- one tensor copy takes both tiles;
+//  * 512 scale bytes of M tile 2P, then 512 of M tile 2P + 1, as 32-bit words
+//    [lane l][r]: byte kb of word (l, r) is the scale of M row 32 r + l in K
+//    block 4 ks + kb, the order tcgen05.st writes them to tensor memory.
+// Rows of missing pair tiles (also the whole second tile of the last pair
+// when the tile count is odd) and K past d are code 0 with scale 127.
 constexpr int kTcStepK = 128;
 constexpr int kTcCodeBytes = 8192;
-constexpr int kTcBlockBytes = kTcCodeBytes + 512;
+constexpr int kTcPairBytes = 2 * kTcCodeBytes + 1024;
 __host__ __device__ inline int tc_msteps(int f) { return (f / 16 + 3) / 4; }
 __host__ __device__ inline int tc_ksteps(int d) { return (d + kTcStepK - 1) / kTcStepK; }
+__host__ __device__ inline int tc_dtiles(int d) { return (d + 127) / 128; }
+// Units of the tcgen05 GEMMs per (slot, token block): pairs of M tiles.
+__host__ __device__ inline int tc_gu_pairs(int f) { return (tc_msteps(f) + 1) / 2; }
+__host__ __device__ inline int tc_dn_pairs(int d) { return (tc_dtiles(d) + 1) / 2; }
 __host__ __device__ inline size_t tc_expert_bytes(int d, int f) {
-  return (size_t)tc_msteps(f) * tc_ksteps(d) * kTcBlockBytes;
+  return (size_t)tc_gu_pairs(f) * tc_ksteps(d) * kTcPairBytes;
 }
 // Activation panels of the tcgen05 gate/up GEMM: per (slot, block of up to 48
-// tokens) and K step, the B operand -- row n = plane * npad + m (hi plane
-// rows, then lo plane rows; npad = tokens rounded up to 8, at least 8) --
-// in core-matrix order ((n / 8) * 8 + kc) * 128 + (n % 8) * 16, then 512
-// scale bytes as words [lane l][r] for B row 32 r + l (127 past the rows).
+// tokens) and K step, the B operand -- N = 2 npad rows, row n = plane * npad
+// + m (hi plane rows, then lo plane rows; npad = tokens rounded up to 8, at
+// least 8) -- in core-matrix order ((n / 8) * 8 + kc) * 128 + (n % 8) * 16,
+// directly followed (at N * 128) by 512 scale bytes as words [lane l][r] for
+// B row 32 r + l (127 past the rows), so that one bulk copy takes the step.
 constexpr int kTcPanelRows = 96;
 constexpr int kTcPanelStep = kTcPanelRows * kTcStepK + 512;
 // The down projection on the same GEMM: a weight copy of the down matrices in
 // the same block format (M tile a = rows 128a .. 128a+127 of d, K steps of 128
 // over f; rows past d are code 0 with scale 127) and per-(slot, token block)
-// panels of h as four MXFP8 planes (row n = plane * npad + m, up to 192 rows;
-// scales as two 512-byte blocks of words [lane l][r % 4] for B row 32 r + l,
-// block r / 4), written by the gate/up GEMM's epilogue.
+// panels of h as four MXFP8 planes (N = 4 npad rows, row n = plane * npad + m,
+// up to 192 rows; then, at N * 128, scales as two 512-byte blocks of words
+// [lane l][r % 4] for B row 32 r + l, block r / 4), written by the gate/up
+// GEMM's epilogue.
 constexpr int kTcPanelRowsD = 192;
 constexpr int kTcPanelStepD = kTcPanelRowsD * kTcStepK + 1024;
-__host__ __device__ inline int tc_dtiles(int d) { return (d + 127) / 128; }
-// Units of the tcgen05 GEMMs per (slot, token block): pairs of M tiles.
-__host__ __device__ inline int tc_gu_pairs(int f) { return (tc_msteps(f) + 1) / 2; }
-__host__ __device__ inline int tc_dn_pairs(int d) { return (tc_dtiles(d) + 1) / 2; }
 __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
-  return (size_t)tc_dtiles(d) * tc_ksteps(f) * kTcBlockBytes;
+  return (size_t)tc_dn_pairs(d) * tc_ksteps(f) * kTcPairBytes;
 }
 
 // ---------------------------------------------------------------- forward parameters

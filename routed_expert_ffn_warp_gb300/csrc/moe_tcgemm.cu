@@ -50,8 +50,7 @@ using namespace dev;
 constexpr int kThr = 512;                  // 16 warps: see the roles below
 constexpr int kMaxTok = kTcGemmRows;       // tokens per unit
 constexpr int kAOp = 128 * kTcStepK;       // widened E2M1 operand: 16 bytes per 16 elements
-constexpr int kAStage = kAOp + 512;        // [operand | SFA]
-constexpr int kCmRows = kTcBlockBytes / 64;  // 64-byte tensor rows per weight block (8,192 code + 512 scale bytes)
+constexpr int kCmRows = kTcPairBytes / 64;  // 64-byte tensor rows per weight block of a tile pair
 constexpr uint32_t kTmemCols = 512;        // accumulators from column 0, scale factors from 384
 constexpr int kSfCol = 384;                // set s (the stage) at +32 s: SFA of M tile 0 / 1 at +0 / +8, SFB at +16
 constexpr int kSfSet = 32;
@@ -65,15 +64,15 @@ constexpr int kEpiPerQuad = kEpiThreads / 128;  // epilogue warps per TMEM lane 
 // B = x in 2 MXFP8 planes, epilogue h = SiLU(gate) * up into the h panels.
 // Down: M tiles of 128 rows of d, K = f, B = h in 4 MXFP8 planes, epilogue
 // part = D. A stage holds one K step of both operands: [A of M tile 0 | A of
-// M tile 1 | B panel step]. MMA lane t issues the MMAs of M tile t of the
-// unit into its own accumulator.
+// M tile 1 | SFA of both | B panel step with its SFB]. MMA lane t issues the
+// MMAs of M tile t of the unit into its own accumulator.
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
   static constexpr int kPanelRows = kDown ? kTcPanelRowsD : kTcPanelRows;
   static constexpr int kPanelStep = kDown ? kTcPanelStepD : kTcPanelStep;
   static constexpr int kSfBlocks = kDown ? 2 : 1;  // 512-byte B scale blocks per panel step (32 rows x 4 words each)
-  static constexpr int kAPair = 2 * kAStage;
+  static constexpr int kAPair = 2 * kAOp + 1024;
   static constexpr int kStage = kAPair + kPanelStep;
   static constexpr int kS = kDown ? 3 : 4;         // stages
   static constexpr int kMma = 2;                   // MMA lanes = M tiles of a unit
@@ -144,8 +143,8 @@ struct TcUnit {
   int mt, nt;   // first M tile of the pair and tiles in it (1 or 2)
   int nks;      // K steps
   int panel;    // panel of the (slot, token block)
-  int y;        // tensor row (64 bytes each) of M tile mt's first weight block (tile mt + 1: + nks * kCmRows)
-  const uint8_t* w;  // weight blocks of M tile mt (K step 0; tile mt + 1: + nks * kTcBlockBytes)
+  int y;        // tensor row (64 bytes each) of the pair's first weight block (K step 0)
+  const uint8_t* w;  // the pair's weight blocks (K step 0)
 };
 
 template <bool kDown>
@@ -163,22 +162,22 @@ __device__ __forceinline__ TcUnit tc_unit(const FwdParams& p, const SlotTab& st,
   g.n = min(kMaxTok, st.sn[s] - kMaxTok * tb);
   g.nks = tc_ksteps(kDown ? g.f : p.d);
   g.panel = st.ppre[s] + tb;
-  const size_t stride = kDown ? p.tcwd_stride : p.tcw_stride;  // a multiple of kTcBlockBytes
-  g.y = (int)((size_t)g.e * (stride / 64)) + g.mt * g.nks * kCmRows;
-  g.w = (kDown ? p.tcwd : p.tcw) + (size_t)g.e * stride + (size_t)g.mt * g.nks * kTcBlockBytes;
+  const size_t stride = kDown ? p.tcwd_stride : p.tcw_stride;  // a multiple of kTcPairBytes
+  g.y = (int)((size_t)g.e * (stride / 64)) + (g.mt / 2) * g.nks * kCmRows;
+  g.w = (kDown ? p.tcwd : p.tcw) + (size_t)g.e * stride + (size_t)(g.mt / 2) * g.nks * kTcPairBytes;
   return g;
 }
 
 __device__ __forceinline__ int tok_of(const FwdParams& p, int q) { return q < p.P ? p.perm[q] / p.k : q - p.P; }
 __device__ __forceinline__ int npad_of(int n) { return max(8, (n + 7) & ~7); }
 
-// Byte offset, within an h panel step, of the E8M0 scale of B row `row` and
-// K block kb: two 512-byte blocks of words [lane][4], block r / 4 holding B
-// rows 32 r + lane in word r % 4 (r = row / 32), the order tcgen05.cp
-// 32x128b copies to tensor memory.
-__device__ __forceinline__ int hsf_off(int row, int kb) {
+// Byte offset, within an h panel step of N = 4 npad rows, of the E8M0 scale of
+// B row `row` and K block kb: behind the rows, two 512-byte blocks of words
+// [lane][4], block r / 4 holding B rows 32 r + lane in word r % 4
+// (r = row / 32), the order tcgen05.st writes them to tensor memory.
+__device__ __forceinline__ int hsf_off(int npad, int row, int kb) {
   const int r = row >> 5;
-  return kTcPanelRowsD * kTcStepK + 512 * (r >> 2) + 16 * (row & 31) + 4 * (r & 3) + kb;
+  return 4 * npad * kTcStepK + 512 * (r >> 2) + 16 * (row & 31) + 4 * (r & 3) + kb;
 }
 
 // The producer's walk over the steps (unit, K step) of the CTA.
@@ -286,7 +285,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   // the other 8 stay as set here
   for (int c = tid; c < kS * 2 * (kAOp / 16); c += kThr)
     *reinterpret_cast<uint2*>(stg + (size_t)(c / (2 * (kAOp / 16))) * M::kStage +
-                              (size_t)((c / (kAOp / 16)) & 1) * kAStage + 16 * (c % (kAOp / 16)) + 8) =
+                              (size_t)((c / (kAOp / 16)) & 1) * kAOp + 16 * (c % (kAOp / 16)) + 8) =
         make_uint2(0u, 0u);
   tc::fence_proxy_async();
   if (tid == 0) {
@@ -316,8 +315,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       ca.g = cp.g = tc_unit<kDown>(p, st, b0);
       // weight blocks are read once: start them towards L2 kPf steps before their tensor copy
       auto prefetch = [&]() {
-        for (int t = 0; t < cp.g.nt; ++t)
-          prefetch_l2(cp.g.w + ((size_t)t * cp.g.nks + cp.ks) * kTcBlockBytes, kTcBlockBytes);
+        prefetch_l2(cp.g.w + (size_t)cp.ks * kTcPairBytes, kTcPairBytes);
         cursor_next<kDown>(p, st, cp, n_units);
       };
       for (int q = 0; q < M::kPf && cp.i < n_units; ++q) prefetch();
@@ -325,13 +323,10 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         const int s = j % kS;
         if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
         uint8_t* sb = stg + (size_t)s * M::kStage;
-        // per M tile: 8,192 code bytes (counted as read from global memory) + 512 scale bytes
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(ca.g.nt * kTcBlockBytes));
-        for (int t = 0; t < ca.g.nt; ++t) {
-          tc::tma_load_2d(sb + t * kAStage, &wmap, 0, ca.g.y + (t * ca.g.nks + ca.ks) * kCmRows, &full[s]);
-          bulk_g2s(sb + t * kAStage + kAOp, ca.g.w + ((size_t)t * ca.g.nks + ca.ks) * kTcBlockBytes + kTcCodeBytes,
-                   512, &full[s]);
-        }
+        // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kTcPairBytes);
+        tc::tma_load_2d(sb, &wmap, 0, ca.g.y + ca.ks * kCmRows, &full[s]);
+        bulk_g2s(sb + 2 * kAOp, ca.g.w + (size_t)ca.ks * kTcPairBytes + 2 * kTcCodeBytes, 1024, &full[s]);
         if (M::kPf > 0 && cp.i < n_units) prefetch();
         cursor_next<kDown>(p, st, ca, n_units);
       }
@@ -350,9 +345,9 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         const int N = M::kPlanes * npad_of(cb.g.n);
         uint8_t* sb = stg + (size_t)s * M::kStage + M::kAPair;
         const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
+        // N rows and their scale words right behind them
         mbar_arrive_expect_tx(&full[s], (uint32_t)(N * kTcStepK + 512 * M::kSfBlocks));
-        bulk_g2s(sb, src, (uint32_t)(N * kTcStepK), &full[s]);
-        bulk_g2s(sb + M::kPanelRows * kTcStepK, src + M::kPanelRows * kTcStepK, 512 * M::kSfBlocks, &full[s]);
+        bulk_g2s(sb, src, (uint32_t)(N * kTcStepK + 512 * M::kSfBlocks), &full[s]);
         cursor_next<kDown>(p, st, cb, n_units);
       }
     }
@@ -373,7 +368,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
           bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status);  // operands landed, scales in TMEM
           tc::fence_after();
           if (mine) {
-            const uint8_t* ab = stg + (size_t)s * M::kStage + (size_t)t * kAStage;
+            const uint8_t* ab = stg + (size_t)s * M::kStage + (size_t)t * kAOp;
             const uint8_t* bb = stg + (size_t)s * M::kStage + M::kAPair;
             const uint32_t sf = tmem + kSfCol + kSfSet * s;
 #pragma unroll
@@ -402,14 +397,14 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         const int s = j % kS;
         bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status);
         const uint8_t* sb = stg + (size_t)s * M::kStage;
-        const uint8_t* sbf = sb + M::kAPair + M::kPanelRows * kTcStepK;
-        const uint4 wa0 = *reinterpret_cast<const uint4*>(sb + kAOp + 16 * lane);
+        const uint8_t* sbf = sb + M::kAPair + M::kPlanes * npad_of(g.n) * kTcStepK;  // SFB behind the N rows
+        const uint4 wa0 = *reinterpret_cast<const uint4*>(sb + 2 * kAOp + 16 * lane);
         const uint4 wb0 = *reinterpret_cast<const uint4*>(sbf + 16 * lane);
         tc::fence_after();
         const uint32_t sf = qbase + kSfSet * s;
         tc::st4(sf, wa0.x, wa0.y, wa0.z, wa0.w);
         if (g.nt > 1) {
-          const uint4 wa1 = *reinterpret_cast<const uint4*>(sb + kAStage + kAOp + 16 * lane);
+          const uint4 wa1 = *reinterpret_cast<const uint4*>(sb + 2 * kAOp + 512 + 16 * lane);
           tc::st4(sf + 8, wa1.x, wa1.y, wa1.z, wa1.w);
         }
         tc::st4(sf + 16, wb0.x, wb0.y, wb0.z, wb0.w);
@@ -497,19 +492,19 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
             }
             if (lane < 4) {
               const uint32_t sv = lane == 0 ? sc[0] : lane == 1 ? sc[1] : lane == 2 ? sc[2] : sc[3];
-              dst[hsf_off(lane * npad + m, 2 * (mt & 1) + b)] = (uint8_t)sv;
+              dst[hsf_off(npad, lane * npad + m, 2 * (mt & 1) + b)] = (uint8_t)sv;
             }
           }
           // 3. scale bytes of the rows past the 4 planes (127), and the half K step
           // past the last M tile when the tile count is odd (codes 0, scales 127)
-          for (int o = et; o < 2 * (kTcPanelRowsD - 4 * npad); o += kEpiThreads)
-            dst[hsf_off(4 * npad + (o >> 1), 2 * (mt & 1) + (o & 1))] = 127;
+          for (int o = et; o < 2 * (256 - 4 * npad); o += kEpiThreads)
+            dst[hsf_off(npad, 4 * npad + (o >> 1), 2 * (mt & 1) + (o & 1))] = 127;
           if ((mt & 1) == 0 && mt + 1 == tc_msteps(g.f)) {
             for (int o = et; o < 4 * npad * 4; o += kEpiThreads) {
               const int row = o >> 2, kc = 4 + (o & 3);
               *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
-            for (int o = et; o < 2 * kTcPanelRowsD; o += kEpiThreads) dst[hsf_off(o >> 1, 2 + (o & 1))] = 127;
+            for (int o = et; o < 2 * 256; o += kEpiThreads) dst[hsf_off(npad, o >> 1, 2 + (o & 1))] = 127;
           }
         }
       }
@@ -535,7 +530,7 @@ __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
   const int n = min(kMaxTok, p.slot_n[s] - kMaxTok * tb), q0 = p.slot_q0[s] + kMaxTok * tb, npad = npad_of(n);
   const int nks = tc_ksteps(p.d);
   uint8_t* dst = p.xpanel + ((size_t)pb * nks + ks) * kTcPanelStep;
-  for (int o = threadIdx.x; o < kTcPanelRows * 8; o += 256) {  // 16-byte chunks (row, kc)
+  for (int o = threadIdx.x; o < 2 * npad * 8; o += 256) {  // 16-byte chunks (row, kc) of the N = 2 npad rows
     const int row = o >> 3, kc = o & 7;
     const int plane = row >= npad, m = row - plane * npad, k0 = kTcStepK * ks + 16 * kc;
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -555,7 +550,7 @@ __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
         w |= (uint32_t)(blk < p.xq_spitch ? sc[blk] : 127) << (8 * kb);
       }
     }
-    *reinterpret_cast<uint32_t*>(dst + kTcPanelRows * kTcStepK + 16 * l + 4 * r) = w;
+    *reinterpret_cast<uint32_t*>(dst + 2 * npad * kTcStepK + 16 * l + 4 * r) = w;
   }
 }
 
@@ -565,7 +560,8 @@ __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
 // down matrix, K = f.
 __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                                  size_t ccs, size_t css, uint8_t* out, size_t out_stride, bool down) {
-  const int nms = down ? tc_dtiles(d) : tc_msteps(f), K = down ? f : d, nks = tc_ksteps(K);
+  // every tile of the pairs, the second tile of an odd last pair included (all code 0, scale 127)
+  const int nms = 2 * (down ? tc_dn_pairs(d) : tc_gu_pairs(f)), K = down ? f : d, nks = tc_ksteps(K);
   const long long total = (long long)n_exp * nms * nks * 128;
   for (long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x; gid < total;
        gid += (long long)gridDim.x * blockDim.x) {
@@ -587,7 +583,8 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
       cr = codes + (size_t)x * ccs + (size_t)row * (d / 2);
       sr = scales + (size_t)x * css + (size_t)row * (d / 32);
     }
-    uint8_t* dst = out + (size_t)x * out_stride + ((size_t)a * nks + ks) * kTcBlockBytes;
+    uint8_t* dst = out + (size_t)x * out_stride + ((size_t)(a >> 1) * nks + ks) * kTcPairBytes;
+    uint8_t* dcode = dst + (size_t)(a & 1) * kTcCodeBytes;
     for (int kc = 0; kc < 8; ++kc) {
       const int k0 = kTcStepK * ks + 16 * kc;
       uint2 v = make_uint2(0u, 0u);
@@ -597,7 +594,7 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
         v.x = (uint32_t)b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) | ((uint32_t)b[3] << 24);
         v.y = (uint32_t)b[4] | ((uint32_t)b[5] << 8) | ((uint32_t)b[6] << 16) | ((uint32_t)b[7] << 24);
       }
-      *reinterpret_cast<uint2*>(dst + ((m >> 3) * 8 + kc) * 64 + (m & 7) * 8) = v;
+      *reinterpret_cast<uint2*>(dcode + ((m >> 3) * 8 + kc) * 64 + (m & 7) * 8) = v;
     }
     uint32_t w = 0;
     for (int kb = 0; kb < 4; ++kb) {
@@ -605,7 +602,7 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
       const uint32_t sc = (live && 32 * blk32 < K) ? sr[blk32] : 127u;
       w |= sc << (8 * kb);
     }
-    *reinterpret_cast<uint32_t*>(dst + kTcCodeBytes + 16 * (m & 31) + 4 * (m >> 5)) = w;
+    *reinterpret_cast<uint32_t*>(dst + 2 * kTcCodeBytes + 512 * (a & 1) + 16 * (m & 31) + 4 * (m >> 5)) = w;
   }
 }
 
@@ -680,8 +677,8 @@ size_t tc_gemm_smem_bytes(int E, bool down) {
 
 // The weight copy as a 2-D tensor of "16 x U4, 16-byte aligned" elements:
 // rows of 128 codes (64 bytes: one core matrix of 8 rows x 16 codes), so that
-// a box of 128 rows is the 8,192 code bytes of one block, widened on the way
-// into shared memory.
+// a box of 256 rows is the 2 x 8,192 code bytes of a tile pair's block,
+// widened on the way into shared memory.
 bool encode_tc_weight_map(const void* base, size_t bytes, void* map) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -694,7 +691,7 @@ bool encode_tc_weight_map(const void* base, size_t bytes, void* map) {
   }
   if (bytes % 64 != 0 || bytes / 64 >= (1ull << 31)) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 64)}, strides[1] = {64};
-  const cuuint32_t box[2] = {128, 128}, es[2] = {1, 1};
+  const cuuint32_t box[2] = {128, 256}, es[2] = {1, 1};
   return encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
