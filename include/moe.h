@@ -70,16 +70,20 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *   device-side wait of every single-kernel decode forward targets a count
  *   nothing reaches and gives up after 2 ms, so the forward completes with
  *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
- * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path that
- *   otherwise serves T > 16 (for testing both paths on the same shapes).
+ * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path (for
+ *   testing both paths on the same shapes).
+ * Path choice per call: the fused single-kernel path serves T <= 16 unless
+ *   the context holds the tcgen05 weight copy and T * top_k > 16; every other
+ *   call takes the multi-kernel path. Within each class a token's output bits
+ *   do not depend on the other tokens of its call.
  * The multi-kernel path runs both expert GEMMs as block-scaled tcgen05 MMAs
  *   (MXFP4 weights x MXFP8 planes of x and of h) from a second copy of the
- *   experts in the MMA's layout, made at load time, whenever t_max > 16 and
- *   the shared-memory tables fit (n_experts up to about 400).
+ *   experts in the MMA's layout, made at load time, whenever t_max * top_k >
+ *   16 and the shared-memory tables fit (n_experts up to 512).
  * MOE_FLAG_TC_GATEUP asks for those MMAs for every t_max (an error if the
  *   tables do not fit); MOE_FLAG_NO_TC keeps the register-decode tensor-core
- *   GEMMs instead (no second copy). Results agree within the bf16 and fp32
- *   tolerances either way. */
+ *   GEMMs instead (no second copy; T <= 16 then always takes the fused
+ *   path). Results agree within the bf16 and fp32 tolerances either way. */
 enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u, MOE_FLAG_NO_TC = 8u };
 
 typedef struct moe_config {

@@ -81,6 +81,13 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The fused single-kernel path: T <= 16 with its shared-memory plan, and,
+// when the context has the tcgen05 weight copy, at most kFusedMaxPairs pairs.
+bool uses_decode(const moe_ctx* ctx, int T) {
+  return T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT &&
+         (!ctx->base.tc_gateup || T * ctx->cfg.top_k <= moe::kFusedMaxPairs);
+}
+
 }  // namespace
 
 extern "C" {
@@ -124,7 +131,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   // the block-scaled tcgen05 GEMMs serve the multi-kernel path unless asked not to
   const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
-                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && c.t_max > moe::kDecodeMaxT);
+                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
@@ -347,7 +354,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
   ctx->last_T = T;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT) {
+  if (uses_decode(ctx, T)) {
     moe::DecParams dp = ctx->dec;
     dp.f = p;
     const bool prof = ctx->n_prof >= 2;
@@ -421,9 +428,6 @@ int moe_get_status(moe_ctx* ctx, int clear) {
   return st;
 }
 
-namespace {
-bool uses_decode(const moe_ctx* ctx, int T) { return T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT; }
-}  // namespace
 
 int moe_profile_events(moe_ctx* ctx, void* const* events, int n_events) {
   if (!ctx) return MOE_ERR_INVALID_ARG;

@@ -156,6 +156,11 @@ struct FwdParams {
 
 // Fused single-kernel decode path (moe_decode.cu), used for T <= kDecodeMaxT.
 constexpr int kDecodeMaxT = 16;
+// Calls with T * k above this many (token, expert) pairs take the multi-kernel
+// path with the tcgen05 GEMMs when the context has their weight copy: from
+// there on the block-scaled GEMMs beat the fused kernel (measured: T=8, k=8
+// and T=16, k=4 run 1.4-1.6x faster; T=1, k=4 runs faster fused).
+constexpr int kFusedMaxPairs = 16;
 struct DecParams {
   FwdParams f;
   int* done;            // [2][E+1] finished gate/up units per slot (half = launch sequence & 1)

@@ -61,7 +61,7 @@ SMALL_SHAPES = [
 def test_small_shapes(m, shape, out_f32, path):
     T, d, F, E, k, S, z = shape
     wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
-    flags = {"fused": 0, "general": m.MOE_FLAG_GENERAL_PATH,
+    flags = {"fused": m.MOE_FLAG_NO_TC, "general": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC,
              "general-tc": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_TC_GATEUP}[path]
     _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32, flags=flags)
 
@@ -74,11 +74,18 @@ def test_wide_scale_exponent_range(m, flags):
 
 
 def test_path_selection(m):
-    wl = synth.WORKLOADS["decode"]
+    """Fused kernel up to 16 (token, expert) pairs, the multi-kernel tcgen05 path above; without the
+    tcgen05 copy (MOE_FLAG_NO_TC) the fused kernel serves every T <= 16."""
+    wl = synth.WORKLOADS["decode"]  # k = 4
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024))
     assert m.moe_launches_per_forward(lay.ctx, 1) == 1 and m.moe_forward_phases(lay.ctx, 1) == ["layer"]
+    assert m.moe_launches_per_forward(lay.ctx, 4) == 1
+    assert m.moe_launches_per_forward(lay.ctx, 5) == 9
+    assert m.moe_launches_per_forward(lay.ctx, 17) == 9
+    lay.close()
+    lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024, flags=m.MOE_FLAG_NO_TC))
     assert m.moe_launches_per_forward(lay.ctx, 16) == 1
-    assert m.moe_launches_per_forward(lay.ctx, 17) > 1
+    assert m.moe_launches_per_forward(lay.ctx, 17) == 7
     lay.close()
 
 
@@ -109,15 +116,25 @@ def test_every_token_count_up_to_16(m, flags):
     layer.close()
 
 
-def test_batch_invariance(m):
-    """A token's output bits do not depend on the batch it is in."""
+@pytest.mark.parametrize("cls", ["fused", "tcgen05"])
+def test_batch_invariance(m, cls):
+    """Within a path class, a token's output bits do not depend on the other tokens of its call:
+    fused (T * k <= 16): a batch of 4 vs single tokens; tcgen05 (T * k > 16): a batch of 16 vs
+    sub-batches of 5 and 11 tokens."""
     wl = synth.WORKLOADS["tiny"].with_(T=16, E=32, k=4)
     L = synth.gen_layer(wl, 5)
     layer = make_layer(m, wl, L, t_max=16, out_f32=True)
-    full = run_gpu(m, layer, L["x"], out_f32=True)
-    for t in (0, 7, 15):
-        one = run_gpu(m, layer, L["x"][t:t + 1].copy(), out_f32=True)
-        assert np.array_equal(one["y"][0], full["y"][t])
+    if cls == "fused":
+        full = run_gpu(m, layer, L["x"][:4].copy(), out_f32=True)
+        for t in (0, 3):
+            one = run_gpu(m, layer, L["x"][t:t + 1].copy(), out_f32=True)
+            assert np.array_equal(one["y"][0], full["y"][t])
+    else:
+        full = run_gpu(m, layer, L["x"], out_f32=True)
+        a = run_gpu(m, layer, L["x"][:5].copy(), out_f32=True)
+        b = run_gpu(m, layer, L["x"][5:].copy(), out_f32=True)
+        assert np.array_equal(a["y"], full["y"][:5])
+        assert np.array_equal(b["y"], full["y"][5:])
     layer.close()
 
 
@@ -269,8 +286,8 @@ def test_fused_and_general_paths_agree_on_full_size(m, name):
     """Both paths, same inputs: routing identical, outputs within fp32 tolerance of each other."""
     wl = synth.WORKLOADS[name]
     L = synth.gen_layer(wl, 1)
-    a = make_layer(m, wl, L, out_f32=True)
-    b = make_layer(m, wl, L, out_f32=True, flags=m.MOE_FLAG_GENERAL_PATH)
+    a = make_layer(m, wl, L, out_f32=True, flags=m.MOE_FLAG_NO_TC)  # fused kernel for every T <= 16
+    b = make_layer(m, wl, L, out_f32=True, flags=m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC)
     ga = run_gpu(m, a, L["x"], out_f32=True)
     gb = run_gpu(m, b, L["x"], out_f32=True)
     assert np.array_equal(ga["ids"], gb["ids"]) and np.array_equal(ga["perm"], gb["perm"])
