@@ -168,7 +168,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
   const size_t o_done = take((size_t)2 * (E + 1) * 4), o_rowcnt = take((size_t)2 * (d / 16) * 4),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
-               o_lw = take((size_t)std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
+               o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
   ctx->ws_bytes = off;
 
   if ((tc && (e = cudaMalloc(&ctx->tcw, ctx->tcw_bytes)) != cudaSuccess) ||

@@ -56,7 +56,8 @@ constexpr int kWarps = 16;
 constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
 constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
 constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
-constexpr int kMaxUS = 8;          // unit slots (partial-sum buffers) per phase, at most
+constexpr int kMaxUS = 8;
+constexpr int kLogitCopies = kLogitWordCopies;  // CTA b polls copy b % kLogitCopies          // unit slots (partial-sum buffers) per phase, at most
 
 struct Shared {
   int* ctl;     // [0, 8) gate/up arrivals, [8, 16) gate/up slot owners, [16, 24) down arrivals, [24, 32) down owners
@@ -79,7 +80,7 @@ struct Shared {
   int* hs_slot;  // (slot, half) list of the down phase
   int* hs_half;
   int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
-              // [4] (slot, half) pairs, [5] pairs of routed slots
+              // [4] (slot, half) pairs, [5] pairs of routed slots, [6] warps done with their gate/up items
   uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
   int* done;      // this launch's half of the global counters
   int* rowcnt;
@@ -268,12 +269,17 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
     if (warp < T) {
       dd v = lane < wpt ? s.red[warp * wpt + lane] : dd{0.f, 0.f};
       for (int o = 8; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
+      if (lane == 0 && f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
+      v.hi = __shfl_sync(0xffffffffu, v.hi, 0);  // lane 0's value in every copy
+      v.lo = __shfl_sync(0xffffffffu, v.lo, 0);
       if (lane == 0) {
-        if (f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
         f.logit_hi[(size_t)warp * f.E + e] = v.hi;  // debug export
         f.logit_lo[(size_t)warp * f.E + e] = v.lo;
-        // the word carries its own value: no other data is published with it
-        unsigned long long* w = p.lwords + ((size_t)warp * f.E + e) * 2;
+      }
+      // the word carries its own value: no other data is published with it;
+      // lane r writes copy r (the readers spread over the copies)
+      if (lane < kLogitCopies) {
+        unsigned long long* w = p.lwords + ((size_t)lane * p.tcap * f.E + (size_t)warp * f.E + e) * 2;
         st_relaxed_u64(w, pack_logit(v.hi, seq));
         st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
       }
@@ -334,7 +340,8 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
   const FwdParams& f = p.f;
   const int lane = threadIdx.x & 31;
   const int E = f.E, k = f.k;
-  const unsigned long long* wt = p.lwords + (size_t)t * E * 2;
+  const unsigned long long* wt =
+      p.lwords + ((size_t)(blockIdx.x % kLogitCopies) * p.tcap * E + (size_t)t * E) * 2;
   float vh[NPL], vl[NPL];
   unsigned valid = 0;
 #pragma unroll
@@ -1046,9 +1053,12 @@ __device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* 
   const Plan pl = make_plan(p, s, w);
   const uint64_t pol = evict_first_policy();
   uint8_t* ring = s.ring + (size_t)w * RG * kGroupBytes;
+  // The ring first carries the warp's gate/up groups only; its down groups
+  // follow once those are consumed, so that while gate/up runs (the critical
+  // path up to h) the HBM stream is gate/up weights alone.
   Cursor cu;
   cu.j = 0;
-  cu.nitems = pl.nguw + pl.ndnw;
+  cu.nitems = pl.nguw;
   cursor_seek(p, s, pl, w, cu);
   for (int i = 0; i < RG; ++i) issue_group(p, s, pl, w, cu, ring + i * kGroupBytes, pol);
   int slot = 0;
@@ -1059,6 +1069,31 @@ __device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* 
     if (un.n <= 8) gateup_item<1, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
     else gateup_item<2, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
   }
+  // Down groups into the ring (its slots are all consumed; the commits still
+  // pending are empty). A warp without gate/up items waits until every warp
+  // with some is done, so its down copies do not compete with them.
+  if (pl.ndnw > 0) {
+    const int with_items = min(kWarps, kChunks * pl.ngu);
+    if (pl.nguw == 0 && with_items > 0 && (threadIdx.x & 31) == 0 && ld_acquire_cta_shared(&s.misc[6]) < with_items) {
+      const uint64_t t0 = globaltimer();
+      while (ld_acquire_cta_shared(&s.misc[6]) < with_items) {
+        if (*abort) break;
+        if (timed_out(t0, p.wait_ns)) {
+          give_up(abort, f.status);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (pl.nguw > 0 && (threadIdx.x & 31) == 0) atomicAdd(&s.misc[6], 1);
+  cu.j = pl.nguw;
+  cu.nitems = pl.nguw + pl.ndnw;
+  cursor_seek(p, s, pl, w, cu);
+  for (int i = 0; i < RG; ++i) {
+    issue_group(p, s, pl, w, cu, ring + slot * kGroupBytes, pol);
+    if (++slot == RG) slot = 0;
+  }
   // D: down items, one (slot, half) pair at a time; every warp takes part in
   // every pair's staging barriers, with or without items of that pair
   const int ud = f.d / 16;
@@ -1066,13 +1101,14 @@ __device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* 
   if (pl.ndn > 0) {
     const int hs_first = pl.d0 / ud, hs_last = (pl.d0 + pl.ndn - 1) / ud;
     for (int hs = hs_first; hs <= hs_last; ++hs) {
-      named_bar(2, kThreads);  // the shared x / previous h is no longer read
       const int hslot = s.hs_slot[hs];
       const int fsl = (s.slot_e[hslot] == f.E) ? f.S : f.F;
-      if ((threadIdx.x & 31) == 0)
+      // one poller per CTA; the barrier after it also ends every read of the
+      // shared x / previous h
+      if (threadIdx.x == 0)
         wait_counter(&s.done[hslot], fsl / 16 + p.test_extra, abort, p.test_extra ? p.test_wait_ns : p.wait_ns,
                      f.status);
-      __syncwarp();
+      named_bar(2, kThreads);
       if (!*abort) stage_h(p, s, hs);
       named_bar(2, kThreads);
       for (; j < pl.nguw + pl.ndnw; ++j) {
@@ -1101,6 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
       s.ctl[3 * kMaxUS + b] = b;
     }
     *abort = 0;
+    s.misc[6] = 0;
   }
   for (int e = tid; e < p.f.E; e += kThreads) s.cnt[e] = 0;
   stage_router(p, s);
@@ -1160,7 +1197,8 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   p.off_red = (int)off;
   off = up(off + (size_t)kWarps * kDecodeMaxT * sizeof(dd), 16);
   const size_t route_bytes = (size_t)(4 * Pm + 5 * (f.E + 1) + 2 * (f.E + 1 + 64) + 8) * 4;
-  // the deepest weight ring per warp that fits: 8, 6 or 4 slots
+  // the deepest weight ring per warp that fits: 8, 6 or 4 slots (a 12-slot
+  // ring measured no faster: the stream is not short of copies in flight)
   const int tries[7][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 6}, {4, 6}, {kMaxUS, 4}, {4, 4}, {2, 4}};
   for (const auto& tr : tries) {
     const int n_us = tr[0], rg_want = tr[1];
@@ -1196,6 +1234,7 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
       e = cudaFuncSetAttribute(decode_layer_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+
     if (e != cudaSuccess) return e;
     configured = max_smem;
   }

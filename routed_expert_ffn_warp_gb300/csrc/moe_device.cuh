@@ -255,6 +255,16 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned l
 // Programmatic dependent launch: wait for the preceding grid / let the next one launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// First statement of every kernel of the forward chain: nothing before it
+// touches global memory, so the kernel sees all writes of the grids before it
+// (each of which waited the same way); the next grid may then be scheduled and
+// sits in its own wait, which hides its launch behind this grid's work. At most
+// two grids of the chain are resident at a time, and only the running one
+// holds tensor memory.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
+}
 
 }  // namespace dev
 }  // namespace moe

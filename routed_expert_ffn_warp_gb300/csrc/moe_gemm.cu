@@ -274,6 +274,7 @@ __device__ void gemm_gu_unit(const FwdParams& p, const GUnit& g, int w, uint8_t*
 }
 
 __global__ void __launch_bounds__(kGThreads, 1) gemm_gateup_kernel(FwdParams p) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* xbar = reinterpret_cast<uint64_t*>(sm);
   __half* xbuf = reinterpret_cast<__half*>(sm + 128);
@@ -461,6 +462,7 @@ __device__ void gemm_dn_unit(const FwdParams& p, const GUnit& g, int w, uint8_t*
 }
 
 __global__ void __launch_bounds__(kGThreads, 1) gemm_down_kernel(FwdParams p) {
+  pdl_enter();
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* hbar = reinterpret_cast<uint64_t*>(sm);
   __half* hbuf = reinterpret_cast<__half*>(sm + 128);

@@ -156,6 +156,8 @@ struct FwdParams {
 
 // Fused single-kernel decode path (moe_decode.cu), used for T <= kDecodeMaxT.
 constexpr int kDecodeMaxT = 16;
+// Copies of every published router logit word of the fused path (readers spread over them).
+constexpr int kLogitWordCopies = 8;
 // Calls with T * k above this many (token, expert) pairs take the multi-kernel
 // path with the tcgen05 GEMMs when the context has their weight copy: from
 // there on the block-scaled GEMMs beat the fused kernel (measured: T=8, k=8
@@ -166,7 +168,7 @@ struct DecParams {
   int* done;            // [2][E+1] finished gate/up units per slot (half = launch sequence & 1)
   int* rowcnt;          // [2][d/16] finished down units per row tile
   unsigned* bar_flags;  // [grid] per-CTA launch sequence numbers (each only grows)
-  unsigned long long* lwords;  // [tcap][E][2] published logits: (fp32 bits << 32) | sequence
+  unsigned long long* lwords;  // [kLogitWordCopies][tcap][E][2] published logits: (fp32 bits << 32) | sequence
   int tcap;             // tokens the x16 shared area holds (min(t_max, kDecodeMaxT))
   int ring_groups;      // 1,088-byte slots of each warp's weight ring
   int n_us;             // partial-sum unit slots per phase
@@ -219,5 +221,24 @@ size_t tc_gemm_smem_bytes(int E, bool down);
 // GEMM loads a weight copy of `bytes` bytes at `base` through; false if the
 // driver refuses it.
 bool encode_tc_weight_map(const void* base, size_t bytes, void* map);
+
+// Launches a kernel of the forward chain with programmatic stream
+// serialization: it may be scheduled once the grid before it has passed its
+// own dependency wait. Every such kernel starts with dev::pdl_enter().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 }  // namespace moe

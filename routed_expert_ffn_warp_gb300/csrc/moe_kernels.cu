@@ -40,6 +40,7 @@ using namespace dev;
 // ---------------------------------------------------------------- prep_x
 
 __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
+  pdl_enter();
   const int t = blockIdx.x;
   const uint16_t* xt = p.x + (size_t)t * p.d;
   __shared__ float wmax[8];
@@ -87,6 +88,7 @@ __device__ __forceinline__ float router_gamma(int d) {
 // memory hit 32 banks. The next chunk of x and W_r is loaded into registers
 // while the current one is multiplied out of shared memory.
 __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
+  pdl_enter();
   __shared__ __align__(16) float xs[kRfK][kRfTok + 4];  // [k][token]
   __shared__ __align__(16) float ws[kRfK][kRfExp + 4];  // [k][expert]
   __shared__ float nsq[2][kRfThreads / 32][32];         // per-warp sums of squares: x rows, W_r rows
@@ -234,6 +236,7 @@ __device__ __forceinline__ void warp_logits_dd(const FwdParams& p, int t, const 
 // are the double-float values for the candidates and the fp32 values (lo = 0)
 // for the rest.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(FwdParams p) {
+  pdl_enter();
   __shared__ float lf[kTopkMaxE], lb[kTopkMaxE], ub[kTopkMaxE];
   __shared__ short cl[kTopkMaxE];
   __shared__ dd part[kTopkThreads / 32][kTopkMaxE];
@@ -435,6 +438,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int* total
 // order) and the shared expert last, from prefix sums of the per-slot unit
 // counts.
 __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
+  pdl_enter();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
   const int E = p.E, T = p.T, P = p.P;
   __shared__ int wc[kBucketChunks][512];  // per (chunk, expert): count, then first position
@@ -533,6 +537,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
 // ---------------------------------------------------------------- combine
 
 __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
+  pdl_enter();
   const int t = blockIdx.y;
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= p.d) return;
@@ -615,9 +620,9 @@ __global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n
 
 void launch_router(FwdParams p, cudaStream_t stream) {
   p.rsplit = router_splits(p.T, p.E, p.d);
-  router_fp32_kernel<<<dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp, p.rsplit), kRfThreads, 0,
-                       stream>>>(p);
-  topk_kernel<<<p.T, kTopkThreads, 0, stream>>>(p);
+  launch_chained(router_fp32_kernel, dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp, p.rsplit),
+                 dim3(kRfThreads), 0, stream, p);
+  launch_chained(topk_kernel, dim3(p.T), dim3(kTopkThreads), 0, stream, p);
 }
 
 const char* const kForwardPhaseNames = "route,gateup,down,combine";
@@ -625,9 +630,9 @@ const char* const kForwardPhaseNames = "route,gateup,down,combine";
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events) {
   if (p.T == 0) return cudaSuccess;
   if (events) cudaEventRecord(events[0], stream);
-  if (!p.tc_gateup) prep_x_kernel<<<p.T, 256, 0, stream>>>(p);  // f16 x of the register-decode GEMMs
+  if (!p.tc_gateup) launch_chained(prep_x_kernel, dim3(p.T), dim3(256), 0, stream, p);  // f16 x of the register-decode GEMMs
   launch_router(p, stream);
-  bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
+  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), 0, stream, p);
   if (events) cudaEventRecord(events[1], stream);
   cudaError_t e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
   if (e != cudaSuccess) return e;
@@ -635,7 +640,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   e = p.tc_gateup ? launch_gemm_down_tc(p, stream, num_sms) : launch_gemm_down(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   if (events) cudaEventRecord(events[3], stream);
-  combine_kernel<<<dim3((p.d + 255) / 256, p.T), 256, 0, stream>>>(p);
+  launch_chained(combine_kernel, dim3((p.d + 255) / 256, p.T), dim3(256), 0, stream, p);
   if (events) cudaEventRecord(events[4], stream);
   return cudaGetLastError();
 }
@@ -643,7 +648,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
   launch_router(p, stream);
-  bucket_kernel<<<1, kBucketThreads, 0, stream>>>(p);
+  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), 0, stream, p);
   return cudaGetLastError();
 }
 

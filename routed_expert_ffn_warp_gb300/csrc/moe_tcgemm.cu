@@ -247,6 +247,7 @@ __device__ __forceinline__ void split_planes4_fixed(float v, uint32_t (&code)[4]
 
 template <bool kDown>
 __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap wmap) {
+  pdl_enter();
   using M = Mode<kDown>;
   constexpr int kS = M::kS, kMma = M::kMma, kBufs = M::kBufs;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -522,6 +523,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
 // plane n / npad, token m = n % npad of the block (rows past the block's
 // tokens are zero, their scales 127).
 __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
+  pdl_enter();
   const int pb = blockIdx.x, ks = blockIdx.y;
   const int ns = *p.n_slots;
   if (pb >= p.panel_prefix[ns]) return;
@@ -608,6 +610,7 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
 
 // x -> two MXFP8 planes per 32-element block: a warp per (token, block), a lane per element.
 __global__ void __launch_bounds__(256) prep_xq_kernel(FwdParams p) {
+  pdl_enter();
   const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nb = p.xq_spitch;  // blocks per row, scale padding included
   if (item >= p.T * nb) return;
@@ -651,12 +654,12 @@ cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int n
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  prep_xq_kernel<<<(p.T * p.xq_spitch + 7) / 8, 256, 0, stream>>>(p);
+  launch_chained(prep_xq_kernel, dim3((p.T * p.xq_spitch + 7) / 8), dim3(256), 0, stream, p);
   // panels: at most ceil(Q / 48) + slots blocks (the kernels skip the ones past the count)
   const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
-  pack_panels_kernel<<<dim3(max_panels, tc_ksteps(p.d)), 256, 0, stream>>>(p);
-  gemm_tc_kernel<false><<<num_sms, kThr, smem, stream>>>(p, *static_cast<const CUtensorMap*>(p.tmap_gu));
-  return cudaGetLastError();
+  launch_chained(pack_panels_kernel, dim3(max_panels, tc_ksteps(p.d)), dim3(256), 0, stream, p);
+  return launch_chained(gemm_tc_kernel<false>, dim3(num_sms), dim3(kThr), smem, stream, p,
+                        *static_cast<const CUtensorMap*>(p.tmap_gu));
 }
 
 cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
@@ -667,8 +670,8 @@ cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  gemm_tc_kernel<true><<<num_sms, kThr, smem, stream>>>(p, *static_cast<const CUtensorMap*>(p.tmap_dn));
-  return cudaGetLastError();
+  return launch_chained(gemm_tc_kernel<true>, dim3(num_sms), dim3(kThr), smem, stream, p,
+                        *static_cast<const CUtensorMap*>(p.tmap_dn));
 }
 
 size_t tc_gemm_smem_bytes(int E, bool down) {
