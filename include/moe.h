@@ -142,10 +142,11 @@ int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, i
 
 /* Debug export of the last forward's router logits as an unevaluated sum of
  * two fp32 numbers, logit = hi + lo: hi, lo fp32 [T][E]. The single-kernel
- * path (T <= 16) computes every logit as a double-float sum (hi = fl(logit)).
- * The multi-kernel path computes every logit in fp32 with an error bound and
- * the double-float sum only for the experts that bound cannot rule out of the
- * top k: those hold hi + lo as above, the others their fp32 value and lo = 0. */
+ * path (T <= 16) and the multi-kernel path with T <= 32 compute every logit as
+ * a double-float sum (hi = fl(logit)). The multi-kernel path with T > 32
+ * computes every logit in fp32 with an error bound and the double-float sum
+ * only for the experts that bound cannot rule out of the top k: those hold
+ * hi + lo as above, the others their fp32 value and lo = 0. */
 int moe_get_logits(moe_ctx* ctx, float* hi, float* lo, void* stream);
 
 /* Device status word of the context (0 = fine, else a MOE_ERR_* code set by a

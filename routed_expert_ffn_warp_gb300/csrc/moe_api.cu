@@ -459,7 +459,8 @@ int moe_launches_per_forward(const moe_ctx* ctx, int T) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (T <= 0) return 0;
   if (uses_decode(ctx, T)) return 1;
-  return ctx->base.tc_gateup ? moe::kLaunchesPerForwardTc : moe::kLaunchesPerForward;
+  const int n = ctx->base.tc_gateup ? moe::kLaunchesPerForwardTc : moe::kLaunchesPerForward;
+  return T <= moe::kRouteDDMaxT ? n - 1 : n;  // one router launch instead of router + top-k
 }
 
 size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }

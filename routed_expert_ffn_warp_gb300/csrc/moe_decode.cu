@@ -4,7 +4,7 @@
 //   A  x is staged in shared memory; CTA b computes the double-float router
 //      logits of experts b, b+G, ... from it and publishes each as two 64-bit
 //      words (value bits | launch sequence number); x is then scaled to f16 in
-//      place.
+//      place (for T <= 8 by spare warps during phase B's poll).
 //   B  token warps poll the published words of all experts (a dataflow
 //      barrier: no grid-wide sync, no atomics), then every CTA redundantly runs
 //      top-k + softmax gates, the counting sort of the T*k pairs and the slot
@@ -288,12 +288,12 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
   }
 }
 
-// Staged x (bf16, in place) -> f16 * 2^sigma_t, one warp per token; K padding zeroed.
-__device__ void scale_x(const DecParams& p, const Shared& s) {
+// Staged x row t (bf16, in place) -> f16 * 2^sigma_t by one warp; K padding zeroed.
+__device__ void scale_x_token(const DecParams& p, const Shared& s, int t) {
   const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int d8 = f.d / 8;
-  for (int t = warp; t < f.T; t += kWarps) {
+  {
     uint4* xr = reinterpret_cast<uint4*>(s.x16 + (size_t)t * p.xstride);
     float m = 0.f;
     for (int o = lane; o < d8; o += 32) {
@@ -322,6 +322,15 @@ __device__ void scale_x(const DecParams& p, const Shared& s) {
     if (lane == 0) s.xinv[t] = pow2f(-sg);
   }
 }
+
+// All tokens, one warp per token.
+__device__ void scale_x(const DecParams& p, const Shared& s) {
+  for (int t = threadIdx.x >> 5; t < p.f.T; t += kWarps) scale_x_token(p, s, t);
+}
+
+// With T <= kWarps / 2 the x scaling runs on warps kWarps-1, kWarps-2, ...
+// while warps 0 .. T-1 poll the logit words and take the top k.
+__device__ __forceinline__ bool scale_x_beside_topk(const DecParams& p) { return p.f.T <= kWarps / 2; }
 
 // ---------------------------------------------------------------- phase B: routing (redundant per CTA)
 
@@ -604,6 +613,8 @@ __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volat
     if (p.f.E <= 128) topk_token<4>(p, s, warp, seq, abort);
     else if (p.f.E <= 256) topk_token<8>(p, s, warp, seq, abort);
     else topk_token<16>(p, s, warp, seq, abort);
+  } else if (scale_x_beside_topk(p) && warp >= kWarps - p.f.T) {
+    scale_x_token(p, s, kWarps - 1 - warp);
   }
   __syncthreads();
   if (warp == 0) {
@@ -1163,9 +1174,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
   __syncthreads();
   s.done = p.done + (size_t)(seq & 1) * (p.f.E + 1);
   s.rowcnt = p.rowcnt + (size_t)(seq & 1) * (p.f.d / 16);
-  router(p, s, seq);
-  scale_x(p, s);
-  __syncthreads();
+  router(p, s, seq);  // its reads of the bf16 x end before its last barrier (it has none without experts)
+  if (!scale_x_beside_topk(p)) {
+    scale_x(p, s);
+    __syncthreads();
+  }
   routing(p, s, seq, abort);
   pdl_launch_dependents();
   stream_layer<RG>(p, s, abort);

@@ -98,6 +98,10 @@ __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
 // ---------------------------------------------------------------- forward parameters
 
 constexpr int kRouterSplits = 4;  // most ranges of d the router's fp32 pass splits into
+// Multi-kernel path with T <= kRouteDDMaxT: every logit as a double-float sum
+// spread over all SMs (router_dd_kernel), the top k inside the bucketing
+// kernel (one warp per token); larger T takes the two-pass fp32 router.
+constexpr int kRouteDDMaxT = 32;
 
 struct FwdParams {
   // sizes
@@ -200,7 +204,7 @@ cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_
 constexpr int kForwardPhases = 4;
 extern const char* const kForwardPhaseNames;  // "route,gateup,down,combine"
 constexpr int kLaunchesPerForward = 7;
-constexpr int kLaunchesPerForwardTc = 9;  // + x planes, x panels (MOE_FLAG_TC_GATEUP)
+constexpr int kLaunchesPerForwardTc = 8;  // no f16 x; + x planes, x panels (tcgen05 GEMMs)
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);
 // Routing only (router logits, top-k gates, counting sort) of the general path.
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);

@@ -5,6 +5,8 @@
 //   router   l[t,e] = W_r[e] . x_t + b[e] in fp32, with an error bound
 //   topk     candidates from the bounds, their logits as double-float (hi + lo)
 //            sums, warp top-k with lower-index tie break, softmax gates
+//            (T <= kRouteDDMaxT: every logit as a double-float sum over all SMs
+//            instead, and the top-k at the start of the bucketing kernel)
 //   bucket   counting sort of the T*k pairs by expert, and the work list
 //   gateup   grouped MXFP4 GEMM on tensor cores: h = SiLU(gate) * up (moe_gemm.cu)
 //   down     grouped MXFP4 GEMM: part = W_down h (moe_gemm.cu)
@@ -390,6 +392,125 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(FwdParams p) {
   }
 }
 
+// ---------------------------------------------------------------- router for few tokens
+//
+// For T <= kRouteDDMaxT the two-pass router above runs on too few blocks to
+// use the GPU (its tiles are 32 tokens x 32 experts), and its candidate pass
+// is serial per token. Here every logit is a double-float sum (TwoProduct via
+// FMA + TwoSum, as in the single-kernel decode path), spread over E x
+// ceil(T / kRdTok) blocks: block (e, token group) has 8 warps, warp w sums the
+// elements of its eighth of d for up to 8 tokens (lanes stride over groups of
+// 8 elements), then a fixed warp tree per token and the 8 warps in order,
+// then the bias. The top k are then taken by the bucketing kernel.
+constexpr int kRdTok = 8, kRdThreads = 256;
+
+__global__ void __launch_bounds__(kRdThreads) router_dd_kernel(FwdParams p) {
+  pdl_enter();
+  __shared__ dd part[kRdThreads / 32][kRdTok];
+  const int e = blockIdx.x, t0 = blockIdx.y * kRdTok;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nt = min(kRdTok, p.T - t0);
+  const int g8 = p.d / 8, gb = g8 * warp / 8, ge = g8 * (warp + 1) / 8;
+  const float4* w4 = reinterpret_cast<const float4*>(p.w_router + (size_t)e * p.d);
+  const uint4* x4 = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.d);
+  dd acc[kRdTok];
+#pragma unroll
+  for (int j = 0; j < kRdTok; ++j) acc[j] = dd{0.f, 0.f};
+  for (int i8 = gb + lane; i8 < ge; i8 += 32) {
+    const float4 w0 = __ldg(w4 + 2 * i8), w1 = __ldg(w4 + 2 * i8 + 1);
+    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int j = 0; j < kRdTok; ++j) {
+      if (j >= nt) break;
+      const uint4 xv = __ldg(x4 + (size_t)j * g8 + i8);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dd_mac(acc[j], __uint_as_float(xw[q] << 16), wv[2 * q]);
+        dd_mac(acc[j], __uint_as_float(xw[q] & 0xFFFF0000u), wv[2 * q + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRdTok; ++j) {
+    if (j >= nt) break;
+    dd v = acc[j];
+    for (int o = 16; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
+    if (lane == 0) part[warp][j] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    const int j = threadIdx.x;
+    dd v = part[0][j];
+    for (int w = 1; w < kRdThreads / 32; ++w) v = dd_add(v, part[w][j]);
+    if (p.bias) v = dd_add(v, dd{p.bias[e], 0.f});
+    p.logit_hi[(size_t)(t0 + j) * p.E + e] = v.hi;
+    p.logit_lo[(size_t)(t0 + j) * p.E + e] = v.lo;
+  }
+}
+
+// Top k of token t by one warp from its double-float logits (normalised
+// pairs): k rounds of a warp arg-max by (hi, lo, lower index), then the
+// softmax of the k selected. NPL = experts per lane.
+template <int NPL>
+__device__ void topk_warp_dd(const FwdParams& p, int t) {
+  const int lane = threadIdx.x & 31, E = p.E, k = p.k;
+  float vh[NPL], vl[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    vh[i] = e < E ? p.logit_hi[(size_t)t * E + e] : -INFINITY;
+    vl[i] = e < E ? p.logit_lo[(size_t)t * E + e] : 0.f;
+  }
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i)
+    if (lane + 32 * i >= E) taken |= 1u << i;
+  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  int sel_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bh = -INFINITY, bl = 0.f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && dd_greater(vh[i], vl[i], e, bh, bl, bi)) {
+        bh = vh[i];
+        bl = vl[i];
+        bi = e;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
+        bh = oh;
+        bl = ol;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) {
+      top_h = bh;
+      top_l = bl;
+    }
+    if (lane == j) {
+      sel_h = bh;
+      sel_l = bl;
+      sel_id = bi;
+    }
+  }
+  float ex = 0.f;
+  if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
+  float sum = ex;
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    p.ids[(size_t)t * k + lane] = sel_id;
+    p.gates[(size_t)t * k + lane] = ex / sum;
+  }
+}
+
 // K ranges of the router's fp32 pass: enough blocks for about two per SM.
 __host__ inline int router_splits(int T, int E, int d) {
   const int tiles = ((T + kRfTok - 1) / kRfTok) * ((E + kRfExp - 1) / kRfExp);
@@ -443,6 +564,14 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   const int E = p.E, T = p.T, P = p.P;
   __shared__ int wc[kBucketChunks][512];  // per (chunk, expert): count, then first position
   __shared__ int wsum[32];
+  if (T <= kRouteDDMaxT) {  // few tokens: the top k from router_dd_kernel's logits, one warp per token
+    if (warp < T) {
+      if (E <= 128) topk_warp_dd<4>(p, warp);
+      else if (E <= 256) topk_warp_dd<8>(p, warp);
+      else topk_warp_dd<16>(p, warp);
+    }
+    __syncthreads();  // this block's ids writes are visible to the whole block
+  }
   const int chunk = (P + kBucketChunks - 1) / kBucketChunks;
   for (int i = tid; i < kBucketChunks * E; i += kBucketThreads) wc[i / E][i % E] = 0;
   __syncthreads();
@@ -619,6 +748,10 @@ __global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n
 }  // namespace
 
 void launch_router(FwdParams p, cudaStream_t stream) {
+  if (p.T <= kRouteDDMaxT) {  // the top k follow in bucket_kernel
+    launch_chained(router_dd_kernel, dim3(p.E, (p.T + kRdTok - 1) / kRdTok), dim3(kRdThreads), 0, stream, p);
+    return;
+  }
   p.rsplit = router_splits(p.T, p.E, p.d);
   launch_chained(router_fp32_kernel, dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp, p.rsplit),
                  dim3(kRfThreads), 0, stream, p);

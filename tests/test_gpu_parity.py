@@ -80,12 +80,15 @@ def test_path_selection(m):
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024))
     assert m.moe_launches_per_forward(lay.ctx, 1) == 1 and m.moe_forward_phases(lay.ctx, 1) == ["layer"]
     assert m.moe_launches_per_forward(lay.ctx, 4) == 1
-    assert m.moe_launches_per_forward(lay.ctx, 5) == 9
-    assert m.moe_launches_per_forward(lay.ctx, 17) == 9
+    # router (one launch up to 32 tokens, fp32 pass + top-k above), bucket, x planes, x panels, 2 GEMMs, combine
+    assert m.moe_launches_per_forward(lay.ctx, 5) == 7
+    assert m.moe_launches_per_forward(lay.ctx, 32) == 7
+    assert m.moe_launches_per_forward(lay.ctx, 33) == 8
     lay.close()
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024, flags=m.MOE_FLAG_NO_TC))
     assert m.moe_launches_per_forward(lay.ctx, 16) == 1
-    assert m.moe_launches_per_forward(lay.ctx, 17) == 7
+    assert m.moe_launches_per_forward(lay.ctx, 17) == 6  # f16 x instead of the planes and panels
+    assert m.moe_launches_per_forward(lay.ctx, 33) == 7
     lay.close()
 
 
@@ -169,13 +172,14 @@ def test_exact_ties_lower_index(m, flags):
         assert list(g["ids"][t]) == expect
 
 
-@pytest.mark.parametrize("flags", [0, 2])
-def test_near_ties_need_double_float(m, flags):
+@pytest.mark.parametrize("T,flags", [(16, 0), (16, 2), (40, 0)])
+def test_near_ties_need_double_float(m, T, flags):
     """Router rows 3 and 7 differ by one ulp in one element and carry a large bias:
     both are every token's top 2, their order is set by a logit difference far
-    below fp32 resolution (the multi-kernel path's fp32 bound cannot order them,
-    its double-float recompute must)."""
-    wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=2)
+    below fp32 resolution. The fused path and the multi-kernel path up to 32
+    tokens sum every logit in double-float; above 32 tokens the multi-kernel
+    path's fp32 bound cannot order them and its double-float recompute must."""
+    wl = synth.WORKLOADS["tiny"].with_(T=T, E=16, k=2)
     L = synth.gen_layer(wl, 6)
     w = L["w_router"].copy()
     w[7] = w[3]
