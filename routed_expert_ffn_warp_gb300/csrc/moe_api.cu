@@ -166,7 +166,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
   // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
-  const size_t o_done = take((size_t)2 * (E + 1) * 4), o_rowcnt = take((size_t)2 * (d / 16) * 4),
+  const size_t Qd = (size_t)std::min(Tm, moe::kDecodeMaxT) * (k + (S > 0 ? 1 : 0));  // pair rows of the fused path
+  const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
                o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
   ctx->ws_bytes = off;
@@ -246,7 +247,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   ctx->load_err = reinterpret_cast<int*>(w + o_lerr);
   moe::DecParams& dp = ctx->dec;
   dp.f = p;
-  dp.done = reinterpret_cast<int*>(w + o_done);
+  dp.hwords = reinterpret_cast<unsigned long long*>(w + o_hw);
+  dp.hswords = reinterpret_cast<unsigned long long*>(w + o_hsw);
   dp.rowcnt = reinterpret_cast<int*>(w + o_rowcnt);
   dp.bar_flags = reinterpret_cast<unsigned*>(w + o_bar);
   dp.lwords = reinterpret_cast<unsigned long long*>(w + o_lw);

@@ -16,13 +16,14 @@
 //      through a private shared-memory ring with cp.async (16-byte copies, no
 //      L1), several KB ahead of its math, so no warp waits on another for
 //      data. The last of a unit's 3 chunk warps to finish adds the 3 partial
-//      sums in chunk order, applies SiLU(gate)*up and writes h (f16 hi + lo
-//      with a power-of-two scale per 16 elements); every finished unit bumps
-//      its slot's counter.
+//      sums in chunk order, applies SiLU(gate)*up and publishes h (f16 hi +
+//      lo with a power-of-two scale per 16 elements) as 64-bit words that
+//      carry the launch sequence number, like the logits.
 //   D  down units (slot, token half of <= 8 tokens, 16 output rows) in that
-//      order, chunked and dealt the same way; the warps prefetch their down
-//      tiles while gate/up still runs. For each (slot, half) of the CTA the
-//      CTA waits (bounded) for the slot's h and stages it in shared memory;
+//      order, chunked and dealt the same way; each warp's down tiles follow
+//      its gate/up tiles in its ring. For each (slot, half) of the CTA the
+//      CTA stages the slot's h in shared memory, polling (bounded) the words
+//      until they carry this launch's number;
 //      the last chunk warp of a unit writes its partial rows, and the CTA
 //      finishing a row tile's last (slot, half) combines it:
 //      y = sum_j g_j part_j (slot order j) + shared, one rounding.
@@ -82,7 +83,6 @@ struct Shared {
   int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
               // [4] (slot, half) pairs, [5] pairs of routed slots, [6] warps done with their gate/up items
   uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
-  int* done;      // this launch's half of the global counters
   int* rowcnt;
 };
 
@@ -125,20 +125,6 @@ __device__ void set_status(int* status, int code) { atomicCAS(status, 0, code); 
 __device__ void give_up(volatile int* abort, int* status) {
   *abort = 1;
   set_status(status, MOE_ERR_TIMEOUT);
-}
-
-__device__ bool wait_counter(const int* ctr, int target, volatile int* abort, long long limit, int* status) {
-  if (*abort) return false;
-  if (ld_acquire(ctr) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  while (ld_acquire(ctr) < target) {
-    if (*abort) return false;
-    if (timed_out(t0, limit)) {
-      give_up(abort, status);
-      return false;
-    }
-  }
-  return true;
 }
 
 // ---------------------------------------------------------------- work units
@@ -812,6 +798,7 @@ __device__ __forceinline__ void free_slot(int* arrivals, int* owner, int next_ow
 // lanes 16-31 of the next one; the f16 scale of h is shared by a token's 16 rows.
 __device__ void gateup_reduce(const DecParams& p, const Shared& s, const Unit& un, const float* pb) {
   const FwdParams& f = p.f;
+  const unsigned seq = (unsigned)s.misc[3];
   const int lane = threadIdx.x & 31, r = lane & 15;
   const int tc = p.tcap, cs = 32 * tc;  // chunk stride
   for (int m0 = 0; m0 < un.n; m0 += 2) {
@@ -833,14 +820,16 @@ __device__ void gateup_reduce(const DecParams& p, const Shared& s, const Unit& u
     if (m < un.n) {
       const int sh = f16_headroom_exponent(mx);
       const int q = un.q0 + m;
-      __half* hi = reinterpret_cast<__half*>(f.hbuf) + (size_t)q * 2 * f.fmax64;
-      __half* lo = hi + f.fmax64;
       const int i = 32 * (un.idx >> 1) + 8 * (r >> 2) + 4 * (un.idx & 1) + (r & 3);
       const float v = h * pow2f(sh);
       const __half vh = __float2half_rn(v);
-      hi[i] = vh;
-      lo[i] = __float2half_rn(v - __half2float(vh));
-      if (r == 0) f.hscale[(size_t)q * f.hgroups + un.idx] = pow2f(-sh);
+      const __half vl = __float2half_rn(v - __half2float(vh));
+      // each value travels with this launch's number: the readers poll the data itself
+      const uint32_t hl = (uint32_t)__half_as_ushort(vh) | ((uint32_t)__half_as_ushort(vl) << 16);
+      st_relaxed_u64(p.hwords + (size_t)q * f.fmax64 + i, ((unsigned long long)hl << 32) | seq);
+      if (r == 0)
+        st_relaxed_u64(p.hswords + (size_t)q * f.hgroups + un.idx,
+                       ((unsigned long long)__float_as_uint(pow2f(-sh)) << 32) | seq);
     }
   }
 }
@@ -898,22 +887,63 @@ __device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
   }
 }
 
-// Stage h of (slot, half) pair hs in shared memory (all threads of the CTA,
-// after the slot's h is complete): planes [m][hi | lo][hstride] and scales.
-__device__ void stage_h(const DecParams& p, const Shared& s, int hs) {
+// Poll one published 64-bit word until it carries `want` in its low half
+// (bounded); returns the word, or the last one read after giving up.
+__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* w, unsigned want, long long limit,
+                                                        const DecParams& p, volatile int* abort) {
+  unsigned long long v = ld_relaxed_u64(w);
+  if ((unsigned)v == want) return v;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(64);
+    v = ld_relaxed_u64(w);
+    if ((unsigned)v == want || *abort) return v;
+    if (timed_out(t0, limit)) {
+      give_up(abort, p.f.status);
+      return v;
+    }
+  }
+}
+
+// Stage h of (slot, half) pair hs in shared memory (all threads, after every
+// warp is done reading the shared x, which this area overlays): planes
+// [m][hi | lo][hstride] and the per-16 scales. The gate/up reducers publish
+// h and its scales as 64-bit words (payload << 32 | launch number), so the
+// staging loads poll the data itself: no counter, no fence on either side.
+// Padding past the slot's ffn is zero.
+__device__ void stage_h(const DecParams& p, const Shared& s, int hs, volatile int* abort) {
   const FwdParams& f = p.f;
+  const unsigned seq = (unsigned)s.misc[3];
   const int slot = s.hs_slot[hs], half = s.hs_half[hs];
   const int q0 = s.slot_q0[slot] + kHalf * half, n = min(kHalf, s.slot_n[slot] - kHalf * half);
-  const int per_row = 2 * f.fmax64 / 8;  // 16-byte pieces of a row's two planes
-  for (int o = threadIdx.x; o < n * per_row; o += kThreads) {
-    const int m = o / per_row, k = o - m * per_row;
-    const int plane = k / (f.fmax64 / 8), kk = k - plane * (f.fmax64 / 8);
-    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(f.hbuf + ((size_t)(q0 + m) * 2 + plane) * f.fmax64) + kk);
-    *reinterpret_cast<uint4*>(s.hst + (size_t)(m * 2 + plane) * p.hstride + 8 * kk) = v;
-  }
+  const int fsl = (s.slot_e[slot] == f.E) ? f.S : f.F;
+  // the scale words; the timeout test makes these wait for a number no launch writes
+  const unsigned want_sc = seq + (unsigned)p.test_extra;
+  const long long lim_sc = p.test_extra ? p.test_wait_ns : p.wait_ns;
   for (int o = threadIdx.x; o < n * f.hgroups; o += kThreads) {
     const int m = o / f.hgroups, k = o - m * f.hgroups;
-    s.hsc[m * f.hgroups + k] = __ldcg(f.hscale + (size_t)(q0 + m) * f.hgroups + k);
+    float v = 0.f;
+    if (16 * k < fsl && !*abort)
+      v = __uint_as_float((unsigned)(poll_word(p.hswords + (size_t)(q0 + m) * f.hgroups + k, want_sc, lim_sc, p,
+                                               abort) >> 32));
+    s.hsc[m * f.hgroups + k] = v;
+  }
+  const int per_row = f.fmax64 / 2;  // element pairs of a row
+  for (int o = threadIdx.x; o < n * per_row; o += kThreads) {
+    const int m = o / per_row, i = 2 * (o - m * per_row);
+    uint32_t hv = 0, lv = 0;  // two f16 of each plane
+    if (i < fsl && !*abort) {
+      const unsigned long long* w = p.hwords + (size_t)(q0 + m) * f.fmax64 + i;
+      unsigned long long a, b;
+      ld_relaxed_u64x2(w, a, b);
+      if ((unsigned)a != seq) a = poll_word(w, seq, p.wait_ns, p, abort);
+      if ((unsigned)b != seq) b = poll_word(w + 1, seq, p.wait_ns, p, abort);
+      const uint32_t pa = (uint32_t)(a >> 32), pb = (uint32_t)(b >> 32);
+      hv = (pa & 0xFFFFu) | (pb << 16);
+      lv = (pa >> 16) | (pb & 0xFFFF0000u);
+    }
+    *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2) * p.hstride + i) = hv;
+    *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2 + 1) * p.hstride + i) = lv;
   }
 }
 
@@ -1006,9 +1036,6 @@ __device__ void gateup_item(const DecParams& p, const Shared& s, const Plan& pl,
   if (!arrive_chunk(s.ctl + us)) return;
   gateup_reduce(p, s, un, pb);
   free_slot(s.ctl + us, s.ctl + kMaxUS + us, it.u + p.n_us);
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) atomicAdd(&s.done[un.slot], 1);
 }
 
 template <int NT, int RG>
@@ -1112,15 +1139,9 @@ __device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* 
   if (pl.ndn > 0) {
     const int hs_first = pl.d0 / ud, hs_last = (pl.d0 + pl.ndn - 1) / ud;
     for (int hs = hs_first; hs <= hs_last; ++hs) {
-      const int hslot = s.hs_slot[hs];
-      const int fsl = (s.slot_e[hslot] == f.E) ? f.S : f.F;
-      // one poller per CTA; the barrier after it also ends every read of the
-      // shared x / previous h
-      if (threadIdx.x == 0)
-        wait_counter(&s.done[hslot], fsl / 16 + p.test_extra, abort, p.test_extra ? p.test_wait_ns : p.wait_ns,
-                     f.status);
+      // the first barrier ends every read of the shared x / previous h
       named_bar(2, kThreads);
-      if (!*abort) stage_h(p, s, hs);
+      stage_h(p, s, hs, abort);
       named_bar(2, kThreads);
       for (; j < pl.nguw + pl.ndnw; ++j) {
         const Item it = item_of(p, s, pl, w, j);
@@ -1165,14 +1186,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
   // This launch counts in half seq & 1 of the counters (zeroed by the previous
   // launch, or at creation) and zeroes the other half for the next launch.
   if (blockIdx.x == 0) {
-    int* dn = p.done + (size_t)((seq + 1) & 1) * (p.f.E + 1);
     int* rc = p.rowcnt + (size_t)((seq + 1) & 1) * (p.f.d / 16);
-    for (int i = tid; i <= p.f.E; i += kThreads) dn[i] = 0;
     for (int i = tid; i < p.f.d / 16; i += kThreads) rc[i] = 0;
   }
   stage_x(p, s);
   __syncthreads();
-  s.done = p.done + (size_t)(seq & 1) * (p.f.E + 1);
   s.rowcnt = p.rowcnt + (size_t)(seq & 1) * (p.f.d / 16);
   router(p, s, seq);  // its reads of the bf16 x end before its last barrier (it has none without experts)
   if (!scale_x_beside_topk(p)) {

@@ -169,7 +169,8 @@ constexpr int kLogitWordCopies = 8;
 constexpr int kFusedMaxPairs = 16;
 struct DecParams {
   FwdParams f;
-  int* done;            // [2][E+1] finished gate/up units per slot (half = launch sequence & 1)
+  unsigned long long* hwords;   // [Qd][fmax64] h as (f16 hi | f16 lo << 16) << 32 | launch sequence
+  unsigned long long* hswords;  // [Qd][hgroups] its per-16 scales: (fp32 bits << 32) | launch sequence
   int* rowcnt;          // [2][d/16] finished down units per row tile
   unsigned* bar_flags;  // [grid] per-CTA launch sequence numbers (each only grows)
   unsigned long long* lwords;  // [kLogitWordCopies][tcap][E][2] published logits: (fp32 bits << 32) | sequence
