@@ -917,33 +917,56 @@ __device__ void stage_h(const DecParams& p, const Shared& s, int hs, volatile in
   const int slot = s.hs_slot[hs], half = s.hs_half[hs];
   const int q0 = s.slot_q0[slot] + kHalf * half, n = min(kHalf, s.slot_n[slot] - kHalf * half);
   const int fsl = (s.slot_e[slot] == f.E) ? f.S : f.F;
-  // the scale words; the timeout test makes these wait for a number no launch writes
+  // Scale words and h words. Each round, every thread first issues all of its
+  // loads (kB of each), then checks them, polls the stale ones and stores: one
+  // round trip per round, not one per word. The timeout test makes the scale
+  // words wait for a number no launch writes.
+  constexpr int kB = 4;
   const unsigned want_sc = seq + (unsigned)p.test_extra;
   const long long lim_sc = p.test_extra ? p.test_wait_ns : p.wait_ns;
-  for (int o = threadIdx.x; o < n * f.hgroups; o += kThreads) {
-    const int m = o / f.hgroups, k = o - m * f.hgroups;
-    float v = 0.f;
-    if (16 * k < fsl && !*abort)
-      v = __uint_as_float((unsigned)(poll_word(p.hswords + (size_t)(q0 + m) * f.hgroups + k, want_sc, lim_sc, p,
-                                               abort) >> 32));
-    s.hsc[m * f.hgroups + k] = v;
-  }
   const int per_row = f.fmax64 / 2;  // element pairs of a row
-  for (int o = threadIdx.x; o < n * per_row; o += kThreads) {
-    const int m = o / per_row, i = 2 * (o - m * per_row);
-    uint32_t hv = 0, lv = 0;  // two f16 of each plane
-    if (i < fsl && !*abort) {
-      const unsigned long long* w = p.hwords + (size_t)(q0 + m) * f.fmax64 + i;
-      unsigned long long a, b;
-      ld_relaxed_u64x2(w, a, b);
-      if ((unsigned)a != seq) a = poll_word(w, seq, p.wait_ns, p, abort);
-      if ((unsigned)b != seq) b = poll_word(w + 1, seq, p.wait_ns, p, abort);
-      const uint32_t pa = (uint32_t)(a >> 32), pb = (uint32_t)(b >> 32);
-      hv = (pa & 0xFFFFu) | (pb << 16);
-      lv = (pa >> 16) | (pb & 0xFFFF0000u);
+  const int nsc = n * f.hgroups, nh = n * per_row, per_round = kThreads * kB;
+  const int rounds = (max(nsc, nh) + per_round - 1) / per_round;
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int o0 = rd * per_round + threadIdx.x;
+    unsigned long long v[kB], a[kB], b[kB];
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int o = o0 + u * kThreads;
+      const int ms = o / f.hgroups, k = o - ms * f.hgroups;
+      v[u] = (o < nsc && 16 * k < fsl) ? ld_relaxed_u64(p.hswords + (size_t)(q0 + ms) * f.hgroups + k) : 0ull;
+      const int m = o / per_row, i = 2 * (o - m * per_row);
+      a[u] = b[u] = 0ull;
+      if (o < nh && i < fsl) ld_relaxed_u64x2(p.hwords + (size_t)(q0 + m) * f.fmax64 + i, a[u], b[u]);
     }
-    *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2) * p.hstride + i) = hv;
-    *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2 + 1) * p.hstride + i) = lv;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const int o = o0 + u * kThreads;
+      if (o < nsc) {
+        const int ms = o / f.hgroups, k = o - ms * f.hgroups;
+        float sc = 0.f;
+        if (16 * k < fsl && !*abort) {
+          if ((unsigned)v[u] != want_sc)
+            v[u] = poll_word(p.hswords + (size_t)(q0 + ms) * f.hgroups + k, want_sc, lim_sc, p, abort);
+          sc = __uint_as_float((unsigned)(v[u] >> 32));
+        }
+        s.hsc[ms * f.hgroups + k] = sc;
+      }
+      if (o < nh) {
+        const int m = o / per_row, i = 2 * (o - m * per_row);
+        uint32_t hv = 0, lv = 0;  // two f16 of each plane
+        if (i < fsl && !*abort) {
+          const unsigned long long* w = p.hwords + (size_t)(q0 + m) * f.fmax64 + i;
+          if ((unsigned)a[u] != seq) a[u] = poll_word(w, seq, p.wait_ns, p, abort);
+          if ((unsigned)b[u] != seq) b[u] = poll_word(w + 1, seq, p.wait_ns, p, abort);
+          const uint32_t pa = (uint32_t)(a[u] >> 32), pb = (uint32_t)(b[u] >> 32);
+          hv = (pa & 0xFFFFu) | (pb << 16);
+          lv = (pa >> 16) | (pb & 0xFFFF0000u);
+        }
+        *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2) * p.hstride + i) = hv;
+        *reinterpret_cast<uint32_t*>(s.hst + (size_t)(m * 2 + 1) * p.hstride + i) = lv;
+      }
+    }
   }
 }
 
