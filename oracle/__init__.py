@@ -68,7 +68,10 @@ def _load():
             lib.oracle_expert_ffn.restype = i32
             lib.oracle_route.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
             lib.oracle_route.restype = i32
-            lib.oracle_layer_tokens.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+            lib.oracle_layer_tokens.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp,
+                                                vp]
+            lib.oracle_shared_gate_token.argtypes = [vp, i32, vp]
+            lib.oracle_shared_gate_token.restype = dbl
             lib.oracle_layer_tokens.restype = i32
             _lib = lib
     return _lib
@@ -171,10 +174,18 @@ def route(x: np.ndarray, w_router: np.ndarray, bias: np.ndarray | None, k: int) 
     return out
 
 
+def shared_gate_token(x_row: np.ndarray, w_sg: np.ndarray) -> float:
+    """sigmoid(w_sg . x_t) of one token (fp64)."""
+    x_row = np.ascontiguousarray(x_row, dtype=np.uint16)
+    w_sg = np.ascontiguousarray(w_sg, dtype=np.float32)
+    return _load().oracle_shared_gate_token(_p(x_row), x_row.shape[0], _p(w_sg))
+
+
 def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router: np.ndarray,
                  bias: np.ndarray | None, codes: np.ndarray, scales: np.ndarray, tokens=None,
-                 want_h: bool = False) -> dict:
-    """fp64 layer output of the listed tokens (default: all): y [n][d], ids, gates, optional h [n][k][F]."""
+                 want_h: bool = False, w_shared_gate: np.ndarray | None = None) -> dict:
+    """fp64 layer output of the listed tokens (default: all): y [n][d], ids, gates, optional h [n][k][F].
+    With w_shared_gate [d] the shared expert's output is scaled by sigmoid(w_shared_gate . x_t)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     T = x.shape[0]
     tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
@@ -184,7 +195,8 @@ def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router
     ids = np.empty((n, k), dtype=np.int32)
     gates = np.empty((n, k), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    sg = None if w_shared_gate is None else np.ascontiguousarray(w_shared_gate, dtype=np.float32)
     _check(_load().oracle_layer_tokens(d, F, E, k, S, _p(x), _p(np.ascontiguousarray(w_router, dtype=np.float32)),
                                        _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
-                                       _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates)), "layer_tokens")
+                                       _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates), _p(sg)), "layer_tokens")
     return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}

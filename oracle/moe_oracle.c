@@ -11,7 +11,8 @@
  *   top-k   the k largest logits of token t, largest first, ties to the lower e
  *   gates   g[t,j] = softmax over the k selected logits
  *   expert  h = SiLU(W_gate x) * (W_up x),   part = W_down h
- *   combine y[t] = sum_j g[t,j] part(t, j) + shared(x_t)   (shared: unweighted)
+ *   combine y[t] = sum_j g[t,j] part(t, j) + s_t shared(x_t)
+ *           s_t = 1 (no gate row), or s_t = sigmoid(w_sg . x_t) with a gate row
  *
  * Sources (page title, section):
  *   "Neural Server" technical page, "How one token and one prompt are
@@ -26,7 +27,13 @@
  *   "Nebula", "Description": the router selects experts and assigns them
  *     normalised weights; gate/up/down expert tensors.
  *   "Running Qwen3.8-Flash-Next on a 32 GB Mac with Transformers",
- *     architecture: routed experts plus one shared expert per layer.
+ *     architecture: routed experts plus one shared expert per layer; its table
+ *     of MoE blocks that carry a gate, a shared_expert and a
+ *     shared_expert_gate (Qwen2-MoE, Qwen3-Next, Qwen3.5-MoE, Qwen3.8).
+ *   "Nebula", the table of components held on the GPU: "shared expert gate",
+ *     F32, 0.000458 GiB = 48 layers x 2,560 x 4 bytes, i.e. one fp32 row of
+ *     the hidden size per layer (48 layers and hidden size 2,560 per the
+ *     Transformers page's model line): one scalar gate per token.
  * None of the pages defines MXFP4's values; they follow the OCP Microscaling
  * Formats (MX) v1.0 specification: E2M1 elements, one E8M0 scale per 32
  * consecutive elements along the reduction axis, value = E2M1 * 2^(e - 127).
@@ -38,7 +45,10 @@
  *   gates: softmax over the k selected logits (equal to the softmax over all
  *   E logits renormalised over the selected k);
  *   ties in top-k go to the lower expert index;
- *   the shared expert is added with weight 1.
+ *   the shared expert is added with weight 1; with a shared-expert gate row
+ *   w_sg [d] its output is scaled by sigmoid(w_sg . x_t) (the pages name the
+ *   tensor and its size, not the formula; the sigmoid of a one-row
+ *   projection is the plainest reading of a per-token gate).
  *
  * Canonical expert-major weight layout (one contiguous byte range per expert):
  *   codes : expert j at j * (3 F d / 2): gate/up [2F][d/2], then down [d][F/2]
@@ -96,6 +106,14 @@ void oracle_logits_token(const uint16_t* x, int d, const float* w_router, const 
     for (int i = 0; i < d; ++i) acc += (double)w_router[(size_t)e * d + i] * oracle_bf16(x[i]);
     logits[e] = acc + (bias ? (double)bias[e] : 0.0);
   }
+}
+
+/* Shared-expert gate of one token: s = 1 / (1 + exp(-z)), z = sum_i w_sg[i] x[i]
+ * in fp64, index order. */
+double oracle_shared_gate_token(const uint16_t* x, int d, const float* w_sg) {
+  double z = 0.0;
+  for (int i = 0; i < d; ++i) z += (double)w_sg[i] * oracle_bf16(x[i]);
+  return 1.0 / (1.0 + exp(-z));
 }
 
 /* Top-k of one token: repeatedly take the largest remaining logit, the lower
@@ -202,13 +220,17 @@ int oracle_route(const uint16_t* x, int T, int d, const float* w_router, const f
 }
 
 /* Layer output of the listed tokens (fp64, unrounded):
- *   y[n] = sum_j g[t,j] * expert(ids[t,j], x_t) + shared(x_t),   t = tokens[n]
- * summed in slot order j, the shared expert (when S > 0) last.
- * h_out (may be NULL) receives h of every (n, j) as [n_tokens][k][F]. */
+ *   y[n] = sum_j g[t,j] * expert(ids[t,j], x_t) + s_t * shared(x_t),   t = tokens[n]
+ * summed in slot order j, the shared expert (when S > 0) last; s_t = 1 when
+ * w_shared_gate is NULL, else oracle_shared_gate_token(x_t) (a gate row needs
+ * a shared expert). h_out (may be NULL) receives h of every (n, j) as
+ * [n_tokens][k][F]. */
 int oracle_layer_tokens(int d, int F, int E, int k, int S, const uint16_t* x, const float* w_router,
                         const float* bias, const uint8_t* codes, const uint8_t* scales, const int32_t* tokens,
-                        int n_tokens, double* y, double* h_out, int32_t* ids_out, double* gates_out) {
+                        int n_tokens, double* y, double* h_out, int32_t* ids_out, double* gates_out,
+                        const float* w_shared_gate) {
   if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || S < 0 || d % 32 || F % 32 || S % 32) return ORACLE_EINVAL;
+  if (w_shared_gate && S == 0) return ORACLE_EINVAL;
   size_t cb = oracle_expert_code_bytes(d, F), sb = oracle_expert_scale_bytes(d, F);
   double* l = (double*)malloc(sizeof(double) * (size_t)E);
   double* xv = (double*)malloc(sizeof(double) * (size_t)d);
@@ -235,7 +257,8 @@ int oracle_layer_tokens(int d, int F, int E, int k, int S, const uint16_t* x, co
     if (S > 0) {
       rc = oracle_expert_ffn(codes + (size_t)E * cb, scales + (size_t)E * sb, d, S, xv, NULL, part);
       if (rc) goto done;
-      for (int r = 0; r < d; ++r) yn[r] += part[r];
+      const double st = w_shared_gate ? oracle_shared_gate_token(xt, d, w_shared_gate) : 1.0;
+      for (int r = 0; r < d; ++r) yn[r] += st * part[r];
     }
   }
 done:

@@ -115,6 +115,7 @@ def _load():
             lib.synth_x.argtypes = [u64, i32, i32, vp]
             lib.synth_router.argtypes = [u64, i32, i32, vp]
             lib.synth_bias_zipf.argtypes = [u64, i32, ctypes.c_double, vp]
+            lib.synth_shared_gate.argtypes = [u64, i32, vp]
             lib.synth_code_bytes.argtypes = [u64, u64, sz, vp]
             lib.synth_scale_bytes.argtypes = [u64, u64, sz, i32, i32, vp]
             lib.synth_experts.argtypes = [u64, i32, i32, i32, i32, i32, i32, vp, vp, i32]
@@ -139,6 +140,13 @@ def gen_x(seed: int, T: int, d: int) -> np.ndarray:
 def gen_router(seed: int, E: int, d: int) -> np.ndarray:
     w = np.empty((E, d), dtype=np.float32)
     _load().synth_router(seed, E, d, _ptr(w))
+    return w
+
+
+def gen_shared_gate(seed: int, d: int) -> np.ndarray:
+    """Shared-expert gate row w_sg [d] fp32, N(0, 1/d), from a stream of its own."""
+    w = np.empty((d,), dtype=np.float32)
+    _load().synth_shared_gate(seed, d, _ptr(w))
     return w
 
 

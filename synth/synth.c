@@ -35,6 +35,7 @@
 #define SYNTH_STREAM_BIAS 3ULL
 #define SYNTH_STREAM_CODES 4ULL
 #define SYNTH_STREAM_SCALES 5ULL
+#define SYNTH_STREAM_SHARED_GATE 6ULL
 
 static inline uint64_t mix64(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
@@ -82,6 +83,12 @@ void synth_router(uint64_t seed, int E, int d, float* w) {
   size_t n = (size_t)E * (size_t)d;
   double sd = 1.0 / sqrt((double)d);
   for (size_t i = 0; i < n; ++i) w[i] = (float)(normal_at(seed, SYNTH_STREAM_ROUTER, i) * sd);
+}
+
+/* Shared-expert gate row w_sg: [d] fp32, N(0, 1/d) (the router's distribution). */
+void synth_shared_gate(uint64_t seed, int d, float* w) {
+  double sd = 1.0 / sqrt((double)d);
+  for (int i = 0; i < d; ++i) w[i] = (float)(normal_at(seed, SYNTH_STREAM_SHARED_GATE, (uint64_t)i) * sd);
 }
 
 /* Zipf(s) log-probability bias over a seeded permutation of ranks 1..E. */
