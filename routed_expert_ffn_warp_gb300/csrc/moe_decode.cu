@@ -57,8 +57,8 @@ constexpr int kWarps = 16;
 constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
 constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
 constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
-constexpr int kMaxUS = 8;
-constexpr int kLogitCopies = kLogitWordCopies;  // CTA b polls copy b % kLogitCopies          // unit slots (partial-sum buffers) per phase, at most
+constexpr int kMaxUS = 8;                       // unit slots (partial-sum buffers) per phase, at most
+constexpr int kLogitCopies = kLogitWordCopies;  // CTA b polls copy b % kLogitCopies
 
 struct Shared {
   int* ctl;     // [0, 8) gate/up arrivals, [8, 16) gate/up slot owners, [16, 24) down arrivals, [24, 32) down owners
