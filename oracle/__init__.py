@@ -72,6 +72,14 @@ def _load():
                                                 vp]
             lib.oracle_shared_gate_token.argtypes = [vp, i32, vp]
             lib.oracle_shared_gate_token.restype = dbl
+            lib.oracle_affine_code.argtypes = [vp, i32, i32, i32, i32]
+            lib.oracle_affine_code.restype = i32
+            lib.oracle_affine_element.argtypes = [vp, vp, vp, i32, i32, i32, i32]
+            lib.oracle_affine_element.restype = dbl
+            lib.oracle_affine_expert_bytes.argtypes = [i32, i32, i32]
+            lib.oracle_affine_expert_bytes.restype = ctypes.c_size_t
+            lib.oracle_expert_ffn_affine.argtypes = [vp, i32, i32, i32, vp, vp]
+            lib.oracle_expert_ffn_affine.restype = i32
             lib.oracle_layer_tokens.restype = i32
             _lib = lib
     return _lib
@@ -200,3 +208,28 @@ def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router
                                        _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
                                        _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates), _p(sg)), "layer_tokens")
     return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}
+
+
+# ---------------------------------------------------------------- affine group-64 experts
+
+def affine_code(packed: np.ndarray, K: int, bits: int, r: int, c: int) -> int:
+    return _load().oracle_affine_code(_p(np.ascontiguousarray(packed)), K, bits, r, c)
+
+
+def affine_element(packed: np.ndarray, scales: np.ndarray, biases: np.ndarray, K: int, bits: int, r: int,
+                   c: int) -> float:
+    return _load().oracle_affine_element(_p(np.ascontiguousarray(packed)), _p(np.ascontiguousarray(scales)),
+                                         _p(np.ascontiguousarray(biases)), K, bits, r, c)
+
+
+def affine_expert_bytes(d: int, f: int, bits: int) -> int:
+    return _load().oracle_affine_expert_bytes(d, f, bits)
+
+
+def expert_ffn_affine(expert: np.ndarray, d: int, f: int, bits: int, x: np.ndarray) -> np.ndarray:
+    """One affine group-64 expert (codes, bf16 scales, bf16 biases in one byte range) on one fp64 vector."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty((d,), dtype=np.float64)
+    _check(_load().oracle_expert_ffn_affine(_p(np.ascontiguousarray(expert)), d, f, bits, _p(x), _p(out)),
+           "expert_ffn_affine")
+    return out

@@ -265,3 +265,72 @@ done:
   free(l); free(xv); free(part); free(ids); free(g);
   return rc;
 }
+
+/* ---------------------------------------------------------------- affine group-64 experts
+ *
+ * A second expert weight format on the pages: "Running Qwen3.8-Flash-Next on a
+ * 32 GB Mac with Transformers", the table of weights ("3-bit MLX affine, group
+ * 64, 2.15 MB per expert") and its comparison bullets ("a 16-bit scale and
+ * bias per 64 weights", about 3.5 bits per weight). Readings (the pages give
+ * neither formula nor packing): an element is w = scale * q + bias with q the
+ * unsigned `bits`-bit code of its group of 64 along the reduction axis;
+ * scale and bias are bf16; a row's codes form one little-endian bit stream,
+ * element c in bits [bits*c, bits*c + bits) of the row (K * bits / 8 bytes).
+ * Per expert: gate/up [2f][d] then down [d][f], codes then scales then biases,
+ * each matrix row-major. */
+
+/* Code c of row r of a packed matrix (rows of K codes of `bits` bits). */
+int oracle_affine_code(const uint8_t* packed, int K, int bits, int r, int c) {
+  const uint8_t* row = packed + (size_t)r * (size_t)K * (size_t)bits / 8;
+  int q = 0;
+  for (int b = 0; b < bits; ++b) {
+    long bit = (long)c * bits + b;
+    q |= ((row[bit / 8] >> (bit % 8)) & 1) << b;
+  }
+  return q;
+}
+
+/* Element (r, c): scale * q + bias of the element's group of 64. */
+double oracle_affine_element(const uint8_t* packed, const uint16_t* scales, const uint16_t* biases, int K, int bits,
+                             int r, int c) {
+  size_t g = (size_t)r * (size_t)(K / 64) + (size_t)(c / 64);
+  return oracle_bf16(scales[g]) * (double)oracle_affine_code(packed, K, bits, r, c) + oracle_bf16(biases[g]);
+}
+
+/* Bytes of one affine expert: packed codes of the 3 f d weights, then a bf16
+ * scale and a bf16 bias per 64 of them. */
+size_t oracle_affine_expert_bytes(int d, int f, int bits) {
+  size_t n = (size_t)3 * (size_t)f * (size_t)d;
+  return n * (size_t)bits / 8 + (n / 64) * 2 * 2;
+}
+
+/* One affine expert (ffn f) on one input vector x[d] (fp64); `expert` points
+ * at its oracle_affine_expert_bytes(d, f, bits) bytes. Same arithmetic as
+ * oracle_expert_ffn, with affine elements. */
+int oracle_expert_ffn_affine(const uint8_t* expert, int d, int f, int bits, const double* x, double* out) {
+  if (d <= 0 || f <= 0 || d % 64 || f % 64 || bits < 1 || bits > 8) return ORACLE_EINVAL;
+  const size_t n_gu = (size_t)2 * f * d, n_dn = (size_t)d * f;
+  const uint8_t* gu_codes = expert;
+  const uint8_t* dn_codes = gu_codes + n_gu * (size_t)bits / 8;
+  const uint16_t* gu_scales = (const uint16_t*)(dn_codes + n_dn * (size_t)bits / 8);
+  const uint16_t* dn_scales = gu_scales + n_gu / 64;
+  const uint16_t* gu_biases = dn_scales + n_dn / 64;
+  const uint16_t* dn_biases = gu_biases + n_gu / 64;
+  double* hv = (double*)malloc(sizeof(double) * (size_t)f);
+  if (!hv) return ORACLE_ENOMEM;
+  for (int i = 0; i < f; ++i) {
+    double gate = 0.0, up = 0.0;
+    for (int c = 0; c < d; ++c) {
+      gate += oracle_affine_element(gu_codes, gu_scales, gu_biases, d, bits, i, c) * x[c];
+      up += oracle_affine_element(gu_codes, gu_scales, gu_biases, d, bits, f + i, c) * x[c];
+    }
+    hv[i] = gate / (1.0 + exp(-gate)) * up;
+  }
+  for (int r = 0; r < d; ++r) {
+    double acc = 0.0;
+    for (int i = 0; i < f; ++i) acc += oracle_affine_element(dn_codes, dn_scales, dn_biases, f, bits, r, i) * hv[i];
+    out[r] = acc;
+  }
+  free(hv);
+  return ORACLE_OK;
+}
