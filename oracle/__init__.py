@@ -11,7 +11,9 @@ their bit-field definitions, the 13,219,200-byte expert of the "Neural Server"
 technical page, hand-computed closed-form layers, brute-force top-k over all
 subsets, exact ties, gate and bucketing invariants, exact power-of-two scaling,
 expert-relabel equivariance, and an independent dense float64 PyTorch
-restatement on tiny layers.
+restatement on tiny layers. The optional sigmoid-gated shared expert
+(tests/test_oracle_shared_gate.py) and the affine group-64 expert format
+(tests/test_oracle_affine.py) have pins of their own.
 """
 from __future__ import annotations
 

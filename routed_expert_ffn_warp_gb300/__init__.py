@@ -60,6 +60,8 @@ _lib = None
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load the compiled library (build it with ``routed_expert_ffn_warp_gb300.build``)."""
     global _lib
+    if _lib is not None:  # every forward call comes through here: no lock once loaded
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(path):
