@@ -74,6 +74,9 @@ def _load():
                                                 vp]
             lib.oracle_shared_gate_token.argtypes = [vp, i32, vp]
             lib.oracle_shared_gate_token.restype = dbl
+            lib.oracle_layer_tokens_shard.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                      i32, vp, vp]
+            lib.oracle_layer_tokens_shard.restype = i32
             lib.oracle_affine_code.argtypes = [vp, i32, i32, i32, i32]
             lib.oracle_affine_code.restype = i32
             lib.oracle_affine_element.argtypes = [vp, vp, vp, i32, i32, i32, i32]
@@ -210,6 +213,25 @@ def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router
                                        _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
                                        _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates), _p(sg)), "layer_tokens")
     return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}
+
+
+def layer_tokens_shard(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router: np.ndarray,
+                       bias: np.ndarray | None, codes: np.ndarray, scales: np.ndarray, e_begin: int, e_end: int,
+                       with_shared: bool, tokens=None, w_shared_gate: np.ndarray | None = None) -> np.ndarray:
+    """One expert shard's part of the layer output [n][d]: global routing, only experts in
+    [e_begin, e_end) contribute, the shared expert only when with_shared."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    y = np.empty((tokens.shape[0], d), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    sg = None if w_shared_gate is None else np.ascontiguousarray(w_shared_gate, dtype=np.float32)
+    _check(_load().oracle_layer_tokens_shard(d, F, E, k, S, _p(x), _p(np.ascontiguousarray(w_router,
+                                                                                         dtype=np.float32)),
+                                             _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
+                                             _p(tokens), tokens.shape[0], e_begin, e_end, 1 if with_shared else 0,
+                                             _p(sg), _p(y)), "layer_tokens_shard")
+    return y
 
 
 # ---------------------------------------------------------------- affine group-64 experts

@@ -266,6 +266,52 @@ done:
   return rc;
 }
 
+/* One expert shard's part of the layer output (fp64, unrounded), for expert
+ * parallelism (one GPU per contiguous range of experts): routing over all E
+ * experts as in oracle_layer_tokens, but only the pairs whose expert is in
+ * [e_begin, e_end) contribute, in slot order, and the shared expert (scaled
+ * as in oracle_layer_tokens) only when with_shared is nonzero. The shards of a
+ * partition of [0, E), one of them with the shared expert, add up to the
+ * layer output. */
+int oracle_layer_tokens_shard(int d, int F, int E, int k, int S, const uint16_t* x, const float* w_router,
+                              const float* bias, const uint8_t* codes, const uint8_t* scales, const int32_t* tokens,
+                              int n_tokens, int e_begin, int e_end, int with_shared, const float* w_shared_gate,
+                              double* y) {
+  if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || S < 0 || d % 32 || F % 32 || S % 32) return ORACLE_EINVAL;
+  if (e_begin < 0 || e_end > E || e_begin > e_end || (w_shared_gate && S == 0)) return ORACLE_EINVAL;
+  size_t cb = oracle_expert_code_bytes(d, F), sb = oracle_expert_scale_bytes(d, F);
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  double* xv = (double*)malloc(sizeof(double) * (size_t)d);
+  double* part = (double*)malloc(sizeof(double) * (size_t)d);
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+  double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  int rc = ORACLE_OK;
+  if (!l || !xv || !part || !ids || !g) { rc = ORACLE_ENOMEM; goto done; }
+  for (int n = 0; n < n_tokens; ++n) {
+    const uint16_t* xt = x + (size_t)tokens[n] * d;
+    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(xt[i]);
+    oracle_logits_token(xt, d, w_router, bias, E, l);
+    oracle_topk_token(l, E, k, ids, g);
+    double* yn = y + (size_t)n * d;
+    for (int r = 0; r < d; ++r) yn[r] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      if (ids[j] < e_begin || ids[j] >= e_end) continue;
+      rc = oracle_expert_ffn(codes + (size_t)ids[j] * cb, scales + (size_t)ids[j] * sb, d, F, xv, NULL, part);
+      if (rc) goto done;
+      for (int r = 0; r < d; ++r) yn[r] += g[j] * part[r];
+    }
+    if (S > 0 && with_shared) {
+      rc = oracle_expert_ffn(codes + (size_t)E * cb, scales + (size_t)E * sb, d, S, xv, NULL, part);
+      if (rc) goto done;
+      const double st = w_shared_gate ? oracle_shared_gate_token(xt, d, w_shared_gate) : 1.0;
+      for (int r = 0; r < d; ++r) yn[r] += st * part[r];
+    }
+  }
+done:
+  free(l); free(xv); free(part); free(ids); free(g);
+  return rc;
+}
+
 /* ---------------------------------------------------------------- affine group-64 experts
  *
  * A second expert weight format on the pages: "Running Qwen3.8-Flash-Next on a
