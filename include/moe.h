@@ -67,8 +67,8 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
 
 /* moe_config.flags bits.
  * MOE_FLAG_TEST_FORCE_TIMEOUT exists for failure-detection tests only: one
- *   device-side wait of every single-kernel decode forward targets a count
- *   nothing reaches and gives up after 2 ms, so the forward completes with
+ *   device-side wait of every single-kernel decode forward waits for a value
+ *   no launch writes and gives up after 2 ms, so the forward completes with
  *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
  * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path (for
  *   testing both paths on the same shapes).

@@ -180,7 +180,7 @@ struct DecParams {
   int xstride, hstride; // f16 row strides of the shared x and h
   int off_x16, off_hsc, off_xinv, off_red, off_pgu, off_pdn, off_route, off_ring, smem_bytes;
   long long wait_ns;       // bound of every device-side wait
-  int test_extra;          // > 0: one wait targets an unreachable count (timeout test)
+  int test_extra;          // > 0: the h staging waits for a launch number no launch writes (timeout test)
   long long test_wait_ns;  // bound of that wait
 };
 bool decode_plan(DecParams& p, int max_smem, int num_sms);
