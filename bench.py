@@ -21,7 +21,12 @@ host-buffer entry point, the CPU oracle on a bounded sample, and SM clocks
 sampled during the timed region.
 
 ``--impl reference``: the CPU oracle (plain fp64 C) as the reference arm on
-the host cores, one layer-token per step.
+all host cores (one single-token layer evaluation per core and step).
+
+By default the line carries, besides the main workload (``--workload``,
+default decode), the other three full-size workloads under ``workloads``
+(``--extra-workloads``), each with its own timing, roofline and e2e, and the
+measured rate of the block-scaled MMA kind the expert GEMMs issue.
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (independent batches, no collective on the data path); rank 0 prints the
@@ -69,12 +74,27 @@ def phase_bytes(wl: synth.Workload, U: int, T: int) -> dict:
     gu = U * (F * d + F * d // 16) + (S * d + S * d // 16 if S else 0) + 2 * T * d
     dn = U * (F * d // 2 + F * d // 32) + (S * d // 2 + S * d // 32 if S else 0)
     route = wl.E * d * 4 + (4 * wl.E if wl.zipf_bias else 0) + 2 * T * d
-    # "layer" is the fused single-kernel path (T <= 16): every byte of the layer in one launch
-    return {"route": route, "gateup": gu, "down": dn, "combine": 2 * T * d, "layer": layer_bytes(wl, U, T)}
+    # "layer" is the fused single-kernel path (T <= 16): every byte of the layer in one launch;
+    # "panels" (tcgen05 path) reads x once
+    return {"route": route, "panels": 2 * T * d, "gateup": gu, "down": dn, "combine": 2 * T * d,
+            "layer": layer_bytes(wl, U, T)}
 
 
 def layer_flops(wl: synth.Workload, T: int) -> int:
     return 2 * T * wl.E * wl.d + 2 * T * wl.k * 3 * wl.d * wl.ffn + 2 * T * 3 * wl.d * wl.shared_ffn
+
+
+def phase_flops(wl: synth.Workload, T: int) -> dict:
+    """Algorithmic flops of the phases: the router, the gate/up and down GEMMs (2 flops per multiply-add)."""
+    P = T * wl.k
+    gu = 2 * P * 2 * wl.ffn * wl.d + 2 * T * 2 * wl.shared_ffn * wl.d
+    dn = 2 * P * wl.ffn * wl.d + 2 * T * wl.shared_ffn * wl.d
+    return {"route": 2 * T * wl.E * wl.d, "gateup": gu, "down": dn, "layer": layer_flops(wl, T)}
+
+
+# dense FP4 / FP8 tensor rates of the GB300 (nominal 13.5 and 4.5 PFLOP/s): the FP4 peak is the
+# measured rate of the FP8-rate MMA kind times this ratio
+FP4_OVER_FP8 = 3.0
 
 
 # ---------------------------------------------------------------- clocks (NVML via ctypes; nvidia-smi fallback)
@@ -205,23 +225,33 @@ def rank_x(wl: synth.Workload, layer: int, rank: int) -> np.ndarray:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(wl: synth.Workload, budget_s: float, max_samples: int, first_layer: int = 0):
-    """Time the CPU oracle on layer-token evaluations of the workload (layer l,
-    token 0 for l = first_layer, ...) until budget_s of oracle time is spent.
-    Input generation is outside the timed region."""
+def oracle_sample(wl: synth.Workload, budget_s: float, max_rounds: int, threads: int, first_round: int = 0):
+    """Time the CPU oracle, as it stands, on whole-layer evaluations of single tokens of the
+    workload's layer 0 (router over all experts, top-k, the k experts, the shared expert,
+    combine; fp64), `threads` tokens per round on `threads` host threads, until budget_s of
+    wall time is spent or max_rounds rounds ran. Each token is a fresh seeded draw from the
+    workload's x distribution; the layer's weights are generated once, outside the timed region."""
     import oracle
-    done, spent = 0, 0.0
-    for i in range(max_samples):
-        layer = (first_layer + i) % wl.layers
-        L = synth.gen_layer(wl, layer)
+    L = synth.gen_layer(wl, 0, T=1)
+    done, spent, rounds = 0, 0.0, 0
+    for r in range(max_rounds):
+        x = synth.gen_x(wl.seed(0) + 7_919 * (first_round + r + 1), threads, wl.d)
         t0 = time.perf_counter()
-        oracle.layer_tokens(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, L["x"], L["w_router"], L["bias"],
-                            L["codes"], L["scales"], tokens=[0])
+        oracle.layer_tokens_parallel(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, x, L["w_router"], L["bias"],
+                                     L["codes"], L["scales"], threads=threads)
         spent += time.perf_counter() - t0
-        done += 1
+        done += threads
+        rounds += 1
         if spent >= budget_s:
             break
-    return done, spent
+    return done, spent, rounds
+
+
+def cpu_sample_text(wl: synth.Workload, n: int, spent: float, threads: int) -> str:
+    return (f"{n} whole-layer evaluations of single tokens (fresh seeded x) through layer 0 of the '{wl.name}' "
+            f"workload (router over all {wl.E} experts, top-{wl.k}, the selected experts"
+            f"{', the shared expert' if wl.shared_ffn else ''}, combine; fp64), {threads} tokens at a time on "
+            f"{threads} host threads, {spent:.1f} s")
 
 
 # ---------------------------------------------------------------- reference arm
@@ -232,50 +262,44 @@ def run_reference(args, wl):
         return 0
     import oracle
     oracle.build()
+    threads = oracle.host_threads()
     for i in range(args.warmup):
-        oracle_sample(wl, 0.0, 1, first_layer=i)
+        oracle_sample(wl, 0.0, 1, threads, first_round=i)
     times = []
+    n_tot = 0
     for i in range(args.steps):
-        n, s = oracle_sample(wl, 0.0, 1, first_layer=args.warmup + i)
-        times.append(s)
+        n, spent, _ = oracle_sample(wl, 0.0, 1, threads, first_round=args.warmup + i)
+        times.append(spent)
+        n_tot += n
     total = sum(times)
-    value = args.steps / total
+    value = n_tot / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(wl, args),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"one layer-token per step: workload '{wl.name}', layer = step index, token 0, "
-                                   "full layer (router, top-k, k experts, combine) in fp64"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "per step: " + cpu_sample_text(wl, threads, total / args.steps, threads)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def config_of(wl: synth.Workload, args) -> dict:
+def config_of(wl: synth.Workload, args, layers: int | None = None) -> dict:
+    nl = args.layers if layers is None else layers
     return {"workload": f"{wl.name}: MoE layer T={wl.T}, d={wl.d}, ffn={wl.ffn}, E={wl.E}, k={wl.k}, "
-                        f"shared_ffn={wl.shared_ffn}, zipf_bias={wl.zipf_bias}, layers={args.layers}, MXFP4 experts",
+                        f"shared_ffn={wl.shared_ffn}, zipf_bias={wl.zipf_bias}, layers={nl}, MXFP4 experts",
             "T": wl.T, "d": wl.d, "ffn": wl.ffn, "n_experts": wl.E, "top_k": wl.k, "shared_ffn": wl.shared_ffn,
-            "layers": args.layers, "zipf_bias": wl.zipf_bias, "parallelism": f"replica x{args.gpus}",
+            "layers": nl, "zipf_bias": wl.zipf_bias, "parallelism": f"replica x{args.gpus}",
             "l2": "inputs larger than L2: each step streams every layer's routed experts from HBM; no flush"}
 
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, wl):
-    import torch
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    from routed_expert_ffn_warp_gb300 import build as lib_build
-    lib_build.build()
-    import routed_expert_ffn_warp_gb300 as m
-
-    nl = args.layers
+def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank: int, local: int,
+                     peaks: dict) -> dict:
+    """All layers of one workload resident; graph-timed value, per-phase roofline, e2e."""
     T = wl.T
     shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T, flags=args.flags)
     codes_h = torch.empty((wl.total_code_bytes,), dtype=torch.uint8, pin_memory=True)
@@ -325,7 +349,7 @@ def run_ours(args, wl):
     stream.synchronize()
     bad = [lay.status() for lay in layers]
     if any(bad):
-        raise RuntimeError(f"device status after warm-up: {bad[:4]}... (a bounded device wait gave up)")
+        raise RuntimeError(f"{wl.name}: device status after warm-up: {bad[:4]}... (a bounded device wait gave up)")
     clocks = ClockSampler(local)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -344,6 +368,7 @@ def run_ours(args, wl):
     ms = reduce_max(ms_local, ws)
     value = whole_job_value(ws, T * nl, ms / 1000.0)
     status = max(lay.status() for lay in layers)
+    del graph
 
     # per-kernel timing: the library records events at its phase boundaries
     phases = m.moe_forward_phases(layers[0].ctx, T)
@@ -370,21 +395,23 @@ def run_ours(args, wl):
             for i, p in enumerate(phases):
                 ph_ms[p] += ev[s][l][i].elapsed_time(ev[s][l][i + 1])
     ph_bytes = {p: 0 for p in phases}
+    ph_flops = {p: 0 for p in phases}
     for u in U:
         pb = phase_bytes(wl, u, T)
+        pf = phase_flops(wl, T)
         for p in phases:
             ph_bytes[p] += pb.get(p, 0) * ksteps
+            ph_flops[p] += pf.get(p, 0) * ksteps
     dom = max(phases, key=lambda p: ph_ms[p])
     launches = ksteps * nl
     if len(phases) == 1:
         # a one-launch layer: the timed region's graph replays hold that kernel alone, so its
         # average launch duration is the timed region's time per layer (no eager gaps)
         ph_ms = {dom: ms / nl * launches}
-    peaks = measured_peaks()
     achieved = ph_bytes[dom] / (ph_ms[dom] / 1000.0) / 1e9
     traffic = ncu_traffic(dom, wl.name)
 
-    # end to end through the host-buffer entry point (pinned x in, result out, every step)
+    # end to end through the host-buffer entry point (pinned x in, result out, every layer)
     with torch.cuda.stream(stream):
         for l in range(nl):
             layers[l].forward_host(xh[l], T, oh[l], stream, synchronize=(l == nl - 1))
@@ -398,44 +425,113 @@ def run_ours(args, wl):
     t_e2e = reduce_max(t_e2e, ws)
     e2e_value = whole_job_value(ws, T * nl, t_e2e)
 
+    launches_per_fwd = m.moe_launches_per_forward(layers[0].ctx, T)
+    weight_bytes = layers[0].weight_bytes()
+    for lay in layers:
+        lay.close()
+    del layers, xs, outs, xh, oh
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    hbm = ws * bytes_step / (ms / 1000.0) / 1e9
+    return {
+        "value": value, "ms_per_step": ms, "us_per_layer": 1000.0 * ms / nl, "layers": nl,
+        "hbm_gbs": hbm, "hbm_frac_of_measured": hbm / ws / peaks["hbm_gbs"],
+        "tflops": ws * flops_step / (ms / 1000.0) / 1e12,
+        "bytes_per_layer": bytes_step / nl, "flops_per_layer": flops_step / nl,
+        "distinct_experts_per_layer": statistics.mean(U),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": ph_bytes[dom] / launches,
+                     "avg_launch_us": 1000.0 * ph_ms[dom] / launches,
+                     "phase_us_per_layer": {p: 1000.0 * ph_ms[p] / launches for p in phases},
+                     "phase_gbs": {p: ph_bytes[p] / (ph_ms[p] / 1000.0) / 1e9 for p in phases if ph_ms[p] > 0},
+                     "phase_tflops": {p: ph_flops[p] / (ph_ms[p] / 1000.0) / 1e12 for p in phases
+                                      if ph_ms[p] > 0 and ph_flops[p] > 0}},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": nl * T * wl.d * 2,
+                "d2h_bytes_per_step": nl * T * wl.d * 2, "via": "moe_forward_host (pinned host buffers)"},
+        "gpu_launches": args.steps * nl * launches_per_fwd, "launches_per_layer": launches_per_fwd,
+        "clocks": clk, "device_status": status, "setup_s": t_gen, "weight_bytes_per_layer": weight_bytes,
+    }
+
+
+def prefill_tensor_view(res: dict, fp4_peak: float | None, peaks: dict) -> dict:
+    """The layer's algorithmic TFLOP/s against the attainable min(FP4 peak, AI x HBM) and the FP4 peak."""
+    ai = res["flops_per_layer"] / res["bytes_per_layer"]
+    out = {"tflops": res["tflops"], "arithmetic_intensity_flop_per_byte": ai,
+           "hbm_bound_tflops": ai * peaks["hbm_gbs"] / 1000.0}
+    if fp4_peak:
+        att = min(fp4_peak, ai * peaks["hbm_gbs"] / 1000.0)
+        out.update({"fp4_peak_tflops": fp4_peak, "attainable_tflops": att, "frac_of_attainable": res["tflops"] / att,
+                    "frac_of_fp4_peak": res["tflops"] / fp4_peak})
+    return out
+
+
+def run_ours(args, wl):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from routed_expert_ffn_warp_gb300 import build as lib_build
+    lib_build.build()
+    import routed_expert_ffn_warp_gb300 as m
+
+    peaks = measured_peaks()
+    main = measure_workload(args, wl, args.layers, m, torch, ws, rank, local, peaks)
+
+    # the block-scaled MMA rate of this GPU (the kind the expert GEMMs issue)
+    mma = None
+    if not args.no_mma_probe:
+        tf, pms = m.moe_probe_mma_rate(local, args.mma_probe_steps)
+        mma = {"kind": "tcgen05.mma kind::mxf8f6f4 (E2M1 x E4M3, UE8M0 scales), M=128 N=192 K=32",
+               "tflops": tf, "ms": pms, "unit": "TFLOP/s",
+               "fp4_peak_tflops": tf * FP4_OVER_FP8,
+               "fp4_peak_source": f"measured mxf8f6f4 rate x {FP4_OVER_FP8:g} (nominal dense FP4 / FP8 ratio, "
+                                  "13.5 / 4.5 PFLOP/s)"}
+
+    extras = {}
+    for name in [w for w in args.extra_workloads.split(",") if w and w != wl.name]:
+        wx = synth.WORKLOADS[name]
+        res = measure_workload(args, wx, wx.layers, m, torch, ws, rank, local, peaks)
+        res["config"] = config_of(wx, args, wx.layers)
+        if name == "prefill":
+            res["tensor"] = prefill_tensor_view(res, mma["fp4_peak_tflops"] if mma else None, peaks)
+        extras[name] = res
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        n, spent = oracle_sample(wl, args.cpu_budget, 64)
-        cpu = {"value": n / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n} layer-token evaluations (layers 0..{n - 1}, token 0 of each) of the '{wl.name}' "
-                         f"workload, full layer in fp64, {spent:.1f} s single-threaded"}
+        threads = oracle.host_threads()
+        n, spent, _ = oracle_sample(wl, args.cpu_budget, 64, threads)
+        cpu = {"value": n / spent, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": cpu_sample_text(wl, n, spent, threads)}
 
-    launches_per_fwd = m.moe_launches_per_forward(layers[0].ctx, T)
-    for lay in layers:
-        lay.close()
     if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return 0
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4-f16-f32acc", "data": "synthetic (seeded counter-based generator; random MXFP4 weights)",
+        "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4-f16-f32acc",
+        "data": "synthetic (seeded counter-based generator; random MXFP4 weights)",
         "config": config_of(wl, args),
-        "hbm_gbs": ws * bytes_step / (ms / 1000.0) / 1e9,
-        "hbm_frac_of_measured": (bytes_step / (ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
-        "tflops": ws * flops_step / (ms / 1000.0) / 1e12,
-        "us_per_layer": 1000.0 * ms / nl,
-        "distinct_experts_per_layer": statistics.mean(U),
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
-                     else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": ph_bytes[dom] / launches,
-                     "avg_launch_us": 1000.0 * ph_ms[dom] / launches,
-                     "phase_ms_share": {p: ph_ms[p] / sum(ph_ms.values()) for p in phases}},
+        "hbm_gbs": main["hbm_gbs"], "hbm_frac_of_measured": main["hbm_frac_of_measured"], "tflops": main["tflops"],
+        "us_per_layer": main["us_per_layer"], "distinct_experts_per_layer": main["distinct_experts_per_layer"],
+        "roofline": main["roofline"],
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": nl * T * wl.d * 2,
-                "d2h_bytes_per_step": nl * T * wl.d * 2, "via": "moe_forward_host (pinned host buffers)"},
-        "gpu_launches": args.steps * nl * launches_per_fwd,
-        "clocks": clk,
-        "device_status": status,
-        "setup_s": t_gen,
+        "e2e": main["e2e"],
+        "gpu_launches": main["gpu_launches"],
+        "clocks": main["clocks"],
+        "device_status": main["device_status"],
+        "setup_s": main["setup_s"],
+        "mma_probe": mma,
+        "workloads": extras,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -453,9 +549,14 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="decode")
     ap.add_argument("--layers", type=int, default=None, help="layers per step (default: the workload's)")
     ap.add_argument("--kernel-steps", type=int, default=3, help="eager steps for per-kernel event timing")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle wall time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 8: register-decode GEMMs instead of tcgen05)")
+    ap.add_argument("--extra-workloads", default="verify,small,prefill",
+                    help="comma-separated workloads measured after the main one and reported under 'workloads' "
+                         "('' for none)")
+    ap.add_argument("--no-mma-probe", action="store_true")
+    ap.add_argument("--mma-probe-steps", type=int, default=200000, help="MMAs per SM of the rate probe")
     args = ap.parse_args(argv)
     wl = synth.WORKLOADS[args.workload]
     if args.layers is None:

@@ -99,49 +99,90 @@ typedef struct moe_config {
 
 typedef struct moe_ctx moe_ctx;
 
-/* Create a context on CUDA device `device`. Allocates all device memory the
- * layer will ever use (weights in the library's packed layout, router, and a
- * workspace sized for t_max); no later call allocates. On success *out holds
- * the context; on failure *out is NULL and the return code says why. */
+/* Create a context for one MoE layer of the shape cfg gives ("Neural Server"
+ * technical page, "What it runs on and what it runs": 128 experts, four
+ * active per token, hidden 2880, per-expert MXFP4 weights; "Running
+ * Qwen3.8-Flash-Next on a 32 GB Mac with Transformers", architecture: one
+ * shared expert beside the routed ones) on CUDA device `device`. Allocates all
+ * device memory the layer will ever use (weights in the library's packed
+ * layout, router, and a workspace sized for t_max); no later call allocates.
+ * Sets the per-device attributes of the library's kernels on `device`. On
+ * success *out holds the context (owned by the caller, freed by moe_destroy);
+ * on failure *out is NULL, nothing is left allocated, and the return code
+ * says why: MOE_ERR_INVALID_ARG (a config field out of range),
+ * MOE_ERR_NOMEM (a device allocation failed), MOE_ERR_CUDA. */
 int moe_create(const moe_config* cfg, int device, moe_ctx** out);
 
-/* Copy the router: w is fp32 [n_experts][d] row-major, bias is fp32
- * [n_experts] or NULL (no bias). Host or device pointers (cudaMemcpyDefault).
- * Synchronous. Section: "Neural Server", "How one token ... processed". */
+/* Copy the router of the layer ("Neural Server" technical page, "How one
+ * token and one prompt are processed": the router and top-k step that turn a
+ * token's hidden state into expert ids and weights): w is fp32
+ * [n_experts][d] row-major, bias is fp32 [n_experts] or NULL (no bias). Host
+ * or device pointers (cudaMemcpyDefault); the caller keeps ownership of both.
+ * Synchronous. Errors: MOE_ERR_INVALID_ARG (w NULL), MOE_ERR_CUDA. */
 int moe_load_router(moe_ctx* ctx, const float* w, const float* bias);
 
-/* Copy all experts (canonical layout above; host or device pointers) and
- * repack them on the device into the library's tile layout. The repack is
- * lossless: every code and scale byte is kept, only their order changes.
- * Synchronous. Returns MOE_ERR_NAN_SCALE if any scale byte is 0xFF. */
+/* Copy all experts (canonical layout above; host or device pointers, still
+ * owned by the caller) and repack them on the device into the library's tile
+ * layout. The "Neural Server" technical page keeps its expert store the same
+ * way ("A 117B-parameter model on one gaming PC": a byte-exact repack of the
+ * checkpoint's MXFP4 tensors; "What it runs on and what it runs": 13,219,200 B
+ * per expert). The repack is lossless: every code and scale byte is kept,
+ * only their order changes. Synchronous; uses a temporary
+ * staging buffer that it frees before returning. Errors: MOE_ERR_INVALID_ARG
+ * (a NULL pointer), MOE_ERR_NAN_SCALE (a scale byte 0xFF, the OCP MX NaN;
+ * the context then counts as not loaded), MOE_ERR_NOMEM, MOE_ERR_CUDA. */
 int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales);
 
-/* Run the layer on T tokens (0 <= T <= t_max). x: bf16 [T][d] row-major in
- * device memory; out: [T][d] row-major in device memory, bf16 or fp32 as the
- * config says. stream: a cudaStream_t (NULL = the legacy default stream).
+/* Run the layer on T tokens (0 <= T <= t_max): every step of the formula at
+ * the top of this file, in the pages' order --
+ *   router logits and top-k with softmax gates: "Neural Server" technical
+ *     page, "How one token and one prompt are processed" (4 ids and 4
+ *     weights per token); "NInfer" Qwen3.8-Flash-Next notes, MoE execution
+ *     (weights renormalised per token);
+ *   grouping of the (token, expert) pairs by expert: "NInfer" notes, MoE
+ *     execution; "Neural Server", "Prompt processing" (tokens grouped by
+ *     expert on the GPU);
+ *   gate/up, SiLU(gate) * up, down per pair: "NInfer" notes, MoE execution
+ *     (fused gate/up kernel, then down); "Neural Server", "Prompt processing"
+ *     (SwiGLU epilogue);
+ *   the shared expert: "Running Qwen3.8-Flash-Next on a 32 GB Mac with
+ *     Transformers", architecture;
+ *   the gate-weighted combine in a fixed order: "NInfer" notes, MoE execution
+ *     (outputs summed independently of the order experts finish in).
+ * x: bf16 [T][d] row-major in device memory; out: [T][d] row-major in device
+ * memory, bf16 or fp32 as the config says; both 16-byte aligned and owned by
+ * the caller. stream: a cudaStream_t (NULL = the legacy default stream).
  * Asynchronous and stream-ordered: only enqueues kernels, performs no host
  * synchronisation and no allocation, so it may be captured in a CUDA graph.
+ * Errors (returned at once, nothing enqueued): MOE_ERR_INVALID_ARG,
+ * MOE_ERR_T_TOO_LARGE, MOE_ERR_NOT_LOADED, MOE_ERR_CUDA (launch failed).
  * Device-side failures are reported by moe_get_status after synchronising. */
 int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream);
 
-/* moe_forward with HOST buffers: enqueues the copy of x (host, bf16 [T][d])
- * into the context, the layer, and the copy of the result back to out (host)
- * on `stream`. With synchronize != 0 it waits for the stream before returning;
+/* moe_forward (same passages) with HOST buffers: enqueues the copy of x
+ * (host, bf16 [T][d]) into the context, the layer, and the copy of the result
+ * back to out (host) on `stream`. With synchronize != 0 it waits for the stream before returning;
  * with 0 the caller synchronises before reading out or reusing x. Pinned host
  * memory is needed for the copies to be asynchronous; pageable works too.
  * Each context has one staging buffer: do not overlap two calls on a context. */
 int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream, int synchronize);
 
-/* Debug export of the last forward's routing (device or host pointers, any
- * may be NULL): ids int32 [T][k], gates fp32 [T][k], counts int32 [E],
- * offsets int32 [E+1], perm int32 [T*k] (pair p = t*k + j, stably sorted by
- * expert). Stream-ordered after the forward on the same stream; the caller
- * synchronises before reading host copies. */
+/* Debug export of the last forward's routing and bucketing ("Neural Server"
+ * technical page, "How one token and one prompt are processed": expert ids
+ * and weights per token; "NInfer" notes, MoE execution: pairs grouped by
+ * expert). Device or host pointers owned by the caller, any may be NULL:
+ * ids int32 [T][k], gates fp32 [T][k], counts int32 [E], offsets int32 [E+1]
+ * (exclusive prefix sum of counts), perm int32 [T*k] (pair p = t*k + j,
+ * stably sorted by expert), inv int32 [T*k] (inv[perm[q]] = q: the row of
+ * pair p in expert order). Stream-ordered after the forward on the same
+ * stream; the caller synchronises before reading host copies. Errors:
+ * MOE_ERR_INVALID_ARG (ctx NULL), MOE_ERR_CUDA (a copy failed). */
 int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
-                    void* stream);
+                    int32_t* inv, void* stream);
 
-/* Debug export of the last forward's router logits as an unevaluated sum of
- * two fp32 numbers, logit = hi + lo: hi, lo fp32 [T][E]. The single-kernel
+/* Debug export of the last forward's router logits (the router of
+ * moe_load_router) as an unevaluated sum of two fp32 numbers, logit = hi +
+ * lo: hi, lo fp32 [T][E], device or host pointers owned by the caller. The single-kernel
  * path (T <= 16) and the multi-kernel path with T <= 32 compute every logit as
  * a double-float sum (hi = fl(logit)). The multi-kernel path with T > 32
  * computes every logit in fp32 with an error bound and the double-float sum
@@ -150,8 +191,10 @@ int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, i
 int moe_get_logits(moe_ctx* ctx, float* hi, float* lo, void* stream);
 
 /* Device status word of the context (0 = fine, else a MOE_ERR_* code set by a
- * kernel, e.g. MOE_ERR_TIMEOUT). Synchronises the context's device; clears the
- * word when `clear` is nonzero. */
+ * kernel, e.g. MOE_ERR_TIMEOUT when a bounded device-side wait gave up). No
+ * page has a counterpart: it is the library's failure report. Synchronises
+ * the context's device; clears the word when `clear` is nonzero. Returns the
+ * word, or MOE_ERR_INVALID_ARG / MOE_ERR_CUDA if it cannot be read. */
 int moe_get_status(moe_ctx* ctx, int clear);
 
 /* Tracing hook. Registers n_events cudaEvent_t handles (created by the
@@ -192,17 +235,42 @@ int moe_launches_per_forward(const moe_ctx* ctx, int T);
 int moe_route_static(const void* x, int T, int d, const float* w_router, const float* bias, int n_experts, int top_k,
                      int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm, void* stream);
 
-/* Text of the last error returned by moe_route_static ("" if none). */
+/* Text of the calling thread's last error returned by moe_route_static (""
+ * if none). The string belongs to the library and stays valid until that
+ * thread's next failing moe_route_static call. */
 const char* moe_route_static_error(void);
 
-/* Bytes of packed expert weights the context holds (codes + scales). */
+/* Measured rate of the block-scaled tensor-core MMA the expert GEMMs issue
+ * (tcgen05.mma kind::mxf8f6f4: E2M1 weights x E4M3 activations with UE8M0
+ * scales, M = 128, N = 192, K = 32) on CUDA device `device`. No page has a
+ * counterpart: it measures this GPU, as the denominator of the GEMMs'
+ * tensor-pipe fraction. One CTA per SM issues mmas_per_sm MMAs back to back
+ * from shared-memory operands (no memory traffic) into tensor memory; the
+ * call times one such launch with CUDA events after a warm-up launch and
+ * returns the dense rate in *tflops (10^12 multiply-adds x 2 per second) and
+ * the launch time in *ms (may be NULL). Synchronous; allocates and frees a
+ * 4-byte status word and two events. Errors: MOE_ERR_INVALID_ARG
+ * (mmas_per_sm outside [1, 2^24] or tflops NULL), MOE_ERR_CUDA,
+ * MOE_ERR_TIMEOUT (the MMAs did not finish within 2 s); text from
+ * moe_probe_error(). */
+int moe_probe_mma_rate(int device, int mmas_per_sm, double* tflops, double* ms);
+
+/* Text of the calling thread's last error returned by moe_probe_mma_rate. */
+const char* moe_probe_error(void);
+
+/* Bytes of packed expert weights the context holds (codes + scales; the
+ * "Neural Server" technical page, "What it runs on and what it runs", counts
+ * 13,219,200 B per gpt-oss-120B expert). 0 for a NULL ctx. */
 size_t moe_weight_bytes(const moe_ctx* ctx);
 
-/* Text of the last error raised on this context ("" if none). NULL ctx gives
- * the text of the last failed moe_create. */
+/* Text of the last error raised on this context ("" if none); no page has a
+ * counterpart. NULL ctx gives the text of the last failed moe_create. The
+ * string belongs to the context and stays valid until its next failing call
+ * or moe_destroy. */
 const char* moe_last_error(const moe_ctx* ctx);
 
-/* Free everything the context owns. NULL is accepted. */
+/* Free everything the context owns (weights, router, workspace). NULL is
+ * accepted. The caller must not have work of this context in flight. */
 void moe_destroy(moe_ctx* ctx);
 
 #ifdef __cplusplus

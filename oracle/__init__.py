@@ -215,6 +215,51 @@ def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router
     return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}
 
 
+def host_threads() -> int:
+    """Host cores this process may run on (its CPU affinity)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def layer_tokens_parallel(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router: np.ndarray,
+                          bias: np.ndarray | None, codes: np.ndarray, scales: np.ndarray, tokens=None,
+                          threads: int | None = None, w_shared_gate: np.ndarray | None = None) -> dict:
+    """layer_tokens for many tokens on several host threads.
+
+    The token list is cut into contiguous chunks, one oracle_layer_tokens call
+    per chunk on a thread pool (ctypes releases the GIL for the duration of the
+    C call). Every token is still evaluated alone by the same fp64 code in the
+    same order, so the results are bit-identical to one single-threaded call;
+    only the wall time changes. Returns the layer_tokens dict plus "threads"."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    threads = host_threads() if threads is None else max(1, int(threads))
+    threads = min(threads, max(1, n))
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    _load()  # load and declare the library once, before the threads start
+    bounds = [(i * n) // threads for i in range(threads + 1)]
+
+    def run(i):
+        return layer_tokens(d, F, E, k, S, x, w_router, bias, codes, scales,
+                            tokens=tokens[bounds[i]:bounds[i + 1]], w_shared_gate=w_shared_gate)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(run, range(threads)))
+    out = {key: np.concatenate([pt[key] for pt in parts]) for key in ("y", "ids", "gates")}
+    out["tokens"] = tokens
+    out["h"] = None
+    out["threads"] = threads
+    return out
+
+
 def layer_tokens_shard(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router: np.ndarray,
                        bias: np.ndarray | None, codes: np.ndarray, scales: np.ndarray, e_begin: int, e_end: int,
                        with_shared: bool, tokens=None, w_shared_gate: np.ndarray | None = None) -> np.ndarray:

@@ -37,8 +37,8 @@ MOE_FLAG_NO_TC = 8
 
 EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
-            "moe_launches_per_forward", "moe_route_static", "moe_route_static_error", "moe_weight_bytes",
-            "moe_last_error", "moe_destroy"]
+            "moe_launches_per_forward", "moe_route_static", "moe_route_static_error", "moe_probe_mma_rate",
+            "moe_probe_error", "moe_weight_bytes", "moe_last_error", "moe_destroy"]
 
 
 class MoeError(RuntimeError):
@@ -77,13 +77,17 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_profile_events.argtypes = [vp, P(vp), i32]
             lib.moe_forward_phases.argtypes = [vp, i32, P(ctypes.c_char_p)]
             lib.moe_launches_per_forward.argtypes = [vp, i32]
-            lib.moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            lib.moe_get_routing.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
             lib.moe_get_logits.argtypes = [vp, vp, vp, vp]
             lib.moe_get_status.argtypes = [vp, i32]
             lib.moe_route_static.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.moe_route_static.restype = i32
             lib.moe_route_static_error.argtypes = []
             lib.moe_route_static_error.restype = ctypes.c_char_p
+            lib.moe_probe_mma_rate.argtypes = [i32, i32, P(ctypes.c_double), P(ctypes.c_double)]
+            lib.moe_probe_mma_rate.restype = i32
+            lib.moe_probe_error.argtypes = []
+            lib.moe_probe_error.restype = ctypes.c_char_p
             lib.moe_weight_bytes.argtypes = [vp]
             lib.moe_weight_bytes.restype = ctypes.c_size_t
             lib.moe_last_error.argtypes = [vp]
@@ -151,9 +155,10 @@ def moe_forward_host(ctx: int, x_host, T: int, out_host, stream=None, synchroniz
                                                 1 if synchronize else 0), "moe_forward_host")
 
 
-def moe_get_routing(ctx: int, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
+def moe_get_routing(ctx: int, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None,
+                    inv=None) -> None:
     _check(ctx, load_library().moe_get_routing(ctx, ptr(ids), ptr(gates), ptr(counts), ptr(offsets), ptr(perm),
-                                               stream_handle(stream)), "moe_get_routing")
+                                               ptr(inv), stream_handle(stream)), "moe_get_routing")
 
 
 def moe_get_logits(ctx: int, hi=None, lo=None, stream=None) -> None:
@@ -193,6 +198,16 @@ def moe_route_static(x, T: int, d: int, w_router, bias, n_experts: int, top_k: i
                               ptr(counts), ptr(offsets), ptr(perm), stream_handle(stream))
     if rc < 0:
         raise MoeError(rc, "moe_route_static: " + lib.moe_route_static_error().decode(errors="replace"))
+
+
+def moe_probe_mma_rate(device: int = 0, mmas_per_sm: int = 200000) -> tuple[float, float]:
+    """(TFLOP/s, ms) of the block-scaled MMA kind the expert GEMMs use, measured on `device`."""
+    lib = load_library()
+    tf, ms = ctypes.c_double(), ctypes.c_double()
+    rc = lib.moe_probe_mma_rate(device, mmas_per_sm, ctypes.byref(tf), ctypes.byref(ms))
+    if rc < 0:
+        raise MoeError(rc, lib.moe_probe_error().decode(errors="replace"))
+    return tf.value, ms.value
 
 
 def moe_weight_bytes(ctx: int) -> int:
@@ -245,8 +260,8 @@ class MoeLayer:
     def forward_host(self, x_host, T: int, out_host, stream=None, synchronize: bool = True) -> None:
         moe_forward_host(self.ctx, x_host, T, out_host, stream, synchronize)
 
-    def routing(self, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None) -> None:
-        moe_get_routing(self.ctx, ids, gates, counts, offsets, perm, stream)
+    def routing(self, ids=None, gates=None, counts=None, offsets=None, perm=None, stream=None, inv=None) -> None:
+        moe_get_routing(self.ctx, ids, gates, counts, offsets, perm, stream, inv)
 
     def logits(self, hi=None, lo=None, stream=None) -> None:
         moe_get_logits(self.ctx, hi, lo, stream)

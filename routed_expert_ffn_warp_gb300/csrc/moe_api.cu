@@ -41,7 +41,7 @@ struct moe_ctx {
   void* out_dev = nullptr;  // host-API staging of out
   int* load_err = nullptr;  // repack NaN-scale flag
   int last_T = 0;
-  cudaEvent_t prof[moe::kForwardPhases + 1] = {};
+  cudaEvent_t prof[moe::kForwardPhasesTc + 1] = {};
   int n_prof = 0;
   int max_smem = 0;
   bool decode_ok = false;  // the fused single-kernel path fits this config
@@ -256,7 +256,16 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   dp.wait_ns = 50000000LL;  // 50 ms: orders of magnitude above a layer's runtime
   dp.test_extra = (c.flags & MOE_FLAG_TEST_FORCE_TIMEOUT) ? 1 : 0;
   dp.test_wait_ns = 2000000LL;  // 2 ms
-  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms);
+  // kernel attributes are per device: set them with this context's device current
+  if ((e = moe::configure_decode(ctx->max_smem)) != cudaSuccess || (e = moe::configure_tcgemm(ctx->max_smem)) != cudaSuccess ||
+      (e = moe::configure_gemm()) != cudaSuccess) {
+    moe_destroy(ctx);
+    return fail(nullptr, MOE_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  }
+  // The fused kernel's CTAs wait on each other (bounded): it is used only when
+  // one CTA per SM fits, so that a grid of one CTA per SM can be resident at once.
+  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms) &&
+                   moe::decode_blocks_per_sm(dp) >= 1;
   *out = ctx;
   return MOE_OK;
 }
@@ -364,7 +373,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
     e = moe::launch_decode(dp, s, ctx->num_sms, ctx->max_smem);
     if (prof && e == cudaSuccess) cudaEventRecord(ctx->prof[1], s);
   } else {
-    e = moe::launch_forward(p, s, ctx->num_sms, ctx->n_prof == moe::kForwardPhases + 1 ? ctx->prof : nullptr);
+    e = moe::launch_forward(p, s, ctx->num_sms, ctx->n_prof == moe::forward_phases(p) + 1 ? ctx->prof : nullptr);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "forward launch");
   return MOE_OK;
@@ -390,7 +399,7 @@ int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, vo
 }
 
 int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets, int32_t* perm,
-                    void* stream) {
+                    int32_t* inv, void* stream) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   DeviceGuard guard(ctx->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -403,6 +412,7 @@ int moe_get_routing(moe_ctx* ctx, int32_t* ids, float* gates, int32_t* counts, i
   if (offsets && e == cudaSuccess)
     e = cudaMemcpyAsync(offsets, p.offsets, (size_t)(ctx->cfg.n_experts + 1) * 4, cudaMemcpyDefault, s);
   if (perm && P && e == cudaSuccess) e = cudaMemcpyAsync(perm, p.perm, P * 4, cudaMemcpyDefault, s);
+  if (inv && P && e == cudaSuccess) e = cudaMemcpyAsync(inv, p.inv, P * 4, cudaMemcpyDefault, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "routing copy");
   return MOE_OK;
 }
@@ -437,7 +447,7 @@ int moe_profile_events(moe_ctx* ctx, void* const* events, int n_events) {
     ctx->n_prof = 0;
     return MOE_OK;
   }
-  if (n_events != 2 && n_events != moe::kForwardPhases + 1)
+  if (n_events != 2 && n_events != moe::forward_phases(ctx->base) + 1)
     return fail(ctx, MOE_ERR_INVALID_ARG, "n_events must be moe_forward_phases(T) + 1");
   for (int i = 0; i < n_events; ++i) {
     if (!events[i]) return fail(ctx, MOE_ERR_INVALID_ARG, "NULL event");
@@ -453,8 +463,8 @@ int moe_forward_phases(const moe_ctx* ctx, int T, const char** names) {
     if (names) *names = "layer";
     return 1;
   }
-  if (names) *names = moe::kForwardPhaseNames;
-  return moe::kForwardPhases;
+  if (names) *names = ctx->base.tc_gateup ? moe::kForwardPhaseNamesTc : moe::kForwardPhaseNames;
+  return moe::forward_phases(ctx->base);
 }
 
 int moe_launches_per_forward(const moe_ctx* ctx, int T) {

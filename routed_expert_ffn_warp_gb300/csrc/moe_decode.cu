@@ -38,7 +38,10 @@
 // Every device-side wait is bounded (%globaltimer); on expiry the CTA records
 // MOE_ERR_TIMEOUT in the status word, stops waiting, and runs to completion,
 // so no wait can hang the GPU. All CTAs must be co-resident: the grid is one
-// CTA per SM and every CTA needs more than half of an SM's shared memory.
+// CTA per SM and every CTA needs more than half of an SM's shared memory;
+// contexts use this kernel only when the occupancy API says one CTA fits on
+// an SM. A GPU shared with another context that holds SMs can still keep a
+// CTA waiting: its waits then give up and the status word reports it.
 #include <stdint.h>
 
 #include <algorithm>
@@ -447,7 +450,10 @@ __device__ void bucket_small(const DecParams& p, const Shared& s) {
   if (lane < P) {
     s.perm[lane] = q;
     s.inv[q] = lane;
-    if (blockIdx.x == 0) f.perm[lane] = q;
+    if (blockIdx.x == 0) {
+      f.perm[lane] = q;
+      f.inv[q] = lane;
+    }
   }
   if (first) {
     const int slot = __popc(firsts & ((1u << lane) - 1u));
@@ -561,7 +567,10 @@ __device__ void bucket_large(const DecParams& p, const Shared& s) {
       const int pos = before + rank;
       s.perm[pos] = q;
       s.inv[q] = pos;
-      if (writer) f.perm[pos] = q;
+      if (writer) {
+        f.perm[pos] = q;
+        f.inv[q] = pos;
+      }
     }
   }
 }
@@ -1280,18 +1289,26 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   return false;
 }
 
-cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem) {
-  static int configured = 0;
-  if (configured < max_smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+cudaError_t configure_decode(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_layer_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  return e;
+}
 
-    if (e != cudaSuccess) return e;
-    configured = max_smem;
-  }
+int decode_blocks_per_sm(const DecParams& p) {
+  int n = 0;
+  cudaError_t e;
+  if (p.ring_groups == 8) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<8>, kThreads, p.smem_bytes);
+  else if (p.ring_groups == 6) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<6>, kThreads, p.smem_bytes);
+  else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<4>, kThreads, p.smem_bytes);
+  return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem) {
+  (void)max_smem;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(kThreads);
@@ -1299,8 +1316,9 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
   cfg.stream = stream;
   // Programmatic dependent launch: the kernel may be scheduled while the
   // preceding kernel drains; it waits (griddepcontrol.wait) before touching
-  // any global memory written by it. Co-residency of the grid holds by
-  // construction (one CTA per SM, more than half an SM's shared memory each).
+  // any global memory written by it. The grid is one CTA per SM, each with
+  // more than half an SM's shared memory; moe_create checks with the occupancy
+  // API that one CTA fits on an SM, so all CTAs of the grid can be resident.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -514,24 +514,19 @@ constexpr size_t kDnSmem =
 
 }  // namespace
 
+cudaError_t configure_gemm() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGuSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDnSmem);
+  return e;
+}
+
 cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGuSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   gemm_gateup_kernel<<<num_sms, kGThreads, kGuSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_down(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDnSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
   gemm_down_kernel<<<num_sms, kGThreads, kDnSmem, stream>>>(p);
   return cudaGetLastError();
 }

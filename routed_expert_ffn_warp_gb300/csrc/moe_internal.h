@@ -185,6 +185,16 @@ struct DecParams {
 };
 bool decode_plan(DecParams& p, int max_smem, int num_sms);
 cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem);
+// CTAs of the fused kernel (with the shared memory of plan p) that fit on one
+// SM of the current device; the fused path needs at least one.
+int decode_blocks_per_sm(const DecParams& p);
+
+// Per-device kernel attributes (the dynamic shared-memory limits of the large
+// kernels). cudaFuncSetAttribute applies to the current device only, so
+// moe_create calls these with its device current, for every context.
+cudaError_t configure_decode(int max_smem);
+cudaError_t configure_tcgemm(int max_smem);
+cudaError_t configure_gemm();
 
 // Expert GEMMs of the general path (moe_gemm.cu). Work units: (slot, group of
 // kGemmTiles 16-row weight tiles, block of up to kGemmRows rows of the slot);
@@ -197,13 +207,20 @@ cudaError_t launch_gemm_down(const FwdParams& p, cudaStream_t stream, int num_sm
 // holds their running counts per slot.
 constexpr int kTcGemmRows = 48;
 cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms);
+// The activation panels of the tcgen05 gate/up GEMM: x as two MXFP8 planes,
+// then one panel per (slot, token block) and K step.
+cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
 
 // Launchers (moe_kernels.cu). All are asynchronous on `stream`.
-// `events` (may be null) receives kForwardPhases + 1 cudaEvent_t to record at
-// the phase boundaries.
+// `events` (may be null) receives forward_phases(p) + 1 cudaEvent_t to record
+// at the phase boundaries. The register-decode path has 4 phases; the tcgen05
+// path 5, so that its two GEMMs are phases of one kernel each.
 constexpr int kForwardPhases = 4;
-extern const char* const kForwardPhaseNames;  // "route,gateup,down,combine"
+constexpr int kForwardPhasesTc = 5;
+extern const char* const kForwardPhaseNames;    // "route,gateup,down,combine"
+extern const char* const kForwardPhaseNamesTc;  // "route,panels,gateup,down,combine"
+inline int forward_phases(const FwdParams& p) { return p.tc_gateup ? kForwardPhasesTc : kForwardPhases; }
 constexpr int kLaunchesPerForward = 7;
 constexpr int kLaunchesPerForwardTc = 8;  // no f16 x; + x planes, x panels (tcgen05 GEMMs)
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);

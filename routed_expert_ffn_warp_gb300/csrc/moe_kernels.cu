@@ -759,22 +759,32 @@ void launch_router(FwdParams p, cudaStream_t stream) {
 }
 
 const char* const kForwardPhaseNames = "route,gateup,down,combine";
+const char* const kForwardPhaseNamesTc = "route,panels,gateup,down,combine";
 
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events) {
   if (p.T == 0) return cudaSuccess;
-  if (events) cudaEventRecord(events[0], stream);
+  int ev = 0;
+  auto mark = [&]() {
+    if (events) cudaEventRecord(events[ev++], stream);
+  };
+  mark();
   if (!p.tc_gateup) launch_chained(prep_x_kernel, dim3(p.T), dim3(256), 0, stream, p);  // f16 x of the register-decode GEMMs
   launch_router(p, stream);
   launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), 0, stream, p);
-  if (events) cudaEventRecord(events[1], stream);
-  cudaError_t e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
+  mark();
+  cudaError_t e = cudaSuccess;
+  if (p.tc_gateup) {
+    if ((e = launch_panels_tc(p, stream)) != cudaSuccess) return e;
+    mark();
+  }
+  e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
   if (e != cudaSuccess) return e;
-  if (events) cudaEventRecord(events[2], stream);
+  mark();
   e = p.tc_gateup ? launch_gemm_down_tc(p, stream, num_sms) : launch_gemm_down(p, stream, num_sms);
   if (e != cudaSuccess) return e;
-  if (events) cudaEventRecord(events[3], stream);
+  mark();
   launch_chained(combine_kernel, dim3((p.d + 255) / 256, p.T), dim3(256), 0, stream, p);
-  if (events) cudaEventRecord(events[4], stream);
+  mark();
   return cudaGetLastError();
 }
 

@@ -31,13 +31,15 @@ static_assert(kOffXsq + moe::kRouterSplits * kMaxLogits * 4 <= kScratchBytes, "s
 
 __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
-std::mutex g_mu;
+std::mutex g_mu;                   // guards g_scratch
 void* g_scratch[kMaxDevices] = {};  // device address of g_route_scratch, per device
-std::string g_err;
+// Error text of the calling thread's last failed call: one string per thread,
+// so the pointer moe_route_static_error hands out is never rewritten by
+// another thread's failure.
+thread_local std::string t_err;
 
 int fail(int code, const std::string& msg) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  g_err = msg;
+  t_err = msg;
   return code;
 }
 
@@ -45,7 +47,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-extern "C" const char* moe_route_static_error(void) { return g_err.c_str(); }
+extern "C" const char* moe_route_static_error(void) { return t_err.c_str(); }
 
 extern "C" int moe_route_static(const void* x, int T, int d, const float* w_router, const float* bias, int n_experts,
                                 int top_k, int32_t* ids, float* gates, int32_t* counts, int32_t* offsets,
@@ -73,8 +75,7 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
       e = cudaGetSymbolAddress(&g_scratch[dev], g_route_scratch);
       if (e != cudaSuccess) {
         g_scratch[dev] = nullptr;
-        g_err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
-        return MOE_ERR_CUDA;
+        return fail(MOE_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
       }
     }
     base = g_scratch[dev];

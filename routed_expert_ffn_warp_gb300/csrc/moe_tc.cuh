@@ -11,9 +11,10 @@
 //    bytes apart;
 //  * scale factors (one E8M0 byte per row and 32-element K block) live in
 //    TMEM: for rows 32 r + l, byte b of column base + r in lane l holds the
-//    scale of K block b, replicated in all four lane quadrants (tcgen05.cp
-//    32x128b.warpx4 of 512-byte blocks [lane][4 words]); the MMA picks the
-//    byte with the scale-factor ids of its instruction descriptor.
+//    scale of K block b, replicated in all four lane quadrants (four warps,
+//    one per quadrant, each storing 512-byte blocks [lane][4 words] with
+//    tcgen05.st); the MMA picks the byte with the scale-factor ids of its
+//    instruction descriptor.
 #pragma once
 #include <stdint.h>
 
@@ -57,13 +58,6 @@ __device__ __forceinline__ void mma_mxf4_mxf8(uint32_t d_tmem, uint64_t adesc, u
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
-}
-// Copy 32 rows x 16 bytes of shared memory (described like an MMA operand:
-// 8-row groups SBO bytes apart) to TMEM lanes 0..31 of 4 consecutive columns
-// at taddr, replicated into all four lane quadrants. Runs in issue order with
-// the MMAs this thread issues after it.
-__device__ __forceinline__ void cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // TMA tiled load of the box at (x, y) of a 2-D tensor map (a kernel parameter
 // declared __grid_constant__) into this CTA's shared memory; completion is

@@ -94,29 +94,45 @@ constexpr size_t tc_smem_fixed() {
   return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (3 * Mode<kDown>::kS + 4) + 16;
 }
 
-__device__ __forceinline__ void bounded_wait(uint64_t* bar, uint32_t parity, int* status) {
-  if (mbar_try_wait(bar, parity)) return;
+// Bounded mbarrier waits. Every role passes every phase of the barriers it
+// waits on in order, so a parity wait never meets a phase two steps old. On
+// expiry the wait records MOE_ERR_TIMEOUT, raises the CTA's abort flag and
+// returns false; once the flag is up every wait returns false at once and
+// every role stops issuing copies and MMAs (the kernel then drains what is in
+// flight before it frees tensor memory, see the end of gemm_tc_kernel).
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
     if ((long long)(globaltimer() - t0) > kWaitNs) {
+      *abort = 1;
       atomicCAS(status, 0, MOE_ERR_TIMEOUT);
-      return;
+      return false;
     }
   }
+  return true;
 }
 // The same wait for the roles off the MMA lanes' critical path (producers,
 // epilogue): each try may suspend the thread for up to 20 us until the phase
 // completes, so that waiting warps leave their issue slots to the MMA lanes.
-__device__ __forceinline__ void bounded_wait_sleep(uint64_t* bar, uint32_t parity, int* status) {
-  if (mbar_try_wait(bar, parity)) return;
+__device__ __forceinline__ bool bounded_wait_sleep(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait_hint(bar, parity, 20000u)) {
+    if (*abort) return false;
     if ((long long)(globaltimer() - t0) > kWaitNs) {
+      *abort = 1;
       atomicCAS(status, 0, MOE_ERR_TIMEOUT);
-      return;
+      return false;
     }
   }
+  return true;
 }
+// After an abort: long enough for every copy and MMA already issued to land
+// (each takes microseconds), so that no copy writes into shared memory and no
+// MMA touches tensor memory after this CTA has freed them.
+constexpr long long kDrainNs = 1000000LL;
 
 __device__ __forceinline__ int find_unit_slot(const int32_t* prefix, int n, int unit) {
   int lo = 0, hi = n - 1;
@@ -259,7 +275,8 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   uint64_t* ready = empty + kS;           // the stage's scale factors are in TMEM set s (4 warps x 32)
   uint64_t* accfull = ready + kS;         // [kBufs] every MMA lane's part of the buffer's unit completed
   uint64_t* accempty = accfull + 2;       // [kBufs]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);  // [0] TMEM address, [1] abort flag
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
   int* tab = reinterpret_cast<int*>(tslot + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ns = *p.n_slots;
@@ -290,6 +307,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         make_uint2(0u, 0u);
   tc::fence_proxy_async();
   if (tid == 0) {
+    *abort = 0;
     for (int s = 0; s < kS; ++s) {
       mbar_init(&full[s], 2);
       mbar_init(&empty[s], kMma);
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       for (int q = 0; q < M::kPf && cp.i < n_units; ++q) prefetch();
       for (int j = 0; ca.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        if (j >= kS && !bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
         uint8_t* sb = stg + (size_t)s * M::kStage;
         // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
         mbar_arrive_expect_tx(&full[s], (uint32_t)kTcPairBytes);
@@ -342,7 +360,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       const int pstride = kDown ? tc_ksteps(p.F > p.S ? p.F : p.S) : tc_ksteps(p.d);
       for (int j = 0; cb.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS) bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status);
+        if (j >= kS && !bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
         const int N = M::kPlanes * npad_of(cb.g.n);
         uint8_t* sb = stg + (size_t)s * M::kStage + M::kAPair;
         const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
@@ -356,17 +374,21 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     if (lane == 0) {
       const int t = warp - kMmaWarp0;  // M tile t of every unit
       int j0 = 0;                      // first K step of unit i
-      for (int i = 0; i < n_units; ++i) {
+      bool ok = true;
+      for (int i = 0; i < n_units && ok; ++i) {
         const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
         const int N = M::kPlanes * npad_of(g.n), acc = i % kBufs;
         const bool mine = t < g.nt;  // a pair of one tile leaves lane 1 without MMAs
-        if (i >= kBufs) bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status);
+        if (i >= kBufs && !bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status, abort)) break;
         tc::fence_after();
         const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
         for (int ks = 0; ks < g.nks; ++ks) {
           const int jj = j0 + ks, s = jj % kS;
           // every lane takes part in every step's hand-off, with or without MMAs
-          bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status);  // operands landed, scales in TMEM
+          if (!bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status, abort)) {  // operands landed, scales in TMEM
+            ok = false;
+            break;
+          }
           tc::fence_after();
           if (mine) {
             const uint8_t* ab = stg + (size_t)s * M::kStage + (size_t)t * kAOp;
@@ -382,6 +404,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
           }
           tc::commit(&empty[s]);
         }
+        if (!ok) break;
         tc::commit(&accfull[acc]);
         j0 += g.nks;
       }
@@ -392,11 +415,14 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     // tile 0 / 1 to columns +0 / +8, SFB to +16 (+4 per 512-byte block)
     const uint32_t qbase = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol;
     int j = 0;
-    for (int i = 0; i < n_units; ++i) {
+    bool ok = true;
+    for (int i = 0; i < n_units && ok; ++i) {
       const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
       for (int ks = 0; ks < g.nks; ++ks, ++j) {
         const int s = j % kS;
-        bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status);
+        // the warp's lanes leave together (one lane's verdict), so tcgen05.st stays warp-uniform
+        ok = __shfl_sync(0xffffffffu, bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status, abort) ? 1 : 0, 0) != 0;
+        if (!ok) break;
         const uint8_t* sb = stg + (size_t)s * M::kStage;
         const uint8_t* sbf = sb + M::kAPair + M::kPlanes * npad_of(g.n) * kTcStepK;  // SFB behind the N rows
         const uint4 wa0 = *reinterpret_cast<const uint4*>(sb + 2 * kAOp + 16 * lane);
@@ -429,7 +455,10 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
     for (int i = 0; i < n_units; ++i) {
       const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
       const int npad = npad_of(g.n), acc = i % kBufs;
-      bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status);
+      // every epilogue thread leaves on the same verdict: the named barriers below need all 256
+      const bool ok = bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status, abort);
+      named_bar(1, kEpiThreads);
+      if (*abort || !ok) break;
       tc::fence_after();
       if (kDown) {  // part rows q0 + m, column 128 (mt + t) + 32 qd + lane: the sum of the 4 planes
         for (int t = 0; t < g.nt; ++t) {
@@ -514,6 +543,10 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   tc::fence_before();
   __syncthreads();
   if (warp == 0) {
+    if (*abort) {  // the roles stopped early: let every copy and MMA already issued finish
+      const uint64_t t0 = globaltimer();
+      while ((long long)(globaltimer() - t0) < kDrainNs) __nanosleep(10000);
+    }
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }
@@ -646,30 +679,28 @@ cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static size_t configured = 0;
-  const size_t smem = tc_gemm_smem_bytes(p.E, false);
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+cudaError_t configure_tcgemm(int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  return e;
+}
+
+cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream) {
   launch_chained(prep_xq_kernel, dim3((p.T * p.xq_spitch + 7) / 8), dim3(256), 0, stream, p);
   // panels: at most ceil(Q / 48) + slots blocks (the kernels skip the ones past the count)
   const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
-  launch_chained(pack_panels_kernel, dim3(max_panels, tc_ksteps(p.d)), dim3(256), 0, stream, p);
+  return launch_chained(pack_panels_kernel, dim3(max_panels, tc_ksteps(p.d)), dim3(256), 0, stream, p);
+}
+
+cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
+  const size_t smem = tc_gemm_smem_bytes(p.E, false);
   return launch_chained(gemm_tc_kernel<false>, dim3(num_sms), dim3(kThr), smem, stream, p,
                         *static_cast<const CUtensorMap*>(p.tmap_gu));
 }
 
 cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  static size_t configured = 0;
   const size_t smem = tc_gemm_smem_bytes(p.E, true);
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
   return launch_chained(gemm_tc_kernel<true>, dim3(num_sms), dim3(kThr), smem, stream, p,
                         *static_cast<const CUtensorMap*>(p.tmap_dn));
 }

@@ -53,15 +53,16 @@ def run_gpu(m, layer, x_bits: np.ndarray, out_f32: bool = False) -> dict:
     counts = torch.empty((E,), dtype=torch.int32, device="cuda")
     offsets = torch.empty((E + 1,), dtype=torch.int32, device="cuda")
     perm = torch.empty((T * k,), dtype=torch.int32, device="cuda")
+    inv = torch.empty((T * k,), dtype=torch.int32, device="cuda")
     lhi = torch.empty((T, E), dtype=torch.float32, device="cuda")
     llo = torch.empty((T, E), dtype=torch.float32, device="cuda")
-    layer.routing(ids, gates, counts, offsets, perm, stream)
+    layer.routing(ids, gates, counts, offsets, perm, stream, inv=inv)
     layer.logits(lhi, llo, stream)
     torch.cuda.synchronize()
     st = layer.status()
     y = out.float().cpu().numpy().astype(np.float64)
     return {"y": y, "ids": ids.cpu().numpy(), "gates": gates.cpu().numpy(), "counts": counts.cpu().numpy(),
-            "offsets": offsets.cpu().numpy(), "perm": perm.cpu().numpy(),
+            "offsets": offsets.cpu().numpy(), "perm": perm.cpu().numpy(), "inv": inv.cpu().numpy(),
             "logits": lhi.cpu().numpy().astype(np.float64) + llo.cpu().numpy().astype(np.float64),
             "status": st}
 
@@ -71,6 +72,7 @@ def check_routing(gpu: dict, ref_route: dict, E: int):
     assert np.array_equal(gpu["counts"], ref_route["counts"])
     assert np.array_equal(gpu["offsets"], ref_route["offsets"])
     assert np.array_equal(gpu["perm"], ref_route["perm"])
+    assert np.array_equal(gpu["inv"], ref_route["inv"])
     assert np.max(np.abs(gpu["gates"] - ref_route["gates"])) <= GATE_TOL
 
 

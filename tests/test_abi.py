@@ -58,3 +58,9 @@ def test_null_context_calls(lib):
     assert lib.moe_get_status(None, 0) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_weight_bytes(None) == 0
     lib.moe_destroy(None)
+
+
+def test_mma_probe_rejects_bad_arguments_without_a_gpu(lib):
+    tf = ctypes.c_double()
+    assert lib.moe_probe_mma_rate(0, 0, ctypes.byref(tf), None) == -1  # MOE_ERR_INVALID_ARG
+    assert b"mmas_per_sm" in lib.moe_probe_error()

@@ -3,7 +3,7 @@
 Routing (ids, counts, offsets, perm) must match bit for bit; gates within
 1e-6; outputs within 2e-2 * ||ref||_inf for bf16 and 1e-4 * ||ref||_inf for
 fp32 outputs. Sizes span several tiles and ragged tails; the full-size
-workloads are checked on sampled tokens (routing on all tokens).
+workloads are checked on every token (the oracle runs on all host cores).
 """
 import numpy as np
 import pytest
@@ -191,6 +191,34 @@ def test_near_ties_need_double_float(m, T, flags):
     assert len({tuple(r) for r in g["ids"]}) == 2  # both orders occur (the sign of x[t, 5] decides)
 
 
+@pytest.mark.parametrize("T", [2, 8])
+def test_near_ties_on_the_fused_kernel(m, T):
+    """The same one-ulp construction on calls the fused single-kernel path takes
+    (T * k <= 16 pairs, a context without the tcgen05 copy): its router sums every
+    logit in double-float inside the kernel, and the order of experts 3 and 7 is
+    decided by a logit difference about 1e-7 of one fp32 ulp of the logits. Token
+    0 has x[0, 5] = +1 and token 1 has x[1, 5] = -1, so both orders occur."""
+    wl = synth.WORKLOADS["tiny"].with_(T=T, E=16, k=2)
+    L = synth.gen_layer(wl, 6)
+    w = L["w_router"].copy()
+    w[7] = w[3]
+    w[7, 5] = np.nextafter(w[3, 5], np.float32(np.inf))
+    b = np.zeros(wl.E, dtype=np.float32)
+    b[3] = b[7] = 50.0
+    x = L["x"].copy()
+    x[0, 5] = 0x3F80  # bf16 +1.0: expert 7's logit is the larger one
+    x[1, 5] = 0xBF80  # bf16 -1.0: expert 3's
+    L = dict(L, w_router=w, bias=b, x=x)
+    layer = make_layer(m, wl, L, t_max=T)
+    assert m.moe_launches_per_forward(layer.ctx, T) == 1, "this case must run on the fused kernel"
+    layer.close()
+    g, ref, _ = _parity(m, wl, L, t_max=T)
+    assert list(g["ids"][0]) == [7, 3] and list(g["ids"][1]) == [3, 7]
+    # the pair is far below fp32 resolution: one fp32 ulp of the logits is ~4e-6
+    lr = oracle.route(x, w, b, wl.k)["logits"]
+    assert 0 < abs(lr[0, 7] - lr[0, 3]) < 1e-6
+
+
 def test_skewed_all_tokens_one_expert(m):
     wl = synth.WORKLOADS["tiny"].with_(T=16, E=16, k=2)
     L = synth.gen_layer(wl, 4)
@@ -243,19 +271,45 @@ def test_forward_host_matches_device(m):
     layer.close()
 
 
-# ---------------------------------------------------------------- full-size workloads (sampled outputs)
+# ---------------------------------------------------------------- full-size workloads (every token)
 
-@pytest.mark.parametrize("name,layer_idx,tokens", [
-    ("decode", 0, None),
-    ("decode", 35, None),
-    ("verify", 0, [0, 9, 15]),
-    ("small", 0, [0, 5, 7]),
-    ("prefill", 0, [0, 511, 1023]),
+_FULL_REF = {}
+
+
+def _full_ref(name: str, layer_idx: int):
+    """Inputs and the oracle's output for every token of one full-size layer (fp64 on all host
+    cores: the thread-parallel driver evaluates each token with the single-threaded code)."""
+    key = (name, layer_idx)
+    if key not in _FULL_REF:
+        wl = synth.WORKLOADS[name]
+        L = synth.gen_layer(wl, layer_idx)
+        ref = oracle.layer_tokens_parallel(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, L["x"], L["w_router"],
+                                           L["bias"], L["codes"], L["scales"])
+        _FULL_REF.clear()  # one full-size layer's inputs at a time
+        _FULL_REF[key] = (wl, L, ref)
+    return _FULL_REF[key]
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("name,layer_idx", [
+    ("decode", 0),
+    ("decode", 35),
+    ("verify", 0),
+    ("small", 0),
+    ("prefill", 0),
 ])
-def test_full_size_workloads(m, name, layer_idx, tokens):
-    wl = synth.WORKLOADS[name]
-    L = synth.gen_layer(wl, layer_idx)
-    _parity(m, wl, L, tokens=tokens)
+def test_full_size_workloads(m, name, layer_idx, out_f32):
+    """Every token of a full-size layer, in the launch configuration the benchmark times (one
+    context with t_max = T; verify and small take the tcgen05 multi-kernel path, decode the fused
+    kernel): routing bit-exact over all tokens, y within the bf16 / fp32 tolerance."""
+    wl, L, ref = _full_ref(name, layer_idx)
+    layer = make_layer(m, wl, L, out_f32=out_f32)
+    g = run_gpu(m, layer, L["x"], out_f32=out_f32)
+    assert g["status"] == 0
+    check_routing(g, oracle_route(wl, L), wl.E)
+    assert np.array_equal(g["ids"], ref["ids"])
+    check_output(g["y"], ref["y"], F32_TOL if out_f32 else BF16_TOL)
+    layer.close()
 
 
 def test_register_decode_gemms_prefill_sampled(m):

@@ -5,8 +5,9 @@ or a code region where allocation is forbidden). moe_route_static runs the
 router, top-k and counting sort with a static device scratch array instead.
 This test calls it twice in a row through the C ABI and compares both results
 with the routing the regular entry point (moe_forward + moe_get_routing)
-produced for the same inputs: ids, counts, offsets and perm bit for bit, gates
-within the gate tolerance of the other tests.
+produced for the same inputs, and with the CPU oracle's routing: ids, counts,
+offsets and perm bit for bit, gates within the gate tolerance of the other
+tests.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
@@ -14,6 +15,7 @@ already run every other test.
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from moe_testlib import GATE_TOL, build_lib, make_layer
 
@@ -68,11 +70,14 @@ def _routing_static(m, wl, L):
 def test_static_routing_matches_forward_twice(m, case):
     L = synth.gen_layer(case, 0)
     ref = _routing_via_forward(m, case, L)
+    orc = oracle.route(L["x"], L["w_router"], L["bias"], case.k)
     for _ in range(2):  # two calls in a row share the static scratch
         got = _routing_static(m, case, L)
         for key in ("ids", "counts", "offsets", "perm"):
             assert np.array_equal(got[key], ref[key]), key
+            assert np.array_equal(got[key], orc[key]), key + " differs from the oracle"
         assert np.max(np.abs(got["gates"] - ref["gates"])) <= GATE_TOL
+        assert np.max(np.abs(got["gates"] - orc["gates"])) <= GATE_TOL
 
 
 def test_static_routing_rejects_sizes_beyond_its_scratch(m):
