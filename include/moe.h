@@ -67,23 +67,22 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
 
 /* moe_config.flags bits.
  * MOE_FLAG_TEST_FORCE_TIMEOUT exists for failure-detection tests only: one
- *   device-side wait of every single-kernel decode forward waits for a value
- *   no launch writes and gives up after 2 ms, so the forward completes with
- *   MOE_ERR_TIMEOUT in the status word (its output is then undefined).
+ *   device-side wait of every single-launch forward (T <= 16) waits for a
+ *   value no launch writes and gives up after 2 ms, so the forward completes
+ *   with MOE_ERR_TIMEOUT in the status word (its output is then undefined).
  * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path (for
  *   testing both paths on the same shapes).
- * Path choice per call: the fused single-kernel path serves T <= 16 unless
- *   the context holds the tcgen05 weight copy and T * top_k > 16; every other
- *   call takes the multi-kernel path. Within each class a token's output bits
- *   do not depend on the other tokens of its call.
- * The multi-kernel path runs both expert GEMMs as block-scaled tcgen05 MMAs
- *   (MXFP4 weights x MXFP8 planes of x and of h) from a second copy of the
- *   experts in the MMA's layout, made at load time, whenever t_max * top_k >
- *   16 and the shared-memory tables fit (n_experts up to 512).
- * MOE_FLAG_TC_GATEUP asks for those MMAs for every t_max (an error if the
- *   tables do not fit); MOE_FLAG_NO_TC keeps the register-decode tensor-core
- *   GEMMs instead (no second copy; T <= 16 then always takes the fused
- *   path). Results agree within the bf16 and fp32 tolerances either way. */
+ * Weights and paths. By default the context stores its experts once, in the
+ *   layout of the block-scaled tcgen05 MMAs (MXFP4 weights x MXFP8 planes of x
+ *   and of h; made at load time, lossless), whenever the shared-memory tables
+ *   fit (n_experts up to 512): forwards with T <= 16 run as one launch
+ *   (the fused tcgen05 kernel), larger T on the multi-kernel path with the
+ *   tcgen05 GEMMs. MOE_FLAG_TC_GATEUP makes that layout mandatory (an error if
+ *   the tables do not fit); MOE_FLAG_NO_TC stores the packed tile layout
+ *   instead, for the mma.sync kernels: the fused mma.sync kernel for T <= 16,
+ *   the register-decode tensor-core GEMMs above. Within each path a token's
+ *   output bits do not depend on the other tokens of its call; results agree
+ *   within the bf16 and fp32 tolerances across paths. */
 enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u, MOE_FLAG_NO_TC = 8u };
 
 typedef struct moe_config {
@@ -242,7 +241,8 @@ const char* moe_route_static_error(void);
 
 /* Measured rate of the block-scaled tensor-core MMA the expert GEMMs issue
  * (tcgen05.mma kind::mxf8f6f4: E2M1 weights x E4M3 activations with UE8M0
- * scales, M = 128, N = 192, K = 32) on CUDA device `device`. No page has a
+ * scales, M = 128, K = 32, N = n: a multiple of 16 in [16, 192]) on CUDA
+ * device `device`. No page has a
  * counterpart: it measures this GPU, as the denominator of the GEMMs'
  * tensor-pipe fraction. One CTA per SM issues mmas_per_sm MMAs back to back
  * from shared-memory operands (no memory traffic) into tensor memory; the
@@ -250,16 +250,18 @@ const char* moe_route_static_error(void);
  * returns the dense rate in *tflops (10^12 multiply-adds x 2 per second) and
  * the launch time in *ms (may be NULL). Synchronous; allocates and frees a
  * 4-byte status word and two events. Errors: MOE_ERR_INVALID_ARG
- * (mmas_per_sm outside [1, 2^24] or tflops NULL), MOE_ERR_CUDA,
+ * (mmas_per_sm outside [1, 2^24], n not as above, or tflops NULL), MOE_ERR_CUDA,
  * MOE_ERR_TIMEOUT (the MMAs did not finish within 2 s); text from
  * moe_probe_error(). */
-int moe_probe_mma_rate(int device, int mmas_per_sm, double* tflops, double* ms);
+int moe_probe_mma_rate(int device, int mmas_per_sm, int n, double* tflops, double* ms);
 
 /* Text of the calling thread's last error returned by moe_probe_mma_rate. */
 const char* moe_probe_error(void);
 
-/* Bytes of packed expert weights the context holds (codes + scales; the
- * "Neural Server" technical page, "What it runs on and what it runs", counts
+/* Bytes of expert weights the context holds in its layout (codes + scales:
+ * the packed tiles, exactly the canonical size, or the tcgen05 blocks, the
+ * canonical size plus the zero padding of partial 128-row tiles; the "Neural
+ * Server" technical page, "What it runs on and what it runs", counts
  * 13,219,200 B per gpt-oss-120B expert). 0 for a NULL ctx. */
 size_t moe_weight_bytes(const moe_ctx* ctx);
 

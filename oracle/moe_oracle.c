@@ -38,7 +38,7 @@
  * Formats (MX) v1.0 specification: E2M1 elements, one E8M0 scale per 32
  * consecutive elements along the reduction axis, value = E2M1 * 2^(e - 127).
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *   nibble order: the low nibble of byte i is element 2i, the high nibble 2i+1;
  *   gate/up: one [2F x d] matrix per expert, rows [0,F) gate, rows [F,2F) up;
  *   SiLU(z) = z / (1 + exp(-z)); no biases, no clamp;

@@ -84,7 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_route_static.restype = i32
             lib.moe_route_static_error.argtypes = []
             lib.moe_route_static_error.restype = ctypes.c_char_p
-            lib.moe_probe_mma_rate.argtypes = [i32, i32, P(ctypes.c_double), P(ctypes.c_double)]
+            lib.moe_probe_mma_rate.argtypes = [i32, i32, i32, P(ctypes.c_double), P(ctypes.c_double)]
             lib.moe_probe_mma_rate.restype = i32
             lib.moe_probe_error.argtypes = []
             lib.moe_probe_error.restype = ctypes.c_char_p
@@ -200,11 +200,11 @@ def moe_route_static(x, T: int, d: int, w_router, bias, n_experts: int, top_k: i
         raise MoeError(rc, "moe_route_static: " + lib.moe_route_static_error().decode(errors="replace"))
 
 
-def moe_probe_mma_rate(device: int = 0, mmas_per_sm: int = 200000) -> tuple[float, float]:
-    """(TFLOP/s, ms) of the block-scaled MMA kind the expert GEMMs use, measured on `device`."""
+def moe_probe_mma_rate(device: int = 0, mmas_per_sm: int = 200000, n: int = 192) -> tuple[float, float]:
+    """(TFLOP/s, ms) of the block-scaled MMA kind the expert GEMMs use (M=128, K=32, N=n), measured on `device`."""
     lib = load_library()
     tf, ms = ctypes.c_double(), ctypes.c_double()
-    rc = lib.moe_probe_mma_rate(device, mmas_per_sm, ctypes.byref(tf), ctypes.byref(ms))
+    rc = lib.moe_probe_mma_rate(device, mmas_per_sm, n, ctypes.byref(tf), ctypes.byref(ms))
     if rc < 0:
         raise MoeError(rc, lib.moe_probe_error().decode(errors="replace"))
     return tf.value, ms.value

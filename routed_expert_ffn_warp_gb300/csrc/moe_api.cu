@@ -28,8 +28,10 @@ struct moe_ctx {
   uint8_t* tcwd = nullptr;  // down copy for the tcgen05 GEMM
   size_t tcwd_bytes = 0;
   size_t tcwd_stride = 0;
-  CUtensorMap tmap_gu{};  // tensor maps the tcgen05 GEMM loads tcw / tcwd through
+  CUtensorMap tmap_gu{};  // tensor maps the tcgen05 kernels load tcw / tcwd through (tile pairs)
   CUtensorMap tmap_dn{};
+  CUtensorMap tmap_gu1{};  // the same with single-tile boxes
+  CUtensorMap tmap_dn1{};
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
@@ -44,8 +46,10 @@ struct moe_ctx {
   cudaEvent_t prof[moe::kForwardPhasesTc + 1] = {};
   int n_prof = 0;
   int max_smem = 0;
-  bool decode_ok = false;  // the fused single-kernel path fits this config
+  bool decode_ok = false;    // the fused mma.sync kernel serves T <= 16 (contexts with the packed copy)
+  bool fused_tc_ok = false;  // the fused tcgen05 kernel serves T <= 16 (contexts with the tcgen05 copies)
   moe::DecParams dec{};
+  moe::TcLayerParams tcl{};
 };
 
 namespace {
@@ -81,11 +85,11 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The fused single-kernel path: T <= 16 with its shared-memory plan, and,
-// when the context has the tcgen05 weight copy, at most kFusedMaxPairs pairs.
+// A single-launch path serves T <= 16 when its plan fits: the tcgen05 kernel
+// for contexts with the tcgen05 weight copies, the mma.sync kernel for those
+// with the packed copy (MOE_FLAG_NO_TC).
 bool uses_decode(const moe_ctx* ctx, int T) {
-  return T > 0 && ctx->decode_ok && T <= moe::kDecodeMaxT &&
-         (!ctx->base.tc_gateup || T * ctx->cfg.top_k <= moe::kFusedMaxPairs);
+  return T > 0 && T <= moe::kDecodeMaxT && (ctx->fused_tc_ok || ctx->decode_ok);
 }
 
 }  // namespace
@@ -122,16 +126,17 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   const int d = c.d, F = c.ffn, E = c.n_experts, k = c.top_k, S = c.shared_ffn, Tm = std::max(c.t_max, 1);
   ctx->expert_stride = moe::expert_packed_bytes(d, F);
-  ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
   const bool tc_fits =
       std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) <= (size_t)ctx->max_smem;
   if ((c.flags & MOE_FLAG_TC_GATEUP) && !tc_fits) {
     delete ctx;
     return fail(nullptr, MOE_ERR_INVALID_ARG, "too many experts for the tcgen05 GEMM's shared-memory tables");
   }
-  // the block-scaled tcgen05 GEMMs serve the multi-kernel path unless asked not to
-  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
-                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs);
+  // The block-scaled tcgen05 kernels (and their weight copies, the only copy such
+  // a context keeps) serve every forward unless asked not to or their tables do
+  // not fit; otherwise the packed copy serves the mma.sync kernels.
+  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) || (!(c.flags & MOE_FLAG_NO_TC) && tc_fits);
+  if (!tc) ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
@@ -170,19 +175,28 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
                o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
+  // fused tcgen05 path: x planes and h planes per K step with their launch-tagged flags, row-tile counters
+  const int tcap = std::min(Tm, moe::kDecodeMaxT), npad = tcap <= 8 ? 8 : (tcap + 7) & ~7;
+  const int xp_step = 2 * npad * 128 + 512, hp_step = 4 * npad * 128 + 512, hp_ks = moe::tc_ksteps(std::max(F, S));
+  const int max_slots = std::min(E, tcap * k) + (S > 0 ? 1 : 0);
+  const size_t o_xpl = take(tc ? (size_t)moe::tc_ksteps(d) * xp_step : 0), o_xfl = take(tc ? (size_t)moe::tc_ksteps(d) * 4 : 0),
+               o_hpl = take(tc ? (size_t)max_slots * hp_ks * hp_step : 0), o_hfl = take(tc ? (size_t)max_slots * hp_ks * 4 : 0),
+               o_dcnt = take((size_t)2 * moe::tc_dtiles(d) * 4);
   ctx->ws_bytes = off;
 
   if ((tc && (e = cudaMalloc(&ctx->tcw, ctx->tcw_bytes)) != cudaSuccess) ||
       (tc && (e = cudaMalloc(&ctx->tcwd, ctx->tcwd_bytes)) != cudaSuccess) ||
-      (e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess ||
+      (!tc && (e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess) ||
       (e = cudaMalloc(&ctx->w_router, (size_t)E * d * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->bias, (size_t)E * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->ws, ctx->ws_bytes)) != cudaSuccess) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
   }
-  if (tc && (!moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu) ||
-             !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn))) {
+  if (tc && (!moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu, 256) ||
+             !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn, 256) ||
+             !moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu1, 128) ||
+             !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn1, 128))) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_CUDA, "cuTensorMapEncodeTiled refused the tcgen05 weight copy");
   }
@@ -217,6 +231,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.hpanel = reinterpret_cast<uint8_t*>(w + o_hpanel);
   p.tmap_gu = &ctx->tmap_gu;
   p.tmap_dn = &ctx->tmap_dn;
+  p.tmap_gu1 = &ctx->tmap_gu1;
+  p.tmap_dn1 = &ctx->tmap_dn1;
   p.panel_prefix = reinterpret_cast<int32_t*>(w + o_pp);
   p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);
@@ -264,8 +280,26 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   // The fused kernel's CTAs wait on each other (bounded): it is used only when
   // one CTA per SM fits, so that a grid of one CTA per SM can be resident at once.
-  ctx->decode_ok = !(c.flags & MOE_FLAG_GENERAL_PATH) && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms) &&
-                   moe::decode_blocks_per_sm(dp) >= 1;
+  if (tc && (e = moe::configure_tc_layer(ctx->max_smem)) != cudaSuccess) {
+    moe_destroy(ctx);
+    return fail(nullptr, MOE_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  }
+  const bool single = !(c.flags & MOE_FLAG_GENERAL_PATH);
+  if (tc) {
+    moe::TcLayerParams& tp = ctx->tcl;
+    tp.d = dp;
+    tp.xplane = reinterpret_cast<uint8_t*>(w + o_xpl);
+    tp.xflag = reinterpret_cast<unsigned*>(w + o_xfl);
+    tp.hpanel = reinterpret_cast<uint8_t*>(w + o_hpl);
+    tp.hflag = reinterpret_cast<unsigned*>(w + o_hfl);
+    tp.dcnt = reinterpret_cast<int*>(w + o_dcnt);
+    tp.hp_ksteps = hp_ks;
+    tp.max_slots = max_slots;
+    ctx->fused_tc_ok = single && moe::tc_layer_plan(tp, ctx->max_smem, ctx->num_sms) && tp.xp_step == xp_step &&
+                       tp.hp_step == hp_step && moe::tc_layer_blocks_per_sm(tp) >= 1;
+  } else {
+    ctx->decode_ok = single && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms) && moe::decode_blocks_per_sm(dp) >= 1;
+  }
   *out = ctx;
   return MOE_OK;
 }
@@ -311,14 +345,14 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
     const int n = std::min(per_chunk, E - x0);
     if ((e = cudaMemcpy(sc, codes + (size_t)x0 * ccs, ccs * n, cudaMemcpyDefault)) != cudaSuccess) break;
     if ((e = cudaMemcpy(ss, scales + (size_t)x0 * css, css * n, cudaMemcpyDefault)) != cudaSuccess) break;
-    if ((e = moe::launch_repack(sc, ss, n, d, F, ccs, css, ctx->packed + (size_t)x0 * ctx->expert_stride,
-                                ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
+    if (ctx->packed && (e = moe::launch_repack(sc, ss, n, d, F, ccs, css, ctx->packed + (size_t)x0 * ctx->expert_stride,
+                                               ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
       break;
     if (ctx->tcw && (e = moe::launch_repack_tc(sc, ss, n, d, F, ccs, css, ctx->tcw + (size_t)x0 * ctx->tcw_stride,
-                                               ctx->tcw_stride, false, 0)) != cudaSuccess)
+                                               ctx->tcw_stride, false, ctx->load_err, 0)) != cudaSuccess)
       break;
     if (ctx->tcwd && (e = moe::launch_repack_tc(sc, ss, n, d, F, ccs, css, ctx->tcwd + (size_t)x0 * ctx->tcwd_stride,
-                                                ctx->tcwd_stride, true, 0)) != cudaSuccess)
+                                                ctx->tcwd_stride, true, ctx->load_err, 0)) != cudaSuccess)
       break;
     e = cudaDeviceSynchronize();
   }
@@ -326,12 +360,12 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
     const size_t sc_b = (size_t)3 * S * d / 2, ss_b = (size_t)3 * S * d / 32;
     if ((e = cudaMemcpy(sc, codes + (size_t)E * ccs, sc_b, cudaMemcpyDefault)) == cudaSuccess &&
         (e = cudaMemcpy(ss, scales + (size_t)E * css, ss_b, cudaMemcpyDefault)) == cudaSuccess &&
-        (e = moe::launch_repack(sc, ss, 1, d, S, sc_b, ss_b, ctx->packed + (size_t)E * ctx->expert_stride,
-                                moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess &&
+        (!ctx->packed || (e = moe::launch_repack(sc, ss, 1, d, S, sc_b, ss_b, ctx->packed + (size_t)E * ctx->expert_stride,
+                                                 moe::expert_packed_bytes(d, S), ctx->load_err, 0)) == cudaSuccess) &&
         (!ctx->tcw || (e = moe::launch_repack_tc(sc, ss, 1, d, S, sc_b, ss_b, ctx->tcw + (size_t)E * ctx->tcw_stride,
-                                                 moe::tc_expert_bytes(d, S), false, 0)) == cudaSuccess) &&
+                                                 moe::tc_expert_bytes(d, S), false, ctx->load_err, 0)) == cudaSuccess) &&
         (!ctx->tcwd || (e = moe::launch_repack_tc(sc, ss, 1, d, S, sc_b, ss_b, ctx->tcwd + (size_t)E * ctx->tcwd_stride,
-                                                  moe::tc_down_bytes(d, S), true, 0)) == cudaSuccess))
+                                                  moe::tc_down_bytes(d, S), true, ctx->load_err, 0)) == cudaSuccess))
       e = cudaDeviceSynchronize();
   }
   int nan_flag = 0;
@@ -370,7 +404,13 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
     dp.f = p;
     const bool prof = ctx->n_prof >= 2;
     if (prof) cudaEventRecord(ctx->prof[0], s);
-    e = moe::launch_decode(dp, s, ctx->num_sms, ctx->max_smem);
+    if (ctx->fused_tc_ok) {
+      moe::TcLayerParams tp = ctx->tcl;
+      tp.d.f = p;
+      e = moe::launch_tc_layer(tp, s, ctx->num_sms);
+    } else {
+      e = moe::launch_decode(dp, s, ctx->num_sms, ctx->max_smem);
+    }
     if (prof && e == cudaSuccess) cudaEventRecord(ctx->prof[1], s);
   } else {
     e = moe::launch_forward(p, s, ctx->num_sms, ctx->n_prof == moe::forward_phases(p) + 1 ? ctx->prof : nullptr);
@@ -475,7 +515,9 @@ int moe_launches_per_forward(const moe_ctx* ctx, int T) {
   return T <= moe::kRouteDDMaxT ? n - 1 : n;  // one router launch instead of router + top-k
 }
 
-size_t moe_weight_bytes(const moe_ctx* ctx) { return ctx ? ctx->packed_bytes : 0; }
+size_t moe_weight_bytes(const moe_ctx* ctx) {
+  return ctx ? ctx->packed_bytes + ctx->tcw_bytes + ctx->tcwd_bytes : 0;
+}
 
 const char* moe_last_error(const moe_ctx* ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
 

@@ -48,6 +48,7 @@
 
 #include "../../include/moe.h"
 #include "moe_device.cuh"
+#include "moe_fused_route.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -55,39 +56,10 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 512;
-constexpr int kWarps = 16;
 constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
 constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
 constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
 constexpr int kMaxUS = 8;                       // unit slots (partial-sum buffers) per phase, at most
-constexpr int kLogitCopies = kLogitWordCopies;  // CTA b polls copy b % kLogitCopies
-
-struct Shared {
-  int* ctl;     // [0, 8) gate/up arrivals, [8, 16) gate/up slot owners, [16, 24) down arrivals, [24, 32) down owners
-  __half* x16;  // phase C: [tcap][xstride] f16 x * 2^sigma_t
-  __half* hst;  // phase D (same memory): [kHalf][2][hstride] f16 h planes of one (slot, half)
-  float* hsc;   //   [kHalf][hgroups] their scales
-  float* xinv;  // [16]
-  dd* red;      // [12 warps][16 tokens] router partials
-  float* pgu;   // [n_us][3 chunks][2][16 rows][tcap] gate/up partial sums
-  float* pdn;   // [n_us][3 chunks][16 rows][min(8, tcap)] down partial sums
-  int* ids;
-  float* gates;
-  int* cnt;
-  int* offs;
-  int* perm;
-  int* inv;
-  int* slot_e;
-  int* slot_n;
-  int* slot_q0;
-  int* hs_slot;  // (slot, half) list of the down phase
-  int* hs_half;
-  int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
-              // [4] (slot, half) pairs, [5] pairs of routed slots, [6] warps done with their gate/up items
-  uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
-  int* rowcnt;
-};
 
 __device__ __forceinline__ Shared carve(uint8_t* sm, const DecParams& p) {
   Shared s;
@@ -99,35 +71,9 @@ __device__ __forceinline__ Shared carve(uint8_t* sm, const DecParams& p) {
   s.red = reinterpret_cast<dd*>(sm + p.off_red);
   s.pgu = reinterpret_cast<float*>(sm + p.off_pgu);
   s.pdn = reinterpret_cast<float*>(sm + p.off_pdn);
-  int* r = reinterpret_cast<int*>(sm + p.off_route);
-  const int Pm = kDecodeMaxT * p.f.k, E = p.f.E;
-  s.ids = r;
-  s.gates = reinterpret_cast<float*>(r + Pm);
-  s.cnt = r + 2 * Pm;
-  s.offs = s.cnt + E;
-  s.perm = s.offs + E + 1;
-  s.inv = s.perm + Pm;
-  s.slot_e = s.inv + Pm;
-  s.slot_n = s.slot_e + E + 1;
-  s.slot_q0 = s.slot_n + E + 1;
-  s.hs_slot = s.slot_q0 + E + 1;
-  s.hs_half = s.hs_slot + E + 1 + 64;
-  s.misc = s.hs_half + E + 1 + 64;
+  carve_route(s, sm, p);
   s.ring = sm + p.off_ring;
   return s;
-}
-
-// ---------------------------------------------------------------- bounded waits
-
-__device__ __forceinline__ bool timed_out(uint64_t t0, long long limit) {
-  return (long long)(globaltimer() - t0) > limit;
-}
-
-__device__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
-
-__device__ void give_up(volatile int* abort, int* status) {
-  *abort = 1;
-  set_status(status, MOE_ERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- work units
@@ -186,97 +132,6 @@ __device__ __forceinline__ void chunk_range(int K64, int c, int& k0, int& k1) {
   k1 = min(K64, k0 + ck);
 }
 
-// ---------------------------------------------------------------- phase A: x, router, x scaling
-
-// Published logit word: (fp32 bits << 32) | launch sequence number.
-__device__ __forceinline__ unsigned long long pack_logit(float v, unsigned seq) {
-  return ((unsigned long long)__float_as_uint(v) << 32) | seq;
-}
-
-// The router rows of this CTA's experts (blockIdx.x, + G, ...) are copied into
-// shared memory (the weight ring, idle until phase C) before the kernel waits
-// for the preceding grid: the router weights are constant inputs of the layer.
-__device__ void stage_router(const DecParams& p, const Shared& s) {
-  const int d4 = p.f.d / 4;
-  float* wsm = reinterpret_cast<float*>(s.ring);
-  int r = 0;
-  for (int e = blockIdx.x; e < p.f.E; e += gridDim.x, ++r)
-    for (int o = threadIdx.x; o < d4; o += kThreads)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(wsm + (size_t)r * p.f.d + 4 * o)),
-                   "l"(p.f.w_router + (size_t)e * p.f.d + 4 * o)
-                   : "memory");
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// x rows (bf16, as stored) into the shared x area with cp.async; all threads.
-// The wait also covers the router rows staged before.
-__device__ void stage_x(const DecParams& p, const Shared& s) {
-  const int d8 = p.f.d / 8;
-  for (int o = threadIdx.x; o < p.f.T * d8; o += kThreads) {
-    const int t = o / d8, i = o - t * d8;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(s.x16 + (size_t)t * p.xstride + 8 * i)),
-                 "l"(p.f.x + (size_t)t * p.f.d + 8 * i)
-                 : "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// Router logits from the staged weights and bf16 x. Token t is taken by the
-// wpt = 16 / T warps [t wpt, (t+1) wpt), each over an interleaved share of d;
-// every lane keeps a double-float sum, then a fixed warp tree and a fixed
-// tree over the token's warps.
-__device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
-  const FwdParams& f = p.f;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int d8 = f.d / 8, T = f.T;
-  const int wpt = max(1, kWarps / T), t = warp / wpt, q = warp - t * wpt;
-  const float* wsm = reinterpret_cast<const float*>(s.ring);
-  int r = 0;
-  for (int e = blockIdx.x; e < f.E; e += gridDim.x, ++r) {
-    const float* wr = wsm + (size_t)r * f.d;
-    if (t < T) {
-      dd acc = dd{0.f, 0.f};
-      for (int o = q * 32 + lane; o < d8; o += 32 * wpt) {
-        const float4 w0 = *reinterpret_cast<const float4*>(wr + 8 * o);
-        const float4 w1 = *reinterpret_cast<const float4*>(wr + 8 * o + 4);
-        const uint4 xv = *reinterpret_cast<const uint4*>(s.x16 + (size_t)t * p.xstride + 8 * o);
-        dd_mac(acc, __uint_as_float(xv.x << 16), w0.x);
-        dd_mac(acc, __uint_as_float(xv.x & 0xFFFF0000u), w0.y);
-        dd_mac(acc, __uint_as_float(xv.y << 16), w0.z);
-        dd_mac(acc, __uint_as_float(xv.y & 0xFFFF0000u), w0.w);
-        dd_mac(acc, __uint_as_float(xv.z << 16), w1.x);
-        dd_mac(acc, __uint_as_float(xv.z & 0xFFFF0000u), w1.y);
-        dd_mac(acc, __uint_as_float(xv.w << 16), w1.z);
-        dd_mac(acc, __uint_as_float(xv.w & 0xFFFF0000u), w1.w);
-      }
-      for (int o = 16; o; o >>= 1) acc = dd_add(acc, dd_shfl_xor(acc, o));
-      if (lane == 0) s.red[warp] = acc;
-    }
-    __syncthreads();
-    // warp t adds token t's wpt warp partials in a fixed tree, then publishes
-    if (warp < T) {
-      dd v = lane < wpt ? s.red[warp * wpt + lane] : dd{0.f, 0.f};
-      for (int o = 8; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
-      if (lane == 0 && f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
-      v.hi = __shfl_sync(0xffffffffu, v.hi, 0);  // lane 0's value in every copy
-      v.lo = __shfl_sync(0xffffffffu, v.lo, 0);
-      if (lane == 0) {
-        f.logit_hi[(size_t)warp * f.E + e] = v.hi;  // debug export
-        f.logit_lo[(size_t)warp * f.E + e] = v.lo;
-      }
-      // the word carries its own value: no other data is published with it;
-      // lane r writes copy r (the readers spread over the copies)
-      if (lane < kLogitCopies) {
-        unsigned long long* w = p.lwords + ((size_t)lane * p.tcap * f.E + (size_t)warp * f.E + e) * 2;
-        st_relaxed_u64(w, pack_logit(v.hi, seq));
-        st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
-      }
-    }
-    __syncthreads();
-  }
-}
-
 // Staged x row t (bf16, in place) -> f16 * 2^sigma_t by one warp; K padding zeroed.
 __device__ void scale_x_token(const DecParams& p, const Shared& s, int t) {
   const FwdParams& f = p.f;
@@ -320,260 +175,6 @@ __device__ void scale_x(const DecParams& p, const Shared& s) {
 // With T <= kWarps / 2 the x scaling runs on warps kWarps-1, kWarps-2, ...
 // while warps 0 .. T-1 poll the logit words and take the top k.
 __device__ __forceinline__ bool scale_x_beside_topk(const DecParams& p) { return p.f.T <= kWarps / 2; }
-
-// ---------------------------------------------------------------- phase B: routing (redundant per CTA)
-
-// Order-preserving map of a float to an unsigned key (-0 folded into +0).
-__device__ __forceinline__ unsigned fkey(float v) {
-  const unsigned u = __float_as_uint(v + 0.f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Top-k of token t by one warp: gather its logits of all E experts from the
-// published words (polling until every word carries this launch's number),
-// k rounds of a three-key warp reduction (logit hi, logit lo, lowest expert
-// index), then the softmax of the k selected logits. NPL = experts per lane.
-template <int NPL>
-__device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned seq, volatile int* abort) {
-  const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31;
-  const int E = f.E, k = f.k;
-  const unsigned long long* wt =
-      p.lwords + ((size_t)(blockIdx.x % kLogitCopies) * p.tcap * E + (size_t)t * E) * 2;
-  float vh[NPL], vl[NPL];
-  unsigned valid = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (lane + 32 * i < E) valid |= 1u << i;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    // every word of the lane in one round of loads, then one check
-    unsigned long long a[NPL], b[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      if ((valid >> i) & 1u) ld_relaxed_u64x2(wt + 2 * (lane + 32 * i), a[i], b[i]);
-      else a[i] = b[i] = (unsigned long long)seq;
-    }
-    bool ready = true;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      vh[i] = __uint_as_float((unsigned)(a[i] >> 32));
-      vl[i] = __uint_as_float((unsigned)(b[i] >> 32));
-      ready = ready && (unsigned)a[i] == seq && (unsigned)b[i] == seq;
-    }
-    if (__all_sync(0xffffffffu, ready)) break;
-    if (*abort || timed_out(t0, p.wait_ns)) {
-      if (lane == 0) give_up(abort, f.status);
-      break;
-    }
-  }
-  unsigned kh[NPL], kl[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    kh[i] = fkey(vh[i]);
-    kl[i] = fkey(vl[i]);
-  }
-  unsigned taken = ~valid;
-  int sel_id = 0;
-  float sel_h = 0.f, sel_l = 0.f;
-  for (int j = 0; j < k; ++j) {
-    unsigned bh = 0, bl = 0;
-    int bi = 0x7fffffff;
-    float fh = 0.f, fl = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const bool free_ = !((taken >> i) & 1u);
-      if (free_ && (kh[i] > bh || (kh[i] == bh && kl[i] > bl))) {  // equal keys keep the lower index
-        bh = kh[i];
-        bl = kl[i];
-        bi = lane + 32 * i;
-        fh = vh[i];
-        fl = vl[i];
-      }
-    }
-    const unsigned mh = __reduce_max_sync(0xffffffffu, bh);
-    const unsigned tie = __ballot_sync(0xffffffffu, bh == mh);
-    int mi;
-    if (__popc(tie) == 1) {  // one lane holds the largest hi part: it wins
-      mi = __shfl_sync(0xffffffffu, bi, __ffs(tie) - 1);
-    } else {  // equal hi parts: the lo part decides, then the lower index
-      const unsigned ml = __reduce_max_sync(0xffffffffu, bh == mh ? bl : 0u);
-      mi = (int)__reduce_min_sync(0xffffffffu, (bh == mh && bl == ml) ? (unsigned)bi : 0x7fffffffu);
-    }
-    const int owner = mi & 31;
-    if (owner == lane) taken |= 1u << (mi >> 5);
-    const float wh = __shfl_sync(0xffffffffu, fh, owner), wl = __shfl_sync(0xffffffffu, fl, owner);
-    if (lane == j) {
-      sel_id = mi;
-      sel_h = wh;
-      sel_l = wl;
-    }
-  }
-  const float top_h = __shfl_sync(0xffffffffu, sel_h, 0), top_l = __shfl_sync(0xffffffffu, sel_l, 0);
-  float ex = 0.f;
-  if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
-  float sum = ex;
-  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    s.ids[t * k + lane] = sel_id;
-    s.gates[t * k + lane] = ex / sum;
-    if (blockIdx.x == 0) {
-      f.ids[t * k + lane] = sel_id;
-      f.gates[t * k + lane] = ex / sum;
-    }
-  }
-}
-
-// Counting sort of P <= 32 pairs by expert with one warp: pair q's position
-// is the number of pairs with a smaller expert, or the same expert and a
-// smaller pair index (a stable sort), counted over all pairs at once.
-__device__ void bucket_small(const DecParams& p, const Shared& s) {
-  const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31;
-  const int P = f.P, E = f.E, T = f.T;
-  const int my_e = lane < P ? s.ids[lane] : 0x7fffffff;
-  int rank = 0;
-  for (int j = 0; j < P; ++j) {
-    const int ej = __shfl_sync(0xffffffffu, my_e, j);
-    rank += (ej < my_e) || (ej == my_e && j < lane);
-  }
-  if (lane < P) s.perm[rank] = lane;
-  __syncwarp();
-  const int qs = lane < P ? s.perm[lane] : 0;
-  const unsigned key = lane < P ? ((unsigned)s.ids[qs] << 8) | (unsigned)qs : 0xffffffffu;
-  __syncwarp();
-  const int e = (int)(key >> 8), q = (int)(key & 0xffu);
-  const int eprev = __shfl_up_sync(0xffffffffu, e, 1);
-  const bool first = lane < P && (lane == 0 || e != eprev);
-  const unsigned firsts = __ballot_sync(0xffffffffu, first);
-  const int ns = __popc(firsts);
-  if (lane < P) {
-    s.perm[lane] = q;
-    s.inv[q] = lane;
-    if (blockIdx.x == 0) {
-      f.perm[lane] = q;
-      f.inv[q] = lane;
-    }
-  }
-  if (first) {
-    const int slot = __popc(firsts & ((1u << lane) - 1u));
-    const unsigned after = firsts & ~((2u << lane) - 1u);  // next first lane, or P
-    const int next = after ? __ffs(after) - 1 : P;
-    s.slot_e[slot] = e;
-    s.slot_q0[slot] = lane;
-    s.slot_n[slot] = next - lane;
-  }
-  if (lane == 0) {
-    s.misc[0] = ns;
-    int tot = ns;
-    if (f.S > 0) {
-      s.slot_e[ns] = E;
-      s.slot_n[ns] = T;
-      s.slot_q0[ns] = P;
-      ++tot;
-    }
-    s.misc[1] = tot;
-  }
-}
-
-// Debug export of counts and offsets for the small-P path (CTA 0, a spare warp).
-__device__ void export_counts_small(const DecParams& p, const Shared& s) {
-  const FwdParams& f = p.f;
-  for (int x = (threadIdx.x & 31); x <= f.E; x += 32) {
-    int c = 0, o = 0;
-    for (int i = 0; i < f.P; ++i) {
-      const int ei = s.ids[i];
-      c += (ei == x);
-      o += (ei < x);
-    }
-    if (x < f.E) f.counts[x] = c;
-    f.offsets[x] = o;
-  }
-}
-
-// Counting sort for larger P with one warp: histogram, exclusive scan, slots,
-// stable ranks within each bucket.
-__device__ void bucket_large(const DecParams& p, const Shared& s) {
-  const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31;
-  const int E = f.E, T = f.T, P = f.P;
-  const bool writer = blockIdx.x == 0;
-  for (int q = lane; q < P; q += 32) atomicAdd(&s.cnt[s.ids[q]], 1);
-  __syncwarp();
-  int loc = 0;  // exclusive scan over E <= 512: lane owns experts [16 lane, 16 lane + 16)
-  for (int i = 0; i < 16; ++i) {
-    const int e = 16 * lane + i;
-    if (e < E) loc += s.cnt[e];
-  }
-  int inc = loc;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  int run = inc - loc;
-  for (int i = 0; i < 16; ++i) {
-    const int e = 16 * lane + i;
-    if (e < E) {
-      s.offs[e] = run;
-      run += s.cnt[e];
-    }
-  }
-  if (lane == 31) s.offs[E] = inc;
-  __syncwarp();
-  int ns = 0;  // slots: the experts that received pairs, in expert order
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const bool has = e < E && s.cnt[e] > 0;
-    const unsigned bal = __ballot_sync(0xffffffffu, has);
-    if (has) {
-      const int pos = ns + __popc(bal & ((1u << lane) - 1u));
-      s.slot_e[pos] = e;
-      s.slot_n[pos] = s.cnt[e];
-      s.slot_q0[pos] = s.offs[e];
-    }
-    ns += __popc(bal);
-  }
-  if (lane == 0) {
-    s.misc[0] = ns;
-    int tot = ns;
-    if (f.S > 0) {
-      s.slot_e[ns] = E;
-      s.slot_n[ns] = T;
-      s.slot_q0[ns] = P;
-      ++tot;
-    }
-    s.misc[1] = tot;
-  }
-  if (writer)
-    for (int i = lane; i <= E; i += 32) {
-      f.offsets[i] = s.offs[i];
-      if (i < E) f.counts[i] = s.cnt[i];
-    }
-  __syncwarp();
-  int* runp = s.cnt;  // the counts are done with; reuse as running offsets
-  for (int i = lane; i < E; i += 32) runp[i] = s.offs[i];
-  __syncwarp();
-  for (int base = 0; base < P; base += 32) {  // stable ranks, pairs in index order
-    const int q = base + lane;
-    const bool valid = q < P;
-    const int e = valid ? s.ids[q] : -1 - lane;
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & ((1u << lane) - 1u));
-    const int before = valid ? runp[e] : 0;
-    __syncwarp();
-    if (valid && rank == 0) runp[e] = before + __popc(same);
-    __syncwarp();
-    if (valid) {
-      const int pos = before + rank;
-      s.perm[pos] = q;
-      s.inv[q] = pos;
-      if (writer) {
-        f.perm[pos] = q;
-        f.inv[q] = pos;
-      }
-    }
-  }
-}
 
 // The (slot, half) pairs of the down phase, in slot order: a slot with more
 // than kHalf tokens contributes two (tokens [0, 8) and [8, n)). One warp.
@@ -1246,6 +847,8 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   // of 64 elements): the 8 rows x 4 16-byte columns of a fragment load hit
   // distinct banks
   p.xstride = f.d64 + 32;
+  p.xs_t = p.xstride;  // rows contiguous: K chunks of 128 follow each other
+  p.xs_k = 128;
   p.hstride = f.fmax64 + 32;
   size_t off = 4 * kMaxUS * 4;
   off = up(off, 128);
@@ -1259,7 +862,7 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   off = up(off + kDecodeMaxT * 4, 16);
   p.off_red = (int)off;
   off = up(off + (size_t)kWarps * kDecodeMaxT * sizeof(dd), 16);
-  const size_t route_bytes = (size_t)(4 * Pm + 5 * (f.E + 1) + 2 * (f.E + 1 + 64) + 8) * 4;
+  const size_t route_bytes = route_region_bytes(f.E, f.k);
   // the deepest weight ring per warp that fits: 8, 6 or 4 slots (a 12-slot
   // ring measured no faster: the stream is not short of copies in flight)
   const int tries[7][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 6}, {4, 6}, {kMaxUS, 4}, {4, 4}, {2, 4}};

@@ -128,6 +128,8 @@ struct FwdParams {
   uint8_t* hpanel;       // h panels of the down step (kTcPanelStepD per K step)
   const void* tmap_gu;   // host: CUtensorMap of tcw (see encode_tc_weight_map)
   const void* tmap_dn;   // host: CUtensorMap of tcwd
+  const void* tmap_gu1;  // host: CUtensorMap of tcw with a one-tile box (128 rows of 64 bytes)
+  const void* tmap_dn1;  // host: CUtensorMap of tcwd with a one-tile box
   int32_t* panel_prefix; // [E+2] first panel of each slot
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
@@ -178,11 +180,40 @@ struct DecParams {
   int ring_groups;      // 1,088-byte slots of each warp's weight ring
   int n_us;             // partial-sum unit slots per phase
   int xstride, hstride; // f16 row strides of the shared x and h
+  int xs_t, xs_k;       // staged bf16 x: element i of token t at t * xs_t + (i / 128) * xs_k + i % 128
   int off_x16, off_hsc, off_xinv, off_red, off_pgu, off_pdn, off_route, off_ring, smem_bytes;
   long long wait_ns;       // bound of every device-side wait
   int test_extra;          // > 0: the h staging waits for a launch number no launch writes (timeout test)
   long long test_wait_ns;  // bound of that wait
 };
+// Fused single-launch layer on the 5th-generation tensor cores
+// (moe_fused_tc.cu), used for T <= kDecodeMaxT when the context holds the
+// tcgen05 weight copies. Routing as in the mma.sync kernel (the DecParams
+// part); gate/up and down as block-scaled tcgen05 MMAs of TMA-loaded weight
+// tiles by MXFP8 activation steps that other CTAs of the same launch publish
+// in global memory behind launch-tagged flags.
+struct TcLayerParams {
+  DecParams d;          // routing: sizes, inputs, workspace, logit words, launch numbers, smem of the routing arrays
+  int npad;             // rows per activation plane the context plans for (tcap rounded up to 8, at least 8)
+  int stages;           // pipeline stages of the ring
+  int bslot;            // bytes of a stage's activation slot: 4 npad rows * 128 + 512
+  int off_ctl, off_hx, off_bars, off_ring, smem_bytes;
+  int router_bytes;     // this CTA's router rows staged at the start of the ring
+  uint8_t* xplane;      // [ksteps(d)][xp_step]: x as two E4M3 planes per K step (rows, then 512 scale bytes)
+  int xp_step;          // bytes per x plane step: 2 npad * 128 + 512
+  unsigned* xflag;      // [ksteps(d)]: launch number of the published x step
+  uint8_t* hpanel;      // [max_slots][hp_ksteps][hp_step]: h of a slot as four E4M3 planes per K step
+  int hp_step;          // bytes per h step: 4 npad * 128 + 512
+  int hp_ksteps;        // K steps per slot: ksteps(max(ffn, shared ffn))
+  int max_slots;        // slots a forward can have: min(E, tcap * k) + (shared expert)
+  unsigned* hflag;      // [max_slots][hp_ksteps]: launch number of the published h step
+  int* dcnt;            // [2][dtiles(d)]: down units finished per 128-row tile; launches alternate halves
+};
+bool tc_layer_plan(TcLayerParams& p, int max_smem, int num_sms);
+cudaError_t launch_tc_layer(const TcLayerParams& p, cudaStream_t stream, int num_sms);
+cudaError_t configure_tc_layer(int max_smem);
+int tc_layer_blocks_per_sm(const TcLayerParams& p);
+
 bool decode_plan(DecParams& p, int max_smem, int num_sms);
 cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, int max_smem);
 // CTAs of the fused kernel (with the shared memory of plan p) that fit on one
@@ -233,16 +264,18 @@ cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp
                           int* err_flag, cudaStream_t stream);
 // The tcgen05 weight copies of n_exp experts from the canonical layout: gate/up
 // (down = false) or down (down = true).
+// A scale byte 0xFF (NaN) sets *err_flag.
 cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                              size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
-                             bool down, cudaStream_t stream);
+                             bool down, int* err_flag, cudaStream_t stream);
 cudaError_t launch_gemm_down_tc(const FwdParams& p, cudaStream_t stream, int num_sms);
 // Dynamic shared memory of the tcgen05 GEMM kernel for E experts.
 size_t tc_gemm_smem_bytes(int E, bool down);
 // Fills `map` (a 64-byte aligned CUtensorMap) with the tensor map the tcgen05
-// GEMM loads a weight copy of `bytes` bytes at `base` through; false if the
-// driver refuses it.
-bool encode_tc_weight_map(const void* base, size_t bytes, void* map);
+// kernels load a weight copy of `bytes` bytes at `base` through, with a box of
+// box_rows rows of 64 bytes (256: both tiles of a pair's K step; 128: one
+// tile); false if the driver refuses it.
+bool encode_tc_weight_map(const void* base, size_t bytes, void* map, int box_rows);
 
 // Launches a kernel of the forward chain with programmatic stream
 // serialization: it may be scheduled once the grid before it has passed its

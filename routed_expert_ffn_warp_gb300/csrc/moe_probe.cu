@@ -1,7 +1,8 @@
 // Measured rate of the block-scaled tensor-core MMA that the expert GEMMs of
 // this library issue: tcgen05.mma kind::mxf8f6f4 with E2M1 weights, E4M3
-// activations and UE8M0 scale factors, M = 128, N = 192, K = 32 -- the shape
-// of the down GEMM's widest unit. Every SM runs one CTA whose single issuing
+// activations and UE8M0 scale factors, M = 128, K = 32 and N = 16 .. 192 (a
+// multiple of 16: the widths the gate/up and down GEMMs issue; 192 is the
+// down GEMM's widest unit). Every SM runs one CTA whose single issuing
 // thread sends MMAs back to back into one TMEM accumulator from operands that
 // stay in shared memory, so the time is the tensor pipe's alone (no memory
 // traffic). The rate is the denominator the prefill GEMMs' tensor-pipe
@@ -21,15 +22,15 @@ namespace {
 
 using namespace dev;
 
-constexpr int kProbeM = 128, kProbeN = 192, kProbeK = 32;
+constexpr int kProbeM = 128, kProbeMaxN = 192, kProbeK = 32;
 constexpr int kProbeThreads = 128;          // four warps: one per TMEM lane quadrant for the scale stores
 constexpr int kProbeA = 16 * 1024;          // A: 16 eight-row groups of 8 core matrices (1,024 bytes each)
-constexpr int kProbeB = 24 * 1024;          // B: 24 eight-row groups
+constexpr int kProbeB = kProbeMaxN / 8 * 1024;  // B: up to 24 eight-row groups
 constexpr uint32_t kProbeCols = 512;        // accumulator at column 0 (192 wide), scale factors at 384
 constexpr int kProbeSf = 384;
 constexpr long long kProbeWaitNs = 2000000000LL;  // 2 s: far above any probe length the host asks for
 
-__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int n_mma, int* status) {
+__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int n_mma, int n, int* status) {
   extern __shared__ __align__(1024) uint8_t sm[];
   uint8_t* a = sm;
   uint8_t* b = sm + kProbeA;
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int n_mma, i
       const int kb = i & 3;  // the four K = 32 blocks of the operand, each with its own scale-factor id
       const uint64_t ad = tc::smem_desc(a + 2 * kb * 128, 128, 8 * 128);
       const uint64_t bd = tc::smem_desc(b + 2 * kb * 128, 128, 8 * 128);
-      tc::mma_mxf4_mxf8(tmem, ad, bd, tc::idesc_mxf4_mxf8(kProbeM, kProbeN, kb, kb), tmem + kProbeSf,
+      tc::mma_mxf4_mxf8(tmem, ad, bd, tc::idesc_mxf4_mxf8(kProbeM, n, kb, kb), tmem + kProbeSf,
                         tmem + kProbeSf + 16, i > 0 ? 1u : 0u);
     }
     tc::commit(bar);
@@ -101,10 +102,11 @@ int probe_fail(int code, const std::string& msg) {
 
 extern "C" const char* moe_probe_error(void) { return moe::t_probe_err.c_str(); }
 
-extern "C" int moe_probe_mma_rate(int device, int mmas_per_sm, double* tflops, double* ms) {
+extern "C" int moe_probe_mma_rate(int device, int mmas_per_sm, int n, double* tflops, double* ms) {
   using namespace moe;
-  if (mmas_per_sm < 1 || mmas_per_sm > (1 << 24) || !tflops)
-    return probe_fail(MOE_ERR_INVALID_ARG, "moe_probe_mma_rate: need 1 <= mmas_per_sm <= 2^24 and tflops != NULL");
+  if (mmas_per_sm < 1 || mmas_per_sm > (1 << 24) || !tflops || n < 16 || n > kProbeMaxN || n % 16)
+    return probe_fail(MOE_ERR_INVALID_ARG, "moe_probe_mma_rate: need 1 <= mmas_per_sm <= 2^24, n a multiple of 16 "
+                                           "in [16, 192] and tflops != NULL");
   int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
   if (prev != device && cudaSetDevice(device) != cudaSuccess)
@@ -125,12 +127,12 @@ extern "C" int moe_probe_mma_rate(int device, int mmas_per_sm, double* tflops, d
   if (e == cudaSuccess) e = cudaEventCreate(&e0);
   if (e == cudaSuccess) e = cudaEventCreate(&e1);
   if (e == cudaSuccess) {
-    mma_rate_kernel<<<sms, kProbeThreads, smem>>>(1024, status);  // warm-up: clocks up, code loaded
+    mma_rate_kernel<<<sms, kProbeThreads, smem>>>(1024, n, status);  // warm-up: clocks up, code loaded
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaEventRecord(e0);
   if (e == cudaSuccess) {
-    mma_rate_kernel<<<sms, kProbeThreads, smem>>>(mmas_per_sm, status);
+    mma_rate_kernel<<<sms, kProbeThreads, smem>>>(mmas_per_sm, n, status);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaEventRecord(e1);
@@ -143,7 +145,7 @@ extern "C" int moe_probe_mma_rate(int device, int mmas_per_sm, double* tflops, d
   } else if (st != 0) {
     rc = probe_fail(st, "moe_probe_mma_rate: the MMAs did not complete within the bound");
   } else {
-    const double flops = 2.0 * kProbeM * kProbeN * kProbeK * (double)mmas_per_sm * (double)sms;
+    const double flops = 2.0 * kProbeM * n * kProbeK * (double)mmas_per_sm * (double)sms;
     *tflops = flops / ((double)t_ms * 1e-3) / 1e12;
     if (ms) *ms = t_ms;
   }

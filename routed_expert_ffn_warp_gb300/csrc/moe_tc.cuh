@@ -18,6 +18,7 @@
 #pragma once
 #include <stdint.h>
 
+#include "../../include/moe.h"
 #include "moe_device.cuh"
 
 namespace moe {
@@ -93,6 +94,105 @@ __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- bounded mbarrier waits
+
+using dev::globaltimer;
+using dev::mbar_try_wait;
+using dev::mbar_try_wait_hint;
+constexpr long long kTcWaitNs = 50000000LL;  // 50 ms: orders of magnitude above any wait of a healthy layer
+
+// Bounded mbarrier waits. Every role passes every phase of the barriers it
+// waits on in order, so a parity wait never meets a phase two steps old. On
+// expiry the wait records MOE_ERR_TIMEOUT, raises the CTA's abort flag and
+// returns false; once the flag is up every wait returns false at once and
+// every role stops issuing copies and MMAs (the kernel then drains what is in
+// flight before it frees tensor memory, see the end of gemm_tc_kernel).
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if ((long long)(globaltimer() - t0) > kTcWaitNs) {
+      *abort = 1;
+      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// The same wait for the roles off the MMA lanes' critical path (producers,
+// epilogue): each try may suspend the thread for up to 20 us until the phase
+// completes, so that waiting warps leave their issue slots to the MMA lanes.
+__device__ __forceinline__ bool bounded_wait_sleep(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait_hint(bar, parity, 20000u)) {
+    if (*abort) return false;
+    if ((long long)(globaltimer() - t0) > kTcWaitNs) {
+      *abort = 1;
+      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// After an abort: long enough for every copy and MMA already issued to land
+// (each takes microseconds), so that no copy writes into shared memory and no
+// MMA touches tensor memory after this CTA has freed them.
+constexpr long long kDrainNs = 1000000LL;
+
+// ---------------------------------------------------------------- MXFP8 planes of a 32-element block
+
+// Split the 32 values of a block (one per lane) into `planes` MXFP8 planes:
+// each an E8M0 block scale (largest magnitude into [128, 256)) and E4M3 codes
+// of what the planes before left over. Plane pl's code goes to code[pl], its
+// scale byte is returned in the matching entry of sc (the same in every lane).
+template <int kPl>
+__device__ __forceinline__ void split_planes(float v, uint32_t (&code)[kPl], uint32_t (&sc)[kPl]) {
+#pragma unroll
+  for (int pl = 0; pl < kPl; ++pl) {
+    float amax = fabsf(v);
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
+    sh = max(-127, min(127, sh));
+    const float ish = __uint_as_float((uint32_t)(127 - sh) << 23), fsh = __uint_as_float((uint32_t)(127 + sh) << 23);
+    // E4M3 by the hardware conversions (round to nearest even, saturating at 448)
+    uint16_t c2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(0.f), "f"(v * ish));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    code[pl] = c2 & 0xFFu;
+    v -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;  // the remainder for the next plane
+    sc[pl] = (uint32_t)(sh + 127);
+  }
+}
+
+
+// Split the 32 values of a block (one per lane) into 4 MXFP8 planes with one
+// reduction: plane 0 takes the block maximum into [128, 256) as above; every
+// later plane's scale is the previous one divided by 32. An E4M3 code of a
+// value below 256 errs by at most 8 (half its spacing there), so a plane's
+// remainder, scaled by 32, stays at most 256 and fits the next plane; after
+// the 4 planes the error is below 2^-19 of the block maximum.
+__device__ __forceinline__ void split_planes4_fixed(float v, uint32_t (&code)[4], uint32_t (&sc)[4]) {
+  float amax = fabsf(v);
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
+#pragma unroll
+  for (int pl = 0; pl < 4; ++pl) {
+    const int s = max(-127, min(127, sh));
+    const float ish = __uint_as_float((uint32_t)(127 - s) << 23), fsh = __uint_as_float((uint32_t)(127 + s) << 23);
+    uint16_t c2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(0.f), "f"(v * ish));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    code[pl] = c2 & 0xFFu;
+    v -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;
+    sc[pl] = (uint32_t)(s + 127);
+    sh -= 5;
+  }
 }
 
 // ---------------------------------------------------------------- E4M3 (OCP FP8, "FN": no infinities)

@@ -54,7 +54,6 @@ constexpr int kCmRows = kTcPairBytes / 64;  // 64-byte tensor rows per weight bl
 constexpr uint32_t kTmemCols = 512;        // accumulators from column 0, scale factors from 384
 constexpr int kSfCol = 384;                // set s (the stage) at +32 s: SFA of M tile 0 / 1 at +0 / +8, SFB at +16
 constexpr int kSfSet = 32;
-constexpr long long kWaitNs = 50000000LL;
 // roles: warp 0 weights, 1 activations, 2 and 3 MMA lanes, 4 .. 7 scale factors to TMEM, 8 .. 15
 // epilogue (a warp's TMEM lane quadrant is warp % 4)
 constexpr int kProducerWarp = 0, kPanelWarp = 1, kMmaWarp0 = 2, kSfWarp0 = 4, kEpiWarp0 = 8, kEpiThreads = 256;
@@ -93,46 +92,6 @@ template <bool kDown>
 constexpr size_t tc_smem_fixed() {
   return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (3 * Mode<kDown>::kS + 4) + 16;
 }
-
-// Bounded mbarrier waits. Every role passes every phase of the barriers it
-// waits on in order, so a parity wait never meets a phase two steps old. On
-// expiry the wait records MOE_ERR_TIMEOUT, raises the CTA's abort flag and
-// returns false; once the flag is up every wait returns false at once and
-// every role stops issuing copies and MMAs (the kernel then drains what is in
-// flight before it frees tensor memory, see the end of gemm_tc_kernel).
-__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if ((long long)(globaltimer() - t0) > kWaitNs) {
-      *abort = 1;
-      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-// The same wait for the roles off the MMA lanes' critical path (producers,
-// epilogue): each try may suspend the thread for up to 20 us until the phase
-// completes, so that waiting warps leave their issue slots to the MMA lanes.
-__device__ __forceinline__ bool bounded_wait_sleep(uint64_t* bar, uint32_t parity, int* status, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait_hint(bar, parity, 20000u)) {
-    if (*abort) return false;
-    if ((long long)(globaltimer() - t0) > kWaitNs) {
-      *abort = 1;
-      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-// After an abort: long enough for every copy and MMA already issued to land
-// (each takes microseconds), so that no copy writes into shared memory and no
-// MMA touches tensor memory after this CTA has freed them.
-constexpr long long kDrainNs = 1000000LL;
 
 __device__ __forceinline__ int find_unit_slot(const int32_t* prefix, int n, int unit) {
   int lo = 0, hi = n - 1;
@@ -208,56 +167,6 @@ __device__ __forceinline__ void cursor_next(const FwdParams& p, const SlotTab& s
   if (++c.ks == c.g.nks) {
     c.ks = 0;
     if (++c.i < n_units) c.g = tc_unit<kDown>(p, st, blockIdx.x + c.i * gridDim.x);
-  }
-}
-
-// Split the 32 values of a block (one per lane) into `planes` MXFP8 planes:
-// each an E8M0 block scale (largest magnitude into [128, 256)) and E4M3 codes
-// of what the planes before left over. Plane pl's code goes to code[pl], its
-// scale byte is returned in the matching entry of sc (the same in every lane).
-template <int kPl>
-__device__ __forceinline__ void split_planes(float v, uint32_t (&code)[kPl], uint32_t (&sc)[kPl]) {
-#pragma unroll
-  for (int pl = 0; pl < kPl; ++pl) {
-    float amax = fabsf(v);
-    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
-    sh = max(-127, min(127, sh));
-    const float ish = __uint_as_float((uint32_t)(127 - sh) << 23), fsh = __uint_as_float((uint32_t)(127 + sh) << 23);
-    // E4M3 by the hardware conversions (round to nearest even, saturating at 448)
-    uint16_t c2;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(0.f), "f"(v * ish));
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
-    code[pl] = c2 & 0xFFu;
-    v -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;  // the remainder for the next plane
-    sc[pl] = (uint32_t)(sh + 127);
-  }
-}
-
-
-// Split the 32 values of a block (one per lane) into 4 MXFP8 planes with one
-// reduction: plane 0 takes the block maximum into [128, 256) as above; every
-// later plane's scale is the previous one divided by 32. An E4M3 code of a
-// value below 256 errs by at most 8 (half its spacing there), so a plane's
-// remainder, scaled by 32, stays at most 256 and fits the next plane; after
-// the 4 planes the error is below 2^-19 of the block maximum.
-__device__ __forceinline__ void split_planes4_fixed(float v, uint32_t (&code)[4], uint32_t (&sc)[4]) {
-  float amax = fabsf(v);
-  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
-#pragma unroll
-  for (int pl = 0; pl < 4; ++pl) {
-    const int s = max(-127, min(127, sh));
-    const float ish = __uint_as_float((uint32_t)(127 - s) << 23), fsh = __uint_as_float((uint32_t)(127 + s) << 23);
-    uint16_t c2;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(0.f), "f"(v * ish));
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
-    code[pl] = c2 & 0xFFu;
-    v -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;
-    sc[pl] = (uint32_t)(s + 127);
-    sh -= 5;
   }
 }
 
@@ -340,7 +249,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       for (int q = 0; q < M::kPf && cp.i < n_units; ++q) prefetch();
       for (int j = 0; ca.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS && !bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
+        if (j >= kS && !tc::bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
         uint8_t* sb = stg + (size_t)s * M::kStage;
         // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
         mbar_arrive_expect_tx(&full[s], (uint32_t)kTcPairBytes);
@@ -360,7 +269,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       const int pstride = kDown ? tc_ksteps(p.F > p.S ? p.F : p.S) : tc_ksteps(p.d);
       for (int j = 0; cb.i < n_units; ++j) {
         const int s = j % kS;
-        if (j >= kS && !bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
+        if (j >= kS && !tc::bounded_wait_sleep(&empty[s], (uint32_t)((j / kS - 1) & 1), p.status, abort)) break;
         const int N = M::kPlanes * npad_of(cb.g.n);
         uint8_t* sb = stg + (size_t)s * M::kStage + M::kAPair;
         const uint8_t* src = (kDown ? p.hpanel : p.xpanel) + ((size_t)cb.g.panel * pstride + cb.ks) * M::kPanelStep;
@@ -379,13 +288,13 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
         const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
         const int N = M::kPlanes * npad_of(g.n), acc = i % kBufs;
         const bool mine = t < g.nt;  // a pair of one tile leaves lane 1 without MMAs
-        if (i >= kBufs && !bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status, abort)) break;
+        if (i >= kBufs && !tc::bounded_wait(&accempty[acc], (uint32_t)((i / kBufs - 1) & 1), p.status, abort)) break;
         tc::fence_after();
         const uint32_t d = tmem + M::kDCol * (kMma * acc + t);
         for (int ks = 0; ks < g.nks; ++ks) {
           const int jj = j0 + ks, s = jj % kS;
           // every lane takes part in every step's hand-off, with or without MMAs
-          if (!bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status, abort)) {  // operands landed, scales in TMEM
+          if (!tc::bounded_wait(&ready[s], (uint32_t)((jj / kS) & 1), p.status, abort)) {  // operands landed, scales in TMEM
             ok = false;
             break;
           }
@@ -421,7 +330,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       for (int ks = 0; ks < g.nks; ++ks, ++j) {
         const int s = j % kS;
         // the warp's lanes leave together (one lane's verdict), so tcgen05.st stays warp-uniform
-        ok = __shfl_sync(0xffffffffu, bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status, abort) ? 1 : 0, 0) != 0;
+        ok = __shfl_sync(0xffffffffu, tc::bounded_wait(&full[s], (uint32_t)((j / kS) & 1), p.status, abort) ? 1 : 0, 0) != 0;
         if (!ok) break;
         const uint8_t* sb = stg + (size_t)s * M::kStage;
         const uint8_t* sbf = sb + M::kAPair + M::kPlanes * npad_of(g.n) * kTcStepK;  // SFB behind the N rows
@@ -456,9 +365,9 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
       const TcUnit g = tc_unit<kDown>(p, st, b0 + i * G);
       const int npad = npad_of(g.n), acc = i % kBufs;
       // every epilogue thread leaves on the same verdict: the named barriers below need all 256
-      const bool ok = bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status, abort);
-      named_bar(1, kEpiThreads);
-      if (*abort || !ok) break;
+      const bool ok = tc::bounded_wait_sleep(&accfull[acc], (uint32_t)((i / kBufs) & 1), p.status, abort);
+      // one verdict for all 256 (the abort flag may rise between two threads' reads of it)
+      if (named_bar_or(1, kEpiThreads, !ok || *abort)) break;
       tc::fence_after();
       if (kDown) {  // part rows q0 + m, column 128 (mt + t) + 32 qd + lane: the sum of the 4 planes
         for (int t = 0; t < g.nt; ++t) {
@@ -513,7 +422,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
               h = gate / (1.f + __expf(-gate)) * up;
             }
             uint32_t code[4], sc[4];
-            split_planes4_fixed(h, code, sc);
+            tc::split_planes4_fixed(h, code, sc);
             const int k = kh + 32 * b + lane;
 #pragma unroll
             for (int pl = 0; pl < 4; ++pl) {
@@ -545,7 +454,7 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   if (warp == 0) {
     if (*abort) {  // the roles stopped early: let every copy and MMA already issued finish
       const uint64_t t0 = globaltimer();
-      while ((long long)(globaltimer() - t0) < kDrainNs) __nanosleep(10000);
+      while ((long long)(globaltimer() - t0) < tc::kDrainNs) __nanosleep(10000);
     }
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
@@ -594,7 +503,7 @@ __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
 // (gate rows for m < 64, up rows after), K = d. Down: row 128a + m of the
 // down matrix, K = f.
 __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
-                                 size_t ccs, size_t css, uint8_t* out, size_t out_stride, bool down) {
+                                 size_t ccs, size_t css, uint8_t* out, size_t out_stride, bool down, int* err) {
   // every tile of the pairs, the second tile of an odd last pair included (all code 0, scale 127)
   const int nms = 2 * (down ? tc_dn_pairs(d) : tc_gu_pairs(f)), K = down ? f : d, nks = tc_ksteps(K);
   const long long total = (long long)n_exp * nms * nks * 128;
@@ -635,6 +544,7 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
     for (int kb = 0; kb < 4; ++kb) {
       const int blk32 = 4 * ks + kb;
       const uint32_t sc = (live && 32 * blk32 < K) ? sr[blk32] : 127u;
+      if (sc == 255u) atomicExch(err, 1);
       w |= sc << (8 * kb);
     }
     *reinterpret_cast<uint32_t*>(dst + 2 * kTcCodeBytes + 512 * (a & 1) + 16 * (m & 31) + 4 * (m >> 5)) = w;
@@ -659,7 +569,7 @@ __global__ void __launch_bounds__(256) prep_xq_kernel(FwdParams p) {
   const int k = 32 * b + lane;
   const float v = k < p.d ? __uint_as_float((uint32_t)p.x[(size_t)t * p.d + k] << 16) : 0.f;
   uint32_t code[2], sc[2];
-  split_planes<2>(v, code, sc);
+  tc::split_planes<2>(v, code, sc);
   uint8_t* qh = p.xq + (size_t)t * 2 * p.d64 + k;
   qh[0] = (uint8_t)code[0];
   qh[p.d64] = (uint8_t)code[1];
@@ -673,9 +583,9 @@ __global__ void __launch_bounds__(256) prep_xq_kernel(FwdParams p) {
 
 cudaError_t launch_repack_tc(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                              size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
-                             bool down, cudaStream_t stream) {
+                             bool down, int* err_flag, cudaStream_t stream) {
   repack_tc_kernel<<<1024, 256, 0, stream>>>(codes, scales, n_exp, d, f, canon_code_stride, canon_scale_stride, out,
-                                             out_stride, down);
+                                             out_stride, down, err_flag);
   return cudaGetLastError();
 }
 
@@ -711,9 +621,9 @@ size_t tc_gemm_smem_bytes(int E, bool down) {
 
 // The weight copy as a 2-D tensor of "16 x U4, 16-byte aligned" elements:
 // rows of 128 codes (64 bytes: one core matrix of 8 rows x 16 codes), so that
-// a box of 256 rows is the 2 x 8,192 code bytes of a tile pair's block,
-// widened on the way into shared memory.
-bool encode_tc_weight_map(const void* base, size_t bytes, void* map) {
+// a box of 256 rows is the 2 x 8,192 code bytes of a tile pair's block and a
+// box of 128 rows one tile's, widened on the way into shared memory.
+bool encode_tc_weight_map(const void* base, size_t bytes, void* map, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -725,7 +635,8 @@ bool encode_tc_weight_map(const void* base, size_t bytes, void* map) {
   }
   if (bytes % 64 != 0 || bytes / 64 >= (1ull << 31)) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)(bytes / 64)}, strides[1] = {64};
-  const cuuint32_t box[2] = {128, 256}, es[2] = {1, 1};
+  if (box_rows != 128 && box_rows != 256) return false;
+  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows}, es[2] = {1, 1};
   return encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims,
                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -62,5 +62,7 @@ def test_null_context_calls(lib):
 
 def test_mma_probe_rejects_bad_arguments_without_a_gpu(lib):
     tf = ctypes.c_double()
-    assert lib.moe_probe_mma_rate(0, 0, ctypes.byref(tf), None) == -1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_mma_rate(0, 0, 192, ctypes.byref(tf), None) == -1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_mma_rate(0, 1000, 24, ctypes.byref(tf), None) == -1  # N not a multiple of 16
+    assert lib.moe_probe_mma_rate(0, 1000, 256, ctypes.byref(tf), None) == -1  # N above the probed widths
     assert b"mmas_per_sm" in lib.moe_probe_error()

@@ -57,12 +57,18 @@ SMALL_SHAPES = [
 
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
 @pytest.mark.parametrize("out_f32", [False, True])
-@pytest.mark.parametrize("path", ["fused", "general", "general-tc"])
+@pytest.mark.parametrize("path", ["fused-tc", "fused", "general", "general-tc"])
 def test_small_shapes(m, shape, out_f32, path):
+    """fused-tc: the single-launch tcgen05 kernel (the default for T <= 16); fused: the single-launch
+    mma.sync kernel (MOE_FLAG_NO_TC); general / general-tc: the multi-kernel path with either GEMM."""
     T, d, F, E, k, S, z = shape
     wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
-    flags = {"fused": m.MOE_FLAG_NO_TC, "general": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC,
+    flags = {"fused-tc": 0, "fused": m.MOE_FLAG_NO_TC, "general": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC,
              "general-tc": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_TC_GATEUP}[path]
+    if path.startswith("fused"):
+        lay = make_layer(m, wl, synth.gen_layer(wl, 17), flags=flags)
+        assert m.moe_launches_per_forward(lay.ctx, T) == 1, "expected the single-launch path"
+        lay.close()
     _parity(m, wl, synth.gen_layer(wl, 17), out_f32=out_f32, flags=flags)
 
 
@@ -74,16 +80,18 @@ def test_wide_scale_exponent_range(m, flags):
 
 
 def test_path_selection(m):
-    """Fused kernel up to 16 (token, expert) pairs, the multi-kernel tcgen05 path above; without the
-    tcgen05 copy (MOE_FLAG_NO_TC) the fused kernel serves every T <= 16."""
+    """Default contexts: one launch (the fused tcgen05 kernel) up to 16 tokens, the multi-kernel tcgen05
+    path above; MOE_FLAG_NO_TC: the fused mma.sync kernel up to 16 tokens, register-decode GEMMs above."""
     wl = synth.WORKLOADS["decode"]  # k = 4
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024))
     assert m.moe_launches_per_forward(lay.ctx, 1) == 1 and m.moe_forward_phases(lay.ctx, 1) == ["layer"]
     assert m.moe_launches_per_forward(lay.ctx, 4) == 1
+    assert m.moe_launches_per_forward(lay.ctx, 16) == 1
     # router (one launch up to 32 tokens, fp32 pass + top-k above), bucket, x planes, x panels, 2 GEMMs, combine
-    assert m.moe_launches_per_forward(lay.ctx, 5) == 7
+    assert m.moe_launches_per_forward(lay.ctx, 17) == 7
     assert m.moe_launches_per_forward(lay.ctx, 32) == 7
     assert m.moe_launches_per_forward(lay.ctx, 33) == 8
+    assert m.moe_forward_phases(lay.ctx, 33) == ["route", "panels", "gateup", "down", "combine"]
     lay.close()
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024, flags=m.MOE_FLAG_NO_TC))
     assert m.moe_launches_per_forward(lay.ctx, 16) == 1
@@ -119,15 +127,15 @@ def test_every_token_count_up_to_16(m, flags):
     layer.close()
 
 
-@pytest.mark.parametrize("cls", ["fused", "tcgen05"])
+@pytest.mark.parametrize("cls", ["single", "batch", "mma.sync"])
 def test_batch_invariance(m, cls):
-    """Within a path class, a token's output bits do not depend on the other tokens of its call:
-    fused (T * k <= 16): a batch of 4 vs single tokens; tcgen05 (T * k > 16): a batch of 16 vs
-    sub-batches of 5 and 11 tokens."""
+    """Within a path, a token's output bits do not depend on the other tokens of its call: the fused
+    tcgen05 kernel with a batch of 4 vs single tokens ("single") and a batch of 16 vs sub-batches of 5
+    and 11 ("batch"); the fused mma.sync kernel (MOE_FLAG_NO_TC) with a batch of 4 vs single tokens."""
     wl = synth.WORKLOADS["tiny"].with_(T=16, E=32, k=4)
     L = synth.gen_layer(wl, 5)
-    layer = make_layer(m, wl, L, t_max=16, out_f32=True)
-    if cls == "fused":
+    layer = make_layer(m, wl, L, t_max=16, out_f32=True, flags=m.MOE_FLAG_NO_TC if cls == "mma.sync" else 0)
+    if cls != "batch":
         full = run_gpu(m, layer, L["x"][:4].copy(), out_f32=True)
         for t in (0, 3):
             one = run_gpu(m, layer, L["x"][t:t + 1].copy(), out_f32=True)
@@ -226,6 +234,20 @@ def test_skewed_all_tokens_one_expert(m):
     b[11] = 100.0
     b[3] = 90.0
     _parity(m, wl, dict(L, bias=b))
+
+
+def test_default_context_stores_one_copy(m):
+    """A default context keeps its experts once, in the tcgen05 layout (tile padding only: the 13,219,200-byte
+    expert of the decode shapes takes at most 7 % more); MOE_FLAG_NO_TC keeps the packed layout, exactly the
+    canonical size."""
+    wl = synth.WORKLOADS["decode"]
+    for t_max in (1, 16, 1024):
+        lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=t_max))
+        assert wl.E * wl.expert_bytes() <= lay.weight_bytes() <= 1.07 * wl.E * wl.expert_bytes()
+        lay.close()
+    lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=16, flags=m.MOE_FLAG_NO_TC))
+    assert lay.weight_bytes() == wl.E * wl.expert_bytes()
+    lay.close()
 
 
 def test_k_equals_E(m):
