@@ -72,15 +72,16 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *   with MOE_ERR_TIMEOUT in the status word (its output is then undefined).
  * MOE_FLAG_GENERAL_PATH makes every forward take the multi-kernel path (for
  *   testing both paths on the same shapes).
- * Weights and paths. By default the context stores its experts once, in the
- *   layout of the block-scaled tcgen05 MMAs (MXFP4 weights x MXFP8 planes of x
- *   and of h; made at load time, lossless), whenever the shared-memory tables
- *   fit (n_experts up to 512): forwards with T <= 16 run as one launch
- *   (the fused tcgen05 kernel), larger T on the multi-kernel path with the
- *   tcgen05 GEMMs. MOE_FLAG_TC_GATEUP makes that layout mandatory (an error if
- *   the tables do not fit); MOE_FLAG_NO_TC stores the packed tile layout
- *   instead, for the mma.sync kernels: the fused mma.sync kernel for T <= 16,
- *   the register-decode tensor-core GEMMs above. Within each path a token's
+ * Weights and paths. A context stores its experts once (made at load time,
+ *   lossless). If t_max * top_k > 16 and the shared-memory tables fit
+ *   (n_experts up to 512) the layout is that of the block-scaled tcgen05 MMAs
+ *   (MXFP4 weights x MXFP8 planes of x and of h): forwards with T <= 16 run as
+ *   one launch (the fused tcgen05 kernel), larger T on the multi-kernel path
+ *   with the tcgen05 GEMMs. Otherwise (every call a few tokens) it is the
+ *   packed tile layout of the fused mma.sync kernel, which serves T <= 16 (and
+ *   the register-decode tensor-core GEMMs larger T). MOE_FLAG_TC_GATEUP forces
+ *   the tcgen05 layout (an error if the tables do not fit); MOE_FLAG_NO_TC
+ *   forces the packed one. Within each path a token's
  *   output bits do not depend on the other tokens of its call; results agree
  *   within the bf16 and fp32 tolerances across paths. */
 enum { MOE_FLAG_TEST_FORCE_TIMEOUT = 1u, MOE_FLAG_GENERAL_PATH = 2u, MOE_FLAG_TC_GATEUP = 4u, MOE_FLAG_NO_TC = 8u };

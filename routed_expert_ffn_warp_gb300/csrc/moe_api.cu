@@ -30,8 +30,8 @@ struct moe_ctx {
   size_t tcwd_stride = 0;
   CUtensorMap tmap_gu{};  // tensor maps the tcgen05 kernels load tcw / tcwd through (tile pairs)
   CUtensorMap tmap_dn{};
-  CUtensorMap tmap_gu1{};  // the same with single-tile boxes
-  CUtensorMap tmap_dn1{};
+  CUtensorMap tmap_gu3{};  // 3-D maps whose box is a whole tile-pair block (codes + scale bytes)
+  CUtensorMap tmap_dn3{};
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
@@ -132,10 +132,13 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete ctx;
     return fail(nullptr, MOE_ERR_INVALID_ARG, "too many experts for the tcgen05 GEMM's shared-memory tables");
   }
-  // The block-scaled tcgen05 kernels (and their weight copies, the only copy such
-  // a context keeps) serve every forward unless asked not to or their tables do
-  // not fit; otherwise the packed copy serves the mma.sync kernels.
-  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) || (!(c.flags & MOE_FLAG_NO_TC) && tc_fits);
+  // One weight copy per context. Contexts whose calls can reach more than
+  // kFusedMaxPairs (token, expert) pairs keep the tcgen05 block layout (the fused
+  // tcgen05 kernel for T <= 16, the tcgen05 GEMMs above); smaller ones -- every
+  // call a few tokens, where the fused mma.sync kernel is the faster -- keep the
+  // packed tiles. MOE_FLAG_TC_GATEUP / MOE_FLAG_NO_TC force either.
+  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
+                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs);
   if (!tc) ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
@@ -195,8 +198,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   }
   if (tc && (!moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu, 256) ||
              !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn, 256) ||
-             !moe::encode_tc_weight_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu1, 128) ||
-             !moe::encode_tc_weight_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn1, 128))) {
+             !moe::encode_tc_block_map(ctx->tcw, ctx->tcw_bytes, &ctx->tmap_gu3) ||
+             !moe::encode_tc_block_map(ctx->tcwd, ctx->tcwd_bytes, &ctx->tmap_dn3))) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_CUDA, "cuTensorMapEncodeTiled refused the tcgen05 weight copy");
   }
@@ -231,8 +234,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.hpanel = reinterpret_cast<uint8_t*>(w + o_hpanel);
   p.tmap_gu = &ctx->tmap_gu;
   p.tmap_dn = &ctx->tmap_dn;
-  p.tmap_gu1 = &ctx->tmap_gu1;
-  p.tmap_dn1 = &ctx->tmap_dn1;
+  p.tmap_gu3 = &ctx->tmap_gu3;
+  p.tmap_dn3 = &ctx->tmap_dn3;
   p.panel_prefix = reinterpret_cast<int32_t*>(w + o_pp);
   p.xq = reinterpret_cast<uint8_t*>(w + o_xq);
   p.xqs = reinterpret_cast<uint8_t*>(w + o_xqs);

@@ -55,14 +55,21 @@ namespace {
 using namespace dev;
 
 constexpr int kAOp = 128 * kTcStepK;    // one widened E2M1 M tile of a K step: 16 bytes per 16 codes
-constexpr int kSfaOff = 2 * kAOp;       // a stage's A scale bytes: 512 per M tile
+constexpr int kSfaOff = 2 * kAOp;       // a stage's A scale bytes as stored: 512 per M tile, [lane][4 words]
 constexpr int kBOff = 2 * kAOp + 1024;  // a stage's activation slot
 constexpr int kAccCols = 64;            // TMEM columns of one accumulator (N <= 64)
-constexpr int kSfCol0 = 256;            // scale-factor set of stage s at kSfCol0 + 16 s: SFA tile 0 / 1 at +0 / +4, SFB +8
+// Scale-factor set of stage s at kSfCol0 + 32 s: SFA of M tile 0 / 1 at +0 / +8,
+// each MMA lane's own copy of SFB at +16 / +24.
+constexpr int kSfCol0 = 256;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kProducerWarp = 0, kActWarp = 1, kMmaWarp0 = 2, kSfWarp0 = 4, kEpiWarp0 = 8, kEpiThreads = 256;
+constexpr int kProducerWarp = 0, kActWarp = 1, kMmaWarp0 = 2, kEpiWarp0 = 8, kEpiThreads = 256;
 constexpr int kHxTok = kDecodeMaxT;     // tokens the gate/up epilogue exchange holds
+// Work items whose whole weight range (K steps x 17,408 bytes, contiguous) the
+// producer starts towards L2 ahead of its tensor copies, one prefetch per
+// item: a CTA's tensor copies alone keep too few bytes in flight to cover HBM
+// latency, while HBM fills L2 at its full rate for every CTA at once.
+constexpr int kPfItems = 2;
 
 __host__ __device__ inline int npad8(int n) { return n <= 8 ? 8 : (n + 7) & ~7; }
 __host__ __device__ inline int tc_stage_bytes(int bslot) { return (kBOff + bslot + 1023) / 1024 * 1024; }
@@ -72,8 +79,8 @@ struct TcItem {
   int down;   // 0: gate/up, 1: down
   int slot;   // slot of the work list
   int e, f;   // expert (E = the shared expert) and its ffn
-  int tile;   // gate/up: pair p (M tiles 2p, 2p + 1); down: 128-row tile of d
-  int nt;     // M tiles (gate/up 1 or 2, down 1)
+  int tile;   // tile pair: gate/up M tiles 2p, 2p + 1 (f in [128 p, 128 p + 128)); down rows [256 p, 256 p + 256) of d
+  int nt;     // M tiles of the pair holding rows (1 for the last pair of an odd tile count)
   int nks;    // K steps of 128
   int q0, n;  // the slot's rows (pairs in expert order, or the shared expert's tokens)
   int nb;     // B rows: gate/up 2 npad8(T) (x planes of every token), down 4 npad8(n)
@@ -87,6 +94,7 @@ __device__ __forceinline__ int tc_token_of(const FwdParams& f, const Shared& s, 
 struct TcWork {
   int nr, nsl;      // routed slots, all slots
   int gpF, gpS;     // gate/up units per routed slot and of the shared slot
+  int dpp;          // down units per slot (tile pairs of d)
   int ngu, ndn;     // this CTA's gate/up and down items
 };
 
@@ -96,9 +104,10 @@ __device__ __forceinline__ TcWork tc_work(const FwdParams& f, const Shared& s) {
   w.nsl = s.misc[1];
   w.gpF = tc_gu_pairs(f.F);
   w.gpS = f.S > 0 ? tc_gu_pairs(f.S) : 0;
+  w.dpp = tc_dn_pairs(f.d);
   const int G = gridDim.x, b = blockIdx.x;
   const int nug = w.nr * w.gpF + (w.nsl > w.nr ? w.gpS : 0);
-  const int nud = w.nsl * tc_dtiles(f.d);
+  const int nud = w.nsl * w.dpp;
   const int bd = G - 1 - b;
   w.ngu = nug > b ? (nug - b + G - 1) / G : 0;
   w.ndn = nud > bd ? (nud - bd + G - 1) / G : 0;
@@ -119,18 +128,17 @@ __device__ __forceinline__ TcItem tc_item(const FwdParams& f, const Shared& s, c
       it.tile = u - w.nr * w.gpF;
     }
   } else {
-    const int dt = tc_dtiles(f.d);
     const int v = (G - 1 - b) + (i - w.ngu) * G;
     it.down = 1;
-    it.slot = v / dt;
-    it.tile = v - it.slot * dt;
+    it.slot = v / w.dpp;
+    it.tile = v - it.slot * w.dpp;
   }
   it.e = s.slot_e[it.slot];
   it.f = it.e == f.E ? f.S : f.F;
   it.q0 = s.slot_q0[it.slot];
   it.n = s.slot_n[it.slot];
   if (it.down) {
-    it.nt = 1;
+    it.nt = min(2, tc_dtiles(f.d) - 2 * it.tile);
     it.nks = tc_ksteps(it.f);
     it.nb = 4 * npad8(it.n);
   } else {
@@ -148,20 +156,26 @@ __device__ __forceinline__ int bop_off(int n, int k) { return ((n >> 3) * 8 + (k
 // one 512-byte block of words [lane l][r] for rows 32 r + l (nb <= 128).
 __device__ __forceinline__ int bsf_off(int nb, int n, int kb) { return nb * 128 + 16 * (n & 31) + 4 * (n >> 5) + kb; }
 
-// Bounded poll (limit ns) of a launch-tagged flag (acquire); false if it gave up.
-__device__ bool tc_poll_flag(const unsigned* flag, unsigned want, long long limit, const DecParams& p,
-                             volatile int* abort) {
-  if (ld_acquire_u(flag) == want) return true;
+// Bounded poll (limit ns) by a whole warp of n launch-tagged flags (acquire):
+// every flag in one round of loads (lane l takes flags l, l + 32, ...), so an
+// item pays one round trip for all of its K steps, not one per step. False if
+// it gave up. Every lane returns the same verdict.
+__device__ bool tc_poll_flags_warp(const unsigned* flags, int n, unsigned want, long long limit, const DecParams& p,
+                                   volatile int* abort) {
+  const int lane = threadIdx.x & 31;
   const uint64_t t0 = globaltimer();
-  while (ld_acquire_u(flag) != want) {
-    if (*abort) return false;
-    if (timed_out(t0, limit)) {
-      give_up(abort, p.f.status);
-      return false;
+  while (true) {
+    bool mine = true;
+    for (int k = lane; k < n; k += 32) mine = (ld_acquire_u(flags + k) == want) && mine;
+    if (__all_sync(0xffffffffu, mine)) return true;
+    int stop = *abort ? 1 : 0;
+    if (!stop && timed_out(t0, limit)) {
+      if (lane == 0) give_up(abort, p.f.status);
+      stop = 1;
     }
-    __nanosleep(32);
+    if (__any_sync(0xffffffffu, stop)) return false;
+    __nanosleep(64);
   }
-  return true;
 }
 
 // Phase A tail: K steps blockIdx.x, + G, ... of x as two E4M3 planes with
@@ -215,11 +229,11 @@ __device__ void tc_routing(const DecParams& p, const Shared& s, unsigned seq, vo
   __syncthreads();
 }
 
-// y rows [128 dt, 128 dt + 128) of every token: sum_j g[t,j] part(pair (t, j)) in
+// y rows [256 dp, 256 dp + 256) of every token: sum_j g[t,j] part(pair (t, j)) in
 // slot order, then the shared expert, one rounding. The 256 epilogue threads.
-__device__ void tc_combine_tile(const FwdParams& f, const Shared& s, int dt, int et) {
-  for (int o = et; o < f.T * 128; o += kEpiThreads) {
-    const int t = o >> 7, row = 128 * dt + (o & 127);
+__device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int et) {
+  for (int o = et; o < f.T * 256; o += kEpiThreads) {
+    const int t = o >> 8, row = 256 * dp + (o & 255);
     if (row >= f.d) continue;
     float y = 0.f;
     for (int j = 0; j < f.k; ++j)
@@ -297,18 +311,20 @@ __device__ void tc_gateup_epilogue(const TcLayerParams& P, const Shared& s, cons
   if (et == 0) st_release_u(P.hflag + (size_t)it.slot * P.hp_ksteps + it.tile, seq);
 }
 
-// Down epilogue of one unit: the fp32 rows part[q0 + j][128 tile + r] (the sum of
-// the four planes' columns), then the row tile's counter; the CTA that brings
-// it to the slot count combines the tile.
+// Down epilogue of one unit (a pair of 128-row tiles of d): the fp32 rows
+// part[q0 + j][128 (2 tile + t) + r] (the sum of the four planes' columns),
+// then the pair's counter; the CTA that brings it to the slot count combines
+// the pair's rows.
 __device__ void tc_down_epilogue(const TcLayerParams& P, const Shared& s, const TcItem& it, uint32_t trow, int acc,
                                  uint64_t* accempty, int* dcnt, int* ctl, int nsl) {
   const FwdParams& f = P.d.f;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3, eg = (warp - kEpiWarp0) >> 2, et = threadIdx.x - kEpiWarp0 * 32;
-  const int npd = it.nb / 4, row = 128 * it.tile + 32 * qd + lane;
-  if (eg == 0) {  // npad8(n) <= 16 columns per plane
+  const int npd = it.nb / 4;
+  if (eg < it.nt) {  // warps 8-11 read tile 0, warps 12-15 tile 1; npad8(n) <= 16 columns per plane
+    const int t = eg, row = 128 * (2 * it.tile + t) + 32 * qd + lane;
     float v[16], w[16];
-    const uint32_t dcol = trow + kAccCols * (2 * acc);
+    const uint32_t dcol = trow + kAccCols * (2 * acc + t);
     tc::ld16(dcol, v);
 #pragma unroll
     for (int pl = 1; pl < 4; ++pl) {
@@ -330,7 +346,7 @@ __device__ void tc_down_epilogue(const TcLayerParams& P, const Shared& s, const 
   named_bar(1, kEpiThreads);
   if (ctl[1]) {
     __threadfence();
-    tc_combine_tile(f, s, it.tile, et);
+    tc_combine_rows(f, s, it.tile, et);
   }
 }
 
@@ -347,7 +363,7 @@ __device__ __forceinline__ Shared tc_carve(uint8_t* sm, const TcLayerParams& P) 
 
 __global__ void __launch_bounds__(kThreads, 1)
     layer_tc_kernel(const TcLayerParams P, const __grid_constant__ CUtensorMap gu2,
-                    const __grid_constant__ CUtensorMap gu1, const __grid_constant__ CUtensorMap dn1) {
+                    const __grid_constant__ CUtensorMap dn2) {
   extern __shared__ __align__(1024) uint8_t sm[];
   const DecParams& p = P.d;
   const FwdParams& f = p.f;
@@ -370,25 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (blockIdx.x == 0)
     for (int i = tid; i < dtiles; i += kThreads) P.dcnt[(size_t)((seq + 1) & 1) * dtiles + i] = 0;
   int* dcnt = P.dcnt + (size_t)(seq & 1) * dtiles;
-  stage_x(p, s);
-  __syncthreads();
-  router(p, s, seq);
-  publish_x_planes(P, s, seq);
-  tc_routing(p, s, seq, abort);
-  pdl_launch_dependents();
-
-  // ---------------------------------------------------------------- expert units on the tensor cores
-  uint8_t* ring = sm + P.off_ring;
+  // barriers and tensor memory now (the preceding grid has finished, so no other CTA holds this SM's TMEM)
   const int S = P.stages, sbytes = tc_stage_bytes(P.bslot);
-  // the tensor copies write the first 8 bytes of every 16-byte operand row; the other 8 are zero
-  for (int c = tid; c < S * 2 * (kAOp / 16); c += kThreads)
-    *reinterpret_cast<uint2*>(ring + (size_t)(c / (2 * (kAOp / 16))) * sbytes + (size_t)(c % (2 * (kAOp / 16))) * 16 +
-                              8) = make_uint2(0u, 0u);
-  tc::fence_proxy_async();
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + P.off_bars);  // both operands of the stage landed
   uint64_t* empty = full + kMaxStages;     // both MMA lanes' reads of the stage completed
-  uint64_t* ready = empty + kMaxStages;    // the stage's scale factors are in TMEM (4 warps x 32)
-  uint64_t* accfull = ready + kMaxStages;  // [2] both MMA lanes' part of the buffer's unit completed
+  uint64_t* accfull = empty + kMaxStages;  // [2] both MMA lanes' part of the buffer's unit completed
   uint64_t* accempty = accfull + 2;        // [2] the epilogue read the buffer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   int* ctl = s.ctl;
@@ -396,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 2);
       mbar_init(&empty[i], 2);
-      mbar_init(&ready[i], 128);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accfull[a], 2);
@@ -405,19 +406,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) tc::alloc(tslot, kTmemCols);
+  stage_x(p, s);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
+  router(p, s, seq);
+  publish_x_planes(P, s, seq);
+  __syncthreads();  // every read of the router rows and the staged x in the ring is done
+  // the tensor copies write the first 8 bytes of every 16-byte operand row; the other 8 are zero
+  uint8_t* ring = sm + P.off_ring;
+  for (int c = tid; c < S * 2 * (kAOp / 16); c += kThreads)
+    *reinterpret_cast<uint2*>(ring + (size_t)(c / (2 * (kAOp / 16))) * sbytes + (size_t)(c % (2 * (kAOp / 16))) * 16 +
+                              8) = make_uint2(0u, 0u);
+  tc::fence_proxy_async();
+  tc_routing(p, s, seq, abort);  // ends with a CTA barrier
+  pdl_launch_dependents();
+
+  // ---------------------------------------------------------------- expert units on the tensor cores
   const TcWork wk = tc_work(f, s);
   const int nit = wk.ngu + wk.ndn;
+  // Every role but the MMA lanes waits with the suspending try_wait: a warp spinning on a barrier takes
+  // issue slots from the MMA lane that shares its scheduler.
 
   if (warp == kProducerWarp) {
-    if (lane == 0) {  // weight tiles: a tensor copy of the codes (widened), a bulk copy of the scale bytes
+    if (lane == 0) {  // weight blocks: a tensor copy of both tiles' codes (widened) and a bulk copy of their scales
+      auto prefetch_item = [&](int i) {
+        const TcItem it = tc_item(f, s, wk, i);
+        const uint8_t* base = (it.down ? f.tcwd + (size_t)it.e * f.tcwd_stride : f.tcw + (size_t)it.e * f.tcw_stride) +
+                              (size_t)it.tile * it.nks * kTcPairBytes;
+        prefetch_l2(base, (uint32_t)(it.nks * kTcPairBytes));
+      };
+      for (int i = 0; i < nit && i < kPfItems; ++i) prefetch_item(i);
       int j = 0;
       bool ok = true;
       for (int i = 0; i < nit && ok; ++i) {
         const TcItem it = tc_item(f, s, wk, i);
+        if (i + kPfItems < nit) prefetch_item(i + kPfItems);
+        const size_t stride = it.down ? f.tcwd_stride : f.tcw_stride;  // a multiple of kTcPairBytes
+        const uint8_t* w0 = (it.down ? f.tcwd : f.tcw) + (size_t)it.e * stride + (size_t)it.tile * it.nks * kTcPairBytes;
+        const int y0 = (int)((size_t)it.e * (stride / 64) + (size_t)it.tile * it.nks * (kTcPairBytes / 64));
         for (int ks = 0; ks < it.nks; ++ks, ++j) {
           const int st = j % S;
           if (j >= S && !tc::bounded_wait_sleep(&empty[st], (uint32_t)((j / S - 1) & 1), f.status, abort)) {
@@ -425,56 +453,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sb = ring + (size_t)st * sbytes;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(it.nt * (kTcCodeBytes + 512)));
-          if (!it.down) {
-            const size_t blk = (size_t)it.tile * it.nks + ks;
-            const int y = (int)((size_t)it.e * (f.tcw_stride / 64) + blk * (kTcPairBytes / 64));
-            tc::tma_load_2d(sb, it.nt == 2 ? &gu2 : &gu1, 0, y, &full[st]);
-            bulk_g2s(sb + kSfaOff, f.tcw + (size_t)it.e * f.tcw_stride + blk * kTcPairBytes + 2 * kTcCodeBytes,
-                     (uint32_t)(512 * it.nt), &full[st]);
-          } else {
-            const int tt = it.tile & 1;
-            const size_t blk = (size_t)(it.tile >> 1) * it.nks + ks;
-            const int y = (int)((size_t)it.e * (f.tcwd_stride / 64) + blk * (kTcPairBytes / 64) + 128 * tt);
-            tc::tma_load_2d(sb, &dn1, 0, y, &full[st]);
-            bulk_g2s(sb + kSfaOff,
-                     f.tcwd + (size_t)it.e * f.tcwd_stride + blk * kTcPairBytes + 2 * kTcCodeBytes + 512 * tt, 512,
-                     &full[st]);
-          }
+          // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
+          mbar_arrive_expect_tx(&full[st], (uint32_t)kTcPairBytes);
+          tc::tma_load_2d(sb, it.down ? &dn2 : &gu2, 0, y0 + ks * (kTcPairBytes / 64), &full[st]);
+          bulk_g2s(sb + kSfaOff, w0 + (size_t)ks * kTcPairBytes + 2 * kTcCodeBytes, 1024, &full[st]);
         }
       }
     }
   } else if (warp == kActWarp) {
-    if (lane == 0) {  // activation steps: x planes (gate/up) or the slot's h planes (down), once published
-      int j = 0;
-      bool ok = true;
-      for (int i = 0; i < nit && ok; ++i) {
-        const TcItem it = tc_item(f, s, wk, i);
-        for (int ks = 0; ks < it.nks; ++ks, ++j) {
-          const int st = j % S;
-          if (j >= S && !tc::bounded_wait_sleep(&empty[st], (uint32_t)((j / S - 1) & 1), f.status, abort)) {
-            ok = false;
+    // activation steps: x planes (gate/up) or the slot's h planes (down). The whole warp checks that
+    // every K step of the item is published, then lane 0 copies them stage by stage.
+    int j = 0;
+    bool ok = true;
+    for (int i = 0; i < nit && ok; ++i) {
+      const TcItem it = tc_item(f, s, wk, i);
+      const unsigned* flags = it.down ? P.hflag + (size_t)it.slot * P.hp_ksteps : P.xflag;
+      // the timeout test makes the h steps wait for a number no launch writes
+      const bool test = it.down && p.test_extra > 0;
+      if (!tc_poll_flags_warp(flags, it.nks, test ? seq + (unsigned)p.test_extra : seq,
+                              test ? p.test_wait_ns : p.wait_ns, p, abort)) {
+        ok = false;
+        break;
+      }
+      int okl = 1;
+      if (lane == 0) {
+        fence_proxy_async_global();  // the producers' generic stores -> these async-proxy reads
+        const uint32_t bytes = (uint32_t)(it.nb * 128 + 512);
+        for (int ks = 0; ks < it.nks; ++ks) {
+          const int jj = j + ks, st = jj % S;
+          if (jj >= S && !tc::bounded_wait_sleep(&empty[st], (uint32_t)((jj / S - 1) & 1), f.status, abort)) {
+            okl = 0;
             break;
           }
-          const size_t hs = (size_t)it.slot * P.hp_ksteps + ks;
-          const unsigned* flag = it.down ? P.hflag + hs : P.xflag + ks;
-          const uint8_t* src = it.down ? P.hpanel + hs * P.hp_step : P.xplane + (size_t)ks * P.xp_step;
-          // the timeout test makes the h steps wait for a number no launch writes
-          const bool test = it.down && p.test_extra > 0;
-          if (!tc_poll_flag(flag, test ? seq + (unsigned)p.test_extra : seq, test ? p.test_wait_ns : p.wait_ns, p,
-                            abort)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
-          const uint32_t bytes = (uint32_t)(it.nb * 128 + 512);
+          const uint8_t* src = it.down ? P.hpanel + ((size_t)it.slot * P.hp_ksteps + ks) * P.hp_step
+                                       : P.xplane + (size_t)ks * P.xp_step;
           mbar_arrive_expect_tx(&full[st], bytes);
           bulk_g2s(ring + (size_t)st * sbytes + kBOff, src, bytes, &full[st]);
         }
       }
+      ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+      j += it.nks;
     }
   } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + 2) {
     if (lane == 0) {  // MMA lane t: M tile t of every unit, into accumulator buffer i % 2
+      // per step: its tile's scale factors and its own copy of the activation's to TMEM (tcgen05.cp),
+      // then the four K = 32 MMAs -- all from this thread, so they run in this order
       const int t = warp - kMmaWarp0;
       int j = 0;
       bool ok = true;
@@ -484,60 +507,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 2 && !tc::bounded_wait(&accempty[acc], (uint32_t)((i / 2 - 1) & 1), f.status, abort)) break;
         tc::fence_after();
         const uint32_t d = tmem + kAccCols * (2 * acc + t);
+        uint32_t idesc[4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) idesc[kb] = tc::idesc_mxf4_mxf8(128, it.nb, kb, kb);
         for (int ks = 0; ks < it.nks; ++ks, ++j) {
           const int st = j % S;
           // every lane takes part in every step's hand-off, with or without MMAs
-          if (!tc::bounded_wait(&ready[st], (uint32_t)((j / S) & 1), f.status, abort)) {
+          if (!tc::bounded_wait(&full[st], (uint32_t)((j / S) & 1), f.status, abort)) {
             ok = false;
             break;
           }
           tc::fence_after();
           if (t < it.nt) {
-            const uint8_t* ab = ring + (size_t)st * sbytes + (size_t)t * kAOp;
-            const uint8_t* bb = ring + (size_t)st * sbytes + kBOff;
-            const uint32_t sf = tmem + kSfCol0 + 16 * st;
+            const uint8_t* sb = ring + (size_t)st * sbytes;
+            const uint32_t sfa = tmem + kSfCol0 + 32 * st + 8 * t, sfb = tmem + kSfCol0 + 32 * st + 16 + 8 * t;
+            tc::cp_32x128b_x4(sfa, tc::smem_desc(sb + kSfaOff + 512 * t, 128, 128));
+            tc::cp_32x128b_x4(sfb, tc::smem_desc(sb + kBOff + it.nb * 128, 128, 128));
+            const uint64_t ad = tc::smem_desc(sb + (size_t)t * kAOp, 128, 8 * 128);
+            const uint64_t bd = tc::smem_desc(sb + kBOff, 128, 8 * 128);
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-              const uint64_t ad = tc::smem_desc(ab + 2 * kb * 128, 128, 8 * 128);
-              const uint64_t bd = tc::smem_desc(bb + 2 * kb * 128, 128, 8 * 128);
-              tc::mma_mxf4_mxf8(d, ad, bd, tc::idesc_mxf4_mxf8(128, it.nb, kb, kb), sf + 4 * t, sf + 8,
-                                (ks > 0 || kb > 0) ? 1u : 0u);
-            }
+            for (int kb = 0; kb < 4; ++kb)  // K block kb starts 2 kb core matrices on (256 bytes, 16 descriptor units)
+              tc::mma_mxf4_mxf8(d, ad + 16 * kb, bd + 16 * kb, idesc[kb], sfa, sfb, (ks > 0 || kb > 0) ? 1u : 0u);
           }
           tc::commit(&empty[st]);
         }
         if (!ok) break;
         tc::commit(&accfull[acc]);
-      }
-    }
-  } else if (warp >= kSfWarp0 && warp < kSfWarp0 + 4) {
-    // scale factors of every stage into TMEM set st, in the warp's lane quadrant
-    // (each quadrant holds the same copy): SFA of M tile 0 / 1 to +0 / +4, SFB to +8
-    const uint32_t qbase = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol0;
-    int j = 0;
-    bool ok = true;
-    for (int i = 0; i < nit && ok; ++i) {
-      const TcItem it = tc_item(f, s, wk, i);
-      for (int ks = 0; ks < it.nks; ++ks, ++j) {
-        const int st = j % S;
-        // the warp's lanes leave together (one lane's verdict), so tcgen05.st stays warp-uniform
-        ok = __shfl_sync(0xffffffffu, tc::bounded_wait(&full[st], (uint32_t)((j / S) & 1), f.status, abort) ? 1 : 0,
-                         0) != 0;
-        if (!ok) break;
-        const uint8_t* sb = ring + (size_t)st * sbytes;
-        const uint4 a0 = *reinterpret_cast<const uint4*>(sb + kSfaOff + 16 * lane);
-        const uint4 b0 = *reinterpret_cast<const uint4*>(sb + kBOff + it.nb * 128 + 16 * lane);
-        tc::fence_after();
-        const uint32_t sf = qbase + 16 * st;
-        tc::st4(sf, a0.x, a0.y, a0.z, a0.w);
-        if (it.nt > 1) {
-          const uint4 a1 = *reinterpret_cast<const uint4*>(sb + kSfaOff + 512 + 16 * lane);
-          tc::st4(sf + 4, a1.x, a1.y, a1.z, a1.w);
-        }
-        tc::st4(sf + 8, b0.x, b0.y, b0.z, b0.w);
-        tc::wait_st();
-        tc::fence_before();
-        mbar_arrive(&ready[st]);
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -627,8 +622,7 @@ cudaError_t launch_tc_layer(const TcLayerParams& P, cudaStream_t stream, int num
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, layer_tc_kernel, P, *static_cast<const CUtensorMap*>(P.d.f.tmap_gu),
-                            *static_cast<const CUtensorMap*>(P.d.f.tmap_gu1),
-                            *static_cast<const CUtensorMap*>(P.d.f.tmap_dn1));
+                            *static_cast<const CUtensorMap*>(P.d.f.tmap_dn));
 }
 
 }  // namespace moe

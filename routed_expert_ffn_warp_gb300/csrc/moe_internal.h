@@ -128,8 +128,8 @@ struct FwdParams {
   uint8_t* hpanel;       // h panels of the down step (kTcPanelStepD per K step)
   const void* tmap_gu;   // host: CUtensorMap of tcw (see encode_tc_weight_map)
   const void* tmap_dn;   // host: CUtensorMap of tcwd
-  const void* tmap_gu1;  // host: CUtensorMap of tcw with a one-tile box (128 rows of 64 bytes)
-  const void* tmap_dn1;  // host: CUtensorMap of tcwd with a one-tile box
+  const void* tmap_gu3;  // host: 3-D CUtensorMap of tcw whose box is one tile-pair block (codes + scales)
+  const void* tmap_dn3;  // host: the same over tcwd
   int32_t* panel_prefix; // [E+2] first panel of each slot
   uint8_t* xq;           // E4M3 [t_max][2 planes][d64]: x = 2^sh hi + 2^sl lo per 32-element block
   uint8_t* xqs;          // E8M0 [t_max][2][xq_spitch]: the planes' block scales
@@ -164,10 +164,13 @@ struct FwdParams {
 constexpr int kDecodeMaxT = 16;
 // Copies of every published router logit word of the fused path (readers spread over them).
 constexpr int kLogitWordCopies = 8;
-// Calls with T * k above this many (token, expert) pairs take the multi-kernel
-// path with the tcgen05 GEMMs when the context has their weight copy: from
-// there on the block-scaled GEMMs beat the fused kernel (measured: T=8, k=8
-// and T=16, k=4 run 1.4-1.6x faster; T=1, k=4 runs faster fused).
+// Contexts whose t_max * k exceeds this many (token, expert) pairs keep the
+// tcgen05 weight layout (fused tcgen05 kernel for T <= 16, tcgen05 GEMMs
+// above); smaller ones keep the packed tiles of the fused mma.sync kernel.
+// Measured on the decode shapes: T=1, k=4 runs faster on the mma.sync kernel
+// (the tcgen05 MMA of a K=32 block costs about 100 cycles whatever N, which
+// caps a CTA near 40 GB/s of weights); T=8, k=8 and T=16, k=4 run faster on
+// the tcgen05 paths.
 constexpr int kFusedMaxPairs = 16;
 struct DecParams {
   FwdParams f;
@@ -276,6 +279,9 @@ size_t tc_gemm_smem_bytes(int E, bool down);
 // box_rows rows of 64 bytes (256: both tiles of a pair's K step; 128: one
 // tile); false if the driver refuses it.
 bool encode_tc_weight_map(const void* base, size_t bytes, void* map, int box_rows);
+// A 3-D tensor map over the same copy whose box is one whole tile-pair block
+// (codes and scale bytes of a K step: kTcPairBytes read, twice that written).
+bool encode_tc_block_map(const void* base, size_t bytes, void* map);
 
 // Launches a kernel of the forward chain with programmatic stream
 // serialization: it may be scheduled once the grid before it has passed its

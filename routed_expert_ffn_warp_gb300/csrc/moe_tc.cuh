@@ -60,6 +60,15 @@ __device__ __forceinline__ void mma_mxf4_mxf8(uint32_t d_tmem, uint64_t adesc, u
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// Copy a 512-byte block of shared memory, 32 rows of 16 bytes (8-row groups
+// 128 bytes apart: the descriptor smem_desc(block, 128, 128)), to TMEM lanes
+// 0..31 of 4 consecutive columns at taddr, replicated into all four lane
+// quadrants: the scale-factor layout of the block-scaled MMAs. It runs in
+// issue order with the MMAs the same thread issues after it; taddr's column
+// must be a multiple of 4.
+__device__ __forceinline__ void cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // TMA tiled load of the box at (x, y) of a 2-D tensor map (a kernel parameter
 // declared __grid_constant__) into this CTA's shared memory; completion is
 // signalled on `bar` as transaction bytes.
@@ -68,6 +77,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           smem_u32(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// The same for the box at (x, y, z) of a 3-D tensor map.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.

@@ -623,6 +623,28 @@ size_t tc_gemm_smem_bytes(int E, bool down) {
 // rows of 128 codes (64 bytes: one core matrix of 8 rows x 16 codes), so that
 // a box of 256 rows is the 2 x 8,192 code bytes of a tile pair's block and a
 // box of 128 rows one tile's, widened on the way into shared memory.
+// The same copy as a 3-D tensor (rows of 64 bytes, groups of 16 rows) with a
+// box of 128 x 16 x 17: the whole 17,408-byte block of a tile pair's K step --
+// both tiles' codes and their 1,024 scale bytes -- in one tensor copy, every
+// 8 bytes widened to 16 (the scale bytes too, which their readers skip over).
+bool encode_tc_block_map(const void* base, size_t bytes, void* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (bytes % kTcPairBytes != 0 || bytes / 1024 >= (1ull << 31)) return false;
+  const cuuint64_t dims[3] = {128, 16, (cuuint64_t)(bytes / 1024)}, strides[2] = {64, 1024};
+  const cuuint32_t box[3] = {128, 16, kTcPairBytes / 1024}, es[3] = {1, 1, 1};
+  return encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims,
+                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tc_weight_map(const void* base, size_t bytes, void* map, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {

@@ -59,11 +59,12 @@ SMALL_SHAPES = [
 @pytest.mark.parametrize("out_f32", [False, True])
 @pytest.mark.parametrize("path", ["fused-tc", "fused", "general", "general-tc"])
 def test_small_shapes(m, shape, out_f32, path):
-    """fused-tc: the single-launch tcgen05 kernel (the default for T <= 16); fused: the single-launch
+    """fused-tc: the single-launch tcgen05 kernel (MOE_FLAG_TC_GATEUP); fused: the single-launch
     mma.sync kernel (MOE_FLAG_NO_TC); general / general-tc: the multi-kernel path with either GEMM."""
     T, d, F, E, k, S, z = shape
     wl = synth.WORKLOADS["tiny"].with_(name="shape", number=9, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S, zipf_bias=z)
-    flags = {"fused-tc": 0, "fused": m.MOE_FLAG_NO_TC, "general": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC,
+    flags = {"fused-tc": m.MOE_FLAG_TC_GATEUP, "fused": m.MOE_FLAG_NO_TC,
+             "general": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_NO_TC,
              "general-tc": m.MOE_FLAG_GENERAL_PATH | m.MOE_FLAG_TC_GATEUP}[path]
     if path.startswith("fused"):
         lay = make_layer(m, wl, synth.gen_layer(wl, 17), flags=flags)
@@ -80,8 +81,9 @@ def test_wide_scale_exponent_range(m, flags):
 
 
 def test_path_selection(m):
-    """Default contexts: one launch (the fused tcgen05 kernel) up to 16 tokens, the multi-kernel tcgen05
-    path above; MOE_FLAG_NO_TC: the fused mma.sync kernel up to 16 tokens, register-decode GEMMs above."""
+    """Contexts whose calls can exceed 16 (token, expert) pairs: one launch (the fused tcgen05 kernel) up to
+    16 tokens, the multi-kernel tcgen05 path above; MOE_FLAG_NO_TC: the fused mma.sync kernel up to 16
+    tokens, register-decode GEMMs above; a decode context (t_max * k <= 16): the fused mma.sync kernel."""
     wl = synth.WORKLOADS["decode"]  # k = 4
     lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=1024))
     assert m.moe_launches_per_forward(lay.ctx, 1) == 1 and m.moe_forward_phases(lay.ctx, 1) == ["layer"]
@@ -97,6 +99,9 @@ def test_path_selection(m):
     assert m.moe_launches_per_forward(lay.ctx, 16) == 1
     assert m.moe_launches_per_forward(lay.ctx, 17) == 6  # f16 x instead of the planes and panels
     assert m.moe_launches_per_forward(lay.ctx, 33) == 7
+    lay.close()
+    lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=4))
+    assert m.moe_launches_per_forward(lay.ctx, 4) == 1 and lay.weight_bytes() == wl.E * wl.expert_bytes()
     lay.close()
 
 
@@ -237,17 +242,18 @@ def test_skewed_all_tokens_one_expert(m):
 
 
 def test_default_context_stores_one_copy(m):
-    """A default context keeps its experts once, in the tcgen05 layout (tile padding only: the 13,219,200-byte
-    expert of the decode shapes takes at most 7 % more); MOE_FLAG_NO_TC keeps the packed layout, exactly the
-    canonical size."""
-    wl = synth.WORKLOADS["decode"]
-    for t_max in (1, 16, 1024):
+    """A context keeps its experts once: in the tcgen05 layout when its calls can exceed 16 (token, expert)
+    pairs (tile padding only: the 13,219,200-byte expert of the decode shapes takes at most 7 % more), in the
+    packed layout, exactly the canonical size, otherwise or with MOE_FLAG_NO_TC."""
+    wl = synth.WORKLOADS["decode"]  # k = 4
+    for t_max in (5, 16, 1024):
         lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=t_max))
-        assert wl.E * wl.expert_bytes() <= lay.weight_bytes() <= 1.07 * wl.E * wl.expert_bytes()
+        assert wl.E * wl.expert_bytes() < lay.weight_bytes() <= 1.07 * wl.E * wl.expert_bytes()
         lay.close()
-    lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=16, flags=m.MOE_FLAG_NO_TC))
-    assert lay.weight_bytes() == wl.E * wl.expert_bytes()
-    lay.close()
+    for t_max, flags in ((1, 0), (4, 0), (16, m.MOE_FLAG_NO_TC)):
+        lay = m.MoeLayer(m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, t_max=t_max, flags=flags))
+        assert lay.weight_bytes() == wl.E * wl.expert_bytes()
+        lay.close()
 
 
 def test_k_equals_E(m):
