@@ -95,6 +95,19 @@ typedef struct moe_config {
   int t_max;      /* largest T a forward will be given; sizes the workspace */
   int out_dtype;  /* MOE_OUT_BF16 (bf16, round to nearest even) or MOE_OUT_F32 */
   unsigned flags; /* MOE_FLAG_* bits; 0 for normal use */
+  /* Expert-parallel shard: this context holds and computes routed experts
+   * [expert_begin, expert_end) only, and the shared expert only if
+   * expert_begin == 0; both 0 (the default) means every expert. Routing still
+   * runs over all n_experts (the router is replicated) and the routing
+   * exports stay global; the output is this shard's part of y -- its pairs'
+   * gate-weighted rows (and the shared expert on the first shard) -- so the
+   * fp32 outputs (MOE_OUT_F32) of a set of shards that partition the experts
+   * add up to the layer, in any fixed order. The pages run the layer on one
+   * GPU or as one pipeline stage per GPU ("NInfer" Qwen3.8-Flash-Next notes,
+   * the multi-GPU run line); sharding by experts is this library's plan for
+   * several GPUs, with the exchange of x and of the partial outputs left to
+   * the caller. */
+  int expert_begin, expert_end;
 } moe_config;
 
 typedef struct moe_ctx moe_ctx;
@@ -121,8 +134,22 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out);
  * Synchronous. Errors: MOE_ERR_INVALID_ARG (w NULL), MOE_ERR_CUDA. */
 int moe_load_router(moe_ctx* ctx, const float* w, const float* bias);
 
-/* Copy all experts (canonical layout above; host or device pointers, still
- * owned by the caller) and repack them on the device into the library's tile
+/* Copy the shared expert's gate row -- the "shared_expert_gate" of the MoE
+ * blocks in "Running Qwen3.8-Flash-Next on a 32 GB Mac with Transformers"
+ * (its table of MoE blocks), held on the GPU as one fp32 row of the hidden
+ * size per layer ("Nebula", table of GPU-resident components): w is fp32 [d],
+ * a host or device pointer the caller keeps; NULL removes the gate. With a
+ * gate row the shared expert's output of token t is scaled by
+ * sigmoid(w . x_t), the dot product summed as a double-float (the pages name
+ * the tensor, not the formula: the sigmoid of a one-row projection is the
+ * plainest reading of a per-token gate); without one it is added with weight
+ * 1. Synchronous. Errors: MOE_ERR_INVALID_ARG (the context has no shared
+ * expert), MOE_ERR_CUDA. */
+int moe_load_shared_gate(moe_ctx* ctx, const float* w);
+
+/* Copy all experts the context holds (canonical layout above: its routed
+ * experts expert_begin .. expert_end - 1 in order, then the shared expert if
+ * it has it; host or device pointers, still owned by the caller) and repack them on the device into the library's tile
  * layout. The "Neural Server" technical page keeps its expert store the same
  * way ("A 117B-parameter model on one gaming PC": a byte-exact repack of the
  * checkpoint's MXFP4 tensors; "What it runs on and what it runs": 13,219,200 B

@@ -35,7 +35,7 @@ MOE_FLAG_GENERAL_PATH = 2
 MOE_FLAG_TC_GATEUP = 4
 MOE_FLAG_NO_TC = 8
 
-EXPORTED = ["moe_create", "moe_load_router", "moe_load_experts", "moe_forward", "moe_forward_host",
+EXPORTED = ["moe_create", "moe_load_router", "moe_load_shared_gate", "moe_load_experts", "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
             "moe_launches_per_forward", "moe_route_static", "moe_route_static_error", "moe_probe_mma_rate",
             "moe_probe_error", "moe_weight_bytes", "moe_last_error", "moe_destroy"]
@@ -50,7 +50,7 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("ffn", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("shared_ffn", ctypes.c_int), ("t_max", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("flags", ctypes.c_uint)]
+                ("flags", ctypes.c_uint), ("expert_begin", ctypes.c_int), ("expert_end", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_create.argtypes = [P(moe_config), i32, P(vp)]
             lib.moe_load_router.argtypes = [vp, vp, vp]
             lib.moe_load_experts.argtypes = [vp, vp, vp]
+            lib.moe_load_shared_gate.argtypes = [vp, vp]
+            lib.moe_load_shared_gate.restype = i32
             lib.moe_forward.argtypes = [vp, vp, i32, vp, vp]
             lib.moe_forward_host.argtypes = [vp, vp, i32, vp, vp, i32]
             lib.moe_profile_events.argtypes = [vp, P(vp), i32]
@@ -140,6 +142,10 @@ def moe_create(cfg: moe_config, device: int = 0) -> int:
 
 def moe_load_router(ctx: int, w, bias=None) -> None:
     _check(ctx, load_library().moe_load_router(ctx, ptr(w), ptr(bias)), "moe_load_router")
+
+
+def moe_load_shared_gate(ctx: int, w=None) -> None:
+    _check(ctx, load_library().moe_load_shared_gate(ctx, ptr(w)), "moe_load_shared_gate")
 
 
 def moe_load_experts(ctx: int, codes, scales) -> None:
@@ -235,10 +241,12 @@ class LayerShape:
     t_max: int = 16
     out_dtype: int = MOE_OUT_BF16
     flags: int = 0
+    expert_begin: int = 0  # an expert-parallel shard [expert_begin, expert_end); 0, 0 = every expert
+    expert_end: int = 0
 
     def config(self) -> moe_config:
         return moe_config(self.d, self.ffn, self.n_experts, self.top_k, self.shared_ffn, self.t_max,
-                          self.out_dtype, self.flags)
+                          self.out_dtype, self.flags, self.expert_begin, self.expert_end)
 
 
 class MoeLayer:
@@ -249,9 +257,11 @@ class MoeLayer:
         self.device = device
         self.ctx = moe_create(shape.config(), device)
 
-    def load(self, w_router, bias, codes, scales) -> "MoeLayer":
+    def load(self, w_router, bias, codes, scales, w_shared_gate=None) -> "MoeLayer":
         moe_load_router(self.ctx, w_router, bias)
         moe_load_experts(self.ctx, codes, scales)
+        if w_shared_gate is not None:
+            moe_load_shared_gate(self.ctx, w_shared_gate)
         return self
 
     def forward(self, x, T: int, out, stream=None) -> None:

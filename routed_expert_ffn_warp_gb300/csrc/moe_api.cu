@@ -35,6 +35,8 @@ struct moe_ctx {
   float* w_router = nullptr;
   float* bias = nullptr;
   bool has_bias = false;
+  float* w_sg = nullptr;  // shared-expert gate row [d] (contexts with a shared expert)
+  bool has_sg = false;
   // workspace (one allocation, zeroed at create)
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -101,14 +103,17 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   *out = nullptr;
   if (!cfg) return fail(nullptr, MOE_ERR_INVALID_ARG, "cfg is NULL");
   const moe_config& c = *cfg;
+  const bool all_experts = c.expert_begin == 0 && c.expert_end == 0;
   if (c.d <= 0 || c.d % 32 || c.ffn <= 0 || c.ffn % 32 || c.shared_ffn < 0 || c.shared_ffn % 32 ||
+      (!all_experts && (c.expert_begin < 0 || c.expert_begin >= c.expert_end || c.expert_end > c.n_experts)) ||
       c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
       c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) ||
       (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH | MOE_FLAG_TC_GATEUP | MOE_FLAG_NO_TC)) ||
       ((c.flags & MOE_FLAG_TC_GATEUP) && (c.flags & MOE_FLAG_NO_TC)))
     return fail(nullptr, MOE_ERR_INVALID_ARG,
                 "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
-                "0 <= t_max <= 65536; out_dtype 0/1; known flags, not both TC_GATEUP and NO_TC)");
+                "0 <= t_max <= 65536; out_dtype 0/1; known flags, not both TC_GATEUP and NO_TC; "
+                "0 <= expert_begin < expert_end <= E or both 0)");
   moe_ctx* ctx = new (std::nothrow) moe_ctx();
   if (!ctx) return fail(nullptr, MOE_ERR_NOMEM, "host allocation failed");
   ctx->cfg = c;
@@ -125,6 +130,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return fail(nullptr, MOE_ERR_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
   }
   const int d = c.d, F = c.ffn, E = c.n_experts, k = c.top_k, S = c.shared_ffn, Tm = std::max(c.t_max, 1);
+  const int eb = all_experts ? 0 : c.expert_begin, ee = all_experts ? E : c.expert_end;
+  const int El = ee - eb;                   // routed experts this context holds
+  const bool Sl = S > 0 && eb == 0;         // ... and the shared expert
   ctx->expert_stride = moe::expert_packed_bytes(d, F);
   const bool tc_fits =
       std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) <= (size_t)ctx->max_smem;
@@ -139,12 +147,12 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // packed tiles. MOE_FLAG_TC_GATEUP / MOE_FLAG_NO_TC force either.
   const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
                   (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs);
-  if (!tc) ctx->packed_bytes = ctx->expert_stride * (size_t)E + (S > 0 ? moe::expert_packed_bytes(d, S) : 0);
+  if (!tc) ctx->packed_bytes = ctx->expert_stride * (size_t)El + (Sl ? moe::expert_packed_bytes(d, S) : 0);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
-    ctx->tcw_bytes = ctx->tcw_stride * (size_t)E + (S > 0 ? moe::tc_expert_bytes(d, S) : 0);
+    ctx->tcw_bytes = ctx->tcw_stride * (size_t)El + (Sl ? moe::tc_expert_bytes(d, S) : 0);
     ctx->tcwd_stride = moe::tc_down_bytes(d, F);
-    ctx->tcwd_bytes = ctx->tcwd_stride * (size_t)E + (S > 0 ? moe::tc_down_bytes(d, S) : 0);
+    ctx->tcwd_bytes = ctx->tcwd_stride * (size_t)El + (Sl ? moe::tc_down_bytes(d, S) : 0);
   }
 
   const size_t Pm = (size_t)Tm * k, Qm = Pm + (S > 0 ? (size_t)Tm : 0);
@@ -177,7 +185,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t Qd = (size_t)std::min(Tm, moe::kDecodeMaxT) * (k + (S > 0 ? 1 : 0));  // pair rows of the fused path
   const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
-               o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * E * 2 * 8);
+               o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * (E + 1) * 2 * 8);
   // fused tcgen05 path: x planes and h planes per K step with their launch-tagged flags, row-tile counters
   const int tcap = std::min(Tm, moe::kDecodeMaxT), npad = tcap <= 8 ? 8 : (tcap + 7) & ~7;
   const int xp_step = 2 * npad * 128 + 512, hp_step = 4 * npad * 128 + 512, hp_ks = moe::tc_ksteps(std::max(F, S));
@@ -192,6 +200,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       (!tc && (e = cudaMalloc(&ctx->packed, ctx->packed_bytes)) != cudaSuccess) ||
       (e = cudaMalloc(&ctx->w_router, (size_t)E * d * 4)) != cudaSuccess ||
       (e = cudaMalloc(&ctx->bias, (size_t)E * 4)) != cudaSuccess ||
+      (S > 0 && (e = cudaMalloc(&ctx->w_sg, (size_t)d * 4)) != cudaSuccess) ||
       (e = cudaMalloc(&ctx->ws, ctx->ws_bytes)) != cudaSuccess) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_NOMEM, std::string("cudaMalloc: ") + cudaGetErrorString(e));
@@ -213,6 +222,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.d = d;
   p.F = F;
   p.E = E;
+  p.e_begin = eb;
+  p.e_end = ee;
   p.k = k;
   p.S = S;
   p.d64 = d64;
@@ -324,11 +335,27 @@ int moe_load_router(moe_ctx* ctx, const float* wr, const float* bias) {
   return MOE_OK;
 }
 
+int moe_load_shared_gate(moe_ctx* ctx, const float* w) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (ctx->cfg.shared_ffn <= 0) return fail(ctx, MOE_ERR_INVALID_ARG, "the context has no shared expert to gate");
+  if (!w) {
+    ctx->has_sg = false;
+    return MOE_OK;
+  }
+  DeviceGuard guard(ctx->device);
+  const cudaError_t e = cudaMemcpy(ctx->w_sg, w, (size_t)ctx->cfg.d * 4, cudaMemcpyDefault);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "shared gate copy");
+  ctx->has_sg = true;
+  return MOE_OK;
+}
+
 int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (!codes || !scales) return fail(ctx, MOE_ERR_INVALID_ARG, "codes or scales are NULL");
   DeviceGuard guard(ctx->device);
-  const int d = ctx->cfg.d, F = ctx->cfg.ffn, E = ctx->cfg.n_experts, S = ctx->cfg.shared_ffn;
+  const int d = ctx->cfg.d, F = ctx->cfg.ffn;
+  const int E = ctx->base.e_end - ctx->base.e_begin;                 // routed experts the context holds
+  const int S = ctx->base.e_begin == 0 ? ctx->cfg.shared_ffn : 0;  // its shared expert, if any
   const size_t ccs = (size_t)3 * F * d / 2, css = (size_t)3 * F * d / 32;  // canonical strides
   const size_t chunk_bytes = (size_t)256 << 20;
   const int per_chunk = (int)std::max<size_t>(1, chunk_bytes / ccs);
@@ -399,6 +426,7 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {
   p.x = static_cast<const uint16_t*>(x);
   p.out = out;
   p.bias = ctx->has_bias ? ctx->bias : nullptr;
+  p.w_sg = ctx->has_sg ? ctx->w_sg : nullptr;
   ctx->last_T = T;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -533,6 +561,7 @@ void moe_destroy(moe_ctx* ctx) {
     cudaFree(ctx->tcwd);
     cudaFree(ctx->w_router);
     cudaFree(ctx->bias);
+    cudaFree(ctx->w_sg);
     cudaFree(ctx->ws);
   }
   delete ctx;

@@ -269,7 +269,7 @@ __device__ __forceinline__ int warp_items(int n_items, int w) { return n_items >
 
 __device__ __forceinline__ Plan make_plan(const DecParams& p, const Shared& s, int w) {
   const FwdParams& f = p.f;
-  const int NUg = s.misc[0] * (f.F / 16) + (f.S > 0 ? f.S / 16 : 0);
+  const int NUg = s.misc[0] * (f.F / 16) + (s.misc[1] > s.misc[0] ? f.S / 16 : 0);  // + the shared slot, if any
   const int NUd = s.misc[4] * (f.d / 16);
   Plan pl;
   int b1;
@@ -305,7 +305,7 @@ __device__ __forceinline__ Item item_of(const DecParams& p, const Shared& s, con
     const Unit un = gu_unit(p, s, pl.g0 + it.u);
     const int K64d = k64_tiles(f.d);
     chunk_range(K64d, it.c, it.k0, it.k1);
-    it.src = f.packed + (size_t)un.e * f.expert_stride + ((size_t)un.idx * K64d + it.k0) * kGroupBytes;
+    it.src = f.packed + (size_t)weight_index(f, un.e) * f.expert_stride + ((size_t)un.idx * K64d + it.k0) * kGroupBytes;
     it.ng = it.k1 - it.k0;
     it.last_bytes = kGroupBytes;
   } else {
@@ -316,7 +316,7 @@ __device__ __forceinline__ Item item_of(const DecParams& p, const Shared& s, con
     const Unit un = dn_unit(p, s, pl.d0 + it.u);
     const int K64f = k64_tiles(un.f);
     chunk_range(K64f, it.c, it.k0, it.k1);
-    it.src = f.packed + (size_t)un.e * f.expert_stride + gu_packed_bytes(f.d, un.f) +
+    it.src = f.packed + (size_t)weight_index(f, un.e) * f.expert_stride + gu_packed_bytes(f.d, un.f) +
              ((size_t)un.idx * K64f + it.k0) * kTileBytes;
     const int nt = it.k1 - it.k0;
     it.ng = (nt + 1) / 2;
@@ -475,7 +475,9 @@ __device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
         const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
 #pragma unroll
         for (int jj = 0; jj < kJ; ++jj)
-          pv[i][jj] = (o < n && j0 + jj < f.k) ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + jj] * f.d + r0 + r) : 0.f;
+          pv[i][jj] = (o < n && j0 + jj < f.k && expert_in_shard(s.ids[t * f.k + j0 + jj], f.e_begin, f.e_end))
+                          ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + jj] * f.d + r0 + r)
+                          : 0.f;  // this shard's pairs only (all of them without sharding)
       }
 #pragma unroll
       for (int i = 0; i < kO; ++i) {
@@ -490,7 +492,7 @@ __device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
       const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
       if (o >= n) continue;
       float y = a[i];
-      if (f.S > 0) y += __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
+      if (f.S > 0 && f.e_begin == 0) y += (f.w_sg ? s.sg[t] : 1.f) * __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
       if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = y;
       else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(y);
     }
@@ -880,7 +882,7 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
     const long long room = (long long)max_smem - (long long)o;
     const int rg = (int)(room / ((long long)kWarps * kGroupBytes));
     // the ring also holds the CTA's router rows during phase A
-    const long long router_bytes = (long long)((f.E + num_sms - 1) / num_sms) * f.d * 4;
+    const long long router_bytes = (long long)((f.E + 1 + num_sms - 1) / num_sms) * f.d * 4;  // + the gate row
     if (rg >= rg_want && (long long)kWarps * rg_want * kGroupBytes >= router_bytes) {
       p.ring_groups = rg_want;
       p.smem_bytes = (int)(o + (size_t)kWarps * rg_want * kGroupBytes);

@@ -46,6 +46,7 @@ struct Shared {
   int* slot_q0;
   int* hs_slot;  // (slot, half) list of the down phase
   int* hs_half;
+  float* sg;  // [16] shared-expert gate of each token (when the context has a gate row)
   int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
               // [4] (slot, half) pairs, [5] pairs of routed slots, [6] warps done with their gate/up items
   uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
@@ -57,7 +58,7 @@ struct Shared {
 // half) list of the mma.sync kernel's down phase, and the misc words.
 __host__ __device__ inline size_t route_region_bytes(int E, int k) {
   const int Pm = kDecodeMaxT * k;
-  return (size_t)(4 * Pm + 5 * (E + 1) + 2 * (E + 1 + 64) + 8) * 4;
+  return (size_t)(4 * Pm + 5 * (E + 1) + 2 * (E + 1 + 64) + 8 + kDecodeMaxT) * 4;
 }
 __device__ __forceinline__ void carve_route(Shared& s, uint8_t* sm, const DecParams& p) {
   int* r = reinterpret_cast<int*>(sm + p.off_route);
@@ -74,6 +75,16 @@ __device__ __forceinline__ void carve_route(Shared& s, uint8_t* sm, const DecPar
   s.hs_slot = s.slot_q0 + E + 1;
   s.hs_half = s.hs_slot + E + 1 + 64;
   s.misc = s.hs_half + E + 1 + 64;
+  s.sg = reinterpret_cast<float*>(s.misc + 8);
+}
+
+// Rows of the router phase: the E expert rows, then the shared-expert gate row
+// (when the context has one) as row E, whose dot product with x_t is published
+// beside the logits but takes no part in the top k. The logit words have E + 1
+// columns per token.
+__device__ __forceinline__ int router_rows(const FwdParams& f) { return f.E + (f.w_sg ? 1 : 0); }
+__device__ __forceinline__ const float* router_row(const FwdParams& f, int e) {
+  return e < f.E ? f.w_router + (size_t)e * f.d : f.w_sg;
 }
 
 // ---------------------------------------------------------------- bounded waits
@@ -103,10 +114,10 @@ __device__ void stage_router(const DecParams& p, const Shared& s) {
   const int d4 = p.f.d / 4;
   float* wsm = reinterpret_cast<float*>(s.ring);
   int r = 0;
-  for (int e = blockIdx.x; e < p.f.E; e += gridDim.x, ++r)
+  for (int e = blockIdx.x; e < router_rows(p.f); e += gridDim.x, ++r)
     for (int o = threadIdx.x; o < d4; o += kThreads)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(wsm + (size_t)r * p.f.d + 4 * o)),
-                   "l"(p.f.w_router + (size_t)e * p.f.d + 4 * o)
+                   "l"(router_row(p.f, e) + 4 * o)
                    : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -143,7 +154,8 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
   const int wpt = max(1, kWarps / T), t = warp / wpt, q = warp - t * wpt;
   const float* wsm = reinterpret_cast<const float*>(s.ring);
   int r = 0;
-  for (int e = blockIdx.x; e < f.E; e += gridDim.x, ++r) {
+  const int LC = f.E + 1;  // logit word columns
+  for (int e = blockIdx.x; e < router_rows(f); e += gridDim.x, ++r) {
     const float* wr = wsm + (size_t)r * f.d;
     if (t < T) {
       dd acc = dd{0.f, 0.f};
@@ -168,17 +180,17 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
     if (warp < T) {
       dd v = lane < wpt ? s.red[warp * wpt + lane] : dd{0.f, 0.f};
       for (int o = 8; o; o >>= 1) v = dd_add(v, dd_shfl_xor(v, o));
-      if (lane == 0 && f.bias) v = dd_add(v, dd{f.bias[e], 0.f});
+      if (lane == 0 && f.bias && e < f.E) v = dd_add(v, dd{f.bias[e], 0.f});
       v.hi = __shfl_sync(0xffffffffu, v.hi, 0);  // lane 0's value in every copy
       v.lo = __shfl_sync(0xffffffffu, v.lo, 0);
-      if (lane == 0) {
+      if (lane == 0 && e < f.E) {
         f.logit_hi[(size_t)warp * f.E + e] = v.hi;  // debug export
         f.logit_lo[(size_t)warp * f.E + e] = v.lo;
       }
       // the word carries its own value: no other data is published with it;
       // lane r writes copy r (the readers spread over the copies)
       if (lane < kLogitCopies) {
-        unsigned long long* w = p.lwords + ((size_t)lane * p.tcap * f.E + (size_t)warp * f.E + e) * 2;
+        unsigned long long* w = p.lwords + ((size_t)lane * p.tcap * LC + (size_t)warp * LC + e) * 2;
         st_relaxed_u64(w, pack_logit(v.hi, seq));
         st_relaxed_u64(w + 1, pack_logit(v.lo, seq));
       }
@@ -205,7 +217,7 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
   const int lane = threadIdx.x & 31;
   const int E = f.E, k = f.k;
   const unsigned long long* wt =
-      p.lwords + ((size_t)(blockIdx.x % kLogitCopies) * p.tcap * E + (size_t)t * E) * 2;
+      p.lwords + ((size_t)(blockIdx.x % kLogitCopies) * p.tcap * (E + 1) + (size_t)t * (E + 1)) * 2;
   float vh[NPL], vl[NPL];
   unsigned valid = 0;
 #pragma unroll
@@ -232,6 +244,20 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
       if (lane == 0) give_up(abort, f.status);
       break;
     }
+  }
+  // the shared-expert gate of token t: sigmoid of its published dot product (word column E)
+  if (f.w_sg && lane == 0) {
+    unsigned long long a, b;
+    ld_relaxed_u64x2(wt + 2 * E, a, b);
+    while (((unsigned)a != seq || (unsigned)b != seq) && !*abort) {
+      if (timed_out(t0, p.wait_ns)) {
+        give_up(abort, f.status);
+        break;
+      }
+      ld_relaxed_u64x2(wt + 2 * E, a, b);
+    }
+    const float z = __uint_as_float((unsigned)(a >> 32)) + __uint_as_float((unsigned)(b >> 32));
+    s.sg[t] = 1.f / (1.f + expf(-z));
   }
   unsigned kh[NPL], kl[NPL];
 #pragma unroll
@@ -310,7 +336,10 @@ __device__ void bucket_small(const DecParams& p, const Shared& s) {
   __syncwarp();
   const int e = (int)(key >> 8), q = (int)(key & 0xffu);
   const int eprev = __shfl_up_sync(0xffffffffu, e, 1);
-  const bool first = lane < P && (lane == 0 || e != eprev);
+  const bool start = lane < P && (lane == 0 || e != eprev);  // first pair of its expert
+  const unsigned starts = __ballot_sync(0xffffffffu, start);
+  // slots: the experts of this context's shard that received pairs
+  const bool first = start && expert_in_shard(e, f.e_begin, f.e_end);
   const unsigned firsts = __ballot_sync(0xffffffffu, first);
   const int ns = __popc(firsts);
   if (lane < P) {
@@ -323,7 +352,7 @@ __device__ void bucket_small(const DecParams& p, const Shared& s) {
   }
   if (first) {
     const int slot = __popc(firsts & ((1u << lane) - 1u));
-    const unsigned after = firsts & ~((2u << lane) - 1u);  // next first lane, or P
+    const unsigned after = starts & ~((2u << lane) - 1u);  // the next expert's first lane, or P
     const int next = after ? __ffs(after) - 1 : P;
     s.slot_e[slot] = e;
     s.slot_q0[slot] = lane;
@@ -332,7 +361,7 @@ __device__ void bucket_small(const DecParams& p, const Shared& s) {
   if (lane == 0) {
     s.misc[0] = ns;
     int tot = ns;
-    if (f.S > 0) {
+    if (f.S > 0 && f.e_begin == 0) {
       s.slot_e[ns] = E;
       s.slot_n[ns] = T;
       s.slot_q0[ns] = P;
@@ -389,7 +418,7 @@ __device__ void bucket_large(const DecParams& p, const Shared& s) {
   int ns = 0;  // slots: the experts that received pairs, in expert order
   for (int e0 = 0; e0 < E; e0 += 32) {
     const int e = e0 + lane;
-    const bool has = e < E && s.cnt[e] > 0;
+    const bool has = e < E && s.cnt[e] > 0 && expert_in_shard(e, f.e_begin, f.e_end);
     const unsigned bal = __ballot_sync(0xffffffffu, has);
     if (has) {
       const int pos = ns + __popc(bal & ((1u << lane) - 1u));
@@ -402,7 +431,7 @@ __device__ void bucket_large(const DecParams& p, const Shared& s) {
   if (lane == 0) {
     s.misc[0] = ns;
     int tot = ns;
-    if (f.S > 0) {
+    if (f.S > 0 && f.e_begin == 0) {
       s.slot_e[ns] = E;
       s.slot_n[ns] = T;
       s.slot_q0[ns] = P;

@@ -236,9 +236,10 @@ __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int
     const int t = o >> 8, row = 256 * dp + (o & 255);
     if (row >= f.d) continue;
     float y = 0.f;
-    for (int j = 0; j < f.k; ++j)
-      y = fmaf(s.gates[t * f.k + j], __ldcg(f.part + (size_t)s.inv[t * f.k + j] * f.d + row), y);
-    if (f.S > 0) y += __ldcg(f.part + (size_t)(f.P + t) * f.d + row);
+    for (int j = 0; j < f.k; ++j)  // this shard's pairs only (all of them without sharding)
+      if (expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
+        y = fmaf(s.gates[t * f.k + j], __ldcg(f.part + (size_t)s.inv[t * f.k + j] * f.d + row), y);
+    if (f.S > 0 && f.e_begin == 0) y += (f.w_sg ? s.sg[t] : 1.f) * __ldcg(f.part + (size_t)(f.P + t) * f.d + row);
     if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + row] = y;
     else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + row] = __float2bfloat16_rn(y);
   }
@@ -433,7 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {  // weight blocks: a tensor copy of both tiles' codes (widened) and a bulk copy of their scales
       auto prefetch_item = [&](int i) {
         const TcItem it = tc_item(f, s, wk, i);
-        const uint8_t* base = (it.down ? f.tcwd + (size_t)it.e * f.tcwd_stride : f.tcw + (size_t)it.e * f.tcw_stride) +
+        const size_t we = (size_t)weight_index(f, it.e);
+        const uint8_t* base = (it.down ? f.tcwd + we * f.tcwd_stride : f.tcw + we * f.tcw_stride) +
                               (size_t)it.tile * it.nks * kTcPairBytes;
         prefetch_l2(base, (uint32_t)(it.nks * kTcPairBytes));
       };
@@ -444,8 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TcItem it = tc_item(f, s, wk, i);
         if (i + kPfItems < nit) prefetch_item(i + kPfItems);
         const size_t stride = it.down ? f.tcwd_stride : f.tcw_stride;  // a multiple of kTcPairBytes
-        const uint8_t* w0 = (it.down ? f.tcwd : f.tcw) + (size_t)it.e * stride + (size_t)it.tile * it.nks * kTcPairBytes;
-        const int y0 = (int)((size_t)it.e * (stride / 64) + (size_t)it.tile * it.nks * (kTcPairBytes / 64));
+        const size_t we = (size_t)weight_index(f, it.e);  // the expert's place in this context's copy
+        const uint8_t* w0 = (it.down ? f.tcwd : f.tcw) + we * stride + (size_t)it.tile * it.nks * kTcPairBytes;
+        const int y0 = (int)(we * (stride / 64) + (size_t)it.tile * it.nks * (kTcPairBytes / 64));
         for (int ks = 0; ks < it.nks; ++ks, ++j) {
           const int st = j % S;
           if (j >= S && !tc::bounded_wait_sleep(&empty[st], (uint32_t)((j / S - 1) & 1), f.status, abort)) {
@@ -589,7 +592,7 @@ bool tc_layer_plan(TcLayerParams& P, int max_smem, int num_sms) {
   if ((size_t)max_smem < off + 2 * sb) return false;
   P.stages = (int)std::min<size_t>(kMaxStages, ((size_t)max_smem - off) / sb);
   // during routing the ring holds this CTA's router rows and the staged x (rows of ksteps(d) * 128 elements)
-  P.router_bytes = (int)up((size_t)((f.E + num_sms - 1) / num_sms) * f.d * 4, 128);
+  P.router_bytes = (int)up((size_t)((f.E + 1 + num_sms - 1) / num_sms) * f.d * 4, 128);  // + the gate row
   p.xs_t = tc_ksteps(f.d) * kTcStepK;
   p.xs_k = kTcStepK;
   if ((size_t)P.router_bytes + (size_t)p.tcap * p.xs_t * 2 > (size_t)P.stages * sb) return false;

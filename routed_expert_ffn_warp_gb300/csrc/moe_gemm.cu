@@ -132,7 +132,7 @@ __device__ __forceinline__ void ws_seek_gu(const FwdParams& p, int w, WStream& w
     const GUnit g = gemm_unit(p, p.gu_prefix, blockIdx.x + ws.i * gridDim.x, false);
     const int tau = g.tile0 + w;
     if (tau < g.f / 16) {
-      ws.src = p.packed + (size_t)g.e * p.expert_stride + (size_t)tau * K64 * kGroup;
+      ws.src = p.packed + (size_t)weight_index(p, g.e) * p.expert_stride + (size_t)tau * K64 * kGroup;
       ws.left = K64;
       return;
     }
@@ -323,7 +323,8 @@ __device__ __forceinline__ void ws_seek_dn(const FwdParams& p, int w, WStream& w
     const int m = g.tile0 + w;
     if (m < p.d / 16) {
       const int K64 = k64_tiles(g.f);
-      ws.src = p.packed + (size_t)g.e * p.expert_stride + gu_packed_bytes(p.d, g.f) + (size_t)m * K64 * kTileBytes;
+      ws.src = p.packed + (size_t)weight_index(p, g.e) * p.expert_stride + gu_packed_bytes(p.d, g.f) +
+               (size_t)m * K64 * kTileBytes;
       ws.kt = 0;
       ws.left = K64;  // tiles
       return;
@@ -482,7 +483,8 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_down_kernel(FwdParams p) {
   cm.nch0 = (k64_tiles(p.F) + kHC - 1) / kHC;
   cm.nch1 = p.S > 0 ? (k64_tiles(p.S) + kHC - 1) / kHC : cm.nch0;
   const int ns = *p.n_slots;
-  const int split = p.S > 0 ? p.dn_prefix[ns - 1] : total;  // first unit of the shared expert
+  // first unit of the shared expert (its slot is last, on the shard with e_begin == 0 only)
+  const int split = (p.S > 0 && p.e_begin == 0) ? p.dn_prefix[ns - 1] : total;
   cm.n_first = split > (int)blockIdx.x ? min(n_units, (split - (int)blockIdx.x + gridDim.x - 1) / gridDim.x) : 0;
   const int n_chunks_total = cm.n_first * cm.nch0 + (n_units - cm.n_first) * cm.nch1;
   load_h_chunk(p, 0, cm, hbuf, hsbuf, &hbar[0]);

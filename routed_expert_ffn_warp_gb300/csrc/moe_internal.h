@@ -97,6 +97,12 @@ __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
 
 // ---------------------------------------------------------------- forward parameters
 
+struct FwdParams;
+// Expert e of the routing (E = the shared expert) -> its index in the
+// context's weight copies, which hold experts e_begin .. e_end - 1 and then the
+// shared expert.
+__host__ __device__ inline bool expert_in_shard(int e, int e_begin, int e_end) { return e >= e_begin && e < e_end; }
+
 constexpr int kRouterSplits = 4;  // most ranges of d the router's fp32 pass splits into
 // Multi-kernel path with T <= kRouteDDMaxT: every logit as a double-float sum
 // spread over all SMs (router_dd_kernel), the top k inside the bucketing
@@ -106,6 +112,8 @@ constexpr int kRouteDDMaxT = 32;
 struct FwdParams {
   // sizes
   int T, d, F, E, k, S;  // S = shared ffn (0 = none)
+  int e_begin, e_end;    // experts this context computes (an expert-parallel shard), [0, E) by default;
+                         // the shared expert belongs to the shard with e_begin == 0
   int P;                 // T * k
   int d64, fmax64;       // padded row pitches (elements) of x16 and h planes
   int hgroups;           // fmax64 / 16: h scale groups per pair row
@@ -114,6 +122,7 @@ struct FwdParams {
   const uint16_t* x;     // bf16 [T][d]
   const float* w_router; // [E][d]
   const float* bias;     // [E] or nullptr
+  const float* w_sg;     // [d] shared-expert gate row, or nullptr (shared expert added with weight 1)
   const uint8_t* packed; // packed experts
   size_t expert_stride;  // packed bytes per routed expert
   // workspace
@@ -258,6 +267,9 @@ inline int forward_phases(const FwdParams& p) { return p.tc_gateup ? kForwardPha
 constexpr int kLaunchesPerForward = 7;
 constexpr int kLaunchesPerForwardTc = 8;  // no f16 x; + x planes, x panels (tcgen05 GEMMs)
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms, cudaEvent_t const* events);
+__host__ __device__ inline int weight_index(const FwdParams& f, int e) {
+  return e == f.E ? f.e_end - f.e_begin : e - f.e_begin;
+}
 // Routing only (router logits, top-k gates, counting sort) of the general path.
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
 // Router logits and top-k of the multi-kernel path (moe_kernels.cu).

@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
     }
   }
   // work list
-  const bool nz = tid < E && cnt > 0;
+  const bool nz = tid < E && cnt > 0 && expert_in_shard(tid, p.e_begin, p.e_end);  // this shard's experts
   const int blocks = (cnt + kGemmRows - 1) / kGemmRows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
   const int ugu = !nz ? 0
                       : p.tc_gateup ? tcb * tc_gu_pairs(p.F) : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
     if (p.tc_gateup) p.panel_prefix[slot] = ppre;
   }
   if (tid == 0) {
-    if (p.S > 0 && T > 0) {
+    if (p.S > 0 && T > 0 && p.e_begin == 0) {
       p.slot_expert[ns] = E;
       p.slot_q0[ns] = P;
       p.slot_n[ns] = T;
@@ -665,17 +665,40 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
 
 // ---------------------------------------------------------------- combine
 
+// The shared-expert gate of token t, sigmoid(w_sg . x_t), by a whole block of
+// 256 threads: a double-float sum in a fixed order (thread-strided, then a warp
+// tree, then the warps in order). Every thread gets the value.
+__device__ float shared_gate_block(const FwdParams& p, int t) {
+  __shared__ dd red[8];
+  __shared__ float g;
+  dd acc = dd{0.f, 0.f};
+  for (int i = threadIdx.x; i < p.d; i += blockDim.x)
+    dd_mac(acc, __uint_as_float((uint32_t)p.x[(size_t)t * p.d + i] << 16), p.w_sg[i]);
+  for (int o = 16; o; o >>= 1) acc = dd_add(acc, dd_shfl_xor(acc, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    dd z = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) z = dd_add(z, red[w]);
+    g = 1.f / (1.f + expf(-(z.hi + z.lo)));
+  }
+  __syncthreads();
+  return g;
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
   pdl_enter();
   const int t = blockIdx.y;
+  const float sg = (p.S > 0 && p.w_sg) ? shared_gate_block(p, t) : 1.f;
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= p.d) return;
   float acc = 0.f;
-  for (int j = 0; j < p.k; ++j) {
+  for (int j = 0; j < p.k; ++j) {  // this shard's pairs only (all of them without sharding)
     const int pj = t * p.k + j;
-    acc = fmaf(p.gates[pj], p.part[(size_t)p.inv[pj] * p.d + r], acc);
+    if (expert_in_shard(p.ids[pj], p.e_begin, p.e_end))
+      acc = fmaf(p.gates[pj], p.part[(size_t)p.inv[pj] * p.d + r], acc);
   }
-  if (p.S > 0) acc += p.part[(size_t)(p.P + t) * p.d + r];
+  if (p.S > 0 && p.e_begin == 0) acc += sg * p.part[(size_t)(p.P + t) * p.d + r];
   if (p.out_f32) reinterpret_cast<float*>(p.out)[(size_t)t * p.d + r] = acc;
   else reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)t * p.d + r] = __float2bfloat16_rn(acc);
 }

@@ -85,6 +85,8 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
   p.T = T;
   p.d = d;
   p.E = n_experts;
+  p.e_begin = 0;
+  p.e_end = n_experts;
   p.k = top_k;
   p.F = 0;
   p.S = 0;

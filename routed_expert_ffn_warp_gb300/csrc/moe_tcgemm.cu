@@ -138,8 +138,9 @@ __device__ __forceinline__ TcUnit tc_unit(const FwdParams& p, const SlotTab& st,
   g.nks = tc_ksteps(kDown ? g.f : p.d);
   g.panel = st.ppre[s] + tb;
   const size_t stride = kDown ? p.tcwd_stride : p.tcw_stride;  // a multiple of kTcPairBytes
-  g.y = (int)((size_t)g.e * (stride / 64)) + (g.mt / 2) * g.nks * kCmRows;
-  g.w = (kDown ? p.tcwd : p.tcw) + (size_t)g.e * stride + (size_t)(g.mt / 2) * g.nks * kTcPairBytes;
+  const size_t we = (size_t)weight_index(p, g.e);  // the expert's place in this context's copy
+  g.y = (int)(we * (stride / 64)) + (g.mt / 2) * g.nks * kCmRows;
+  g.w = (kDown ? p.tcwd : p.tcw) + we * stride + (size_t)(g.mt / 2) * g.nks * kTcPairBytes;
   return g;
 }
 

@@ -30,12 +30,12 @@ def build_lib():
 
 
 def make_layer(m, wl: synth.Workload, L: dict, t_max: int | None = None, out_f32: bool = False, device: int = 0,
-               flags: int = 0):
+               flags: int = 0, w_shared_gate=None):
     shape = m.LayerShape(d=wl.d, ffn=wl.ffn, n_experts=wl.E, top_k=wl.k, shared_ffn=wl.shared_ffn,
                          t_max=wl.T if t_max is None else t_max,
                          out_dtype=m.MOE_OUT_F32 if out_f32 else m.MOE_OUT_BF16, flags=flags)
     layer = m.MoeLayer(shape, device)
-    layer.load(L["w_router"], L["bias"], L["codes"], L["scales"])
+    layer.load(L["w_router"], L["bias"], L["codes"], L["scales"], w_shared_gate=w_shared_gate)
     return layer
 
 
@@ -83,9 +83,9 @@ def check_output(y_gpu: np.ndarray, y_ref: np.ndarray, tol: float):
     return err / scale if scale > 0 else 0.0
 
 
-def oracle_layer(wl: synth.Workload, L: dict, tokens=None) -> dict:
+def oracle_layer(wl: synth.Workload, L: dict, tokens=None, w_shared_gate=None) -> dict:
     return oracle.layer_tokens(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, L["x"], L["w_router"], L["bias"],
-                               L["codes"], L["scales"], tokens=tokens)
+                               L["codes"], L["scales"], tokens=tokens, w_shared_gate=w_shared_gate)
 
 
 def oracle_route(wl: synth.Workload, L: dict) -> dict:
