@@ -456,15 +456,24 @@ def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank:
     }
 
 
-def prefill_tensor_view(res: dict, fp4_peak: float | None, peaks: dict) -> dict:
-    """The layer's algorithmic TFLOP/s against the attainable min(FP4 peak, AI x HBM) and the FP4 peak."""
+def prefill_tensor_view(res: dict, mma: dict | None, peaks: dict) -> dict:
+    """The layer's algorithmic TFLOP/s against the attainable min(FP4 peak, AI x HBM), the FP4 peak, and the
+    measured rate of the MMA kind the GEMMs issue (which runs at the FP8 rate on x split into two planes:
+    the tensor pipe does twice the algorithmic flops of the gate/up GEMM and four times those of down)."""
     ai = res["flops_per_layer"] / res["bytes_per_layer"]
     out = {"tflops": res["tflops"], "arithmetic_intensity_flop_per_byte": ai,
            "hbm_bound_tflops": ai * peaks["hbm_gbs"] / 1000.0}
-    if fp4_peak:
-        att = min(fp4_peak, ai * peaks["hbm_gbs"] / 1000.0)
-        out.update({"fp4_peak_tflops": fp4_peak, "attainable_tflops": att, "frac_of_attainable": res["tflops"] / att,
-                    "frac_of_fp4_peak": res["tflops"] / fp4_peak})
+    if mma:
+        fp4 = mma["fp4_peak_tflops"]
+        att = min(fp4, ai * peaks["hbm_gbs"] / 1000.0)
+        out.update({"fp4_peak_tflops": fp4, "attainable_tflops": att, "frac_of_attainable": res["tflops"] / att,
+                    "frac_of_fp4_peak": res["tflops"] / fp4, "mxf8f6f4_tflops": mma["tflops"],
+                    "frac_of_mxf8f6f4_rate": res["tflops"] / mma["tflops"]})
+        ph = res["roofline"].get("phase_tflops", {})
+        if "gateup" in ph:  # pipe flops = 2 x algorithmic (two planes of x)
+            out["gateup_pipe_frac_of_mxf8f6f4_rate"] = 2 * ph["gateup"] / mma["tflops"]
+        if "down" in ph:  # four planes of h
+            out["down_pipe_frac_of_mxf8f6f4_rate"] = 4 * ph["down"] / mma["tflops"]
     return out
 
 
@@ -497,8 +506,8 @@ def run_ours(args, wl):
         wx = synth.WORKLOADS[name]
         res = measure_workload(args, wx, wx.layers, m, torch, ws, rank, local, peaks)
         res["config"] = config_of(wx, args, wx.layers)
-        if name == "prefill":
-            res["tensor"] = prefill_tensor_view(res, mma["fp4_peak_tflops"] if mma else None, peaks)
+        if name.startswith("prefill"):
+            res["tensor"] = prefill_tensor_view(res, mma, peaks)
         extras[name] = res
 
     cpu = None
@@ -552,7 +561,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle wall time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 8: register-decode GEMMs instead of tcgen05)")
-    ap.add_argument("--extra-workloads", default="verify,small,prefill",
+    ap.add_argument("--extra-workloads", default="verify,small,prefill,prefill16k",
                     help="comma-separated workloads measured after the main one and reported under 'workloads' "
                          "('' for none)")
     ap.add_argument("--no-mma-probe", action="store_true")

@@ -16,8 +16,10 @@ Workloads (shapes and distributions of the layers the pages run):
 * ``small``   T=8, d=2048, ffn=512, E=256, k=8, shared expert ffn=2048, 48 layers.
 * ``prefill`` T=1024, d=ffn=2880, E=128, k=4, no bias, 4 layers.
 
+* ``prefill16k`` T=16384, same shapes, one layer: a ridge-crossing prompt chunk
+              (512 tokens per expert on average).
 Layer ``l`` of workload number ``c`` (tiny=1, decode=2, verify=3, small=4,
-prefill=5) uses seed ``1000*c + l``; the tiny layer uses seed 0.
+prefill=5, prefill16k=6) uses seed ``1000*c + l``; the tiny layer uses seed 0.
 """
 from __future__ import annotations
 
@@ -89,6 +91,10 @@ WORKLOADS: dict[str, Workload] = {
     "verify": Workload("verify", 3, T=16, d=2880, ffn=2880, E=128, k=4, shared_ffn=0, layers=36, zipf_bias=1.1),
     "small": Workload("small", 4, T=8, d=2048, ffn=512, E=256, k=8, shared_ffn=2048, layers=48, zipf_bias=0.0),
     "prefill": Workload("prefill", 5, T=1024, d=2880, ffn=2880, E=128, k=4, shared_ffn=0, layers=4, zipf_bias=0.0),
+    # a ridge-crossing prompt chunk: 512 tokens per expert on average, where the expert GEMMs reuse every
+    # weight tile across many token blocks and the tensor cores, not HBM, bind
+    "prefill16k": Workload("prefill16k", 6, T=16384, d=2880, ffn=2880, E=128, k=4, shared_ffn=0, layers=1,
+                           zipf_bias=0.0),
 }
 
 

@@ -340,6 +340,27 @@ def test_full_size_workloads(m, name, layer_idx, out_f32):
     layer.close()
 
 
+def test_ridge_crossing_prefill_chunk(m):
+    """The 16,384-token chunk (512 tokens per expert on average) on the tcgen05 multi-kernel path: routing,
+    counts, offsets, perm and inv bit-exact over all tokens; y on 64 tokens spread over the chunk (the
+    oracle's cost), at the bf16 and fp32 tolerances."""
+    wl = synth.WORKLOADS["prefill16k"]
+    L = synth.gen_layer(wl, 0)
+    tokens = list(range(0, wl.T, wl.T // 64))
+    ref = oracle.layer_tokens_parallel(wl.d, wl.ffn, wl.E, wl.k, 0, L["x"], L["w_router"], L["bias"], L["codes"],
+                                       L["scales"], tokens=tokens)
+    rr = oracle_route(wl, L)
+    for out_f32 in (False, True):
+        layer = make_layer(m, wl, L, out_f32=out_f32)
+        assert m.moe_launches_per_forward(layer.ctx, wl.T) == 8
+        g = run_gpu(m, layer, L["x"], out_f32=out_f32)
+        assert g["status"] == 0
+        check_routing(g, rr, wl.E)
+        assert np.min(g["counts"]) >= 300  # every expert well past the ridge
+        check_output(g["y"][tokens], ref["y"], F32_TOL if out_f32 else BF16_TOL)
+        layer.close()
+
+
 def test_register_decode_gemms_prefill_sampled(m):
     """The multi-kernel path without the tcgen05 GEMMs (MOE_FLAG_NO_TC) on the full prefill chunk."""
     wl = synth.WORKLOADS["prefill"]
