@@ -85,12 +85,18 @@ def _load():
             lib.oracle_affine_expert_bytes.restype = ctypes.c_size_t
             lib.oracle_expert_ffn_affine.argtypes = [vp, i32, i32, i32, vp, vp]
             lib.oracle_expert_ffn_affine.restype = i32
+            lib.oracle_layer_tokens_affine.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp,
+                                                       vp, vp, vp]
+            lib.oracle_layer_tokens_affine.restype = i32
             lib.oracle_layer_tokens.restype = i32
             _lib = lib
     return _lib
 
 
 def _p(a):
+    """Address of a C-contiguous array. The caller must hold a reference to `a`
+    until the C call returns: never pass a temporary made in the call's own
+    argument list (it may be freed before the call runs)."""
     if a is None:
         return None
     assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "need a C-contiguous numpy array"
@@ -160,7 +166,9 @@ def expert_ffn(codes_e: np.ndarray, scales_e: np.ndarray, d: int, f: int, x: np.
     x = np.ascontiguousarray(x, dtype=np.float64)
     h = np.empty((f,), dtype=np.float64)
     out = np.empty((d,), dtype=np.float64)
-    _check(_load().oracle_expert_ffn(_p(np.ascontiguousarray(codes_e)), _p(np.ascontiguousarray(scales_e)),
+    codes_e = np.ascontiguousarray(codes_e)
+    scales_e = np.ascontiguousarray(scales_e)
+    _check(_load().oracle_expert_ffn(_p(codes_e), _p(scales_e),
                                      d, f, _p(x), _p(h), _p(out)), "expert_ffn")
     return h, out
 
@@ -209,8 +217,11 @@ def layer_tokens(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_router
     gates = np.empty((n, k), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     sg = None if w_shared_gate is None else np.ascontiguousarray(w_shared_gate, dtype=np.float32)
-    _check(_load().oracle_layer_tokens(d, F, E, k, S, _p(x), _p(np.ascontiguousarray(w_router, dtype=np.float32)),
-                                       _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    _check(_load().oracle_layer_tokens(d, F, E, k, S, _p(x), _p(w_router),
+                                       _p(b), _p(codes), _p(scales),
                                        _p(tokens), n, _p(y), _p(h), _p(ids), _p(gates), _p(sg)), "layer_tokens")
     return {"y": y, "h": h, "ids": ids, "gates": gates, "tokens": tokens}
 
@@ -271,9 +282,10 @@ def layer_tokens_shard(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_
     y = np.empty((tokens.shape[0], d), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     sg = None if w_shared_gate is None else np.ascontiguousarray(w_shared_gate, dtype=np.float32)
-    _check(_load().oracle_layer_tokens_shard(d, F, E, k, S, _p(x), _p(np.ascontiguousarray(w_router,
-                                                                                         dtype=np.float32)),
-                                             _p(b), _p(np.ascontiguousarray(codes)), _p(np.ascontiguousarray(scales)),
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    _check(_load().oracle_layer_tokens_shard(d, F, E, k, S, _p(x), _p(w_router), _p(b), _p(codes), _p(scales),
                                              _p(tokens), tokens.shape[0], e_begin, e_end, 1 if with_shared else 0,
                                              _p(sg), _p(y)), "layer_tokens_shard")
     return y
@@ -282,13 +294,14 @@ def layer_tokens_shard(d: int, F: int, E: int, k: int, S: int, x: np.ndarray, w_
 # ---------------------------------------------------------------- affine group-64 experts
 
 def affine_code(packed: np.ndarray, K: int, bits: int, r: int, c: int) -> int:
-    return _load().oracle_affine_code(_p(np.ascontiguousarray(packed)), K, bits, r, c)
+    packed = np.ascontiguousarray(packed)
+    return _load().oracle_affine_code(_p(packed), K, bits, r, c)
 
 
 def affine_element(packed: np.ndarray, scales: np.ndarray, biases: np.ndarray, K: int, bits: int, r: int,
                    c: int) -> float:
-    return _load().oracle_affine_element(_p(np.ascontiguousarray(packed)), _p(np.ascontiguousarray(scales)),
-                                         _p(np.ascontiguousarray(biases)), K, bits, r, c)
+    packed, scales, biases = (np.ascontiguousarray(a) for a in (packed, scales, biases))
+    return _load().oracle_affine_element(_p(packed), _p(scales), _p(biases), K, bits, r, c)
 
 
 def affine_expert_bytes(d: int, f: int, bits: int) -> int:
@@ -299,6 +312,56 @@ def expert_ffn_affine(expert: np.ndarray, d: int, f: int, bits: int, x: np.ndarr
     """One affine group-64 expert (codes, bf16 scales, bf16 biases in one byte range) on one fp64 vector."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty((d,), dtype=np.float64)
-    _check(_load().oracle_expert_ffn_affine(_p(np.ascontiguousarray(expert)), d, f, bits, _p(x), _p(out)),
+    expert = np.ascontiguousarray(expert)
+    _check(_load().oracle_expert_ffn_affine(_p(expert), d, f, bits, _p(x), _p(out)),
            "expert_ffn_affine")
+    return out
+
+
+def layer_tokens_affine(d: int, F: int, E: int, k: int, S: int, bits: int, x: np.ndarray, w_router: np.ndarray,
+                        bias: np.ndarray | None, experts: np.ndarray, tokens=None,
+                        w_shared_gate: np.ndarray | None = None) -> dict:
+    """fp64 layer output of the listed tokens with affine group-64 experts: y [n][d], ids, gates."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    y = np.empty((n, d), dtype=np.float64)
+    ids = np.empty((n, k), dtype=np.int32)
+    gates = np.empty((n, k), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    sg = None if w_shared_gate is None else np.ascontiguousarray(w_shared_gate, dtype=np.float32)
+    w_router = np.ascontiguousarray(w_router, dtype=np.float32)
+    experts = np.ascontiguousarray(experts)
+    _check(_load().oracle_layer_tokens_affine(d, F, E, k, S, bits, _p(x), _p(w_router), _p(b),
+                                              _p(experts), _p(tokens), n, _p(y), _p(ids),
+                                              _p(gates), _p(sg)), "layer_tokens_affine")
+    return {"y": y, "ids": ids, "gates": gates, "tokens": tokens}
+
+
+def layer_tokens_affine_parallel(d: int, F: int, E: int, k: int, S: int, bits: int, x: np.ndarray,
+                                 w_router: np.ndarray, bias: np.ndarray | None, experts: np.ndarray, tokens=None,
+                                 threads: int | None = None, w_shared_gate: np.ndarray | None = None) -> dict:
+    """layer_tokens_affine over a thread pool, one contiguous chunk of tokens per call (bit-identical)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    threads = host_threads() if threads is None else max(1, int(threads))
+    threads = min(threads, max(1, n))
+    experts = np.ascontiguousarray(experts)
+    _load()
+    bounds = [(i * n) // threads for i in range(threads + 1)]
+
+    def run(i):
+        return layer_tokens_affine(d, F, E, k, S, bits, x, w_router, bias, experts,
+                                   tokens=tokens[bounds[i]:bounds[i + 1]], w_shared_gate=w_shared_gate)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(run, range(threads)))
+    out = {key: np.concatenate([pt[key] for pt in parts]) for key in ("y", "ids", "gates")}
+    out["tokens"] = tokens
+    out["threads"] = threads
     return out

@@ -380,3 +380,48 @@ int oracle_expert_ffn_affine(const uint8_t* expert, int d, int f, int bits, cons
   free(hv);
   return ORACLE_OK;
 }
+
+/* The layer of oracle_layer_tokens with affine group-64 experts: the same
+ * routing, gate weighting and shared expert (optionally gated), each expert
+ * (ffn F, the shared one ffn S) evaluated by oracle_expert_ffn_affine from
+ * its oracle_affine_expert_bytes(d, f, bits) bytes, experts back to back in
+ * `experts` (routed 0..E-1, then the shared one). y is fp64 and unrounded. */
+int oracle_layer_tokens_affine(int d, int F, int E, int k, int S, int bits, const uint16_t* x, const float* w_router,
+                               const float* bias, const uint8_t* experts, const int32_t* tokens, int n_tokens,
+                               double* y, int32_t* ids_out, double* gates_out, const float* w_shared_gate) {
+  if (d <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || S < 0 || d % 64 || F % 64 || S % 64 || bits < 1 || bits > 8)
+    return ORACLE_EINVAL;
+  if (w_shared_gate && S == 0) return ORACLE_EINVAL;
+  size_t eb = oracle_affine_expert_bytes(d, F, bits);
+  double* l = (double*)malloc(sizeof(double) * (size_t)E);
+  double* xv = (double*)malloc(sizeof(double) * (size_t)d);
+  double* part = (double*)malloc(sizeof(double) * (size_t)d);
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+  double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  int rc = ORACLE_OK;
+  if (!l || !xv || !part || !ids || !g) { rc = ORACLE_ENOMEM; goto done; }
+  for (int n = 0; n < n_tokens; ++n) {
+    const uint16_t* xt = x + (size_t)tokens[n] * d;
+    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(xt[i]);
+    oracle_logits_token(xt, d, w_router, bias, E, l);
+    oracle_topk_token(l, E, k, ids, g);
+    if (ids_out) memcpy(ids_out + (size_t)n * k, ids, sizeof(int32_t) * (size_t)k);
+    if (gates_out) memcpy(gates_out + (size_t)n * k, g, sizeof(double) * (size_t)k);
+    double* yn = y + (size_t)n * d;
+    for (int r = 0; r < d; ++r) yn[r] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      rc = oracle_expert_ffn_affine(experts + (size_t)ids[j] * eb, d, F, bits, xv, part);
+      if (rc) goto done;
+      for (int r = 0; r < d; ++r) yn[r] += g[j] * part[r];
+    }
+    if (S > 0) {
+      rc = oracle_expert_ffn_affine(experts + (size_t)E * eb, d, S, bits, xv, part);
+      if (rc) goto done;
+      const double st = w_shared_gate ? oracle_shared_gate_token(xt, d, w_shared_gate) : 1.0;
+      for (int r = 0; r < d; ++r) yn[r] += st * part[r];
+    }
+  }
+done:
+  free(l); free(xv); free(part); free(ids); free(g);
+  return rc;
+}

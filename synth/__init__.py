@@ -18,8 +18,13 @@ Workloads (shapes and distributions of the layers the pages run):
 
 * ``prefill16k`` T=16384, same shapes, one layer: a ridge-crossing prompt chunk
               (512 tokens per expert on average).
+* ``affine3`` T=1, d=2560, ffn=640, E=512, k=10, shared expert ffn=640, 48 layers,
+              3-bit affine group-64 experts ("Running Qwen3.8-Flash-Next on a
+              32 GB Mac with Transformers", architecture and the table of where
+              every weight lives; the shared expert's ffn is not printed there
+              and is taken equal to the routed one).
 Layer ``l`` of workload number ``c`` (tiny=1, decode=2, verify=3, small=4,
-prefill=5, prefill16k=6) uses seed ``1000*c + l``; the tiny layer uses seed 0.
+prefill=5, prefill16k=6, affine3=7) uses seed ``1000*c + l``; the tiny layer uses seed 0.
 """
 from __future__ import annotations
 
@@ -52,6 +57,7 @@ class Workload:
     zipf_bias: float  # 0.0 = no router bias
     scale_lo: int = 120
     scale_hi: int = 124
+    affine_bits: int = 0  # 0: MXFP4 experts; else affine group-64 experts with codes of this width
 
     def seed(self, layer: int) -> int:
         return 0 if self.name == "tiny" else 1000 * self.number + layer
@@ -79,6 +85,16 @@ class Workload:
     def total_scale_bytes(self) -> int:
         return self.E * self.scale_bytes() + (self.scale_bytes(self.shared_ffn) if self.shared_ffn else 0)
 
+    def affine_bytes(self, f: int | None = None) -> int:
+        """Bytes of one affine expert: codes of its 3 f d weights, a bf16 scale and bias per 64."""
+        f = self.ffn if f is None else f
+        n = 3 * f * self.d
+        return n * self.affine_bits // 8 + n // 16
+
+    @property
+    def total_affine_bytes(self) -> int:
+        return self.E * self.affine_bytes() + (self.affine_bytes(self.shared_ffn) if self.shared_ffn else 0)
+
     def with_(self, **kw) -> "Workload":
         d = dict(self.__dict__)
         d.update(kw)
@@ -95,6 +111,10 @@ WORKLOADS: dict[str, Workload] = {
     # weight tile across many token blocks and the tensor cores, not HBM, bind
     "prefill16k": Workload("prefill16k", 6, T=16384, d=2880, ffn=2880, E=128, k=4, shared_ffn=0, layers=1,
                            zipf_bias=0.0),
+    # decode of the affine-expert model: 512 routed experts of ffn 640 (top 10) and one shared expert per layer,
+    # 3-bit codes with a bf16 scale and bias per 64 weights
+    "affine3": Workload("affine3", 7, T=1, d=2560, ffn=640, E=512, k=10, shared_ffn=640, layers=48, zipf_bias=0.0,
+                        affine_bits=3),
 }
 
 
@@ -126,6 +146,8 @@ def _load():
             lib.synth_scale_bytes.argtypes = [u64, u64, sz, i32, i32, vp]
             lib.synth_experts.argtypes = [u64, i32, i32, i32, i32, i32, i32, vp, vp, i32]
             lib.synth_experts.restype = i32
+            lib.synth_experts_affine.argtypes = [u64, i32, i32, i32, i32, i32, vp, i32]
+            lib.synth_experts_affine.restype = i32
             _lib = lib
     return _lib
 
@@ -179,6 +201,21 @@ def gen_experts(wl: Workload, seed: int, codes: np.ndarray | None = None, scales
     return codes, scales
 
 
+def gen_experts_affine(wl: Workload, seed: int, out: np.ndarray | None = None, bits: int | None = None,
+                       nthreads: int | None = None) -> np.ndarray:
+    """All affine experts of a layer (canonical affine layout, expert-major; shared expert last)."""
+    bits = wl.affine_bits if bits is None else bits
+    w = wl.with_(affine_bits=bits)
+    if out is None:
+        out = np.empty((w.total_affine_bytes,), dtype=np.uint8)
+    assert out.nbytes >= w.total_affine_bytes
+    if nthreads is None:
+        nthreads = max(1, min(32, len(os.sched_getaffinity(0))))
+    if _load().synth_experts_affine(seed, wl.d, wl.ffn, wl.shared_ffn, wl.E, bits, _ptr(out), nthreads) != 0:
+        raise RuntimeError("synth_experts_affine failed")
+    return out
+
+
 def gen_layer(wl: Workload, layer: int = 0, T: int | None = None, with_experts: bool = True) -> dict:
     """All inputs of one layer: x (bf16 bits), router weights, optional bias, expert codes/scales."""
     seed = wl.seed(layer)
@@ -189,7 +226,9 @@ def gen_layer(wl: Workload, layer: int = 0, T: int | None = None, with_experts: 
         "w_router": gen_router(seed, wl.E, wl.d),
         "bias": gen_bias(seed, wl.E, wl.zipf_bias) if wl.zipf_bias > 0 else None,
     }
-    if with_experts:
+    if with_experts and wl.affine_bits:
+        out["experts"] = gen_experts_affine(wl, seed)
+    elif with_experts:
         out["codes"], out["scales"] = gen_experts(wl, seed)
     return out
 

@@ -20,6 +20,12 @@
  *   scales   uniform integer exponent byte in [lo, hi] inclusive.
  *   bias     Zipf(s) log-probabilities over a seeded random permutation of
  *            ranks: b[e] = -s * ln(rank(e)), rank a permutation of 1..E.
+ *   affine experts (group 64, `bits`-bit codes): codes uniform bits; per
+ *            group a bf16 scale 2^e (1 + m/128), e uniform in {-9, -8, -7},
+ *            m uniform in 0..127, and a bf16 bias
+ *            -scale (2^bits - 1) / 2 (0.75 + 0.5u'), u, u' uniform in (0, 1),
+ *            so the weights of a group straddle zero as a quantised
+ *            zero-mean row does.
  *
  * Build flags must keep floating point contraction off (-ffp-contract=off)
  * so the same seed gives the same bits on x86-64 and AArch64.
@@ -36,6 +42,7 @@
 #define SYNTH_STREAM_CODES 4ULL
 #define SYNTH_STREAM_SCALES 5ULL
 #define SYNTH_STREAM_SHARED_GATE 6ULL
+#define SYNTH_STREAM_AFFINE 7ULL
 
 static inline uint64_t mix64(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
@@ -172,6 +179,76 @@ int synth_experts(uint64_t seed, int d, int F, int S, int E, int lo, int hi, uin
     if (t > 0 && pthread_create(&th[t], NULL, synth_experts_worker, &jobs[t]) != 0) return -1;
   }
   synth_experts_worker(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+  return 0;
+}
+
+/*
+ * Affine group-64 experts in their canonical layout: per expert (ffn f) the
+ * codes of the gate/up rows [2f][d] then of the down rows [d][f] (each row a
+ * little-endian stream of `bits`-bit fields), then the bf16 scales of gate/up
+ * [2f][d/64] and of down [d][f/64], then the bf16 biases in the same order.
+ * Expert j (the shared one is j == E) draws from stream j of its own key, so
+ * its bytes do not depend on E or on the other experts.
+ */
+static size_t affine_bytes_of(int d, int f, int bits) {
+  size_t n = (size_t)3 * (size_t)f * (size_t)d;
+  return n * (size_t)bits / 8 + n / 16;
+}
+
+void synth_affine_expert(uint64_t seed, uint64_t stream, int d, int f, int bits, uint8_t* out) {
+  size_t n = (size_t)3 * (size_t)f * (size_t)d, code_bytes = n * (size_t)bits / 8, groups = n / 64;
+  synth_code_bytes(seed, (SYNTH_STREAM_AFFINE << 32) ^ stream, code_bytes, out);
+  uint64_t key = stream_key(seed, (SYNTH_STREAM_AFFINE << 40) ^ stream);
+  uint8_t* sc = out + code_bytes;
+  uint8_t* bi = sc + 2 * groups;
+  double half_range = 0.5 * (double)((1 << bits) - 1);
+  for (size_t g = 0; g < groups; ++g) {
+    uint64_t r = draw(key, g);
+    double u = ((double)(r >> 40) + 0.5) * (1.0 / 16777216.0);
+    double v = ((double)(r & 0xFFFFFFULL) + 0.5) * (1.0 / 16777216.0);
+    /* scale: bf16 2^e (1 + m / 128), e uniform in {-9, -8, -7}, m uniform in 0..127 (built exactly) */
+    int e2 = -9 + (int)(u * 3.0);
+    uint16_t s16 = (uint16_t)(((uint32_t)(127 + e2) << 7) | (uint32_t)((r >> 24) & 0x7F));
+    uint32_t sbits = (uint32_t)s16 << 16;
+    float s32;
+    memcpy(&s32, &sbits, 4);
+    uint16_t b16 = f32_to_bf16_rne((float)(-(double)s32 * half_range * (0.75 + 0.5 * v)));
+    sc[2 * g] = (uint8_t)(s16 & 0xFF);
+    sc[2 * g + 1] = (uint8_t)(s16 >> 8);
+    bi[2 * g] = (uint8_t)(b16 & 0xFF);
+    bi[2 * g + 1] = (uint8_t)(b16 >> 8);
+  }
+}
+
+typedef struct {
+  uint64_t seed;
+  int d, F, S, E, bits;
+  uint8_t* out;
+  int first, stride;
+} synth_affine_job;
+
+static void* synth_affine_worker(void* arg) {
+  synth_affine_job* j = (synth_affine_job*)arg;
+  int n = j->E + (j->S > 0 ? 1 : 0);
+  for (int e = j->first; e < n; e += j->stride) {
+    int f = (e < j->E) ? j->F : j->S;
+    synth_affine_expert(j->seed, (uint64_t)e, j->d, f, j->bits, j->out + (size_t)e * affine_bytes_of(j->d, j->F, j->bits));
+  }
+  return NULL;
+}
+
+int synth_experts_affine(uint64_t seed, int d, int F, int S, int E, int bits, uint8_t* out, int nthreads) {
+  if (bits < 1 || bits > 8 || d % 64 || F % 64 || S % 64) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  synth_affine_job jobs[256];
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = (synth_affine_job){seed, d, F, S, E, bits, out, t, nthreads};
+    if (t > 0 && pthread_create(&th[t], NULL, synth_affine_worker, &jobs[t]) != 0) return -1;
+  }
+  synth_affine_worker(&jobs[0]);
   for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
   return 0;
 }

@@ -93,3 +93,27 @@ def test_affine_expert_equals_mxfp4_expert_on_common_values():
 def test_affine_rejects_shapes_off_the_group():
     with pytest.raises(ValueError):
         oracle.expert_ffn_affine(np.zeros(1024, dtype=np.uint8), 96, 64, 3, np.zeros(96))
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_affine_layer_equals_mxfp4_layer_on_common_values(gated):
+    """The affine layer (routing, gate weights, shared expert) against the MXFP4 layer oracle on
+    experts both formats hold exactly: every output bit agrees."""
+    rng = np.random.default_rng(11)
+    d, F, S, E, k, T = 128, 128, 64, 4, 2, 5
+    experts = [_both_formats(rng, d, F) for _ in range(E)] + [_both_formats(rng, d, S)]
+    codes = np.concatenate([e[0] for e in experts])
+    scales = np.concatenate([e[1] for e in experts])
+    affine = np.concatenate([e[2] for e in experts])
+    x = (rng.standard_normal((T, d)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w_router = rng.standard_normal((E, d)).astype(np.float32) / np.sqrt(d)
+    w_sg = rng.standard_normal(d).astype(np.float32) / np.sqrt(d) if gated else None
+    mx = oracle.layer_tokens(d, F, E, k, S, x, w_router, None, codes, scales, w_shared_gate=w_sg)
+    af = oracle.layer_tokens_affine(d, F, E, k, S, 3, x, w_router, None, affine, w_shared_gate=w_sg)
+    assert np.array_equal(af["ids"], mx["ids"])
+    assert np.array_equal(af["gates"], mx["gates"])
+    assert np.abs(mx["y"]).max() > 0
+    assert np.array_equal(af["y"], mx["y"])
+    par = oracle.layer_tokens_affine_parallel(d, F, E, k, S, 3, x, w_router, None, affine, threads=3,
+                                              w_shared_gate=w_sg)
+    assert np.array_equal(par["y"], af["y"])
