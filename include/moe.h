@@ -108,7 +108,17 @@ typedef struct moe_config {
    * several GPUs, with the exchange of x and of the partial outputs left to
    * the caller. */
   int expert_begin, expert_end;
+  /* Expert weight format: MOE_FORMAT_MXFP4 (0, the default) or
+   * MOE_FORMAT_AFFINE64 (affine group-64 experts, loaded by
+   * moe_load_experts_affine), with weight_bits its code width (2, 3, 4 or 8;
+   * ignored for MXFP4). Affine contexts need d, ffn and shared_ffn multiples
+   * of 64, take the multi-kernel path for every T and reject
+   * MOE_FLAG_TC_GATEUP. */
+  int weight_format;
+  int weight_bits;
 } moe_config;
+
+enum { MOE_FORMAT_MXFP4 = 0, MOE_FORMAT_AFFINE64 = 1 };
 
 typedef struct moe_ctx moe_ctx;
 
@@ -159,6 +169,30 @@ int moe_load_shared_gate(moe_ctx* ctx, const float* w);
  * (a NULL pointer), MOE_ERR_NAN_SCALE (a scale byte 0xFF, the OCP MX NaN;
  * the context then counts as not loaded), MOE_ERR_NOMEM, MOE_ERR_CUDA. */
 int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales);
+
+/* Copy all experts of an affine context (weight_format MOE_FORMAT_AFFINE64)
+ * and repack them on the device -- the second expert format of the pages:
+ * "Running Qwen3.8-Flash-Next on a 32 GB Mac with Transformers", the table of
+ * where every weight lives (3-bit affine experts, group 64, 2.15 MB per
+ * expert) and the notes under the decode table (a 16-bit scale and bias per
+ * 64 weights). Weight = scale * q + bias, q an unsigned weight_bits-bit code.
+ * `experts` holds the routed experts the context holds, in order, then the
+ * shared expert if it has it; each expert (ffn f) in the canonical affine
+ * layout of affine_expert_bytes(d, f, bits) = 3 f d bits / 8 + 3 f d / 16
+ * bytes:
+ *   codes of the gate/up rows [2f][d] (gate rows 0..f-1, up rows f..2f-1),
+ *     then of the down rows [d][f]; each row one little-endian bit stream,
+ *     element c at bits [bits c, bits c + bits) of it;
+ *   bf16 scales of gate/up [2f][d/64], then of down [d][f/64];
+ *   bf16 biases in the same order.
+ * Host or device pointer, owned by the caller; the repack is lossless (every
+ * code, scale and bias kept, only the order changes). Synchronous; uses a
+ * temporary staging buffer that it frees before returning. Errors:
+ * MOE_ERR_INVALID_ARG (NULL, or not an affine context), MOE_ERR_NAN_SCALE (a
+ * scale or bias that is Inf or NaN; the context then counts as not loaded),
+ * MOE_ERR_NOMEM, MOE_ERR_CUDA. moe_load_experts on an affine context returns
+ * MOE_ERR_INVALID_ARG. */
+int moe_load_experts_affine(moe_ctx* ctx, const uint8_t* experts);
 
 /* Run the layer on T tokens (0 <= T <= t_max): every step of the formula at
  * the top of this file, in the pages' order --

@@ -34,8 +34,11 @@ MOE_FLAG_TEST_FORCE_TIMEOUT = 1
 MOE_FLAG_GENERAL_PATH = 2
 MOE_FLAG_TC_GATEUP = 4
 MOE_FLAG_NO_TC = 8
+MOE_FORMAT_MXFP4 = 0
+MOE_FORMAT_AFFINE64 = 1
 
-EXPORTED = ["moe_create", "moe_load_router", "moe_load_shared_gate", "moe_load_experts", "moe_forward", "moe_forward_host",
+EXPORTED = ["moe_create", "moe_load_router", "moe_load_shared_gate", "moe_load_experts", "moe_load_experts_affine",
+            "moe_forward", "moe_forward_host",
             "moe_get_routing", "moe_get_logits", "moe_get_status", "moe_profile_events", "moe_forward_phases",
             "moe_launches_per_forward", "moe_route_static", "moe_route_static_error", "moe_probe_mma_rate",
             "moe_probe_error", "moe_weight_bytes", "moe_last_error", "moe_destroy"]
@@ -50,7 +53,8 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int), ("ffn", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("shared_ffn", ctypes.c_int), ("t_max", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("flags", ctypes.c_uint), ("expert_begin", ctypes.c_int), ("expert_end", ctypes.c_int)]
+                ("flags", ctypes.c_uint), ("expert_begin", ctypes.c_int), ("expert_end", ctypes.c_int),
+                ("weight_format", ctypes.c_int), ("weight_bits", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -72,6 +76,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.moe_create.argtypes = [P(moe_config), i32, P(vp)]
             lib.moe_load_router.argtypes = [vp, vp, vp]
             lib.moe_load_experts.argtypes = [vp, vp, vp]
+            lib.moe_load_experts_affine.argtypes = [vp, vp]
+            lib.moe_load_experts_affine.restype = i32
             lib.moe_load_shared_gate.argtypes = [vp, vp]
             lib.moe_load_shared_gate.restype = i32
             lib.moe_forward.argtypes = [vp, vp, i32, vp, vp]
@@ -150,6 +156,10 @@ def moe_load_shared_gate(ctx: int, w=None) -> None:
 
 def moe_load_experts(ctx: int, codes, scales) -> None:
     _check(ctx, load_library().moe_load_experts(ctx, ptr(codes), ptr(scales)), "moe_load_experts")
+
+
+def moe_load_experts_affine(ctx: int, experts) -> None:
+    _check(ctx, load_library().moe_load_experts_affine(ctx, ptr(experts)), "moe_load_experts_affine")
 
 
 def moe_forward(ctx: int, x, T: int, out, stream=None) -> None:
@@ -243,10 +253,13 @@ class LayerShape:
     flags: int = 0
     expert_begin: int = 0  # an expert-parallel shard [expert_begin, expert_end); 0, 0 = every expert
     expert_end: int = 0
+    weight_format: int = MOE_FORMAT_MXFP4  # or MOE_FORMAT_AFFINE64 with weight_bits 2, 3, 4 or 8
+    weight_bits: int = 0
 
     def config(self) -> moe_config:
         return moe_config(self.d, self.ffn, self.n_experts, self.top_k, self.shared_ffn, self.t_max,
-                          self.out_dtype, self.flags, self.expert_begin, self.expert_end)
+                          self.out_dtype, self.flags, self.expert_begin, self.expert_end, self.weight_format,
+                          self.weight_bits)
 
 
 class MoeLayer:
@@ -260,6 +273,14 @@ class MoeLayer:
     def load(self, w_router, bias, codes, scales, w_shared_gate=None) -> "MoeLayer":
         moe_load_router(self.ctx, w_router, bias)
         moe_load_experts(self.ctx, codes, scales)
+        if w_shared_gate is not None:
+            moe_load_shared_gate(self.ctx, w_shared_gate)
+        return self
+
+    def load_affine(self, w_router, bias, experts, w_shared_gate=None) -> "MoeLayer":
+        """Router and affine group-64 experts (canonical affine bytes of every expert, in order)."""
+        moe_load_router(self.ctx, w_router, bias)
+        moe_load_experts_affine(self.ctx, experts)
         if w_shared_gate is not None:
             moe_load_shared_gate(self.ctx, w_shared_gate)
         return self

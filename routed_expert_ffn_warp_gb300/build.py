@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode.cu", "moe_fused_tc.cu", "moe_gemm.cu", "moe_tcgemm.cu", "moe_static.cu",
+SOURCES = ["moe_api.cu", "moe_kernels.cu", "moe_decode.cu", "moe_fused_tc.cu", "moe_gemm.cu", "moe_affine.cu", "moe_tcgemm.cu",
+           "moe_static.cu",
            "moe_probe.cu"]
 HEADERS = ["moe_internal.h", "moe_device.cuh", "moe_tc.cuh", "moe_fused_route.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -109,11 +109,18 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       c.n_experts < 1 || c.n_experts > 512 || c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32 ||
       c.t_max < 0 || c.t_max > 65536 || (c.out_dtype != MOE_OUT_BF16 && c.out_dtype != MOE_OUT_F32) ||
       (c.flags & ~(unsigned)(MOE_FLAG_TEST_FORCE_TIMEOUT | MOE_FLAG_GENERAL_PATH | MOE_FLAG_TC_GATEUP | MOE_FLAG_NO_TC)) ||
-      ((c.flags & MOE_FLAG_TC_GATEUP) && (c.flags & MOE_FLAG_NO_TC)))
+      ((c.flags & MOE_FLAG_TC_GATEUP) && (c.flags & MOE_FLAG_NO_TC)) ||
+      (c.weight_format != MOE_FORMAT_MXFP4 && c.weight_format != MOE_FORMAT_AFFINE64))
     return fail(nullptr, MOE_ERR_INVALID_ARG,
                 "config out of range (d, ffn, shared_ffn multiples of 32; 1 <= E <= 512; 1 <= k <= min(E, 32); "
                 "0 <= t_max <= 65536; out_dtype 0/1; known flags, not both TC_GATEUP and NO_TC; "
-                "0 <= expert_begin < expert_end <= E or both 0)");
+                "0 <= expert_begin < expert_end <= E or both 0; a known weight_format)");
+  const bool affine = c.weight_format == MOE_FORMAT_AFFINE64;
+  if (affine && (!moe::affine_bits_supported(c.weight_bits) || c.d % 64 || c.ffn % 64 || c.shared_ffn % 64 ||
+                 (c.flags & MOE_FLAG_TC_GATEUP)))
+    return fail(nullptr, MOE_ERR_INVALID_ARG,
+                "affine experts need weight_bits 2, 3, 4 or 8, d, ffn and shared_ffn multiples of 64, and no "
+                "MOE_FLAG_TC_GATEUP");
   moe_ctx* ctx = new (std::nothrow) moe_ctx();
   if (!ctx) return fail(nullptr, MOE_ERR_NOMEM, "host allocation failed");
   ctx->cfg = c;
@@ -133,7 +140,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const int eb = all_experts ? 0 : c.expert_begin, ee = all_experts ? E : c.expert_end;
   const int El = ee - eb;                   // routed experts this context holds
   const bool Sl = S > 0 && eb == 0;         // ... and the shared expert
-  ctx->expert_stride = moe::expert_packed_bytes(d, F);
+  const int abits = affine ? c.weight_bits : 0;
+  ctx->expert_stride = affine ? moe::aff_expert_bytes(d, F, abits) : moe::expert_packed_bytes(d, F);
   const bool tc_fits =
       std::max(moe::tc_gemm_smem_bytes(E, false), moe::tc_gemm_smem_bytes(E, true)) <= (size_t)ctx->max_smem;
   if ((c.flags & MOE_FLAG_TC_GATEUP) && !tc_fits) {
@@ -145,9 +153,12 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // tcgen05 kernel for T <= 16, the tcgen05 GEMMs above); smaller ones -- every
   // call a few tokens, where the fused mma.sync kernel is the faster -- keep the
   // packed tiles. MOE_FLAG_TC_GATEUP / MOE_FLAG_NO_TC force either.
-  const bool tc = (c.flags & MOE_FLAG_TC_GATEUP) ||
-                  (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs);
-  if (!tc) ctx->packed_bytes = ctx->expert_stride * (size_t)El + (Sl ? moe::expert_packed_bytes(d, S) : 0);
+  // Affine contexts keep their own tiles (the packed pointer) and always take the multi-kernel path.
+  const bool tc = !affine && ((c.flags & MOE_FLAG_TC_GATEUP) ||
+                              (!(c.flags & MOE_FLAG_NO_TC) && tc_fits && (long long)c.t_max * k > moe::kFusedMaxPairs));
+  if (!tc)
+    ctx->packed_bytes = ctx->expert_stride * (size_t)El +
+                        (Sl ? (affine ? moe::aff_expert_bytes(d, S, abits) : moe::expert_packed_bytes(d, S)) : 0);
   if (tc) {
     ctx->tcw_stride = moe::tc_expert_bytes(d, F);
     ctx->tcw_bytes = ctx->tcw_stride * (size_t)El + (Sl ? moe::tc_expert_bytes(d, S) : 0);
@@ -181,6 +192,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_h = take(Qm * 2 * fmax64 * 2), o_hs = take(Qm * hgroups * 4), o_part = take(Qm * d * 4);
   const size_t o_xd = take((size_t)Tm * d * 2), o_od = take((size_t)Tm * d * (c.out_dtype == MOE_OUT_F32 ? 4 : 2));
   const size_t o_status = take(4), o_lerr = take(4);
+  // affine experts: group sums of x (per 64) and of h (per 16)
+  const int xg_pitch = (d / 64 + 3) / 4 * 4;
+  const size_t o_xg = take(affine ? (size_t)Tm * xg_pitch * 4 : 0), o_hb = take(affine ? Qm * hgroups * 4 : 0);
   // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
   const size_t Qd = (size_t)std::min(Tm, moe::kDecodeMaxT) * (k + (S > 0 ? 1 : 0));  // pair rows of the fused path
   const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
@@ -235,6 +249,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.bias = nullptr;
   p.packed = ctx->packed;
   p.expert_stride = ctx->expert_stride;
+  p.aff_bits = abits;
+  p.xgsum = affine ? reinterpret_cast<float*>(w + o_xg) : nullptr;
+  p.xg_pitch = xg_pitch;
+  p.hbsum = affine ? reinterpret_cast<float*>(w + o_hb) : nullptr;
   p.x16 = reinterpret_cast<uint16_t*>(w + o_x16);
   p.xinv = reinterpret_cast<float*>(w + o_xinv);
   p.tcw = ctx->tcw;
@@ -288,7 +306,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   dp.test_wait_ns = 2000000LL;  // 2 ms
   // kernel attributes are per device: set them with this context's device current
   if ((e = moe::configure_decode(ctx->max_smem)) != cudaSuccess || (e = moe::configure_tcgemm(ctx->max_smem)) != cudaSuccess ||
-      (e = moe::configure_gemm()) != cudaSuccess) {
+      (e = moe::configure_gemm()) != cudaSuccess || (e = moe::configure_affine()) != cudaSuccess) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   }
@@ -311,7 +329,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     tp.max_slots = max_slots;
     ctx->fused_tc_ok = single && moe::tc_layer_plan(tp, ctx->max_smem, ctx->num_sms) && tp.xp_step == xp_step &&
                        tp.hp_step == hp_step && moe::tc_layer_blocks_per_sm(tp) >= 1;
-  } else {
+  } else if (!affine) {
     ctx->decode_ok = single && moe::decode_plan(dp, ctx->max_smem, ctx->num_sms) && moe::decode_blocks_per_sm(dp) >= 1;
   }
   *out = ctx;
@@ -352,6 +370,8 @@ int moe_load_shared_gate(moe_ctx* ctx, const float* w) {
 int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) {
   if (!ctx) return MOE_ERR_INVALID_ARG;
   if (!codes || !scales) return fail(ctx, MOE_ERR_INVALID_ARG, "codes or scales are NULL");
+  if (ctx->base.aff_bits)
+    return fail(ctx, MOE_ERR_INVALID_ARG, "the context holds affine experts: load them with moe_load_experts_affine");
   DeviceGuard guard(ctx->device);
   const int d = ctx->cfg.d, F = ctx->cfg.ffn;
   const int E = ctx->base.e_end - ctx->base.e_begin;                 // routed experts the context holds
@@ -409,6 +429,47 @@ int moe_load_experts(moe_ctx* ctx, const uint8_t* codes, const uint8_t* scales) 
   }
   ctx->experts_loaded = true;
   return rc;
+}
+
+int moe_load_experts_affine(moe_ctx* ctx, const uint8_t* experts) {
+  if (!ctx) return MOE_ERR_INVALID_ARG;
+  if (!experts) return fail(ctx, MOE_ERR_INVALID_ARG, "experts is NULL");
+  const int bits = ctx->base.aff_bits;
+  if (!bits) return fail(ctx, MOE_ERR_INVALID_ARG, "the context holds MXFP4 experts: load them with moe_load_experts");
+  DeviceGuard guard(ctx->device);
+  const int d = ctx->cfg.d, F = ctx->cfg.ffn;
+  const int E = ctx->base.e_end - ctx->base.e_begin;
+  const int S = ctx->base.e_begin == 0 ? ctx->cfg.shared_ffn : 0;
+  const size_t cs = moe::aff_expert_bytes(d, F, bits);  // canonical bytes per routed expert (= repacked bytes)
+  const size_t cs_s = S > 0 ? moe::aff_expert_bytes(d, S, bits) : 0;
+  const int per_chunk = (int)std::max<size_t>(1, ((size_t)256 << 20) / cs);
+  uint8_t* st = nullptr;
+  cudaError_t e = cudaMalloc(&st, std::max(cs * (size_t)std::min(per_chunk, std::max(E, 1)), cs_s));
+  if (e != cudaSuccess) return fail(ctx, MOE_ERR_NOMEM, std::string("staging cudaMalloc: ") + cudaGetErrorString(e));
+  e = cudaMemset(ctx->load_err, 0, 4);
+  for (int x0 = 0; x0 < E && e == cudaSuccess; x0 += per_chunk) {
+    const int n = std::min(per_chunk, E - x0);
+    if ((e = cudaMemcpy(st, experts + (size_t)x0 * cs, cs * n, cudaMemcpyDefault)) != cudaSuccess) break;
+    if ((e = moe::launch_repack_affine(st, n, d, F, bits, cs, ctx->packed + (size_t)x0 * ctx->expert_stride,
+                                       ctx->expert_stride, ctx->load_err, 0)) != cudaSuccess)
+      break;
+    e = cudaDeviceSynchronize();
+  }
+  if (e == cudaSuccess && S > 0 &&
+      (e = cudaMemcpy(st, experts + (size_t)E * cs, cs_s, cudaMemcpyDefault)) == cudaSuccess &&
+      (e = moe::launch_repack_affine(st, 1, d, S, bits, cs_s, ctx->packed + (size_t)E * ctx->expert_stride, cs_s,
+                                     ctx->load_err, 0)) == cudaSuccess)
+    e = cudaDeviceSynchronize();
+  int bad = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bad, ctx->load_err, 4, cudaMemcpyDeviceToHost);
+  cudaFree(st);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "affine expert load");
+  if (bad) {
+    ctx->experts_loaded = false;
+    return fail(ctx, MOE_ERR_NAN_SCALE, "an affine scale or bias is Inf or NaN");
+  }
+  ctx->experts_loaded = true;
+  return MOE_OK;
 }
 
 int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream) {

@@ -44,51 +44,6 @@ constexpr int kHC = 4;                  // k tiles per h chunk
 constexpr int kXS = kXC * 64 + 32;      // f16 per row of an x chunk
 constexpr int kHS = kHC * 64 + 32;      // f16 per (row, plane) of an h chunk
 
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// Arrive on `bar` once all of this thread's earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Bounded wait for a staged chunk (its copies always land; the bound only
-// guarantees that no wait can hang): on expiry the status word says timeout.
-__device__ __forceinline__ void wait_chunk(uint64_t* bar, uint32_t parity, int* status) {
-  if (mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if ((long long)(globaltimer() - t0) > 50000000LL) {
-      atomicCAS(status, 0, MOE_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
-// D = A * B (no accumulator input).
-__device__ __forceinline__ void mma_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};\n"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-__device__ __forceinline__ int find_unit_slot(const int32_t* prefix, int n, int unit) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= unit) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
 // A unit of either GEMM: slot, group of kGemmTiles weight tiles, block of rows.
 struct GUnit {
   int e, f;      // expert (E = shared), its ffn

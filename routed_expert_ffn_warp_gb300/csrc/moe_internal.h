@@ -95,6 +95,41 @@ __host__ __device__ inline size_t tc_down_bytes(int d, int f) {
   return (size_t)tc_dn_pairs(d) * tc_ksteps(f) * kTcPairBytes;
 }
 
+// ---------------------------------------------------------------- affine group-64 experts
+//
+// Second weight format: w = scale * q + bias with q an unsigned `bits`-bit code
+// and one bf16 scale and one bf16 bias per 64 consecutive weights along the
+// reduction axis. Canonical layout per expert (what the load call takes): the
+// codes of the gate/up rows [2f][d] then of the down rows [d][f], each row one
+// little-endian bit stream (element c at bits [bits c, bits c + bits)); then
+// the scales of gate/up [2f][d/64] and of down [d][f/64]; then the biases in
+// the same order. The library repacks every expert into tiles of 16 rows x 64
+// columns (one group of each row), aff_tile_bytes(bits) bytes:
+//  * 128 bits code bytes. Lane L = 4 g + c of a warp owns the `bits` 32-bit
+//    words at byte 4 bits L. They carry the lane's 16 code pairs p = 4 kb + r
+//    of the m16n8k16 A fragments (kb: k16 block, r: A register): row
+//    g + 8 (r & 1), columns 16 kb + 4 c + 2 (r >> 1) and the column after it.
+//    Pair p's first code is field p (bits [bits p, bits p + bits)) of a
+//    16 bits-bit "first" stream, its second code field p of a "second" stream;
+//    word j holds bits [16 j, 16 j + 16) of the first stream in its low half
+//    and the same bits of the second stream in its high half, so a shift and a
+//    mask give both codes of an A register at once.
+//  * 64 bytes: for row pair (g, g + 8) the 64-bit word at 8 g: bf16 scale of
+//    row g | scale of row g + 8 << 16, then bias of row g | bias of row g + 8 << 16.
+// Gate/up pair tile tau holds gate rows 16 tau .. 16 tau + 15 and up rows
+// f + 16 tau ..; tiles ordered [tau][kt][gate, up], then the down tiles [m][kt]
+// (rows 16 m ..). A repacked expert has as many bytes as its canonical form.
+__host__ __device__ inline int aff_tile_bytes(int bits) { return 128 * bits + 64; }
+__host__ __device__ inline size_t aff_gu_bytes(int d, int f, int bits) {
+  return (size_t)(f / 16) * (size_t)(d / 64) * 2 * aff_tile_bytes(bits);
+}
+__host__ __device__ inline size_t aff_expert_bytes(int d, int f, int bits) {
+  return (size_t)3 * (size_t)(f / 16) * (size_t)(d / 64) * aff_tile_bytes(bits);
+}
+// Rows (pairs) per work item of the affine GEMMs; one item = (slot, one
+// 16-row weight tile, block of up to kAffRows rows of the slot).
+constexpr int kAffRows = 32;
+
 // ---------------------------------------------------------------- forward parameters
 
 struct FwdParams;
@@ -123,8 +158,12 @@ struct FwdParams {
   const float* w_router; // [E][d]
   const float* bias;     // [E] or nullptr
   const float* w_sg;     // [d] shared-expert gate row, or nullptr (shared expert added with weight 1)
-  const uint8_t* packed; // packed experts
+  const uint8_t* packed; // packed experts (the affine tiles when aff_bits > 0)
   size_t expert_stride;  // packed bytes per routed expert
+  int aff_bits;          // 0: MXFP4 experts; 2..8: affine group-64 experts of that code width
+  float* xgsum;          // affine: [t_max][xg_pitch] sum of each 64-element group of x16 (else null)
+  int xg_pitch;
+  float* hbsum;          // affine: [Q_max][hgroups] sum of each 16-element group of h (as its f16 planes hold it)
   // workspace
   uint16_t* x16;         // f16 [t_max][d64], x * 2^sigma_t
   float* xinv;           // [t_max]: 2^-sigma_t
@@ -254,6 +293,16 @@ cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int n
 // then one panel per (slot, token block) and K step.
 cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
+// The same GEMMs for affine group-64 experts (moe_affine.cu): one warp per
+// work item (gu_prefix / dn_prefix count items when aff_bits > 0).
+cudaError_t configure_affine();
+bool affine_bits_supported(int bits);
+cudaError_t launch_affine_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
+cudaError_t launch_affine_down(const FwdParams& p, cudaStream_t stream, int num_sms);
+// Affine tiles of n_exp experts (ffn f) from their canonical bytes (canon_stride
+// apart); a scale or bias that is not finite sets *err_flag.
+cudaError_t launch_repack_affine(const uint8_t* canon, int n_exp, int d, int f, int bits, size_t canon_stride,
+                                 uint8_t* out, size_t out_stride, int* err_flag, cudaStream_t stream);
 
 // Launchers (moe_kernels.cu). All are asynchronous on `stream`.
 // `events` (may be null) receives forward_phases(p) + 1 cudaEvent_t to record

@@ -59,6 +59,14 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
   for (int i = threadIdx.x; i < p.d; i += blockDim.x)
     dst[i] = __float2half_rn(__uint_as_float((uint32_t)xt[i] << 16) * sc);
   if (threadIdx.x == 0) p.xinv[t] = pow2f(-s);
+  if (p.xgsum) {  // affine experts: the sum of every 64-element group of the f16 x, in element order
+    __syncthreads();
+    for (int g = threadIdx.x; g < p.d / 64; g += blockDim.x) {
+      float a = 0.f;
+      for (int i = 0; i < 64; ++i) a += __half2float(dst[64 * g + i]);
+      p.xgsum[(size_t)t * p.xg_pitch + g] = a;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- router
@@ -623,10 +631,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   }
   // work list
   const bool nz = tid < E && cnt > 0 && expert_in_shard(tid, p.e_begin, p.e_end);  // this shard's experts
-  const int blocks = (cnt + kGemmRows - 1) / kGemmRows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
-  const int ugu = !nz ? 0
-                      : p.tc_gateup ? tcb * tc_gu_pairs(p.F) : blocks * ((p.F / 16 + kGemmTiles - 1) / kGemmTiles);
-  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dn_pairs(p.d) : blocks * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+  // register-decode units: kGemmTiles tiles x kGemmRows rows; affine items: 1 tile x kAffRows rows
+  const int rows = p.aff_bits ? kAffRows : kGemmRows, gt = p.aff_bits ? 1 : kGemmTiles;
+  const int blocks = (cnt + rows - 1) / rows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
+  const int ugu = !nz ? 0 : p.tc_gateup ? tcb * tc_gu_pairs(p.F) : blocks * ((p.F / 16 + gt - 1) / gt);
+  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dn_pairs(p.d) : blocks * ((p.d / 16 + gt - 1) / gt);
   int ns, gu, dn, pn;
   const int slot = block_exclusive_scan(nz ? 1 : 0, wsum, &ns);
   const int gpre = block_exclusive_scan(ugu, wsum, &gu);
@@ -649,11 +658,9 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       p.dn_prefix[ns] = dn;
       if (p.tc_gateup) p.panel_prefix[ns] = pn;
       pn += (T + kTcGemmRows - 1) / kTcGemmRows;
-      const int sb = (T + kGemmRows - 1) / kGemmRows;
-      gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_gu_pairs(p.S)
-                        : sb * ((p.S / 16 + kGemmTiles - 1) / kGemmTiles);
-      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dn_pairs(p.d)
-                        : sb * ((p.d / 16 + kGemmTiles - 1) / kGemmTiles);
+      const int sb = (T + rows - 1) / rows;
+      gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_gu_pairs(p.S) : sb * ((p.S / 16 + gt - 1) / gt);
+      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dn_pairs(p.d) : sb * ((p.d / 16 + gt - 1) / gt);
       ++ns;
     }
     p.gu_prefix[ns] = gu;
@@ -800,10 +807,14 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
     if ((e = launch_panels_tc(p, stream)) != cudaSuccess) return e;
     mark();
   }
-  e = p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms) : launch_gemm_gateup(p, stream, num_sms);
+  e = p.aff_bits    ? launch_affine_gateup(p, stream, num_sms)
+      : p.tc_gateup ? launch_gemm_gateup_tc(p, stream, num_sms)
+                    : launch_gemm_gateup(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   mark();
-  e = p.tc_gateup ? launch_gemm_down_tc(p, stream, num_sms) : launch_gemm_down(p, stream, num_sms);
+  e = p.aff_bits    ? launch_affine_down(p, stream, num_sms)
+      : p.tc_gateup ? launch_gemm_down_tc(p, stream, num_sms)
+                    : launch_gemm_down(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   mark();
   launch_chained(combine_kernel, dim3((p.d + 255) / 256, p.T), dim3(256), 0, stream, p);

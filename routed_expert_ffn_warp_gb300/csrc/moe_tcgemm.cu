@@ -93,16 +93,6 @@ constexpr size_t tc_smem_fixed() {
   return (size_t)Mode<kDown>::kS * Mode<kDown>::kStage + Mode<kDown>::kEpiSmem + 8 * (3 * Mode<kDown>::kS + 4) + 16;
 }
 
-__device__ __forceinline__ int find_unit_slot(const int32_t* prefix, int n, int unit) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= unit) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
 struct SlotTab {
   const int* upre;   // units before each slot
   const int* ppre;   // panels before each slot
