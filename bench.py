@@ -58,12 +58,17 @@ UNIT = "tokens/s"
 
 # ---------------------------------------------------------------- algorithmic work (per layer)
 
+def expert_bytes(wl: synth.Workload, f: int | None = None) -> int:
+    """Stored bytes of one expert of ffn f in the workload's format (MXFP4 or affine group-64)."""
+    return wl.affine_bytes(f) if wl.affine_bits else wl.expert_bytes(f)
+
+
 def layer_bytes(wl: synth.Workload, U: int, T: int) -> int:
     """Bytes the method must move for one layer call: the U distinct routed experts
     (+ the shared expert), router weights (+ bias), x in and y out (bf16)."""
-    b = U * wl.expert_bytes() + wl.E * wl.d * 4 + 2 * T * wl.d + 2 * T * wl.d
+    b = U * expert_bytes(wl) + wl.E * wl.d * 4 + 2 * T * wl.d + 2 * T * wl.d
     if wl.shared_ffn:
-        b += wl.expert_bytes(wl.shared_ffn)
+        b += expert_bytes(wl, wl.shared_ffn)
     if wl.zipf_bias:
         b += 4 * wl.E
     return b
@@ -71,8 +76,9 @@ def layer_bytes(wl: synth.Workload, U: int, T: int) -> int:
 
 def phase_bytes(wl: synth.Workload, U: int, T: int) -> dict:
     d, F, S = wl.d, wl.ffn, wl.shared_ffn
-    gu = U * (F * d + F * d // 16) + (S * d + S * d // 16 if S else 0) + 2 * T * d
-    dn = U * (F * d // 2 + F * d // 32) + (S * d // 2 + S * d // 32 if S else 0)
+    # gate/up holds 2/3 of an expert's bytes, down 1/3, in either format
+    gu = U * 2 * expert_bytes(wl) // 3 + (2 * expert_bytes(wl, S) // 3 if S else 0) + 2 * T * d
+    dn = U * expert_bytes(wl) // 3 + (expert_bytes(wl, S) // 3 if S else 0)
     route = wl.E * d * 4 + (4 * wl.E if wl.zipf_bias else 0) + 2 * T * d
     # "layer" is the fused single-kernel path (T <= 16): every byte of the layer in one launch;
     # "panels" (tcgen05 path) reads x once
@@ -289,7 +295,8 @@ def run_reference(args, wl):
 def config_of(wl: synth.Workload, args, layers: int | None = None) -> dict:
     nl = args.layers if layers is None else layers
     return {"workload": f"{wl.name}: MoE layer T={wl.T}, d={wl.d}, ffn={wl.ffn}, E={wl.E}, k={wl.k}, "
-                        f"shared_ffn={wl.shared_ffn}, zipf_bias={wl.zipf_bias}, layers={nl}, MXFP4 experts",
+                        f"shared_ffn={wl.shared_ffn}, zipf_bias={wl.zipf_bias}, layers={nl}, "
+                        + (f"{wl.affine_bits}-bit affine group-64 experts" if wl.affine_bits else "MXFP4 experts"),
             "T": wl.T, "d": wl.d, "ffn": wl.ffn, "n_experts": wl.E, "top_k": wl.k, "shared_ffn": wl.shared_ffn,
             "layers": nl, "zipf_bias": wl.zipf_bias, "parallelism": f"replica x{args.gpus}",
             "l2": "inputs larger than L2: each step streams every layer's routed experts from HBM; no flush"}
@@ -301,16 +308,26 @@ def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank:
                      peaks: dict) -> dict:
     """All layers of one workload resident; graph-timed value, per-phase roofline, e2e."""
     T = wl.T
-    shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T, flags=args.flags)
-    codes_h = torch.empty((wl.total_code_bytes,), dtype=torch.uint8, pin_memory=True)
-    scales_h = torch.empty((wl.total_scale_bytes,), dtype=torch.uint8, pin_memory=True)
+    if wl.affine_bits:
+        shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T, flags=args.flags & ~4,
+                             weight_format=m.MOE_FORMAT_AFFINE64, weight_bits=wl.affine_bits)
+        codes_h = torch.empty((wl.total_affine_bytes,), dtype=torch.uint8, pin_memory=True)
+        scales_h = None
+    else:
+        shape = m.LayerShape(wl.d, wl.ffn, wl.E, wl.k, wl.shared_ffn, t_max=T, flags=args.flags)
+        codes_h = torch.empty((wl.total_code_bytes,), dtype=torch.uint8, pin_memory=True)
+        scales_h = torch.empty((wl.total_scale_bytes,), dtype=torch.uint8, pin_memory=True)
     layers, xs, outs, xh, oh = [], [], [], [], []
     t_gen = time.perf_counter()
     for l in range(nl):
         L = synth.gen_layer(wl, l, with_experts=False)
-        synth.gen_experts(wl, wl.seed(l), codes_h.numpy(), scales_h.numpy())
         lay = m.MoeLayer(shape, device=local)
-        lay.load(L["w_router"], L["bias"], codes_h, scales_h)
+        if wl.affine_bits:
+            synth.gen_experts_affine(wl, wl.seed(l), codes_h.numpy())
+            lay.load_affine(L["w_router"], L["bias"], codes_h)
+        else:
+            synth.gen_experts(wl, wl.seed(l), codes_h.numpy(), scales_h.numpy())
+            lay.load(L["w_router"], L["bias"], codes_h, scales_h)
         layers.append(lay)
         x = rank_x(wl, l, rank)
         xh.append(torch.from_numpy(x.view(np.int16).copy()).pin_memory())
@@ -508,6 +525,8 @@ def run_ours(args, wl):
         res["config"] = config_of(wx, args, wx.layers)
         if name.startswith("prefill"):
             res["tensor"] = prefill_tensor_view(res, mma, peaks)
+        if wx.affine_bits:
+            res["dtype"] = f"affine{wx.affine_bits}-f16-f32acc"
         extras[name] = res
 
     cpu = None
@@ -561,7 +580,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle wall time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="moe_config.flags of every layer (e.g. 8: register-decode GEMMs instead of tcgen05)")
-    ap.add_argument("--extra-workloads", default="verify,small,prefill,prefill16k",
+    ap.add_argument("--extra-workloads", default="verify,small,prefill,prefill16k,affine3",
                     help="comma-separated workloads measured after the main one and reported under 'workloads' "
                          "('' for none)")
     ap.add_argument("--no-mma-probe", action="store_true")

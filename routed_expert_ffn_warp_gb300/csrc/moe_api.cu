@@ -195,6 +195,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   // affine experts: group sums of x (per 64) and of h (per 16)
   const int xg_pitch = (d / 64 + 3) / 4 * 4;
   const size_t o_xg = take(affine ? (size_t)Tm * xg_pitch * 4 : 0), o_hb = take(affine ? Qm * hgroups * 4 : 0);
+  // a row of zeros that absent activation rows of the affine GEMMs read (never written)
+  const size_t o_zero = take(affine ? (size_t)4 * std::max(d64, fmax64) : 0);
   // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
   const size_t Qd = (size_t)std::min(Tm, moe::kDecodeMaxT) * (k + (S > 0 ? 1 : 0));  // pair rows of the fused path
   const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
@@ -253,6 +255,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   p.xgsum = affine ? reinterpret_cast<float*>(w + o_xg) : nullptr;
   p.xg_pitch = xg_pitch;
   p.hbsum = affine ? reinterpret_cast<float*>(w + o_hb) : nullptr;
+  p.zeros = affine ? w + o_zero : nullptr;
   p.x16 = reinterpret_cast<uint16_t*>(w + o_x16);
   p.xinv = reinterpret_cast<float*>(w + o_xinv);
   p.tcw = ctx->tcw;

@@ -126,9 +126,12 @@ __host__ __device__ inline size_t aff_gu_bytes(int d, int f, int bits) {
 __host__ __device__ inline size_t aff_expert_bytes(int d, int f, int bits) {
   return (size_t)3 * (size_t)(f / 16) * (size_t)(d / 64) * aff_tile_bytes(bits);
 }
-// Rows (pairs) per work item of the affine GEMMs; one item = (slot, one
-// 16-row weight tile, block of up to kAffRows rows of the slot).
-constexpr int kAffRows = 32;
+// Rows (pairs) per work unit of the affine GEMMs; a gate/up unit = (slot, one
+// 16-row pair tile, block of up to kAffRows rows of the slot).
+constexpr int kAffRows = 16;
+// Row tiles per down work unit of the affine GEMMs: unit = (slot, kAffDnTiles
+// 16-row tiles of d, block of rows).
+constexpr int kAffDnTiles = 4;
 
 // ---------------------------------------------------------------- forward parameters
 
@@ -161,9 +164,11 @@ struct FwdParams {
   const uint8_t* packed; // packed experts (the affine tiles when aff_bits > 0)
   size_t expert_stride;  // packed bytes per routed expert
   int aff_bits;          // 0: MXFP4 experts; 2..8: affine group-64 experts of that code width
-  float* xgsum;          // affine: [t_max][xg_pitch] sum of each 64-element group of x16 (else null)
+  float* xgsum;          // affine: [t_max][xg_pitch] sum of each 64-element group of x16, times 2^-24 (else null)
   int xg_pitch;
-  float* hbsum;          // affine: [Q_max][hgroups] sum of each 16-element group of h (as its f16 planes hold it)
+  float* hbsum;          // affine: [Q_max][hgroups] sum of each 16-element group of h (as its f16 planes hold
+                         // it) times 2^-24; xgsum holds its sums times 2^-24 too
+  const void* zeros;     // affine: a zero row (4 max(d64, fmax64) bytes) for absent activation rows
   // workspace
   uint16_t* x16;         // f16 [t_max][d64], x * 2^sigma_t
   float* xinv;           // [t_max]: 2^-sigma_t
@@ -293,8 +298,8 @@ cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int n
 // then one panel per (slot, token block) and K step.
 cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_gemm_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);
-// The same GEMMs for affine group-64 experts (moe_affine.cu): one warp per
-// work item (gu_prefix / dn_prefix count items when aff_bits > 0).
+// The same GEMMs for affine group-64 experts (moe_affine.cu): gu_prefix /
+// dn_prefix count their units when aff_bits > 0.
 cudaError_t configure_affine();
 bool affine_bits_supported(int bits);
 cudaError_t launch_affine_gateup(const FwdParams& p, cudaStream_t stream, int num_sms);

@@ -59,12 +59,13 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
   for (int i = threadIdx.x; i < p.d; i += blockDim.x)
     dst[i] = __float2half_rn(__uint_as_float((uint32_t)xt[i] << 16) * sc);
   if (threadIdx.x == 0) p.xinv[t] = pow2f(-s);
-  if (p.xgsum) {  // affine experts: the sum of every 64-element group of the f16 x, in element order
-    __syncthreads();
-    for (int g = threadIdx.x; g < p.d / 64; g += blockDim.x) {
-      float a = 0.f;
-      for (int i = 0; i < 64; ++i) a += __half2float(dst[64 * g + i]);
-      p.xgsum[(size_t)t * p.xg_pitch + g] = a;
+  if (p.xgsum) {  // affine experts: the sum of every 64-element group of the f16 x, one warp per group
+    __syncthreads();  // (fixed order: element pairs per lane, then a butterfly over the lanes)
+    const int lane = threadIdx.x & 31;
+    for (int g = threadIdx.x >> 5; g < p.d / 64; g += blockDim.x >> 5) {
+      float a = __half2float(dst[64 * g + 2 * lane]) + __half2float(dst[64 * g + 2 * lane + 1]);
+      for (int o = 1; o < 32; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (lane == 0) p.xgsum[(size_t)t * p.xg_pitch + g] = a * 0x1p-24f;  // the scale of the codes' f16 form
     }
   }
 }
@@ -631,11 +632,13 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   }
   // work list
   const bool nz = tid < E && cnt > 0 && expert_in_shard(tid, p.e_begin, p.e_end);  // this shard's experts
-  // register-decode units: kGemmTiles tiles x kGemmRows rows; affine items: 1 tile x kAffRows rows
-  const int rows = p.aff_bits ? kAffRows : kGemmRows, gt = p.aff_bits ? 1 : kGemmTiles;
+  // register-decode units: kGemmTiles tiles x kGemmRows rows; affine units: 1 pair tile (gate/up) or
+  // kAffDnTiles row tiles (down) x kAffRows rows
+  const int rows = p.aff_bits ? kAffRows : kGemmRows, gt = p.aff_bits ? 1 : kGemmTiles,
+            dt = p.aff_bits ? kAffDnTiles : kGemmTiles;
   const int blocks = (cnt + rows - 1) / rows, tcb = (cnt + kTcGemmRows - 1) / kTcGemmRows;
   const int ugu = !nz ? 0 : p.tc_gateup ? tcb * tc_gu_pairs(p.F) : blocks * ((p.F / 16 + gt - 1) / gt);
-  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dn_pairs(p.d) : blocks * ((p.d / 16 + gt - 1) / gt);
+  const int udn = !nz ? 0 : p.tc_gateup ? tcb * tc_dn_pairs(p.d) : blocks * ((p.d / 16 + dt - 1) / dt);
   int ns, gu, dn, pn;
   const int slot = block_exclusive_scan(nz ? 1 : 0, wsum, &ns);
   const int gpre = block_exclusive_scan(ugu, wsum, &gu);
@@ -660,7 +663,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
       pn += (T + kTcGemmRows - 1) / kTcGemmRows;
       const int sb = (T + rows - 1) / rows;
       gu += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_gu_pairs(p.S) : sb * ((p.S / 16 + gt - 1) / gt);
-      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dn_pairs(p.d) : sb * ((p.d / 16 + gt - 1) / gt);
+      dn += p.tc_gateup ? (T + kTcGemmRows - 1) / kTcGemmRows * tc_dn_pairs(p.d) : sb * ((p.d / 16 + dt - 1) / dt);
       ++ns;
     }
     p.gu_prefix[ns] = gu;
