@@ -95,8 +95,23 @@ __device__ __forceinline__ void aff_frag(const uint32_t (&w)[B], uint32_t (&a)[4
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-// 8 bytes of activations (shared or global memory, through a generic address)
-__device__ __forceinline__ uint2 ld8(const uint16_t* p) { return *reinterpret_cast<const uint2*>(p); }
+// Activations: global memory (read-only path) or staged in shared memory (32-bit addresses).
+__device__ __forceinline__ uint2 ldg8(const uint16_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ uint2 lds8(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds4f(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds16f(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
 
 __device__ __forceinline__ int token_of_row(const FwdParams& p, int q) { return q < p.P ? p.perm[q] / p.k : q - p.P; }
 
@@ -198,6 +213,8 @@ __device__ __forceinline__ void load_tile(const uint8_t* tile, int lane, uint32_
 }
 
 // Activations of the launch: in shared memory when staged, else in global memory.
+// Staged, every array is followed by one row of zeros (row T, 2Q or Q) that
+// absent rows read; from global memory they read p.zeros.
 struct Act {
   const uint16_t* x;   // gate/up: x16 rows of tokens, xrow f16 apart
   int xrow;
@@ -208,6 +225,8 @@ struct Act {
   const float* hs;     // h scales and group sums per row q, hgrow floats apart
   const float* hb;
   int hgrow;
+  const uint16_t* zx;  // the zero rows of x (h) and of the per-row floats
+  const float* zf;
 };
 
 // Copy `rows` rows of `bytes` bytes (both strides multiples of 16) with all threads.
@@ -223,34 +242,36 @@ __device__ __forceinline__ void stage_rows(void* dst, int dst_stride, const void
 
 // Bytes of the staged activations of a call (0: they are read from global memory).
 __host__ __device__ inline int gu_stage_bytes(const FwdParams& p) {
-  const size_t b = (size_t)p.T * (p.d64 + kAXPad) * 2 + (size_t)p.T * p.xg_pitch * 4;
+  const size_t b = (size_t)(p.T + 1) * (p.d64 + kAXPad) * 2 + (size_t)(p.T + 1) * p.xg_pitch * 4;
   return b <= (size_t)kAStageMax ? (int)b : 0;
 }
 __host__ __device__ inline int dn_rows(const FwdParams& p) { return p.P + ((p.S > 0 && p.e_begin == 0) ? p.T : 0); }
 __host__ __device__ inline int dn_stage_bytes(const FwdParams& p) {
   const size_t q = (size_t)dn_rows(p);
-  const size_t b = q * 2 * (p.fmax64 + kAXPad) * 2 + q * p.hgroups * 4 * 2;
+  const size_t b = (2 * q + 1) * (p.fmax64 + kAXPad) * 2 + (q + 1) * p.hgroups * 4 * 2;
   return b <= (size_t)kAStageMax ? (int)b : 0;
 }
 
 // ---------------------------------------------------------------- gate/up
 
-template <int B, int NT>
+template <int B, int NT, bool S>
 __device__ void gu_share_compute(const FwdParams& p, const AUnit& un, const Share& sh, uint8_t* ring, int& slot,
                                  AStream& ws, const Act& A, float* red) {
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) % kAW, gq = lane >> 2, c = lane & 3;
-  const uint16_t* xr[NT];  // B fragment row 8 nt + gq: its token's x row (the zero row past the block)
+  const uint16_t* xr[NT];  // B fragment row 8 nt + gq: its token's x row (a zero row past the block)
   const float* xs[NT][2];  // C fragment column 8 nt + 2c + j: its token's group sums (zeros past the block)
+  uint32_t xa[NT], sa[NT][2];  // the same as shared-memory addresses (staged)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int m = 8 * nt + gq;
-    xr[nt] = m < un.n ? A.x + (size_t)token_of_row(p, un.q0 + m) * A.xrow + 4 * c
-                      : static_cast<const uint16_t*>(p.zeros);
+    xr[nt] = (m < un.n ? A.x + (size_t)token_of_row(p, un.q0 + m) * A.xrow : A.zx) + 4 * c;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int mc = 8 * nt + 2 * c + j;
-      xs[nt][j] = mc < un.n ? A.xg + (size_t)token_of_row(p, un.q0 + mc) * A.xgrow : static_cast<const float*>(p.zeros);
+      xs[nt][j] = mc < un.n ? A.xg + (size_t)token_of_row(p, un.q0 + mc) * A.xgrow : A.zf;
+      if (S) sa[nt][j] = smem_u32(xs[nt][j]);
     }
+    if (S) xa[nt] = smem_u32(xr[nt]);
   }
   float acc[2][NT][4];
 #pragma unroll
@@ -278,7 +299,7 @@ __device__ void gu_share_compute(const FwdParams& p, const AUnit& un, const Shar
     aff_frag<B, KB>(wd[0], a0);                                                                         \
     aff_frag<B, KB>(wd[1], a1);                                                                         \
     _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                                  \
-      const uint2 bx = ld8(xr[nt] + 64 * kt + 16 * KB);                                                  \
+      const uint2 bx = S ? lds8(xa[nt] + 2 * (64 * kt + 16 * KB)) : ldg8(xr[nt] + 64 * kt + 16 * KB);    \
       if (KB < 2) {                                                                                     \
         mma_z(t[KB & 1][0][nt], a0, bx.x, bx.y);                                                        \
         mma_z(t[KB & 1][1][nt], a1, bx.x, bx.y);                                                        \
@@ -296,7 +317,8 @@ __device__ void gu_share_compute(const FwdParams& p, const AUnit& un, const Shar
     // the group's affine terms: rows gq (C registers 0, 1) and gq + 8 (2, 3)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float xs0 = xs[nt][0][kt], xs1 = xs[nt][1][kt];
+      const float xs0 = S ? lds4f(sa[nt][0] + 4 * kt) : __ldg(xs[nt][0] + kt);
+      const float xs1 = S ? lds4f(sa[nt][1] + 4 * kt) : __ldg(xs[nt][1] + kt);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const float s0 = bf16_lo(sb[h].x), s1 = bf16_hi(sb[h].x);
@@ -386,26 +408,32 @@ __global__ void __launch_bounds__(kAThreads, 1) aff_gateup_kernel(FwdParams p) {
   uint64_t* sbar = reinterpret_cast<uint64_t*>(stage + kAStageMax);
   Act A{};
   const int stage_bytes = gu_stage_bytes(p);
-  if (stage_bytes) {  // x16 and its group sums of every token, before the weight streams start
+  if (stage_bytes) {  // x16 and its group sums of every token (+ a zero row each), before the weight streams
+    A.xrow = p.d64 + kAXPad;
+    A.xgrow = p.xg_pitch;
+    uint16_t* xs = reinterpret_cast<uint16_t*>(stage);
+    float* xg = reinterpret_cast<float*>(stage + (size_t)(p.T + 1) * A.xrow * 2);
+    A.x = xs;
+    A.xg = xg;
+    A.zx = xs + (size_t)p.T * A.xrow;
+    A.zf = xg + (size_t)p.T * A.xgrow;
     if (threadIdx.x == 0) {
       mbar_init(sbar, kAThreads);
       fence_mbar_init();
     }
+    for (int i = threadIdx.x; i < A.xrow; i += kAThreads) const_cast<uint16_t*>(A.zx)[i] = 0;
+    for (int i = threadIdx.x; i < A.xgrow; i += kAThreads) const_cast<float*>(A.zf)[i] = 0.f;
     __syncthreads();
-    A.xrow = p.d64 + kAXPad;
-    A.xgrow = p.xg_pitch;
-    uint16_t* xs = reinterpret_cast<uint16_t*>(stage);
-    float* xg = reinterpret_cast<float*>(stage + (size_t)p.T * A.xrow * 2);
     stage_rows(xs, A.xrow * 2, p.x16, p.d64 * 2, p.T, p.d64 * 2);
     stage_rows(xg, A.xgrow * 4, p.xgsum, p.xg_pitch * 4, p.T, p.xg_pitch * 4);
     cp_arrive(sbar);
-    A.x = xs;
-    A.xg = xg;
   } else {
     A.x = p.x16;
     A.xrow = p.d64;
     A.xg = p.xgsum;
     A.xgrow = p.xg_pitch;
+    A.zx = static_cast<const uint16_t*>(p.zeros);
+    A.zf = static_cast<const float*>(p.zeros);
   }
   AStream ws;
   ws.i = team;
@@ -419,8 +447,13 @@ __global__ void __launch_bounds__(kAThreads, 1) aff_gateup_kernel(FwdParams p) {
     const AUnit un = aff_unit(p, p.gu_prefix, blockIdx.x + i * gridDim.x, false);
     const Share sh = gu_share(p, un, w);
     float* rb = red + (size_t)(j & 1) * kAGuRedBuf;
-    if (un.n <= 8) gu_share_compute<B, 1>(p, un, sh, ring, slot, ws, A, rb);
-    else gu_share_compute<B, 2>(p, un, sh, ring, slot, ws, A, rb);
+    if (stage_bytes) {
+      if (un.n <= 8) gu_share_compute<B, 1, true>(p, un, sh, ring, slot, ws, A, rb);
+      else gu_share_compute<B, 2, true>(p, un, sh, ring, slot, ws, A, rb);
+    } else {
+      if (un.n <= 8) gu_share_compute<B, 1, false>(p, un, sh, ring, slot, ws, A, rb);
+      else gu_share_compute<B, 2, false>(p, un, sh, ring, slot, ws, A, rb);
+    }
     named_bar(1 + team, kATeamThreads);  // every warp's partial sums of the unit are in rb
     if (w == j % kAW) {
       if (un.n <= 8) gu_epilogue<1>(p, un, rb);
@@ -432,20 +465,25 @@ __global__ void __launch_bounds__(kAThreads, 1) aff_gateup_kernel(FwdParams p) {
 
 // ---------------------------------------------------------------- down
 
-template <int B, int NT>
+template <int B, int NT, bool S>
 __device__ void dn_share_compute(const FwdParams& p, const AUnit& un, const Share& sh, uint8_t* ring, int& slot,
                                  AStream& ws, const Act& A, float* red) {
   const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) % kAW, gq = lane >> 2, c = lane & 3;
   const uint16_t* hr[NT];  // B fragment row gq of n8 tile nt = (block row 4 nt + gq / 2, plane gq % 2)
   const float* hsr[NT];    // C fragment columns 2c, 2c + 1 = both planes of block row 4 nt + c: its scales
   const float* hbr[NT];    // ... and group sums (zero rows past the block)
+  uint32_t ha[NT], hsa[NT], hba[NT];  // the same as shared-memory addresses (staged)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int r = 4 * nt + (gq >> 1), rc = 4 * nt + c;
-    hr[nt] = r < un.n ? A.h + (size_t)((un.q0 + r) * 2 + (gq & 1)) * A.hrow + 4 * c
-                      : static_cast<const uint16_t*>(p.zeros);
-    hsr[nt] = rc < un.n ? A.hs + (size_t)(un.q0 + rc) * A.hgrow : static_cast<const float*>(p.zeros);
-    hbr[nt] = rc < un.n ? A.hb + (size_t)(un.q0 + rc) * A.hgrow : static_cast<const float*>(p.zeros);
+    hr[nt] = (r < un.n ? A.h + (size_t)((un.q0 + r) * 2 + (gq & 1)) * A.hrow : A.zx) + 4 * c;
+    hsr[nt] = rc < un.n ? A.hs + (size_t)(un.q0 + rc) * A.hgrow : A.zf;
+    hbr[nt] = rc < un.n ? A.hb + (size_t)(un.q0 + rc) * A.hgrow : A.zf;
+    if (S) {
+      ha[nt] = smem_u32(hr[nt]);
+      hsa[nt] = smem_u32(hsr[nt]);
+      hba[nt] = smem_u32(hbr[nt]);
+    }
   }
   float acc[NT][2];
 #pragma unroll
@@ -473,10 +511,10 @@ __device__ void dn_share_compute(const FwdParams& p, const AUnit& un, const Shar
     uint32_t a[4];                                                                                      \
     aff_frag<B, KB>(wd, a);                                                                             \
     _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) {                                                  \
-      const uint2 bh = ld8(hr[nt] + 64 * kt + 16 * KB);                                                  \
+      const uint2 bh = S ? lds8(ha[nt] + 2 * (64 * kt + 16 * KB)) : ldg8(hr[nt] + 64 * kt + 16 * KB);    \
       float t[4];                                                                                       \
       mma_z(t, a, bh.x, bh.y);                                                                          \
-      const float hs = hsr[nt][4 * kt + KB];                                                            \
+      const float hs = S ? lds4f(hsa[nt] + 4 * (4 * kt + KB)) : __ldg(hsr[nt] + 4 * kt + KB);            \
       gp[nt][0] = fmaf(t[0] + t[1], hs, gp[nt][0]);                                                     \
       gp[nt][1] = fmaf(t[2] + t[3], hs, gp[nt][1]);                                                     \
     }                                                                                                   \
@@ -490,7 +528,7 @@ __device__ void dn_share_compute(const FwdParams& p, const AUnit& un, const Shar
     const float b0 = bf16_lo(sb.y), b1 = bf16_hi(sb.y);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float4 g = *reinterpret_cast<const float4*>(hbr[nt] + 4 * kt);
+      const float4 g = S ? lds16f(hba[nt] + 16 * kt) : __ldg(reinterpret_cast<const float4*>(hbr[nt] + 4 * kt));
       const float hsum = ((g.x + g.y) + g.z) + g.w;
       acc[nt][0] = fmaf(s0, gp[nt][0], fmaf(b0, hsum, acc[nt][0]));
       acc[nt][1] = fmaf(s1, gp[nt][1], fmaf(b1, hsum, acc[nt][1]));
@@ -541,31 +579,37 @@ __global__ void __launch_bounds__(kAThreads, 1) aff_down_kernel(FwdParams p) {
   uint64_t* sbar = reinterpret_cast<uint64_t*>(stage + kAStageMax);
   Act A{};
   const int stage_bytes = dn_stage_bytes(p);
-  if (stage_bytes) {  // both h planes, scales and group sums of every row, before the weight streams start
-    if (threadIdx.x == 0) {
-      mbar_init(sbar, kAThreads);
-      fence_mbar_init();
-    }
-    __syncthreads();
+  if (stage_bytes) {  // both h planes, scales and group sums of every row (+ zero rows), before the weight streams
     const int Q = dn_rows(p);
     A.hrow = p.fmax64 + kAXPad;
     A.hgrow = p.hgroups;
     uint16_t* hs = reinterpret_cast<uint16_t*>(stage);
-    float* sc = reinterpret_cast<float*>(stage + (size_t)Q * 2 * A.hrow * 2);
-    float* gs = sc + (size_t)Q * A.hgrow;
+    float* sc = reinterpret_cast<float*>(stage + (size_t)(2 * Q + 1) * A.hrow * 2);
+    float* gs = sc + (size_t)(Q + 1) * A.hgrow;
+    A.h = hs;
+    A.hs = sc;
+    A.hb = gs;
+    A.zx = hs + (size_t)2 * Q * A.hrow;
+    A.zf = sc + (size_t)Q * A.hgrow;
+    if (threadIdx.x == 0) {
+      mbar_init(sbar, kAThreads);
+      fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < A.hrow; i += kAThreads) const_cast<uint16_t*>(A.zx)[i] = 0;
+    for (int i = threadIdx.x; i < A.hgrow; i += kAThreads) const_cast<float*>(A.zf)[i] = 0.f;
+    __syncthreads();
     stage_rows(hs, A.hrow * 2, p.hbuf, p.fmax64 * 2, 2 * Q, p.fmax64 * 2);
     stage_rows(sc, A.hgrow * 4, p.hscale, p.hgroups * 4, Q, p.hgroups * 4);
     stage_rows(gs, A.hgrow * 4, p.hbsum, p.hgroups * 4, Q, p.hgroups * 4);
     cp_arrive(sbar);
-    A.h = hs;
-    A.hs = sc;
-    A.hb = gs;
   } else {
     A.h = p.hbuf;
     A.hrow = p.fmax64;
     A.hs = p.hscale;
     A.hb = p.hbsum;
     A.hgrow = p.hgroups;
+    A.zx = static_cast<const uint16_t*>(p.zeros);
+    A.zf = static_cast<const float*>(p.zeros);
   }
   AStream ws;
   ws.i = team;
@@ -580,9 +624,15 @@ __global__ void __launch_bounds__(kAThreads, 1) aff_down_kernel(FwdParams p) {
     const Share sh = dn_share(p, un, w);
     float* rb = red + (size_t)(j & 1) * kADnRedBuf;
     const int nt = (un.n + 3) / 4;  // 4 block rows (both planes) per n8 tile
-    if (nt <= 1) dn_share_compute<B, 1>(p, un, sh, ring, slot, ws, A, rb);
-    else if (nt <= 2) dn_share_compute<B, 2>(p, un, sh, ring, slot, ws, A, rb);
-    else dn_share_compute<B, 4>(p, un, sh, ring, slot, ws, A, rb);
+    if (stage_bytes) {
+      if (nt <= 1) dn_share_compute<B, 1, true>(p, un, sh, ring, slot, ws, A, rb);
+      else if (nt <= 2) dn_share_compute<B, 2, true>(p, un, sh, ring, slot, ws, A, rb);
+      else dn_share_compute<B, 4, true>(p, un, sh, ring, slot, ws, A, rb);
+    } else {
+      if (nt <= 1) dn_share_compute<B, 1, false>(p, un, sh, ring, slot, ws, A, rb);
+      else if (nt <= 2) dn_share_compute<B, 2, false>(p, un, sh, ring, slot, ws, A, rb);
+      else dn_share_compute<B, 4, false>(p, un, sh, ring, slot, ws, A, rb);
+    }
     named_bar(1 + team, kATeamThreads);  // every warp's partial sums of the unit are in rb
     if (w < kADnTiles) {
       if (nt <= 1) dn_epilogue<1>(p, un, rb);
@@ -674,15 +724,16 @@ __global__ void repack_affine_kernel(const uint8_t* canon, int n_exp, int d, int
   }
 }
 
+// Both GEMMs join the forward chain's programmatic launches: each may be
+// scheduled while the grid before it drains and waits for it (pdl_enter)
+// before reading anything that grid wrote.
 template <int B>
 cudaError_t launch_gu(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  aff_gateup_kernel<B><<<num_sms, kAThreads, kAGuSmemMax, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(aff_gateup_kernel<B>, dim3(num_sms), dim3(kAThreads), kAGuSmemMax, stream, p);
 }
 template <int B>
 cudaError_t launch_dn(const FwdParams& p, cudaStream_t stream, int num_sms) {
-  aff_down_kernel<B><<<num_sms, kAThreads, kADnSmemMax, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(aff_down_kernel<B>, dim3(num_sms), dim3(kAThreads), kADnSmemMax, stream, p);
 }
 template <int B>
 cudaError_t configure_bits() {
