@@ -86,63 +86,71 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
 // selection equals that of double-float logits for all experts: an expert
 // whose upper bound is below the k-th largest lower bound is beaten by at
 // least k others.
-constexpr int kRfTok = 32, kRfExp = 32, kRfK = 128, kRfThreads = 128;
+constexpr int kRfTok = 64, kRfExp = 32, kRfK = 128, kRfThreads = 128;
+constexpr int kRfKS = 64;  // elements of d staged in shared memory at a time (half a partial sum)
 
 __device__ __forceinline__ float router_gamma(int d) {
   const float D = (float)(kRfK + (d + kRfK - 1) / kRfK + 3);
   return D * 0x1p-24f / (1.f - D * 0x1p-24f);
 }
 
-// Block (32 tokens, 32 experts, range z of d); thread (token pair tid / 8,
-// expert quad tid % 8) in the products. Loads: lane l takes token (expert) l,
-// warps and repeats step through K, so that the transposed stores to shared
-// memory hit 32 banks. The next chunk of x and W_r is loaded into registers
-// while the current one is multiplied out of shared memory.
+// Block (64 tokens, 32 experts, range z of d); thread (token quad tid / 8,
+// expert quad tid % 8) keeps 16 products in registers, two 16-byte shared
+// loads per 16 multiply-adds. Each partial sum runs over 128 elements of d
+// (two staged halves of 64) from zero, then is added to the thread's total.
+// Loads: x rows as 8-element groups (thread t takes token t % 64), W_r rows as
+// 4-element groups (thread t takes expert t % 32); warps step through K, so
+// the transposed stores to shared memory hit 32 banks. The next half is
+// loaded into registers while the current one is multiplied out of shared
+// memory. The squares of the loaded x (W_r) elements are summed by the 2 (4)
+// threads of a token (an expert) and added in thread order at the end.
 __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
   pdl_enter();
-  __shared__ __align__(16) float xs[kRfK][kRfTok + 4];  // [k][token]
-  __shared__ __align__(16) float ws[kRfK][kRfExp + 4];  // [k][expert]
-  __shared__ float nsq[2][kRfThreads / 32][32];         // per-warp sums of squares: x rows, W_r rows
-  constexpr int kXL = kRfTok * kRfK / 8 / kRfThreads;   // 8-element x loads per thread and chunk
-  constexpr int kWL = kRfExp * kRfK / 4 / kRfThreads;   // 4-element W_r loads per thread and chunk
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ __align__(16) float xs[kRfKS][kRfTok];  // [k][token]
+  __shared__ __align__(16) float ws[kRfKS][kRfExp];  // [k][expert]
+  __shared__ float nsq[kRfThreads];
+  constexpr int kXL = kRfTok * kRfKS / 8 / kRfThreads;  // 8-element x loads per thread and half
+  constexpr int kWL = kRfExp * kRfKS / 4 / kRfThreads;  // 4-element W_r loads per thread and half
+  const int tid = threadIdx.x;
   const int t0 = blockIdx.x * kRfTok, e0 = blockIdx.y * kRfExp, z = blockIdx.z;
   const int nch = (p.d + kRfK - 1) / kRfK, cps = (nch + p.rsplit - 1) / p.rsplit;
   const int kbeg = z * cps * kRfK, kend = min(p.d, (z + 1) * cps * kRfK);
   const int tt = tid >> 3, te = tid & 7;
-  float tot[2][4] = {};
-  float xsq = 0.f, wsq = 0.f;  // sums of squares of token t0 + lane's and expert e0 + lane's loaded elements
+  const int xt = tid % kRfTok, xg = tid / kRfTok;  // load role: token row, first 8-element group
+  const int we = tid % kRfExp, wg = tid / kRfExp;  // load role: expert row, first 4-element group
+  float tot[4][4] = {}, c[4][4] = {};
+  float xsq = 0.f, wsq = 0.f;
   uint4 xr[kXL];
   float4 wr[kWL];
-  const bool xok = t0 + lane < p.T, wok = e0 + lane < p.E;
-  const uint16_t* xrow = p.x + (size_t)(t0 + lane) * p.d;
-  const float* wrow = p.w_router + (size_t)(e0 + lane) * p.d;
+  const bool xok = t0 + xt < p.T, wok = e0 + we < p.E;
+  const uint16_t* xrow = p.x + (size_t)(t0 + xt) * p.d;
+  const float* wrow = p.w_router + (size_t)(e0 + we) * p.d;
   auto load = [&](int kc) {
 #pragma unroll
     for (int j = 0; j < kXL; ++j) {
-      const int k8 = 8 * (warp + (kRfThreads / 32) * j);
+      const int k8 = 8 * (xg + (kRfThreads / kRfTok) * j);
       xr[j] = make_uint4(0u, 0u, 0u, 0u);
       if (xok && kc + k8 < kend) xr[j] = __ldg(reinterpret_cast<const uint4*>(xrow + kc + k8));
     }
 #pragma unroll
     for (int j = 0; j < kWL; ++j) {
-      const int k4 = 4 * (warp + (kRfThreads / 32) * j);
+      const int k4 = 4 * (wg + (kRfThreads / kRfExp) * j);
       wr[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (wok && kc + k4 < kend) wr[j] = __ldg(reinterpret_cast<const float4*>(wrow + kc + k4));
     }
   };
   if (kbeg < kend) load(kbeg);
-  for (int kc = kbeg; kc < kend; kc += kRfK) {
+  for (int kc = kbeg; kc < kend; kc += kRfKS) {
 #pragma unroll
     for (int j = 0; j < kXL; ++j) {
-      const int k8 = 8 * (warp + (kRfThreads / 32) * j);
+      const int k8 = 8 * (xg + (kRfThreads / kRfTok) * j);
       const uint32_t w4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
       float sq = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float a = __uint_as_float(w4[q] << 16), b = __uint_as_float(w4[q] & 0xFFFF0000u);
-        xs[k8 + 2 * q][lane] = a;
-        xs[k8 + 2 * q + 1][lane] = b;
+        xs[k8 + 2 * q][xt] = a;
+        xs[k8 + 2 * q + 1][xt] = b;
         sq = fmaf(a, a, sq);
         sq = fmaf(b, b, sq);
       }
@@ -150,36 +158,41 @@ __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
     }
 #pragma unroll
     for (int j = 0; j < kWL; ++j) {
-      const int k4 = 4 * (warp + (kRfThreads / 32) * j);
-      ws[k4][lane] = wr[j].x;
-      ws[k4 + 1][lane] = wr[j].y;
-      ws[k4 + 2][lane] = wr[j].z;
-      ws[k4 + 3][lane] = wr[j].w;
+      const int k4 = 4 * (wg + (kRfThreads / kRfExp) * j);
+      ws[k4][we] = wr[j].x;
+      ws[k4 + 1][we] = wr[j].y;
+      ws[k4 + 2][we] = wr[j].z;
+      ws[k4 + 3][we] = wr[j].w;
       wsq += fmaf(wr[j].x, wr[j].x, fmaf(wr[j].y, wr[j].y, fmaf(wr[j].z, wr[j].z, wr[j].w * wr[j].w)));
     }
     __syncthreads();
-    if (kc + kRfK < kend) load(kc + kRfK);
-    float c[2][4] = {};
+    if (kc + kRfKS < kend) load(kc + kRfKS);
 #pragma unroll 16
-    for (int k = 0; k < kRfK; ++k) {
-      const float2 xv = *reinterpret_cast<const float2*>(&xs[k][2 * tt]);
+    for (int k = 0; k < kRfKS; ++k) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[k][4 * tt]);
       const float4 wv = *reinterpret_cast<const float4*>(&ws[k][4 * te]);
-      const float xa[2] = {xv.x, xv.y}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) c[a][b] = fmaf(xa[a], wa[b], c[a][b]);
     }
+    // a partial sum ends every 128 elements of d (and at the end of the range)
+    if (((kc - kbeg) / kRfKS) % (kRfK / kRfKS) == kRfK / kRfKS - 1 || kc + kRfKS >= kend) {
 #pragma unroll
-    for (int a = 0; a < 2; ++a)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) tot[a][b] += c[a][b];
+        for (int b = 0; b < 4; ++b) {
+          tot[a][b] += c[a][b];
+          c[a][b] = 0.f;
+        }
+    }
     __syncthreads();
   }
   float* plane = p.logit_hi + (size_t)z * p.lstride;  // partial sums of range z
 #pragma unroll
-  for (int a = 0; a < 2; ++a) {
-    const int t = t0 + 2 * tt + a;
+  for (int a = 0; a < 4; ++a) {
+    const int t = t0 + 4 * tt + a;
     if (t >= p.T) continue;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -187,15 +200,21 @@ __global__ void __launch_bounds__(kRfThreads) router_fp32_kernel(FwdParams p) {
       if (e < p.E) plane[(size_t)t * p.E + e] = tot[a][b];
     }
   }
-  // sums of squares of range z: the four warps' sums in warp order
-  nsq[0][warp][lane] = xsq;
-  nsq[1][warp][lane] = wsq;
+  // sums of squares of range z: a token's (expert's) threads in thread order
+  nsq[tid] = xsq;
   __syncthreads();
-  if (warp < 2) {
+  if (tid < kRfTok && blockIdx.y == 0 && xok) {
     float sq = 0.f;
-    for (int w = 0; w < kRfThreads / 32; ++w) sq += nsq[warp][w][lane];
-    if (warp == 0 && blockIdx.y == 0 && xok) p.xsq[(size_t)z * p.lstride / p.E + t0 + lane] = sq;
-    if (warp == 1 && blockIdx.x == 0 && wok) p.wsq[z * p.E + e0 + lane] = sq;
+    for (int i = 0; i < kRfThreads / kRfTok; ++i) sq += nsq[tid + kRfTok * i];
+    p.xsq[(size_t)z * p.lstride / p.E + t0 + tid] = sq;
+  }
+  __syncthreads();
+  nsq[tid] = wsq;
+  __syncthreads();
+  if (tid < kRfExp && blockIdx.x == 0 && wok) {
+    float sq = 0.f;
+    for (int i = 0; i < kRfThreads / kRfExp; ++i) sq += nsq[tid + kRfExp * i];
+    p.wsq[z * p.E + e0 + tid] = sq;
   }
 }
 
