@@ -26,8 +26,9 @@
 //      lane (TMA tensor copies that widen the E2M1 codes, plus the scale
 //      bytes), an activation producer lane (bulk copies of x or h steps once
 //      their flags carry this launch's number), two MMA lanes (M tiles 0 and
-//      1 of a unit), four warps moving each stage's scale factors into tensor
-//      memory, and eight epilogue warps.
+//      1 of a unit), each copying its stage's scale factors into tensor memory
+//      (tcgen05.cp) ahead of its MMAs, and eight epilogue warps; warps 4-7
+//      take part in phases A and B only.
 //
 // Weights come from the tcgen05 copies of the experts (tc_expert_bytes,
 // tc_down_bytes): nothing else is stored. Every wait is bounded; a CTA whose
