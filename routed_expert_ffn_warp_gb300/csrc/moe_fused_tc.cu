@@ -66,11 +66,12 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kProducerWarp = 0, kActWarp = 1, kMmaWarp0 = 2, kEpiWarp0 = 8, kEpiThreads = 256;
 constexpr int kHxTok = kDecodeMaxT;     // tokens the gate/up epilogue exchange holds
-// Work items whose whole weight range (K steps x 17,408 bytes, contiguous) the
-// producer starts towards L2 ahead of its tensor copies, one prefetch per
-// item: a CTA's tensor copies alone keep too few bytes in flight to cover HBM
-// latency, while HBM fills L2 at its full rate for every CTA at once.
-constexpr int kPfItems = 2;
+// K steps (17,408-byte weight blocks, across item boundaries) the producer
+// starts towards L2 ahead of its tensor copies: a CTA's few ring stages alone
+// keep too few bytes in flight to cover HBM latency, while HBM fills L2 at its
+// full rate for every CTA at once. A window, not whole items: whole items of
+// the large shapes put most of L2 in flight and evicted their own lines.
+constexpr int kPfSteps = 12;
 
 __host__ __device__ inline int npad8(int n) { return n <= 8 ? 8 : (n + 7) & ~7; }
 __host__ __device__ inline int tc_stage_bytes(int bslot) { return (kBOff + bslot + 1023) / 1024 * 1024; }
@@ -433,19 +434,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {  // weight blocks: a tensor copy of both tiles' codes (widened) and a bulk copy of their scales
-      auto prefetch_item = [&](int i) {
-        const TcItem it = tc_item(f, s, wk, i);
-        const size_t we = (size_t)weight_index(f, it.e);
-        const uint8_t* base = (it.down ? f.tcwd + we * f.tcwd_stride : f.tcw + we * f.tcw_stride) +
-                              (size_t)it.tile * it.nks * kTcPairBytes;
-        prefetch_l2(base, (uint32_t)(it.nks * kTcPairBytes));
+      // prefetch cursor: item pi, its K step ps, its first block pbase; pj blocks started so far
+      int pi = 0, ps = 0, pn = 0, pj = 0;
+      const uint8_t* pbase = nullptr;
+      auto prefetch_to = [&](int upto) {
+        while (pj < upto && pi < nit) {
+          if (ps == 0) {
+            const TcItem pt = tc_item(f, s, wk, pi);
+            const size_t we = (size_t)weight_index(f, pt.e);
+            pbase = (pt.down ? f.tcwd + we * f.tcwd_stride : f.tcw + we * f.tcw_stride) +
+                    (size_t)pt.tile * pt.nks * kTcPairBytes;
+            pn = pt.nks;
+          }
+          prefetch_l2(pbase + (size_t)ps * kTcPairBytes, (uint32_t)kTcPairBytes);
+          ++pj;
+          if (++ps == pn) {
+            ps = 0;
+            ++pi;
+          }
+        }
       };
-      for (int i = 0; i < nit && i < kPfItems; ++i) prefetch_item(i);
+      prefetch_to(kPfSteps);
       int j = 0;
       bool ok = true;
       for (int i = 0; i < nit && ok; ++i) {
         const TcItem it = tc_item(f, s, wk, i);
-        if (i + kPfItems < nit) prefetch_item(i + kPfItems);
         const size_t stride = it.down ? f.tcwd_stride : f.tcw_stride;  // a multiple of kTcPairBytes
         const size_t we = (size_t)weight_index(f, it.e);  // the expert's place in this context's copy
         const uint8_t* w0 = (it.down ? f.tcwd : f.tcw) + we * stride + (size_t)it.tile * it.nks * kTcPairBytes;
@@ -456,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          prefetch_to(j + 1 + kPfSteps);
           uint8_t* sb = ring + (size_t)st * sbytes;
           // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
           mbar_arrive_expect_tx(&full[st], (uint32_t)kTcPairBytes);
