@@ -213,9 +213,12 @@ __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volat
     scale_x_token(p, s, kWarps - 1 - warp);
   }
   __syncthreads();
+  if (p.f.P > 32) {  // the whole CTA sorts
+    bucket_large(p, s);
+    __syncthreads();
+  }
   if (warp == 0) {
     if (p.f.P <= 32) bucket_small(p, s);
-    else bucket_large(p, s);
     __syncwarp();
     build_halves(s);
   } else if (warp == 1 && blockIdx.x == 0 && p.f.P <= 32) {

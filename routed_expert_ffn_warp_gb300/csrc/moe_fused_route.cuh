@@ -385,87 +385,73 @@ __device__ void export_counts_small(const DecParams& p, const Shared& s) {
     f.offsets[x] = o;
   }
 }
-
-// Counting sort for larger P with one warp: histogram, exclusive scan, slots,
-// stable ranks within each bucket.
+// Counting sort of P > 32 pairs by expert with all kThreads threads of the
+// CTA (every thread must call it; ids are in shared memory): per-expert
+// counts by shared atomics, one block scan over the experts that yields both
+// the offsets and the slot list (count and "has pairs" packed in one word),
+// then every pair's stable rank among the earlier pairs of its expert. Three
+// CTA barriers instead of a single warp's long dependent chains.
 __device__ void bucket_large(const DecParams& p, const Shared& s) {
   const FwdParams& f = p.f;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = f.E, T = f.T, P = f.P;
   const bool writer = blockIdx.x == 0;
-  for (int q = lane; q < P; q += 32) atomicAdd(&s.cnt[s.ids[q]], 1);
-  __syncwarp();
-  int loc = 0;  // exclusive scan over E <= 512: lane owns experts [16 lane, 16 lane + 16)
-  for (int i = 0; i < 16; ++i) {
-    const int e = 16 * lane + i;
-    if (e < E) loc += s.cnt[e];
-  }
-  int inc = loc;
+  int* wsum = s.hs_half;  // [kWarps] scratch (the down halves are built after this)
+  for (int q = tid; q < P; q += kThreads) atomicAdd(&s.cnt[s.ids[q]], 1);
+  __syncthreads();
+  // expert tid: count in the high half, "a slot of this shard" in the low half
+  const int c = tid < E ? s.cnt[tid] : 0;
+  const int has = (c > 0 && expert_in_shard(tid, f.e_begin, f.e_end)) ? 1 : 0;
+  const int v = (c << 16) | has;
+  int inc = v;
   for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
+    const int u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
   }
-  int run = inc - loc;
-  for (int i = 0; i < 16; ++i) {
-    const int e = 16 * lane + i;
-    if (e < E) {
-      s.offs[e] = run;
-      run += s.cnt[e];
-    }
-  }
-  if (lane == 31) s.offs[E] = inc;
-  __syncwarp();
-  int ns = 0;  // slots: the experts that received pairs, in expert order
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    const int e = e0 + lane;
-    const bool has = e < E && s.cnt[e] > 0 && expert_in_shard(e, f.e_begin, f.e_end);
-    const unsigned bal = __ballot_sync(0xffffffffu, has);
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += wsum[w];
+  const int excl = before + inc - v;
+  if (tid < E) {
+    const int off = excl >> 16, slot = excl & 0xFFFF;
+    s.offs[tid] = off;
     if (has) {
-      const int pos = ns + __popc(bal & ((1u << lane) - 1u));
-      s.slot_e[pos] = e;
-      s.slot_n[pos] = s.cnt[e];
-      s.slot_q0[pos] = s.offs[e];
+      s.slot_e[slot] = tid;
+      s.slot_n[slot] = c;
+      s.slot_q0[slot] = off;
     }
-    ns += __popc(bal);
-  }
-  if (lane == 0) {
-    s.misc[0] = ns;
-    int tot = ns;
-    if (f.S > 0 && f.e_begin == 0) {
-      s.slot_e[ns] = E;
-      s.slot_n[ns] = T;
-      s.slot_q0[ns] = P;
-      ++tot;
+    if (writer) {
+      f.offsets[tid] = off;
+      f.counts[tid] = c;
     }
-    s.misc[1] = tot;
-  }
-  if (writer)
-    for (int i = lane; i <= E; i += 32) {
-      f.offsets[i] = s.offs[i];
-      if (i < E) f.counts[i] = s.cnt[i];
-    }
-  __syncwarp();
-  int* runp = s.cnt;  // the counts are done with; reuse as running offsets
-  for (int i = lane; i < E; i += 32) runp[i] = s.offs[i];
-  __syncwarp();
-  for (int base = 0; base < P; base += 32) {  // stable ranks, pairs in index order
-    const int q = base + lane;
-    const bool valid = q < P;
-    const int e = valid ? s.ids[q] : -1 - lane;
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(same & ((1u << lane) - 1u));
-    const int before = valid ? runp[e] : 0;
-    __syncwarp();
-    if (valid && rank == 0) runp[e] = before + __popc(same);
-    __syncwarp();
-    if (valid) {
-      const int pos = before + rank;
-      s.perm[pos] = q;
-      s.inv[q] = pos;
-      if (writer) {
-        f.perm[pos] = q;
-        f.inv[q] = pos;
+    if (tid == E - 1) {
+      const int total = excl + v, ns = total & 0xFFFF;
+      s.offs[E] = total >> 16;
+      if (writer) f.offsets[E] = total >> 16;
+      s.misc[0] = ns;
+      int tot = ns;
+      if (f.S > 0 && f.e_begin == 0) {
+        s.slot_e[ns] = E;
+        s.slot_n[ns] = T;
+        s.slot_q0[ns] = P;
+        ++tot;
       }
+      s.misc[1] = tot;
+    }
+  }
+  __syncthreads();
+  // stable ranks: pair q goes after the earlier pairs of its expert
+  for (int q = tid; q < P; q += kThreads) {
+    const int e = s.ids[q];
+    int r = 0;
+    for (int q2 = 0; q2 < q; ++q2) r += s.ids[q2] == e;
+    const int pos = s.offs[e] + r;
+    s.perm[pos] = q;
+    s.inv[q] = pos;
+    if (writer) {
+      f.perm[pos] = q;
+      f.inv[q] = pos;
     }
   }
 }

@@ -222,10 +222,11 @@ __device__ void tc_routing(const DecParams& p, const Shared& s, unsigned seq, vo
     else topk_token<16>(p, s, warp, seq, abort);
   }
   __syncthreads();
-  if (warp == 0) {
-    if (p.f.P <= 32) bucket_small(p, s);
-    else bucket_large(p, s);
-  } else if (warp == 1 && blockIdx.x == 0 && p.f.P <= 32) {
+  if (p.f.P > 32) {
+    bucket_large(p, s);  // the whole CTA sorts
+  } else if (warp == 0) {
+    bucket_small(p, s);
+  } else if (warp == 1 && blockIdx.x == 0) {
     export_counts_small(p, s);
   }
   __syncthreads();
