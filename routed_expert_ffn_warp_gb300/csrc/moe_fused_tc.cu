@@ -455,7 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      prefetch_to(kPfSteps);
       int j = 0;
       bool ok = true;
       for (int i = 0; i < nit && ok; ++i) {
@@ -470,12 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          prefetch_to(j + 1 + kPfSteps);
           uint8_t* sb = ring + (size_t)st * sbytes;
           // both tiles' 2 x 8,192 code bytes (counted as read from global memory) + 1,024 scale bytes
           mbar_arrive_expect_tx(&full[st], (uint32_t)kTcPairBytes);
           tc::tma_load_2d(sb, it.down ? &dn2 : &gu2, 0, y0 + ks * (kTcPairBytes / 64), &full[st]);
           bulk_g2s(sb + kSfaOff, w0 + (size_t)ks * kTcPairBytes + 2 * kTcCodeBytes, 1024, &full[st]);
+          // the window ahead, at most two blocks per step so the first copies are not held back
+          prefetch_to(min(j + 1 + kPfSteps, pj + 2));
         }
       }
     }

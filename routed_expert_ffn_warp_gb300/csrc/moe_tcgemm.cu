@@ -542,31 +542,67 @@ __global__ void repack_tc_kernel(const uint8_t* codes, const uint8_t* scales, in
   }
 }
 
-// x -> two MXFP8 planes per 32-element block: a warp per (token, block), a lane per element.
+// x as two E4M3 planes per 32-element block (what split_planes<2> computes
+// for one element per lane), four threads per block of 32: each thread loads
+// 8 bf16 at once, the block maximum of each plane comes from two shuffles
+// within the four, and every thread stores its 8 codes per plane in one 8-byte
+// store. The bits equal the one-element-per-lane form (the same maxima and
+// conversions).
 __global__ void __launch_bounds__(256) prep_xq_kernel(FwdParams p) {
   pdl_enter();
-  const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * blockDim.x + threadIdx.x, sub = g & 3;
   const int nb = p.xq_spitch;  // blocks per row, scale padding included
-  if (item >= p.T * nb) return;
-  const int t = item / nb, b = item - t * nb;
+  if (g >= p.T * nb * 4) return;  // whole groups of four: T nb 4 and the block size are multiples of 4
+  const int item = g >> 2, t = item / nb, b = item - t * nb;
   uint8_t* qs = p.xqs + (size_t)t * 2 * p.xq_spitch + b;
   if (32 * b >= p.d64) {  // scale padding
-    if (lane == 0) {
+    if (sub == 0) {
       qs[0] = 127;
       qs[p.xq_spitch] = 127;
     }
     return;
   }
-  const int k = 32 * b + lane;
-  const float v = k < p.d ? __uint_as_float((uint32_t)p.x[(size_t)t * p.d + k] << 16) : 0.f;
-  uint32_t code[2], sc[2];
-  tc::split_planes<2>(v, code, sc);
-  uint8_t* qh = p.xq + (size_t)t * 2 * p.d64 + k;
-  qh[0] = (uint8_t)code[0];
-  qh[p.d64] = (uint8_t)code[1];
-  if (lane == 0) {
-    qs[0] = (uint8_t)sc[0];
-    qs[p.xq_spitch] = (uint8_t)sc[1];
+  const int k0 = 32 * b + 8 * sub;
+  // the four threads of a block take every branch together (the exits above are per block): the
+  // shuffles name just them
+  const unsigned gmask = 0xFu << (threadIdx.x & 28);
+  float v[8];
+  if (k0 < p.d) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + k0);
+    const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w4[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = 0.f;
+  }
+  uint8_t* qh = p.xq + (size_t)t * 2 * p.d64 + k0;
+#pragma unroll
+  for (int pl = 0; pl < 2; ++pl) {
+    float amax = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(v[q]));
+    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+    int sh = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
+    sh = max(-127, min(127, sh));
+    const float ish = __uint_as_float((uint32_t)(127 - sh) << 23), fsh = __uint_as_float((uint32_t)(127 + sh) << 23);
+    uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint16_t c2;  // low byte: element 2q, high byte: element 2q + 1
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(v[2 * q + 1] * ish), "f"(v[2 * q] * ish));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+      v[2 * q] -= __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))) * fsh;
+      v[2 * q + 1] -= __half2float(__ushort_as_half((unsigned short)(h2 >> 16))) * fsh;
+      codes[q >> 1] |= (uint32_t)c2 << (16 * (q & 1));
+    }
+    *reinterpret_cast<uint2*>(qh + (size_t)pl * p.d64) = make_uint2(codes[0], codes[1]);
+    if (sub == 0) qs[(size_t)pl * p.xq_spitch] = (uint8_t)(sh + 127);
   }
 }
 
@@ -588,7 +624,7 @@ cudaError_t configure_tcgemm(int max_smem) {
 }
 
 cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream) {
-  launch_chained(prep_xq_kernel, dim3((p.T * p.xq_spitch + 7) / 8), dim3(256), 0, stream, p);
+  launch_chained(prep_xq_kernel, dim3((p.T * p.xq_spitch * 4 + 255) / 256), dim3(256), 0, stream, p);
   // panels: at most ceil(Q / 48) + slots blocks (the kernels skip the ones past the count)
   const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
   return launch_chained(pack_panels_kernel, dim3(max_panels, tc_ksteps(p.d)), dim3(256), 0, stream, p);
