@@ -715,21 +715,51 @@ __device__ float shared_gate_block(const FwdParams& p, int t) {
   return g;
 }
 
+// y_t = sum_j g_j part_j (pair order) + s_t shared_t, one rounding. A block
+// takes 1,024 elements of one token's row (4 per thread, 16-byte loads): the
+// token's k (gate, row) pairs are read once into shared memory, then every
+// thread's k row loads are independent of each other.
+constexpr int kCombineVec = 4;
 __global__ void __launch_bounds__(256) combine_kernel(FwdParams p) {
   pdl_enter();
+  __shared__ float gk[32];
+  __shared__ const float* rk[32];
   const int t = blockIdx.y;
   const float sg = (p.S > 0 && p.w_sg) ? shared_gate_block(p, t) : 1.f;
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= p.d) return;
-  float acc = 0.f;
-  for (int j = 0; j < p.k; ++j) {  // this shard's pairs only (all of them without sharding)
-    const int pj = t * p.k + j;
-    if (expert_in_shard(p.ids[pj], p.e_begin, p.e_end))
-      acc = fmaf(p.gates[pj], p.part[(size_t)p.inv[pj] * p.d + r], acc);
+  if (threadIdx.x < p.k) {  // this shard's pairs only (all of them without sharding); others weigh 0
+    const int pj = t * p.k + threadIdx.x;
+    const bool mine = expert_in_shard(p.ids[pj], p.e_begin, p.e_end);
+    gk[threadIdx.x] = mine ? p.gates[pj] : 0.f;
+    rk[threadIdx.x] = mine ? p.part + (size_t)p.inv[pj] * p.d : nullptr;
   }
-  if (p.S > 0 && p.e_begin == 0) acc += sg * p.part[(size_t)(p.P + t) * p.d + r];
-  if (p.out_f32) reinterpret_cast<float*>(p.out)[(size_t)t * p.d + r] = acc;
-  else reinterpret_cast<__nv_bfloat16*>(p.out)[(size_t)t * p.d + r] = __float2bfloat16_rn(acc);
+  __syncthreads();
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) * kCombineVec;
+  if (r >= p.d) return;
+  float acc[kCombineVec] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < p.k; ++j) {
+    if (!rk[j]) continue;
+    const float4 v = *reinterpret_cast<const float4*>(rk[j] + r);
+    const float g = gk[j];
+    acc[0] = fmaf(g, v.x, acc[0]);
+    acc[1] = fmaf(g, v.y, acc[1]);
+    acc[2] = fmaf(g, v.z, acc[2]);
+    acc[3] = fmaf(g, v.w, acc[3]);
+  }
+  if (p.S > 0 && p.e_begin == 0) {
+    const float4 v = *reinterpret_cast<const float4*>(p.part + (size_t)(p.P + t) * p.d + r);
+    acc[0] += sg * v.x;
+    acc[1] += sg * v.y;
+    acc[2] += sg * v.z;
+    acc[3] += sg * v.w;
+  }
+  if (p.out_f32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)t * p.d + r) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)t * p.d + r;
+    *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[0], acc[1]);
+    *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc[2], acc[3]);
+  }
 }
 
 // ---------------------------------------------------------------- repack
@@ -839,7 +869,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
                     : launch_gemm_down(p, stream, num_sms);
   if (e != cudaSuccess) return e;
   mark();
-  launch_chained(combine_kernel, dim3((p.d + 255) / 256, p.T), dim3(256), 0, stream, p);
+  launch_chained(combine_kernel, dim3((p.d / kCombineVec + 255) / 256, p.T), dim3(256), 0, stream, p);
   mark();
   return cudaGetLastError();
 }

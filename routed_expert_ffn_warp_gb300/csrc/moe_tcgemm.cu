@@ -455,37 +455,41 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
 // Activation panels: one CTA per (panel, K step). Panel rows n < 2 npad:
 // plane n / npad, token m = n % npad of the block (rows past the block's
 // tokens are zero, their scales 127).
+constexpr int kPanelSteps = 4;  // K steps of the x panels per block
 __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
   pdl_enter();
-  const int pb = blockIdx.x, ks = blockIdx.y;
+  const int pb = blockIdx.x;
   const int ns = *p.n_slots;
   if (pb >= p.panel_prefix[ns]) return;
   const int s = find_unit_slot(p.panel_prefix, ns, pb);
   const int tb = pb - p.panel_prefix[s];
   const int n = min(kMaxTok, p.slot_n[s] - kMaxTok * tb), q0 = p.slot_q0[s] + kMaxTok * tb, npad = npad_of(n);
   const int nks = tc_ksteps(p.d);
-  uint8_t* dst = p.xpanel + ((size_t)pb * nks + ks) * kTcPanelStep;
-  for (int o = threadIdx.x; o < 2 * npad * 8; o += 256) {  // 16-byte chunks (row, kc) of the N = 2 npad rows
-    const int row = o >> 3, kc = o & 7;
-    const int plane = row >= npad, m = row - plane * npad, k0 = kTcStepK * ks + 16 * kc;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < 2 * npad && m < n && k0 < p.d64)
-      v = *reinterpret_cast<const uint4*>(p.xq + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.d64 + k0);
-    *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = v;
-  }
-  if (threadIdx.x < 128) {  // scale word (lane l, r) for B row 32 r + l
-    const int l = threadIdx.x >> 2, r = threadIdx.x & 3, row = 32 * r + l;
-    const int plane = row >= npad, m = row - plane * npad;
-    uint32_t w = 0x7F7F7F7Fu;
-    if (row < 2 * npad && m < n) {
-      const uint8_t* sc = p.xqs + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.xq_spitch;
-      w = 0;
-      for (int kb = 0; kb < 4; ++kb) {
-        const int blk = 4 * ks + kb;
-        w |= (uint32_t)(blk < p.xq_spitch ? sc[blk] : 127) << (8 * kb);
-      }
+  // kPanelSteps K steps per block: the slot lookup and the rows' tokens serve all of them
+  for (int ks = blockIdx.y * kPanelSteps; ks < min(nks, (blockIdx.y + 1) * kPanelSteps); ++ks) {
+    uint8_t* dst = p.xpanel + ((size_t)pb * nks + ks) * kTcPanelStep;
+    for (int o = threadIdx.x; o < 2 * npad * 8; o += 256) {  // 16-byte chunks (row, kc) of the N = 2 npad rows
+      const int row = o >> 3, kc = o & 7;
+      const int plane = row >= npad, m = row - plane * npad, k0 = kTcStepK * ks + 16 * kc;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row < 2 * npad && m < n && k0 < p.d64)
+        v = *reinterpret_cast<const uint4*>(p.xq + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.d64 + k0);
+      *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = v;
     }
-    *reinterpret_cast<uint32_t*>(dst + 2 * npad * kTcStepK + 16 * l + 4 * r) = w;
+    if (threadIdx.x < 128) {  // scale word (lane l, r) for B row 32 r + l
+      const int l = threadIdx.x >> 2, r = threadIdx.x & 3, row = 32 * r + l;
+      const int plane = row >= npad, m = row - plane * npad;
+      uint32_t w = 0x7F7F7F7Fu;
+      if (row < 2 * npad && m < n) {
+        const uint8_t* sc = p.xqs + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.xq_spitch;
+        w = 0;
+        for (int kb = 0; kb < 4; ++kb) {
+          const int blk = 4 * ks + kb;
+          w |= (uint32_t)(blk < p.xq_spitch ? sc[blk] : 127) << (8 * kb);
+        }
+      }
+      *reinterpret_cast<uint32_t*>(dst + 2 * npad * kTcStepK + 16 * l + 4 * r) = w;
+    }
   }
 }
 
@@ -627,7 +631,8 @@ cudaError_t launch_panels_tc(const FwdParams& p, cudaStream_t stream) {
   launch_chained(prep_xq_kernel, dim3((p.T * p.xq_spitch * 4 + 255) / 256), dim3(256), 0, stream, p);
   // panels: at most ceil(Q / 48) + slots blocks (the kernels skip the ones past the count)
   const int max_panels = (p.P + p.T) / kTcGemmRows + p.E + 2;
-  return launch_chained(pack_panels_kernel, dim3(max_panels, tc_ksteps(p.d)), dim3(256), 0, stream, p);
+  return launch_chained(pack_panels_kernel, dim3(max_panels, (tc_ksteps(p.d) + kPanelSteps - 1) / kPanelSteps),
+                        dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_gemm_gateup_tc(const FwdParams& p, cudaStream_t stream, int num_sms) {
