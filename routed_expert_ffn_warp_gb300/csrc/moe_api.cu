@@ -309,7 +309,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   dp.test_wait_ns = 2000000LL;  // 2 ms
   // kernel attributes are per device: set them with this context's device current
   if ((e = moe::configure_decode(ctx->max_smem)) != cudaSuccess || (e = moe::configure_tcgemm(ctx->max_smem)) != cudaSuccess ||
-      (e = moe::configure_gemm()) != cudaSuccess || (e = moe::configure_affine()) != cudaSuccess) {
+      (e = moe::configure_gemm()) != cudaSuccess || (e = moe::configure_affine()) != cudaSuccess ||
+      (e = moe::configure_kernels()) != cudaSuccess) {
     moe_destroy(ctx);
     return fail(nullptr, MOE_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   }

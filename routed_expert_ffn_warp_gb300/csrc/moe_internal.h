@@ -282,6 +282,7 @@ int decode_blocks_per_sm(const DecParams& p);
 cudaError_t configure_decode(int max_smem);
 cudaError_t configure_tcgemm(int max_smem);
 cudaError_t configure_gemm();
+cudaError_t configure_kernels();  // the bucketing kernel's shared-memory limit (moe_kernels.cu)
 
 // Expert GEMMs of the general path (moe_gemm.cu). Work units: (slot, group of
 // kGemmTiles 16-row weight tiles, block of up to kGemmRows rows of the slot);

@@ -551,7 +551,8 @@ __host__ inline int router_splits(int T, int E, int d) {
 // ---------------------------------------------------------------- bucketing and work list
 
 constexpr int kBucketThreads = 1024;
-constexpr int kBucketChunks = 16;  // warps that count and place the pairs, each over a contiguous chunk
+constexpr int kBucketChunks = 32;  // warps that count and place the pairs, each over a contiguous chunk
+constexpr int kBucketSmem = kBucketChunks * 512 * 4;  // per (chunk, expert) counts, dynamic shared memory
 
 // Exclusive prefix sum over the block (every thread gives v; threads past the
 // data give 0); returns the prefix and, in *total, the block's sum.
@@ -590,7 +591,8 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   pdl_enter();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
   const int E = p.E, T = p.T, P = p.P;
-  __shared__ int wc[kBucketChunks][512];  // per (chunk, expert): count, then first position
+  extern __shared__ int wc_mem[];
+  int (*wc)[512] = reinterpret_cast<int (*)[512]>(wc_mem);  // per (chunk, expert): count, then first position
   __shared__ int wsum[32];
   if (T <= kRouteDDMaxT) {  // few tokens: the top k from router_dd_kernel's logits, one warp per token
     if (warp < T) {
@@ -840,6 +842,10 @@ void launch_router(FwdParams p, cudaStream_t stream) {
   launch_chained(topk_kernel, dim3(p.T), dim3(kTopkThreads), 0, stream, p);
 }
 
+cudaError_t configure_kernels() {
+  return cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBucketSmem);
+}
+
 const char* const kForwardPhaseNames = "route,gateup,down,combine";
 const char* const kForwardPhaseNamesTc = "route,panels,gateup,down,combine";
 
@@ -852,7 +858,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
   mark();
   if (!p.tc_gateup) launch_chained(prep_x_kernel, dim3(p.T), dim3(256), 0, stream, p);  // f16 x of the register-decode GEMMs
   launch_router(p, stream);
-  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), 0, stream, p);
+  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), kBucketSmem, stream, p);
   mark();
   cudaError_t e = cudaSuccess;
   if (p.tc_gateup) {
@@ -877,7 +883,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
   launch_router(p, stream);
-  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), 0, stream, p);
+  launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), kBucketSmem, stream, p);
   return cudaGetLastError();
 }
 

@@ -112,6 +112,9 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
   p.slot_n = p.slot_q0 + 513;
   p.gu_prefix = p.slot_n + 513;
   p.dn_prefix = p.gu_prefix + 514;
+  // the bucketing kernel's shared-memory limit is a per-device attribute (no context sets it here)
+  if ((e = moe::configure_kernels()) != cudaSuccess)
+    return fail(MOE_ERR_CUDA, std::string("moe_route_static: ") + cudaGetErrorString(e));
   e = moe::launch_route(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(MOE_ERR_CUDA, std::string("moe_route_static launch: ") + cudaGetErrorString(e));
   return MOE_OK;
