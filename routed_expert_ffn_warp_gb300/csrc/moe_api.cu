@@ -608,7 +608,9 @@ int moe_launches_per_forward(const moe_ctx* ctx, int T) {
   if (T <= 0) return 0;
   if (uses_decode(ctx, T)) return 1;
   const int n = ctx->base.tc_gateup ? moe::kLaunchesPerForwardTc : moe::kLaunchesPerForward;
-  return T <= moe::kRouteDDMaxT ? n - 1 : n;  // one router launch instead of router + top-k
+  if (T > moe::kRouteDDMaxT) return n;
+  // one router launch instead of router + top-k; without the tcgen05 layout it also prepares the f16 x
+  return ctx->base.tc_gateup ? n - 1 : n - 2;
 }
 
 size_t moe_weight_bytes(const moe_ctx* ctx) {

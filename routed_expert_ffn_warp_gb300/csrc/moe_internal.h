@@ -328,7 +328,8 @@ __host__ __device__ inline int weight_index(const FwdParams& f, int e) {
 // Routing only (router logits, top-k gates, counting sort) of the general path.
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream);
 // Router logits and top-k of the multi-kernel path (moe_kernels.cu).
-void launch_router(FwdParams p, cudaStream_t stream);
+// with_prep_x: also the f16 x (and affine group sums) for the register-decode / affine GEMMs when T <= 32.
+void launch_router(FwdParams p, cudaStream_t stream, bool with_prep_x);
 cudaError_t launch_repack(const uint8_t* codes, const uint8_t* scales, int n_exp, int d, int f,
                           size_t canon_code_stride, size_t canon_scale_stride, uint8_t* out, size_t out_stride,
                           int* err_flag, cudaStream_t stream);

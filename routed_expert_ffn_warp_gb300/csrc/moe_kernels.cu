@@ -41,9 +41,9 @@ using namespace dev;
 
 // ---------------------------------------------------------------- prep_x
 
-__global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
-  pdl_enter();
-  const int t = blockIdx.x;
+// f16 x of token t (x * 2^sigma_t), 2^-sigma_t and, for affine experts, the
+// group sums: by one block of 256 threads (all of them call it).
+__device__ void prep_x_token(const FwdParams& p, int t) {
   const uint16_t* xt = p.x + (size_t)t * p.d;
   __shared__ float wmax[8];
   float m = 0.f;
@@ -68,6 +68,11 @@ __global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
       if (lane == 0) p.xgsum[(size_t)t * p.xg_pitch + g] = a * 0x1p-24f;  // the scale of the codes' f16 form
     }
   }
+}
+
+__global__ void __launch_bounds__(256) prep_x_kernel(FwdParams p) {
+  pdl_enter();
+  prep_x_token(p, blockIdx.x);
 }
 
 // ---------------------------------------------------------------- router
@@ -434,6 +439,13 @@ constexpr int kRdTok = 8, kRdThreads = 256;
 
 __global__ void __launch_bounds__(kRdThreads) router_dd_kernel(FwdParams p) {
   pdl_enter();
+  if ((int)blockIdx.x == p.E) {  // the extra block column: the f16 x of the register-decode GEMMs
+    for (int t = blockIdx.y * kRdTok; t < min(p.T, (int)(blockIdx.y + 1) * kRdTok); ++t) {
+      prep_x_token(p, t);
+      __syncthreads();  // prep_x_token's shared maxima are reused by the next token
+    }
+    return;
+  }
   __shared__ dd part[kRdThreads / 32][kRdTok];
   const int e = blockIdx.x, t0 = blockIdx.y * kRdTok;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -539,6 +551,135 @@ __device__ void topk_warp_dd(const FwdParams& p, int t) {
   }
 }
 
+// Order-preserving map of a float to an unsigned key (-0 folded into +0).
+__device__ __forceinline__ unsigned sort_key(float v) {
+  const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The top k of one token over E <= 512 experts with the whole block (for
+// decode-sized calls, where one warp's k rounds over E / 32 logits per lane are
+// a long dependent chain): a radix select of the k-th largest logit hi part in
+// four 8-bit passes (block histograms), the experts at or above it gathered
+// (at most k plus the ones tied on hi with the k-th), then one warp orders
+// those few by (hi, lo, lower index) as topk_warp_dd does and forms the gates
+// the same way -- the same ids, order and gate bits. More than 32 tied
+// candidates (never with continuous logits) fall back to topk_warp_dd.
+// `mem` holds 512 words of shared memory.
+__device__ void topk_radix_dd(const FwdParams& p, int* mem) {
+  const int E = p.E, k = p.k, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* hist = mem;            // [256]
+  int* ctl = mem + 256;       // [0] prefix, [1] rank left, [2] candidates
+  int* cand = mem + 264;      // [32] candidate experts
+  const unsigned key = tid < E ? sort_key(p.logit_hi[tid]) : 0u;
+  if (tid == 0) {
+    ctl[0] = 0;
+    ctl[1] = k;
+    ctl[2] = 0;
+  }
+  unsigned prefix = 0u, mask = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    {  // one shared atomic per (warp, bin): most keys share their leading digits
+      const bool in = tid < E && (key & mask) == prefix;
+      const unsigned act = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const unsigned bin = (key >> shift) & 255u;
+        const unsigned same = __match_any_sync(act, bin);
+        if ((same & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[bin], __popc(same));
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // the digit of the rank-left-th largest among the keys that match so far
+      const int left = ctl[1];
+      int c[8], tot = 0;  // lane holds bins 255 - 8 lane - j, from the top
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        tot += c[j];
+      }
+      int incl = tot;  // bins above and at this lane's block, counted from the top
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int above = incl - tot;
+      if (above < left && incl >= left) {  // exactly one lane holds the digit
+        int run = above;
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= left) {
+            ctl[0] = (int)((unsigned)ctl[0] | ((unsigned)(255 - 8 * lane - j) << shift));
+            ctl[1] = left - run;
+            break;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = (unsigned)ctl[0];
+    mask |= 255u << shift;
+  }
+  // the k-th largest hi key is `prefix`: gather every expert at or above it
+  {
+    const bool in = tid < E && key >= prefix;
+    const unsigned act = __ballot_sync(0xffffffffu, in);
+    int base = 0;
+    if (lane == 0 && act) base = atomicAdd(&ctl[2], __popc(act));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(act & ((1u << lane) - 1u));
+    if (in && pos < 32) cand[pos] = tid;
+  }
+  __syncthreads();
+  const int nc = ctl[2];
+  if (nc > 32) {  // pathological ties on the hi parts
+    if (warp == 0) {
+      if (E <= 256) topk_warp_dd<8>(p, 0);
+      else topk_warp_dd<16>(p, 0);
+    }
+    return;
+  }
+  if (warp != 0) return;
+  const int e = lane < nc ? cand[lane] : 0x7fffffff;
+  const float vh = lane < nc ? p.logit_hi[e] : -INFINITY, vl = lane < nc ? p.logit_lo[e] : 0.f;
+  bool taken = lane >= nc;
+  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  int sel_id = 0;
+  for (int j = 0; j < k; ++j) {  // k rounds over one candidate per lane, as topk_warp_dd
+    float bh = taken ? -INFINITY : vh, bl = taken ? 0.f : vl;
+    int bi = taken ? 0x7fffffff : e;
+    for (int o = 16; o; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
+        bh = oh;
+        bl = ol;
+        bi = oi;
+      }
+    }
+    if (bi == e && lane < nc) taken = true;
+    if (j == 0) {
+      top_h = bh;
+      top_l = bl;
+    }
+    if (lane == j) {
+      sel_h = bh;
+      sel_l = bl;
+      sel_id = bi;
+    }
+  }
+  float ex = 0.f;
+  if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
+  float sum = ex;
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    p.ids[lane] = sel_id;
+    p.gates[lane] = ex / sum;
+  }
+}
+
 // K ranges of the router's fp32 pass: enough blocks for about two per SM.
 __host__ inline int router_splits(int T, int E, int d) {
   const int tiles = ((T + kRfTok - 1) / kRfTok) * ((E + kRfExp - 1) / kRfExp);
@@ -594,7 +735,10 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   extern __shared__ int wc_mem[];
   int (*wc)[512] = reinterpret_cast<int (*)[512]>(wc_mem);  // per (chunk, expert): count, then first position
   __shared__ int wsum[32];
-  if (T <= kRouteDDMaxT) {  // few tokens: the top k from router_dd_kernel's logits, one warp per token
+  if (T == 1 && E > 128) {  // one token over many experts: the whole block selects
+    topk_radix_dd(p, wc_mem);
+    __syncthreads();  // this block's ids writes are visible to the whole block (and wc_mem is free again)
+  } else if (T <= kRouteDDMaxT) {  // few tokens: the top k from router_dd_kernel's logits, one warp per token
     if (warp < T) {
       if (E <= 128) topk_warp_dd<4>(p, warp);
       else if (E <= 256) topk_warp_dd<8>(p, warp);
@@ -602,10 +746,12 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
     }
     __syncthreads();  // this block's ids writes are visible to the whole block
   }
-  const int chunk = (P + kBucketChunks - 1) / kBucketChunks;
-  for (int i = tid; i < kBucketChunks * E; i += kBucketThreads) wc[i / E][i % E] = 0;
+  // chunk warps: up to kBucketChunks, about 32 pairs each at least (few pairs, few chunks)
+  const int nch = max(1, min(kBucketChunks, (P + 31) / 32));
+  const int chunk = (P + nch - 1) / nch;
+  for (int i = tid; i < nch * E; i += kBucketThreads) wc[i / E][i % E] = 0;
   __syncthreads();
-  if (warp < kBucketChunks) {
+  if (warp < nch) {
     const int q1 = min(P, (warp + 1) * chunk);
     for (int base = warp * chunk; base < q1; base += 32) {
       const int q = base + lane;
@@ -618,7 +764,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   __syncthreads();
   int cnt = 0;
   if (tid < E)
-    for (int w = 0; w < kBucketChunks; ++w) {
+    for (int w = 0; w < nch; ++w) {
       const int c = wc[w][tid];
       wc[w][tid] = cnt;
       cnt += c;
@@ -628,11 +774,11 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(FwdParams p) {
   if (tid < E) {
     p.counts[tid] = cnt;
     p.offsets[tid] = off;
-    for (int w = 0; w < kBucketChunks; ++w) wc[w][tid] += off;
+    for (int w = 0; w < nch; ++w) wc[w][tid] += off;
   }
   if (tid == 0) p.offsets[E] = tot;
   __syncthreads();
-  if (warp < kBucketChunks) {
+  if (warp < nch) {
     const int q1 = min(P, (warp + 1) * chunk);
     for (int base = warp * chunk; base < q1; base += 32) {
       const int q = base + lane;
@@ -831,9 +977,10 @@ __global__ void repack_kernel(const uint8_t* codes, const uint8_t* scales, int n
 
 }  // namespace
 
-void launch_router(FwdParams p, cudaStream_t stream) {
-  if (p.T <= kRouteDDMaxT) {  // the top k follow in bucket_kernel
-    launch_chained(router_dd_kernel, dim3(p.E, (p.T + kRdTok - 1) / kRdTok), dim3(kRdThreads), 0, stream, p);
+void launch_router(FwdParams p, cudaStream_t stream, bool with_prep_x) {
+  if (p.T <= kRouteDDMaxT) {  // the top k follow in bucket_kernel; one more block column prepares x if asked
+    launch_chained(router_dd_kernel, dim3(p.E + (with_prep_x ? 1 : 0), (p.T + kRdTok - 1) / kRdTok), dim3(kRdThreads),
+                   0, stream, p);
     return;
   }
   p.rsplit = router_splits(p.T, p.E, p.d);
@@ -856,8 +1003,9 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
     if (events) cudaEventRecord(events[ev++], stream);
   };
   mark();
-  if (!p.tc_gateup) launch_chained(prep_x_kernel, dim3(p.T), dim3(256), 0, stream, p);  // f16 x of the register-decode GEMMs
-  launch_router(p, stream);
+  // f16 x of the register-decode and affine GEMMs: inside the router launch for T <= kRouteDDMaxT
+  if (!p.tc_gateup && p.T > kRouteDDMaxT) launch_chained(prep_x_kernel, dim3(p.T), dim3(256), 0, stream, p);
+  launch_router(p, stream, !p.tc_gateup);
   launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), kBucketSmem, stream, p);
   mark();
   cudaError_t e = cudaSuccess;
@@ -882,7 +1030,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t stream, int num_sms,
 
 cudaError_t launch_route(const FwdParams& p, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  launch_router(p, stream);
+  launch_router(p, stream, false);
   launch_chained(bucket_kernel, dim3(1), dim3(kBucketThreads), kBucketSmem, stream, p);
   return cudaGetLastError();
 }

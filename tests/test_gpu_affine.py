@@ -3,7 +3,7 @@ and bias per 64 weights ("Running Qwen3.8-Flash-Next on a 32 GB Mac with Transfo
 experts in 3-bit affine form, group 64, 2.15 MB each; a 16-bit scale and bias per 64 weights).
 
 Routing must match the oracle bit for bit; the layer output within the fp32 / bf16 tolerances of
-the MXFP4 tests, at code widths 2, 3, 4 and 8, at shapes whose slots cross the 32-row work blocks
+the MXFP4 tests, at code widths 2, 3, 4 and 8, at shapes whose slots cross the 16-row work blocks
 and have ragged tails, with and without the gated shared expert, at the full size of the affine
 decode workload (d = 2560, ffn = 640, E = 512, k = 10, shared ffn 640) in the launch configuration
 the benchmark times, for expert-parallel shards, and token by token against a batch (batch
@@ -161,3 +161,14 @@ def test_affine_configs_and_loads_are_checked(m):
         m.moe_load_experts_affine(mx.ctx, L["experts"])
     assert ei.value.code == m.MOE_ERR_INVALID_ARG
     mx.close()
+
+
+def test_affine_launch_count(m):
+    """The affine chain: router (which also prepares the f16 x up to 32 tokens), bucketing with the top k,
+    two GEMMs, combine; above 32 tokens a separate x preparation and the two-pass router."""
+    lay = m.MoeLayer(m.LayerShape(d=128, ffn=64, n_experts=4, top_k=2, t_max=64,
+                                  weight_format=m.MOE_FORMAT_AFFINE64, weight_bits=3))
+    assert m.moe_launches_per_forward(lay.ctx, 1) == 5
+    assert m.moe_launches_per_forward(lay.ctx, 32) == 5
+    assert m.moe_launches_per_forward(lay.ctx, 33) == 7
+    lay.close()
