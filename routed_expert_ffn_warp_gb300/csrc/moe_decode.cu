@@ -502,24 +502,6 @@ __device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
   }
 }
 
-// Poll one published 64-bit word until it carries `want` in its low half
-// (bounded); returns the word, or the last one read after giving up.
-__device__ __forceinline__ unsigned long long poll_word(const unsigned long long* w, unsigned want, long long limit,
-                                                        const DecParams& p, volatile int* abort) {
-  unsigned long long v = ld_relaxed_u64(w);
-  if ((unsigned)v == want) return v;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    __nanosleep(64);
-    v = ld_relaxed_u64(w);
-    if ((unsigned)v == want || *abort) return v;
-    if (timed_out(t0, limit)) {
-      give_up(abort, p.f.status);
-      return v;
-    }
-  }
-}
-
 // Stage h of (slot, half) pair hs in shared memory (all threads, after every
 // warp is done reading the shared x, which this area overlays): planes
 // [m][hi | lo][hstride] and the per-16 scales. The gate/up reducers publish
@@ -533,47 +515,62 @@ __device__ void stage_h(const DecParams& p, const Shared& s, int hs, volatile in
   const int q0 = s.slot_q0[slot] + kHalf * half, n = min(kHalf, s.slot_n[slot] - kHalf * half);
   const int fsl = (s.slot_e[slot] == f.E) ? f.S : f.F;
   // Scale words and h words. Each round, every thread first issues all of its
-  // loads (kB of each), then checks them, polls the stale ones and stores: one
-  // round trip per round, not one per word. The timeout test makes the scale
+  // loads (kB of each), then reloads every word that does not yet carry this
+  // launch's number, all of them together, until none is stale (bounded): one
+  // round trip per retry, not one per word. The timeout test makes the scale
   // words wait for a number no launch writes.
   constexpr int kB = 4;
   const unsigned want_sc = seq + (unsigned)p.test_extra;
-  const long long lim_sc = p.test_extra ? p.test_wait_ns : p.wait_ns;
+  const long long lim = p.test_extra ? p.test_wait_ns : p.wait_ns;
   const int per_row = f.fmax64 / 2;  // element pairs of a row
   const int nsc = n * f.hgroups, nh = n * per_row, per_round = kThreads * kB;
   const int rounds = (max(nsc, nh) + per_round - 1) / per_round;
   for (int rd = 0; rd < rounds; ++rd) {
     const int o0 = rd * per_round + threadIdx.x;
     unsigned long long v[kB], a[kB], b[kB];
+    const unsigned long long* wsc[kB];
+    const unsigned long long* wh[kB];
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
       const int o = o0 + u * kThreads;
       const int ms = o / f.hgroups, k = o - ms * f.hgroups;
-      v[u] = (o < nsc && 16 * k < fsl) ? ld_relaxed_u64(p.hswords + (size_t)(q0 + ms) * f.hgroups + k) : 0ull;
       const int m = o / per_row, i = 2 * (o - m * per_row);
-      a[u] = b[u] = 0ull;
-      if (o < nh && i < fsl) ld_relaxed_u64x2(p.hwords + (size_t)(q0 + m) * f.fmax64 + i, a[u], b[u]);
+      wsc[u] = (o < nsc && 16 * k < fsl) ? p.hswords + (size_t)(q0 + ms) * f.hgroups + k : nullptr;
+      wh[u] = (o < nh && i < fsl) ? p.hwords + (size_t)(q0 + m) * f.fmax64 + i : nullptr;
+      v[u] = wsc[u] ? ld_relaxed_u64(wsc[u]) : (unsigned long long)want_sc;
+      a[u] = b[u] = (unsigned long long)seq;
+      if (wh[u]) ld_relaxed_u64x2(wh[u], a[u], b[u]);
     }
+    uint64_t t0 = 0;
+    while (true) {
+      bool stale = false;
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        stale = stale || (unsigned)v[u] != want_sc || (unsigned)a[u] != seq || (unsigned)b[u] != seq;
+      if (!stale || *abort) break;
+      if (t0 == 0) t0 = globaltimer();
+      else if (timed_out(t0, lim)) {
+        give_up(abort, f.status);
+        break;
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        if ((unsigned)v[u] != want_sc) v[u] = ld_relaxed_u64(wsc[u]);
+        if ((unsigned)a[u] != seq || (unsigned)b[u] != seq) ld_relaxed_u64x2(wh[u], a[u], b[u]);
+      }
+    }
+    const bool ok = !*abort;
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
       const int o = o0 + u * kThreads;
       if (o < nsc) {
         const int ms = o / f.hgroups, k = o - ms * f.hgroups;
-        float sc = 0.f;
-        if (16 * k < fsl && !*abort) {
-          if ((unsigned)v[u] != want_sc)
-            v[u] = poll_word(p.hswords + (size_t)(q0 + ms) * f.hgroups + k, want_sc, lim_sc, p, abort);
-          sc = __uint_as_float((unsigned)(v[u] >> 32));
-        }
-        s.hsc[ms * f.hgroups + k] = sc;
+        s.hsc[ms * f.hgroups + k] = (wsc[u] && ok) ? __uint_as_float((unsigned)(v[u] >> 32)) : 0.f;
       }
       if (o < nh) {
         const int m = o / per_row, i = 2 * (o - m * per_row);
         uint32_t hv = 0, lv = 0;  // two f16 of each plane
-        if (i < fsl && !*abort) {
-          const unsigned long long* w = p.hwords + (size_t)(q0 + m) * f.fmax64 + i;
-          if ((unsigned)a[u] != seq) a[u] = poll_word(w, seq, p.wait_ns, p, abort);
-          if ((unsigned)b[u] != seq) b[u] = poll_word(w + 1, seq, p.wait_ns, p, abort);
+        if (wh[u] && ok) {
           const uint32_t pa = (uint32_t)(a[u] >> 32), pb = (uint32_t)(b[u] >> 32);
           hv = (pa & 0xFFFFu) | (pb << 16);
           lv = (pa >> 16) | (pb & 0xFFFF0000u);
@@ -683,15 +680,31 @@ __device__ void down_item(const DecParams& p, const Shared& s, const Plan& pl, c
   float acc[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
-  for (int kt = it.k0; kt < it.k1; kt += 2) {
-    cp_async_wait<RG - 1>();
-    __syncwarp();
-    uint8_t* sl = ring + slot * kGroupBytes;
-    down_tile_smem<NT>(p, s, sl, kt, un.n, acc);
-    if (kt + 1 < it.k1) down_tile_smem<NT>(p, s, sl + kTileBytes, kt + 1, un.n, acc);
-    __syncwarp();
-    issue_group(p, s, pl, w, cu, sl, pol);
-    if (++slot == RG) slot = 0;
+  // two groups (four tiles) per round where the item has them, as in gate/up
+  for (int kt = it.k0; kt < it.k1; kt += 4) {
+    uint8_t* sl0 = ring + slot * kGroupBytes;
+    const int s1 = slot + 1 == RG ? 0 : slot + 1;
+    uint8_t* sl1 = ring + s1 * kGroupBytes;
+    if (kt + 2 < it.k1) {
+      cp_async_wait<RG - 2>();
+      __syncwarp();
+      down_tile_smem<NT>(p, s, sl0, kt, un.n, acc);
+      down_tile_smem<NT>(p, s, sl0 + kTileBytes, kt + 1, un.n, acc);
+      down_tile_smem<NT>(p, s, sl1, kt + 2, un.n, acc);
+      if (kt + 3 < it.k1) down_tile_smem<NT>(p, s, sl1 + kTileBytes, kt + 3, un.n, acc);
+      __syncwarp();
+      issue_group(p, s, pl, w, cu, sl0, pol);
+      issue_group(p, s, pl, w, cu, sl1, pol);
+      slot = s1 + 1 == RG ? 0 : s1 + 1;
+    } else {
+      cp_async_wait<RG - 1>();
+      __syncwarp();
+      down_tile_smem<NT>(p, s, sl0, kt, un.n, acc);
+      if (kt + 1 < it.k1) down_tile_smem<NT>(p, s, sl0 + kTileBytes, kt + 1, un.n, acc);
+      __syncwarp();
+      issue_group(p, s, pl, w, cu, sl0, pol);
+      slot = s1;
+    }
   }
   const int us = it.u % p.n_us;
   if (!claim_slot(p, s.ctl + 3 * kMaxUS + us, it.u, abort)) return;
@@ -798,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
   extern __shared__ __align__(128) uint8_t sm[];
   Shared s = carve(sm, p);
   volatile int* abort = &s.misc[2];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     for (int b = 0; b < kMaxUS; ++b) {
       s.ctl[b] = 0;               // gate/up arrivals
@@ -847,7 +860,7 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   const FwdParams& f = p.f;
   if (f.E > 512 || f.k * kDecodeMaxT > 512) return false;
   auto up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
-  const int Pm = kDecodeMaxT * f.k, hh = std::min(kHalf, p.tcap);
+  const int hh = std::min(kHalf, p.tcap);
   // f16 row strides 64 bytes past a multiple of 128 (d64, fmax64 are multiples
   // of 64 elements): the 8 rows x 4 16-byte columns of a fragment load hit
   // distinct banks

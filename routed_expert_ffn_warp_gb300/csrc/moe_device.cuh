@@ -154,11 +154,35 @@ __device__ __forceinline__ dd dd_shfl_xor(dd a, int m) {
   r.lo = __shfl_xor_sync(0xffffffffu, a.lo, m);
   return r;
 }
-__device__ __forceinline__ bool dd_greater(float ah, float al, int ai, float bh, float bl, int bi) {
-  // (a > b) in value, then the lower index first; pairs are normalised (|lo| <= ulp(hi)/2).
-  if (ah != bh) return ah > bh;
-  if (al != bl) return al > bl;
-  return ai < bi;
+// Order-preserving map of a float to an unsigned key (-0 folded into +0): a > b
+// as floats iff key(a) > key(b). Every non-NaN float maps above 0x003FFFFF, so
+// key 0 can stand for "no candidate". unkey inverts it (+0 for -0).
+__device__ __forceinline__ unsigned fkey(float v) {
+  const unsigned u = __float_as_uint(v + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// The warp's best candidate: the largest logit (hi, lo) -- hi decides, then lo,
+// which for normalised pairs (|lo| <= ulp(hi)/2) is the order of the values --
+// then the lowest index, by three redux.sync and no branch: (mh, ml)
+// are the winner's keys, the return value its index. A lane without a
+// candidate passes keys (0, 0) and index 0x7fffffff.
+__device__ __forceinline__ int warp_best_dd(unsigned kh, unsigned kl, int idx, unsigned& mh, unsigned& ml) {
+  mh = __reduce_max_sync(0xffffffffu, kh);
+  ml = __reduce_max_sync(0xffffffffu, kh == mh ? kl : 0u);
+  return (int)__reduce_min_sync(0xffffffffu, (kh == mh && kl == ml) ? (unsigned)idx : 0x7fffffffu);
+}
+
+// A lane's running best of its own candidates in the same order, branch-free
+// (a divergent branch per candidate costs more than the comparisons).
+__device__ __forceinline__ void lane_best_dd(unsigned kh, unsigned kl, int idx, unsigned& bh, unsigned& bl, int& bi) {
+  const bool better = kh > bh || (kh == bh && (kl > bl || (kl == bl && idx < bi)));
+  bh = better ? kh : bh;
+  bl = better ? kl : bl;
+  bi = better ? idx : bi;
 }
 
 

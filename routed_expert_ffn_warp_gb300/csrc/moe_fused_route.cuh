@@ -201,12 +201,6 @@ __device__ void router(const DecParams& p, const Shared& s, unsigned seq) {
 
 // ---------------------------------------------------------------- phase B: routing (redundant per CTA)
 
-// Order-preserving map of a float to an unsigned key (-0 folded into +0).
-__device__ __forceinline__ unsigned fkey(float v) {
-  const unsigned u = __float_as_uint(v + 0.f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Top-k of token t by one warp: gather its logits of all E experts from the
 // published words (polling until every word carries this launch's number),
 // k rounds of a three-key warp reduction (logit hi, logit lo, lowest expert
@@ -259,47 +253,31 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
     const float z = __uint_as_float((unsigned)(a >> 32)) + __uint_as_float((unsigned)(b >> 32));
     s.sg[t] = 1.f / (1.f + expf(-z));
   }
+  // keys of the lane's candidates; taken and absent ones are (0, 0)
   unsigned kh[NPL], kl[NPL];
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
-    kh[i] = fkey(vh[i]);
-    kl[i] = fkey(vl[i]);
+    kh[i] = ((valid >> i) & 1u) ? fkey(vh[i]) : 0u;
+    kl[i] = ((valid >> i) & 1u) ? fkey(vl[i]) : 0u;
   }
-  unsigned taken = ~valid;
   int sel_id = 0;
   float sel_h = 0.f, sel_l = 0.f;
   for (int j = 0; j < k; ++j) {
     unsigned bh = 0, bl = 0;
     int bi = 0x7fffffff;
-    float fh = 0.f, fl = 0.f;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const bool free_ = !((taken >> i) & 1u);
-      if (free_ && (kh[i] > bh || (kh[i] == bh && kl[i] > bl))) {  // equal keys keep the lower index
-        bh = kh[i];
-        bl = kl[i];
-        bi = lane + 32 * i;
-        fh = vh[i];
-        fl = vl[i];
-      }
+    for (int i = 0; i < NPL; ++i) lane_best_dd(kh[i], kl[i], lane + 32 * i, bh, bl, bi);
+    unsigned mh, ml;
+    const int mi = warp_best_dd(bh, bl, bi, mh, ml);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {  // the owner retires the winner
+      const bool won = lane + 32 * i == mi;
+      kh[i] = won ? 0u : kh[i];
+      kl[i] = won ? 0u : kl[i];
     }
-    const unsigned mh = __reduce_max_sync(0xffffffffu, bh);
-    const unsigned tie = __ballot_sync(0xffffffffu, bh == mh);
-    int mi;
-    if (__popc(tie) == 1) {  // one lane holds the largest hi part: it wins
-      mi = __shfl_sync(0xffffffffu, bi, __ffs(tie) - 1);
-    } else {  // equal hi parts: the lo part decides, then the lower index
-      const unsigned ml = __reduce_max_sync(0xffffffffu, bh == mh ? bl : 0u);
-      mi = (int)__reduce_min_sync(0xffffffffu, (bh == mh && bl == ml) ? (unsigned)bi : 0x7fffffffu);
-    }
-    const int owner = mi & 31;
-    if (owner == lane) taken |= 1u << (mi >> 5);
-    const float wh = __shfl_sync(0xffffffffu, fh, owner), wl = __shfl_sync(0xffffffffu, fl, owner);
-    if (lane == j) {
-      sel_id = mi;
-      sel_h = wh;
-      sel_l = wl;
-    }
+    sel_id = lane == j ? mi : sel_id;
+    sel_h = lane == j ? unkey(mh) : sel_h;
+    sel_l = lane == j ? unkey(ml) : sel_l;
   }
   const float top_h = __shfl_sync(0xffffffffu, sel_h, 0), top_l = __shfl_sync(0xffffffffu, sel_l, 0);
   float ex = 0.f;

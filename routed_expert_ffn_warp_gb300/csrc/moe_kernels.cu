@@ -357,64 +357,46 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(FwdParams p) {
   __syncthreads();
   if (warp != 0) return;
   // candidates c = lane + 32 i: the quarters in order, then the bias
-  float vh[kTopkMaxE / 32], vl[kTopkMaxE / 32];
+  unsigned kh[kTopkMaxE / 32], kl[kTopkMaxE / 32];  // absent and taken candidates: (0, 0)
   int vid[kTopkMaxE / 32];
 #pragma unroll
   for (int i = 0; i < kTopkMaxE / 32; ++i) {
     const int c = lane + 32 * i;
-    vh[i] = -INFINITY;
-    vl[i] = 0.f;
+    kh[i] = kl[i] = 0u;
     vid[i] = 0x7fffffff;
     if (c < nc) {
       dd v = part[0][c];
       for (int w = 1; w < kTopkThreads / 32; ++w) v = dd_add(v, part[w][c]);
       const int e = cl[c];
       if (p.bias) v = dd_add(v, dd{p.bias[e], 0.f});
-      vh[i] = v.hi;
-      vl[i] = v.lo;
+      kh[i] = fkey(v.hi);
+      kl[i] = fkey(v.lo);
       vid[i] = e;
       p.logit_hi[(size_t)t * E + e] = v.hi;
       p.logit_lo[(size_t)t * E + e] = v.lo;
     }
   }
-  uint32_t taken = 0;
-  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  float sel_h = 0.f, sel_l = 0.f;
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bh = -INFINITY, bl = 0.f;
-    int bi = 0x7fffffff, bs = 0;
+    unsigned bh = 0, bl = 0;
+    int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kTopkMaxE / 32; ++i) {
-      if (lane + 32 * i < nc && !((taken >> i) & 1u) && dd_greater(vh[i], vl[i], vid[i], bh, bl, bi)) {
-        bh = vh[i];
-        bl = vl[i];
-        bi = vid[i];
-        bs = lane + 32 * i;
-      }
+    for (int i = 0; i < kTopkMaxE / 32; ++i) lane_best_dd(kh[i], kl[i], vid[i], bh, bl, bi);
+    unsigned mh, ml;
+    const int mi = warp_best_dd(bh, bl, bi, mh, ml);
+#pragma unroll
+    for (int i = 0; i < kTopkMaxE / 32; ++i) {  // expert ids are distinct: one candidate retires
+      const bool won = vid[i] == mi;
+      kh[i] = won ? 0u : kh[i];
+      kl[i] = won ? 0u : kl[i];
+      vid[i] = won ? 0x7fffffff : vid[i];
     }
-    for (int o = 16; o; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const int os = __shfl_xor_sync(0xffffffffu, bs, o);
-      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
-        bh = oh;
-        bl = ol;
-        bi = oi;
-        bs = os;
-      }
-    }
-    if ((bs & 31) == lane) taken |= 1u << (bs >> 5);
-    if (j == 0) {
-      top_h = bh;
-      top_l = bl;
-    }
-    if (lane == j) {
-      sel_h = bh;
-      sel_l = bl;
-      sel_id = bi;
-    }
+    sel_id = lane == j ? mi : sel_id;
+    sel_h = lane == j ? unkey(mh) : sel_h;
+    sel_l = lane == j ? unkey(ml) : sel_l;
   }
+  const float top_h = __shfl_sync(0xffffffffu, sel_h, 0), top_l = __shfl_sync(0xffffffffu, sel_l, 0);
   float ex = 0.f;
   if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
   float sum = ex;
@@ -495,52 +477,33 @@ __global__ void __launch_bounds__(kRdThreads) router_dd_kernel(FwdParams p) {
 template <int NPL>
 __device__ void topk_warp_dd(const FwdParams& p, int t) {
   const int lane = threadIdx.x & 31, E = p.E, k = p.k;
-  float vh[NPL], vl[NPL];
+  unsigned kh[NPL], kl[NPL];  // absent and taken candidates: (0, 0)
 #pragma unroll
   for (int i = 0; i < NPL; ++i) {
     const int e = lane + 32 * i;
-    vh[i] = e < E ? p.logit_hi[(size_t)t * E + e] : -INFINITY;
-    vl[i] = e < E ? p.logit_lo[(size_t)t * E + e] : 0.f;
+    kh[i] = e < E ? fkey(p.logit_hi[(size_t)t * E + e]) : 0u;
+    kl[i] = e < E ? fkey(p.logit_lo[(size_t)t * E + e]) : 0u;
   }
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < NPL; ++i)
-    if (lane + 32 * i >= E) taken |= 1u << i;
-  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  float sel_h = 0.f, sel_l = 0.f;
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bh = -INFINITY, bl = 0.f;
+    unsigned bh = 0, bl = 0;
     int bi = 0x7fffffff;
 #pragma unroll
+    for (int i = 0; i < NPL; ++i) lane_best_dd(kh[i], kl[i], lane + 32 * i, bh, bl, bi);
+    unsigned mh, ml;
+    const int mi = warp_best_dd(bh, bl, bi, mh, ml);
+#pragma unroll
     for (int i = 0; i < NPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && dd_greater(vh[i], vl[i], e, bh, bl, bi)) {
-        bh = vh[i];
-        bl = vl[i];
-        bi = e;
-      }
+      const bool won = lane + 32 * i == mi;
+      kh[i] = won ? 0u : kh[i];
+      kl[i] = won ? 0u : kl[i];
     }
-    for (int o = 16; o; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
-        bh = oh;
-        bl = ol;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j == 0) {
-      top_h = bh;
-      top_l = bl;
-    }
-    if (lane == j) {
-      sel_h = bh;
-      sel_l = bl;
-      sel_id = bi;
-    }
+    sel_id = lane == j ? mi : sel_id;
+    sel_h = lane == j ? unkey(mh) : sel_h;
+    sel_l = lane == j ? unkey(ml) : sel_l;
   }
+  const float top_h = __shfl_sync(0xffffffffu, sel_h, 0), top_l = __shfl_sync(0xffffffffu, sel_l, 0);
   float ex = 0.f;
   if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
   float sum = ex;
@@ -549,12 +512,6 @@ __device__ void topk_warp_dd(const FwdParams& p, int t) {
     p.ids[(size_t)t * k + lane] = sel_id;
     p.gates[(size_t)t * k + lane] = ex / sum;
   }
-}
-
-// Order-preserving map of a float to an unsigned key (-0 folded into +0).
-__device__ __forceinline__ unsigned sort_key(float v) {
-  const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // The top k of one token over E <= 512 experts with the whole block (for
@@ -571,7 +528,7 @@ __device__ void topk_radix_dd(const FwdParams& p, int* mem) {
   int* hist = mem;            // [256]
   int* ctl = mem + 256;       // [0] prefix, [1] rank left, [2] candidates
   int* cand = mem + 264;      // [32] candidate experts
-  const unsigned key = tid < E ? sort_key(p.logit_hi[tid]) : 0u;
+  const unsigned key = tid < E ? fkey(p.logit_hi[tid]) : 0u;
   if (tid == 0) {
     ctl[0] = 0;
     ctl[1] = k;
@@ -642,34 +599,22 @@ __device__ void topk_radix_dd(const FwdParams& p, int* mem) {
   }
   if (warp != 0) return;
   const int e = lane < nc ? cand[lane] : 0x7fffffff;
-  const float vh = lane < nc ? p.logit_hi[e] : -INFINITY, vl = lane < nc ? p.logit_lo[e] : 0.f;
-  bool taken = lane >= nc;
-  float sel_h = 0.f, sel_l = 0.f, top_h = 0.f, top_l = 0.f;
+  unsigned ckh = lane < nc ? fkey(p.logit_hi[e]) : 0u, ckl = lane < nc ? fkey(p.logit_lo[e]) : 0u;
+  int cid = e;
+  float sel_h = 0.f, sel_l = 0.f;
   int sel_id = 0;
   for (int j = 0; j < k; ++j) {  // k rounds over one candidate per lane, as topk_warp_dd
-    float bh = taken ? -INFINITY : vh, bl = taken ? 0.f : vl;
-    int bi = taken ? 0x7fffffff : e;
-    for (int o = 16; o; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (dd_greater(oh, ol, oi, bh, bl, bi)) {
-        bh = oh;
-        bl = ol;
-        bi = oi;
-      }
-    }
-    if (bi == e && lane < nc) taken = true;
-    if (j == 0) {
-      top_h = bh;
-      top_l = bl;
-    }
-    if (lane == j) {
-      sel_h = bh;
-      sel_l = bl;
-      sel_id = bi;
-    }
+    unsigned mh, ml;
+    const int mi = warp_best_dd(ckh, ckl, cid, mh, ml);
+    const bool won = cid == mi;
+    ckh = won ? 0u : ckh;
+    ckl = won ? 0u : ckl;
+    cid = won ? 0x7fffffff : cid;
+    sel_id = lane == j ? mi : sel_id;
+    sel_h = lane == j ? unkey(mh) : sel_h;
+    sel_l = lane == j ? unkey(ml) : sel_l;
   }
+  const float top_h = __shfl_sync(0xffffffffu, sel_h, 0), top_l = __shfl_sync(0xffffffffu, sel_l, 0);
   float ex = 0.f;
   if (lane < k) ex = expf((sel_h - top_h) + (sel_l - top_l));
   float sum = ex;

@@ -68,7 +68,6 @@ constexpr int kEpiPerQuad = kEpiThreads / 128;  // epilogue warps per TMEM lane 
 template <bool kDown>
 struct Mode {
   static constexpr int kPlanes = kDown ? 4 : 2;
-  static constexpr int kPanelRows = kDown ? kTcPanelRowsD : kTcPanelRows;
   static constexpr int kPanelStep = kDown ? kTcPanelStepD : kTcPanelStep;
   static constexpr int kSfBlocks = kDown ? 2 : 1;  // 512-byte B scale blocks per panel step (32 rows x 4 words each)
   static constexpr int kAPair = 2 * kAOp + 1024;
