@@ -60,6 +60,7 @@ constexpr int kChunks = 3;         // fixed k-tile chunks of every unit
 constexpr int kHalf = 8;           // tokens of a down unit (a slot with more tokens has two halves)
 constexpr int kGroupBytes = 2 * kTileBytes;  // a ring slot: one gate/up tile pair or two down tiles
 constexpr int kMaxUS = 8;                       // unit slots (partial-sum buffers) per phase, at most
+constexpr int kRing = 4;                        // groups in each warp's weight ring
 
 __device__ __forceinline__ Shared carve(uint8_t* sm, const DecParams& p) {
   Shared s;
@@ -177,7 +178,9 @@ __device__ void scale_x(const DecParams& p, const Shared& s) {
 __device__ __forceinline__ bool scale_x_beside_topk(const DecParams& p) { return p.f.T <= kWarps / 2; }
 
 // The (slot, half) pairs of the down phase, in slot order: a slot with more
-// than kHalf tokens contributes two (tokens [0, 8) and [8, n)). One warp.
+// than kHalf tokens contributes two (tokens [0, 8) and [8, n)). One warp,
+// after the whole CTA's sort of more than 32 pairs (the small sort lists them
+// itself).
 __device__ void build_halves(const Shared& s) {
   const int lane = threadIdx.x & 31;
   const int nsl = s.misc[1], nr = s.misc[0];
@@ -218,9 +221,12 @@ __device__ void routing(const DecParams& p, const Shared& s, unsigned seq, volat
     __syncthreads();
   }
   if (warp == 0) {
-    if (p.f.P <= 32) bucket_small(p, s);
-    __syncwarp();
-    build_halves(s);
+    if (p.f.P <= 32) {
+      bucket_small<kHalf>(p, s);
+    } else {
+      __syncwarp();
+      build_halves(s);
+    }
   } else if (warp == 1 && blockIdx.x == 0 && p.f.P <= 32) {
     export_counts_small(p, s);
   }
@@ -881,11 +887,14 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
   p.off_red = (int)off;
   off = up(off + (size_t)kWarps * kDecodeMaxT * sizeof(dd), 16);
   const size_t route_bytes = route_region_bytes(f.E, f.k);
-  // the deepest weight ring per warp that fits: 8, 6 or 4 slots (a 12-slot
-  // ring measured no faster: the stream is not short of copies in flight)
-  const int tries[7][2] = {{kMaxUS, 8}, {4, 8}, {kMaxUS, 6}, {4, 6}, {kMaxUS, 4}, {4, 4}, {2, 4}};
-  for (const auto& tr : tries) {
-    const int n_us = tr[0], rg_want = tr[1];
+  // Each warp's weight ring holds kRing groups: measured on the decode layer,
+  // 4 groups per warp (70 KB per SM in flight, about the HBM rate times its
+  // latency) beat 8 (25.4 -> 24.2 us per layer), 6, 3 and 2: deeper rings only
+  // queue copies that hold up the warp that issues them. The ring region also
+  // holds the CTA's router rows during phase A, so it is at least that large.
+  const long long router_bytes = (long long)((f.E + 1 + num_sms - 1) / num_sms) * f.d * 4;  // + the gate row
+  const size_t ring_bytes = std::max((size_t)kWarps * kRing * kGroupBytes, (size_t)router_bytes);
+  for (const int n_us : {kMaxUS, 4, 2}) {
     size_t o = off;
     p.n_us = n_us;
     p.off_pgu = (int)o;
@@ -895,13 +904,9 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
     p.off_route = (int)o;
     o = up(o + route_bytes, 128);
     p.off_ring = (int)o;
-    const long long room = (long long)max_smem - (long long)o;
-    const int rg = (int)(room / ((long long)kWarps * kGroupBytes));
-    // the ring also holds the CTA's router rows during phase A
-    const long long router_bytes = (long long)((f.E + 1 + num_sms - 1) / num_sms) * f.d * 4;  // + the gate row
-    if (rg >= rg_want && (long long)kWarps * rg_want * kGroupBytes >= router_bytes) {
-      p.ring_groups = rg_want;
-      p.smem_bytes = (int)(o + (size_t)kWarps * rg_want * kGroupBytes);
+    if ((long long)(o + ring_bytes) <= (long long)max_smem) {
+      p.ring_groups = kRing;
+      p.smem_bytes = (int)(o + ring_bytes);
       // one CTA per SM: more than half of the shared memory keeps a second CTA out
       if (p.smem_bytes <= max_smem / 2) p.smem_bytes = max_smem / 2 + 128;
       return true;
@@ -911,20 +916,12 @@ bool decode_plan(DecParams& p, int max_smem, int num_sms) {
 }
 
 cudaError_t configure_decode(int max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_layer_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_layer_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  return e;
+  return cudaFuncSetAttribute(decode_layer_kernel<kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
 int decode_blocks_per_sm(const DecParams& p) {
   int n = 0;
-  cudaError_t e;
-  if (p.ring_groups == 8) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<8>, kThreads, p.smem_bytes);
-  else if (p.ring_groups == 6) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<6>, kThreads, p.smem_bytes);
-  else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<4>, kThreads, p.smem_bytes);
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<kRing>, kThreads, p.smem_bytes);
   return e == cudaSuccess ? n : 0;
 }
 
@@ -945,9 +942,7 @@ cudaError_t launch_decode(const DecParams& p, cudaStream_t stream, int num_sms, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.ring_groups == 8) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, p);
-  if (p.ring_groups == 6) return cudaLaunchKernelEx(&cfg, decode_layer_kernel<6>, p);
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<4>, p);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<kRing>, p);
 }
 
 }  // namespace moe

@@ -294,58 +294,82 @@ __device__ void topk_token(const DecParams& p, const Shared& s, int t, unsigned 
   }
 }
 
-// Counting sort of P <= 32 pairs by expert with one warp: pair q's position
-// is the number of pairs with a smaller expert, or the same expert and a
-// smaller pair index (a stable sort), counted over all pairs at once.
+// Counting sort of P <= 32 pairs by expert with one warp. Lane q reads every
+// pair's expert (broadcast shared-memory loads) and counts for its own pair q
+// the pairs of smaller experts (the first sorted position of its expert), of
+// its expert, and before it in the stable order (its sorted position); two
+// ballots mark the first pair of every expert of the shard (and those with
+// more than HALF pairs), and one more pass counts the slots below each: no
+// shuffles and no branches in the loops. With HALF > 0 it also lists the
+// (slot, half) pairs of the mma.sync kernel's down phase: a slot with more than
+// HALF tokens has two, tokens [0, HALF) and [HALF, n).
+template <int HALF>
 __device__ void bucket_small(const DecParams& p, const Shared& s) {
   const FwdParams& f = p.f;
   const int lane = threadIdx.x & 31;
   const int P = f.P, E = f.E, T = f.T;
-  const int my_e = lane < P ? s.ids[lane] : 0x7fffffff;
-  int rank = 0;
+  const bool act = lane < P;
+  const int e = act ? s.ids[lane] : 0x7fffffff;
+  int below = 0, same = 0, rank = 0;
   for (int j = 0; j < P; ++j) {
-    const int ej = __shfl_sync(0xffffffffu, my_e, j);
-    rank += (ej < my_e) || (ej == my_e && j < lane);
+    const int ej = s.ids[j];
+    below += ej < e;
+    same += ej == e;
+    rank += (ej < e) || (ej == e && j < lane);
   }
-  if (lane < P) s.perm[rank] = lane;
-  __syncwarp();
-  const int qs = lane < P ? s.perm[lane] : 0;
-  const unsigned key = lane < P ? ((unsigned)s.ids[qs] << 8) | (unsigned)qs : 0xffffffffu;
-  __syncwarp();
-  const int e = (int)(key >> 8), q = (int)(key & 0xffu);
-  const int eprev = __shfl_up_sync(0xffffffffu, e, 1);
-  const bool start = lane < P && (lane == 0 || e != eprev);  // first pair of its expert
-  const unsigned starts = __ballot_sync(0xffffffffu, start);
-  // slots: the experts of this context's shard that received pairs
-  const bool first = start && expert_in_shard(e, f.e_begin, f.e_end);
-  const unsigned firsts = __ballot_sync(0xffffffffu, first);
-  const int ns = __popc(firsts);
-  if (lane < P) {
-    s.perm[lane] = q;
-    s.inv[q] = lane;
+  const bool in = act && rank == below && expert_in_shard(e, f.e_begin, f.e_end);  // first pair of a shard expert
+  const unsigned firsts = __ballot_sync(0xffffffffu, in);
+  const unsigned bigs = HALF > 0 ? __ballot_sync(0xffffffffu, in && same > HALF) : 0u;
+  int slot = 0, big = 0;
+  for (int j = 0; j < P; ++j) {
+    const int ej = s.ids[j];
+    slot += ((firsts >> j) & 1u) && ej < e;
+    big += ((bigs >> j) & 1u) && ej < e;
+  }
+  if (act) {
+    s.perm[rank] = lane;
+    s.inv[lane] = rank;
     if (blockIdx.x == 0) {
-      f.perm[lane] = q;
-      f.inv[q] = lane;
+      f.perm[rank] = lane;
+      f.inv[lane] = rank;
     }
   }
-  if (first) {
-    const int slot = __popc(firsts & ((1u << lane) - 1u));
-    const unsigned after = starts & ~((2u << lane) - 1u);  // the next expert's first lane, or P
-    const int next = after ? __ffs(after) - 1 : P;
+  if (in) {
     s.slot_e[slot] = e;
-    s.slot_q0[slot] = lane;
-    s.slot_n[slot] = next - lane;
+    s.slot_q0[slot] = below;
+    s.slot_n[slot] = same;
+    if (HALF > 0) {
+      s.hs_slot[slot + big] = slot;
+      s.hs_half[slot + big] = 0;
+      if (same > HALF) {
+        s.hs_slot[slot + big + 1] = slot;
+        s.hs_half[slot + big + 1] = 1;
+      }
+    }
   }
   if (lane == 0) {
+    const int ns = __popc(firsts), nh = ns + __popc(bigs);
     s.misc[0] = ns;
-    int tot = ns;
-    if (f.S > 0 && f.e_begin == 0) {
+    int tot = ns, th = nh;
+    if (f.S > 0 && f.e_begin == 0) {  // the shared expert: slot ns, every token
       s.slot_e[ns] = E;
       s.slot_n[ns] = T;
       s.slot_q0[ns] = P;
       ++tot;
+      if (HALF > 0) {
+        s.hs_slot[th] = ns;
+        s.hs_half[th++] = 0;
+        if (T > HALF) {
+          s.hs_slot[th] = ns;
+          s.hs_half[th++] = 1;
+        }
+      }
     }
     s.misc[1] = tot;
+    if (HALF > 0) {
+      s.misc[4] = th;
+      s.misc[5] = nh;
+    }
   }
 }
 

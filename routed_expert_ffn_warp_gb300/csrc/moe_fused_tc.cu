@@ -225,7 +225,7 @@ __device__ void tc_routing(const DecParams& p, const Shared& s, unsigned seq, vo
   if (p.f.P > 32) {
     bucket_large(p, s);  // the whole CTA sorts
   } else if (warp == 0) {
-    bucket_small(p, s);
+    bucket_small<0>(p, s);
   } else if (warp == 1 && blockIdx.x == 0) {
     export_counts_small(p, s);
   }
