@@ -197,9 +197,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   const size_t o_xg = take(affine ? (size_t)Tm * xg_pitch * 4 : 0), o_hb = take(affine ? Qm * hgroups * 4 : 0);
   // a row of zeros that absent activation rows of the affine GEMMs read (never written)
   const size_t o_zero = take(affine ? (size_t)4 * std::max(d64, fmax64) : 0);
-  // fused-path counters: two halves, used by alternate launches (see moe_decode.cu)
+  // fused mma.sync path: launch-tagged words of h, its scales and the partial down rows
   const size_t Qd = (size_t)std::min(Tm, moe::kDecodeMaxT) * (k + (S > 0 ? 1 : 0));  // pair rows of the fused path
-  const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_rowcnt = take((size_t)2 * (d / 16) * 4),
+  const size_t o_hw = take(Qd * fmax64 * 8), o_hsw = take(Qd * hgroups * 8), o_pw = take(Qd * d * 8),
                o_bar = take((size_t)std::max(ctx->num_sms, 1) * 4),
                o_lw = take((size_t)moe::kLogitWordCopies * std::min(Tm, moe::kDecodeMaxT) * (E + 1) * 2 * 8);
   // fused tcgen05 path: x planes and h planes per K step with their launch-tagged flags, row-tile counters
@@ -300,7 +300,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   dp.f = p;
   dp.hwords = reinterpret_cast<unsigned long long*>(w + o_hw);
   dp.hswords = reinterpret_cast<unsigned long long*>(w + o_hsw);
-  dp.rowcnt = reinterpret_cast<int*>(w + o_rowcnt);
+  dp.pwords = reinterpret_cast<unsigned long long*>(w + o_pw);
   dp.bar_flags = reinterpret_cast<unsigned*>(w + o_bar);
   dp.lwords = reinterpret_cast<unsigned long long*>(w + o_lw);
   dp.tcap = std::min(Tm, moe::kDecodeMaxT);

@@ -24,9 +24,10 @@
 //      its gate/up tiles in its ring. For each (slot, half) of the CTA the
 //      CTA stages the slot's h in shared memory, polling (bounded) the words
 //      until they carry this launch's number;
-//      the last chunk warp of a unit writes its partial rows, and the CTA
-//      finishing a row tile's last (slot, half) combines it:
-//      y = sum_j g_j part_j (slot order j) + shared, one rounding.
+//      the last chunk warp of a unit publishes its partial rows as tagged
+//      words, and the warp holding a row tile's unit of the last (slot, half)
+//      combines the tile once every pair's words carry this launch's number:
+//      y = sum_j g_j part_j (top-k order j) + shared, one rounding.
 //
 // The pages: expert pairs grouped by expert, one pass over each selected
 // expert's rows for all of its tokens, fused gate/up then down, a row summed
@@ -454,9 +455,11 @@ __device__ void gateup_reduce(const DecParams& p, const Shared& s, const Unit& u
 }
 
 // Down unit epilogue (the last chunk warp): the unit's 16 partial rows of each
-// of its tokens; the CTA finishing a row tile's last (slot, half) combines it.
+// of its tokens, published as 64-bit words that carry the launch sequence
+// number (payload fp32 bits << 32), like h: the combining CTA polls the data.
 __device__ void down_reduce(const DecParams& p, const Shared& s, const Unit& un, const float* pb) {
   const FwdParams& f = p.f;
+  const unsigned seq = (unsigned)s.misc[3];
   const int lane = threadIdx.x & 31;
   const int hh = min(kHalf, p.tcap), cs = 16 * hh;
   for (int o = lane; o < 16 * un.n; o += 32) {
@@ -464,47 +467,74 @@ __device__ void down_reduce(const DecParams& p, const Shared& s, const Unit& un,
     float a = 0.f;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) a += pb[c * cs + r * hh + m];
-    f.part[(size_t)(un.q0 + m) * f.d + 16 * un.idx + r] = a;
+    st_relaxed_u64(p.pwords + (size_t)(un.q0 + m) * f.d + 16 * un.idx + r,
+                   ((unsigned long long)__float_as_uint(a) << 32) | seq);
   }
 }
 
-__device__ void combine_rows(const DecParams& p, const Shared& s, int idx) {
+// Wait (bounded) until each of the n words at w[i] carries launch number seq
+// in its low half, reloading all the stale ones together; v[i] holds them.
+// A null w[i] counts as present.
+template <int N>
+__device__ __forceinline__ void poll_words(const DecParams& p, const unsigned long long* const (&w)[N],
+                                           unsigned long long (&v)[N], unsigned seq, volatile int* abort) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = w[i] ? ld_relaxed_u64(w[i]) : (unsigned long long)seq;
+  uint64_t t0 = 0;
+  while (true) {
+    bool stale = false;
+#pragma unroll
+    for (int i = 0; i < N; ++i) stale = stale || (unsigned)v[i] != seq;
+    if (!stale || *abort) return;
+    if (t0 == 0) t0 = globaltimer();
+    else if (timed_out(t0, p.wait_ns)) {
+      give_up(abort, p.f.status);
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((unsigned)v[i] != seq) v[i] = ld_relaxed_u64(w[i]);
+  }
+}
+
+// Row tile idx of every token, by the CTA that runs the tile's down unit of
+// the last (slot, half) pair: y = sum_j g_j part_j (the token's pairs in
+// top-k order; pairs of other shards add 0) + shared, one rounding. The
+// partial rows come from the tile's down units in other CTAs as tagged words:
+// no fence, no counter, one round trip once they are all written.
+__device__ void combine_rows(const DecParams& p, const Shared& s, int idx, volatile int* abort) {
   const FwdParams& f = p.f;
+  const unsigned seq = (unsigned)s.misc[3];
   const int lane = threadIdx.x & 31;
   const int r0 = 16 * idx, n = f.T * 16;
-  constexpr int kO = 2, kJ = 8;  // outputs per lane and pairs per round: their loads are all in flight at once
-  for (int o0 = lane; o0 < n; o0 += 32 * kO) {
-    float a[kO];
+  constexpr int kJ = 8;  // pairs whose words are in flight together
+  for (int o = lane; o < n; o += 32) {
+    const int t = o >> 4, r = o & 15;
+    float a = 0.f;
+    for (int j0 = 0; j0 < f.k; j0 += kJ) {  // sums kept in top-k order
+      const unsigned long long* w[kJ];
+      unsigned long long v[kJ];
 #pragma unroll
-    for (int i = 0; i < kO; ++i) a[i] = 0.f;
-    for (int j0 = 0; j0 < f.k; j0 += kJ) {  // sums kept in slot order
-      float pv[kO][kJ];
-#pragma unroll
-      for (int i = 0; i < kO; ++i) {
-        const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
-#pragma unroll
-        for (int jj = 0; jj < kJ; ++jj)
-          pv[i][jj] = (o < n && j0 + jj < f.k && expert_in_shard(s.ids[t * f.k + j0 + jj], f.e_begin, f.e_end))
-                          ? __ldcg(f.part + (size_t)s.inv[t * f.k + j0 + jj] * f.d + r0 + r)
-                          : 0.f;  // this shard's pairs only (all of them without sharding)
+      for (int jj = 0; jj < kJ; ++jj) {
+        const int j = j0 + jj;
+        w[jj] = (j < f.k && expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
+                    ? p.pwords + (size_t)s.inv[t * f.k + j] * f.d + r0 + r
+                    : nullptr;  // this shard's pairs only (all of them without sharding)
       }
+      poll_words<kJ>(p, w, v, seq, abort);
 #pragma unroll
-      for (int i = 0; i < kO; ++i) {
-        const int t = (o0 + 32 * i) >> 4;
-#pragma unroll
-        for (int jj = 0; jj < kJ; ++jj)
-          if (j0 + jj < f.k && o0 + 32 * i < n) a[i] = fmaf(s.gates[t * f.k + j0 + jj], pv[i][jj], a[i]);
-      }
+      for (int jj = 0; jj < kJ; ++jj)
+        if (j0 + jj < f.k) a = fmaf(s.gates[t * f.k + j0 + jj], w[jj] ? __uint_as_float((unsigned)(v[jj] >> 32)) : 0.f, a);
     }
-#pragma unroll
-    for (int i = 0; i < kO; ++i) {
-      const int o = o0 + 32 * i, t = o >> 4, r = o & 15;
-      if (o >= n) continue;
-      float y = a[i];
-      if (f.S > 0 && f.e_begin == 0) y += (f.w_sg ? s.sg[t] : 1.f) * __ldcg(f.part + (size_t)(f.P + t) * f.d + r0 + r);
-      if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = y;
-      else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(y);
+    float y = a;
+    if (f.S > 0 && f.e_begin == 0) {
+      const unsigned long long* w[1] = {p.pwords + (size_t)(f.P + t) * f.d + r0 + r};
+      unsigned long long v[1];
+      poll_words<1>(p, w, v, seq, abort);
+      y += (f.w_sg ? s.sg[t] : 1.f) * __uint_as_float((unsigned)(v[0] >> 32));
     }
+    if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + r0 + r] = y;
+    else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + r0 + r] = __float2bfloat16_rn(y);
   }
 }
 
@@ -680,7 +710,7 @@ __device__ void gateup_item(const DecParams& p, const Shared& s, const Plan& pl,
 }
 
 template <int NT, int RG>
-__device__ void down_item(const DecParams& p, const Shared& s, const Plan& pl, const Item& it, const Unit& un,
+__device__ void down_item(const DecParams& p, const Shared& s, const Plan& pl, const Item& it, const Unit& un, int hs,
                           uint8_t* ring, int& slot, Cursor& cu, uint64_t pol, int w, volatile int* abort) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   float acc[NT][2];
@@ -730,14 +760,9 @@ __device__ void down_item(const DecParams& p, const Shared& s, const Plan& pl, c
   if (!arrive_chunk(s.ctl + 2 * kMaxUS + us)) return;
   down_reduce(p, s, un, pb);
   free_slot(s.ctl + 2 * kMaxUS + us, s.ctl + 3 * kMaxUS + us, it.u + p.n_us);
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(&s.rowcnt[un.idx], 1) == s.misc[4] - 1;
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (last) {
-    __threadfence();
-    combine_rows(p, s, un.idx);
+  if (hs == s.misc[4] - 1) {  // the tile's last (slot, half): this warp combines the tile
+    __syncwarp();  // the warp's own words are written
+    combine_rows(p, s, un.idx, abort);
   }
 }
 
@@ -804,8 +829,8 @@ __device__ void stream_layer(const DecParams& p, const Shared& s, volatile int* 
         const Item it = item_of(p, s, pl, w, j);
         const Unit un = dn_unit(p, s, pl.d0 + it.u);
         if ((pl.d0 + it.u) / ud != hs) break;
-        if (un.n <= 4) down_item<1, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
-        else down_item<2, RG>(p, s, pl, it, un, ring, slot, cu, pol, w, abort);
+        if (un.n <= 4) down_item<1, RG>(p, s, pl, it, un, hs, ring, slot, cu, pol, w, abort);
+        else down_item<2, RG>(p, s, pl, it, un, hs, ring, slot, cu, pol, w, abort);
       }
     }
   }
@@ -840,15 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(DecParams p) 
   }
   __syncthreads();
   const unsigned seq = (unsigned)s.misc[3];
-  // This launch counts in half seq & 1 of the counters (zeroed by the previous
-  // launch, or at creation) and zeroes the other half for the next launch.
-  if (blockIdx.x == 0) {
-    int* rc = p.rowcnt + (size_t)((seq + 1) & 1) * (p.f.d / 16);
-    for (int i = tid; i < p.f.d / 16; i += kThreads) rc[i] = 0;
-  }
   stage_x(p, s);
   __syncthreads();
-  s.rowcnt = p.rowcnt + (size_t)(seq & 1) * (p.f.d / 16);
   router(p, s, seq);  // its reads of the bf16 x end before its last barrier (it has none without experts)
   if (!scale_x_beside_topk(p)) {
     scale_x(p, s);

@@ -50,7 +50,6 @@ struct Shared {
   int* misc;  // [0] n_routed, [1] n_slots, [2] abort, [3] launch sequence number,
               // [4] (slot, half) pairs, [5] pairs of routed slots, [6] warps done with their gate/up items
   uint8_t* ring;  // [16 warps][ring_groups][kGroupBytes]
-  int* rowcnt;
 };
 
 // The routing arrays of both kernels at p.off_route (route_region_bytes long):

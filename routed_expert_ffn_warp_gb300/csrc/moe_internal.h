@@ -229,7 +229,7 @@ struct DecParams {
   FwdParams f;
   unsigned long long* hwords;   // [Qd][fmax64] h as (f16 hi | f16 lo << 16) << 32 | launch sequence
   unsigned long long* hswords;  // [Qd][hgroups] its per-16 scales: (fp32 bits << 32) | launch sequence
-  int* rowcnt;          // [2][d/16] finished down units per row tile
+  unsigned long long* pwords;   // [Qd][d] partial down rows: (fp32 bits << 32) | launch sequence
   unsigned* bar_flags;  // [grid] per-CTA launch sequence numbers (each only grows)
   unsigned long long* lwords;  // [kLogitWordCopies][tcap][E][2] published logits: (fp32 bits << 32) | sequence
   int tcap;             // tokens the x16 shared area holds (min(t_max, kDecodeMaxT))
