@@ -141,7 +141,7 @@ struct FwdParams;
 // shared expert.
 __host__ __device__ inline bool expert_in_shard(int e, int e_begin, int e_end) { return e >= e_begin && e < e_end; }
 
-constexpr int kRouterSplits = 4;  // most ranges of d the router's fp32 pass splits into
+constexpr int kRouterSplits = 8;  // most ranges of d the router's fp32 pass splits into
 // Multi-kernel path with T <= kRouteDDMaxT: every logit as a double-float sum
 // spread over all SMs (router_dd_kernel), the top k inside the bucketing
 // kernel (one warp per token); larger T takes the two-pass fp32 router.
@@ -191,6 +191,7 @@ struct FwdParams {
   float* logit_lo;       // = logit_hi + lstride
   size_t lstride;        // t_max * E
   int rsplit;            // ranges of d in the router's fp32 pass (set by the launcher)
+  int rsplit_max;        // most ranges the workspace holds planes for (0: kRouterSplits)
   float* xsq;            // [kRouterSplits][t_max]: sums of squares of x_t per range (lstride / E apart)
   float* wsq;            // [kRouterSplits][E]: sums of squares of W_r[e] per range
   int32_t* ids;          // [t_max][k]

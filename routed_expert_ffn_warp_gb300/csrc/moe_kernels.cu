@@ -297,28 +297,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(FwdParams p) {
   __syncthreads();
   if (warp == 0) {
     // the k-th largest lower bound (ties: lower index first, for a fixed choice)
+    // k rounds over keys of the lower bounds (taken ones retired), each lane's
+    // best by selects and the warp's by redux.sync: no divergent branch
     uint32_t taken = 0;
     float kth = -INFINITY;
+    const int ni = (E + 31) / 32;
     for (int j = 0; j < k; ++j) {
-      float b = -INFINITY;
+      unsigned bh = 0, bl = 0;
       int bi = 0x7fffffff;
-      for (int i = 0; 32 * i + lane < E; ++i) {
+      for (int i = 0; i < ni; ++i) {
         const int e = 32 * i + lane;
-        if (!((taken >> i) & 1u) && (lb[e] > b || (lb[e] == b && e < bi))) {
-          b = lb[e];
-          bi = e;
-        }
+        const unsigned key = (e < E && !((taken >> i) & 1u)) ? fkey(lb[e]) : 0u;
+        lane_best_dd(key, 0u, e, bh, bl, bi);
       }
-      for (int o = 16; o; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, b, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ob > b || (ob == b && oi < bi)) {
-          b = ob;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      kth = b;
+      unsigned mh, ml;
+      const int mi = warp_best_dd(bh, bl, bi, mh, ml);
+      taken |= ((mi & 31) == lane) ? 1u << (mi >> 5) : 0u;
+      kth = unkey(mh);
     }
     int nc = 0;
     for (int i = 0; 32 * i < E; ++i) {
@@ -626,11 +621,15 @@ __device__ void topk_radix_dd(const FwdParams& p, int* mem) {
 }
 
 // K ranges of the router's fp32 pass: enough blocks for about two per SM.
-__host__ inline int router_splits(int T, int E, int d) {
+// Ranges of d for the fp32 pass: about four blocks per SM (measured on the
+// 1,024-token layer: 256 blocks -> 512 blocks, 516 -> 506 us per layer; more
+// ranges change no rounding count of the certified bound), at most `cap` and
+// one per 128-element chunk.
+__host__ inline int router_splits(int T, int E, int d, int cap) {
   const int tiles = ((T + kRfTok - 1) / kRfTok) * ((E + kRfExp - 1) / kRfExp);
   const int nch = (d + kRfK - 1) / kRfK;
-  int s = (296 + tiles - 1) / tiles;
-  s = s < 1 ? 1 : s > kRouterSplits ? kRouterSplits : s;
+  int s = (608 + tiles - 1) / tiles;
+  s = s < 1 ? 1 : s > cap ? cap : s;
   return s < nch ? s : nch;
 }
 
@@ -928,7 +927,7 @@ void launch_router(FwdParams p, cudaStream_t stream, bool with_prep_x) {
                    0, stream, p);
     return;
   }
-  p.rsplit = router_splits(p.T, p.E, p.d);
+  p.rsplit = router_splits(p.T, p.E, p.d, p.rsplit_max > 0 ? p.rsplit_max : kRouterSplits);
   launch_chained(router_fp32_kernel, dim3((p.T + kRfTok - 1) / kRfTok, (p.E + kRfExp - 1) / kRfExp, p.rsplit),
                  dim3(kRfThreads), 0, stream, p);
   launch_chained(topk_kernel, dim3(p.T), dim3(kTopkThreads), 0, stream, p);

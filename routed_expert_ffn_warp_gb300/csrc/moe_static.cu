@@ -21,13 +21,14 @@ constexpr int kMaxDevices = 64;
 // planes (the first two are the logits' hi and lo), inverse permutation,
 // work-list slots, sums of squares of the router rows and of x (these are
 // fully rewritten by every call; no part must start at zero).
+constexpr int kStaticSplits = 4;  // ranges of d of the router's fp32 pass this array has planes for
 constexpr size_t kOffHi = 0;
-constexpr size_t kOffInv = kOffHi + moe::kRouterSplits * kMaxLogits * 4;
+constexpr size_t kOffInv = kOffHi + kStaticSplits * kMaxLogits * 4;
 constexpr size_t kOffSlots = kOffInv + kMaxPairs * 4;
 constexpr size_t kSlotInts = 1 + 3 * 513 + 2 * 514;
 constexpr size_t kOffWsq = (kOffSlots + kSlotInts * 4 + 255) / 256 * 256;
-constexpr size_t kOffXsq = kOffWsq + moe::kRouterSplits * 512 * 4;
-static_assert(kOffXsq + moe::kRouterSplits * kMaxLogits * 4 <= kScratchBytes, "scratch layout exceeds the array");
+constexpr size_t kOffXsq = kOffWsq + kStaticSplits * 512 * 4;
+static_assert(kOffXsq + kStaticSplits * kMaxLogits * 4 <= kScratchBytes, "scratch layout exceeds the array");
 
 __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
@@ -96,6 +97,7 @@ extern "C" int moe_route_static(const void* x, int T, int d, const float* w_rout
   p.bias = bias;
   p.logit_hi = reinterpret_cast<float*>(sc + kOffHi);
   p.lstride = (size_t)T * n_experts;
+  p.rsplit_max = kStaticSplits;
   p.logit_lo = p.logit_hi + p.lstride;
   p.wsq = reinterpret_cast<float*>(sc + kOffWsq);
   p.xsq = reinterpret_cast<float*>(sc + kOffXsq);
