@@ -451,12 +451,18 @@ __global__ void __launch_bounds__(kThr, 1) gemm_tc_kernel(const FwdParams p, con
   }
 }
 
-// Activation panels: one CTA per (panel, K step). Panel rows n < 2 npad:
-// plane n / npad, token m = n % npad of the block (rows past the block's
-// tokens are zero, their scales 127).
+// Activation panels: one CTA per (panel, kPanelSteps K steps). Panel rows
+// n < 2 npad: plane n / npad, token m = n % npad of the block (rows past the
+// block's tokens are zero, their scales 127). The rows' tokens are looked up
+// once into shared memory; then every thread issues all of its 16-byte loads
+// of the block's K steps before its first store, so the block waits for one
+// round trip, not one per chunk.
 constexpr int kPanelSteps = 4;  // K steps of the x panels per block
-__global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
+constexpr int kPanelThreads = 256;
+constexpr int kPanelLoads = (2 * kMaxTok * 8 * kPanelSteps + kPanelThreads - 1) / kPanelThreads;  // per thread
+__global__ void __launch_bounds__(kPanelThreads) pack_panels_kernel(FwdParams p) {
   pdl_enter();
+  __shared__ int tok[2 * kMaxTok];  // token of each panel row, -1 for padding rows
   const int pb = blockIdx.x;
   const int ns = *p.n_slots;
   if (pb >= p.panel_prefix[ns]) return;
@@ -464,30 +470,46 @@ __global__ void __launch_bounds__(256) pack_panels_kernel(FwdParams p) {
   const int tb = pb - p.panel_prefix[s];
   const int n = min(kMaxTok, p.slot_n[s] - kMaxTok * tb), q0 = p.slot_q0[s] + kMaxTok * tb, npad = npad_of(n);
   const int nks = tc_ksteps(p.d);
-  // kPanelSteps K steps per block: the slot lookup and the rows' tokens serve all of them
-  for (int ks = blockIdx.y * kPanelSteps; ks < min(nks, (blockIdx.y + 1) * kPanelSteps); ++ks) {
-    uint8_t* dst = p.xpanel + ((size_t)pb * nks + ks) * kTcPanelStep;
-    for (int o = threadIdx.x; o < 2 * npad * 8; o += 256) {  // 16-byte chunks (row, kc) of the N = 2 npad rows
-      const int row = o >> 3, kc = o & 7;
-      const int plane = row >= npad, m = row - plane * npad, k0 = kTcStepK * ks + 16 * kc;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (row < 2 * npad && m < n && k0 < p.d64)
-        v = *reinterpret_cast<const uint4*>(p.xq + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.d64 + k0);
-      *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = v;
-    }
-    if (threadIdx.x < 128) {  // scale word (lane l, r) for B row 32 r + l
-      const int l = threadIdx.x >> 2, r = threadIdx.x & 3, row = 32 * r + l;
-      const int plane = row >= npad, m = row - plane * npad;
+  for (int r = threadIdx.x; r < 2 * npad; r += kPanelThreads) {
+    const int m = r - (r >= npad ? npad : 0);
+    tok[r] = m < n ? tok_of(p, q0 + m) : -1;
+  }
+  __syncthreads();
+  const int ks0 = blockIdx.y * kPanelSteps, nk = min(nks, ks0 + kPanelSteps) - ks0;
+  const int nch = 2 * npad * 8;  // 16-byte chunks (row, kc) of one K step's N = 2 npad rows
+  uint4 v[kPanelLoads];
+#pragma unroll
+  for (int i = 0; i < kPanelLoads; ++i) {
+    const int o = threadIdx.x + kPanelThreads * i, kk = o / nch, c = o - kk * nch;
+    const int row = c >> 3, k0 = kTcStepK * (ks0 + kk) + 16 * (c & 7);
+    const int t = kk < nk ? tok[row] : -1;
+    v[i] = make_uint4(0, 0, 0, 0);
+    if (t >= 0 && k0 < p.d64)
+      v[i] = __ldg(reinterpret_cast<const uint4*>(p.xq + ((size_t)t * 2 + (row >= npad)) * p.d64 + k0));
+  }
+#pragma unroll
+  for (int i = 0; i < kPanelLoads; ++i) {
+    const int o = threadIdx.x + kPanelThreads * i, kk = o / nch, c = o - kk * nch;
+    if (kk >= nk) continue;
+    const int row = c >> 3, kc = c & 7;
+    uint8_t* dst = p.xpanel + ((size_t)pb * nks + ks0 + kk) * kTcPanelStep;
+    *reinterpret_cast<uint4*>(dst + ((row >> 3) * 8 + kc) * 128 + (row & 7) * 16) = v[i];
+  }
+  if (threadIdx.x < 128) {  // scale word (lane l, r) for B row 32 r + l, every K step of the block
+    const int l = threadIdx.x >> 2, r = threadIdx.x & 3, row = 32 * r + l;
+    const int t = row < 2 * npad ? tok[row] : -1;
+    const uint8_t* sc = t >= 0 ? p.xqs + ((size_t)t * 2 + (row >= npad)) * p.xq_spitch : nullptr;
+    for (int kk = 0; kk < nk; ++kk) {
+      const int ks = ks0 + kk;
       uint32_t w = 0x7F7F7F7Fu;
-      if (row < 2 * npad && m < n) {
-        const uint8_t* sc = p.xqs + ((size_t)tok_of(p, q0 + m) * 2 + plane) * p.xq_spitch;
+      if (sc) {
         w = 0;
         for (int kb = 0; kb < 4; ++kb) {
           const int blk = 4 * ks + kb;
           w |= (uint32_t)(blk < p.xq_spitch ? sc[blk] : 127) << (8 * kb);
         }
       }
-      *reinterpret_cast<uint32_t*>(dst + 2 * npad * kTcStepK + 16 * l + 4 * r) = w;
+      *reinterpret_cast<uint32_t*>(p.xpanel + ((size_t)pb * nks + ks) * kTcPanelStep + 2 * npad * kTcStepK + 16 * l + 4 * r) = w;
     }
   }
 }
