@@ -180,18 +180,21 @@ __device__ bool tc_poll_flags_warp(const unsigned* flags, int n, unsigned want, 
   }
 }
 
-// Phase A tail: K steps blockIdx.x, + G, ... of x as two E4M3 planes with
-// E8M0 scales per 32-element block (x = 2^sh hi + 2^sl lo), rows n = plane *
-// npad + t for every token (padding tokens and elements past d are zero), in
-// the MMA's operand order, then the scale block; each step's flag is raised
-// to `seq` once its bytes are written.
+// Phase A tail: K steps G-1-blockIdx.x, + G, ... of x as two E4M3 planes
+// with E8M0 scales per 32-element block (x = 2^sh hi + 2^sl lo), rows n =
+// plane * npad + t for every token (padding tokens and elements past d are
+// zero), in the MMA's operand order, then the scale block; each step's flag
+// is raised to `seq` once its bytes are written. The last CTAs take them:
+// they hold the fewest router rows (none when E < G), so the planes are ready
+// early and no CTA's routing waits behind them (measured: verify 77.1 -> 76.4,
+// small 59.6 -> 58.2 us per layer).
 __device__ void publish_x_planes(const TcLayerParams& P, const Shared& s, unsigned seq) {
   const DecParams& p = P.d;
   const FwdParams& f = p.f;
   const int nks = tc_ksteps(f.d), npad = npad8(f.T), nb = 2 * npad;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(s.x16);
-  for (int ks = blockIdx.x; ks < nks; ks += gridDim.x) {
+  for (int ks = gridDim.x - 1 - blockIdx.x; ks < nks; ks += gridDim.x) {
     uint8_t* dst = P.xplane + (size_t)ks * P.xp_step;
     // scale words of the rows past the planes (never read by the MMAs) hold 2^0
     for (int o = threadIdx.x; o < 128; o += kThreads) reinterpret_cast<uint32_t*>(dst + nb * 128)[o] = 0x7F7F7F7Fu;
@@ -235,16 +238,50 @@ __device__ void tc_routing(const DecParams& p, const Shared& s, unsigned seq, vo
 // y rows [256 dp, 256 dp + 256) of every token: sum_j g[t,j] part(pair (t, j)) in
 // slot order, then the shared expert, one rounding. The 256 epilogue threads.
 __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int et) {
-  for (int o = et; o < f.T * 256; o += kEpiThreads) {
-    const int t = o >> 8, row = 256 * dp + (o & 255);
-    if (row >= f.d) continue;
-    float y = 0.f;
-    for (int j = 0; j < f.k; ++j)  // this shard's pairs only (all of them without sharding)
-      if (expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
-        y = fmaf(s.gates[t * f.k + j], __ldcg(f.part + (size_t)s.inv[t * f.k + j] * f.d + row), y);
-    if (f.S > 0 && f.e_begin == 0) y += (f.w_sg ? s.sg[t] : 1.f) * __ldcg(f.part + (size_t)(f.P + t) * f.d + row);
-    if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + row] = y;
-    else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + row] = __float2bfloat16_rn(y);
+  // thread et: row 256 dp + et of every token; the loads of kO tokens x kJ
+  // pairs are all in flight together (one L2 round trip each, not one per
+  // pair and token), the sums kept in pair order
+  const int row = 256 * dp + et;
+  if (row >= f.d) return;
+  constexpr int kO = 4, kJ = 8;
+  const bool shared = f.S > 0 && f.e_begin == 0;
+  for (int t0 = 0; t0 < f.T; t0 += kO) {
+    float a[kO];
+#pragma unroll
+    for (int i = 0; i < kO; ++i) a[i] = 0.f;
+    for (int j0 = 0; j0 < f.k; j0 += kJ) {
+      float v[kO][kJ];
+#pragma unroll
+      for (int i = 0; i < kO; ++i)
+#pragma unroll
+        for (int jj = 0; jj < kJ; ++jj) {
+          const int t = t0 + i, j = j0 + jj;
+          v[i][jj] = (t < f.T && j < f.k && expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
+                         ? __ldcg(f.part + (size_t)s.inv[t * f.k + j] * f.d + row)
+                         : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < kO; ++i)
+#pragma unroll
+        for (int jj = 0; jj < kJ; ++jj) {
+          const int t = t0 + i, j = j0 + jj;  // this shard's pairs only (all of them without sharding)
+          if (t < f.T && j < f.k && expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
+            a[i] = fmaf(s.gates[t * f.k + j], v[i][jj], a[i]);
+        }
+    }
+    float sh[kO];
+#pragma unroll
+    for (int i = 0; i < kO; ++i)
+      sh[i] = (shared && t0 + i < f.T) ? __ldcg(f.part + (size_t)(f.P + t0 + i) * f.d + row) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kO; ++i) {
+      const int t = t0 + i;
+      if (t >= f.T) continue;
+      float y = a[i];
+      if (shared) y += (f.w_sg ? s.sg[t] : 1.f) * sh[i];
+      if (f.out_f32) reinterpret_cast<float*>(f.out)[(size_t)t * f.d + row] = y;
+      else reinterpret_cast<__nv_bfloat16*>(f.out)[(size_t)t * f.d + row] = __float2bfloat16_rn(y);
+    }
   }
 }
 
