@@ -238,12 +238,13 @@ __device__ void tc_routing(const DecParams& p, const Shared& s, unsigned seq, vo
 // y rows [256 dp, 256 dp + 256) of every token: sum_j g[t,j] part(pair (t, j)) in
 // slot order, then the shared expert, one rounding. The 256 epilogue threads.
 __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int et) {
-  // thread et: row 256 dp + et of every token; the loads of kO tokens x kJ
-  // pairs are all in flight together (one L2 round trip each, not one per
-  // pair and token), the sums kept in pair order
+  // thread et: row 256 dp + et of every token. The loads of kO tokens x kJ
+  // pairs are unconditional (a pair that does not count reads partial row 0
+  // and adds nothing), so all of them are in flight together: one L2 round
+  // trip per round instead of one per pair and token. Sums in pair order.
   const int row = 256 * dp + et;
   if (row >= f.d) return;
-  constexpr int kO = 4, kJ = 8;
+  constexpr int kO = 4, kJ = 4;
   const bool shared = f.S > 0 && f.e_begin == 0;
   for (int t0 = 0; t0 < f.T; t0 += kO) {
     float a[kO];
@@ -251,28 +252,27 @@ __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int
     for (int i = 0; i < kO; ++i) a[i] = 0.f;
     for (int j0 = 0; j0 < f.k; j0 += kJ) {
       float v[kO][kJ];
+      unsigned ok = 0u;
 #pragma unroll
       for (int i = 0; i < kO; ++i)
 #pragma unroll
         for (int jj = 0; jj < kJ; ++jj) {
-          const int t = t0 + i, j = j0 + jj;
-          v[i][jj] = (t < f.T && j < f.k && expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
-                         ? __ldcg(f.part + (size_t)s.inv[t * f.k + j] * f.d + row)
-                         : 0.f;
+          const int t = t0 + i, j = j0 + jj, pj = t * f.k + j;
+          // this shard's pairs only (all of them without sharding)
+          const bool c = t < f.T && j < f.k && expert_in_shard(s.ids[pj], f.e_begin, f.e_end);
+          ok |= (c ? 1u : 0u) << (i * kJ + jj);
+          v[i][jj] = __ldcg(f.part + (size_t)(c ? s.inv[pj] : 0) * f.d + row);
         }
 #pragma unroll
       for (int i = 0; i < kO; ++i)
 #pragma unroll
-        for (int jj = 0; jj < kJ; ++jj) {
-          const int t = t0 + i, j = j0 + jj;  // this shard's pairs only (all of them without sharding)
-          if (t < f.T && j < f.k && expert_in_shard(s.ids[t * f.k + j], f.e_begin, f.e_end))
-            a[i] = fmaf(s.gates[t * f.k + j], v[i][jj], a[i]);
-        }
+        for (int jj = 0; jj < kJ; ++jj)
+          if ((ok >> (i * kJ + jj)) & 1u) a[i] = fmaf(s.gates[(t0 + i) * f.k + j0 + jj], v[i][jj], a[i]);
     }
     float sh[kO];
 #pragma unroll
     for (int i = 0; i < kO; ++i)
-      sh[i] = (shared && t0 + i < f.T) ? __ldcg(f.part + (size_t)(f.P + t0 + i) * f.d + row) : 0.f;
+      sh[i] = shared ? __ldcg(f.part + (size_t)(f.P + min(t0 + i, f.T - 1)) * f.d + row) : 0.f;
 #pragma unroll
     for (int i = 0; i < kO; ++i) {
       const int t = t0 + i;
