@@ -245,6 +245,7 @@ __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int
   const int row = 256 * dp + et;
   if (row >= f.d) return;
   constexpr int kO = 4, kJ = 4;
+  static_assert(kO * kJ <= 64, "pair mask");
   const bool shared = f.S > 0 && f.e_begin == 0;
   for (int t0 = 0; t0 < f.T; t0 += kO) {
     float a[kO];
@@ -252,7 +253,7 @@ __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int
     for (int i = 0; i < kO; ++i) a[i] = 0.f;
     for (int j0 = 0; j0 < f.k; j0 += kJ) {
       float v[kO][kJ];
-      unsigned ok = 0u;
+      unsigned long long ok = 0ull;  // bit i kJ + jj: pair (t0 + i, j0 + jj) counts
 #pragma unroll
       for (int i = 0; i < kO; ++i)
 #pragma unroll
@@ -260,14 +261,14 @@ __device__ void tc_combine_rows(const FwdParams& f, const Shared& s, int dp, int
           const int t = t0 + i, j = j0 + jj, pj = t * f.k + j;
           // this shard's pairs only (all of them without sharding)
           const bool c = t < f.T && j < f.k && expert_in_shard(s.ids[pj], f.e_begin, f.e_end);
-          ok |= (c ? 1u : 0u) << (i * kJ + jj);
+          ok |= (c ? 1ull : 0ull) << (i * kJ + jj);
           v[i][jj] = __ldcg(f.part + (size_t)(c ? s.inv[pj] : 0) * f.d + row);
         }
 #pragma unroll
       for (int i = 0; i < kO; ++i)
 #pragma unroll
         for (int jj = 0; jj < kJ; ++jj)
-          if ((ok >> (i * kJ + jj)) & 1u) a[i] = fmaf(s.gates[(t0 + i) * f.k + j0 + jj], v[i][jj], a[i]);
+          if ((ok >> (i * kJ + jj)) & 1ull) a[i] = fmaf(s.gates[(t0 + i) * f.k + j0 + jj], v[i][jj], a[i]);
     }
     float sh[kO];
 #pragma unroll
