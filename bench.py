@@ -38,6 +38,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import re
 import os
 import statistics
 import sys
@@ -173,24 +174,35 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+_COMMENT_OR_STRING = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'', re.S)
+
+
+def code_text(src: str) -> str:
+    """C/CUDA source with its comments removed and whitespace collapsed (string and character
+    literals kept): what the compiler sees of it, so comment-only edits keep a capture's key."""
+    out = _COMMENT_OR_STRING.sub(lambda mt: " " if mt.group(0)[0] == "/" else mt.group(0), src)
+    return " ".join(out.split())
+
+
+def kernel_source_hash(sources) -> str:
+    """Hash of the code of the files (repo-relative paths) that one kernel is compiled from."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "routed_expert_ffn_warp_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    for rel in sorted(sources):
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(rel.encode() + b"\0" + code_text(f.read()).encode() + b"\0")
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(phase: str, workload: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernels."""
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current code of the
+    kernel's translation unit (its .cu file and the headers it includes, listed with the entry)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(workload, {}).get(phase)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or not ent.get("sources") or ent.get("source_hash") != kernel_source_hash(ent["sources"]):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -467,7 +479,10 @@ def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank:
                      "phase_tflops": {p: ph_flops[p] / (ph_ms[p] / 1000.0) / 1e12 for p in phases
                                       if ph_ms[p] > 0 and ph_flops[p] > 0}},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": nl * T * wl.d * 2,
-                "d2h_bytes_per_step": nl * T * wl.d * 2, "via": "moe_forward_host (pinned host buffers)"},
+                "d2h_bytes_per_step": nl * T * wl.d * 2,
+                "via": "moe_forward_host (pinned host buffers; " + (
+                    "the single-launch kernel reads x and writes y over the CPU-GPU link)" if launches_per_fwd == 1
+                    else "copies into and out of the context's staging buffers)")},
         "gpu_launches": args.steps * nl * launches_per_fwd, "launches_per_layer": launches_per_fwd,
         "clocks": clk, "device_status": status, "setup_s": t_gen, "weight_bytes_per_layer": weight_bytes,
     }
