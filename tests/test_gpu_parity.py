@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from moe_testlib import (BF16_TOL, F32_TOL, build_lib, check_output, check_routing, make_layer, oracle_layer,
+from moe_testlib import (BF16_TOL, F32_TOL, bf16_bits_to_f64, build_lib, check_output, check_routing, make_layer, oracle_layer,
                          oracle_route, run_gpu)
 
 pytestmark = pytest.mark.gpu
@@ -296,6 +296,39 @@ def test_forward_host_matches_device(m):
     layer.forward_host(L["x"], wl.T, out)
     y = (out.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert np.array_equal(y, g["y"])
+    layer.close()
+
+
+@pytest.mark.parametrize("path,out_f32", [("fused", False), ("fused-tc", True), ("fused-tc", False)])
+def test_forward_host_mapped_buffers(m, path, out_f32):
+    """Page-locked host buffers on a single-launch call: the kernel reads x from the caller's
+    buffer and writes y into theirs over the CPU-GPU link. The result equals the device-buffer
+    call's bit for bit on two calls in a row (with fresh inputs for the second), the single-launch
+    kernel ran, and x and out that share bytes still give the device result (the staging copies)."""
+    torch = pytest.importorskip("torch")
+    T, t_max = 7, 16
+    wl = synth.WORKLOADS["tiny"].with_(name="mapped", T=T, d=288, ffn=320, E=32, k=4, shared_ffn=64)
+    flags = m.MOE_FLAG_NO_TC if path == "fused" else m.MOE_FLAG_TC_GATEUP
+    L = synth.gen_layer(wl, 31)
+    layer = make_layer(m, wl, L, t_max=t_max, out_f32=out_f32, flags=flags)
+    assert m.moe_launches_per_forward(layer.ctx, T) == 1
+    odt = torch.float32 if out_f32 else torch.int16
+    for call in range(2):
+        xb = L["x"] if call == 0 else synth.gen_layer(wl, 32)["x"]
+        g = run_gpu(m, layer, xb, out_f32=out_f32)
+        x_h = torch.from_numpy(xb.view(np.int16).copy()).pin_memory()
+        out_h = torch.full((T, wl.d), -1, dtype=odt).pin_memory()
+        layer.forward_host(x_h, T, out_h)
+        yo = out_h.numpy()
+        y = yo.astype(np.float64) if out_f32 else bf16_bits_to_f64(yo.view(np.uint16))
+        assert np.array_equal(y, g["y"]), f"call {call}"
+        assert layer.status() == 0
+    # in place: out over x (bf16 out only: the same bytes per row)
+    if not out_f32:
+        buf = torch.from_numpy(L["x"].view(np.int16).copy()).pin_memory()
+        layer.forward_host(buf, T, buf)
+        g = run_gpu(m, layer, L["x"])
+        assert np.array_equal(bf16_bits_to_f64(buf.numpy().view(np.uint16)), g["y"])
     layer.close()
 
 
