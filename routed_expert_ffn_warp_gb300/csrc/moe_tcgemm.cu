@@ -76,9 +76,12 @@ struct Mode {
   static constexpr int kMma = 2;                   // MMA lanes = M tiles of a unit
   static constexpr int kDCol = kDown ? 192 : 96;   // accumulator width (N <= kDCol); buffer b, lane t at kDCol (kMma b + t)
   static constexpr int kBufs = kDown ? 1 : 2;      // accumulator buffers (units in flight between MMA and epilogue)
-  // L2 prefetch distance of the weight blocks, in K steps (measured: it
-  // shortens the down GEMM and lengthens gate/up, whose panel reads compete)
-  static constexpr int kPf = kDown ? 12 : 0;
+  // L2 prefetch distance of the weight blocks, in K steps. Measured on the
+  // 1,024-token prefill layer (us per layer of the GEMM): gate/up 0 / 3 / 4 /
+  // 6 / 8 steps 249.7 / 237.7 / 236.1-237.4 / 238.4 / 238.7 (longer windows
+  // compete with its panel reads); down 8 / 12 / 24 steps 156.6 / 157.5-159.1 /
+  // 203.0.
+  static constexpr int kPf = kDown ? 12 : 4;
   static constexpr int kEpiSmem = kDown ? 0 : 4 * kMaxTok * 32 * 4;  // gate/up values of one M tile [4 blocks][token][32]
   static_assert(kBufs * kMma * kDCol <= kSfCol && kSfCol + kS * kSfSet <= (int)kTmemCols, "TMEM columns");
 };
