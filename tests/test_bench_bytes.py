@@ -50,3 +50,19 @@ def test_layer_flops():
     assert bench.layer_flops(synth.WORKLOADS["prefill"], 1024) == 204_598_149_120  # 204.6 GFLOP per layer
     wl = synth.WORKLOADS["small"]
     assert bench.layer_flops(wl, 8) == 2 * 8 * 256 * 2048 + 2 * 64 * 3 * 2048 * 512 + 2 * 8 * 3 * 2048 * 2048
+
+
+def test_traffic_key_ignores_comments_and_follows_code(tmp_path, monkeypatch):
+    """The key a committed DRAM-traffic figure is stored under: comment and whitespace edits keep it,
+    any change to the code (a constant, a string literal) changes it."""
+    src = 'int a = 4; // four\n/* block\n comment */ const char* s = "//kept";\n'
+    assert bench.code_text(src) == 'int a = 4; const char* s = "//kept";'
+    (tmp_path / "k.cu").write_text(src)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash(["k.cu"])
+    (tmp_path / "k.cu").write_text(src.replace("// four", "// 4 steps").replace("\n/*", "\n\n  /*"))
+    assert bench.kernel_source_hash(["k.cu"]) == h0
+    (tmp_path / "k.cu").write_text(src.replace("a = 4", "a = 6"))
+    assert bench.kernel_source_hash(["k.cu"]) != h0
+    (tmp_path / "k.cu").write_text(src.replace('"//kept"', '"//kepT"'))
+    assert bench.kernel_source_hash(["k.cu"]) != h0
