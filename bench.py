@@ -165,6 +165,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
+# moe_forward_host reads x and writes y in place (no staging copies) for single-launch calls on at
+# most this many bytes of x with page-locked mapped buffers (include/moe.h)
+MAPPED_X_BYTES = 16384
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -481,7 +486,8 @@ def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank:
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": nl * T * wl.d * 2,
                 "d2h_bytes_per_step": nl * T * wl.d * 2,
                 "via": "moe_forward_host (pinned host buffers; " + (
-                    "the single-launch kernel reads x and writes y over the CPU-GPU link)" if launches_per_fwd == 1
+                    "the single-launch kernel reads x and writes y over the CPU-GPU link)"
+                    if launches_per_fwd == 1 and T * wl.d * 2 <= MAPPED_X_BYTES
                     else "copies into and out of the context's staging buffers)")},
         "gpu_launches": args.steps * nl * launches_per_fwd, "launches_per_layer": launches_per_fwd,
         "clocks": clk, "device_status": status, "setup_s": t_gen, "weight_bytes_per_layer": weight_bytes,
