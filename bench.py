@@ -165,8 +165,8 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
-# moe_forward_host reads x and writes y in place (no staging copies) for single-launch calls on at
-# most this many bytes of x with page-locked mapped buffers (include/moe.h)
+# moe_forward_host writes y in place into a page-locked mapped buffer, and reads x in place too for
+# single-launch calls on at most this many bytes of x (include/moe.h)
 MAPPED_X_BYTES = 16384
 
 
@@ -488,7 +488,7 @@ def measure_workload(args, wl: synth.Workload, nl: int, m, torch, ws: int, rank:
                 "via": "moe_forward_host (pinned host buffers; " + (
                     "the single-launch kernel reads x and writes y over the CPU-GPU link)"
                     if launches_per_fwd == 1 and T * wl.d * 2 <= MAPPED_X_BYTES
-                    else "copies into and out of the context's staging buffers)")},
+                    else "x copied into the context, y written over the CPU-GPU link by the kernels)")},
         "gpu_launches": args.steps * nl * launches_per_fwd, "launches_per_layer": launches_per_fwd,
         "clocks": clk, "device_status": status, "setup_s": t_gen, "weight_bytes_per_layer": weight_bytes,
     }

@@ -225,13 +225,13 @@ int moe_forward(moe_ctx* ctx, const void* x, int T, void* out, void* stream);
  * back to out (host) on `stream`. With synchronize != 0 it waits for the stream before returning;
  * with 0 the caller synchronises before reading out or reusing x. Pinned host
  * memory is needed for the copies to be asynchronous; pageable works too.
- * When the call runs a single-launch kernel (moe_launches_per_forward == 1)
- * on at most 16 KB of x (a decode-sized call: every CTA of those kernels
- * stages all of x, so larger x is faster through the copies), and both
- * buffers are page-locked and mapped into the device's address space
- * (cudaHostAlloc / cudaMallocHost, torch pin_memory) and share no bytes, no
- * copy is enqueued: the kernel reads x from x_host and writes out_host
- * directly over the CPU-GPU link (the same bytes; the same result bits).
+ * Page-locked buffers mapped into the device's address space (cudaHostAlloc /
+ * cudaMallocHost, torch pin_memory) skip the staging copies: the kernels
+ * write y straight into such an out_host, and a call that runs a
+ * single-launch kernel (moe_launches_per_forward == 1) on at most 16 KB of x
+ * also reads x straight from such an x_host (every CTA of those kernels
+ * stages all of x, so larger x is faster through the copy; so is an x that
+ * shares bytes with out). Same bytes, same result bits.
  * Each context has one staging buffer: do not overlap two calls on a context. */
 int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, void* stream, int synchronize);
 

@@ -537,36 +537,36 @@ int moe_forward_host(moe_ctx* ctx, const void* x_host, int T, void* out_host, vo
   const size_t xb = (size_t)T * ctx->cfg.d * 2;
   const size_t ob = (size_t)T * ctx->cfg.d * (ctx->cfg.out_dtype == MOE_OUT_F32 ? 4 : 2);
   cudaError_t e = cudaSuccess;
-  // A call that runs one of the single-launch kernels on at most
-  // kMappedXBytes of x, with both buffers page-locked and mapped: the kernel
-  // stages x from the caller's buffer and writes y into theirs over the
-  // CPU-GPU link. No copy-engine operation sits between consecutive layer
+  // In-place host buffers. A page-locked buffer mapped into the device's
+  // address space (cudaHostAlloc / cudaMallocHost, torch pin_memory) is passed
+  // to the kernels as is instead of going through the context's staging
+  // buffers: no copy-engine operation then sits between consecutive layer
   // kernels on the stream, so each next kernel is still scheduled while the
   // previous one drains (programmatic dependent launch), as with device
-  // buffers. Every CTA stages all of x, so the link carries one copy of x per
-  // SM: measured on GB300, a 5,760-byte token (d = 2880) went from 36.3 to
-  // 28.4 us per layer end to end, while 8 tokens of d = 2048 (32 KB) and 16
-  // of d = 2880 (92 KB) were slower than the copies. Buffers that overlap take
-  // the copies too.
+  // buffers.
+  //  * out: whenever it is mapped. Every kernel that writes y writes each
+  //    element once and reads none back, so the link carries y once.
+  //  * x: only for the single-launch kernels on at most kMappedXBytes of x.
+  //    Every CTA of those kernels stages all of x, so the link carries one
+  //    copy of x per SM: measured on GB300, a 5,760-byte token (d = 2880) went
+  //    from 36.3 to 28.4 us per layer end to end with both buffers in place,
+  //    while 8 tokens of d = 2048 (32 KB) and 16 of d = 2880 (92 KB) were
+  //    slower than through the copy. When x and out share bytes, x is copied.
   constexpr size_t kMappedXBytes = 16384;
-  if (T > 0 && xb <= kMappedXBytes && uses_decode(ctx, T)) {
+  const void* od = T > 0 ? mapped_host_address(out_host) : nullptr;
+  if (od && !aligned16(od)) od = nullptr;
+  const void* xd =
+      (T > 0 && xb <= kMappedXBytes && uses_decode(ctx, T)) ? mapped_host_address(x_host) : nullptr;
+  if (xd && !aligned16(xd)) xd = nullptr;
+  if (xd && od) {
     const uintptr_t x0 = reinterpret_cast<uintptr_t>(x_host), o0 = reinterpret_cast<uintptr_t>(out_host);
-    const bool apart = x0 + xb <= o0 || o0 + ob <= x0;
-    const void* xd = apart ? mapped_host_address(x_host) : nullptr;
-    const void* od = xd ? mapped_host_address(out_host) : nullptr;
-    if (xd && od && aligned16(xd) && aligned16(od)) {
-      int rc = moe_forward(ctx, xd, T, const_cast<void*>(od), stream);
-      if (rc != MOE_OK) return rc;
-      if (synchronize) e = cudaStreamSynchronize(s);
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "synchronize");
-      return MOE_OK;
-    }
+    if (!(x0 + xb <= o0 || o0 + ob <= x0)) xd = nullptr;  // y would overwrite x while CTAs still read it
   }
-  if (T > 0) e = cudaMemcpyAsync(ctx->x_dev, x_host, xb, cudaMemcpyDefault, s);
+  if (T > 0 && !xd) e = cudaMemcpyAsync(ctx->x_dev, x_host, xb, cudaMemcpyDefault, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "x copy");
-  int rc = moe_forward(ctx, ctx->x_dev, T, ctx->out_dev, stream);
+  int rc = moe_forward(ctx, xd ? xd : ctx->x_dev, T, od ? const_cast<void*>(od) : ctx->out_dev, stream);
   if (rc != MOE_OK) return rc;
-  if (T > 0) e = cudaMemcpyAsync(out_host, ctx->out_dev, ob, cudaMemcpyDefault, s);
+  if (T > 0 && !od) e = cudaMemcpyAsync(out_host, ctx->out_dev, ob, cudaMemcpyDefault, s);
   if (e == cudaSuccess && synchronize) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "out copy");
   return MOE_OK;

@@ -299,19 +299,20 @@ def test_forward_host_matches_device(m):
     layer.close()
 
 
-@pytest.mark.parametrize("path,out_f32", [("fused", False), ("fused-tc", True), ("fused-tc", False)])
-def test_forward_host_mapped_buffers(m, path, out_f32):
-    """Page-locked host buffers on a single-launch call: the kernel reads x from the caller's
-    buffer and writes y into theirs over the CPU-GPU link. The result equals the device-buffer
-    call's bit for bit on two calls in a row (with fresh inputs for the second), the single-launch
-    kernel ran, and x and out that share bytes still give the device result (the staging copies)."""
+@pytest.mark.parametrize("path,out_f32,T,d", [("fused", False, 7, 288), ("fused-tc", True, 7, 288),
+                                              ("fused-tc", False, 7, 288), ("fused-tc", False, 16, 1024),
+                                              ("general", True, 40, 288)])
+def test_forward_host_mapped_buffers(m, path, out_f32, T, d):
+    """Page-locked host buffers: the kernels write y straight into out_host, and a single-launch call on
+    at most 16 KB of x also reads x from x_host (T=7, d=288); larger x (T=16, d=1024) and the multi-kernel
+    path (T=40) copy x in first. The result equals the device-buffer call's bit for bit on two calls in a
+    row (fresh inputs for the second), and x and out that share bytes still give the device result."""
     torch = pytest.importorskip("torch")
-    T, t_max = 7, 16
-    wl = synth.WORKLOADS["tiny"].with_(name="mapped", T=T, d=288, ffn=320, E=32, k=4, shared_ffn=64)
-    flags = m.MOE_FLAG_NO_TC if path == "fused" else m.MOE_FLAG_TC_GATEUP
+    wl = synth.WORKLOADS["tiny"].with_(name="mapped", T=T, d=d, ffn=320, E=32, k=4, shared_ffn=64)
+    flags = {"fused": m.MOE_FLAG_NO_TC, "fused-tc": m.MOE_FLAG_TC_GATEUP, "general": m.MOE_FLAG_TC_GATEUP}[path]
     L = synth.gen_layer(wl, 31)
-    layer = make_layer(m, wl, L, t_max=t_max, out_f32=out_f32, flags=flags)
-    assert m.moe_launches_per_forward(layer.ctx, T) == 1
+    layer = make_layer(m, wl, L, t_max=max(T, 16), out_f32=out_f32, flags=flags)
+    assert (m.moe_launches_per_forward(layer.ctx, T) == 1) == path.startswith("fused")
     odt = torch.float32 if out_f32 else torch.int16
     for call in range(2):
         xb = L["x"] if call == 0 else synth.gen_layer(wl, 32)["x"]
