@@ -46,15 +46,18 @@ def _shard_layer(m, wl, L, b, e, flags, w_sg=None):
     return layer, codes.nbytes + scales.nbytes
 
 
+# (T, d, ffn, E, k, shared ffn), shard boundaries, gated shared expert (only where there is a shared expert)
+SHARD_CASES = [(shape, cuts, gated)
+               for shape, cuts in [((6, 256, 192, 16, 4, 64), [0, 5, 11, 16]),
+                                   ((16, 160, 96, 8, 2, 0), [0, 3, 8]),
+                                   ((20, 224, 128, 32, 4, 96), [0, 16, 32])]
+               for gated in (False, True) if shape[5] > 0 or not gated]
+
+
 @pytest.mark.parametrize("path", ["fused-tc", "fused", "general", "general-tc"])
-@pytest.mark.parametrize("shape,cuts", [((6, 256, 192, 16, 4, 64), [0, 5, 11, 16]),
-                                        ((16, 160, 96, 8, 2, 0), [0, 3, 8]),
-                                        ((20, 224, 128, 32, 4, 96), [0, 16, 32])])
-@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("shape,cuts,gated", SHARD_CASES)
 def test_shards_match_the_oracle_and_add_up(m, path, shape, cuts, gated):
     T, d, F, E, k, S = shape
-    if gated and S == 0:
-        pytest.skip("no shared expert to gate")
     wl = synth.WORKLOADS["tiny"].with_(name="shard", number=13, T=T, d=d, ffn=F, E=E, k=k, shared_ffn=S)
     L = synth.gen_layer(wl, 2)
     w_sg = synth.gen_shared_gate(L["seed"], d) if gated else None
