@@ -515,6 +515,22 @@ def prefill_tensor_view(res: dict, mma: dict | None, peaks: dict) -> dict:
     return out
 
 
+def provenance(peaks: dict, roofline: dict, mma) -> dict:
+    """Where each figure of the line comes from: MEASURED in this run or by ncu, CALCULATED from
+    measured figures, or ASSUMED (a fallback constant)."""
+    return {
+        "value, ms_per_step, us_per_layer, e2e, clocks, cpu_baseline": "MEASURED (CUDA events / wall clock, this run)",
+        "roofline.achieved": "CALCULATED: algorithmic bytes per launch (pinned to the page's expert size) / "
+                             "MEASURED average launch time",
+        "roofline.peak": "MEASURED (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                         else "ASSUMED (fallback 6.8 TB/s)",
+        "roofline.traffic": "MEASURED (ncu DRAM counters on the current kernel code, profiles/traffic.json)"
+                            if roofline.get("traffic") is not None else "none taken on the current kernel code",
+        "mma_probe.tflops": "MEASURED (this run)" if mma else "not run",
+        "mma_probe.fp4_peak_tflops": f"CALCULATED ({FP4_OVER_FP8:g} x the measured rate)" if mma else "not run",
+    }
+
+
 def run_ours(args, wl):
     import torch
     ws, rank, local = dist_env()
@@ -581,6 +597,7 @@ def run_ours(args, wl):
         "setup_s": main["setup_s"],
         "mma_probe": mma,
         "workloads": extras,
+        "provenance": provenance(peaks, main["roofline"], mma),
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

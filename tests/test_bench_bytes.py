@@ -66,3 +66,13 @@ def test_traffic_key_ignores_comments_and_follows_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash(["k.cu"]) != h0
     (tmp_path / "k.cu").write_text(src.replace('"//kept"', '"//kepT"'))
     assert bench.kernel_source_hash(["k.cu"]) != h0
+
+
+def test_provenance_labels():
+    """The line says which figures are measured, calculated or assumed."""
+    pv = bench.provenance({"source": "measured"}, {"traffic": 54487808}, {"tflops": 4870.0})
+    assert pv["roofline.peak"].startswith("MEASURED") and pv["roofline.traffic"].startswith("MEASURED")
+    assert pv["mma_probe.fp4_peak_tflops"].startswith("CALCULATED")
+    pv = bench.provenance({"source": "fallback"}, {"traffic": None}, None)
+    assert pv["roofline.peak"].startswith("ASSUMED") and "none" in pv["roofline.traffic"]
+    assert pv["mma_probe.tflops"] == "not run"
