@@ -66,3 +66,11 @@ def test_mma_probe_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.moe_probe_mma_rate(0, 1000, 24, ctypes.byref(tf), None) == -1  # N not a multiple of 16
     assert lib.moe_probe_mma_rate(0, 1000, 256, ctypes.byref(tf), None) == -1  # N above the probed widths
     assert b"mmas_per_sm" in lib.moe_probe_error()
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the compiled library the binding raises: there is no CPU fallback to silently take over."""
+    import routed_expert_ffn_warp_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        m.load_library(str(tmp_path / "libmoe_gb300.so"))
